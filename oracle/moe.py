@@ -1,0 +1,267 @@
+"""Oracle: top-K routed SwiGLU MoE layer, forward and backward in float64 (test infrastructure only).
+
+Forward being differentiated (the plainest reading shared by the three pages): for each token t and
+each of its K routing slots k, with e = ids[t, k] and score s[t, k],
+
+    h   = x_t @ W1_e + b1_e                 W1_e [H, 2I]: columns 0..I-1 gate, I..2I-1 up
+    a   = SiLU(gate) * up                   SiLU(z) = z * sigmoid(z)
+    y   = a @ W2_e + b2_e                   W2_e [I, H]
+    out_t = sum_k s[t, k] * y
+
+Backward (sonic-moe backward.py `_down_projection_backward_act` with `gemm_dgated(...,
+colvec_scale=s, colvec_reduce=True)`, `db2_and_ds_kernel`, `_down_projection_backward_weight`,
+`_up_projection_backward_act`, `db1_kernel`, `_up_projection_backward_weight`,
+`_token_broadcast_backward`; blockwise MoE backward page, returned gradients):
+
+    dA_raw = dout_t @ W2_e^T                ds[t,k] = <dA_raw, a> + <dout_t, b2_e>
+    dA     = s * dA_raw                     a'      = s * a
+    dgate  = dA * up * SiLU'(gate)          dup     = dA * SiLU(gate)        dh = [dgate | dup]
+    dW2_e  = sum_rows a'^T dout_t           db2_e   = sum_rows s * dout_t
+    dW1_e  = sum_rows x_t^T dh              db1_e   = sum_rows dh
+    dx_t   = sum_k dh @ W1_e^T
+
+The gate/up pre-activation h of each (t, k) is an input (the forward's checkpoint).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import mxfp8 as mx
+
+
+def _f64(a):
+    if a is None:
+        return None
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            return a.detach().to("cpu", torch.float64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(a, dtype=np.float64)
+
+
+def sigmoid(z):
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def silu(z):
+    return z * sigmoid(z)
+
+
+def dsilu(z):
+    sg = sigmoid(z)
+    return sg * (1.0 + z * (1.0 - sg))
+
+
+def rows_of_expert(ids: np.ndarray, e: int):
+    """(t, k) of every row routed to expert e, in ascending flat order t*K + k."""
+    flat = np.nonzero(np.asarray(ids).reshape(-1) == e)[0]
+    K = ids.shape[1]
+    return flat // K, flat % K
+
+
+def moe_forward(x, W1, b1, W2, b2, s, ids):
+    """out [T,H] and the pre-activations h [T,K,2I] (used by the pins, never by the GPU path)."""
+    x, W1, W2, s = _f64(x), _f64(W1), _f64(W2), _f64(s)
+    b1, b2 = _f64(b1), _f64(b2)
+    ids = np.asarray(ids)
+    T, H = x.shape
+    E, _, I2 = W1.shape
+    I = I2 // 2
+    K = ids.shape[1]
+    out = np.zeros((T, H))
+    h = np.zeros((T, K, I2))
+    for e in range(E):
+        t, k = rows_of_expert(ids, e)
+        if t.size == 0:
+            continue
+        he = x[t] @ W1[e] + (b1[e] if b1 is not None else 0.0)
+        a = silu(he[:, :I]) * he[:, I:]
+        y = a @ W2[e] + (b2[e] if b2 is not None else 0.0)
+        np.add.at(out, t, s[t, k][:, None] * y)
+        h[t, k] = he
+    return out, h
+
+
+def moe_backward(x, dout, W1, W2, s, ids, h, b2=None, with_bias=False):
+    """All gradients of the MoE layer in float64 (the BF16 path's reference).
+
+    x, dout [T,H]; W1 [E,H,2I]; W2 [E,I,H]; s [T,K]; ids [T,K]; h [T,K,2I]; b2 [E,H] or None.
+    Returns dict(dx [T,H], dW1 [E,H,2I], dW2 [E,I,H], ds [T,K], db1 [E,2I], db2 [E,H]);
+    db1/db2 are None unless with_bias.
+    """
+    x, dout, W1, W2, s, h = map(_f64, (x, dout, W1, W2, s, h))
+    b2 = _f64(b2)
+    ids = np.asarray(ids)
+    T, H = x.shape
+    E, _, I2 = W1.shape
+    I = I2 // 2
+    K = ids.shape[1]
+    dx = np.zeros((T, H))
+    ds = np.zeros((T, K))
+    dW1 = np.zeros((E, H, I2))
+    dW2 = np.zeros((E, I, H))
+    db1 = np.zeros((E, I2)) if with_bias else None
+    db2 = np.zeros((E, H)) if with_bias else None
+    for e in range(E):
+        t, k = rows_of_expert(ids, e)
+        if t.size == 0:
+            continue
+        g = dout[t]                                   # gathered upstream gradient rows
+        gate, up = h[t, k, :I], h[t, k, I:]
+        a = silu(gate) * up
+        sr = s[t, k][:, None]
+        dA_raw = g @ W2[e].T
+        ds[t, k] = np.sum(dA_raw * a, axis=1)
+        if b2 is not None:
+            ds[t, k] += g @ b2[e]
+        dA = sr * dA_raw
+        dh = np.concatenate([dA * up * dsilu(gate), dA * silu(gate)], axis=1)
+        dW2[e] = (sr * a).T @ g
+        dW1[e] = x[t].T @ dh
+        if with_bias:
+            db2[e] = np.sum(sr * g, axis=0)
+            db1[e] = np.sum(dh, axis=0)
+        np.add.at(dx, t, dh @ W1[e].T)
+    return dict(dx=dx, dW1=dW1, dW2=dW2, ds=ds, db1=db1, db2=db2)
+
+
+# ----------------------------------------------------------------------------------------------
+# MXFP8 path
+# ----------------------------------------------------------------------------------------------
+
+def _to_f32(a):
+    """Round float64 to the nearest float32 (where the kernel takes a quantisation decision)."""
+    return np.asarray(a, dtype=np.float32).astype(np.float64)
+
+
+def _to_bf16(a):
+    """Round float64 to the nearest bfloat16 (round-to-nearest-even on the float32 value)."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64)).to(torch.bfloat16).to(
+        torch.float64).numpy()
+
+
+def _col_roundtrip(v, fmt, quant):
+    """Quantise along rows (axis 0) in groups of 32 consecutive rows; zero-pad the last group."""
+    n = v.shape[0]
+    npad = -(-n // 32) * 32
+    if npad != n:
+        v = np.concatenate([v, np.zeros((npad - n,) + v.shape[1:])], axis=0)
+    return quant(v, fmt, 0)[:n]
+
+
+def moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=1, fp8_act=mx.E5M2, fp8_w=mx.E4M3,
+                       b2=None, with_bias=False, experts=None, tokens=None, quant=None):
+    """MoE backward with every GEMM operand MXFP8-quantised along its contraction dimension.
+
+    Quantisation points (reading of the MXFP8 blockwise backward page; weights pre-quantised,
+    activations quantised after the per-expert gather):
+      G1  dA_raw  = Q_H(dout_g) @ Q_H(W2_e)^T                 groups along H
+      G2  dx_exp  = Q_2I(dh) @ Q_2I(W1_e)^T, stored BF16      groups along 2I
+      G3  dW2_e   = Q_tok(a')^T @ Q_tok(dout_g)    (affinity on I, a' = s*a)
+                  = Q_tok(a)^T  @ Q_tok(s*dout_g)  (affinity on H)
+      G4  dW1_e   = Q_tok(x_g)^T @ Q_tok(dh)                  groups of 32 grouped rows
+    Activation-side operands use fp8_act, weights fp8_w.  dh, a' and s*dout are rounded to float32
+    before their quantisation, as the kernel quantises float32 values.  ds, db1 and db2 use the
+    unquantised epilogue values.  `experts` limits dW1/dW2/db1/db2 to those experts, `tokens`
+    limits dx/ds to those tokens (both default to all).  `quant(v, fmt, axis)` defaults to the
+    MX round trip; tests substitute the identity to check the wiring.
+    """
+    quant = quant or mx.mx_roundtrip
+    x, dout, W1, W2, s, h = map(_f64, (x, dout, W1, W2, s, h))
+    b2 = _f64(b2)
+    ids = np.asarray(ids)
+    T, H = x.shape
+    E, _, I2 = W1.shape
+    I = I2 // 2
+    K = ids.shape[1]
+    expert_set = range(E) if experts is None else experts
+    token_mask = np.ones(T, bool)
+    if tokens is not None:
+        token_mask[:] = False
+        token_mask[np.asarray(tokens)] = True
+    dx = np.zeros((T, H))
+    ds = np.zeros((T, K))
+    dW1 = np.zeros((E, H, I2))
+    dW2 = np.zeros((E, I, H))
+    db1 = np.zeros((E, I2)) if with_bias else None
+    db2 = np.zeros((E, H)) if with_bias else None
+    want_w = set(expert_set)
+    for e in range(E):
+        t, k = rows_of_expert(ids, e)
+        if t.size == 0:
+            continue
+        need_w = e in want_w
+        sel = np.ones(t.size, bool) if need_w else token_mask[t]
+        if not sel.any():
+            continue
+        t, k = t[sel], k[sel]            # need_w keeps every row, so column groups stay intact
+        W2q = quant(W2[e], fp8_w, 1)     # [I,H] groups along H
+        W1q = quant(W1[e], fp8_w, 1)     # [H,2I] groups along 2I
+        g = dout[t]
+        gq = quant(g, fp8_act, 1)
+        gate, up = h[t, k, :I], h[t, k, I:]
+        a = silu(gate) * up
+        sr = s[t, k][:, None]
+        dA_raw = gq @ W2q.T
+        dsv = np.sum(dA_raw * a, axis=1)
+        if b2 is not None:
+            dsv = dsv + g @ b2[e]
+        dA = sr * dA_raw
+        dh = _to_f32(np.concatenate([dA * up * dsilu(gate), dA * silu(gate)], axis=1))
+        dx_exp = _to_bf16(quant(dh, fp8_act, 1) @ W1q.T)
+        tm = token_mask[t]
+        ds[t[tm], k[tm]] = dsv[tm]
+        np.add.at(dx, t[tm], dx_exp[tm])
+        if need_w:
+            if affinity == 1:
+                dW2[e] = _col_roundtrip(_to_f32(sr * a), fp8_act, quant).T @ _col_roundtrip(g, fp8_act, quant)
+            else:
+                dW2[e] = _col_roundtrip(_to_f32(a), fp8_act, quant).T @ _col_roundtrip(_to_f32(sr * g), fp8_act, quant)
+            dW1[e] = _col_roundtrip(x[t], fp8_act, quant).T @ _col_roundtrip(dh, fp8_act, quant)
+            if with_bias:
+                db2[e] = np.sum(sr * g, axis=0)
+                db1[e] = np.sum(dh, axis=0)
+    return dict(dx=dx, dW1=dW1, dW2=dW2, ds=ds, db1=db1, db2=db2)
+
+
+def moe_backward_sampled(x, dout, W1, W2, s, ids, h, experts, tokens, b2=None, with_bias=False):
+    """BF16-path backward restricted to dW/db of `experts` and dx/ds of `tokens` (same formulas)."""
+    x, dout, W1, W2, s, h = map(_f64, (x, dout, W1, W2, s, h))
+    b2 = _f64(b2)
+    ids = np.asarray(ids)
+    T, H = x.shape
+    E, _, I2 = W1.shape
+    I = I2 // 2
+    K = ids.shape[1]
+    out = dict(dx={}, ds={}, dW1={}, dW2={}, db1={}, db2={})
+    for e in experts:
+        t, k = rows_of_expert(ids, e)
+        g = dout[t]
+        gate, up = h[t, k, :I], h[t, k, I:]
+        a = silu(gate) * up
+        sr = s[t, k][:, None]
+        dA = sr * (g @ W2[e].T)
+        dh = np.concatenate([dA * up * dsilu(gate), dA * silu(gate)], axis=1)
+        out["dW2"][e] = (sr * a).T @ g
+        out["dW1"][e] = x[t].T @ dh
+        if with_bias:
+            out["db2"][e] = np.sum(sr * g, axis=0)
+            out["db1"][e] = np.sum(dh, axis=0)
+    for tt in tokens:
+        dxt = np.zeros(H)
+        dst = np.zeros(K)
+        for kk in range(K):
+            e = int(ids[tt, kk])
+            gate, up = h[tt, kk, :I], h[tt, kk, I:]
+            a = silu(gate) * up
+            dA_raw = dout[tt] @ W2[e].T
+            dst[kk] = dA_raw @ a + (dout[tt] @ b2[e] if b2 is not None else 0.0)
+            dA = s[tt, kk] * dA_raw
+            dh = np.concatenate([dA * up * dsilu(gate), dA * silu(gate)])
+            dxt += dh @ W1[e].T
+        out["dx"][tt] = dxt
+        out["ds"][tt] = dst
+    return out

@@ -1,0 +1,221 @@
+"""Pins for oracle.moe: finite differences, float64 torch autograd, the dense-MLP reduction,
+token-permutation invariance, closed-form identities and the MXFP8 quantisation points."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe as om
+from oracle import mxfp8 as mx
+
+
+def _problem(T=6, H=8, I=4, E=3, K=2, seed=0, bias=True):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, H))
+    dout = rng.standard_normal((T, H))
+    W1 = rng.standard_normal((E, H, 2 * I)) * 0.3
+    W2 = rng.standard_normal((E, I, H)) * 0.3
+    b1 = rng.standard_normal((E, 2 * I)) * 0.1 if bias else None
+    b2 = rng.standard_normal((E, H)) * 0.1 if bias else None
+    ids = np.stack([rng.permutation(E)[:K] for _ in range(T)])
+    s = rng.random((T, K)) + 0.1
+    s = s / s.sum(1, keepdims=True)
+    return x, dout, W1, b1, W2, b2, s, ids
+
+
+def _grads(x, dout, W1, b1, W2, b2, s, ids):
+    _, h = om.moe_forward(x, W1, b1, W2, b2, s, ids)
+    return om.moe_backward(x, dout, W1, W2, s, ids, h, b2=b2, with_bias=b1 is not None)
+
+
+def test_finite_differences():
+    x, dout, W1, b1, W2, b2, s, ids = _problem()
+    g = _grads(x, dout, W1, b1, W2, b2, s, ids)
+
+    def loss(x, W1, b1, W2, b2, s):
+        out, _ = om.moe_forward(x, W1, b1, W2, b2, s, ids)
+        return float(np.sum(out * dout))
+
+    args = dict(x=x, W1=W1, b1=b1, W2=W2, b2=b2, s=s)
+    names = dict(x="dx", W1="dW1", b1="db1", W2="dW2", b2="db2", s="ds")
+    eps = 1e-6
+    for name, arr in args.items():
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            plus = {k: v.copy() for k, v in args.items()}
+            minus = {k: v.copy() for k, v in args.items()}
+            plus[name][idx] += eps
+            minus[name][idx] -= eps
+            num[idx] = (loss(**plus) - loss(**minus)) / (2 * eps)
+        ana = g[names[name]]
+        rel = np.max(np.abs(num - ana)) / max(np.max(np.abs(ana)), 1e-30)
+        assert rel < 1e-7, (name, rel)
+
+
+def _torch_forward(x, W1, b1, W2, b2, s, ids):
+    """Loop-over-experts forward in torch float64 (differentiated by torch autograd)."""
+    T, H = x.shape
+    I = W1.shape[2] // 2
+    out = torch.zeros(T, H, dtype=torch.float64)
+    for e in range(W1.shape[0]):
+        t, k = torch.nonzero(ids == e, as_tuple=True)
+        if t.numel() == 0:
+            continue
+        h = x[t] @ W1[e] + (b1[e] if b1 is not None else 0)
+        a = torch.nn.functional.silu(h[:, :I]) * h[:, I:]
+        y = a @ W2[e] + (b2[e] if b2 is not None else 0)
+        out = out.index_add(0, t, s[t, k][:, None] * y)
+    return out
+
+
+@pytest.mark.parametrize("bias", [False, True])
+def test_torch_autograd_tiny_config_shapes(bias):
+    T, H, I, E, K = 256, 128, 256, 4, 2
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T, H, I, E, K, seed=11, bias=bias)
+    g = _grads(x, dout, W1, b1, W2, b2, s, ids)
+    tt = {n: torch.tensor(v, requires_grad=True) for n, v in
+          dict(x=x, W1=W1, W2=W2, s=s).items()}
+    tb1 = torch.tensor(b1, requires_grad=True) if bias else None
+    tb2 = torch.tensor(b2, requires_grad=True) if bias else None
+    out = _torch_forward(tt["x"], tt["W1"], tb1, tt["W2"], tb2, tt["s"], torch.tensor(ids))
+    (out * torch.tensor(dout)).sum().backward()
+    pairs = [("dx", tt["x"]), ("dW1", tt["W1"]), ("dW2", tt["W2"]), ("ds", tt["s"])]
+    if bias:
+        pairs += [("db1", tb1), ("db2", tb2)]
+    for name, t in pairs:
+        ref = t.grad.numpy()
+        err = np.linalg.norm(g[name] - ref) / np.linalg.norm(ref)
+        assert err < 1e-12, (name, err)
+
+
+def test_dense_mlp_reduction():
+    """E=1, K=1, s=1: the layer is a dense SwiGLU MLP; compare with autograd of that MLP."""
+    rng = np.random.default_rng(2)
+    T, H, I = 16, 12, 10
+    x, dout = rng.standard_normal((T, H)), rng.standard_normal((T, H))
+    W1 = rng.standard_normal((1, H, 2 * I)) * 0.3
+    W2 = rng.standard_normal((1, I, H)) * 0.3
+    ids = np.zeros((T, 1), dtype=np.int64)
+    s = np.ones((T, 1))
+    g = _grads(x, dout, W1, None, W2, None, s, ids)
+    tx = torch.tensor(x, requires_grad=True)
+    tg = torch.tensor(W1[0][:, :I], requires_grad=True)
+    tu = torch.tensor(W1[0][:, I:], requires_grad=True)
+    td = torch.tensor(W2[0], requires_grad=True)
+    y = (torch.nn.functional.silu(tx @ tg) * (tx @ tu)) @ td
+    (y * torch.tensor(dout)).sum().backward()
+    assert np.allclose(g["dx"], tx.grad.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(g["dW1"][0], np.concatenate([tg.grad.numpy(), tu.grad.numpy()], 1), rtol=1e-12, atol=1e-12)
+    assert np.allclose(g["dW2"][0], td.grad.numpy(), rtol=1e-12, atol=1e-12)
+    y_np = y.detach().numpy()
+    assert np.allclose(g["ds"][:, 0], np.sum(dout * y_np, 1), rtol=1e-12, atol=1e-12)
+
+
+def test_token_permutation_invariance():
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=20, H=8, I=6, E=4, K=2, seed=4)
+    g = _grads(x, dout, W1, b1, W2, b2, s, ids)
+    p = np.random.default_rng(9).permutation(20)
+    gp = _grads(x[p], dout[p], W1, b1, W2, b2, s[p], ids[p])
+    for n in ("dx", "ds"):
+        assert np.allclose(gp[n], g[n][p], rtol=1e-12, atol=1e-12)
+    for n in ("dW1", "dW2", "db1", "db2"):
+        assert np.allclose(gp[n], g[n], rtol=1e-12, atol=1e-12)
+
+
+def test_closed_form_identities():
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=30, H=10, I=6, E=5, K=3, seed=6)
+    out, h = om.moe_forward(x, W1, b1, W2, b2, s, ids)
+    g = om.moe_backward(x, dout, W1, W2, s, ids, h, b2=b2, with_bias=True)
+    lhs = np.sum(dout * out)
+    assert np.isclose(np.sum(s * g["ds"]), lhs, rtol=1e-12)
+    assert np.isclose(np.sum(g["dW2"] * W2) + np.sum(g["db2"] * b2), lhs, rtol=1e-12)
+    # <dx, x> = sum_r <dh_r, x_r W1_e> = sum_e <dW1_e, W1_e>
+    assert np.isclose(np.sum(g["dx"] * x), np.sum(g["dW1"] * W1), rtol=1e-12)
+    # renormalised scores: sum_e db2_e = sum_t dout_t
+    assert np.allclose(g["db2"].sum(0), dout.sum(0), rtol=1e-12, atol=1e-12)
+
+
+def test_linearity_in_scores():
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=12, seed=8)
+    _, h = om.moe_forward(x, W1, b1, W2, b2, s, ids)
+    g1 = om.moe_backward(x, dout, W1, W2, s, ids, h, b2=b2, with_bias=True)
+    g3 = om.moe_backward(x, dout, W1, W2, 3 * s, ids, h, b2=b2, with_bias=True)
+    for n in ("dx", "dW1", "dW2", "db1", "db2"):
+        assert np.allclose(g3[n], 3 * g1[n], rtol=1e-12, atol=1e-12)
+    assert np.allclose(g3["ds"], g1["ds"], rtol=1e-12, atol=1e-12)
+
+
+def test_sampled_matches_full():
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=24, H=8, I=6, E=4, K=2, seed=12)
+    _, h = om.moe_forward(x, W1, b1, W2, b2, s, ids)
+    g = om.moe_backward(x, dout, W1, W2, s, ids, h, b2=b2, with_bias=True)
+    sm = om.moe_backward_sampled(x, dout, W1, W2, s, ids, h, experts=[1, 3], tokens=[0, 5, 23],
+                                 b2=b2, with_bias=True)
+    for e in (1, 3):
+        for n in ("dW1", "dW2", "db1", "db2"):
+            assert np.allclose(sm[n][e], g[n][e], rtol=1e-12, atol=1e-12)
+    for t in (0, 5, 23):
+        assert np.allclose(sm["dx"][t], g["dx"][t], rtol=1e-12, atol=1e-12)
+        assert np.allclose(sm["ds"][t], g["ds"][t], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------------------------
+# MXFP8 path
+# ---------------------------------------------------------------------------------------------
+
+def _identity(v, fmt, axis):
+    return v
+
+
+@pytest.mark.parametrize("affinity", [0, 1])
+def test_mxfp8_wiring_without_quantisation(affinity):
+    """With the quantiser replaced by the identity, the MXFP8 path is the plain backward up to
+    the float32 / bfloat16 roundings of its stored intermediates."""
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=40, H=32, I=32, E=3, K=2, seed=13)
+    _, h = om.moe_forward(x, W1, b1, W2, b2, s, ids)
+    ref = om.moe_backward(x, dout, W1, W2, s, ids, h, b2=b2, with_bias=True)
+    got = om.moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=affinity, b2=b2,
+                                with_bias=True, quant=_identity)
+    for n, tol in (("dW1", 1e-6), ("dW2", 1e-6), ("ds", 1e-12), ("db1", 1e-6), ("db2", 1e-12),
+                   ("dx", 4e-3)):
+        err = np.linalg.norm(got[n] - ref[n]) / np.linalg.norm(ref[n])
+        assert err < tol, (n, err)
+
+
+def test_mxfp8_error_within_quantisation_bound():
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=64, H=64, I=64, E=2, K=2, seed=14, bias=False)
+    _, h = om.moe_forward(x, W1, None, W2, None, s, ids)
+    ref = om.moe_backward(x, dout, W1, W2, s, ids, h)
+    got = om.moe_backward_mxfp8(x, dout, W1, W2, s, ids, h)
+    for n in ("dx", "dW1", "dW2", "ds"):
+        err = np.linalg.norm(got[n] - ref[n]) / np.linalg.norm(ref[n])
+        assert 1e-3 < err < 0.15, (n, err)   # quantisation applied, and only quantisation error
+
+
+def test_mxfp8_groups_follow_contraction_axes():
+    """Scaling one token's dout row by 2^j must scale exactly that token's ds and dx by 2^j (G1
+    and G2 group along H and 2I, per row); scaling one feature column of x by 2^j must scale
+    exactly that row of every dW1_e by 2^j (G4 groups along tokens, per feature).  Grouping along
+    the other axis would mix rows of different scale into one group and break the equalities."""
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=64, H=64, I=32, E=2, K=2, seed=15, bias=False)
+    _, h = om.moe_forward(x, W1, None, W2, None, s, ids)
+    base = om.moe_backward_mxfp8(x, dout, W1, W2, s, ids, h)
+    j = np.where(np.arange(64) % 3 == 0, 7, np.where(np.arange(64) % 3 == 1, -6, 0))
+    row = np.ldexp(1.0, j)[:, None]
+    g = om.moe_backward_mxfp8(x, dout * row, W1, W2, s, ids, h)
+    assert np.array_equal(g["ds"], base["ds"] * row)
+    assert np.array_equal(g["dx"], base["dx"] * row)
+    g = om.moe_backward_mxfp8(x * row.T, dout, W1, W2, s, ids, h)   # h kept: only G4 sees x
+    assert np.array_equal(g["dW1"], base["dW1"] * row[None, :, :])
+    assert np.array_equal(g["dW2"], base["dW2"]) and np.array_equal(g["ds"], base["ds"])
+
+
+def test_mxfp8_restrictions_match_full():
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=64, H=32, I=32, E=3, K=2, seed=16, bias=False)
+    _, h = om.moe_forward(x, W1, None, W2, None, s, ids)
+    full = om.moe_backward_mxfp8(x, dout, W1, W2, s, ids, h)
+    part = om.moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, experts=[2], tokens=[3, 40])
+    assert np.array_equal(part["dW1"][2], full["dW1"][2])
+    assert np.array_equal(part["dW2"][2], full["dW2"][2])
+    for t in (3, 40):
+        assert np.allclose(part["dx"][t], full["dx"][t], rtol=0, atol=1e-12)
+        assert np.array_equal(part["ds"][t], full["ds"][t])
