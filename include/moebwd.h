@@ -1,0 +1,242 @@
+/*
+ * moebwd -- backward pass of a top-K routed SwiGLU Mixture-of-Experts layer on one GB300 GPU
+ * (sm_103a), BF16 and MXFP8, plus the dense MXFP8 linear backward.  C ABI.
+ *
+ * Sources of the operations (pages):
+ *   [BW]  "Blockwise MM Backward MXFP8 Kernel API Reference" (blockwise_mm_bwd_mxfp8): parameters
+ *         hidden_states, expert_affinities_masked, gate_up_proj_weight [E,H,2,I],
+ *         down_proj_weight [E,I,H], token_position_to_id [N*B], block_to_expert [N,1],
+ *         output_hidden_states_grad, block_size in {128,256,512,1024},
+ *         gate_up_proj_act_checkpoint_T [N,2,I,B], gate_up_weight_scales, down_weight_scales;
+ *         the returned gradient tuple; "Dimensions": N = (T*TopK - (E-1))/B + E - 1.
+ *   [MM]  "Matmul MXFP8 Backward Kernel API Reference" (matmul_mxfp8_backward): "Forward pass
+ *         convention" Y = X @ W^T; dX = dY @ W; dW = dY^T @ X; float8_dtype; output_dtype.
+ *   [SM]  sonic-moe functional/backward.py: expert_frequency_offset, x_gather_idx, s_scatter_idx,
+ *         s_reverse_scatter_idx; _down_projection_backward_act (gemm_dgated with colvec_scale and
+ *         colvec_reduce), db2_and_ds_kernel, _down_projection_backward_weight,
+ *         _up_projection_backward_act, db1_kernel, _up_projection_backward_weight,
+ *         _token_broadcast_backward.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked (device) are CUDA device pointers on the current device; (host) are host.
+ *     The library never allocates device memory: scratch comes from the caller's workspace,
+ *     whose size the matching *_workspace_size() call reports.  Workspace pointers must be
+ *     256-byte aligned.
+ *   - BF16 tensors are passed as `const void*` / `void*` holding IEEE bfloat16 values; all
+ *     matrices are dense row-major with the shapes given.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream) and do
+ *     not synchronise the host.  Inputs are never modified; outputs are overwritten.
+ *   - Return value: MOE_OK, or a negative MOE_ERR_* code; moe_last_error() then holds a message
+ *     (per host thread).  Errors detected on the device (invalid expert ids, a pipeline wait that
+ *     ran out of time) are OR-ed into the caller's `status_dev` word, readable after the stream
+ *     has been synchronised; a nonzero word means the outputs are not valid.
+ */
+#ifndef MOEBWD_H
+#define MOEBWD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same handle as cudaStream_t */
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = -1,     /* null pointer, bad shape, misaligned buffer, workspace too small */
+  MOE_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. H not a multiple of 128) */
+  MOE_ERR_CUDA = -3,        /* a CUDA launch or driver call failed */
+  MOE_ERR_DEVICE = -4       /* reserved: device-side errors are reported through status_dev */
+};
+
+/* Bits of the device status word. */
+enum {
+  MOE_STATUS_BAD_EXPERT_ID = 1, /* some ids[t,k] outside [0,E); those rows are skipped */
+  MOE_STATUS_TIMEOUT = 2        /* a pipeline wait exceeded its time limit; outputs invalid */
+};
+
+enum { MOE_PREC_BF16 = 0, MOE_PREC_MXFP8 = 1 };
+/* Where the routing affinity multiplies in the forward ([BW] down_proj_act_checkpoint "Affinity H
+ * mode", scaled_intermediate_checkpoint_T "Affinity I mode").  The forward value is the same in
+ * both; the mode selects which operand of the dW_down GEMM carries the score. */
+enum { MOE_AFFINITY_ON_H = 0, MOE_AFFINITY_ON_I = 1 };
+enum { MOE_FP8_E4M3 = 0, MOE_FP8_E5M2 = 1 };
+/* Quantisation direction of mxfp8_quantize. */
+enum { MOE_QUANT_ROWWISE = 0, MOE_QUANT_COLWISE = 1 };
+/* Layout of E8M0 scale bytes. */
+enum { MOE_SF_PLAIN = 0, MOE_SF_TILED = 1 };
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char* moe_last_error(void);
+
+/* Library version string. */
+const char* moe_version(void);
+
+/* ------------------------------------------------------------------------------------------ */
+/* Routing metadata                                                                            */
+/* ------------------------------------------------------------------------------------------ */
+
+/* [BW] "Dimensions": N = ceil((T*K - (E-1)) / B) + E - 1, the largest number of blocks any
+ * routing of T*K rows over E experts needs (the "/" is read as a ceiling division); T*K when
+ * T*K < E - 1; 0 when T*K == 0.  Pure host function. */
+int64_t moe_num_blocks_bound(int64_t T, int K, int E, int block_size);
+
+/* Bytes of workspace moe_route_meta needs. */
+size_t moe_route_meta_workspace_size(int T, int K, int E, int block_size);
+
+/* Routing metadata from expert ids ([BW] token_position_to_id, block_to_expert; [SM]
+ * expert_frequency_offset, x_gather_idx, s_scatter_idx, s_reverse_scatter_idx).
+ *
+ * ids (device) int32 [T,K].  Rows are grouped by expert; inside an expert the order is by flat
+ * index f = t*K + k (stable).  Outputs (device, int32), with TKv = number of valid ids:
+ *   expert_offsets [E+1]        exclusive prefix of per-expert row counts
+ *   x_gather_idx [T*K]          grouped row r < TKv -> token t
+ *   s_scatter_idx [T*K]         grouped row r < TKv -> flat index f
+ *   s_reverse_scatter_idx [T*K] flat f -> grouped row, -1 for an invalid id
+ *   token_position_to_id [N*B]  slot -> token, -1 for padding (N = moe_num_blocks_bound)
+ *   block_to_expert [N]         block -> expert, -1 for blocks >= *num_blocks
+ *   block_offsets [E+1]         exclusive prefix of ceil(n_e / B)
+ *   num_blocks [1]              total blocks in use
+ * status_dev (device) int32 [1]: MOE_STATUS_BAD_EXPERT_ID is OR-ed in for ids outside [0,E).
+ * Entries x_gather_idx / s_scatter_idx [TKv, T*K) are left unchanged.  block_size must be one of
+ * 128, 256, 512, 1024; 1 <= E <= 4096; T*K < 2^31. */
+int moe_route_meta(const int32_t* ids, int T, int K, int E, int block_size, int32_t* expert_offsets,
+                   int32_t* x_gather_idx, int32_t* s_scatter_idx, int32_t* s_reverse_scatter_idx,
+                   int32_t* token_position_to_id, int32_t* block_to_expert, int32_t* block_offsets,
+                   int32_t* num_blocks, int32_t* status_dev, void* workspace, size_t workspace_bytes,
+                   moe_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* MXFP8 quantisation                                                                          */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Quantise a BF16 matrix to MXFP8: groups of 32 consecutive elements along one dimension share an
+ * E8M0 scale ([BW] first paragraph, gate_up_weight_scales; [MM] float8_dtype).  Scale rule (OCP
+ * MX v1.0): byte = clamp(floor(log2(amax)) - emax + 127, 0, 254), emax = 8 (e4m3) / 15 (e5m2),
+ * floor(log2) taken from the binary exponent of amax; element = round-to-nearest-even of
+ * v * 2^(127 - byte), saturated to +-448 / +-57344; zero encodes as 0x00.
+ *
+ * in (device) bf16 [src_rows, cols] with row stride `ld` elements (ld >= cols, ld % 8 == 0).
+ * row_index (device, nullable) int32 [rows]: output row r reads input row row_index[r], -1 reads
+ *   zeros; NULL means row r reads row r (then rows <= src_rows).
+ * axis = MOE_QUANT_ROWWISE: groups run along cols; q (device) is [rows, cols];
+ *   scales (device) are [rows, cols/32] (PLAIN) or tiled for the [rows, cols] matrix.
+ * axis = MOE_QUANT_COLWISE: groups run along rows; q (device) holds the TRANSPOSED matrix
+ *   [cols, rows] so that every group is contiguous; scales are [cols, rows/32] (PLAIN) or tiled
+ *   for the [cols, rows] matrix.
+ * Tiled scale layout (MOE_SF_TILED), the one the block-scaled tensor-core MMA consumes, for a
+ * quantised matrix [R, C] (groups along C): 512-byte atoms of 128 rows x 4 groups, atom (R/128 x
+ * C/128 grid, row-major) at byte ((r/128)*(C/128) + c/128)*512, inside it byte
+ * (r%32)*16 + ((r%128)/32)*4 + (c/32)%4.  It requires R % 128 == 0 and C % 128 == 0.
+ * The grouped dimension must be a multiple of 32, the other a multiple of 16 (ROWWISE) or
+ * 128 (COLWISE). */
+int mxfp8_quantize(const void* in, int64_t src_rows, int64_t rows, int64_t cols, int64_t ld,
+                   const int32_t* row_index, int axis, int fp8_fmt, uint8_t* q, uint8_t* scales,
+                   int scale_layout, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* MoE layer backward                                                                          */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Arguments of moe_bwd.  Forward being differentiated ([BW] Background; [SM] backward.py): for
+ * every token t and slot k with e = ids[t,k], h = x_t W1_e + b1_e (gate = h[:I], up = h[I:]),
+ * a = SiLU(gate) * up, y = a W2_e + b2_e, out_t = sum_k s[t,k] y.  The pass returns
+ *   dx = d<dout,out>/dx [T,H] (bf16), dW1 [E,H,2I] (bf16), dW2 [E,I,H] (bf16),
+ *   ds[t,k] = <dout_t, y> [T,K] (fp32), db1 [E,2I] and db2 [E,H] (fp32, when has_bias).
+ * Experts that receive no row get zero gradients. */
+typedef struct MoeBwdArgs {
+  int T, H, I, E, K;  /* tokens, hidden, intermediate (per half), experts, top-K */
+  int block_size;     /* B in {128,256,512,1024}: block layout of the checkpoint */
+  int precision;      /* MOE_PREC_BF16 or MOE_PREC_MXFP8 */
+  int affinity;       /* MOE_AFFINITY_ON_H or MOE_AFFINITY_ON_I */
+  int fp8_act;        /* MXFP8: format of activation-side operands (dout, x, dh, a'), default E5M2 */
+  int fp8_w;          /* MXFP8: format of the pre-quantised weights, default E4M3 */
+  int has_bias;       /* produce db1/db2 and add <dout_t, b2_e> to ds (BF16 precision only) */
+
+  const void* x;     /* (device) bf16 [T,H]  hidden_states */
+  const void* dout;  /* (device) bf16 [T,H]  output_hidden_states_grad */
+  const void* W1;    /* (device) bf16 [E,H,2I] gate|up weights (BF16 precision) */
+  const void* W2;    /* (device) bf16 [E,I,H] down weights (BF16 precision) */
+  const uint8_t* W1_q;  /* (device) MXFP8: W1 as [E*H, 2I] quantised ROWWISE (groups along 2I) */
+  const uint8_t* W1_sf; /*          its scales, MOE_SF_TILED for the [E*H, 2I] matrix */
+  const uint8_t* W2_q;  /* (device) MXFP8: W2 as [E*I, H] quantised ROWWISE (groups along H) */
+  const uint8_t* W2_sf; /*          its scales, MOE_SF_TILED for the [E*I, H] matrix */
+  const void* b2;       /* (device) bf16 [E,H] down bias (has_bias) */
+  const float* s;       /* (device) fp32 [T,K] routing scores */
+  const int32_t* ids;   /* (device) int32 [T,K] expert ids */
+  const void* gate_up_ckpt; /* (device) bf16 [N,2,I,B] gate/up pre-activation checkpoint in the
+                               block layout of moe_route_meta (N = moe_num_blocks_bound):
+                               gate of the j-th row of expert e at [blk,0,:,b], up at [blk,1,:,b],
+                               slot blk*B + b = block_offsets[e]*B + j. */
+
+  void* dx;     /* (device) bf16 [T,H] */
+  void* dW1;    /* (device) bf16 [E,H,2I] */
+  void* dW2;    /* (device) bf16 [E,I,H] */
+  float* ds;    /* (device) fp32 [T,K] */
+  float* db1;   /* (device) fp32 [E,2I] (has_bias) */
+  float* db2;   /* (device) fp32 [E,H] (has_bias) */
+
+  int32_t* status_dev;    /* (device) int32 [1]; reset to 0 by the call, then OR-ed with MOE_STATUS_* */
+  void* workspace;        /* (device) scratch, 256-byte aligned */
+  size_t workspace_bytes; /* >= moe_bwd_workspace_size(args) */
+} MoeBwdArgs;
+
+/* Bytes of workspace moe_bwd needs for these shapes and options (pointers are not read). */
+size_t moe_bwd_workspace_size(const MoeBwdArgs* args);
+
+/* The whole backward on `stream`: routing metadata, gathers/quantisation, the four grouped GEMMs
+ * (dA with the fused dSwiGLU/ds epilogue, dW_down, dx_expanded, dW_gate_up), the top-K
+ * scatter-sum into dx, ds and the bias gradients.  Requirements: H % 128 == 0, I % 128 == 0,
+ * 1 <= K <= E <= 4096, T*K < 2^31, x/dout/weights 16-byte aligned. */
+int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream);
+
+/* Regions of the moe_bwd workspace (for inspection of intermediates in tests and debugging).
+ * Rows of the grouped operands are "tile rows": the rows of expert e occupy
+ * [tile_offsets[e], tile_offsets[e] + n_e) with tile_offsets[e] a multiple of 128 and padding rows
+ * zero; P = capacity of the tile-row space. */
+enum {
+  MOE_WS_EXPERT_OFFSETS = 0, /* int32 [E+1] */
+  MOE_WS_TILE_OFFSETS,       /* int32 [E+1] */
+  MOE_WS_BLOCK_OFFSETS,      /* int32 [E+1] */
+  MOE_WS_TILE_ROW_FLAT,      /* int32 [P]   tile row -> flat t*K+k, -1 padding */
+  MOE_WS_FLAT_TILE_ROW,      /* int32 [T*K] flat -> tile row, -1 invalid id */
+  MOE_WS_DOUT_G,             /* G1 A operand: dout rows [P,H] (bf16 | fp8) */
+  MOE_WS_DOUT_G_SF,          /*   its tiled scales (MXFP8) */
+  MOE_WS_DOUT_GT,            /* G3 B operand: [H,P] (bf16 | fp8), s-scaled for affinity on H */
+  MOE_WS_DOUT_GT_SF,
+  MOE_WS_X_GT,               /* G4 A operand: [H,P] */
+  MOE_WS_X_GT_SF,
+  MOE_WS_DH,                 /* G2 A operand: dh [P,2I] */
+  MOE_WS_DH_SF,
+  MOE_WS_DH_T,               /* G4 B operand: dh^T [2I,P] */
+  MOE_WS_DH_T_SF,
+  MOE_WS_AP_T,               /* G3 A operand: a'^T [I,P] (s*a for affinity on I, a on H) */
+  MOE_WS_AP_T_SF,
+  MOE_WS_DX_EXP,             /* G2 output: dx_expanded [P,H] bf16 */
+  MOE_WS_NUM_REGIONS
+};
+/* Offset and size in bytes of one region inside the workspace (0 bytes when unused). */
+int moe_bwd_workspace_region(const MoeBwdArgs* args, int region, size_t* offset, size_t* bytes);
+
+/* Capacity P of the tile-row space for these shapes. */
+int64_t moe_tile_rows_capacity(int T, int K, int E);
+
+/* ------------------------------------------------------------------------------------------ */
+/* Dense linear backward (the E=1, K=1 degenerate case)                                        */
+/* ------------------------------------------------------------------------------------------ */
+
+/* [MM] "Forward pass convention": Y = X @ W^T with X [M,K], W [N,K]; returns dX = dY @ W [M,K]
+ * and dW = dY^T @ X [N,K] in bf16.  precision MOE_PREC_MXFP8 quantises every operand in 32-groups
+ * along its GEMM's contraction dimension (dY and W along N for dX; dY and X along M for dW) with
+ * `fp8_fmt` (the page's default is e5m2); MOE_PREC_BF16 multiplies the BF16 values directly.
+ * dY, W, X, dX, dW (device) bf16; M, N, K multiples of 128. */
+size_t linear_bwd_workspace_size(int64_t M, int64_t N, int64_t K, int precision);
+int linear_bwd(const void* dY, const void* W, const void* X, int64_t M, int64_t N, int64_t K, int precision,
+               int fp8_fmt, void* dX, void* dW, void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOEBWD_H */

@@ -1,0 +1,14 @@
+// BF16 instantiations of the tcgen05 grouped GEMM (kind::f16, FP32 accumulation in TMEM).
+#include "gemm_kernel.cuh"
+
+namespace moebwd {
+
+int launch_gemm_bf16(int BN, const GemmParams& p, const void* tmA, const void* tmB, int grid, cudaStream_t st) {
+  if (p.epi == kEpiStore)
+    return BN == 256 ? gemm_launch_instance<false, 256, kEpiStore>(p, tmA, tmB, grid, st)
+                     : gemm_launch_instance<false, 128, kEpiStore>(p, tmA, tmB, grid, st);
+  return BN == 256 ? gemm_launch_instance<false, 256, kEpiDSwiGLU>(p, tmA, tmB, grid, st)
+                   : gemm_launch_instance<false, 128, kEpiDSwiGLU>(p, tmA, tmB, grid, st);
+}
+
+}  // namespace moebwd

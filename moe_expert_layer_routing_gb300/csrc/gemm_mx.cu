@@ -1,0 +1,15 @@
+// MXFP8 instantiations of the tcgen05 grouped GEMM (kind::mxf8f6f4 block-scaled, E8M0 scales per
+// 32 K-elements staged into TMEM with tcgen05.cp, FP32 accumulation in TMEM).
+#include "gemm_kernel.cuh"
+
+namespace moebwd {
+
+int launch_gemm_mx(int BN, const GemmParams& p, const void* tmA, const void* tmB, int grid, cudaStream_t st) {
+  if (p.epi == kEpiStore)
+    return BN == 256 ? gemm_launch_instance<true, 256, kEpiStore>(p, tmA, tmB, grid, st)
+                     : gemm_launch_instance<true, 128, kEpiStore>(p, tmA, tmB, grid, st);
+  return BN == 256 ? gemm_launch_instance<true, 256, kEpiDSwiGLU>(p, tmA, tmB, grid, st)
+                   : gemm_launch_instance<true, 128, kEpiDSwiGLU>(p, tmA, tmB, grid, st);
+}
+
+}  // namespace moebwd

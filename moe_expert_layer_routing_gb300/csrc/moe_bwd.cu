@@ -1,0 +1,522 @@
+// Host side of the MoE backward and of the dense linear backward: argument checks, workspace
+// layout, and the launch sequence on one stream (no host synchronisation):
+//
+//   route meta -> prep (gather, transpose, quantise) -> G1 dA + dSwiGLU epilogue ->
+//   G3 dW2 (K-grouped) -> G2 dx_expanded (M-grouped) -> G4 dW1 (K-grouped) ->
+//   dx scatter-sum, ds finalize, bias column sums
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "moebwd_internal.h"
+
+namespace moebwd {
+
+int launch_gemm(bool mx, int BN, const GemmParams& p, const void* A, int64_t a_rows, int64_t a_cols, const void* B,
+                int64_t b_rows, int64_t b_cols, cudaStream_t st) {
+  alignas(64) CUtensorMap ta, tb;
+  const int es = mx ? 1 : 2;
+  const uint32_t bke = mx ? 128 : 64;
+  if (!make_tmap_2d(&ta, A, es, (uint64_t)a_rows, (uint64_t)a_cols, (uint64_t)a_cols * es, 128, bke))
+    return MOE_ERR_INVALID;
+  if (!make_tmap_2d(&tb, B, es, (uint64_t)b_rows, (uint64_t)b_cols, (uint64_t)b_cols * es, (uint32_t)BN, bke))
+    return MOE_ERR_INVALID;
+  const int64_t tiles = (int64_t)(p.mode == kMGrouped ? p.m_tiles : p.num_experts * p.m_tiles) * p.n_tiles;
+  const int grid = (int)std::min<int64_t>(tiles, device_sm_count());
+  if (grid <= 0) return MOE_OK;
+  return mx ? launch_gemm_mx(BN, p, &ta, &tb, grid, st) : launch_gemm_bf16(BN, p, &ta, &tb, grid, st);
+}
+
+// ------------------------------------------------------------------------------------------
+// workspace layout
+// ------------------------------------------------------------------------------------------
+enum Region {
+  R_CHUNK_COUNTS, R_EXPERT_OFFSETS, R_BLOCK_OFFSETS, R_TILE_OFFSETS, R_EXPERT_ORDER, R_SCALARS,
+  R_X_GATHER, R_S_SCATTER, R_S_REV, R_TPID, R_B2E, R_TILE_ROW_FLAT, R_FLAT_TILE_ROW, R_TILE_EXPERT,
+  R_DOUT_G, R_DOUT_G_SF, R_DOUT_GT, R_DOUT_GT_SF, R_X_GT, R_X_GT_SF, R_DH, R_DH_SF, R_DH_T, R_DH_T_SF,
+  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNT
+};
+
+struct Layout {
+  size_t off[R_COUNT];
+  size_t bytes[R_COUNT];
+  size_t total;
+  int64_t P, Nb, TK;
+  int BN1, BN2, BN3, BN4;
+};
+
+static int64_t tile_capacity(int64_t TK, int E) {
+  if (TK <= 0) return 0;
+  const int64_t ne = std::min<int64_t>(E, TK);
+  return (TK + ne * (kTileM - 1) + kTileM - 1) / kTileM * kTileM;
+}
+
+static int64_t blocks_bound(int64_t T, int K, int E, int B) {
+  const int64_t TK = T * K;
+  if (TK <= 0) return 0;
+  const int64_t num = TK - (E - 1);
+  if (num <= 0) return TK;
+  return (num + B - 1) / B + E - 1;
+}
+
+static Layout make_layout(const MoeBwdArgs& a) {
+  Layout L{};
+  const bool mx = a.precision == MOE_PREC_MXFP8;
+  const int64_t es = mx ? 1 : 2;
+  L.TK = (int64_t)a.T * a.K;
+  L.P = tile_capacity(L.TK, a.E);
+  L.Nb = blocks_bound(a.T, a.K, a.E, a.block_size);
+  L.BN1 = a.I % 256 == 0 ? 256 : 128;
+  L.BN2 = a.H % 256 == 0 ? 256 : 128;
+  L.BN3 = L.BN2;
+  L.BN4 = 256;
+  const int64_t P = L.P, H = a.H, I = a.I, E = a.E;
+  size_t b[R_COUNT] = {};
+  b[R_CHUNK_COUNTS] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, route_nchunks(L.TK)) * E;
+  b[R_EXPERT_OFFSETS] = b[R_BLOCK_OFFSETS] = b[R_TILE_OFFSETS] = sizeof(int32_t) * (E + 1);
+  b[R_EXPERT_ORDER] = sizeof(int32_t) * E;
+  b[R_SCALARS] = 16;
+  b[R_X_GATHER] = b[R_S_SCATTER] = b[R_S_REV] = b[R_FLAT_TILE_ROW] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, L.TK);
+  b[R_TPID] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, L.Nb * a.block_size);
+  b[R_B2E] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, L.Nb);
+  b[R_TILE_ROW_FLAT] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, P);
+  b[R_TILE_EXPERT] = sizeof(int32_t) * (size_t)(P / kTileM + 1);
+  b[R_DOUT_G] = (size_t)(P * H * es);
+  b[R_DOUT_GT] = (size_t)(H * P * es);
+  b[R_X_GT] = (size_t)(H * P * es);
+  b[R_DH] = (size_t)(P * 2 * I * es);
+  b[R_DH_T] = (size_t)(2 * I * P * es);
+  b[R_AP_T] = (size_t)(I * P * es);
+  if (mx) {
+    b[R_DOUT_G_SF] = (size_t)(P * H / 32);
+    b[R_DOUT_GT_SF] = (size_t)(H * P / 32);
+    b[R_X_GT_SF] = (size_t)(H * P / 32);
+    b[R_DH_SF] = (size_t)(P * 2 * I / 32);
+    b[R_DH_T_SF] = (size_t)(2 * I * P / 32);
+    b[R_AP_T_SF] = (size_t)(I * P / 32);
+  }
+  b[R_DX_EXP] = (size_t)(P * H * 2);
+  b[R_DS_PART] = sizeof(float) * (size_t)(P * (I / L.BN1));
+  b[R_DS_BIAS] = a.has_bias ? sizeof(float) * (size_t)P : 0;
+  size_t off = 0;
+  for (int r = 0; r < R_COUNT; ++r) {
+    L.off[r] = off;
+    L.bytes[r] = b[r];
+    off = align_up(off + b[r], 256);
+  }
+  L.total = off;
+  return L;
+}
+
+static int check_args(const MoeBwdArgs* a, bool need_ptrs) {
+  if (!a) return fail(MOE_ERR_INVALID, "moe_bwd: null args");
+  if (a->T < 0 || a->H <= 0 || a->I <= 0 || a->E <= 0 || a->K <= 0)
+    return fail(MOE_ERR_INVALID, "moe_bwd: sizes must be positive (T >= 0)");
+  if (a->E > kMaxExperts) return fail(MOE_ERR_UNSUPPORTED, "moe_bwd: E above %d", kMaxExperts);
+  if (a->K > a->E || a->K > 64) return fail(MOE_ERR_INVALID, "moe_bwd: need K <= E and K <= 64");
+  if (a->H % 128 || a->I % 128) return fail(MOE_ERR_UNSUPPORTED, "moe_bwd: H and I must be multiples of 128");
+  if (a->block_size != 128 && a->block_size != 256 && a->block_size != 512 && a->block_size != 1024)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_bwd: block_size must be 128, 256, 512 or 1024");
+  if ((int64_t)a->T * a->K >= (int64_t)1 << 31) return fail(MOE_ERR_UNSUPPORTED, "moe_bwd: T*K too large");
+  if (a->precision != MOE_PREC_BF16 && a->precision != MOE_PREC_MXFP8)
+    return fail(MOE_ERR_INVALID, "moe_bwd: bad precision");
+  if (a->affinity != MOE_AFFINITY_ON_H && a->affinity != MOE_AFFINITY_ON_I)
+    return fail(MOE_ERR_INVALID, "moe_bwd: bad affinity");
+  const bool mx = a->precision == MOE_PREC_MXFP8;
+  if (mx && ((a->fp8_act != MOE_FP8_E4M3 && a->fp8_act != MOE_FP8_E5M2) ||
+             (a->fp8_w != MOE_FP8_E4M3 && a->fp8_w != MOE_FP8_E5M2)))
+    return fail(MOE_ERR_INVALID, "moe_bwd: bad fp8 format");
+  if (mx && a->has_bias) return fail(MOE_ERR_UNSUPPORTED, "moe_bwd: bias gradients are implemented for BF16 only");
+  if (!need_ptrs) return MOE_OK;
+  const void* req[] = {a->x, a->dout, a->s, a->ids, a->gate_up_ckpt, a->dx, a->dW1, a->dW2, a->ds, a->status_dev};
+  for (const void* q : req)
+    if (!q) return fail(MOE_ERR_INVALID, "moe_bwd: required pointer is null");
+  if (mx ? (!a->W1_q || !a->W1_sf || !a->W2_q || !a->W2_sf) : (!a->W1 || !a->W2))
+    return fail(MOE_ERR_INVALID, "moe_bwd: weights are null");
+  if (a->has_bias && (!a->b2 || !a->db1 || !a->db2)) return fail(MOE_ERR_INVALID, "moe_bwd: bias pointers are null");
+  const void* al16[] = {a->x, a->dout, mx ? (const void*)a->W1_q : a->W1, mx ? (const void*)a->W2_q : a->W2,
+                        a->W1_sf, a->W2_sf, a->dx, a->dW1, a->dW2, a->b2};
+  for (const void* q : al16)
+    if (reinterpret_cast<uintptr_t>(q) & 15) return fail(MOE_ERR_INVALID, "moe_bwd: tensors must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(a->workspace) & 255)
+    return fail(MOE_ERR_INVALID, "moe_bwd: workspace must be 256-byte aligned");
+  return MOE_OK;
+}
+
+template <typename T>
+static T* reg(const Layout& L, void* ws, int r) {
+  return L.bytes[r] ? reinterpret_cast<T*>(static_cast<char*>(ws) + L.off[r]) : nullptr;
+}
+
+}  // namespace moebwd
+
+using namespace moebwd;
+
+extern "C" int64_t moe_num_blocks_bound(int64_t T, int K, int E, int block_size) {
+  if (block_size <= 0 || E <= 0 || K <= 0 || T < 0) return 0;
+  return blocks_bound(T, K, E, block_size);
+}
+
+extern "C" int64_t moe_tile_rows_capacity(int T, int K, int E) { return tile_capacity((int64_t)T * K, E); }
+
+extern "C" size_t moe_bwd_workspace_size(const MoeBwdArgs* args) {
+  if (check_args(args, false) != MOE_OK) return 0;
+  return make_layout(*args).total;
+}
+
+extern "C" int moe_bwd_workspace_region(const MoeBwdArgs* args, int region, size_t* offset, size_t* bytes) {
+  clear_error();
+  int rc = check_args(args, false);
+  if (rc) return rc;
+  if (!offset || !bytes) return fail(MOE_ERR_INVALID, "moe_bwd_workspace_region: null output");
+  static const int map[MOE_WS_NUM_REGIONS] = {R_EXPERT_OFFSETS, R_TILE_OFFSETS, R_BLOCK_OFFSETS, R_TILE_ROW_FLAT,
+                                              R_FLAT_TILE_ROW,  R_DOUT_G,       R_DOUT_G_SF,     R_DOUT_GT,
+                                              R_DOUT_GT_SF,     R_X_GT,         R_X_GT_SF,       R_DH,
+                                              R_DH_SF,          R_DH_T,         R_DH_T_SF,       R_AP_T,
+                                              R_AP_T_SF,        R_DX_EXP};
+  if (region < 0 || region >= MOE_WS_NUM_REGIONS) return fail(MOE_ERR_INVALID, "bad region");
+  const Layout L = make_layout(*args);
+  *offset = L.off[map[region]];
+  *bytes = L.bytes[map[region]];
+  return MOE_OK;
+}
+
+extern "C" size_t moe_route_meta_workspace_size(int T, int K, int E, int block_size) {
+  if (T < 0 || K <= 0 || E <= 0 || E > kMaxExperts) return 0;
+  MoeBwdArgs a{};
+  a.T = T; a.K = K; a.E = E; a.block_size = block_size; a.H = 128; a.I = 128;
+  const Layout L = make_layout(a);
+  // the routing regions come first in the layout
+  return L.off[R_DOUT_G];
+}
+
+extern "C" int moe_route_meta(const int32_t* ids, int T, int K, int E, int block_size, int32_t* expert_offsets,
+                              int32_t* x_gather_idx, int32_t* s_scatter_idx, int32_t* s_reverse_scatter_idx,
+                              int32_t* token_position_to_id, int32_t* block_to_expert, int32_t* block_offsets,
+                              int32_t* num_blocks, int32_t* status_dev, void* workspace, size_t workspace_bytes,
+                              moe_stream_t stream) {
+  clear_error();
+  if (T < 0 || K <= 0 || E <= 0 || K > E) return fail(MOE_ERR_INVALID, "moe_route_meta: bad sizes");
+  if (E > kMaxExperts) return fail(MOE_ERR_UNSUPPORTED, "moe_route_meta: E above %d", kMaxExperts);
+  if (block_size != 128 && block_size != 256 && block_size != 512 && block_size != 1024)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_route_meta: block_size must be 128, 256, 512 or 1024");
+  if ((int64_t)T * K >= (int64_t)1 << 31) return fail(MOE_ERR_UNSUPPORTED, "moe_route_meta: T*K too large");
+  if (!ids || !expert_offsets || !x_gather_idx || !s_scatter_idx || !s_reverse_scatter_idx || !token_position_to_id ||
+      !block_to_expert || !block_offsets || !num_blocks || !status_dev || !workspace)
+    return fail(MOE_ERR_INVALID, "moe_route_meta: null pointer");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return fail(MOE_ERR_INVALID, "moe_route_meta: workspace must be 256-byte aligned");
+  const size_t need = moe_route_meta_workspace_size(T, K, E, block_size);
+  if (workspace_bytes < need) return fail(MOE_ERR_INVALID, "moe_route_meta: workspace too small (%zu < %zu)", workspace_bytes, need);
+  MoeBwdArgs a{};
+  a.T = T; a.K = K; a.E = E; a.block_size = block_size; a.H = 128; a.I = 128;
+  const Layout L = make_layout(a);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int rc = cuda_check(cudaMemsetAsync(status_dev, 0, sizeof(int32_t), st), "memset status");
+  if (rc) return rc;
+  RouteBufs r{};
+  r.chunk_counts = reg<int32_t>(L, workspace, R_CHUNK_COUNTS);
+  r.expert_offsets = expert_offsets;
+  r.block_offsets = block_offsets;
+  r.tile_offsets = reg<int32_t>(L, workspace, R_TILE_OFFSETS);
+  r.expert_order = reg<int32_t>(L, workspace, R_EXPERT_ORDER);
+  r.scalars = reg<int32_t>(L, workspace, R_SCALARS);
+  r.x_gather_idx = x_gather_idx;
+  r.s_scatter_idx = s_scatter_idx;
+  r.s_reverse = s_reverse_scatter_idx;
+  r.token_position_to_id = token_position_to_id;
+  r.block_to_expert = block_to_expert;
+  r.tile_row_flat = reg<int32_t>(L, workspace, R_TILE_ROW_FLAT);
+  r.flat_tile_row = reg<int32_t>(L, workspace, R_FLAT_TILE_ROW);
+  r.tile_expert = reg<int32_t>(L, workspace, R_TILE_EXPERT);
+  r.num_blocks_out = num_blocks;
+  r.status = status_dev;
+  return launch_route_meta(ids, T, K, E, block_size, L.Nb, L.P, r, st);
+}
+
+extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
+  clear_error();
+  int rc = check_args(args, true);
+  if (rc) return rc;
+  const MoeBwdArgs& a = *args;
+  const Layout L = make_layout(a);
+  if (a.workspace_bytes < L.total)
+    return fail(MOE_ERR_INVALID, "moe_bwd: workspace too small (%zu < %zu)", a.workspace_bytes, L.total);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  void* ws = a.workspace;
+  const bool mx = a.precision == MOE_PREC_MXFP8;
+  const int64_t H = a.H, I = a.I, E = a.E, P = L.P, TK = L.TK;
+  if ((rc = cuda_check(cudaMemsetAsync(a.status_dev, 0, sizeof(int32_t), st), "memset status"))) return rc;
+  if (TK == 0) {  // no routed rows: every gradient is zero
+    if ((rc = cuda_check(cudaMemsetAsync(a.dW1, 0, (size_t)(E * H * 2 * I * 2), st), "memset dW1"))) return rc;
+    if ((rc = cuda_check(cudaMemsetAsync(a.dW2, 0, (size_t)(E * I * H * 2), st), "memset dW2"))) return rc;
+    if (a.has_bias) {
+      if ((rc = cuda_check(cudaMemsetAsync(a.db1, 0, (size_t)(E * 2 * I * 4), st), "memset db1"))) return rc;
+      if ((rc = cuda_check(cudaMemsetAsync(a.db2, 0, (size_t)(E * H * 4), st), "memset db2"))) return rc;
+    }
+    return MOE_OK;
+  }
+
+  int32_t* tile_offsets = reg<int32_t>(L, ws, R_TILE_OFFSETS);
+  int32_t* expert_order = reg<int32_t>(L, ws, R_EXPERT_ORDER);
+  int32_t* scalars = reg<int32_t>(L, ws, R_SCALARS);
+  int32_t* tile_row_flat = reg<int32_t>(L, ws, R_TILE_ROW_FLAT);
+  int32_t* flat_tile_row = reg<int32_t>(L, ws, R_FLAT_TILE_ROW);
+  int32_t* tile_expert = reg<int32_t>(L, ws, R_TILE_EXPERT);
+  int32_t* block_offsets = reg<int32_t>(L, ws, R_BLOCK_OFFSETS);
+
+  // 1. routing metadata
+  RouteBufs r{};
+  r.chunk_counts = reg<int32_t>(L, ws, R_CHUNK_COUNTS);
+  r.expert_offsets = reg<int32_t>(L, ws, R_EXPERT_OFFSETS);
+  r.block_offsets = block_offsets;
+  r.tile_offsets = tile_offsets;
+  r.expert_order = expert_order;
+  r.scalars = scalars;
+  r.x_gather_idx = reg<int32_t>(L, ws, R_X_GATHER);
+  r.s_scatter_idx = reg<int32_t>(L, ws, R_S_SCATTER);
+  r.s_reverse = reg<int32_t>(L, ws, R_S_REV);
+  r.token_position_to_id = reg<int32_t>(L, ws, R_TPID);
+  r.block_to_expert = reg<int32_t>(L, ws, R_B2E);
+  r.tile_row_flat = tile_row_flat;
+  r.flat_tile_row = flat_tile_row;
+  r.tile_expert = tile_expert;
+  r.num_blocks_out = nullptr;
+  r.status = a.status_dev;
+  if ((rc = launch_route_meta(a.ids, a.T, a.K, a.E, a.block_size, L.Nb, P, r, st))) return rc;
+
+  // 2. gathered / transposed / quantised activation operands
+  PrepArgs pa{};
+  pa.dout = static_cast<const uint16_t*>(a.dout);
+  pa.x = static_cast<const uint16_t*>(a.x);
+  pa.s = a.s;
+  pa.b2 = a.has_bias ? static_cast<const uint16_t*>(a.b2) : nullptr;
+  pa.tile_row_flat = tile_row_flat;
+  pa.tile_expert = tile_expert;
+  pa.num_tiles = scalars + 1;
+  pa.H = a.H;
+  pa.K = a.K;
+  pa.P = P;
+  pa.mx = mx;
+  pa.fmt = a.fp8_act;
+  pa.scale_t = a.affinity == MOE_AFFINITY_ON_H;
+  pa.dout_g = reg<void>(L, ws, R_DOUT_G);
+  pa.dout_g_sf = reg<uint8_t>(L, ws, R_DOUT_G_SF);
+  pa.dout_gt = reg<void>(L, ws, R_DOUT_GT);
+  pa.dout_gt_sf = reg<uint8_t>(L, ws, R_DOUT_GT_SF);
+  pa.x_gt = reg<void>(L, ws, R_X_GT);
+  pa.x_gt_sf = reg<uint8_t>(L, ws, R_X_GT_SF);
+  pa.ds_bias = a.has_bias ? reg<float>(L, ws, R_DS_BIAS) : nullptr;
+  if ((rc = launch_prep(pa, st))) return rc;
+
+  const void* W1 = mx ? static_cast<const void*>(a.W1_q) : a.W1;
+  const void* W2 = mx ? static_cast<const void*>(a.W2_q) : a.W2;
+
+  // 3. G1: dA_raw = dout_g W2_e^T with the dSwiGLU / ds epilogue
+  {
+    GemmParams p{};
+    p.mode = kMGrouped;
+    p.M = (int)P; p.N = (int)I; p.K = (int)H;
+    p.m_tiles = (int)(P / kTileM);
+    p.n_tiles = (int)(I / L.BN1);
+    p.num_experts = (int)E;
+    p.tile_expert = tile_expert;
+    p.num_tiles = scalars + 1;
+    p.b_rows_per_expert = (int)I;
+    p.sfa = reg<uint8_t>(L, ws, R_DOUT_G_SF);
+    p.sfb = a.W2_sf;
+    p.sfa_ktiles = p.sfb_ktiles = (int)(H / 128);
+    p.fmt_a = a.fp8_act; p.fmt_b = a.fp8_w;
+    p.epi = kEpiDSwiGLU;
+    p.s = a.s;
+    p.tile_row_flat = tile_row_flat;
+    p.e_tile_offsets = tile_offsets;
+    p.block_offsets = block_offsets;
+    p.ckpt = static_cast<const uint16_t*>(a.gate_up_ckpt);
+    p.I = a.I; p.B = a.block_size;
+    p.affinity_on_i = a.affinity == MOE_AFFINITY_ON_I;
+    p.fmt_act = a.fp8_act;
+    p.P = P;
+    p.dh = reg<void>(L, ws, R_DH); p.dh_sf = reg<uint8_t>(L, ws, R_DH_SF);
+    p.dht = reg<void>(L, ws, R_DH_T); p.dht_sf = reg<uint8_t>(L, ws, R_DH_T_SF);
+    p.apt = reg<void>(L, ws, R_AP_T); p.apt_sf = reg<uint8_t>(L, ws, R_AP_T_SF);
+    p.ds_part = reg<float>(L, ws, R_DS_PART);
+    p.status = a.status_dev;
+    if ((rc = launch_gemm(mx, L.BN1, p, reg<void>(L, ws, R_DOUT_G), P, H, W2, E * I, H, st))) return rc;
+  }
+  // 4. G3: dW2_e = a'^T dout_g over the expert's tile rows
+  {
+    GemmParams p{};
+    p.mode = kKGrouped;
+    p.M = (int)I; p.N = (int)H;
+    p.m_tiles = (int)(I / kTileM);
+    p.n_tiles = (int)(H / L.BN3);
+    p.num_experts = (int)E;
+    p.tile_offsets = tile_offsets;
+    p.expert_order = expert_order;
+    p.sfa = reg<uint8_t>(L, ws, R_AP_T_SF);
+    p.sfb = reg<uint8_t>(L, ws, R_DOUT_GT_SF);
+    p.sfa_ktiles = p.sfb_ktiles = (int)(P / 128);
+    p.fmt_a = a.fp8_act; p.fmt_b = a.fp8_act;
+    p.epi = kEpiStore;
+    p.out = a.dW2; p.ldo = H; p.out_expert_stride = I * H;
+    p.status = a.status_dev;
+    if ((rc = launch_gemm(mx, L.BN3, p, reg<void>(L, ws, R_AP_T), I, P, reg<void>(L, ws, R_DOUT_GT), H, P, st)))
+      return rc;
+  }
+  // 5. G2: dx_expanded = dh W1_e^T
+  {
+    GemmParams p{};
+    p.mode = kMGrouped;
+    p.M = (int)P; p.N = (int)H; p.K = (int)(2 * I);
+    p.m_tiles = (int)(P / kTileM);
+    p.n_tiles = (int)(H / L.BN2);
+    p.num_experts = (int)E;
+    p.tile_expert = tile_expert;
+    p.num_tiles = scalars + 1;
+    p.b_rows_per_expert = (int)H;
+    p.sfa = reg<uint8_t>(L, ws, R_DH_SF);
+    p.sfb = a.W1_sf;
+    p.sfa_ktiles = p.sfb_ktiles = (int)(2 * I / 128);
+    p.fmt_a = a.fp8_act; p.fmt_b = a.fp8_w;
+    p.epi = kEpiStore;
+    p.out = reg<void>(L, ws, R_DX_EXP); p.ldo = H;
+    p.status = a.status_dev;
+    if ((rc = launch_gemm(mx, L.BN2, p, reg<void>(L, ws, R_DH), P, 2 * I, W1, E * H, 2 * I, st))) return rc;
+  }
+  // 6. G4: dW1_e = x_g^T dh over the expert's tile rows
+  {
+    GemmParams p{};
+    p.mode = kKGrouped;
+    p.M = (int)H; p.N = (int)(2 * I);
+    p.m_tiles = (int)(H / kTileM);
+    p.n_tiles = (int)(2 * I / L.BN4);
+    p.num_experts = (int)E;
+    p.tile_offsets = tile_offsets;
+    p.expert_order = expert_order;
+    p.sfa = reg<uint8_t>(L, ws, R_X_GT_SF);
+    p.sfb = reg<uint8_t>(L, ws, R_DH_T_SF);
+    p.sfa_ktiles = p.sfb_ktiles = (int)(P / 128);
+    p.fmt_a = a.fp8_act; p.fmt_b = a.fp8_act;
+    p.epi = kEpiStore;
+    p.out = a.dW1; p.ldo = 2 * I; p.out_expert_stride = H * 2 * I;
+    p.status = a.status_dev;
+    if ((rc = launch_gemm(mx, L.BN4, p, reg<void>(L, ws, R_X_GT), H, P, reg<void>(L, ws, R_DH_T), 2 * I, P, st)))
+      return rc;
+  }
+  // 7. reductions
+  if ((rc = launch_dx_scatter_sum(reg<uint16_t>(L, ws, R_DX_EXP), flat_tile_row, a.T, a.K, a.H,
+                                  static_cast<uint16_t*>(a.dx), st)))
+    return rc;
+  if ((rc = launch_ds_finalize(reg<float>(L, ws, R_DS_PART), (int)(I / L.BN1), a.has_bias ? reg<float>(L, ws, R_DS_BIAS) : nullptr,
+                               flat_tile_row, TK, a.ds, st)))
+    return rc;
+  if (a.has_bias) {
+    if ((rc = launch_segment_rowsum(reg<uint16_t>(L, ws, R_DH_T), P, (int)(2 * I), tile_offsets, (int)E, nullptr,
+                                    tile_row_flat, a.db1, st)))
+      return rc;
+    if ((rc = launch_segment_rowsum(reg<uint16_t>(L, ws, R_DOUT_GT), P, (int)H, tile_offsets, (int)E,
+                                    a.affinity == MOE_AFFINITY_ON_I ? a.s : nullptr, tile_row_flat, a.db2, st)))
+      return rc;
+  }
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------------------------------------
+// dense linear backward
+// ------------------------------------------------------------------------------------------
+namespace {
+struct LinLayout {
+  size_t off[8], bytes[8], total;
+};
+LinLayout lin_layout(int64_t M, int64_t N, int64_t K, int precision) {
+  LinLayout L{};
+  const bool mx = precision == MOE_PREC_MXFP8;
+  const int64_t es = mx ? 1 : 2;
+  // 0 dY (rowwise, mx only) 1 its sf | 2 W^T [K,N] 3 sf | 4 dY^T [N,M] 5 sf | 6 X^T [K,M] 7 sf
+  size_t b[8] = {mx ? (size_t)(M * N) : 0, mx ? (size_t)(M * N / 32) : 0, (size_t)(K * N * es), mx ? (size_t)(K * N / 32) : 0,
+                 (size_t)(N * M * es), mx ? (size_t)(N * M / 32) : 0, (size_t)(K * M * es), mx ? (size_t)(K * M / 32) : 0};
+  size_t off = 0;
+  for (int i = 0; i < 8; ++i) {
+    L.off[i] = off;
+    L.bytes[i] = b[i];
+    off = align_up(off + b[i], 256);
+  }
+  L.total = off;
+  return L;
+}
+}  // namespace
+
+extern "C" size_t linear_bwd_workspace_size(int64_t M, int64_t N, int64_t K, int precision) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return lin_layout(M, N, K, precision).total;
+}
+
+extern "C" int linear_bwd(const void* dY, const void* W, const void* X, int64_t M, int64_t N, int64_t K, int precision,
+                          int fp8_fmt, void* dX, void* dW, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  clear_error();
+  if (!dY || !W || !X || !dX || !dW || !workspace) return fail(MOE_ERR_INVALID, "linear_bwd: null pointer");
+  if (M <= 0 || N <= 0 || K <= 0) return fail(MOE_ERR_INVALID, "linear_bwd: sizes must be positive");
+  if (M % 128 || N % 128 || K % 128) return fail(MOE_ERR_UNSUPPORTED, "linear_bwd: M, N, K must be multiples of 128");
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return fail(MOE_ERR_UNSUPPORTED, "linear_bwd: too large");
+  if (precision != MOE_PREC_BF16 && precision != MOE_PREC_MXFP8) return fail(MOE_ERR_INVALID, "linear_bwd: bad precision");
+  if (precision == MOE_PREC_MXFP8 && fp8_fmt != MOE_FP8_E4M3 && fp8_fmt != MOE_FP8_E5M2)
+    return fail(MOE_ERR_INVALID, "linear_bwd: bad fp8 format");
+  const void* al[] = {dY, W, X, dX, dW};
+  for (const void* q : al)
+    if (reinterpret_cast<uintptr_t>(q) & 15) return fail(MOE_ERR_INVALID, "linear_bwd: tensors must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(MOE_ERR_INVALID, "linear_bwd: workspace must be 256-byte aligned");
+  const LinLayout L = lin_layout(M, N, K, precision);
+  if (workspace_bytes < L.total) return fail(MOE_ERR_INVALID, "linear_bwd: workspace too small (%zu < %zu)", workspace_bytes, L.total);
+  const bool mx = precision == MOE_PREC_MXFP8;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  auto R = [&](int i) { return L.bytes[i] ? static_cast<void*>(ws + L.off[i]) : nullptr; };
+  const uint16_t* dYb = static_cast<const uint16_t*>(dY);
+  int rc;
+  // operands: dX = dY @ W contracts over N, dW = dY^T @ X contracts over M
+  if (mx && (rc = launch_quant_rowwise(dYb, M, M, N, N, nullptr, fp8_fmt, static_cast<uint8_t*>(R(0)),
+                                       static_cast<uint8_t*>(R(1)), 1, st)))
+    return rc;
+  if ((rc = launch_quant_colwise(static_cast<const uint16_t*>(W), N, N, K, K, nullptr, mx, fp8_fmt, R(2),
+                                 static_cast<uint8_t*>(R(3)), 1, st)))
+    return rc;
+  if ((rc = launch_quant_colwise(dYb, M, M, N, N, nullptr, mx, fp8_fmt, R(4), static_cast<uint8_t*>(R(5)), 1, st)))
+    return rc;
+  if ((rc = launch_quant_colwise(static_cast<const uint16_t*>(X), M, M, K, K, nullptr, mx, fp8_fmt, R(6),
+                                 static_cast<uint8_t*>(R(7)), 1, st)))
+    return rc;
+  const int BN = K % 256 == 0 ? 256 : 128;
+  {
+    GemmParams p{};
+    p.mode = kMGrouped;
+    p.M = (int)M; p.N = (int)K; p.K = (int)N;
+    p.m_tiles = (int)(M / 128);
+    p.n_tiles = (int)(K / BN);
+    p.num_experts = 1;
+    p.sfa = static_cast<const uint8_t*>(R(1));
+    p.sfb = static_cast<const uint8_t*>(R(3));
+    p.sfa_ktiles = p.sfb_ktiles = (int)(N / 128);
+    p.fmt_a = p.fmt_b = fp8_fmt;
+    p.epi = kEpiStore;
+    p.out = dX; p.ldo = K;
+    if ((rc = launch_gemm(mx, BN, p, mx ? R(0) : dY, M, N, R(2), K, N, st))) return rc;
+  }
+  {
+    GemmParams p{};
+    p.mode = kMGrouped;
+    p.M = (int)N; p.N = (int)K; p.K = (int)M;
+    p.m_tiles = (int)(N / 128);
+    p.n_tiles = (int)(K / BN);
+    p.num_experts = 1;
+    p.sfa = static_cast<const uint8_t*>(R(5));
+    p.sfb = static_cast<const uint8_t*>(R(7));
+    p.sfa_ktiles = p.sfb_ktiles = (int)(M / 128);
+    p.fmt_a = p.fmt_b = fp8_fmt;
+    p.epi = kEpiStore;
+    p.out = dW; p.ldo = K;
+    if ((rc = launch_gemm(mx, BN, p, R(4), N, M, R(6), K, M, st))) return rc;
+  }
+  return MOE_OK;
+}

@@ -1,0 +1,144 @@
+// Internal declarations shared by the translation units of libmoebwd.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moebwd.h"
+
+namespace moebwd {
+
+// Upper limit of any single pipeline wait inside a kernel before it reports MOE_STATUS_TIMEOUT.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+constexpr int kTileM = 128;       // rows of a GEMM tile = UMMA M = tile-row padding granule
+constexpr int kMaxExperts = 1024;
+constexpr int kRouteChunk = 4096; // flat ids per CTA in the routing kernels
+
+// ------------------------------------------------------------------------------------------
+// host helpers (host.cu)
+// ------------------------------------------------------------------------------------------
+int fail(int code, const char* fmt, ...);
+void clear_error();
+int cuda_check(cudaError_t e, const char* what);
+int device_sm_count();
+size_t align_up(size_t v, size_t a);
+
+// 2D tensor map over a row-major [rows, cols] matrix of `elem_bytes`-byte elements with the given
+// row pitch, box [box_rows, box_cols], 128-byte swizzle.  Returns false on failure (message set).
+bool make_tmap_2d(void* out_tmap /* CUtensorMap* */, const void* base, int elem_bytes, uint64_t rows,
+                  uint64_t cols, uint64_t row_pitch_bytes, uint32_t box_rows, uint32_t box_cols);
+
+// ------------------------------------------------------------------------------------------
+// routing (route_meta.cu)
+// ------------------------------------------------------------------------------------------
+struct RouteBufs {
+  int32_t* chunk_counts;      // [nchunks*E]
+  int32_t* expert_offsets;    // [E+1]
+  int32_t* block_offsets;     // [E+1]
+  int32_t* tile_offsets;      // [E+1]
+  int32_t* expert_order;      // [E] experts by descending row count
+  int32_t* scalars;           // [4]: num_blocks, num_tiles
+  int32_t* x_gather_idx;      // [TK]
+  int32_t* s_scatter_idx;     // [TK]
+  int32_t* s_reverse;         // [TK]
+  int32_t* token_position_to_id;  // [Nb*B]
+  int32_t* block_to_expert;   // [Nb]
+  int32_t* tile_row_flat;     // [P]
+  int32_t* flat_tile_row;     // [TK]
+  int32_t* tile_expert;       // [P/128]
+  int32_t* num_blocks_out;    // nullable public copy of scalars[0]
+  int32_t* status;
+};
+int route_nchunks(int64_t TK);
+int launch_route_meta(const int32_t* ids, int T, int K, int E, int B, int64_t Nb, int64_t P,
+                      const RouteBufs& r, cudaStream_t st);
+
+// ------------------------------------------------------------------------------------------
+// gathers / quantisation (prep.cu)
+// ------------------------------------------------------------------------------------------
+struct PrepArgs {
+  const uint16_t* dout;      // [T,H] bf16
+  const uint16_t* x;         // [T,H] bf16
+  const float* s;            // [T*K]
+  const uint16_t* b2;        // [E,H] bf16 or null
+  const int32_t* tile_row_flat;
+  const int32_t* tile_expert;
+  const int32_t* num_tiles;  // device scalar
+  int H, K;
+  int64_t P;                 // tile-row capacity (leading dim of transposed outputs)
+  int mx, fmt, scale_t;      // MXFP8 outputs; fp8 format; multiply dout^T by s (affinity on H)
+  void* dout_g; uint8_t* dout_g_sf;    // [P,H]
+  void* dout_gt; uint8_t* dout_gt_sf;  // [H,P]
+  void* x_gt; uint8_t* x_gt_sf;        // [H,P]
+  float* ds_bias;                      // [P] <dout_t, b2_e> or null
+};
+int launch_prep(const PrepArgs& a, cudaStream_t st);
+
+int launch_quant_rowwise(const uint16_t* in, int64_t src_rows, int64_t rows, int64_t cols, int64_t ld,
+                         const int32_t* row_index, int fmt, uint8_t* q, uint8_t* sf, int tiled, cudaStream_t st);
+// colwise: out is the transposed [cols, rows] matrix, fp8 (+scales) when mx, else bf16
+int launch_quant_colwise(const uint16_t* in, int64_t src_rows, int64_t rows, int64_t cols, int64_t ld,
+                         const int32_t* row_index, int mx, int fmt, void* q, uint8_t* sf, int tiled,
+                         cudaStream_t st);
+
+// ------------------------------------------------------------------------------------------
+// tcgen05 grouped GEMM (gemm_*.cu)
+// ------------------------------------------------------------------------------------------
+enum GemmMode { kMGrouped = 0, kKGrouped = 1 };
+enum EpiKind { kEpiStore = 0, kEpiDSwiGLU = 1 };
+
+struct GemmParams {
+  int mode;
+  int M, N, K;             // M-grouped: K = contraction; K-grouped: M, N per expert
+  int m_tiles;             // M-grouped: capacity tiles (used when num_tiles is null); K-grouped: M/128
+  int n_tiles;             // N / BN
+  int num_experts;
+  const int32_t* tile_expert;   // M-grouped: expert of each 128-row tile (null: expert 0)
+  const int32_t* num_tiles;     // M-grouped: device count of tiles (null: m_tiles)
+  const int32_t* tile_offsets;  // K-grouped: [E+1] tile-row offsets
+  const int32_t* expert_order;  // K-grouped: [E] processing order (null: 0..E-1)
+  int b_rows_per_expert;        // M-grouped: B rows per expert (0: shared B)
+  // block scales (MXFP8)
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  int sfa_ktiles, sfb_ktiles;   // 128-column tiles along K in the tiled scale layouts
+  int fmt_a, fmt_b;
+  // epilogue
+  int epi;
+  void* out;
+  int64_t ldo;
+  int64_t out_expert_stride;    // K-grouped: elements between experts' outputs
+  // dSwiGLU epilogue (G1)
+  const float* s;
+  const int32_t* tile_row_flat;
+  const int32_t* e_tile_offsets;
+  const int32_t* block_offsets;
+  const uint16_t* ckpt;         // [N,2,I,B]
+  int I, B, affinity_on_i, fmt_act;
+  int64_t P;
+  void* dh; uint8_t* dh_sf;
+  void* dht; uint8_t* dht_sf;
+  void* apt; uint8_t* apt_sf;
+  float* ds_part;               // [P, I/BN]
+  int32_t* status;
+};
+
+// A [rows, K] and B [rows, K] K-major operands (bf16 or fp8 bytes), tile counts in p.
+int launch_gemm(bool mx, int BN, const GemmParams& p, const void* A, int64_t a_rows, int64_t a_cols,
+                const void* B, int64_t b_rows, int64_t b_cols, cudaStream_t st);
+int launch_gemm_bf16(int BN, const GemmParams& p, const void* tmA, const void* tmB, int grid, cudaStream_t st);
+int launch_gemm_mx(int BN, const GemmParams& p, const void* tmA, const void* tmB, int grid, cudaStream_t st);
+
+// ------------------------------------------------------------------------------------------
+// reductions (reduce.cu)
+// ------------------------------------------------------------------------------------------
+int launch_dx_scatter_sum(const uint16_t* dx_exp, const int32_t* flat_tile_row, int T, int K, int H,
+                          uint16_t* dx, cudaStream_t st);
+int launch_ds_finalize(const float* ds_part, int nparts, const float* ds_bias, const int32_t* flat_tile_row,
+                       int64_t TK, float* ds, cudaStream_t st);
+// out[e, j] = sum over tile rows p of expert e of buf[j, p] (* w[flat(p)] when w != null)
+int launch_segment_rowsum(const uint16_t* buf, int64_t ld, int R, const int32_t* tile_offsets, int E,
+                          const float* w, const int32_t* tile_row_flat, float* out, cudaStream_t st);
+
+}  // namespace moebwd

@@ -1,0 +1,67 @@
+// Device-side MXFP8 helpers: E8M0 scale from a group amax, FP8 encoding, tiled scale offsets,
+// bf16 packing.  Shared by the quantisers and the GEMM epilogues.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cstdint>
+
+namespace moebwd {
+
+// OCP MX rule: byte = clamp(floor(log2(amax)) - emax + 127, 0, 254) with floor(log2(amax)) read
+// from the binary exponent field (a zero / subnormal amax gives byte 0); emax = 8 (e4m3), 15 (e5m2).
+__device__ __forceinline__ uint32_t e8m0_byte(uint32_t amax_bits, int fmt) {
+  const int e = (int)((amax_bits >> 23) & 0xFFu);
+  const int b = e - (fmt == MOE_FP8_E4M3 ? 8 : 15);
+  return (uint32_t)(b < 0 ? 0 : (b > 254 ? 254 : b));
+}
+
+// 2^(127 - byte) as a float (byte <= 246 for finite inputs, so this is a normal number).
+__device__ __forceinline__ float e8m0_inv_scale(uint32_t byte) {
+  return __uint_as_float((254u - byte) << 23);
+}
+
+// Round-to-nearest-even FP8 code of x, saturating to the largest finite value; zero -> 0x00.
+__device__ __forceinline__ uint32_t fp8_code(float x, int fmt) {
+  const __nv_fp8_storage_t c =
+      __nv_cvt_float_to_fp8(x, __NV_SATFINITE, fmt == MOE_FP8_E4M3 ? __NV_E4M3 : __NV_E5M2);
+  const uint32_t u = (uint32_t)c;
+  return (u & 0x7Fu) ? u : 0u;
+}
+
+// Byte offset of the scale of element (r, c) of an [R, C] matrix quantised along C, in the tiled
+// layout consumed by the block-scaled MMA: 512-byte atoms of 128 rows x 4 groups, atom grid
+// row-major over (R/128, C/128), inside an atom (r%32)*16 + ((r%128)/32)*4 + (c/32)%4.
+__device__ __forceinline__ int64_t sf_tiled_offset(int64_t r, int64_t c, int64_t C) {
+  return ((r >> 7) * (C >> 7) + (c >> 7)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + ((c >> 5) & 3);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
+}
+
+// Quantise 32 values of one group into 32 FP8 codes (packed little-endian into 8 words) and
+// return the scale byte.
+__device__ __forceinline__ uint32_t quantize_group32(const float (&v)[32], int fmt, uint32_t (&w)[8]) {
+  float am = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) am = fmaxf(am, fabsf(v[j]));
+  const uint32_t byte = e8m0_byte(__float_as_uint(am), fmt);
+  const float inv = e8m0_inv_scale(byte);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    w[j] = fp8_code(v[4 * j] * inv, fmt) | (fp8_code(v[4 * j + 1] * inv, fmt) << 8) |
+           (fp8_code(v[4 * j + 2] * inv, fmt) << 16) | (fp8_code(v[4 * j + 3] * inv, fmt) << 24);
+  }
+  return byte;
+}
+
+}  // namespace moebwd

@@ -1,0 +1,109 @@
+// Reductions after the grouped GEMMs:
+//   dx_scatter_sum   dx[t] = sum_k dx_expanded[row(t,k)]   (sonic-moe _token_broadcast_backward),
+//                    fp32 accumulation in ascending k, 16-byte vector loads, one CTA per token row
+//   ds_finalize      ds[f] = sum of the dA-epilogue partials of its row + <dout_t, b2_e>
+//                    (gemm_dgated colvec_reduce and db2_and_ds_kernel)
+//   segment_rowsum   db[e, j] = sum over the tile rows of expert e of buf[j, p] (* w_p)
+//                    (db1_kernel and the db2 half of db2_and_ds_kernel), one warp per (e, j)
+#include <cuda_runtime.h>
+
+#include "moebwd_internal.h"
+#include "mx_device.cuh"
+
+namespace moebwd {
+
+__global__ void __launch_bounds__(256) dx_scatter_sum_kernel(const uint16_t* __restrict__ dx_exp,
+                                                             const int32_t* __restrict__ flat_tile_row, int K, int H,
+                                                             uint16_t* __restrict__ dx) {
+  const int64_t t = blockIdx.x;
+  __shared__ int32_t rows[64];
+  if (threadIdx.x < K) rows[threadIdx.x] = flat_tile_row[t * K + threadIdx.x];
+  __syncthreads();
+  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < K; ++k) {
+      const int p = rows[k];
+      if (p < 0) continue;
+      const uint4 v = *reinterpret_cast<const uint4*>(dx_exp + (int64_t)p * H + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc[2 * j] += __uint_as_float(w[j] << 16);
+        acc[2 * j + 1] += __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+    }
+    *reinterpret_cast<uint4*>(dx + t * H + c) =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                   pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
+int launch_dx_scatter_sum(const uint16_t* dx_exp, const int32_t* flat_tile_row, int T, int K, int H, uint16_t* dx,
+                          cudaStream_t st) {
+  if (T == 0) return MOE_OK;
+  if (K > 64) return fail(MOE_ERR_UNSUPPORTED, "top-K above 64");
+  dx_scatter_sum_kernel<<<T, 256, 0, st>>>(dx_exp, flat_tile_row, K, H, dx);
+  return cuda_check(cudaGetLastError(), "dx_scatter_sum");
+}
+
+__global__ void ds_finalize_kernel(const float* __restrict__ ds_part, int nparts, const float* __restrict__ ds_bias,
+                                   const int32_t* __restrict__ flat_tile_row, int64_t TK, float* __restrict__ ds) {
+  const int64_t f = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (f >= TK) return;
+  const int p = flat_tile_row[f];
+  float v = 0.f;
+  if (p >= 0) {
+    for (int n = 0; n < nparts; ++n) v += ds_part[(int64_t)p * nparts + n];
+    if (ds_bias) v += ds_bias[p];
+  }
+  ds[f] = v;
+}
+
+int launch_ds_finalize(const float* ds_part, int nparts, const float* ds_bias, const int32_t* flat_tile_row,
+                       int64_t TK, float* ds, cudaStream_t st) {
+  if (TK == 0) return MOE_OK;
+  ds_finalize_kernel<<<(unsigned)((TK + 255) / 256), 256, 0, st>>>(ds_part, nparts, ds_bias, flat_tile_row, TK, ds);
+  return cuda_check(cudaGetLastError(), "ds_finalize");
+}
+
+__global__ void __launch_bounds__(256) segment_rowsum_kernel(const uint16_t* __restrict__ buf, int64_t ld, int R,
+                                                             const int32_t* __restrict__ tile_offsets,
+                                                             const float* __restrict__ w,
+                                                             const int32_t* __restrict__ tile_row_flat,
+                                                             float* __restrict__ out) {
+  const int e = blockIdx.y;
+  const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (j >= R) return;
+  const int64_t beg = tile_offsets[e], end = tile_offsets[e + 1];
+  const uint16_t* row = buf + (int64_t)j * ld;
+  float acc = 0.f;
+  for (int64_t p = beg + lane * 8; p < end; p += 256) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + p);
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float lo = __uint_as_float(wv[q] << 16), hi = __uint_as_float(wv[q] & 0xFFFF0000u);
+      if (w) {
+        const int f0 = tile_row_flat[p + 2 * q], f1 = tile_row_flat[p + 2 * q + 1];
+        lo = f0 >= 0 ? lo * w[f0] : 0.f;
+        hi = f1 >= 0 ? hi * w[f1] : 0.f;
+      }
+      acc += lo;
+      acc += hi;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) out[(int64_t)e * R + j] = acc;
+}
+
+int launch_segment_rowsum(const uint16_t* buf, int64_t ld, int R, const int32_t* tile_offsets, int E, const float* w,
+                          const int32_t* tile_row_flat, float* out, cudaStream_t st) {
+  if (R == 0 || E == 0) return MOE_OK;
+  dim3 grid((unsigned)((R + 7) / 8), (unsigned)E);
+  segment_rowsum_kernel<<<grid, 256, 0, st>>>(buf, ld, R, tile_offsets, w, tile_row_flat, out);
+  return cuda_check(cudaGetLastError(), "segment_rowsum");
+}
+
+}  // namespace moebwd

@@ -1,0 +1,237 @@
+// Routing metadata: expert histogram, prefix offsets, a deterministic stable grouping of the flat
+// (t, k) rows by expert, the block layout (token_position_to_id / block_to_expert, blockwise MoE
+// backward page) and the 128-row tile layout used by the grouped GEMMs.
+//
+// Three kernels, no host synchronisation:
+//   route_count   one CTA per 4096 flat ids: per-chunk expert histogram (shared-memory atomics)
+//   route_scan    one CTA: per-expert totals, exclusive scans (rows, blocks, tiles), per-chunk
+//                 bases, block/tile owner tables, experts ordered by load
+//   route_scatter one CTA per chunk: warp-level match_any ranks give every row its stable position
+#include <cuda_runtime.h>
+
+#include "moebwd_internal.h"
+
+namespace moebwd {
+
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kIdsPerWarp = kRouteChunk / kRouteWarps;  // 512
+
+int route_nchunks(int64_t TK) { return (int)((TK + kRouteChunk - 1) / kRouteChunk); }
+
+__global__ void route_count_kernel(const int32_t* __restrict__ ids, int64_t TK, int E,
+                                   int32_t* __restrict__ chunk_counts, int32_t* status) {
+  extern __shared__ int32_t hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t base = (int64_t)blockIdx.x * kRouteChunk;
+  const int64_t end = min(base + (int64_t)kRouteChunk, TK);
+  int bad = 0;
+  for (int64_t f = base + threadIdx.x; f < end; f += blockDim.x) {
+    const int e = ids[f];
+    if (e >= 0 && e < E)
+      atomicAdd(&hist[e], 1);
+    else
+      bad = 1;
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, MOE_STATUS_BAD_EXPERT_ID);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
+// Exclusive scan of v[0..n) in place by one CTA of 1024 threads; returns the total.
+__device__ int block_exclusive_scan(int32_t* v, int n, int32_t* warp_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int per = (n + 1023) / 1024;
+  const int beg = min(tid * per, n), end = min(beg + per, n);
+  int local = 0;
+  for (int i = beg; i < end; ++i) local += v[i];
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int t = warp_tot[lane];
+    int ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) ti += y;
+    }
+    warp_tot[lane] = ti - t;  // exclusive prefix of warp totals
+    if (lane == 31) warp_tot[32] = ti;
+  }
+  __syncthreads();
+  int run = warp_tot[w] + incl - local;
+  for (int i = beg; i < end; ++i) {
+    const int x = v[i];
+    v[i] = run;
+    run += x;
+  }
+  const int total = warp_tot[32];
+  __syncthreads();
+  return total;
+}
+
+__global__ void __launch_bounds__(1024) route_scan_kernel(int nchunks, int E, int B, int32_t* chunk_counts,
+                                                          int32_t* expert_offsets, int32_t* block_offsets,
+                                                          int32_t* tile_offsets, int32_t* expert_order,
+                                                          int32_t* block_to_expert, int32_t* tile_expert,
+                                                          int32_t* scalars, int32_t* num_blocks_out) {
+  __shared__ int32_t cnt[kMaxExperts + 1];
+  __shared__ int32_t rows[kMaxExperts + 1];
+  __shared__ int32_t blks[kMaxExperts + 1];
+  __shared__ int32_t tiles[kMaxExperts + 1];
+  __shared__ int32_t wt[33];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int tot = 0;
+    for (int c = 0; c < nchunks; ++c) tot += chunk_counts[(int64_t)c * E + e];
+    cnt[e] = tot;
+    rows[e] = tot;
+    blks[e] = (tot + B - 1) / B;
+    tiles[e] = (tot + kTileM - 1) / kTileM;
+  }
+  __syncthreads();
+  const int tot_rows = block_exclusive_scan(rows, E, wt);
+  const int tot_blks = block_exclusive_scan(blks, E, wt);
+  const int tot_tiles = block_exclusive_scan(tiles, E, wt);
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    expert_offsets[e] = e < E ? rows[e] : tot_rows;
+    block_offsets[e] = e < E ? blks[e] : tot_blks;
+    tile_offsets[e] = (e < E ? tiles[e] : tot_tiles) * kTileM;
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = rows[e];
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = chunk_counts[(int64_t)c * E + e];
+      chunk_counts[(int64_t)c * E + e] = run;
+      run += v;
+    }
+    const int b_end = (e + 1 < E) ? blks[e + 1] : tot_blks;
+    for (int b = blks[e]; b < b_end; ++b) block_to_expert[b] = e;
+    const int t_end = (e + 1 < E) ? tiles[e + 1] : tot_tiles;
+    for (int t = tiles[e]; t < t_end; ++t) tile_expert[t] = e;
+    // experts by descending load, ties by index
+    const int me = cnt[e];
+    int rank = 0;
+    for (int o = 0; o < E; ++o) rank += (cnt[o] > me) || (cnt[o] == me && o < e);
+    expert_order[rank] = e;
+  }
+  if (threadIdx.x == 0) {
+    scalars[0] = tot_blks;
+    scalars[1] = tot_tiles;
+    if (num_blocks_out) *num_blocks_out = tot_blks;
+  }
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_scatter_kernel(
+    const int32_t* __restrict__ ids, int64_t TK, int K, int E, int B, const int32_t* __restrict__ chunk_base,
+    const int32_t* __restrict__ expert_offsets, const int32_t* __restrict__ block_offsets,
+    const int32_t* __restrict__ tile_offsets, int32_t* x_gather_idx, int32_t* s_scatter_idx, int32_t* s_reverse,
+    int32_t* token_position_to_id, int32_t* tile_row_flat, int32_t* flat_tile_row) {
+  extern __shared__ int32_t sm[];
+  int32_t* wbase = sm;                       // [warps][E]
+  int32_t* eo = wbase + kRouteWarps * E;     // [E]
+  int32_t* bo = eo + E;                      // [E]
+  int32_t* to = bo + E;                      // [E]
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kRouteWarps * E; i += blockDim.x) wbase[i] = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    eo[e] = expert_offsets[e];
+    bo[e] = block_offsets[e];
+    to[e] = tile_offsets[e];
+  }
+  __syncthreads();
+  const int64_t wbeg = (int64_t)blockIdx.x * kRouteChunk + (int64_t)w * kIdsPerWarp;
+  // pass 1: rows per expert in this warp's slice
+  for (int it = 0; it < kIdsPerWarp / 32; ++it) {
+    const int64_t f = wbeg + it * 32 + lane;
+    const int e = f < TK ? ids[f] : -1;
+    const bool valid = e >= 0 && e < E;
+    const int key = valid ? e : -1;
+    const unsigned grp = __match_any_sync(0xffffffffu, key);
+    if (valid && lane == __ffs(grp) - 1) wbase[w * E + e] += __popc(grp);
+  }
+  __syncthreads();
+  // per-expert bases of the warps of this chunk, in warp order
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = chunk_base[(int64_t)blockIdx.x * E + e];
+    for (int ww = 0; ww < kRouteWarps; ++ww) {
+      const int v = wbase[ww * E + e];
+      wbase[ww * E + e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  // pass 2: stable positions
+  const unsigned lt = (1u << lane) - 1u;
+  for (int it = 0; it < kIdsPerWarp / 32; ++it) {
+    const int64_t f = wbeg + it * 32 + lane;
+    const bool in = f < TK;
+    const int e = in ? ids[f] : -1;
+    const bool valid = e >= 0 && e < E;
+    const int key = valid ? e : -1;
+    const unsigned grp = __match_any_sync(0xffffffffu, key);
+    if (valid) {
+      const int r = wbase[w * E + e] + __popc(grp & lt);
+      const int t = (int)(f / K);
+      x_gather_idx[r] = t;
+      s_scatter_idx[r] = (int)f;
+      s_reverse[f] = r;
+      const int j = r - eo[e];
+      token_position_to_id[(int64_t)bo[e] * B + j] = t;
+      const int p = to[e] + j;
+      tile_row_flat[p] = (int)f;
+      flat_tile_row[f] = p;
+    } else if (in) {
+      s_reverse[f] = -1;
+      flat_tile_row[f] = -1;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(grp) - 1) wbase[w * E + e] += __popc(grp);
+    __syncwarp();
+  }
+}
+
+int launch_route_meta(const int32_t* ids, int T, int K, int E, int B, int64_t Nb, int64_t P, const RouteBufs& r,
+                      cudaStream_t st) {
+  const int64_t TK = (int64_t)T * K;
+  int rc;
+  if ((rc = cuda_check(cudaMemsetAsync(r.token_position_to_id, 0xFF, sizeof(int32_t) * (size_t)(Nb * B), st),
+                       "memset token_position_to_id")))
+    return rc;
+  if ((rc = cuda_check(cudaMemsetAsync(r.block_to_expert, 0xFF, sizeof(int32_t) * (size_t)(Nb > 0 ? Nb : 1), st),
+                       "memset block_to_expert")))
+    return rc;
+  if ((rc = cuda_check(cudaMemsetAsync(r.tile_row_flat, 0xFF, sizeof(int32_t) * (size_t)P, st), "memset tile rows")))
+    return rc;
+  if ((rc = cuda_check(cudaMemsetAsync(r.tile_expert, 0xFF, sizeof(int32_t) * (size_t)(P / kTileM + 1), st),
+                       "memset tile experts")))
+    return rc;
+  const int nch = route_nchunks(TK);
+  if (nch > 0) {
+    route_count_kernel<<<nch, kRouteThreads, sizeof(int32_t) * E, st>>>(ids, TK, E, r.chunk_counts, r.status);
+    if ((rc = cuda_check(cudaGetLastError(), "route_count"))) return rc;
+  }
+  route_scan_kernel<<<1, 1024, 0, st>>>(nch, E, B, r.chunk_counts, r.expert_offsets, r.block_offsets, r.tile_offsets,
+                                        r.expert_order, r.block_to_expert, r.tile_expert, r.scalars, r.num_blocks_out);
+  if ((rc = cuda_check(cudaGetLastError(), "route_scan"))) return rc;
+  if (nch > 0) {
+    const size_t smem = sizeof(int32_t) * (size_t)(kRouteWarps * E + 3 * E);
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if ((rc = cuda_check(e, "route_scatter attribute"))) return rc;
+    }
+    route_scatter_kernel<<<nch, kRouteThreads, smem, st>>>(ids, TK, K, E, B, r.chunk_counts, r.expert_offsets,
+                                                           r.block_offsets, r.tile_offsets, r.x_gather_idx,
+                                                           r.s_scatter_idx, r.s_reverse, r.token_position_to_id,
+                                                           r.tile_row_flat, r.flat_tile_row);
+    if ((rc = cuda_check(cudaGetLastError(), "route_scatter"))) return rc;
+  }
+  return MOE_OK;
+}
+
+}  // namespace moebwd

@@ -1,0 +1,168 @@
+"""GPU parity of the MoE backward (BF16 and MXFP8) and the dense linear backward against the oracle,
+at sizes the oracle finishes in seconds: several 128-row tiles, ragged expert loads, empty experts,
+single-row experts, invalid ids, both affinity modes, biases, both N-tile widths."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import (BF16_TOL, MXFP8_TOL, compare_outputs, np64, oracle_bwd, oracle_h, oracle_meta,
+                     rel_fro, run_gpu, tiled_sf_to_plain)
+from moe_expert_layer_routing_gb300.inputs import (AFFINITY_ON_H, AFFINITY_ON_I, CONFIGS, PREC_MXFP8,
+                                                   make_linear_inputs, make_moe_inputs, small_moe, with_ids,
+                                                   LinearConfig)
+from oracle import linear as olin
+from oracle import mxfp8 as omx
+
+pytestmark = pytest.mark.gpu
+
+
+def _ragged_ids(T, K, E, seed, empty=(0,), single=(1,), hot=None):
+    rng = np.random.default_rng(seed)
+    allowed = [e for e in range(E) if e not in empty and e not in single]
+    p = np.ones(len(allowed))
+    if hot is not None:
+        p[allowed.index(hot)] = 20.0
+    p /= p.sum()
+    ids = np.stack([rng.choice(allowed, size=K, replace=False, p=p) for _ in range(T)])
+    for i, e in enumerate(single):
+        ids[i, K - 1] = e
+    return torch.from_numpy(ids.astype(np.int32))
+
+
+def _check(inp, tol):
+    op, got = run_gpu(inp)
+    assert int(got["status"].item()) == 0, f"device status {int(got['status'].item())}"
+    ref = oracle_bwd(inp)
+    return compare_outputs(got, ref, tol)
+
+
+def test_tiny_bf16_config():
+    _check(make_moe_inputs(CONFIGS["tiny_bf16"]), BF16_TOL)
+
+
+@pytest.mark.parametrize("affinity", [AFFINITY_ON_H, AFFINITY_ON_I])
+def test_bf16_bias_ragged(affinity):
+    cfg = small_moe("ragged_bias", T=300, H=256, I=384, E=8, K=3, B=256, seed=21, bias=True, affinity=affinity)
+    inp = make_moe_inputs(cfg)
+    inp = with_ids(inp, _ragged_ids(300, 3, 8, seed=5, hot=2))
+    _check(inp, BF16_TOL)
+
+
+def test_bf16_single_expert_top1():
+    cfg = small_moe("dense_like", T=200, H=384, I=128, E=1, K=1, B=128, seed=22)
+    _check(make_moe_inputs(cfg), BF16_TOL)
+
+
+def test_bf16_many_tiles_wide_hidden():
+    cfg = small_moe("wide", T=700, H=640, I=256, E=6, K=2, B=512, seed=23)
+    inp = with_ids(make_moe_inputs(cfg), _ragged_ids(700, 2, 6, seed=7, empty=(3,), single=(), hot=0))
+    _check(inp, BF16_TOL)
+
+
+def test_bf16_invalid_ids_are_reported_and_skipped():
+    cfg = small_moe("bad_ids", T=128, H=128, I=128, E=4, K=2, B=128, seed=24)
+    inp = make_moe_inputs(cfg)
+    ids = inp.ids.clone()
+    ids[5, 0] = 4
+    ids[9, 1] = -3
+    inp = with_ids(inp, ids)
+    op, got = run_gpu(inp)
+    import moe_expert_layer_routing_gb300 as mb
+    assert int(got["status"].item()) == mb.STATUS_BAD_EXPERT_ID
+    ref = oracle_bwd(inp)
+    compare_outputs(got, ref, BF16_TOL)
+    assert float(got["ds"][5, 0]) == 0.0 and float(got["ds"][9, 1]) == 0.0
+
+
+def test_bf16_intermediates_match_oracle():
+    """dh and the gathered operands in the workspace match the oracle's own values."""
+    inp = make_moe_inputs(CONFIGS["tiny_bf16"])
+    op, got = run_gpu(inp)
+    meta = oracle_meta(inp)
+    cfg = inp.cfg
+    h = oracle_h(inp, meta)
+    P = op.tile_rows
+    flat = op.region("TILE_ROW_FLAT").view(torch.int32).cpu().numpy()[:P]
+    valid = flat >= 0
+    t, k = flat[valid] // cfg.K, flat[valid] % cfg.K
+    dout_g = op.region("DOUT_G").view(torch.bfloat16).reshape(P, cfg.H).cpu()
+    assert torch.equal(dout_g[torch.from_numpy(valid)], inp.dout[torch.from_numpy(t)])
+    assert torch.all(dout_g[torch.from_numpy(~valid)] == 0)
+    x_gt = op.region("X_GT").view(torch.bfloat16).reshape(cfg.H, P).cpu()
+    assert torch.equal(x_gt.T[torch.from_numpy(valid)], inp.x[torch.from_numpy(t)])
+    # dh from the oracle's formulas
+    from oracle import moe as om
+    x, dout, W2, s = map(om._f64, (inp.x, inp.dout, inp.W2, inp.s))
+    ids = inp.ids.numpy()
+    e = ids[t, k]
+    g = dout[t]
+    dA_raw = np.einsum("rh,rih->ri", g, W2[e])
+    gate, up = h[t, k, :cfg.I], h[t, k, cfg.I:]
+    dA = s[t, k][:, None] * dA_raw
+    dh_ref = np.concatenate([dA * up * om.dsilu(gate), dA * om.silu(gate)], 1)
+    dh = np64(op.region("DH").view(torch.bfloat16).reshape(P, 2 * cfg.I))
+    assert rel_fro(dh[valid], dh_ref) < BF16_TOL
+    assert np.all(dh[~valid] == 0)
+    dht = np64(op.region("DH_T").view(torch.bfloat16).reshape(2 * cfg.I, P))
+    assert np.array_equal(dht.T, dh)
+
+
+# ----------------------------------------------------------------------------------------------
+# MXFP8
+# ----------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("affinity", [AFFINITY_ON_I, AFFINITY_ON_H])
+def test_mxfp8_small(affinity):
+    cfg = small_moe("mx_small", T=256, H=256, I=256, E=4, K=2, B=256, seed=31, precision=PREC_MXFP8,
+                    affinity=affinity)
+    _check(make_moe_inputs(cfg), MXFP8_TOL)
+
+
+def test_mxfp8_ragged_many_tiles():
+    cfg = small_moe("mx_ragged", T=900, H=384, I=384, E=8, K=3, B=512, seed=32, precision=PREC_MXFP8,
+                    affinity=AFFINITY_ON_I)
+    inp = with_ids(make_moe_inputs(cfg), _ragged_ids(900, 3, 8, seed=9, empty=(0, 6), single=(1,), hot=3))
+    _check(inp, MXFP8_TOL)
+
+
+def test_mxfp8_quantised_operands_match_oracle_codes():
+    """The gathered dout operand of G1 is quantised bit-exactly; dh codes agree with the oracle's
+    quantisation of its own dh except for rare rounding-boundary cases."""
+    cfg = small_moe("mx_codes", T=256, H=256, I=256, E=4, K=2, B=256, seed=33, precision=PREC_MXFP8,
+                    affinity=AFFINITY_ON_I)
+    inp = make_moe_inputs(cfg)
+    op, got = run_gpu(inp)
+    P = op.tile_rows
+    flat = op.region("TILE_ROW_FLAT").view(torch.int32).cpu().numpy()[:P]
+    valid = flat >= 0
+    t = flat // cfg.K
+    rows = np.where(valid[:, None], inp.dout.double().numpy()[np.where(valid, t, 0)], 0.0)
+    rq, rs = omx.mx_quantize(rows, cfg.fp8_act, axis=1)
+    q = op.region("DOUT_G").cpu().numpy().reshape(P, cfg.H)
+    sf = tiled_sf_to_plain(op.region("DOUT_G_SF").cpu().numpy(), P, cfg.H)
+    assert np.array_equal(q, rq) and np.array_equal(sf, rs)
+
+
+def test_linear_bwd_small_both_precisions():
+    import moe_expert_layer_routing_gb300 as mb
+    inp = make_linear_inputs(LinearConfig("lin_small", M=256, N=384, K=512, seed=41))
+    for prec, tol, fn in ((mb.PREC_MXFP8, MXFP8_TOL, olin.linear_backward_mxfp8),
+                          (mb.PREC_BF16, BF16_TOL, olin.linear_backward)):
+        got = mb.linear_bwd(inp.dY.cuda(), inp.W.cuda(), inp.X.cuda(), precision=prec)
+        torch.cuda.synchronize()
+        ref = fn(inp.dY, inp.W, inp.X)
+        assert rel_fro(np64(got["dX"]), ref["dX"]) < tol
+        assert rel_fro(np64(got["dW"]), ref["dW"]) < tol
+
+
+def test_linear_bwd_dense_4096_config():
+    """The dense MXFP8 workload at full size (oracle float64 matmuls of 4096^3)."""
+    import moe_expert_layer_routing_gb300 as mb
+    inp = make_linear_inputs(CONFIGS["dense_mxfp8_4096"], device="cuda")
+    got = mb.linear_bwd(inp.dY, inp.W, inp.X, precision=mb.PREC_MXFP8)
+    torch.cuda.synchronize()
+    ref = olin.linear_backward_mxfp8(inp.dY.cpu(), inp.W.cpu(), inp.X.cpu())
+    assert rel_fro(np64(got["dX"]), ref["dX"]) < MXFP8_TOL
+    assert rel_fro(np64(got["dW"]), ref["dW"]) < MXFP8_TOL

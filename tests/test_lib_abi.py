@@ -1,0 +1,79 @@
+"""CPU checks of the C-ABI library: it builds, loads, and exports every declared entry point; host
+functions without device work behave as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moebwd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from moe_expert_layer_routing_gb300 import _build
+    _build.build()
+    import moe_expert_layer_routing_gb300 as mb
+    return mb.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s+\*?([a-z_][a-z0-9_]*)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 12, names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in moebwd.h but not exported"
+    import moe_expert_layer_routing_gb300 as mb
+    assert sorted(mb.EXPORTED) == names
+
+
+def test_block_bound_matches_oracle(lib):
+    from oracle.route_meta import num_blocks_bound
+    for T, K, E, B in [(256, 2, 4, 128), (16384, 8, 64, 128), (32768, 8, 128, 256), (65536, 8, 128, 512),
+                       (3, 1, 8, 128), (0, 2, 4, 128), (10, 1, 2, 128)]:
+        assert lib.moe_num_blocks_bound(T, K, E, B) == num_blocks_bound(T, K, E, B)
+    assert lib.moe_num_blocks_bound(16384, 8, 64, 128) == 1087
+    assert lib.moe_num_blocks_bound(65536, 8, 128, 512) == 1151
+
+
+def test_workspace_queries(lib):
+    import moe_expert_layer_routing_gb300 as mb
+    a = mb.MoeBwdArgs(T=256, H=128, I=256, E=4, K=2, block_size=128)
+    assert lib.moe_bwd_workspace_size(ctypes.byref(a)) > 0
+    bad = mb.MoeBwdArgs(T=256, H=100, I=256, E=4, K=2, block_size=128)
+    assert lib.moe_bwd_workspace_size(ctypes.byref(bad)) == 0
+    assert b"multiples of 128" in lib.moe_last_error()
+    bad2 = mb.MoeBwdArgs(T=256, H=128, I=256, E=4, K=2, block_size=96)
+    assert lib.moe_bwd_workspace_size(ctypes.byref(bad2)) == 0
+    off, nb = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.moe_bwd_workspace_region(ctypes.byref(a), mb.WS_REGIONS.index("DH"), ctypes.byref(off),
+                                        ctypes.byref(nb)) == 0
+    P = lib.moe_tile_rows_capacity(256, 2, 4)
+    assert P % 128 == 0 and P >= 512
+    assert nb.value == P * 2 * 256 * 2 and off.value % 256 == 0
+    assert lib.moe_route_meta_workspace_size(256, 2, 4, 128) > 0
+    assert lib.linear_bwd_workspace_size(4096, 4096, 4096, 1) > 0
+
+
+def test_host_argument_errors(lib):
+    import moe_expert_layer_routing_gb300 as mb
+    a = mb.MoeBwdArgs(T=256, H=128, I=256, E=4, K=2, block_size=128)
+    assert lib.moe_bwd(ctypes.byref(a), None) == -1          # null pointers, caught on the host
+    assert b"null" in lib.moe_last_error()
+    assert lib.mxfp8_quantize(None, 1, 1, 32, 32, None, 0, 0, None, None, 1, None) == -1
+    assert lib.linear_bwd(None, None, None, 128, 128, 128, 1, 1, None, None, None, 0, None) == -1
+    assert lib.moe_route_meta(None, 4, 2, 4, 100, *([None] * 10), 0, None) == -2
+
+
+def test_product_path_refuses_cpu_tensors():
+    import torch
+    import moe_expert_layer_routing_gb300 as mb
+    with pytest.raises(mb.MoeError):
+        mb.mxfp8_quantize(torch.zeros(32, 32, dtype=torch.bfloat16))
