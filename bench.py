@@ -1,0 +1,425 @@
+"""Benchmark: MoE expert-layer backward on GB300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one full backward pass (routing metadata, gathers / quantisation, the four grouped GEMMs,
+dx scatter-sum, ds, bias sums) over one synthetic batch of the named workload.  `value` is useful
+tensor FLOP/s (12*T*K*H*I per MoE step, 4*M*N*K per dense step; padding rows and quantisation
+excluded) with inputs resident in HBM; `e2e` is the same metric with the step's activations copied
+from pinned host memory and dx/ds copied back inside the timed region.  With N > 1 (torchrun), every
+rank runs an independent replica (the pass has no exchange step), value = sum over ranks / max time.
+`--impl reference` times the CPU float64 oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "imbalanced_mxfp8"
+FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
+FP8_OVER_BF16 = 2.0   # nominal dense ratio 4.5 / 2.25 PFLOP/s
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "moe_expert_layer_routing_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, stage: str):
+    """DRAM bytes per launch of a stage from a committed ncu summary, only if it was captured on
+    the current kernel sources (a line `traffic workload=.. stage=.. bytes_per_launch=.. source_sha=..`)."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    sha = source_sha()
+    pat = re.compile(r"traffic workload=(\S+) stage=(\S+) bytes_per_launch=(\d+) source_sha=(\w+)")
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith((".md", ".txt")):
+            continue
+        for line in open(os.path.join(pdir, name)):
+            m = pat.search(line)
+            if m and m.group(1) == workload and m.group(2) == stage and m.group(4) == sha:
+                return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        if not sm:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["unsampled"], samples=0)
+        sm_sorted = sorted(sm)
+        busy = [v for v in sm_sorted if v > 0.5 * max(sm_sorted)] or sm_sorted
+        return dict(sm_mhz=busy[len(busy) // 2], sm_max_mhz=max(mx), reasons=sorted(reasons), samples=len(sm))
+
+
+# ---------------------------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle sample (the baseline, never the product path)
+# ---------------------------------------------------------------------------------------------
+def oracle_sample_moe(inp, target_rows: int):
+    """Pick the lightest non-empty experts until target_rows rows; return a timing closure."""
+    import numpy as np
+    from oracle import moe as om
+    from oracle import sample as osm
+    cfg = inp.cfg
+    ids = inp.ids.cpu().numpy()
+    counts = np.bincount(ids.reshape(-1), minlength=cfg.E)
+    order = [e for e in np.argsort(counts, kind="stable") if counts[e] > 0]
+    chosen, rows = [], 0
+    for e in order:
+        chosen.append(int(e))
+        rows += int(counts[e])
+        if rows >= target_rows:
+            break
+    cpu = lambda t: None if t is None else t.cpu()  # noqa: E731
+    sub = osm.subproblem(cpu(inp.x), cpu(inp.dout), cpu(inp.W1), cpu(inp.W2), inp.s.cpu().numpy(), ids,
+                         cpu(inp.ckpt), cfg.block_size, experts=chosen, b2=cpu(inp.b2))
+
+    def run():
+        if cfg.precision == 1:
+            om.moe_backward_mxfp8(sub["x"], sub["dout"], sub["W1"], sub["W2"], sub["s"], sub["ids"], sub["h"],
+                                  affinity=cfg.affinity, fp8_act=cfg.fp8_act, fp8_w=cfg.fp8_w)
+        else:
+            om.moe_backward(sub["x"], sub["dout"], sub["W1"], sub["W2"], sub["s"], sub["ids"], sub["h"],
+                            b2=sub["b2"], with_bias=cfg.bias)
+
+    flops = 12.0 * rows * cfg.H * cfg.I
+    desc = f"{len(chosen)} lightest non-empty experts, {rows} routed rows (all their tokens), all outputs"
+    return run, flops, desc
+
+
+def oracle_sample_linear(inp, rows: int):
+    import torch
+    from oracle import linear as ol
+    dY = inp.dY[:rows].cpu()
+    X = inp.X[:rows].cpu()
+    W = inp.W.cpu()
+
+    def run():
+        ol.linear_backward_mxfp8(dY, W, X)
+
+    flops = 4.0 * rows * inp.cfg.N * inp.cfg.K
+    desc = f"first {rows} of {inp.cfg.M} rows of dY and X (dX rows and a dW partial over them)"
+    return run, flops, desc
+
+
+def time_oracle(run, flops, max_s):
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        run()
+        n += 1
+        if time.perf_counter() - t0 > max_s or n >= 50:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return flops / dt / 1e12, n
+
+
+# ---------------------------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+
+    from moe_expert_layer_routing_gb300.inputs import CONFIGS, LinearConfig, make_linear_inputs, make_moe_inputs
+
+    world, rank, local = dist_setup(args.gpus)
+    cfg = CONFIGS[args.workload]
+    is_linear = isinstance(cfg, LinearConfig)
+    cores = len(os.sched_getaffinity(0))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inp = make_linear_inputs(cfg) if is_linear else make_moe_inputs(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
+        run, flops, desc = oracle_sample_linear(inp, 128) if is_linear else oracle_sample_moe(inp, 256)
+        for _ in range(args.warmup):
+            run()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            run()
+        dt = (time.perf_counter() - t0) / args.steps
+        value = flops / dt / 1e12
+        line = dict(metric=f"{'dense linear' if is_linear else 'MoE'}-backward useful TFLOP/s", value=value,
+                    unit="TFLOP/s", n_gpus=0, steps=args.steps, warmup=args.warmup, ms_per_step=dt * 1e3,
+                    higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+                    impl="reference", config=dict(workload=cfg.name),
+                    cpu_baseline=dict(value=value, unit="TFLOP/s", cores=cores, kind="oracle", sample=desc),
+                    e2e=dict(value=value, unit="TFLOP/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+        print(json.dumps(line), flush=True)
+        return
+
+    import moe_expert_layer_routing_gb300 as mb
+    from __graft_entry__ import build
+    if rank == 0:
+        build()
+    barrier(world)
+    mb.lib()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+
+    # ---------------------------------------------------------------- problem setup (untimed)
+    if is_linear:
+        inp = make_linear_inputs(cfg, device=dev)
+        op = mb.LinearBwd(cfg.M, cfg.N, cfg.K, mb.PREC_MXFP8, cfg.fp8, dev)
+        step = lambda: op.run(inp.dY, inp.W, inp.X)  # noqa: E731
+        flops = float(cfg.useful_flops())
+        tokens = cfg.M
+        prec = mb.PREC_MXFP8
+        in_bytes = sum(t.numel() * t.element_size() for t in (inp.dY, inp.W, inp.X))
+    else:
+        inp = make_moe_inputs(cfg, device=dev)
+        op = mb.MoeBwd(T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K, block_size=cfg.block_size,
+                       precision=cfg.precision, affinity=cfg.affinity, fp8_act=cfg.fp8_act, fp8_w=cfg.fp8_w,
+                       has_bias=cfg.bias, device=dev)
+        kw = dict(x=inp.x, dout=inp.dout, s=inp.s, ids=inp.ids, ckpt=inp.ckpt, b2=inp.b2 if cfg.bias else None)
+        if cfg.precision == mb.PREC_MXFP8:       # weights pre-quantised once, outside the timed region
+            W1_q, W1_sf = mb.quantize_weights(inp.W1, cfg.fp8_w)
+            W2_q, W2_sf = mb.quantize_weights(inp.W2, cfg.fp8_w)
+            kw.update(W1_q=W1_q, W1_sf=W1_sf, W2_q=W2_q, W2_sf=W2_sf)
+        else:
+            kw.update(W1=inp.W1, W2=inp.W2)
+        op.bind(**kw)
+        step = lambda: op.run()  # noqa: E731
+        flops = float(cfg.useful_flops())
+        tokens = cfg.T
+        prec = cfg.precision
+        in_bytes = sum(t.numel() * t.element_size() for t in kw.values() if t is not None)
+
+    # ---------------------------------------------------------------- device-resident timing
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if not is_linear:
+        st0 = int(op.status.item())
+        if st0 != 0:
+            raise SystemExit(f"device status {st0} after warm-up")
+    launches0 = mb.kernel_launches()
+    if not is_linear:
+        mb.profile_enable(True)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = allreduce_max(ms, world)
+    launches = mb.kernel_launches() - launches0
+    stages = None
+    if not is_linear:
+        stages, ncalls = mb.profile_read()
+        mb.profile_enable(False)
+        stages = {k: v / max(ncalls, 1) for k, v in stages.items()}
+    value = flops * world / (ms * 1e-3) / 1e12
+
+    # ---------------------------------------------------------------- roofline of the dominant kernel
+    peak_tf = peaks["bf16_tflops"] * (FP8_OVER_BF16 if prec == 1 else 1.0)
+    if not is_linear:
+        H, I, TK = cfg.H, cfg.I, cfg.T * cfg.K
+        stage_flops = {"G1_dA_dswiglu": 2.0 * TK * H * I, "G3_dW2": 2.0 * TK * H * I,
+                       "G2_dx_expanded": 4.0 * TK * H * I, "G4_dW1": 4.0 * TK * H * I}
+        dom = max(stage_flops, key=lambda k: stages[k])
+        achieved = stage_flops[dom] / (stages[dom] * 1e-3) / 1e12
+        roofline = dict(bound="tensor", kernel=dom, achieved=achieved, peak=peak_tf, unit="TFLOP/s",
+                        frac=achieved / peak_tf, traffic=recorded_traffic(cfg.name, dom),
+                        peak_source=f"{peak_src} bf16 burst" + (" x2 (nominal fp8/bf16)" if prec == 1 else ""))
+    else:
+        achieved = value / world
+        roofline = dict(bound="tensor", kernel="linear_bwd (dX and dW GEMMs + quantisation)", achieved=achieved,
+                        peak=peak_tf, unit="TFLOP/s", frac=achieved / peak_tf, traffic=None,
+                        peak_source=f"{peak_src} bf16 burst x2 (nominal fp8/bf16)")
+
+    # ---------------------------------------------------------------- end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        if is_linear:
+            host_in = {k: getattr(inp, k).cpu().pin_memory() for k in ("dY", "W", "X")}
+            dev_in = {k: getattr(inp, k) for k in ("dY", "W", "X")}
+            host_out = {k: torch.empty_like(getattr(op, k), device="cpu").pin_memory() for k in ("dX", "dW")}
+            dev_out = {k: getattr(op, k) for k in ("dX", "dW")}
+        else:
+            names = ["x", "dout", "s", "ids", "ckpt"]
+            host_in = {k: getattr(inp, k).cpu().pin_memory() for k in names}
+            dev_in = {k: getattr(inp, k) for k in names}
+            host_out = {k: torch.empty_like(getattr(op, k), device="cpu").pin_memory() for k in ("dx", "ds")}
+            dev_out = {k: getattr(op, k) for k in ("dx", "ds")}
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+        def e2e_step():
+            for k, t in host_in.items():
+                dev_in[k].copy_(t, non_blocking=True)
+            step()
+            for k, t in host_out.items():
+                t.copy_(dev_out[k], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = allreduce_max(e0.elapsed_time(e1) / args.steps, world)
+        e2e = dict(value=flops * world / (ems * 1e-3) / 1e12, unit="TFLOP/s", ms_per_step=ems,
+                   h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                   note="activations (x, dout, s, ids, checkpoint) in, dx and ds out; weights and weight "
+                        "gradients stay resident" if not is_linear else "dY, W, X in; dX, dW out")
+
+    if rank != 0:
+        barrier(world)
+        return
+    # ---------------------------------------------------------------- CPU oracle baseline (rank 0, N=1)
+    cpu_baseline = None
+    if world == 1 and not args.no_cpu:
+        if is_linear:
+            run, cflops, desc = oracle_sample_linear(inp, 512)
+        else:
+            run, cflops, desc = oracle_sample_moe(inp, 1024 if cfg.H * cfg.I < 4e6 else 512)
+        cval, n = time_oracle(run, cflops, 15.0)
+        cpu_baseline = dict(value=cval, unit="TFLOP/s", cores=cores, kind="oracle", sample=desc + f"; {n} run(s)")
+
+    l2_note = f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB resident inputs > 0.13 GB L2)"
+    if is_linear:
+        conf = dict(workload=cfg.name, M=cfg.M, N=cfg.N, K=cfg.K, precision="mxfp8 e5m2", l2=l2_note,
+                    parallelism=f"replicas x{world}")
+    else:
+        conf = dict(workload=cfg.name, T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, top_k=cfg.K, block_size=cfg.block_size,
+                    precision="mxfp8 (e4m3 weights, e5m2 activations, E8M0 scales)" if prec == 1 else "bf16",
+                    affinity="on_I" if cfg.affinity == 1 else "on_H", bias=cfg.bias, l2=l2_note,
+                    parallelism=f"replicas x{world}")
+    line = dict(
+        metric="MoE-backward TFLOP/s (BF16, MXFP8) & % of tensor peak; tokens/s" if not is_linear
+        else "dense MXFP8 linear-backward TFLOP/s & % of tensor peak",
+        value=value, unit="TFLOP/s", n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=ms,
+        higher_is_better=True, scaling="weak", vs_baseline=None,
+        dtype="mxfp8" if prec == 1 else "bf16", data="synthetic (seeded; shapes and routing of the workload)",
+        config=conf, tokens_per_s=tokens * world / (ms * 1e-3), pct_of_tensor_peak=100.0 * value / world / peak_tf,
+        roofline=roofline, cpu_baseline=cpu_baseline, e2e=e2e, clocks=clk.summary(), gpu_launches=launches,
+        stage_ms=stages, source_sha=source_sha())
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+if __name__ == "__main__":
+    main()

@@ -224,6 +224,33 @@ int moe_bwd_workspace_region(const MoeBwdArgs* args, int region, size_t* offset,
 int64_t moe_tile_rows_capacity(int T, int K, int E);
 
 /* ------------------------------------------------------------------------------------------ */
+/* Instrumentation                                                                             */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Stages of moe_bwd, in launch order. */
+enum {
+  MOE_STAGE_ROUTE = 0, /* routing metadata */
+  MOE_STAGE_PREP,      /* gathered / transposed / quantised activation operands */
+  MOE_STAGE_G1,        /* dA = dout_g W2_e^T with the dSwiGLU + ds epilogue */
+  MOE_STAGE_G3,        /* dW2_e = a'^T dout_g */
+  MOE_STAGE_G2,        /* dx_expanded = dh W1_e */
+  MOE_STAGE_G4,        /* dW1_e = x_g^T dh */
+  MOE_STAGE_REDUCE,    /* dx scatter-sum, ds, bias sums */
+  MOE_NUM_STAGES
+};
+
+/* Stage timing.  While enabled, every moe_bwd call records CUDA events on its own stream at the
+ * stage boundaries (no host synchronisation; up to 1024 calls are kept).  moe_profile_read waits
+ * for the recorded events and returns, per stage, the total milliseconds over the profiled calls
+ * (stage_ms[MOE_NUM_STAGES]) and the number of calls.  Enabling (or disabling) discards what was
+ * recorded.  Process-global host state; not thread-safe. */
+int moe_profile_enable(int enable);
+int moe_profile_read(double* stage_ms, int max_stages, int* calls);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t moe_kernel_launches(void);
+
+/* ------------------------------------------------------------------------------------------ */
 /* Dense linear backward (the E=1, K=1 degenerate case)                                        */
 /* ------------------------------------------------------------------------------------------ */
 

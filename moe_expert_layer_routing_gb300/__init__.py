@@ -28,7 +28,9 @@ WS_REGIONS = ["EXPERT_OFFSETS", "TILE_OFFSETS", "BLOCK_OFFSETS", "TILE_ROW_FLAT"
 EXPORTED = ["moe_last_error", "moe_version", "moe_num_blocks_bound", "moe_route_meta_workspace_size",
             "moe_route_meta", "mxfp8_quantize", "moe_bwd_workspace_size", "moe_bwd",
             "moe_bwd_workspace_region", "moe_tile_rows_capacity", "linear_bwd_workspace_size",
-            "linear_bwd"]
+            "linear_bwd", "moe_profile_enable", "moe_profile_read", "moe_kernel_launches"]
+
+STAGES = ["route", "prep", "G1_dA_dswiglu", "G3_dW2", "G2_dx_expanded", "G4_dW1", "reduce"]
 
 
 class MoeError(RuntimeError):
@@ -71,6 +73,9 @@ def lib():
         "moe_tile_rows_capacity": ([i32, i32, i32], i64),
         "linear_bwd_workspace_size": ([i64, i64, i64, i32], sz),
         "linear_bwd": ([vp, vp, vp, i64, i64, i64, i32, i32, vp, vp, vp, sz, vp], i32),
+        "moe_profile_enable": ([i32], i32),
+        "moe_profile_read": ([ctypes.POINTER(ctypes.c_double), i32, ctypes.POINTER(i32)], i32),
+        "moe_kernel_launches": ([], ctypes.c_uint64),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -100,6 +105,24 @@ def _need_cuda(*ts):
             raise MoeError("tensors must be CUDA tensors (there is no CPU path)")
         if t is not None and not t.is_contiguous():
             raise MoeError("tensors must be contiguous")
+
+
+def profile_enable(enable: bool = True):
+    """Start (or stop) recording per-stage CUDA events inside moe_bwd; discards earlier records."""
+    _check(lib().moe_profile_enable(int(enable)), "moe_profile_enable")
+
+
+def profile_read() -> tuple[dict, int]:
+    """Total milliseconds per stage over the profiled moe_bwd calls, and the number of calls."""
+    arr = (ctypes.c_double * len(STAGES))()
+    calls = ctypes.c_int()
+    _check(lib().moe_profile_read(arr, len(STAGES), ctypes.byref(calls)), "moe_profile_read")
+    return {n: arr[i] for i, n in enumerate(STAGES)}, calls.value
+
+
+def kernel_launches() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib().moe_kernel_launches())
 
 
 def num_blocks_bound(T: int, K: int, E: int, block_size: int) -> int:

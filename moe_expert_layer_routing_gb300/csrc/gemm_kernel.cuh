@@ -455,6 +455,7 @@ int gemm_launch_instance(const GemmParams& p, const void* tmA, const void* tmB, 
   if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(gemm)");
   kern<<<grid, 192, C::SMEM_BYTES, st>>>(*static_cast<const CUtensorMap*>(tmA),
                                         *static_cast<const CUtensorMap*>(tmB), p);
+  count_launch();
   return cuda_check(cudaGetLastError(), "gemm launch");
 }
 

@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "moebwd_internal.h"
@@ -36,6 +37,9 @@ int device_sm_count() {
 }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -82,4 +86,5 @@ bool make_tmap_2d(void* out_tmap, const void* base, int elem_bytes, uint64_t row
 }  // namespace moebwd
 
 extern "C" const char* moe_last_error(void) { return moebwd::g_err; }
+extern "C" uint64_t moe_kernel_launches(void) { return moebwd::g_launches.load(); }
 extern "C" const char* moe_version(void) { return "moebwd 0.1 (sm_103a tcgen05)"; }

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <vector>
 
 #include "moebwd_internal.h"
 
@@ -144,6 +145,27 @@ static int check_args(const MoeBwdArgs* a, bool need_ptrs) {
   return MOE_OK;
 }
 
+// ------------------------------------------------------------------------------------------
+// stage profiler: a ring of event sets recorded on the call's stream, read on demand
+// ------------------------------------------------------------------------------------------
+struct Profiler {
+  static constexpr int kRing = 1024;
+  bool on = false;
+  int calls = 0;
+  std::vector<cudaEvent_t> ev;  // kRing * (MOE_NUM_STAGES + 1)
+};
+static Profiler g_prof;
+
+static void prof_mark(cudaStream_t st, int slot, int boundary) {
+  if (!g_prof.on || slot < 0) return;
+  cudaEventRecord(g_prof.ev[(size_t)slot * (MOE_NUM_STAGES + 1) + boundary], st);
+}
+
+static int prof_slot() {
+  if (!g_prof.on || g_prof.calls >= Profiler::kRing) return -1;
+  return g_prof.calls++;
+}
+
 template <typename T>
 static T* reg(const Layout& L, void* ws, int r) {
   return L.bytes[r] ? reinterpret_cast<T*>(static_cast<char*>(ws) + L.off[r]) : nullptr;
@@ -258,6 +280,8 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     return MOE_OK;
   }
 
+  const int slot = prof_slot();
+  prof_mark(st, slot, 0);
   int32_t* tile_offsets = reg<int32_t>(L, ws, R_TILE_OFFSETS);
   int32_t* expert_order = reg<int32_t>(L, ws, R_EXPERT_ORDER);
   int32_t* scalars = reg<int32_t>(L, ws, R_SCALARS);
@@ -285,6 +309,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   r.num_blocks_out = nullptr;
   r.status = a.status_dev;
   if ((rc = launch_route_meta(a.ids, a.T, a.K, a.E, a.block_size, L.Nb, P, r, st))) return rc;
+  prof_mark(st, slot, 1);
 
   // 2. gathered / transposed / quantised activation operands
   PrepArgs pa{};
@@ -309,6 +334,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   pa.x_gt_sf = reg<uint8_t>(L, ws, R_X_GT_SF);
   pa.ds_bias = a.has_bias ? reg<float>(L, ws, R_DS_BIAS) : nullptr;
   if ((rc = launch_prep(pa, st))) return rc;
+  prof_mark(st, slot, 2);
 
   const void* W1 = mx ? static_cast<const void*>(a.W1_q) : a.W1;
   const void* W2 = mx ? static_cast<const void*>(a.W2_q) : a.W2;
@@ -345,6 +371,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.status = a.status_dev;
     if ((rc = launch_gemm(mx, L.BN1, p, reg<void>(L, ws, R_DOUT_G), P, H, W2, E * I, H, st))) return rc;
   }
+  prof_mark(st, slot, 3);
   // 4. G3: dW2_e = a'^T dout_g over the expert's tile rows
   {
     GemmParams p{};
@@ -365,6 +392,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     if ((rc = launch_gemm(mx, L.BN3, p, reg<void>(L, ws, R_AP_T), I, P, reg<void>(L, ws, R_DOUT_GT), H, P, st)))
       return rc;
   }
+  prof_mark(st, slot, 4);
   // 5. G2: dx_expanded = dh W1_e^T
   {
     GemmParams p{};
@@ -385,6 +413,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.status = a.status_dev;
     if ((rc = launch_gemm(mx, L.BN2, p, reg<void>(L, ws, R_DH), P, 2 * I, W1, E * H, 2 * I, st))) return rc;
   }
+  prof_mark(st, slot, 5);
   // 6. G4: dW1_e = x_g^T dh over the expert's tile rows
   {
     GemmParams p{};
@@ -405,6 +434,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     if ((rc = launch_gemm(mx, L.BN4, p, reg<void>(L, ws, R_X_GT), H, P, reg<void>(L, ws, R_DH_T), 2 * I, P, st)))
       return rc;
   }
+  prof_mark(st, slot, 6);
   // 7. reductions
   if ((rc = launch_dx_scatter_sum(reg<uint16_t>(L, ws, R_DX_EXP), flat_tile_row, a.T, a.K, a.H,
                                   static_cast<uint16_t*>(a.dx), st)))
@@ -419,6 +449,42 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     if ((rc = launch_segment_rowsum(reg<uint16_t>(L, ws, R_DOUT_GT), P, (int)H, tile_offsets, (int)E,
                                     a.affinity == MOE_AFFINITY_ON_I ? a.s : nullptr, tile_row_flat, a.db2, st)))
       return rc;
+  }
+  prof_mark(st, slot, 7);
+  return MOE_OK;
+}
+
+extern "C" int moe_profile_enable(int enable) {
+  clear_error();
+  if (g_prof.ev.empty() && enable) {
+    g_prof.ev.resize((size_t)Profiler::kRing * (MOE_NUM_STAGES + 1));
+    for (auto& e : g_prof.ev) {
+      int rc = cuda_check(cudaEventCreate(&e), "cudaEventCreate");
+      if (rc) {
+        g_prof.ev.clear();
+        return rc;
+      }
+    }
+  }
+  g_prof.on = enable != 0;
+  g_prof.calls = 0;
+  return MOE_OK;
+}
+
+extern "C" int moe_profile_read(double* stage_ms, int max_stages, int* calls) {
+  clear_error();
+  if (!stage_ms || max_stages < 0) return fail(MOE_ERR_INVALID, "moe_profile_read: null output");
+  for (int i = 0; i < max_stages; ++i) stage_ms[i] = 0.0;
+  if (calls) *calls = g_prof.calls;
+  for (int c = 0; c < g_prof.calls; ++c) {
+    cudaEvent_t* e = &g_prof.ev[(size_t)c * (MOE_NUM_STAGES + 1)];
+    int rc = cuda_check(cudaEventSynchronize(e[MOE_NUM_STAGES]), "cudaEventSynchronize");
+    if (rc) return rc;
+    for (int i = 0; i < MOE_NUM_STAGES && i < max_stages; ++i) {
+      float ms = 0.f;
+      if ((rc = cuda_check(cudaEventElapsedTime(&ms, e[i], e[i + 1]), "cudaEventElapsedTime"))) return rc;
+      stage_ms[i] += ms;
+    }
   }
   return MOE_OK;
 }

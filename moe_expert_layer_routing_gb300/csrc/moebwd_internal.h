@@ -23,6 +23,7 @@ void clear_error();
 int cuda_check(cudaError_t e, const char* what);
 int device_sm_count();
 size_t align_up(size_t v, size_t a);
+void count_launch();   // one kernel launched by this library
 
 // 2D tensor map over a row-major [rows, cols] matrix of `elem_bytes`-byte elements with the given
 // row pitch, box [box_rows, box_cols], 128-byte swizzle.  Returns false on failure (message set).

@@ -159,6 +159,7 @@ int launch_prep(const PrepArgs& a, cudaStream_t st) {
     else { if (bias) MOE_PREP(false, false, true); else MOE_PREP(false, false, false); }
   }
 #undef MOE_PREP
+  count_launch();
   return cuda_check(cudaGetLastError(), "prep");
 }
 
@@ -269,6 +270,7 @@ int launch_quant_rowwise(const uint16_t* in, int64_t src_rows, int64_t rows, int
   const int64_t cap = (int64_t)device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
   quant_rowwise_kernel<<<(unsigned)blocks, 256, 0, st>>>(in, src_rows, rows, cols, ld, row_index, fmt, q, sf, tiled);
+  count_launch();
   return cuda_check(cudaGetLastError(), "quant_rowwise");
 }
 
@@ -280,6 +282,7 @@ int launch_quant_colwise(const uint16_t* in, int64_t src_rows, int64_t rows, int
     quant_colwise_kernel<true><<<grid, 256, 0, st>>>(in, src_rows, rows, cols, ld, row_index, fmt, q, sf, tiled);
   else
     quant_colwise_kernel<false><<<grid, 256, 0, st>>>(in, src_rows, rows, cols, ld, row_index, fmt, q, sf, tiled);
+  count_launch();
   return cuda_check(cudaGetLastError(), "quant_colwise");
 }
 

@@ -43,6 +43,7 @@ int launch_dx_scatter_sum(const uint16_t* dx_exp, const int32_t* flat_tile_row, 
   if (T == 0) return MOE_OK;
   if (K > 64) return fail(MOE_ERR_UNSUPPORTED, "top-K above 64");
   dx_scatter_sum_kernel<<<T, 256, 0, st>>>(dx_exp, flat_tile_row, K, H, dx);
+  count_launch();
   return cuda_check(cudaGetLastError(), "dx_scatter_sum");
 }
 
@@ -63,6 +64,7 @@ int launch_ds_finalize(const float* ds_part, int nparts, const float* ds_bias, c
                        int64_t TK, float* ds, cudaStream_t st) {
   if (TK == 0) return MOE_OK;
   ds_finalize_kernel<<<(unsigned)((TK + 255) / 256), 256, 0, st>>>(ds_part, nparts, ds_bias, flat_tile_row, TK, ds);
+  count_launch();
   return cuda_check(cudaGetLastError(), "ds_finalize");
 }
 
@@ -103,6 +105,7 @@ int launch_segment_rowsum(const uint16_t* buf, int64_t ld, int R, const int32_t*
   if (R == 0 || E == 0) return MOE_OK;
   dim3 grid((unsigned)((R + 7) / 8), (unsigned)E);
   segment_rowsum_kernel<<<grid, 256, 0, st>>>(buf, ld, R, tile_offsets, w, tile_row_flat, out);
+  count_launch();
   return cuda_check(cudaGetLastError(), "segment_rowsum");
 }
 

@@ -214,10 +214,12 @@ int launch_route_meta(const int32_t* ids, int T, int K, int E, int B, int64_t Nb
   const int nch = route_nchunks(TK);
   if (nch > 0) {
     route_count_kernel<<<nch, kRouteThreads, sizeof(int32_t) * E, st>>>(ids, TK, E, r.chunk_counts, r.status);
+    count_launch();
     if ((rc = cuda_check(cudaGetLastError(), "route_count"))) return rc;
   }
   route_scan_kernel<<<1, 1024, 0, st>>>(nch, E, B, r.chunk_counts, r.expert_offsets, r.block_offsets, r.tile_offsets,
                                         r.expert_order, r.block_to_expert, r.tile_expert, r.scalars, r.num_blocks_out);
+  count_launch();
   if ((rc = cuda_check(cudaGetLastError(), "route_scan"))) return rc;
   if (nch > 0) {
     const size_t smem = sizeof(int32_t) * (size_t)(kRouteWarps * E + 3 * E);
@@ -229,6 +231,7 @@ int launch_route_meta(const int32_t* ids, int T, int K, int E, int B, int64_t Nb
                                                            r.block_offsets, r.tile_offsets, r.x_gather_idx,
                                                            r.s_scatter_idx, r.s_reverse, r.token_position_to_id,
                                                            r.tile_row_flat, r.flat_tile_row);
+    count_launch();
     if ((rc = cuda_check(cudaGetLastError(), "route_scatter"))) return rc;
   }
   return MOE_OK;

@@ -84,13 +84,14 @@ def test_bf16_intermediates_match_oracle():
     cfg = inp.cfg
     h = oracle_h(inp, meta)
     P = op.tile_rows
-    flat = op.region("TILE_ROW_FLAT").view(torch.int32).cpu().numpy()[:P]
+    used = int(op.region("TILE_OFFSETS").view(torch.int32)[cfg.E].item())   # rows of the used tiles
+    flat = op.region("TILE_ROW_FLAT").view(torch.int32).cpu().numpy()[:used]
     valid = flat >= 0
     t, k = flat[valid] // cfg.K, flat[valid] % cfg.K
-    dout_g = op.region("DOUT_G").view(torch.bfloat16).reshape(P, cfg.H).cpu()
+    dout_g = op.region("DOUT_G").view(torch.bfloat16).reshape(P, cfg.H).cpu()[:used]
     assert torch.equal(dout_g[torch.from_numpy(valid)], inp.dout[torch.from_numpy(t)])
     assert torch.all(dout_g[torch.from_numpy(~valid)] == 0)
-    x_gt = op.region("X_GT").view(torch.bfloat16).reshape(cfg.H, P).cpu()
+    x_gt = op.region("X_GT").view(torch.bfloat16).reshape(cfg.H, P).cpu()[:, :used]
     assert torch.equal(x_gt.T[torch.from_numpy(valid)], inp.x[torch.from_numpy(t)])
     # dh from the oracle's formulas
     from oracle import moe as om
@@ -102,10 +103,10 @@ def test_bf16_intermediates_match_oracle():
     gate, up = h[t, k, :cfg.I], h[t, k, cfg.I:]
     dA = s[t, k][:, None] * dA_raw
     dh_ref = np.concatenate([dA * up * om.dsilu(gate), dA * om.silu(gate)], 1)
-    dh = np64(op.region("DH").view(torch.bfloat16).reshape(P, 2 * cfg.I))
+    dh = np64(op.region("DH").view(torch.bfloat16).reshape(P, 2 * cfg.I))[:used]
     assert rel_fro(dh[valid], dh_ref) < BF16_TOL
     assert np.all(dh[~valid] == 0)
-    dht = np64(op.region("DH_T").view(torch.bfloat16).reshape(2 * cfg.I, P))
+    dht = np64(op.region("DH_T").view(torch.bfloat16).reshape(2 * cfg.I, P))[:, :used]
     assert np.array_equal(dht.T, dh)
 
 
@@ -135,13 +136,14 @@ def test_mxfp8_quantised_operands_match_oracle_codes():
     inp = make_moe_inputs(cfg)
     op, got = run_gpu(inp)
     P = op.tile_rows
-    flat = op.region("TILE_ROW_FLAT").view(torch.int32).cpu().numpy()[:P]
+    used = int(op.region("TILE_OFFSETS").view(torch.int32)[cfg.E].item())
+    flat = op.region("TILE_ROW_FLAT").view(torch.int32).cpu().numpy()[:used]
     valid = flat >= 0
     t = flat // cfg.K
     rows = np.where(valid[:, None], inp.dout.double().numpy()[np.where(valid, t, 0)], 0.0)
     rq, rs = omx.mx_quantize(rows, cfg.fp8_act, axis=1)
-    q = op.region("DOUT_G").cpu().numpy().reshape(P, cfg.H)
-    sf = tiled_sf_to_plain(op.region("DOUT_G_SF").cpu().numpy(), P, cfg.H)
+    q = op.region("DOUT_G").cpu().numpy().reshape(P, cfg.H)[:used]
+    sf = tiled_sf_to_plain(op.region("DOUT_G_SF").cpu().numpy(), P, cfg.H)[:used]
     assert np.array_equal(q, rq) and np.array_equal(sf, rs)
 
 

@@ -219,3 +219,34 @@ def test_mxfp8_restrictions_match_full():
     for t in (3, 40):
         assert np.allclose(part["dx"][t], full["dx"][t], rtol=0, atol=1e-12)
         assert np.array_equal(part["ds"][t], full["ds"][t])
+
+
+@pytest.mark.parametrize("mxfp8", [False, True])
+def test_subproblems_reproduce_full_problem(mxfp8):
+    """oracle.sample: expert samples keep those experts' weight gradients, token samples keep those
+    tokens' dx and ds, exactly."""
+    from oracle import route_meta as orm
+    from oracle import sample as osm
+    rng = np.random.default_rng(17)
+    T, H, I, E, K, B = 90, 64, 32, 5, 2, 128
+    x = torch.from_numpy(rng.standard_normal((T, H))).to(torch.bfloat16)
+    dout = torch.from_numpy(rng.standard_normal((T, H))).to(torch.bfloat16)
+    W1 = torch.from_numpy(rng.standard_normal((E, H, 2 * I)) * 0.1).to(torch.bfloat16)
+    W2 = torch.from_numpy(rng.standard_normal((E, I, H)) * 0.1).to(torch.bfloat16)
+    ids = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    s = rng.random((T, K))
+    N = orm.num_blocks_bound(T, K, E, B)
+    ckpt = torch.from_numpy(rng.standard_normal((N, 2, I, B))).to(torch.bfloat16)
+    meta = orm.route_meta(ids, E, B)
+    h = orm.checkpoint_rows(ckpt.double().numpy(), meta, T, K)
+    run = (lambda xx, dd, w1, w2, ss, ii, hh: om.moe_backward_mxfp8(xx, dd, w1, w2, ss, ii, hh)) if mxfp8 else \
+          (lambda xx, dd, w1, w2, ss, ii, hh: om.moe_backward(xx, dd, w1, w2, ss, ii, hh))
+    full = run(x, dout, W1, W2, s, ids, h)
+    sub = osm.subproblem(x, dout, W1, W2, s, ids, ckpt, B, experts=[1, 3])
+    g = run(sub["x"], sub["dout"], sub["W1"], sub["W2"], sub["s"], sub["ids"], sub["h"])
+    for j, e in enumerate(sub["experts"]):
+        assert np.array_equal(g["dW1"][j], full["dW1"][e]) and np.array_equal(g["dW2"][j], full["dW2"][e])
+    sub = osm.subproblem(x, dout, W1, W2, s, ids, ckpt, B, tokens=[0, 7, 44, 89])
+    g = run(sub["x"], sub["dout"], sub["W1"], sub["W2"], sub["s"], sub["ids"], sub["h"])
+    assert np.allclose(g["dx"], full["dx"][sub["tokens"]], rtol=0, atol=1e-12)
+    assert np.array_equal(g["ds"], full["ds"][sub["tokens"]])
