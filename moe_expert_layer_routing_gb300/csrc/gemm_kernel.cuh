@@ -36,8 +36,24 @@ struct GemmCfg {
   static constexpr int SFA_BYTES = MX ? 512 : 0;
   static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int EPI_WARP_BYTES = (EPI == kEpiDSwiGLU) ? (MX ? 3 * 32 * 32 : 3 * 32 * 40 * 2) : 0;
-  static constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
+  // dSwiGLU epilogue: one 32x32 transposition buffer per warp and a double-buffered checkpoint chunk
+  // (gate and up, 32 features x 128 tile rows each) filled by TMA one chunk ahead.
+  // dSwiGLU: 8 epilogue warps (two per TMEM lane quarter, each taking 16 of every 32 columns)
+  static constexpr int EPI_WARPS = (EPI == kEpiDSwiGLU) ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int EPI_WARP_BYTES = (EPI == kEpiDSwiGLU) ? 3 * 16 * 33 * 4 : 0;  // fp32 transposes
+  static constexpr int XCHG_BYTES = (EPI == kEpiDSwiGLU) ? 4 * 2 * 2 * 32 * 4 : 0;   // pair amax exchange
+  static constexpr int CK_CHUNK_BYTES = 2 * 32 * 128 * 2;
+  static constexpr int CK_BYTES = (EPI == kEpiDSwiGLU) ? 2 * CK_CHUNK_BYTES : 0;
+  // Store epilogue with a single TMEM accumulator: the tile is drained into a 128B-swizzled bf16
+  // staging tile in shared memory (TMEM released at once) and written by TMA stores.
+#ifdef MOEBWD_NO_TMA_STORE
+  static constexpr bool TMA_STORE = false;
+#else
+  static constexpr bool TMA_STORE = (EPI == kEpiStore) && ((MX && BN == 256) ? 1 : 2) == 1;
+#endif
+  static constexpr int STAGING_BYTES = TMA_STORE ? BM * BN * 2 : 0;
+  static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES + XCHG_BYTES + CK_BYTES + STAGING_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int STAGES_FIT = (kSmemLimit - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
@@ -48,9 +64,11 @@ struct GemmCfg {
   static constexpr int TMEM_COLS = COLS_NEEDED <= 32 ? 32 : COLS_NEEDED <= 64 ? 64 : COLS_NEEDED <= 128 ? 128
                                  : COLS_NEEDED <= 256 ? 256 : 512;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+  static constexpr int NCHUNK = BN / 32;
   static_assert(STAGES >= 2, "shared memory too small for a 2-stage pipeline");
   static_assert(COLS_NEEDED <= 512, "TMEM overflow");
   static_assert(SMEM_BYTES <= kSmemLimit, "shared memory overflow");
+  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && STAGING_BYTES % 1024 == 0, "tile alignment");
 };
 
 struct TileInfo {
@@ -138,143 +156,154 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const TileInfo& t
   }
 }
 
-// 32 rows (the warp's lanes) x 32 columns (v[]) written transposed: out[(row0 + c) * P + p0 + lane].
-__device__ __forceinline__ void store_transposed_bf16(uint16_t* buf, const float (&v)[32], uint16_t* out,
-                                                      int64_t P, int64_t row0, int64_t p0, int lane) {
-#pragma unroll
-  for (int j = 0; j < 32; ++j) buf[j * 40 + lane] = float_to_bf16_bits(v[j]);
-  __syncwarp();
-  const uint4* src = reinterpret_cast<const uint4*>(buf + lane * 40);
-  uint4* dst = reinterpret_cast<uint4*>(out + (row0 + lane) * P + p0);
-  const uint4 a = src[0], b = src[1], c = src[2], d = src[3];
-  dst[0] = a;
-  dst[1] = b;
-  dst[2] = c;
-  dst[3] = d;
-  __syncwarp();
+// Location of a tile's rows in the block checkpoint [N, 2, I, B]: block index and the slot of its first
+// row inside that block (the 128 rows of a tile never straddle a block since B % 128 == 0).
+__device__ __forceinline__ void tile_ckpt_origin(const GemmParams& p, const TileInfo& ti, int64_t& blk, int& b0) {
+  const int64_t j0 = (int64_t)ti.mt * 128 - p.e_tile_offsets[ti.e];
+  const int64_t slot0 = (int64_t)p.block_offsets[ti.e] * p.B + j0;
+  blk = slot0 / p.B;
+  b0 = (int)(slot0 - blk * p.B);
 }
 
-// Same, quantised along the 32 rows (groups of 32 tile rows) with one scale per output row.
-__device__ __forceinline__ void store_transposed_mx(uint8_t* buf, const float (&v)[32], uint8_t* out, uint8_t* sf,
-                                                    int64_t P, int64_t row0, int64_t p0, int lane, int fmt) {
-  uint32_t mybyte = 0;
+// Transposed store of 16 columns x 32 rows: v[j] of lane r is element (r, j).  The block is
+// transposed through shared memory as fp32 (pitch 33, conflict free); lane j < 16 then writes
+// output row row0 + j, columns p0..p0+31 (bf16, or fp8 codes + one scale quantised along them).
+template <bool MX>
+__device__ __forceinline__ void store_transposed16(float* buf, const float (&v)[16], void* out, uint8_t* sf,
+                                                   int64_t P, int64_t row0, int64_t p0, int lane, int fmt) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const uint32_t am = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[j])));
-    const uint32_t byte = e8m0_byte(am, fmt);
-    buf[j * 32 + lane] = (uint8_t)fp8_code(v[j] * e8m0_inv_scale(byte), fmt);
-    if (lane == j) mybyte = byte;
+  for (int j = 0; j < 16; ++j) buf[j * 33 + lane] = v[j];
+  __syncwarp();
+  if (lane < 16) {
+    float col[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) col[i] = buf[lane * 33 + i];
+    if constexpr (MX) {
+      uint32_t w[8];
+      const uint32_t byte = quantize_group32(col, fmt, w);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + (row0 + lane) * P + p0);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      sf[sf_tiled_offset(row0 + lane, p0, P)] = (uint8_t)byte;
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (row0 + lane) * P + p0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        dst[q] = make_uint4(pack_bf16x2(col[8 * q + 0], col[8 * q + 1]), pack_bf16x2(col[8 * q + 2], col[8 * q + 3]),
+                            pack_bf16x2(col[8 * q + 4], col[8 * q + 5]), pack_bf16x2(col[8 * q + 6], col[8 * q + 7]));
+    }
   }
   __syncwarp();
-  const uint4* src = reinterpret_cast<const uint4*>(buf + lane * 32);
-  uint4* dst = reinterpret_cast<uint4*>(out + (row0 + lane) * P + p0);
-  const uint4 a = src[0], b = src[1];
-  dst[0] = a;
-  dst[1] = b;
-  sf[sf_tiled_offset(row0 + lane, p0, P)] = (uint8_t)mybyte;
-  __syncwarp();
 }
 
-// G1 epilogue: from dA_raw (accumulator) and the checkpointed gate/up pre-activations compute
+// G1 epilogue, 16 columns (half `half` of a 32-column chunk starting at feature i0) of one warp:
+// from dA_raw (accumulator) and the checkpointed gate/up pre-activations (staged in shared memory,
+// [gate|up][32 features][128 rows]) compute
 //   ds += <dA_raw, a>,  dA = s dA_raw,  dgate = dA up SiLU'(gate),  dup = dA SiLU(gate),  a' = s a
-// and write dh [P,2I] (row-major), dh^T [2I,P], a'^T [I,P] (bf16, or fp8 + scales), plus this
-// tile's partial ds.  Padding rows produce zeros.
-template <bool MX, int BN>
-__device__ __forceinline__ void epi_dswiglu(const GemmParams& p, const TileInfo& ti, uint32_t taddr, int m,
-                                            int lane, uint8_t* wsm) {
-  const int64_t prow = (int64_t)ti.mt * 128 + m;
-  const int f = p.tile_row_flat[prow];
-  const bool valid = f >= 0;
-  const float sv = valid ? p.s[f] : 0.f;
-  const int64_t j = prow - p.e_tile_offsets[ti.e];
-  const int64_t slot = (int64_t)p.block_offsets[ti.e] * p.B + j;
-  const int64_t blk = slot / p.B, b = slot - (slot / p.B) * p.B;
-  const uint16_t* gb = p.ckpt + (blk * 2 + 0) * (int64_t)p.I * p.B + b;
-  const uint16_t* ub = p.ckpt + (blk * 2 + 1) * (int64_t)p.I * p.B + b;
+// and write dh [P,2I] (row-major), dh^T [2I,P], a'^T [I,P] (bf16, or fp8 + scales).  The row-wise
+// MXFP8 groups of dh (32 features) span both warps of a pair: partial amax values are exchanged
+// through `xchg` with a pair barrier.  Padding rows produce zeros.
+template <bool MX>
+__device__ __forceinline__ void epi_dswiglu_half(const GemmParams& p, uint32_t taddr, int64_t prow, int m, int lane,
+                                                 bool valid, float sv, int i0, int half, const uint16_t* ck,
+                                                 float* tbuf, float* xchg, int pair_id, float& ds_acc) {
   const int I = p.I;
   const int64_t P = p.P;
-  const int64_t p0 = (int64_t)ti.mt * 128 + (m & ~31);
-  float ds_acc = 0.f;
-#pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
-    const int i0 = ti.nt * BN + c * 32;
-    uint32_t r[32];
-    tmem_ld_32x32b_x32(taddr + c * 32, r);
-    tmem_ld_wait();
-    float dg[32], du[32], ap[32];
+  const int64_t p0 = prow - lane;
+  uint32_t r[16];
+  tmem_ld_32x32b_x16(taddr, r);
+  tmem_ld_wait();
+  float dg[16], du[16], ap[16];
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) {
-      float v = __uint_as_float(r[jj]);
-      float g = 0.f, u = 0.f;
-      if (valid) {
-        g = bf16_bits_to_float(gb[(int64_t)(i0 + jj) * p.B]);
-        u = bf16_bits_to_float(ub[(int64_t)(i0 + jj) * p.B]);
-      } else {
-        v = 0.f;
-      }
-      const float sg = 1.f / (1.f + __expf(-g));
-      const float sl = g * sg;
-      const float a = sl * u;
-      ds_acc = fmaf(v, a, ds_acc);
-      const float dA = sv * v;
-      dg[jj] = dA * u * (sg * (1.f + g * (1.f - sg)));
-      du[jj] = dA * sl;
-      ap[jj] = p.affinity_on_i ? sv * a : a;
+  for (int jj = 0; jj < 16; ++jj) {
+    float v = __uint_as_float(r[jj]);
+    float g = bf16_bits_to_float(ck[(half * 16 + jj) * 128 + m]);
+    float u = bf16_bits_to_float(ck[32 * 128 + (half * 16 + jj) * 128 + m]);
+    if (!valid) v = g = u = 0.f;
+    const float sg = __fdividef(1.f, 1.f + __expf(-g));
+    const float sl = g * sg;
+    const float a = sl * u;
+    ds_acc = fmaf(v, a, ds_acc);
+    const float dA = sv * v;
+    dg[jj] = dA * u * (sg * (1.f + g * (1.f - sg)));
+    du[jj] = dA * sl;
+    ap[jj] = p.affinity_on_i ? sv * a : a;
+  }
+  const int c0 = i0 + half * 16;  // first feature of this warp's 16 columns
+  if constexpr (MX) {
+    float amg = 0.f, amu = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      amg = fmaxf(amg, fabsf(dg[jj]));
+      amu = fmaxf(amu, fabsf(du[jj]));
     }
-    if constexpr (MX) {
-      uint8_t* dh = static_cast<uint8_t*>(p.dh) + prow * (2 * (int64_t)I);
-      uint32_t w[8];
-      uint32_t byte = quantize_group32(dg, p.fmt_act, w);
-      reinterpret_cast<uint4*>(dh + i0)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      reinterpret_cast<uint4*>(dh + i0)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      p.dh_sf[sf_tiled_offset(prow, i0, 2 * (int64_t)I)] = (uint8_t)byte;
-      byte = quantize_group32(du, p.fmt_act, w);
-      reinterpret_cast<uint4*>(dh + I + i0)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      reinterpret_cast<uint4*>(dh + I + i0)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      p.dh_sf[sf_tiled_offset(prow, I + i0, 2 * (int64_t)I)] = (uint8_t)byte;
-      store_transposed_mx(wsm, dg, static_cast<uint8_t*>(p.dht), p.dht_sf, P, i0, p0, lane, p.fmt_act);
-      store_transposed_mx(wsm + 1024, du, static_cast<uint8_t*>(p.dht), p.dht_sf, P, I + i0, p0, lane, p.fmt_act);
-      store_transposed_mx(wsm + 2048, ap, static_cast<uint8_t*>(p.apt), p.apt_sf, P, i0, p0, lane, p.fmt_act);
-    } else {
-      uint16_t* dh = static_cast<uint16_t*>(p.dh) + prow * (2 * (int64_t)I);
-      uint4* dgp = reinterpret_cast<uint4*>(dh + i0);
-      uint4* dup = reinterpret_cast<uint4*>(dh + I + i0);
+    // xchg layout: [half][gate|up][32 lanes]
+    xchg[(half * 2 + 0) * 32 + lane] = amg;
+    xchg[(half * 2 + 1) * 32 + lane] = amu;
+    pair_bar(pair_id);
+    amg = fmaxf(amg, xchg[((1 - half) * 2 + 0) * 32 + lane]);
+    amu = fmaxf(amu, xchg[((1 - half) * 2 + 1) * 32 + lane]);
+    uint8_t* dh = static_cast<uint8_t*>(p.dh) + prow * (2 * (int64_t)I);
+    const uint32_t bg = e8m0_byte(__float_as_uint(amg), p.fmt_act), bu = e8m0_byte(__float_as_uint(amu), p.fmt_act);
+    const float ig = e8m0_inv_scale(bg), iu = e8m0_inv_scale(bu);
+    uint4 qg, qu;
+    qg.x = fp8x4(dg[0] * ig, dg[1] * ig, dg[2] * ig, dg[3] * ig, p.fmt_act);
+    qg.y = fp8x4(dg[4] * ig, dg[5] * ig, dg[6] * ig, dg[7] * ig, p.fmt_act);
+    qg.z = fp8x4(dg[8] * ig, dg[9] * ig, dg[10] * ig, dg[11] * ig, p.fmt_act);
+    qg.w = fp8x4(dg[12] * ig, dg[13] * ig, dg[14] * ig, dg[15] * ig, p.fmt_act);
+    qu.x = fp8x4(du[0] * iu, du[1] * iu, du[2] * iu, du[3] * iu, p.fmt_act);
+    qu.y = fp8x4(du[4] * iu, du[5] * iu, du[6] * iu, du[7] * iu, p.fmt_act);
+    qu.z = fp8x4(du[8] * iu, du[9] * iu, du[10] * iu, du[11] * iu, p.fmt_act);
+    qu.w = fp8x4(du[12] * iu, du[13] * iu, du[14] * iu, du[15] * iu, p.fmt_act);
+    *reinterpret_cast<uint4*>(dh + c0) = qg;
+    *reinterpret_cast<uint4*>(dh + I + c0) = qu;
+    if (half == 0) {
+      p.dh_sf[sf_tiled_offset(prow, i0, 2 * (int64_t)I)] = (uint8_t)bg;
+      p.dh_sf[sf_tiled_offset(prow, I + i0, 2 * (int64_t)I)] = (uint8_t)bu;
+    }
+  } else {
+    pair_bar(pair_id);  // keep the pair barrier count identical on both paths
+    uint16_t* dh = static_cast<uint16_t*>(p.dh) + prow * (2 * (int64_t)I);
+    uint4* dgp = reinterpret_cast<uint4*>(dh + c0);
+    uint4* dup = reinterpret_cast<uint4*>(dh + I + c0);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        dgp[q] = make_uint4(pack_bf16x2(dg[8 * q + 0], dg[8 * q + 1]), pack_bf16x2(dg[8 * q + 2], dg[8 * q + 3]),
-                            pack_bf16x2(dg[8 * q + 4], dg[8 * q + 5]), pack_bf16x2(dg[8 * q + 6], dg[8 * q + 7]));
-        dup[q] = make_uint4(pack_bf16x2(du[8 * q + 0], du[8 * q + 1]), pack_bf16x2(du[8 * q + 2], du[8 * q + 3]),
-                            pack_bf16x2(du[8 * q + 4], du[8 * q + 5]), pack_bf16x2(du[8 * q + 6], du[8 * q + 7]));
-      }
-      uint16_t* buf = reinterpret_cast<uint16_t*>(wsm);
-      store_transposed_bf16(buf, dg, static_cast<uint16_t*>(p.dht), P, i0, p0, lane);
-      store_transposed_bf16(buf + 32 * 40, du, static_cast<uint16_t*>(p.dht), P, I + i0, p0, lane);
-      store_transposed_bf16(buf + 2 * 32 * 40, ap, static_cast<uint16_t*>(p.apt), P, i0, p0, lane);
+    for (int q = 0; q < 2; ++q) {
+      dgp[q] = make_uint4(pack_bf16x2(dg[8 * q + 0], dg[8 * q + 1]), pack_bf16x2(dg[8 * q + 2], dg[8 * q + 3]),
+                          pack_bf16x2(dg[8 * q + 4], dg[8 * q + 5]), pack_bf16x2(dg[8 * q + 6], dg[8 * q + 7]));
+      dup[q] = make_uint4(pack_bf16x2(du[8 * q + 0], du[8 * q + 1]), pack_bf16x2(du[8 * q + 2], du[8 * q + 3]),
+                          pack_bf16x2(du[8 * q + 4], du[8 * q + 5]), pack_bf16x2(du[8 * q + 6], du[8 * q + 7]));
     }
   }
-  p.ds_part[prow * (int64_t)(I / BN) + ti.nt] = valid ? ds_acc : 0.f;
+  store_transposed16<MX>(tbuf, dg, p.dht, p.dht_sf, P, c0, p0, lane, p.fmt_act);
+  store_transposed16<MX>(tbuf + 16 * 33, du, p.dht, p.dht_sf, P, I + c0, p0, lane, p.fmt_act);
+  store_transposed16<MX>(tbuf + 2 * 16 * 33, ap, p.apt, p.apt_sf, P, c0, p0, lane, p.fmt_act);
 }
+
 
 // ------------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------------
 template <bool MX, int BN, int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ GemmParams p) {
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams p) {
   using C = GemmCfg<MX, BN, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smA = smem;
   uint8_t* smB = smA + C::STAGES * C::A_BYTES;
-  uint8_t* smSFA = smB + C::STAGES * C::B_BYTES;
+  uint8_t* smStage = smB + C::STAGES * C::B_BYTES;      // output staging (TMA-store epilogue), 1024-aligned
+  uint8_t* smSFA = smStage + C::STAGING_BYTES;
   uint8_t* smSFB = smSFA + C::STAGES * C::SFA_BYTES;
-  uint8_t* smEPI = smSFB + C::STAGES * C::SFB_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smEPI + C::EPI_BYTES);
+  uint8_t* smCK = smSFB + C::STAGES * C::SFB_BYTES;     // checkpoint chunks (dSwiGLU epilogue), 512-aligned
+  uint8_t* smEPI = smCK + C::CK_BYTES;
+  float* smXchg = reinterpret_cast<float*>(smEPI + C::EPI_WARPS * C::EPI_WARP_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smEPI + C::EPI_WARPS * C::EPI_WARP_BYTES + C::XCHG_BYTES);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
-  uint64_t* done = tempty + 2;
+  uint64_t* ck_full = tempty + 2;
+  uint64_t* done = ck_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -288,13 +317,15 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], C::EPI_WARPS);
+      mbar_init(&ck_full[a], 1);
     }
     mbar_init(done, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (EPI == kEpiDSwiGLU || C::TMA_STORE) prefetch_tmap(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -375,17 +406,13 @@ __global__ void __launch_bounds__(192, 1)
             for (int h = 0; h < BN / 128; ++h)
               tmem_cp_32x128b_warpx4(sfb_t + 4 * h, make_smem_desc(smem_u32(smSFB + s * C::SFB_BYTES + h * 512), 0,
                                                                    128, kSwizzleNone));
+// one MMA per 32-wide K step over all BN columns; the scales of B rows 128..255 sit in the four
+// TMEM columns after those of rows 0..127
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t adesc = kmajor_sw128_desc(a0 + kk * 32);
-#pragma unroll
-              for (int h = 0; h < BN / 128; ++h) {
-                const uint64_t bdesc = kmajor_sw128_desc(b0 + h * 128 * 128 + kk * 32);
-                mma_mxf8(d + h * 128, adesc, bdesc,
-                         idesc_mxf8(128, 128, (uint32_t)p.fmt_a, (uint32_t)p.fmt_b, (uint32_t)kk, (uint32_t)kk),
-                         sfa_t, sfb_t + 4 * h, (kb | kk) != 0);
-              }
-            }
+            for (int kk = 0; kk < 4; ++kk)
+              mma_mxf8(d, kmajor_sw128_desc(a0 + kk * 32), kmajor_sw128_desc(b0 + kk * 32),
+                       idesc_mxf8(128, BN, (uint32_t)p.fmt_a, (uint32_t)p.fmt_b, (uint32_t)kk, (uint32_t)kk), sfa_t,
+                       sfb_t, (kb | kk) != 0);
           } else {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
@@ -416,18 +443,118 @@ __global__ void __launch_bounds__(192, 1)
     // ---------------- epilogue warps 2..5 ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int m = 32 * q + lane;
+    const int half = (warp - 2) >> 2;  // dSwiGLU: which 16 of every 32 columns
     uint8_t* wsm = smEPI + (warp - 2) * C::EPI_WARP_BYTES;
+    float* xchg = smXchg + q * (2 * 2 * 32);
+    const bool ck_leader = (EPI == kEpiDSwiGLU) && warp == 2 && lane == 0;
+    // checkpoint chunk n of the schedule goes to buffer n % 2; ck_issued = chunks issued so far
+    int64_t ck_next = 0, ck_issued = 0;
+    auto issue_ck = [&](int t, int c) {
+      const TileInfo tn = gemm_decode_tile<BN, C::BKE>(p, t);
+      int64_t blk;
+      int b0;
+      tile_ckpt_origin(p, tn, blk, b0);
+      const int buf = (int)(ck_issued & 1);
+      uint8_t* dst = smCK + buf * C::CK_CHUNK_BYTES;
+      const int i0 = tn.nt * BN + c * 32;
+      mbar_arrive_expect_tx(&ck_full[buf], C::CK_CHUNK_BYTES);
+      tma_load_2d(dst, &tmC, &ck_full[buf], b0, (int)((blk * 2 + 0) * p.I + i0));
+      tma_load_2d(dst + C::CK_CHUNK_BYTES / 2, &tmC, &ck_full[buf], b0, (int)((blk * 2 + 1) * p.I + i0));
+      ++ck_issued;
+    };
+    if (ck_leader && (int)blockIdx.x < total) issue_ck(blockIdx.x, 0);
     int acc = 0;
     uint32_t aph = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const TileInfo ti = gemm_decode_tile<BN, C::BKE>(p, t);
-      if (!mbar_wait_bounded(&tfull[acc], aph, p.status, abort_flag)) break;
+      const bool got = mbar_wait_bounded(&tfull[acc], aph, p.status, abort_flag);
+      if constexpr (EPI == kEpiDSwiGLU || C::TMA_STORE) {
+        // these epilogues synchronise their four warps with a named barrier: take every exit
+        // decision after a barrier, from the shared abort flag, so no warp is left waiting
+        epilogue_bar<32 * C::EPI_WARPS>();
+        if (*abort_flag) break;
+      } else if (!got) {
+        break;
+      }
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-      if constexpr (EPI == kEpiStore) {
+      if constexpr (C::TMA_STORE) {
+        // (1) the previous tile's stores must have read the staging tile before it is rewritten
+        if (warp == 2 && lane == 0) bulk_wait_read_all();
+        epilogue_bar<32 * C::EPI_WARPS>();
+        // (2) TMEM -> bf16 -> staging slab (64 columns x 128 rows, 128B swizzle), then TMEM is free
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          if (ti.nk > 0) {
+            tmem_ld_32x32b_x32(taddr + c * 32, r);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+          }
+          uint8_t* slab = smStage + (c >> 1) * (128 * 128);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int chunk = (c & 1) * 4 + q4;
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * q4 + 0]), __uint_as_float(r[8 * q4 + 1]));
+            w.y = pack_bf16x2(__uint_as_float(r[8 * q4 + 2]), __uint_as_float(r[8 * q4 + 3]));
+            w.z = pack_bf16x2(__uint_as_float(r[8 * q4 + 4]), __uint_as_float(r[8 * q4 + 5]));
+            w.w = pack_bf16x2(__uint_as_float(r[8 * q4 + 6]), __uint_as_float(r[8 * q4 + 7]));
+            *reinterpret_cast<uint4*>(slab + m * 128 + ((chunk ^ (m & 7)) << 4)) = w;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        // (3) make the staging writes visible to the async proxy, then one thread issues the stores
+        fence_proxy_async_smem();
+        epilogue_bar<32 * C::EPI_WARPS>();
+        if (warp == 2 && lane == 0) {
+          const int orow = (p.mode == kMGrouped ? 0 : ti.e * p.M) + ti.mt * 128;
+#pragma unroll 1
+          for (int sl = 0; sl < BN / 64; ++sl) tma_store_2d(&tmC, smStage + sl * (128 * 128), ti.nt * BN + sl * 64, orow);
+          bulk_commit();
+        }
+        if (++acc == C::ACC_STAGES) {
+          acc = 0;
+          aph ^= 1u;
+        }
+        continue;
+      } else if constexpr (EPI == kEpiStore) {
         epi_store<BN>(p, ti, taddr, m);
       } else {
-        epi_dswiglu<MX, BN>(p, ti, taddr, m, lane, wsm);
+        const int64_t prow = (int64_t)ti.mt * 128 + m;
+        const int f = p.tile_row_flat[prow];
+        const bool valid = f >= 0;
+        const float sv = valid ? p.s[f] : 0.f;
+        float ds_acc = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          if (ck_leader) {  // keep one chunk in flight ahead of the one being consumed
+            if (c + 1 < C::NCHUNK)
+              issue_ck(t, c + 1);
+            else if (t + (int)gridDim.x < total)
+              issue_ck(t + gridDim.x, 0);
+          }
+          const int buf = (int)(ck_next & 1);
+          // on a failed wait the chunk is still walked (garbage in, flagged by the status word) so
+          // that both warps of a pair reach the same barriers
+          mbar_wait_bounded(&ck_full[buf], (uint32_t)((ck_next >> 1) & 1), p.status, abort_flag);
+          epi_dswiglu_half<MX>(p, taddr + c * 32 + half * 16, prow, m, lane, valid, sv, ti.nt * BN + c * 32, half,
+                               reinterpret_cast<const uint16_t*>(smCK + buf * C::CK_CHUNK_BYTES),
+                               reinterpret_cast<float*>(wsm), xchg, 2 + q, ds_acc);
+          ++ck_next;
+          epilogue_bar<32 * C::EPI_WARPS>();  // every epilogue thread is done with this buffer before it is refilled
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+        p.ds_part[prow * (int64_t)(2 * (p.I / BN)) + 2 * ti.nt + half] = valid ? ds_acc : 0.f;
       }
       tc_fence_before();
       __syncwarp();
@@ -436,6 +563,10 @@ __global__ void __launch_bounds__(192, 1)
         acc = 0;
         aph ^= 1u;
       }
+    }
+    if (C::TMA_STORE && warp == 2 && lane == 0) bulk_wait_all();  // stores complete before exit
+    if (ck_leader) {  // drain checkpoint copies still in flight
+      for (int64_t n = ck_next; n < ck_issued; ++n) mbar_wait_drain(&ck_full[n & 1], (uint32_t)((n >> 1) & 1), p.status);
     }
   }
 
@@ -448,13 +579,15 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 template <bool MX, int BN, int EPI>
-int gemm_launch_instance(const GemmParams& p, const void* tmA, const void* tmB, int grid, cudaStream_t st) {
+int gemm_launch_instance(const GemmParams& p, const void* tmA, const void* tmB, const void* tmC, int grid,
+                         cudaStream_t st) {
   using C = GemmCfg<MX, BN, EPI>;
   auto kern = gemm_kernel<MX, BN, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(gemm)");
-  kern<<<grid, 192, C::SMEM_BYTES, st>>>(*static_cast<const CUtensorMap*>(tmA),
-                                        *static_cast<const CUtensorMap*>(tmB), p);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(*static_cast<const CUtensorMap*>(tmA),
+                                        *static_cast<const CUtensorMap*>(tmB),
+                                        *static_cast<const CUtensorMap*>(tmC), p);
   count_launch();
   return cuda_check(cudaGetLastError(), "gemm launch");
 }

@@ -4,12 +4,13 @@
 
 namespace moebwd {
 
-int launch_gemm_mx(int BN, const GemmParams& p, const void* tmA, const void* tmB, int grid, cudaStream_t st) {
+int launch_gemm_mx(int BN, const GemmParams& p, const void* tmA, const void* tmB, const void* tmC, int grid,
+                     cudaStream_t st) {
   if (p.epi == kEpiStore)
-    return BN == 256 ? gemm_launch_instance<true, 256, kEpiStore>(p, tmA, tmB, grid, st)
-                     : gemm_launch_instance<true, 128, kEpiStore>(p, tmA, tmB, grid, st);
-  return BN == 256 ? gemm_launch_instance<true, 256, kEpiDSwiGLU>(p, tmA, tmB, grid, st)
-                   : gemm_launch_instance<true, 128, kEpiDSwiGLU>(p, tmA, tmB, grid, st);
+    return BN == 256 ? gemm_launch_instance<true, 256, kEpiStore>(p, tmA, tmB, tmC, grid, st)
+                     : gemm_launch_instance<true, 128, kEpiStore>(p, tmA, tmB, tmC, grid, st);
+  return BN == 256 ? gemm_launch_instance<true, 256, kEpiDSwiGLU>(p, tmA, tmB, tmC, grid, st)
+                   : gemm_launch_instance<true, 128, kEpiDSwiGLU>(p, tmA, tmB, tmC, grid, st);
 }
 
 }  // namespace moebwd

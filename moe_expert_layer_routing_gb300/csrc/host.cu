@@ -60,7 +60,7 @@ static EncodeTiledFn encode_fn() {
 }
 
 bool make_tmap_2d(void* out_tmap, const void* base, int elem_bytes, uint64_t rows, uint64_t cols,
-                  uint64_t row_pitch_bytes, uint32_t box_rows, uint32_t box_cols) {
+                  uint64_t row_pitch_bytes, uint32_t box_rows, uint32_t box_cols, bool swizzle128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
@@ -74,7 +74,8 @@ bool make_tmap_2d(void* out_tmap, const void* base, int elem_bytes, uint64_t row
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     fail(MOE_ERR_INVALID, "cuTensorMapEncodeTiled failed (%d): rows=%llu cols=%llu pitch=%llu box=%ux%u", (int)r,
          (unsigned long long)rows, (unsigned long long)cols, (unsigned long long)row_pitch_bytes, box_rows, box_cols);

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <vector>
 
 #include "moebwd_internal.h"
@@ -15,18 +16,28 @@
 namespace moebwd {
 
 int launch_gemm(bool mx, int BN, const GemmParams& p, const void* A, int64_t a_rows, int64_t a_cols, const void* B,
-                int64_t b_rows, int64_t b_cols, cudaStream_t st) {
-  alignas(64) CUtensorMap ta, tb;
+                int64_t b_rows, int64_t b_cols, cudaStream_t st, const void* ckpt, int64_t ck_rows, int64_t ck_cols) {
+  alignas(64) CUtensorMap ta, tb, tc;
   const int es = mx ? 1 : 2;
   const uint32_t bke = mx ? 128 : 64;
   if (!make_tmap_2d(&ta, A, es, (uint64_t)a_rows, (uint64_t)a_cols, (uint64_t)a_cols * es, 128, bke))
     return MOE_ERR_INVALID;
   if (!make_tmap_2d(&tb, B, es, (uint64_t)b_rows, (uint64_t)b_cols, (uint64_t)b_cols * es, (uint32_t)BN, bke))
     return MOE_ERR_INVALID;
+  if (ckpt) {  // checkpoint chunks: 32 features x 128 rows of the [N*2*I, B] view, unswizzled
+    if (!make_tmap_2d(&tc, ckpt, 2, (uint64_t)ck_rows, (uint64_t)ck_cols, (uint64_t)ck_cols * 2, 32, 128, false))
+      return MOE_ERR_INVALID;
+  } else if (p.epi == kEpiStore) {  // output [rows, N] bf16, 64-column x 128-row boxes, 128B swizzle
+    const int64_t out_rows = p.mode == kMGrouped ? (int64_t)p.m_tiles * 128 : (int64_t)p.num_experts * p.M;
+    if (!make_tmap_2d(&tc, p.out, 2, (uint64_t)out_rows, (uint64_t)p.N, (uint64_t)p.ldo * 2, 128, 64, true))
+      return MOE_ERR_INVALID;
+  } else {
+    tc = ta;
+  }
   const int64_t tiles = (int64_t)(p.mode == kMGrouped ? p.m_tiles : p.num_experts * p.m_tiles) * p.n_tiles;
   const int grid = (int)std::min<int64_t>(tiles, device_sm_count());
   if (grid <= 0) return MOE_OK;
-  return mx ? launch_gemm_mx(BN, p, &ta, &tb, grid, st) : launch_gemm_bf16(BN, p, &ta, &tb, grid, st);
+  return mx ? launch_gemm_mx(BN, p, &ta, &tb, &tc, grid, st) : launch_gemm_bf16(BN, p, &ta, &tb, &tc, grid, st);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -61,6 +72,14 @@ static int64_t blocks_bound(int64_t T, int K, int E, int B) {
   return (num + B - 1) / B + E - 1;
 }
 
+// Tile-width override for tuning runs: the variable, if set to 128 or 256 dividing n, wins.
+static int bn_override(const char* name, int dflt, int64_t n) {
+  const char* v = getenv(name);
+  if (!v) return dflt;
+  const int bn = atoi(v);
+  return (bn == 128 || bn == 256) && n % bn == 0 ? bn : dflt;
+}
+
 static Layout make_layout(const MoeBwdArgs& a) {
   Layout L{};
   const bool mx = a.precision == MOE_PREC_MXFP8;
@@ -68,10 +87,16 @@ static Layout make_layout(const MoeBwdArgs& a) {
   L.TK = (int64_t)a.T * a.K;
   L.P = tile_capacity(L.TK, a.E);
   L.Nb = blocks_bound(a.T, a.K, a.E, a.block_size);
-  L.BN1 = a.I % 256 == 0 ? 256 : 128;
+  // N-tile widths: G1 carries the heavy dSwiGLU epilogue, so it takes 128 columns with a
+  // double-buffered TMEM accumulator; the store-epilogue GEMMs take 256 where N allows.
+  L.BN1 = 128;
   L.BN2 = a.H % 256 == 0 ? 256 : 128;
   L.BN3 = L.BN2;
   L.BN4 = 256;
+  L.BN1 = bn_override("MOEBWD_BN_G1", L.BN1, a.I);
+  L.BN2 = bn_override("MOEBWD_BN_G2", L.BN2, a.H);
+  L.BN3 = bn_override("MOEBWD_BN_G3", L.BN3, a.H);
+  L.BN4 = bn_override("MOEBWD_BN_G4", L.BN4, 2 * a.I);
   const int64_t P = L.P, H = a.H, I = a.I, E = a.E;
   size_t b[R_COUNT] = {};
   b[R_CHUNK_COUNTS] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, route_nchunks(L.TK)) * E;
@@ -98,7 +123,7 @@ static Layout make_layout(const MoeBwdArgs& a) {
     b[R_AP_T_SF] = (size_t)(I * P / 32);
   }
   b[R_DX_EXP] = (size_t)(P * H * 2);
-  b[R_DS_PART] = sizeof(float) * (size_t)(P * (I / L.BN1));
+  b[R_DS_PART] = sizeof(float) * (size_t)(P * 2 * (I / L.BN1));  // two column halves per N tile
   b[R_DS_BIAS] = a.has_bias ? sizeof(float) * (size_t)P : 0;
   size_t off = 0;
   for (int r = 0; r < R_COUNT; ++r) {
@@ -369,7 +394,9 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.apt = reg<void>(L, ws, R_AP_T); p.apt_sf = reg<uint8_t>(L, ws, R_AP_T_SF);
     p.ds_part = reg<float>(L, ws, R_DS_PART);
     p.status = a.status_dev;
-    if ((rc = launch_gemm(mx, L.BN1, p, reg<void>(L, ws, R_DOUT_G), P, H, W2, E * I, H, st))) return rc;
+    if ((rc = launch_gemm(mx, L.BN1, p, reg<void>(L, ws, R_DOUT_G), P, H, W2, E * I, H, st, a.gate_up_ckpt,
+                          L.Nb * 2 * I, a.block_size)))
+      return rc;
   }
   prof_mark(st, slot, 3);
   // 4. G3: dW2_e = a'^T dout_g over the expert's tile rows
@@ -439,7 +466,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   if ((rc = launch_dx_scatter_sum(reg<uint16_t>(L, ws, R_DX_EXP), flat_tile_row, a.T, a.K, a.H,
                                   static_cast<uint16_t*>(a.dx), st)))
     return rc;
-  if ((rc = launch_ds_finalize(reg<float>(L, ws, R_DS_PART), (int)(I / L.BN1), a.has_bias ? reg<float>(L, ws, R_DS_BIAS) : nullptr,
+  if ((rc = launch_ds_finalize(reg<float>(L, ws, R_DS_PART), (int)(2 * (I / L.BN1)), a.has_bias ? reg<float>(L, ws, R_DS_BIAS) : nullptr,
                                flat_tile_row, TK, a.ds, st)))
     return rc;
   if (a.has_bias) {

@@ -26,9 +26,10 @@ size_t align_up(size_t v, size_t a);
 void count_launch();   // one kernel launched by this library
 
 // 2D tensor map over a row-major [rows, cols] matrix of `elem_bytes`-byte elements with the given
-// row pitch, box [box_rows, box_cols], 128-byte swizzle.  Returns false on failure (message set).
+// row pitch, box [box_rows, box_cols], 128-byte swizzle (or none).  Returns false on failure (message set).
 bool make_tmap_2d(void* out_tmap /* CUtensorMap* */, const void* base, int elem_bytes, uint64_t rows,
-                  uint64_t cols, uint64_t row_pitch_bytes, uint32_t box_rows, uint32_t box_cols);
+                  uint64_t cols, uint64_t row_pitch_bytes, uint32_t box_rows, uint32_t box_cols,
+                  bool swizzle128 = true);
 
 // ------------------------------------------------------------------------------------------
 // routing (route_meta.cu)
@@ -126,10 +127,14 @@ struct GemmParams {
 };
 
 // A [rows, K] and B [rows, K] K-major operands (bf16 or fp8 bytes), tile counts in p.
+// The dSwiGLU epilogue also reads the checkpoint [N*2*I, B] (bf16) through a third tensor map.
 int launch_gemm(bool mx, int BN, const GemmParams& p, const void* A, int64_t a_rows, int64_t a_cols,
-                const void* B, int64_t b_rows, int64_t b_cols, cudaStream_t st);
-int launch_gemm_bf16(int BN, const GemmParams& p, const void* tmA, const void* tmB, int grid, cudaStream_t st);
-int launch_gemm_mx(int BN, const GemmParams& p, const void* tmA, const void* tmB, int grid, cudaStream_t st);
+                const void* B, int64_t b_rows, int64_t b_cols, cudaStream_t st, const void* ckpt = nullptr,
+                int64_t ck_rows = 0, int64_t ck_cols = 0);
+int launch_gemm_bf16(int BN, const GemmParams& p, const void* tmA, const void* tmB, const void* tmC, int grid,
+                     cudaStream_t st);
+int launch_gemm_mx(int BN, const GemmParams& p, const void* tmA, const void* tmB, const void* tmC, int grid,
+                   cudaStream_t st);
 
 // ------------------------------------------------------------------------------------------
 // reductions (reduce.cu)

@@ -48,6 +48,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
 }
 
+// Four FP8 codes (little-endian in one word) of a, b, c, d: two paired round-to-nearest-even
+// saturating conversions, then every code with zero magnitude made +0 (code 0x00).
+__device__ __forceinline__ uint32_t fp8x4(float a, float b, float c, float d, int fmt) {
+  uint16_t lo, hi;
+  if (fmt == MOE_FP8_E4M3) {
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  } else {
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  }
+  const uint32_t w = (uint32_t)lo | ((uint32_t)hi << 16);
+  const uint32_t mag = w & 0x7F7F7F7Fu;
+  const uint32_t nonzero = (mag + 0x7F7F7F7Fu) & 0x80808080u;  // per byte: 0x80 iff magnitude != 0
+  return mag | (w & nonzero);
+}
+
 // Quantise 32 values of one group into 32 FP8 codes (packed little-endian into 8 words) and
 // return the scale byte.
 __device__ __forceinline__ uint32_t quantize_group32(const float (&v)[32], int fmt, uint32_t (&w)[8]) {
@@ -57,10 +74,8 @@ __device__ __forceinline__ uint32_t quantize_group32(const float (&v)[32], int f
   const uint32_t byte = e8m0_byte(__float_as_uint(am), fmt);
   const float inv = e8m0_inv_scale(byte);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    w[j] = fp8_code(v[4 * j] * inv, fmt) | (fp8_code(v[4 * j + 1] * inv, fmt) << 8) |
-           (fp8_code(v[4 * j + 2] * inv, fmt) << 16) | (fp8_code(v[4 * j + 3] * inv, fmt) << 24);
-  }
+  for (int j = 0; j < 8; ++j)
+    w[j] = fp8x4(v[4 * j] * inv, v[4 * j + 1] * inv, v[4 * j + 2] * inv, v[4 * j + 3] * inv, fmt);
   return byte;
 }
 

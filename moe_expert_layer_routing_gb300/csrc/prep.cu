@@ -15,18 +15,25 @@
 
 namespace moebwd {
 
-constexpr int kPrepChunk = 64;   // H columns per step
-constexpr int kPrepPitch = 66;   // bf16 row pitch of the shared-memory tiles (bank-conflict free)
+constexpr int kPrepPitch = 66;       // bf16 row pitch of the 64-column tiles of the generic quantiser
+constexpr int kPrepCols = 256;       // H columns per step of the MoE prep kernel
+constexpr int kPrepTilePitch = 264;  // bf16 row pitch of its [128][256] tile (528 B: 16 B aligned)
+constexpr int kPrepSmem = 128 * kPrepTilePitch * 2;
 
+// Per 256-column chunk and per tensor (dout, then x): phase 1, each warp reads whole 512-byte row
+// segments of 16 gathered rows (16-byte vectors, 16 in flight per thread), writes the row-major
+// dout_g chunk and stages the tile in shared memory; phase 2, each thread owns one column and
+// writes its four 32-row groups of the transposed output (128 contiguous bytes for fp8, 256 for
+// bf16, per output row).
 template <bool MX, bool SCALE_T, bool BIAS>
-__global__ void __launch_bounds__(256) prep_kernel(const PrepArgs a) {
+__global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
   const int tile = blockIdx.x;
   if (tile >= *a.num_tiles) return;
-  __shared__ uint16_t sd[128 * kPrepPitch];
-  __shared__ uint16_t sx[128 * kPrepPitch];
+  extern __shared__ uint4 prep_smem[];
+  uint16_t* st = reinterpret_cast<uint16_t*>(prep_smem);
   __shared__ int32_t s_tok[128];
   __shared__ float s_s[128];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = a.H;
   const int64_t P = a.P;
   const int64_t prow0 = (int64_t)tile * 128;
@@ -37,130 +44,135 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepArgs a) {
   }
   const int e = BIAS ? a.tile_expert[tile] : 0;
   __syncthreads();
-  const int vec = tid & 7;
-  float bias_acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int h0 = 0; h0 < H; h0 += kPrepChunk) {
-    // ---- phase 1: gathered row loads, row-major dout_g, shared-memory staging ----
+  float bias_acc[16];
 #pragma unroll
-    for (int r4 = 0; r4 < 4; ++r4) {
-      const int row = (tid >> 3) + 32 * r4;
-      const int t = s_tok[row];
-      const int64_t col = h0 + vec * 8;
-      uint4 dv = make_uint4(0, 0, 0, 0), xv = make_uint4(0, 0, 0, 0);
-      if (t >= 0) {
-        dv = *reinterpret_cast<const uint4*>(a.dout + (int64_t)t * H + col);
-        xv = *reinterpret_cast<const uint4*>(a.x + (int64_t)t * H + col);
-      }
-      const int64_t prow = prow0 + row;
-      uint32_t* sdw = reinterpret_cast<uint32_t*>(sd + row * kPrepPitch + vec * 8);
-      uint32_t* sxw = reinterpret_cast<uint32_t*>(sx + row * kPrepPitch + vec * 8);
-      sdw[0] = dv.x; sdw[1] = dv.y; sdw[2] = dv.z; sdw[3] = dv.w;
-      sxw[0] = xv.x; sxw[1] = xv.y; sxw[2] = xv.z; sxw[3] = xv.w;
-      float d8[8];
-      const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+  for (int r = 0; r < 16; ++r) bias_acc[r] = 0.f;
+  for (int h0 = 0; h0 < H; h0 += kPrepCols) {
+    const int ncol = min(kPrepCols, H - h0);
+    const int col = h0 + lane * 8;
+    const bool colok = lane * 8 < ncol;
+#pragma unroll 1
+    for (int which = 0; which < 2; ++which) {
+      const uint16_t* src = which == 0 ? a.dout : a.x;
+      // ---- phase 1 ----
+      uint4 v[16];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        d8[2 * j] = __uint_as_float(dw[j] << 16);
-        d8[2 * j + 1] = __uint_as_float(dw[j] & 0xFFFF0000u);
+      for (int r = 0; r < 16; ++r) {
+        const int row = warp + 8 * r;
+        const int t = s_tok[row];
+        v[r] = make_uint4(0, 0, 0, 0);
+        if (t >= 0 && colok) v[r] = *reinterpret_cast<const uint4*>(src + (int64_t)t * H + col);
       }
-      if constexpr (BIAS) {
-        const uint4 bv = *reinterpret_cast<const uint4*>(a.b2 + (int64_t)e * H + col);
-        const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+      uint4 bv = make_uint4(0, 0, 0, 0);
+      if (BIAS && which == 0 && colok) bv = *reinterpret_cast<const uint4*>(a.b2 + (int64_t)e * H + col);
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const int row = warp + 8 * r;
+        const int64_t prow = prow0 + row;
+        if (colok) *reinterpret_cast<uint4*>(st + row * kPrepTilePitch + lane * 8) = v[r];
+        if (which != 0) continue;
+        const uint32_t dw[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+        float d8[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          bias_acc[r4] = fmaf(d8[2 * j], __uint_as_float(bw[j] << 16), bias_acc[r4]);
-          bias_acc[r4] = fmaf(d8[2 * j + 1], __uint_as_float(bw[j] & 0xFFFF0000u), bias_acc[r4]);
+          d8[2 * j] = __uint_as_float(dw[j] << 16);
+          d8[2 * j + 1] = __uint_as_float(dw[j] & 0xFFFF0000u);
+        }
+        if constexpr (BIAS) {
+          const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            bias_acc[r] = fmaf(d8[2 * j], __uint_as_float(bw[j] << 16), bias_acc[r]);
+            bias_acc[r] = fmaf(d8[2 * j + 1], __uint_as_float(bw[j] & 0xFFFF0000u), bias_acc[r]);
+          }
+        }
+        if constexpr (MX) {
+          float am = 0.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(d8[j]));
+          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+          if (!colok) continue;
+          const uint32_t byte = e8m0_byte(__float_as_uint(am), a.fmt);
+          const float inv = e8m0_inv_scale(byte);
+          uint2 q;
+          q.x = fp8x4(d8[0] * inv, d8[1] * inv, d8[2] * inv, d8[3] * inv, a.fmt);
+          q.y = fp8x4(d8[4] * inv, d8[5] * inv, d8[6] * inv, d8[7] * inv, a.fmt);
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.dout_g) + prow * H + col) = q;
+          if ((lane & 3) == 0) a.dout_g_sf[sf_tiled_offset(prow, col, H)] = (uint8_t)byte;
+        } else {
+          if (colok) *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dout_g) + prow * H + col) = v[r];
         }
       }
-      if constexpr (MX) {
-        float am = 0.f;
+      __syncthreads();
+      // ---- phase 2 ----
+      if (tid < ncol) {
+        const int h = tid;
+        const int64_t orow = h0 + h;
+        void* outp = which == 0 ? a.dout_gt : a.x_gt;
+        uint8_t* outsf = which == 0 ? a.dout_gt_sf : a.x_gt_sf;
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
+          float c32[32];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(d8[j]));
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-        const uint32_t byte = e8m0_byte(__float_as_uint(am), a.fmt);
-        const float inv = e8m0_inv_scale(byte);
-        uint2 q;
-        q.x = fp8_code(d8[0] * inv, a.fmt) | (fp8_code(d8[1] * inv, a.fmt) << 8) |
-              (fp8_code(d8[2] * inv, a.fmt) << 16) | (fp8_code(d8[3] * inv, a.fmt) << 24);
-        q.y = fp8_code(d8[4] * inv, a.fmt) | (fp8_code(d8[5] * inv, a.fmt) << 8) |
-              (fp8_code(d8[6] * inv, a.fmt) << 16) | (fp8_code(d8[7] * inv, a.fmt) << 24);
-        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.dout_g) + prow * H + col) = q;
-        if ((vec & 3) == 0) a.dout_g_sf[sf_tiled_offset(prow, col, H)] = (uint8_t)byte;
-      } else {
-        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dout_g) + prow * H + col) = dv;
-      }
-    }
-    __syncthreads();
-    // ---- phase 2: transposed writes, one (column, 32-row group) per thread ----
-    {
-      const int h = tid & 63;
-      const int g = tid >> 6;
-      float dcol[32], xcol[32];
+          for (int j = 0; j < 32; ++j) {
+            const int row = g * 32 + j;
+            float x = bf16_bits_to_float(st[row * kPrepTilePitch + h]);
+            if (SCALE_T && which == 0) x *= s_s[row];
+            c32[j] = x;
+          }
+          const int64_t ocol = prow0 + g * 32;
+          if constexpr (MX) {
+            uint32_t w[8];
+            const uint32_t byte = quantize_group32(c32, a.fmt, w);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(outp) + orow * P + ocol);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            outsf[sf_tiled_offset(orow, ocol, P)] = (uint8_t)byte;
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(outp) + orow * P + ocol);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int row = g * 32 + j;
-        float dvv = bf16_bits_to_float(sd[row * kPrepPitch + h]);
-        if constexpr (SCALE_T) dvv *= s_s[row];
-        dcol[j] = dvv;
-        xcol[j] = bf16_bits_to_float(sx[row * kPrepPitch + h]);
-      }
-      const int64_t orow = h0 + h;
-      const int64_t ocol = prow0 + g * 32;
-      if constexpr (MX) {
-        uint32_t w[8];
-        uint32_t byte = quantize_group32(dcol, a.fmt, w);
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dout_gt) + orow * P + ocol);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        a.dout_gt_sf[sf_tiled_offset(orow, ocol, P)] = (uint8_t)byte;
-        byte = quantize_group32(xcol, a.fmt, w);
-        dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.x_gt) + orow * P + ocol);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        a.x_gt_sf[sf_tiled_offset(orow, ocol, P)] = (uint8_t)byte;
-      } else {
-        uint4* dd = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dout_gt) + orow * P + ocol);
-        uint4* xd = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.x_gt) + orow * P + ocol);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          dd[q] = make_uint4(pack_bf16x2(dcol[8 * q + 0], dcol[8 * q + 1]), pack_bf16x2(dcol[8 * q + 2], dcol[8 * q + 3]),
-                             pack_bf16x2(dcol[8 * q + 4], dcol[8 * q + 5]), pack_bf16x2(dcol[8 * q + 6], dcol[8 * q + 7]));
-          xd[q] = make_uint4(pack_bf16x2(xcol[8 * q + 0], xcol[8 * q + 1]), pack_bf16x2(xcol[8 * q + 2], xcol[8 * q + 3]),
-                             pack_bf16x2(xcol[8 * q + 4], xcol[8 * q + 5]), pack_bf16x2(xcol[8 * q + 6], xcol[8 * q + 7]));
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pack_bf16x2(c32[8 * q + 0], c32[8 * q + 1]), pack_bf16x2(c32[8 * q + 2], c32[8 * q + 3]),
+                                  pack_bf16x2(c32[8 * q + 4], c32[8 * q + 5]), pack_bf16x2(c32[8 * q + 6], c32[8 * q + 7]));
+          }
         }
       }
+      __syncthreads();
     }
-    __syncthreads();
   }
   if constexpr (BIAS) {
 #pragma unroll
-    for (int r4 = 0; r4 < 4; ++r4) {
-      float v = bias_acc[r4];
-      v += __shfl_xor_sync(0xffffffffu, v, 1);
-      v += __shfl_xor_sync(0xffffffffu, v, 2);
-      v += __shfl_xor_sync(0xffffffffu, v, 4);
-      const int row = (tid >> 3) + 32 * r4;
-      if (vec == 0) a.ds_bias[prow0 + row] = s_tok[row] >= 0 ? v : 0.f;
+    for (int r = 0; r < 16; ++r) {
+      float v = bias_acc[r];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      const int row = warp + 8 * r;
+      if (lane == 0) a.ds_bias[prow0 + row] = s_tok[row] >= 0 ? v : 0.f;
     }
   }
+}
+
+template <bool MX, bool SCALE_T, bool BIAS>
+static int prep_launch(const PrepArgs& a, int grid, cudaStream_t st) {
+  auto k = prep_kernel<MX, SCALE_T, BIAS>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+  if (e != cudaSuccess) return cuda_check(e, "prep attribute");
+  k<<<grid, 256, kPrepSmem, st>>>(a);
+  count_launch();
+  return cuda_check(cudaGetLastError(), "prep");
 }
 
 int launch_prep(const PrepArgs& a, cudaStream_t st) {
   const int grid = (int)(a.P / 128);
   if (grid == 0) return MOE_OK;
   const bool bias = a.ds_bias != nullptr;
-#define MOE_PREP(MXV, ST, BI) prep_kernel<MXV, ST, BI><<<grid, 256, 0, st>>>(a)
   if (a.mx) {
-    if (a.scale_t) { if (bias) MOE_PREP(true, true, true); else MOE_PREP(true, true, false); }
-    else { if (bias) MOE_PREP(true, false, true); else MOE_PREP(true, false, false); }
-  } else {
-    if (a.scale_t) { if (bias) MOE_PREP(false, true, true); else MOE_PREP(false, true, false); }
-    else { if (bias) MOE_PREP(false, false, true); else MOE_PREP(false, false, false); }
+    if (a.scale_t) return bias ? prep_launch<true, true, true>(a, grid, st) : prep_launch<true, true, false>(a, grid, st);
+    return bias ? prep_launch<true, false, true>(a, grid, st) : prep_launch<true, false, false>(a, grid, st);
   }
-#undef MOE_PREP
-  count_launch();
-  return cuda_check(cudaGetLastError(), "prep");
+  if (a.scale_t) return bias ? prep_launch<false, true, true>(a, grid, st) : prep_launch<false, true, false>(a, grid, st);
+  return bias ? prep_launch<false, false, true>(a, grid, st) : prep_launch<false, false, false>(a, grid, st);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -202,10 +214,8 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint16_t* __re
     const uint32_t byte = e8m0_byte(__float_as_uint(am), fmt);
     const float inv = e8m0_inv_scale(byte);
     uint2 o;
-    o.x = fp8_code(d[0] * inv, fmt) | (fp8_code(d[1] * inv, fmt) << 8) | (fp8_code(d[2] * inv, fmt) << 16) |
-          (fp8_code(d[3] * inv, fmt) << 24);
-    o.y = fp8_code(d[4] * inv, fmt) | (fp8_code(d[5] * inv, fmt) << 8) | (fp8_code(d[6] * inv, fmt) << 16) |
-          (fp8_code(d[7] * inv, fmt) << 24);
+    o.x = fp8x4(d[0] * inv, d[1] * inv, d[2] * inv, d[3] * inv, fmt);
+    o.y = fp8x4(d[4] * inv, d[5] * inv, d[6] * inv, d[7] * inv, fmt);
     *reinterpret_cast<uint2*>(q + r * cols + c) = o;
     if (((c >> 3) & 3) == 0) sf[tiled ? sf_tiled_offset(r, c, cols) : r * (cols / 32) + c / 32] = (uint8_t)byte;
   }
