@@ -54,7 +54,8 @@ struct GemmCfg {
 #endif
   static constexpr int STAGING_BYTES = TMA_STORE ? BM * BN * 2 : 0;
   static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES + XCHG_BYTES + CK_BYTES + STAGING_BYTES;
-  static constexpr int BAR_BYTES = 256;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int RING = 4;  // tile indices published by the producer ahead of the consumers
   static constexpr int STAGES_FIT = (kSmemLimit - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int ACC_STAGES = (MX && BN == 256) ? 1 : 2;
@@ -304,7 +305,10 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* ck_full = tempty + 2;
   uint64_t* done = ck_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* tile_full = done + 1;          // ring slot r holds a tile index (producer arrives)
+  uint64_t* tile_empty = tile_full + C::RING;  // every consumer warp has read slot r
+  volatile int* tile_ring = reinterpret_cast<volatile int*>(tile_empty + C::RING);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(tile_ring) + C::RING);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -321,6 +325,10 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       mbar_init(&ck_full[a], 1);
     }
     mbar_init(done, 1);
+    for (int r = 0; r < C::RING; ++r) {
+      mbar_init(&tile_full[r], 1);
+      mbar_init(&tile_empty[r], 1 + C::EPI_WARPS);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
@@ -336,6 +344,8 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = gemm_total_tiles(p);
+  // Dynamic schedule: the producer claims tiles from a global counter (heaviest experts first in
+  // the K-grouped order) and publishes each index, then -1, through the ring.
 
   if (warp == 0) {
     if (lane == 0) {
@@ -343,7 +353,19 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       int s = 0;
       uint32_t ph = 0;
       int64_t issued = 0;
-      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int rs = 0;
+      uint32_t rph = 0;
+      for (;;) {
+        int t = atomicAdd(p.tile_counter, 1);
+        if (t >= total) t = -1;
+        if (!mbar_wait_bounded(&tile_empty[rs], rph ^ 1u, p.status, abort_flag)) break;
+        tile_ring[rs] = t;
+        mbar_arrive(&tile_full[rs]);
+        if (++rs == C::RING) {
+          rs = 0;
+          rph ^= 1u;
+        }
+        if (t < 0) break;
         const TileInfo ti = gemm_decode_tile<BN, C::BKE>(p, t);
         bool ok = true;
         for (int kb = 0; kb < ti.nk; ++kb) {
@@ -385,7 +407,17 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       int s = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int rs = 0;
+      uint32_t rph = 0;
+      while (ok) {
+        if (!mbar_wait_bounded(&tile_full[rs], rph, p.status, abort_flag)) break;
+        const int t = tile_ring[rs];
+        mbar_arrive(&tile_empty[rs]);
+        if (++rs == C::RING) {
+          rs = 0;
+          rph ^= 1u;
+        }
+        if (t < 0) break;
         const TileInfo ti = gemm_decode_tile<BN, C::BKE>(p, t);
         if (!mbar_wait_bounded(&tempty[acc], aph ^ 1u, p.status, abort_flag)) break;
         tc_fence_after();
@@ -462,12 +494,31 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       tma_load_2d(dst + C::CK_CHUNK_BYTES / 2, &tmC, &ck_full[buf], b0, (int)((blk * 2 + 1) * p.I + i0));
       ++ck_issued;
     };
-    if (ck_leader && (int)blockIdx.x < total) issue_ck(blockIdx.x, 0);
+    bool ck0_ready = false;  // chunk 0 of the coming tile already issued (prefetched)
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    int rs = 0;
+    uint32_t rph = 0;
+    while (ok) {
+      const bool gt = mbar_wait_bounded(&tile_full[rs], rph, p.status, abort_flag);
+      const int t = gt ? tile_ring[rs] : -1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tile_empty[rs]);
+      if (++rs == C::RING) {
+        rs = 0;
+        rph ^= 1u;
+      }
+      if constexpr (EPI == kEpiDSwiGLU || C::TMA_STORE) {
+        epilogue_bar<32 * C::EPI_WARPS>();  // uniform exit decision (see below)
+        if (*abort_flag) break;
+      }
+      if (t < 0) break;
       const TileInfo ti = gemm_decode_tile<BN, C::BKE>(p, t);
+      if (ck_leader) {
+        if (!ck0_ready) issue_ck(t, 0);
+        ck0_ready = false;
+      }
       const bool got = mbar_wait_bounded(&tfull[acc], aph, p.status, abort_flag);
       if constexpr (EPI == kEpiDSwiGLU || C::TMA_STORE) {
         // these epilogues synchronise their four warps with a named barrier: take every exit
@@ -534,10 +585,15 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
 #pragma unroll 1
         for (int c = 0; c < C::NCHUNK; ++c) {
           if (ck_leader) {  // keep one chunk in flight ahead of the one being consumed
-            if (c + 1 < C::NCHUNK)
+            if (c + 1 < C::NCHUNK) {
               issue_ck(t, c + 1);
-            else if (t + (int)gridDim.x < total)
-              issue_ck(t + gridDim.x, 0);
+            } else if (mbar_wait_bounded(&tile_full[rs], rph, p.status, abort_flag)) {
+              const int tn = tile_ring[rs];  // peek: the slot stays valid until this warp reads it
+              if (tn >= 0) {
+                issue_ck(tn, 0);
+                ck0_ready = true;
+              }
+            }
           }
           const int buf = (int)(ck_next & 1);
           // on a failed wait the chunk is still walked (garbage in, flagged by the status word) so

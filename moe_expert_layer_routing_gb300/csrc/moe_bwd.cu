@@ -47,7 +47,7 @@ enum Region {
   R_CHUNK_COUNTS, R_EXPERT_OFFSETS, R_BLOCK_OFFSETS, R_TILE_OFFSETS, R_EXPERT_ORDER, R_SCALARS,
   R_X_GATHER, R_S_SCATTER, R_S_REV, R_TPID, R_B2E, R_TILE_ROW_FLAT, R_FLAT_TILE_ROW, R_TILE_EXPERT,
   R_DOUT_G, R_DOUT_G_SF, R_DOUT_GT, R_DOUT_GT_SF, R_X_GT, R_X_GT_SF, R_DH, R_DH_SF, R_DH_T, R_DH_T_SF,
-  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNT
+  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_COUNT
 };
 
 struct Layout {
@@ -125,6 +125,7 @@ static Layout make_layout(const MoeBwdArgs& a) {
   b[R_DX_EXP] = (size_t)(P * H * 2);
   b[R_DS_PART] = sizeof(float) * (size_t)(P * 2 * (I / L.BN1));  // two column halves per N tile
   b[R_DS_BIAS] = a.has_bias ? sizeof(float) * (size_t)P : 0;
+  b[R_COUNTERS] = 64;  // one tile counter per grouped GEMM
   size_t off = 0;
   for (int r = 0; r < R_COUNT; ++r) {
     L.off[r] = off;
@@ -307,6 +308,8 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
 
   const int slot = prof_slot();
   prof_mark(st, slot, 0);
+  int32_t* counters = reg<int32_t>(L, ws, R_COUNTERS);
+  if ((rc = cuda_check(cudaMemsetAsync(counters, 0, L.bytes[R_COUNTERS], st), "memset tile counters"))) return rc;
   int32_t* tile_offsets = reg<int32_t>(L, ws, R_TILE_OFFSETS);
   int32_t* expert_order = reg<int32_t>(L, ws, R_EXPERT_ORDER);
   int32_t* scalars = reg<int32_t>(L, ws, R_SCALARS);
@@ -393,6 +396,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.dht = reg<void>(L, ws, R_DH_T); p.dht_sf = reg<uint8_t>(L, ws, R_DH_T_SF);
     p.apt = reg<void>(L, ws, R_AP_T); p.apt_sf = reg<uint8_t>(L, ws, R_AP_T_SF);
     p.ds_part = reg<float>(L, ws, R_DS_PART);
+    p.tile_counter = counters + 0;
     p.status = a.status_dev;
     if ((rc = launch_gemm(mx, L.BN1, p, reg<void>(L, ws, R_DOUT_G), P, H, W2, E * I, H, st, a.gate_up_ckpt,
                           L.Nb * 2 * I, a.block_size)))
@@ -415,6 +419,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.fmt_a = a.fp8_act; p.fmt_b = a.fp8_act;
     p.epi = kEpiStore;
     p.out = a.dW2; p.ldo = H; p.out_expert_stride = I * H;
+    p.tile_counter = counters + 1;
     p.status = a.status_dev;
     if ((rc = launch_gemm(mx, L.BN3, p, reg<void>(L, ws, R_AP_T), I, P, reg<void>(L, ws, R_DOUT_GT), H, P, st)))
       return rc;
@@ -437,6 +442,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.fmt_a = a.fp8_act; p.fmt_b = a.fp8_w;
     p.epi = kEpiStore;
     p.out = reg<void>(L, ws, R_DX_EXP); p.ldo = H;
+    p.tile_counter = counters + 2;
     p.status = a.status_dev;
     if ((rc = launch_gemm(mx, L.BN2, p, reg<void>(L, ws, R_DH), P, 2 * I, W1, E * H, 2 * I, st))) return rc;
   }
@@ -457,6 +463,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.fmt_a = a.fp8_act; p.fmt_b = a.fp8_act;
     p.epi = kEpiStore;
     p.out = a.dW1; p.ldo = 2 * I; p.out_expert_stride = H * 2 * I;
+    p.tile_counter = counters + 3;
     p.status = a.status_dev;
     if ((rc = launch_gemm(mx, L.BN4, p, reg<void>(L, ws, R_X_GT), H, P, reg<void>(L, ws, R_DH_T), 2 * I, P, st)))
       return rc;
@@ -521,17 +528,18 @@ extern "C" int moe_profile_read(double* stage_ms, int max_stages, int* calls) {
 // ------------------------------------------------------------------------------------------
 namespace {
 struct LinLayout {
-  size_t off[8], bytes[8], total;
+  size_t off[9], bytes[9], total;
 };
 LinLayout lin_layout(int64_t M, int64_t N, int64_t K, int precision) {
   LinLayout L{};
   const bool mx = precision == MOE_PREC_MXFP8;
   const int64_t es = mx ? 1 : 2;
-  // 0 dY (rowwise, mx only) 1 its sf | 2 W^T [K,N] 3 sf | 4 dY^T [N,M] 5 sf | 6 X^T [K,M] 7 sf
-  size_t b[8] = {mx ? (size_t)(M * N) : 0, mx ? (size_t)(M * N / 32) : 0, (size_t)(K * N * es), mx ? (size_t)(K * N / 32) : 0,
-                 (size_t)(N * M * es), mx ? (size_t)(N * M / 32) : 0, (size_t)(K * M * es), mx ? (size_t)(K * M / 32) : 0};
+  // 0 dY (rowwise, mx only) 1 its sf | 2 W^T [K,N] 3 sf | 4 dY^T [N,M] 5 sf | 6 X^T [K,M] 7 sf | 8 counters
+  size_t b[9] = {mx ? (size_t)(M * N) : 0, mx ? (size_t)(M * N / 32) : 0, (size_t)(K * N * es), mx ? (size_t)(K * N / 32) : 0,
+                 (size_t)(N * M * es), mx ? (size_t)(N * M / 32) : 0, (size_t)(K * M * es), mx ? (size_t)(K * M / 32) : 0,
+                 64 /* tile counters */};
   size_t off = 0;
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 9; ++i) {
     L.off[i] = off;
     L.bytes[i] = b[i];
     off = align_up(off + b[i], 256);
@@ -567,7 +575,9 @@ extern "C" int linear_bwd(const void* dY, const void* W, const void* X, int64_t 
   char* ws = static_cast<char*>(workspace);
   auto R = [&](int i) { return L.bytes[i] ? static_cast<void*>(ws + L.off[i]) : nullptr; };
   const uint16_t* dYb = static_cast<const uint16_t*>(dY);
-  int rc;
+  int32_t* counters = static_cast<int32_t*>(R(8));
+  int rc = cuda_check(cudaMemsetAsync(counters, 0, L.bytes[8], st), "memset tile counters");
+  if (rc) return rc;
   // operands: dX = dY @ W contracts over N, dW = dY^T @ X contracts over M
   if (mx && (rc = launch_quant_rowwise(dYb, M, M, N, N, nullptr, fp8_fmt, static_cast<uint8_t*>(R(0)),
                                        static_cast<uint8_t*>(R(1)), 1, st)))
@@ -594,6 +604,7 @@ extern "C" int linear_bwd(const void* dY, const void* W, const void* X, int64_t 
     p.fmt_a = p.fmt_b = fp8_fmt;
     p.epi = kEpiStore;
     p.out = dX; p.ldo = K;
+    p.tile_counter = counters + 0;
     if ((rc = launch_gemm(mx, BN, p, mx ? R(0) : dY, M, N, R(2), K, N, st))) return rc;
   }
   {
@@ -609,6 +620,7 @@ extern "C" int linear_bwd(const void* dY, const void* W, const void* X, int64_t 
     p.fmt_a = p.fmt_b = fp8_fmt;
     p.epi = kEpiStore;
     p.out = dW; p.ldo = K;
+    p.tile_counter = counters + 1;
     if ((rc = launch_gemm(mx, BN, p, R(4), N, M, R(6), K, M, st))) return rc;
   }
   return MOE_OK;

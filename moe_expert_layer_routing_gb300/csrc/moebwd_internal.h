@@ -122,7 +122,8 @@ struct GemmParams {
   void* dh; uint8_t* dh_sf;
   void* dht; uint8_t* dht_sf;
   void* apt; uint8_t* apt_sf;
-  float* ds_part;               // [P, I/BN]
+  float* ds_part;               // [P, 2*I/BN]
+  int32_t* tile_counter;        // zeroed before the launch: dynamic tile claims
   int32_t* status;
 };
 
