@@ -49,6 +49,69 @@ def source_sha():
     return h.hexdigest()[:16]
 
 
+def recorded_mxfp8_peak():
+    """MXFP8 dense GEMM peak measured through cuBLAS on this machine (`bench.py --measure-peaks`),
+    from a committed summary line `mxfp8_peak burst_tflops=.. sustained_tflops=..`."""
+    pdir = os.path.join(ROOT, "profiles")
+    pat = re.compile(r"mxfp8_peak burst_tflops=([0-9.]+) sustained_tflops=([0-9.]+)")
+    if os.path.isdir(pdir):
+        for name in sorted(os.listdir(pdir)):
+            if name.endswith((".md", ".txt")):
+                for line in open(os.path.join(pdir, name)):
+                    m = pat.search(line)
+                    if m:
+                        return float(m.group(1)), float(m.group(2))
+    return None
+
+
+def measure_peaks():
+    """Dense 8192^3 GEMMs through the vendor library: bf16 (torch.matmul) and MXFP8
+    (torch._scaled_mm, e4m3 operands, E8M0 scales per 32 K-elements), burst and ~3 s sustained."""
+    import torch
+    M = N = K = 8192
+    dev = "cuda"
+    res = {}
+
+    def timed(f, secs):
+        for _ in range(5):
+            f()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        best = 1e30
+        for _ in range(10):
+            e0.record()
+            f()
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        n, t0 = 0, time.time()
+        e0.record()
+        while time.time() - t0 < secs:
+            f()
+            n += 1
+        e1.record()
+        torch.cuda.synchronize()
+        return 2.0 * M * N * K / (best * 1e-3) / 1e12, 2.0 * M * N * K * n / (e0.elapsed_time(e1) * 1e-3) / 1e12
+
+    a = torch.randn(M, K, device=dev, dtype=torch.bfloat16)
+    b = torch.randn(N, K, device=dev, dtype=torch.bfloat16)
+    res["bf16_tflops_burst"], res["bf16_tflops_sustained"] = timed(lambda: a @ b.t(), 3.0)
+    try:
+        a8, b8 = a.to(torch.float8_e4m3fn), b.to(torch.float8_e4m3fn)
+        ns = ((M + 127) // 128 * 128) * ((K // 32 + 3) // 4 * 4)
+        sa = torch.full((ns,), 127, dtype=torch.uint8, device=dev).view(torch.float8_e8m0fnu)
+        sb = torch.full((ns,), 127, dtype=torch.uint8, device=dev).view(torch.float8_e8m0fnu)
+        f = lambda: torch._scaled_mm(a8, b8.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)  # noqa: E731
+        res["mxfp8_tflops_burst"], res["mxfp8_tflops_sustained"] = timed(f, 3.0)
+    except Exception as ex:  # library without block-scaled FP8 support
+        res["mxfp8_error"] = repr(ex)[:300]
+    res["how"] = "8192^3 GEMMs, CUDA events, best of 10 (burst) and back to back for 3 s (sustained)"
+    print(json.dumps(res), flush=True)
+    if "mxfp8_tflops_burst" in res:
+        print(f"mxfp8_peak burst_tflops={res['mxfp8_tflops_burst']:.1f} "
+              f"sustained_tflops={res['mxfp8_tflops_sustained']:.1f}", flush=True)
+
+
 def recorded_traffic(workload: str, stage: str):
     """DRAM bytes per launch of a stage from a committed ncu summary, only if it was captured on
     the current kernel sources (a line `traffic workload=.. stage=.. bytes_per_launch=.. source_sha=..`)."""
@@ -225,7 +288,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--measure-peaks", action="store_true", help="library GEMM peaks only")
     args = ap.parse_args()
+    if args.measure_peaks:
+        measure_peaks()
+        return
     args.warmup = max(args.warmup, 3)
 
     import torch
@@ -338,12 +405,18 @@ def main():
         achieved = stage_flops[dom] / (stages[dom] * 1e-3) / 1e12
         roofline = dict(bound="tensor", kernel=dom, achieved=achieved, peak=peak_tf, unit="TFLOP/s",
                         frac=achieved / peak_tf, traffic=recorded_traffic(cfg.name, dom),
+                        algorithmic_flops_per_launch=stage_flops[dom],
                         peak_source=f"{peak_src} bf16 burst" + (" x2 (nominal fp8/bf16)" if prec == 1 else ""))
     else:
         achieved = value / world
         roofline = dict(bound="tensor", kernel="linear_bwd (dX and dW GEMMs + quantisation)", achieved=achieved,
                         peak=peak_tf, unit="TFLOP/s", frac=achieved / peak_tf, traffic=None,
                         peak_source=f"{peak_src} bf16 burst x2 (nominal fp8/bf16)")
+
+    lib_peak = recorded_mxfp8_peak()
+    if prec == 1 and lib_peak:
+        roofline["frac_of_mxfp8_library"] = roofline["achieved"] / lib_peak[0]
+        roofline["mxfp8_library_peak"] = lib_peak[0]
 
     # ---------------------------------------------------------------- end to end through host buffers
     e2e = None
@@ -415,6 +488,7 @@ def main():
         higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="mxfp8" if prec == 1 else "bf16", data="synthetic (seeded; shapes and routing of the workload)",
         config=conf, tokens_per_s=tokens * world / (ms * 1e-3), pct_of_tensor_peak=100.0 * value / world / peak_tf,
+        pct_of_mxfp8_library_peak=(100.0 * value / world / lib_peak[0]) if (prec == 1 and lib_peak) else None,
         roofline=roofline, cpu_baseline=cpu_baseline, e2e=e2e, clocks=clk.summary(), gpu_launches=launches,
         stage_ms=stages, source_sha=source_sha())
     print(json.dumps(line), flush=True)
