@@ -108,6 +108,22 @@ int moe_route_meta(const int32_t* ids, int T, int K, int E, int block_size, int3
                    int32_t* num_blocks, int32_t* status_dev, void* workspace, size_t workspace_bytes,
                    moe_stream_t stream);
 
+/* moe_route_meta without a workspace, for callers that cannot allocate device memory (code inside
+ * a memory pool or arena without raw allocations, hooks that may not call cudaMalloc mid-step,
+ * callers that must not allocate after start-up).  None of the source pages has a counterpart: it is
+ * an interface addition of this library.  Same arguments, outputs and errors as moe_route_meta, minus
+ * the workspace: the scratch is a fixed 4 MiB device array owned by the library (held on every GPU
+ * that loads it, until exit), which admits about T*K <= 150k routed rows for E <= 128 (the exact
+ * limit is moe_route_meta_workspace_size(T,K,E,B) <= 4 MiB; larger sizes return
+ * MOE_ERR_UNSUPPORTED with a message and launch nothing).  The first call on a device looks up the
+ * array's device address and should come before any stream capture.  All calls on a device share
+ * the array: calls that overlap on the GPU race and must be serialised by the caller.  Allocates
+ * no memory. */
+int moe_route_meta_noalloc(const int32_t* ids, int T, int K, int E, int block_size, int32_t* expert_offsets,
+                           int32_t* x_gather_idx, int32_t* s_scatter_idx, int32_t* s_reverse_scatter_idx,
+                           int32_t* token_position_to_id, int32_t* block_to_expert, int32_t* block_offsets,
+                           int32_t* num_blocks, int32_t* status_dev, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------------------------ */
 /* MXFP8 quantisation                                                                          */
 /* ------------------------------------------------------------------------------------------ */

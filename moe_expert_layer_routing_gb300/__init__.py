@@ -28,7 +28,8 @@ WS_REGIONS = ["EXPERT_OFFSETS", "TILE_OFFSETS", "BLOCK_OFFSETS", "TILE_ROW_FLAT"
 EXPORTED = ["moe_last_error", "moe_version", "moe_num_blocks_bound", "moe_route_meta_workspace_size",
             "moe_route_meta", "mxfp8_quantize", "moe_bwd_workspace_size", "moe_bwd",
             "moe_bwd_workspace_region", "moe_tile_rows_capacity", "linear_bwd_workspace_size",
-            "linear_bwd", "moe_profile_enable", "moe_profile_read", "moe_kernel_launches"]
+            "linear_bwd", "moe_profile_enable", "moe_profile_read", "moe_kernel_launches",
+            "moe_route_meta_noalloc"]
 
 STAGES = ["route", "prep", "G1_dA_dswiglu", "G3_dW2", "G2_dx_expanded", "G4_dW1", "reduce"]
 
@@ -76,6 +77,7 @@ def lib():
         "moe_profile_enable": ([i32], i32),
         "moe_profile_read": ([ctypes.POINTER(ctypes.c_double), i32, ctypes.POINTER(i32)], i32),
         "moe_kernel_launches": ([], ctypes.c_uint64),
+        "moe_route_meta_noalloc": ([vp, i32, i32, i32, i32] + [vp] * 9 + [vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
