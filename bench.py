@@ -419,45 +419,74 @@ def main():
         roofline["mxfp8_library_peak"] = lib_peak[0]
 
     # ---------------------------------------------------------------- end to end through host buffers
+    # Each step copies its activations from pinned host memory and reads dx/ds (or dX/dW) back.
+    # Two bound problems alternate so that step i+1's host->device copy (copy stream) overlaps
+    # step i's backward (compute stream); events order every buffer reuse.
     e2e = None
     if not args.no_e2e:
         if is_linear:
-            host_in = {k: getattr(inp, k).cpu().pin_memory() for k in ("dY", "W", "X")}
-            dev_in = {k: getattr(inp, k) for k in ("dY", "W", "X")}
-            host_out = {k: torch.empty_like(getattr(op, k), device="cpu").pin_memory() for k in ("dX", "dW")}
-            dev_out = {k: getattr(op, k) for k in ("dX", "dW")}
+            names, onames = ["dY", "W", "X"], ["dX", "dW"]
+            ops = [op, mb.LinearBwd(cfg.M, cfg.N, cfg.K, mb.PREC_MXFP8, cfg.fp8, dev)]
+            dev_in = [{k: getattr(inp, k) for k in names}, {k: torch.empty_like(getattr(inp, k)) for k in names}]
+            runs = [lambda b: ops[b].run(dev_in[b]["dY"], dev_in[b]["W"], dev_in[b]["X"])] * 2
         else:
-            names = ["x", "dout", "s", "ids", "ckpt"]
-            host_in = {k: getattr(inp, k).cpu().pin_memory() for k in names}
-            dev_in = {k: getattr(inp, k) for k in names}
-            host_out = {k: torch.empty_like(getattr(op, k), device="cpu").pin_memory() for k in ("dx", "ds")}
-            dev_out = {k: getattr(op, k) for k in ("dx", "ds")}
+            names, onames = ["x", "dout", "s", "ids", "ckpt"], ["dx", "ds"]
+            op2 = mb.MoeBwd(T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K, block_size=cfg.block_size,
+                            precision=cfg.precision, affinity=cfg.affinity, fp8_act=cfg.fp8_act, fp8_w=cfg.fp8_w,
+                            has_bias=cfg.bias, device=dev)
+            ops = [op, op2]
+            dev_in = [{k: getattr(inp, k) for k in names}, {k: torch.empty_like(getattr(inp, k)) for k in names}]
+            kw2 = dict(kw)
+            kw2.update(dev_in[1])
+            op2.bind(**kw2)
+            runs = [lambda b: ops[b].run()] * 2
+        host_in = {k: getattr(inp, k).cpu().pin_memory() for k in names}
+        host_out = [{k: torch.empty_like(getattr(o, k), device="cpu").pin_memory() for k in onames} for o in ops]
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
+        copy = torch.cuda.Stream()      # host -> device
+        back = torch.cuda.Stream()      # device -> host
+        comp = stream
+        in_ready = [torch.cuda.Event(), torch.cuda.Event()]
+        done = [torch.cuda.Event(), torch.cuda.Event()]
+        out_read = [torch.cuda.Event(), torch.cuda.Event()]
 
-        def e2e_step():
-            for k, t in host_in.items():
-                dev_in[k].copy_(t, non_blocking=True)
-            step()
-            for k, t in host_out.items():
-                t.copy_(dev_out[k], non_blocking=True)
+        def e2e_steps(n):
+            for i in range(n):
+                b = i & 1
+                with torch.cuda.stream(copy):
+                    copy.wait_event(done[b])       # buffer b's previous backward has consumed its inputs
+                    for k, t in host_in.items():
+                        dev_in[b][k].copy_(t, non_blocking=True)
+                    in_ready[b].record(copy)
+                comp.wait_event(in_ready[b])
+                comp.wait_event(out_read[b])       # buffer b's previous outputs have been read back
+                runs[b](b)
+                done[b].record(comp)
+                with torch.cuda.stream(back):
+                    back.wait_event(done[b])
+                    for k, t in host_out[b].items():
+                        t.copy_(getattr(ops[b], k), non_blocking=True)
+                    out_read[b].record(back)
 
-        for _ in range(2):
-            e2e_step()
+        e2e_steps(2)
         torch.cuda.synchronize()
         barrier(world)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
+        e0.record(copy)
+        comp.wait_event(e0)
+        e2e_steps(args.steps)
+        comp.wait_stream(back)
+        e1.record(comp)
         torch.cuda.synchronize()
         ems = allreduce_max(e0.elapsed_time(e1) / args.steps, world)
         e2e = dict(value=flops * world / (ems * 1e-3) / 1e12, unit="TFLOP/s", ms_per_step=ems,
                    h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
-                   note="activations (x, dout, s, ids, checkpoint) in, dx and ds out; weights and weight "
-                        "gradients stay resident" if not is_linear else "dY, W, X in; dX, dW out")
+                   note=("activations (x, dout, s, ids, checkpoint) in, dx and ds out; weights and weight "
+                         "gradients stay resident; copies overlap the previous step's backward" if not is_linear
+                         else "dY, W, X in; dX, dW out; copies overlap the previous step"))
+        del ops, dev_in
 
     if rank != 0:
         barrier(world)

@@ -240,6 +240,29 @@ int moe_bwd_workspace_region(const MoeBwdArgs* args, int region, size_t* offset,
 int64_t moe_tile_rows_capacity(int T, int K, int E);
 
 /* ------------------------------------------------------------------------------------------ */
+/* Router backward (the consumer of ds)                                                        */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Forms of the router forward ([SM] `_topk_softmax_bwd`, `_topk_bwd`). */
+enum {
+  MOE_ROUTER_SOFTMAX_OVER_TOPK = 0, /* s = softmax over the K selected logits */
+  MOE_ROUTER_TOPK_OVER_SOFTMAX = 1, /* s = top-K of softmax over all E logits (renorm: / their sum) */
+  MOE_ROUTER_TOPK = 2               /* s = the K selected logits */
+};
+
+/* Gradient of the router logits from the gradient of the routing scores (dscores = moe_bwd's ds).
+ *   SOFTMAX_OVER_TOPK: dlogits[idx_k] = s_k (g_k - <g, s>), 0 elsewhere; needs `scores` (forward s).
+ *   TOPK_OVER_SOFTMAX: p = softmax(logits) recomputed over all E; dr = (g - <g, s>) / sum(p[idx])
+ *                      when `renorm` (needs `scores`), else g; dlogits = p (scatter(dr) - <dr, p[idx]>)
+ *                      for every logit; needs `logits`.
+ *   TOPK:              dlogits[idx_k] = g_k, 0 elsewhere.
+ * logits (device) fp32 [T,E]; scores, dscores (device) fp32 [T,K]; ids (device) int32 [T,K];
+ * dlogits (device) fp32 [T,E], fully written.  K <= 64.  Repeated ids accumulate; ids outside [0,E)
+ * are skipped.  fp32 arithmetic. */
+int moe_router_bwd(int mode, int renorm, const float* logits, const float* scores, const float* dscores,
+                   const int32_t* ids, int T, int K, int E, float* dlogits, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------ */
 /* Instrumentation                                                                             */
 /* ------------------------------------------------------------------------------------------ */
 

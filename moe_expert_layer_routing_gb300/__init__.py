@@ -29,7 +29,7 @@ EXPORTED = ["moe_last_error", "moe_version", "moe_num_blocks_bound", "moe_route_
             "moe_route_meta", "mxfp8_quantize", "moe_bwd_workspace_size", "moe_bwd",
             "moe_bwd_workspace_region", "moe_tile_rows_capacity", "linear_bwd_workspace_size",
             "linear_bwd", "moe_profile_enable", "moe_profile_read", "moe_kernel_launches",
-            "moe_route_meta_noalloc"]
+            "moe_route_meta_noalloc", "moe_router_bwd"]
 
 STAGES = ["route", "prep", "G1_dA_dswiglu", "G3_dW2", "G2_dx_expanded", "G4_dW1", "reduce"]
 
@@ -78,6 +78,7 @@ def lib():
         "moe_profile_read": ([ctypes.POINTER(ctypes.c_double), i32, ctypes.POINTER(i32)], i32),
         "moe_kernel_launches": ([], ctypes.c_uint64),
         "moe_route_meta_noalloc": ([vp, i32, i32, i32, i32] + [vp] * 9 + [vp], i32),
+        "moe_router_bwd": ([i32, i32, vp, vp, vp, vp, i32, i32, i32, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -279,6 +280,21 @@ def moe_bwd(*, x, dout, s, ids, ckpt, E, I, block_size, W1=None, W2=None, W1_q=N
             W2_sf=W2_sf, b2=b2).run(stream)
     out = op.outputs()
     out["_op"] = op
+    return out
+
+
+ROUTER_SOFTMAX_OVER_TOPK, ROUTER_TOPK_OVER_SOFTMAX, ROUTER_TOPK = 0, 1, 2
+
+
+def router_bwd(mode: int, ids: torch.Tensor, dscores: torch.Tensor, E: int, logits=None, scores=None,
+               renorm: bool = False, stream=None) -> torch.Tensor:
+    """moe_router_bwd: gradient of the router logits [T, E] from the scores' gradient [T, K]."""
+    _need_cuda(ids, dscores, logits, scores)
+    T, K = ids.shape
+    out = torch.empty(T, E, dtype=torch.float32, device=ids.device)
+    rc = lib().moe_router_bwd(mode, int(renorm), _ptr(logits), _ptr(scores), _ptr(dscores), _ptr(ids), T, K, E,
+                              _ptr(out), _stream(stream))
+    _check(rc, "moe_router_bwd")
     return out
 
 

@@ -39,8 +39,6 @@ struct GemmCfg {
   // dSwiGLU epilogue: one 32x32 transposition buffer per warp and a double-buffered checkpoint chunk
   // (gate and up, 32 features x 128 tile rows each) filled by TMA one chunk ahead.
   // dSwiGLU: 8 epilogue warps (two per TMEM lane quarter, each taking 16 of every 32 columns)
-  static constexpr int EPI_WARPS = (EPI == kEpiDSwiGLU) ? 8 : 4;
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int EPI_WARP_BYTES = (EPI == kEpiDSwiGLU) ? 3 * 16 * 33 * 4 : 0;  // fp32 transposes
   static constexpr int XCHG_BYTES = (EPI == kEpiDSwiGLU) ? 4 * 2 * 2 * 32 * 4 : 0;   // pair amax exchange
   static constexpr int CK_CHUNK_BYTES = 2 * 32 * 128 * 2;
@@ -53,6 +51,9 @@ struct GemmCfg {
   static constexpr bool TMA_STORE = (EPI == kEpiStore) && ((MX && BN == 256) ? 1 : 2) == 1;
 #endif
   static constexpr int STAGING_BYTES = TMA_STORE ? BM * BN * 2 : 0;
+  // dSwiGLU and TMA-store epilogues: 8 warps, two per TMEM lane quarter, splitting the columns
+  static constexpr int EPI_WARPS = (EPI == kEpiDSwiGLU || TMA_STORE) ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES + XCHG_BYTES + CK_BYTES + STAGING_BYTES;
   static constexpr int BAR_BYTES = 512;
   static constexpr int RING = 4;  // tile indices published by the producer ahead of the consumers
@@ -167,32 +168,39 @@ __device__ __forceinline__ void tile_ckpt_origin(const GemmParams& p, const Tile
 }
 
 // Transposed store of 16 columns x 32 rows: v[j] of lane r is element (r, j).  The block is
-// transposed through shared memory as fp32 (pitch 33, conflict free); lane j < 16 then writes
-// output row row0 + j, columns p0..p0+31 (bf16, or fp8 codes + one scale quantised along them).
+// transposed through shared memory as fp32 (pitch 33, conflict free); lane l then handles column
+// l % 16, rows 16*(l / 16) .. +15, so output row row0 + l % 16 gets columns p0..p0+31 from two lanes
+// (bf16, or fp8 codes with one scale quantised along all 32: the two lanes combine their amax).
 template <bool MX>
 __device__ __forceinline__ void store_transposed16(float* buf, const float (&v)[16], void* out, uint8_t* sf,
                                                    int64_t P, int64_t row0, int64_t p0, int lane, int fmt) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) buf[j * 33 + lane] = v[j];
   __syncwarp();
-  if (lane < 16) {
-    float col[32];
+  const int c = lane & 15, rh = lane >> 4;
+  float col[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) col[i] = buf[lane * 33 + i];
-    if constexpr (MX) {
-      uint32_t w[8];
-      const uint32_t byte = quantize_group32(col, fmt, w);
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + (row0 + lane) * P + p0);
-      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      sf[sf_tiled_offset(row0 + lane, p0, P)] = (uint8_t)byte;
-    } else {
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (row0 + lane) * P + p0);
+  for (int i = 0; i < 16; ++i) col[i] = buf[c * 33 + rh * 16 + i];
+  if constexpr (MX) {
+    float am = 0.f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        dst[q] = make_uint4(pack_bf16x2(col[8 * q + 0], col[8 * q + 1]), pack_bf16x2(col[8 * q + 2], col[8 * q + 3]),
-                            pack_bf16x2(col[8 * q + 4], col[8 * q + 5]), pack_bf16x2(col[8 * q + 6], col[8 * q + 7]));
-    }
+    for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(col[i]));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 16));
+    const uint32_t byte = e8m0_byte(__float_as_uint(am), fmt);
+    const float inv = e8m0_inv_scale(byte);
+    uint4 q;
+    q.x = fp8x4(col[0] * inv, col[1] * inv, col[2] * inv, col[3] * inv, fmt);
+    q.y = fp8x4(col[4] * inv, col[5] * inv, col[6] * inv, col[7] * inv, fmt);
+    q.z = fp8x4(col[8] * inv, col[9] * inv, col[10] * inv, col[11] * inv, fmt);
+    q.w = fp8x4(col[12] * inv, col[13] * inv, col[14] * inv, col[15] * inv, fmt);
+    *reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + (row0 + c) * P + p0 + rh * 16) = q;
+    if (rh == 0) sf[sf_tiled_offset(row0 + c, p0, P)] = (uint8_t)byte;
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (row0 + c) * P + p0 + rh * 16);
+    dst[0] = make_uint4(pack_bf16x2(col[0], col[1]), pack_bf16x2(col[2], col[3]), pack_bf16x2(col[4], col[5]),
+                        pack_bf16x2(col[6], col[7]));
+    dst[1] = make_uint4(pack_bf16x2(col[8], col[9]), pack_bf16x2(col[10], col[11]), pack_bf16x2(col[12], col[13]),
+                        pack_bf16x2(col[14], col[15]));
   }
   __syncwarp();
 }
@@ -475,7 +483,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
     // ---------------- epilogue warps 2..5 ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int m = 32 * q + lane;
-    const int half = (warp - 2) >> 2;  // dSwiGLU: which 16 of every 32 columns
+    const int half = (warp - 2) >> 2;  // dSwiGLU: which 16 of every 32 columns; TMA store: which half
     uint8_t* wsm = smEPI + (warp - 2) * C::EPI_WARP_BYTES;
     float* xchg = smXchg + q * (2 * 2 * 32);
     const bool ck_leader = (EPI == kEpiDSwiGLU) && warp == 2 && lane == 0;
@@ -536,7 +544,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         epilogue_bar<32 * C::EPI_WARPS>();
         // (2) TMEM -> bf16 -> staging slab (64 columns x 128 rows, 128B swizzle), then TMEM is free
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {  // this warp's half of the columns
           uint32_t r[32];
           if (ti.nk > 0) {
             tmem_ld_32x32b_x32(taddr + c * 32, r);

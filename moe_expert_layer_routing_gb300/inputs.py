@@ -117,7 +117,7 @@ def _zipf_bias(E: int, alpha: float, gen: torch.Generator, device) -> torch.Tens
 def _route(cfg: MoeConfig, gen: torch.Generator, device):
     logits = torch.randn(cfg.T, cfg.E, generator=gen, device=device)
     if cfg.zipf_alpha <= 0.0:
-        return _topk_route(logits, cfg.K) + (None,)
+        return _topk_route(logits, cfg.K) + (None, logits)
     bias = _zipf_bias(cfg.E, cfg.zipf_alpha, gen, device)
 
     def loads(c):
@@ -136,7 +136,7 @@ def _route(cfg: MoeConfig, gen: torch.Generator, device):
         else:
             lo = mid
     s, ids = _topk_route(logits + hi * bias, cfg.K)
-    return s, ids, hi
+    return s, ids, hi, logits + hi * bias
 
 
 @dataclass
@@ -175,10 +175,10 @@ def make_moe_inputs(cfg: MoeConfig, device="cpu") -> MoeInputs:
     if cfg.bias:
         b1 = (torch.randn(E, 2 * I, generator=gen, device=device) * 0.01).to(torch.bfloat16)
         b2 = (torch.randn(E, H, generator=gen, device=device) * 0.01).to(torch.bfloat16)
-    s, ids, zs = _route(cfg, gen, device)
+    s, ids, zs, logits = _route(cfg, gen, device)
     N = num_blocks_bound(T, K, E, B)
     ckpt = (torch.randn(N, 2, I, B, generator=gen, device=device) * (0.02 * math.sqrt(H))).to(torch.bfloat16)
-    return MoeInputs(cfg, x, dout, W1, W2, b1, b2, s, ids, ckpt, zs)
+    return MoeInputs(cfg, x, dout, W1, W2, b1, b2, s, ids, ckpt, zs, extra=dict(logits=logits.float().contiguous()))
 
 
 @dataclass
