@@ -50,7 +50,8 @@ struct GemmCfg {
 #else
   static constexpr bool TMA_STORE = (EPI == kEpiStore) && ((MX && BN == 256) ? 1 : 2) == 1;
 #endif
-  static constexpr int STAGING_BYTES = TMA_STORE ? BM * BN * 2 : 0;
+  // one 64-column staging slab (16 KB) keeps a fourth pipeline stage in shared memory
+  static constexpr int STAGING_BYTES = TMA_STORE ? BM * 64 * 2 : 0;
   // dSwiGLU and TMA-store epilogues: 8 warps, two per TMEM lane quarter, splitting the columns
   static constexpr int EPI_WARPS = (EPI == kEpiDSwiGLU || TMA_STORE) ? 8 : 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
@@ -539,12 +540,12 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
       if constexpr (C::TMA_STORE) {
-        // (1) the previous tile's stores must have read the staging tile before it is rewritten
-        if (warp == 2 && lane == 0) bulk_wait_read_all();
-        epilogue_bar<32 * C::EPI_WARPS>();
-        // (2) TMEM -> bf16 -> staging slab (64 columns x 128 rows, 128B swizzle), then TMEM is free
+        // one 64-column slab at a time through a single staging slab; TMEM is free after the last
 #pragma unroll 1
-        for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {  // this warp's half of the columns
+        for (int sl = 0; sl < BN / 64; ++sl) {
+          if (warp == 2 && lane == 0) bulk_wait_read_all();
+          epilogue_bar<32 * C::EPI_WARPS>();
+          const int c = sl * 2 + half;
           uint32_t r[32];
           if (ti.nk > 0) {
             tmem_ld_32x32b_x32(taddr + c * 32, r);
@@ -553,29 +554,28 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = 0u;
           }
-          uint8_t* slab = smStage + (c >> 1) * (128 * 128);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
-            const int chunk = (c & 1) * 4 + q4;
+            const int chunk = half * 4 + q4;
             uint4 w;
             w.x = pack_bf16x2(__uint_as_float(r[8 * q4 + 0]), __uint_as_float(r[8 * q4 + 1]));
             w.y = pack_bf16x2(__uint_as_float(r[8 * q4 + 2]), __uint_as_float(r[8 * q4 + 3]));
             w.z = pack_bf16x2(__uint_as_float(r[8 * q4 + 4]), __uint_as_float(r[8 * q4 + 5]));
             w.w = pack_bf16x2(__uint_as_float(r[8 * q4 + 6]), __uint_as_float(r[8 * q4 + 7]));
-            *reinterpret_cast<uint4*>(slab + m * 128 + ((chunk ^ (m & 7)) << 4)) = w;
+            *reinterpret_cast<uint4*>(smStage + m * 128 + ((chunk ^ (m & 7)) << 4)) = w;
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
-        // (3) make the staging writes visible to the async proxy, then one thread issues the stores
-        fence_proxy_async_smem();
-        epilogue_bar<32 * C::EPI_WARPS>();
-        if (warp == 2 && lane == 0) {
-          const int orow = (p.mode == kMGrouped ? 0 : ti.e * p.M) + ti.mt * 128;
-#pragma unroll 1
-          for (int sl = 0; sl < BN / 64; ++sl) tma_store_2d(&tmC, smStage + sl * (128 * 128), ti.nt * BN + sl * 64, orow);
-          bulk_commit();
+          if (sl == BN / 64 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+          fence_proxy_async_smem();
+          epilogue_bar<32 * C::EPI_WARPS>();
+          if (warp == 2 && lane == 0) {
+            const int orow = (p.mode == kMGrouped ? 0 : ti.e * p.M) + ti.mt * 128;
+            tma_store_2d(&tmC, smStage, ti.nt * BN + sl * 64, orow);
+            bulk_commit();
+          }
         }
         if (++acc == C::ACC_STAGES) {
           acc = 0;
