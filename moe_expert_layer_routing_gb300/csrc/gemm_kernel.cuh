@@ -40,7 +40,7 @@ struct GemmCfg {
   // (gate and up, 32 features x 128 tile rows each) filled by TMA one chunk ahead.
   // dSwiGLU: 8 epilogue warps (two per TMEM lane quarter, each taking 16 of every 32 columns)
   static constexpr int EPI_WARP_BYTES = (EPI == kEpiDSwiGLU) ? 3 * 16 * 33 * 4 : 0;  // fp32 transposes
-  static constexpr int XCHG_BYTES = (EPI == kEpiDSwiGLU) ? 4 * 2 * 2 * 32 * 4 : 0;   // pair amax exchange
+  static constexpr int XCHG_BYTES = (EPI == kEpiDSwiGLU) ? 2 * 4 * 2 * 2 * 32 * 4 : 0;  // pair amax exchange, x2 by chunk parity
   static constexpr int CK_CHUNK_BYTES = 2 * 32 * 128 * 2;
   static constexpr int CK_BYTES = (EPI == kEpiDSwiGLU) ? 2 * CK_CHUNK_BYTES : 0;
   // Store epilogue with a single TMEM accumulator: the tile is drained into a 128B-swizzled bf16
@@ -313,7 +313,8 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* ck_full = tempty + 2;
-  uint64_t* done = ck_full + 2;
+  uint64_t* ck_empty = ck_full + 2;  // every epilogue warp has consumed the checkpoint buffer
+  uint64_t* done = ck_empty + 2;
   uint64_t* tile_full = done + 1;          // ring slot r holds a tile index (producer arrives)
   uint64_t* tile_empty = tile_full + C::RING;  // every consumer warp has read slot r
   volatile int* tile_ring = reinterpret_cast<volatile int*>(tile_empty + C::RING);
@@ -332,6 +333,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], C::EPI_WARPS);
       mbar_init(&ck_full[a], 1);
+      mbar_init(&ck_empty[a], C::EPI_WARPS);
     }
     mbar_init(done, 1);
     for (int r = 0; r < C::RING; ++r) {
@@ -486,7 +488,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
     const int m = 32 * q + lane;
     const int half = (warp - 2) >> 2;  // dSwiGLU: which 16 of every 32 columns; TMA store: which half
     uint8_t* wsm = smEPI + (warp - 2) * C::EPI_WARP_BYTES;
-    float* xchg = smXchg + q * (2 * 2 * 32);
+    float* xchg = smXchg + q * (2 * 2 * 32);  // + (chunk parity) * 4 * 2 * 2 * 32
     const bool ck_leader = (EPI == kEpiDSwiGLU) && warp == 2 && lane == 0;
     // checkpoint chunk n of the schedule goes to buffer n % 2; ck_issued = chunks issued so far
     int64_t ck_next = 0, ck_issued = 0;
@@ -498,6 +500,10 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       const int buf = (int)(ck_issued & 1);
       uint8_t* dst = smCK + buf * C::CK_CHUNK_BYTES;
       const int i0 = tn.nt * BN + c * 32;
+      // the buffer's previous chunk (two back) must have been consumed by every epilogue warp
+      if (ck_issued >= 2 &&
+          !mbar_wait_bounded(&ck_empty[buf], (uint32_t)(((ck_issued - 2) >> 1) & 1), p.status, abort_flag))
+        return;
       mbar_arrive_expect_tx(&ck_full[buf], C::CK_CHUNK_BYTES);
       tma_load_2d(dst, &tmC, &ck_full[buf], b0, (int)((blk * 2 + 0) * p.I + i0));
       tma_load_2d(dst + C::CK_CHUNK_BYTES / 2, &tmC, &ck_full[buf], b0, (int)((blk * 2 + 1) * p.I + i0));
@@ -609,15 +615,12 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
           mbar_wait_bounded(&ck_full[buf], (uint32_t)((ck_next >> 1) & 1), p.status, abort_flag);
           epi_dswiglu_half<MX>(p, taddr + c * 32 + half * 16, prow, m, lane, valid, sv, ti.nt * BN + c * 32, half,
                                reinterpret_cast<const uint16_t*>(smCK + buf * C::CK_CHUNK_BYTES),
-                               reinterpret_cast<float*>(wsm), xchg, 2 + q, ds_acc);
+                               reinterpret_cast<float*>(wsm), xchg + (int)(ck_next & 1) * (4 * 2 * 2 * 32), 2 + q,
+                               ds_acc);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ck_empty[buf]);  // this warp no longer reads the buffer
           ++ck_next;
-          epilogue_bar<32 * C::EPI_WARPS>();  // every epilogue thread is done with this buffer before it is refilled
-          if (*abort_flag) {
-            ok = false;
-            break;
-          }
         }
-        if (!ok) break;
         p.ds_part[prow * (int64_t)(2 * (p.I / BN)) + 2 * ti.nt + half] = valid ? ds_acc : 0.f;
       }
       tc_fence_before();

@@ -13,7 +13,7 @@ list, and the dense matmul backward page, "Forward pass convention"):
   finegrained_bf16   T=16384 H=2048 I=1024 E=64  K=8  B=128  BF16  affinity on H, biases
   manyexpert_mxfp8   T=32768 H=2048 I=768  E=128 K=8  B=256  MXFP8 affinity on I
   imbalanced_mxfp8   T=65536 H=4096 I=1536 E=128 K=8  B=512  MXFP8 affinity on I, Zipf routing
-plus two reduced shapes (profile_*_small) used only to size ncu captures.
+plus reduced shapes (profile_*) used only to size ncu captures.
 """
 from __future__ import annotations
 
@@ -85,6 +85,9 @@ CONFIGS = {
     "profile_mxfp8_small": MoeConfig("profile_mxfp8_small", T=8192, H=2048, I=768, E=32, K=8,
                                      block_size=256, precision=PREC_MXFP8, affinity=AFFINITY_ON_I,
                                      seed=1005),
+    "profile_mxfp8_medium": MoeConfig("profile_mxfp8_medium", T=16384, H=4096, I=768, E=32, K=8,
+                                      block_size=256, precision=PREC_MXFP8, affinity=AFFINITY_ON_I,
+                                      seed=1007),
     "profile_bf16_small": MoeConfig("profile_bf16_small", T=8192, H=2048, I=1024, E=32, K=8,
                                     block_size=128, bias=True, seed=1006),
 }
