@@ -26,6 +26,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "imbalanced_mxfp8"
+METRIC_MOE = "MoE-backward TFLOP/s (BF16, MXFP8) & % of tensor peak; tokens/s"
+METRIC_LINEAR = "dense MXFP8 linear-backward TFLOP/s & % of tensor peak"
 FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
 FP8_OVER_BF16 = 2.0   # nominal dense ratio 4.5 / 2.25 PFLOP/s
 
@@ -130,6 +132,15 @@ def recorded_traffic(workload: str, stage: str):
     return None
 
 
+def workload_config(cfg, is_linear, world):
+    if is_linear:
+        return dict(workload=cfg.name, M=cfg.M, N=cfg.N, K=cfg.K, precision="mxfp8 e5m2",
+                    parallelism=f"replicas x{world}")
+    return dict(workload=cfg.name, T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, top_k=cfg.K, block_size=cfg.block_size,
+                precision="mxfp8 (e4m3 weights, e5m2 activations, E8M0 scales)" if cfg.precision == 1 else "bf16",
+                affinity="on_I" if cfg.affinity == 1 else "on_H", bias=cfg.bias, parallelism=f"replicas x{world}")
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -207,11 +218,13 @@ def barrier(world):
 
 
 def allreduce_max(v: float, world: int) -> float:
+    """Max over ranks (the slowest rank's time defines a step)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -220,23 +233,20 @@ def allreduce_max(v: float, world: int) -> float:
 # CPU oracle sample (the baseline, never the product path)
 # ---------------------------------------------------------------------------------------------
 def oracle_sample_moe(inp, target_rows: int):
-    """Pick the lightest non-empty experts until target_rows rows; return a timing closure."""
+    """The non-empty expert whose load is closest to target_rows, with all its tokens (the oracle's
+    cost is dominated per expert by its weight quantisation and per row by the four contractions)."""
     import numpy as np
     from oracle import moe as om
     from oracle import sample as osm
     cfg = inp.cfg
     ids = inp.ids.cpu().numpy()
-    counts = np.bincount(ids.reshape(-1), minlength=cfg.E)
-    order = [e for e in np.argsort(counts, kind="stable") if counts[e] > 0]
-    chosen, rows = [], 0
-    for e in order:
-        chosen.append(int(e))
-        rows += int(counts[e])
-        if rows >= target_rows:
-            break
+    counts = np.bincount(ids.reshape(-1)[(ids.reshape(-1) >= 0) & (ids.reshape(-1) < cfg.E)], minlength=cfg.E)
+    nz = np.nonzero(counts)[0]
+    e = int(nz[np.argmin(np.abs(counts[nz] - target_rows))])
+    rows = int(counts[e])
     cpu = lambda t: None if t is None else t.cpu()  # noqa: E731
     sub = osm.subproblem(cpu(inp.x), cpu(inp.dout), cpu(inp.W1), cpu(inp.W2), inp.s.cpu().numpy(), ids,
-                         cpu(inp.ckpt), cfg.block_size, experts=chosen, b2=cpu(inp.b2))
+                         cpu(inp.ckpt), cfg.block_size, experts=[e], b2=cpu(inp.b2))
 
     def run():
         if cfg.precision == 1:
@@ -247,7 +257,7 @@ def oracle_sample_moe(inp, target_rows: int):
                             b2=sub["b2"], with_bias=cfg.bias)
 
     flops = 12.0 * rows * cfg.H * cfg.I
-    desc = f"{len(chosen)} lightest non-empty experts, {rows} routed rows (all their tokens), all outputs"
+    desc = f"expert {e} with {rows} routed rows (all its tokens), all of its outputs"
     return run, flops, desc
 
 
@@ -308,7 +318,7 @@ def main():
         if rank != 0:
             return
         inp = make_linear_inputs(cfg) if is_linear else make_moe_inputs(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
-        run, flops, desc = oracle_sample_linear(inp, 128) if is_linear else oracle_sample_moe(inp, 256)
+        run, flops, desc = oracle_sample_linear(inp, 128) if is_linear else oracle_sample_moe(inp, 128)
         for _ in range(args.warmup):
             run()
         t0 = time.perf_counter()
@@ -316,10 +326,10 @@ def main():
             run()
         dt = (time.perf_counter() - t0) / args.steps
         value = flops / dt / 1e12
-        line = dict(metric=f"{'dense linear' if is_linear else 'MoE'}-backward useful TFLOP/s", value=value,
-                    unit="TFLOP/s", n_gpus=0, steps=args.steps, warmup=args.warmup, ms_per_step=dt * 1e3,
+        line = dict(metric=METRIC_LINEAR if is_linear else METRIC_MOE, value=value,
+                    unit="TFLOP/s", n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=dt * 1e3,
                     higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
-                    impl="reference", config=dict(workload=cfg.name),
+                    impl="reference", config=workload_config(cfg, is_linear, 1),
                     cpu_baseline=dict(value=value, unit="TFLOP/s", cores=cores, kind="oracle", sample=desc),
                     e2e=dict(value=value, unit="TFLOP/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
         print(json.dumps(line), flush=True)
@@ -413,6 +423,28 @@ def main():
                         peak=peak_tf, unit="TFLOP/s", frac=achieved / peak_tf, traffic=None,
                         peak_source=f"{peak_src} bf16 burst x2 (nominal fp8/bf16)")
 
+    # ---------------------------------------------------------------- router backward (consumes ds)
+    next_rows = None
+    if not is_linear:
+        logits = inp.extra["logits"]
+        dl = mb.router_bwd(mb.ROUTER_TOPK_OVER_SOFTMAX, inp.ids, op.ds, cfg.E, logits=logits, scores=inp.s, renorm=True)
+        for _ in range(3):
+            mb.router_bwd(mb.ROUTER_TOPK_OVER_SOFTMAX, inp.ids, op.ds, cfg.E, logits=logits, scores=inp.s, renorm=True)
+        r0 = torch.cuda.Event(enable_timing=True)
+        r1 = torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        for _ in range(args.steps):
+            mb.router_bwd(mb.ROUTER_TOPK_OVER_SOFTMAX, inp.ids, op.ds, cfg.E, logits=logits, scores=inp.s, renorm=True)
+        r1.record(stream)
+        torch.cuda.synchronize()
+        rms = r0.elapsed_time(r1) / args.steps
+        rbytes = cfg.T * cfg.E * 4 * 2 + cfg.T * cfg.K * 4 * 3   # logits in, dlogits out; ds, scores, ids in
+        gbs = rbytes / (rms * 1e-3) / 1e9
+        next_rows = dict(router_bwd=dict(form="top-K over softmax, renormalised", ms=rms, bound="hbm",
+                                         algorithmic_bytes=rbytes, achieved_gbs=gbs, peak_gbs=peaks["hbm_gbs"],
+                                         frac=gbs / peaks["hbm_gbs"]))
+        del dl
+
     lib_peak = recorded_mxfp8_peak()
     if prec == 1 and lib_peak:
         roofline["frac_of_mxfp8_library"] = roofline["achieved"] / lib_peak[0]
@@ -497,28 +529,21 @@ def main():
         if is_linear:
             run, cflops, desc = oracle_sample_linear(inp, 512)
         else:
-            run, cflops, desc = oracle_sample_moe(inp, 1024 if cfg.H * cfg.I < 4e6 else 512)
+            run, cflops, desc = oracle_sample_moe(inp, 512)
         cval, n = time_oracle(run, cflops, 15.0)
         cpu_baseline = dict(value=cval, unit="TFLOP/s", cores=cores, kind="oracle", sample=desc + f"; {n} run(s)")
 
-    l2_note = f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB resident inputs > 0.13 GB L2)"
-    if is_linear:
-        conf = dict(workload=cfg.name, M=cfg.M, N=cfg.N, K=cfg.K, precision="mxfp8 e5m2", l2=l2_note,
-                    parallelism=f"replicas x{world}")
-    else:
-        conf = dict(workload=cfg.name, T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, top_k=cfg.K, block_size=cfg.block_size,
-                    precision="mxfp8 (e4m3 weights, e5m2 activations, E8M0 scales)" if prec == 1 else "bf16",
-                    affinity="on_I" if cfg.affinity == 1 else "on_H", bias=cfg.bias, l2=l2_note,
-                    parallelism=f"replicas x{world}")
+    conf = workload_config(cfg, is_linear, world)
+    conf["l2"] = f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB resident inputs > 0.13 GB L2)"
     line = dict(
-        metric="MoE-backward TFLOP/s (BF16, MXFP8) & % of tensor peak; tokens/s" if not is_linear
-        else "dense MXFP8 linear-backward TFLOP/s & % of tensor peak",
+        metric=METRIC_LINEAR if is_linear else METRIC_MOE,
         value=value, unit="TFLOP/s", n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=ms,
         higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="mxfp8" if prec == 1 else "bf16", data="synthetic (seeded; shapes and routing of the workload)",
         config=conf, tokens_per_s=tokens * world / (ms * 1e-3), pct_of_tensor_peak=100.0 * value / world / peak_tf,
         pct_of_mxfp8_library_peak=(100.0 * value / world / lib_peak[0]) if (prec == 1 and lib_peak) else None,
         roofline=roofline, cpu_baseline=cpu_baseline, e2e=e2e, clocks=clk.summary(), gpu_launches=launches,
+        next_rows=next_rows,
         stage_ms=stages, source_sha=source_sha())
     print(json.dumps(line), flush=True)
     barrier(world)
