@@ -22,57 +22,69 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(int mode, int renorm, c
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  const int32_t* idt = ids + (int64_t)t * K;
-  const float* gt = g + (int64_t)t * K;
+  // the K selected slots of this token: lane k (and k - 32) holds slot k's id, gradient and score
+  int id0 = -1, id1 = -1;
+  float g0 = 0.f, g1 = 0.f, s0 = 0.f, s1 = 0.f;
+  if (lane < K) {
+    id0 = ids[(int64_t)t * K + lane];
+    g0 = g[(int64_t)t * K + lane];
+    if (scores) s0 = scores[(int64_t)t * K + lane];
+  }
+  if (lane + 32 < K) {
+    id1 = ids[(int64_t)t * K + lane + 32];
+    g1 = g[(int64_t)t * K + lane + 32];
+    if (scores) s1 = scores[(int64_t)t * K + lane + 32];
+  }
+  if (id0 >= E) id0 = -1;
+  if (id1 >= E) id1 = -1;
+  const float* lt = logits ? logits + (int64_t)t * E : nullptr;
   float* out = dl + (int64_t)t * E;
-  if (mode == MOE_ROUTER_TOPK || mode == MOE_ROUTER_SOFTMAX_OVER_TOPK) {
-    float dot = 0.f;
-    if (mode == MOE_ROUTER_SOFTMAX_OVER_TOPK)
-      for (int k = 0; k < K; ++k) {
-        const int e = idt[k];
-        if (e >= 0 && e < E) dot = fmaf(gt[k], scores[(int64_t)t * K + k], dot);
-      }
-    for (int e = lane; e < E; e += 32) {
-      float v = 0.f;
-      for (int k = 0; k < K; ++k)
-        if (idt[k] == e)
-          v += mode == MOE_ROUTER_TOPK ? gt[k] : scores[(int64_t)t * K + k] * (gt[k] - dot);
-      out[e] = v;
+  // per-slot weight w_k scattered to logit id_k, and the shift applied (top-K over softmax) below
+  float mx = 0.f, inv = 1.f, dot = 0.f;
+  float w0 = 0.f, w1 = 0.f;
+  if (mode == MOE_ROUTER_TOPK) {
+    w0 = g0;
+    w1 = g1;
+  } else if (mode == MOE_ROUTER_SOFTMAX_OVER_TOPK) {
+    float d = (id0 >= 0 ? g0 * s0 : 0.f) + (id1 >= 0 ? g1 * s1 : 0.f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+    w0 = s0 * (g0 - d);
+    w1 = s1 * (g1 - d);
+  } else {
+    mx = -INFINITY;
+    for (int e = lane; e < E; e += 32) mx = fmaxf(mx, lt[e]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float sum = 0.f;
+    for (int e = lane; e < E; e += 32) sum += __expf(lt[e] - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    inv = 1.f / sum;
+    const float p0 = id0 >= 0 ? __expf(lt[id0] - mx) * inv : 0.f;
+    const float p1 = id1 >= 0 ? __expf(lt[id1] - mx) * inv : 0.f;
+    float S = p0 + p1, ds = (id0 >= 0 ? g0 * s0 : 0.f) + (id1 >= 0 ? g1 * s1 : 0.f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      S += __shfl_xor_sync(0xffffffffu, S, o);
+      ds += __shfl_xor_sync(0xffffffffu, ds, o);
     }
-    return;
-  }
-  // top-K over softmax: recompute p over all E logits
-  const float* lt = logits + (int64_t)t * E;
-  float mx = -INFINITY;
-  for (int e = lane; e < E; e += 32) mx = fmaxf(mx, lt[e]);
+    w0 = renorm ? (g0 - ds) / S : g0;  // dr of each selected slot
+    w1 = renorm ? (g1 - ds) / S : g1;
+    float d = (id0 >= 0 ? w0 * p0 : 0.f) + (id1 >= 0 ? w1 * p1 : 0.f);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float sum = 0.f;
-  for (int e = lane; e < E; e += 32) sum += __expf(lt[e] - mx);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  const float inv = 1.f / sum;
-  // selected probabilities, optional renormalisation, <dr, r>
-  float S = 0.f, dot_s = 0.f;
-  for (int k = 0; k < K; ++k) {
-    const int e = idt[k];
-    if (e < 0 || e >= E) continue;
-    S += __expf(lt[e] - mx) * inv;
-    if (renorm) dot_s = fmaf(gt[k], scores[(int64_t)t * K + k], dot_s);
+    for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+    dot = d;
   }
-  const float rS = renorm ? 1.f / S : 1.f;
-  float dot = 0.f;
-  for (int k = 0; k < K; ++k) {
-    const int e = idt[k];
-    if (e < 0 || e >= E) continue;
-    const float dr = renorm ? (gt[k] - dot_s) * rS : gt[k];
-    dot = fmaf(dr, __expf(lt[e] - mx) * inv, dot);
-  }
-  for (int e = lane; e < E; e += 32) {
+  for (int e0 = 0; e0 < E; e0 += 32) {
+    const int e = e0 + lane;
     float dp = 0.f;
-    for (int k = 0; k < K; ++k)
-      if (idt[k] == e) dp += renorm ? (gt[k] - dot_s) * rS : gt[k];
-    out[e] = __expf(lt[e] - mx) * inv * (dp - dot);
+    for (int k = 0; k < K; ++k) {  // broadcast slot k; uniform loop, every lane takes part
+      const int idk = __shfl_sync(0xffffffffu, k < 32 ? id0 : id1, k & 31);
+      const float wk = __shfl_sync(0xffffffffu, k < 32 ? w0 : w1, k & 31);
+      if (idk == e) dp += wk;
+    }
+    if (e < E) out[e] = mode == MOE_ROUTER_TOPK_OVER_SOFTMAX ? __expf(lt[e] - mx) * inv * (dp - dot) : dp;
   }
 }
 
