@@ -197,6 +197,9 @@ typedef struct MoeBwdArgs {
   int32_t* status_dev;    /* (device) int32 [1]; reset to 0 by the call, then OR-ed with MOE_STATUS_* */
   void* workspace;        /* (device) scratch, 256-byte aligned */
   size_t workspace_bytes; /* >= moe_bwd_workspace_size(args) */
+  int accumulate;         /* [BW] accumulation / grad-init: 0 overwrites dW1, dW2, db1, db2; 1 adds this
+                             pass's gradients to their current contents (bf16 adds for dW, fp32 for db).
+                             dx and ds are always overwritten. */
 } MoeBwdArgs;
 
 /* Bytes of workspace moe_bwd needs for these shapes and options (pointers are not read). */

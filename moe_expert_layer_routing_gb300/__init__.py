@@ -45,7 +45,7 @@ class MoeBwdArgs(ctypes.Structure):
                [(n, ctypes.c_void_p) for n in
                 ("x", "dout", "W1", "W2", "W1_q", "W1_sf", "W2_q", "W2_sf", "b2", "s", "ids",
                  "gate_up_ckpt", "dx", "dW1", "dW2", "ds", "db1", "db2", "status_dev", "workspace")] + \
-               [("workspace_bytes", ctypes.c_size_t)]
+               [("workspace_bytes", ctypes.c_size_t), ("accumulate", ctypes.c_int)]
 
 
 _lib = None
@@ -205,8 +205,9 @@ class MoeBwd:
     run() enqueues moe_bwd on the stream (no host synchronisation)."""
 
     def __init__(self, *, T, H, I, E, K, block_size, precision=PREC_BF16, affinity=AFFINITY_ON_H,
-                 fp8_act=FP8_E5M2, fp8_w=FP8_E4M3, has_bias=False, device="cuda"):
+                 fp8_act=FP8_E5M2, fp8_w=FP8_E4M3, has_bias=False, accumulate=False, device="cuda"):
         self.a = MoeBwdArgs()
+        self.a.accumulate = int(bool(accumulate))
         for k, v in dict(T=T, H=H, I=I, E=E, K=K, block_size=block_size, precision=precision,
                          affinity=affinity, fp8_act=fp8_act, fp8_w=fp8_w, has_bias=int(bool(has_bias))).items():
             setattr(self.a, k, int(v))

@@ -147,6 +147,19 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const TileInfo& t
       for (int j = 0; j < 32; ++j) r[j] = 0u;
     }
     uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+    if (p.accumulate) {  // read-add-write of the bf16 output
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 o = d4[q];
+        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          r[8 * q + 2 * j] = __float_as_uint(__uint_as_float(r[8 * q + 2 * j]) + __uint_as_float(ow[j] << 16));
+          r[8 * q + 2 * j + 1] =
+              __float_as_uint(__uint_as_float(r[8 * q + 2 * j + 1]) + __uint_as_float(ow[j] & 0xFFFF0000u));
+        }
+      }
+    }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       uint4 w;
@@ -579,7 +592,10 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
           epilogue_bar<32 * C::EPI_WARPS>();
           if (warp == 2 && lane == 0) {
             const int orow = (p.mode == kMGrouped ? 0 : ti.e * p.M) + ti.mt * 128;
-            tma_store_2d(&tmC, smStage, ti.nt * BN + sl * 64, orow);
+            if (p.accumulate)
+              tma_reduce_add_2d(&tmC, smStage, ti.nt * BN + sl * 64, orow);
+            else
+              tma_store_2d(&tmC, smStage, ti.nt * BN + sl * 64, orow);
             bulk_commit();
           }
         }

@@ -146,6 +146,7 @@ static int check_args(const MoeBwdArgs* a, bool need_ptrs) {
   if (a->block_size != 128 && a->block_size != 256 && a->block_size != 512 && a->block_size != 1024)
     return fail(MOE_ERR_UNSUPPORTED, "moe_bwd: block_size must be 128, 256, 512 or 1024");
   if ((int64_t)a->T * a->K >= (int64_t)1 << 31) return fail(MOE_ERR_UNSUPPORTED, "moe_bwd: T*K too large");
+  if (a->accumulate != 0 && a->accumulate != 1) return fail(MOE_ERR_INVALID, "moe_bwd: accumulate must be 0 or 1");
   if (a->precision != MOE_PREC_BF16 && a->precision != MOE_PREC_MXFP8)
     return fail(MOE_ERR_INVALID, "moe_bwd: bad precision");
   if (a->affinity != MOE_AFFINITY_ON_H && a->affinity != MOE_AFFINITY_ON_I)
@@ -296,6 +297,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   const bool mx = a.precision == MOE_PREC_MXFP8;
   const int64_t H = a.H, I = a.I, E = a.E, P = L.P, TK = L.TK;
   if ((rc = cuda_check(cudaMemsetAsync(a.status_dev, 0, sizeof(int32_t), st), "memset status"))) return rc;
+  if (TK == 0 && a.accumulate) return MOE_OK;  // nothing to add
   if (TK == 0) {  // no routed rows: every gradient is zero
     if ((rc = cuda_check(cudaMemsetAsync(a.dW1, 0, (size_t)(E * H * 2 * I * 2), st), "memset dW1"))) return rc;
     if ((rc = cuda_check(cudaMemsetAsync(a.dW2, 0, (size_t)(E * I * H * 2), st), "memset dW2"))) return rc;
@@ -419,6 +421,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.fmt_a = a.fp8_act; p.fmt_b = a.fp8_act;
     p.epi = kEpiStore;
     p.out = a.dW2; p.ldo = H; p.out_expert_stride = I * H;
+    p.accumulate = a.accumulate;
     p.tile_counter = counters + 1;
     p.status = a.status_dev;
     if ((rc = launch_gemm(mx, L.BN3, p, reg<void>(L, ws, R_AP_T), I, P, reg<void>(L, ws, R_DOUT_GT), H, P, st)))
@@ -463,6 +466,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.fmt_a = a.fp8_act; p.fmt_b = a.fp8_act;
     p.epi = kEpiStore;
     p.out = a.dW1; p.ldo = 2 * I; p.out_expert_stride = H * 2 * I;
+    p.accumulate = a.accumulate;
     p.tile_counter = counters + 3;
     p.status = a.status_dev;
     if ((rc = launch_gemm(mx, L.BN4, p, reg<void>(L, ws, R_X_GT), H, P, reg<void>(L, ws, R_DH_T), 2 * I, P, st)))
@@ -478,10 +482,11 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     return rc;
   if (a.has_bias) {
     if ((rc = launch_segment_rowsum(reg<uint16_t>(L, ws, R_DH_T), P, (int)(2 * I), tile_offsets, (int)E, nullptr,
-                                    tile_row_flat, a.db1, st)))
+                                    tile_row_flat, a.db1, st, a.accumulate)))
       return rc;
     if ((rc = launch_segment_rowsum(reg<uint16_t>(L, ws, R_DOUT_GT), P, (int)H, tile_offsets, (int)E,
-                                    a.affinity == MOE_AFFINITY_ON_I ? a.s : nullptr, tile_row_flat, a.db2, st)))
+                                    a.affinity == MOE_AFFINITY_ON_I ? a.s : nullptr, tile_row_flat, a.db2, st,
+                                    a.accumulate)))
       return rc;
   }
   prof_mark(st, slot, 7);

@@ -124,6 +124,7 @@ struct GemmParams {
   void* apt; uint8_t* apt_sf;
   float* ds_part;               // [P, 2*I/BN]
   int32_t* tile_counter;        // zeroed before the launch: dynamic tile claims
+  int accumulate;               // store epilogue: add the tile to the output instead of overwriting
   int32_t* status;
 };
 
@@ -146,6 +147,7 @@ int launch_ds_finalize(const float* ds_part, int nparts, const float* ds_bias, c
                        int64_t TK, float* ds, cudaStream_t st);
 // out[e, j] = sum over tile rows p of expert e of buf[j, p] (* w[flat(p)] when w != null)
 int launch_segment_rowsum(const uint16_t* buf, int64_t ld, int R, const int32_t* tile_offsets, int E,
-                          const float* w, const int32_t* tile_row_flat, float* out, cudaStream_t st);
+                          const float* w, const int32_t* tile_row_flat, float* out, cudaStream_t st,
+                          int accumulate = 0);
 
 }  // namespace moebwd

@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(256) segment_rowsum_kernel(const uint16_t* __r
                                                              const int32_t* __restrict__ tile_offsets,
                                                              const float* __restrict__ w,
                                                              const int32_t* __restrict__ tile_row_flat,
-                                                             float* __restrict__ out) {
+                                                             float* __restrict__ out, int accumulate) {
   const int e = blockIdx.y;
   const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -97,14 +97,14 @@ __global__ void __launch_bounds__(256) segment_rowsum_kernel(const uint16_t* __r
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) out[(int64_t)e * R + j] = acc;
+  if (lane == 0) out[(int64_t)e * R + j] = accumulate ? out[(int64_t)e * R + j] + acc : acc;
 }
 
 int launch_segment_rowsum(const uint16_t* buf, int64_t ld, int R, const int32_t* tile_offsets, int E, const float* w,
-                          const int32_t* tile_row_flat, float* out, cudaStream_t st) {
+                          const int32_t* tile_row_flat, float* out, cudaStream_t st, int accumulate) {
   if (R == 0 || E == 0) return MOE_OK;
   dim3 grid((unsigned)((R + 7) / 8), (unsigned)E);
-  segment_rowsum_kernel<<<grid, 256, 0, st>>>(buf, ld, R, tile_offsets, w, tile_row_flat, out);
+  segment_rowsum_kernel<<<grid, 256, 0, st>>>(buf, ld, R, tile_offsets, w, tile_row_flat, out, accumulate);
   count_launch();
   return cuda_check(cudaGetLastError(), "segment_rowsum");
 }

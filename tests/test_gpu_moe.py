@@ -168,3 +168,47 @@ def test_linear_bwd_dense_4096_config():
     ref = olin.linear_backward_mxfp8(inp.dY.cpu(), inp.W.cpu(), inp.X.cpu())
     assert rel_fro(np64(got["dX"]), ref["dX"]) < MXFP8_TOL
     assert rel_fro(np64(got["dW"]), ref["dW"]) < MXFP8_TOL
+
+
+@pytest.mark.parametrize("mx", [False, True])
+def test_accumulate_adds_weight_and_bias_gradients(mx):
+    """accumulate=1: dW1, dW2 (and db1, db2) are added to their previous contents, here twice in a
+    row onto a random start; dx and ds are overwritten.  Tolerance: the path's bar plus the bf16
+    rounding of the accumulated sums (measured against the size of the added gradients)."""
+    import moe_expert_layer_routing_gb300 as mb
+    from helpers import to_device
+    if mx:
+        cfg = small_moe("acc_mx", T=300, H=256, I=256, E=4, K=2, B=256, seed=41, precision=PREC_MXFP8,
+                        affinity=AFFINITY_ON_I)
+    else:
+        cfg = small_moe("acc_bf16", T=300, H=256, I=384, E=6, K=2, B=128, seed=42, bias=True)
+    inp = make_moe_inputs(cfg)
+    ref = oracle_bwd(inp)
+    d = to_device(inp)
+    op = mb.MoeBwd(T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K, block_size=cfg.block_size, precision=cfg.precision,
+                   affinity=cfg.affinity, has_bias=cfg.bias, accumulate=True)
+    kw = dict(x=d.x, dout=d.dout, s=d.s, ids=d.ids, ckpt=d.ckpt, b2=d.b2 if cfg.bias else None)
+    if mx:
+        W1_q, W1_sf = mb.quantize_weights(d.W1, cfg.fp8_w)
+        W2_q, W2_sf = mb.quantize_weights(d.W2, cfg.fp8_w)
+        kw.update(W1_q=W1_q, W1_sf=W1_sf, W2_q=W2_q, W2_sf=W2_sf)
+    else:
+        kw.update(W1=d.W1, W2=d.W2)
+    op.bind(**kw)
+    g = torch.Generator().manual_seed(5)
+    names = ["dW1", "dW2"] + (["db1", "db2"] if cfg.bias else [])
+    init = {}
+    for n in names:
+        t = getattr(op, n)
+        scale = float(np.std(ref[n])) if np.std(ref[n]) > 0 else 1.0
+        init[n] = (torch.randn(t.shape, generator=g) * scale).to(t.dtype)
+        t.copy_(init[n].cuda())
+    op.run()
+    op.run()
+    torch.cuda.synchronize()
+    assert int(op.status.item()) == 0
+    tol = (MXFP8_TOL if mx else BF16_TOL) + 4e-3
+    for n in names:
+        got = np64(getattr(op, n)) - init[n].double().numpy()
+        assert rel_fro(got, 2 * ref[n]) < tol, n
+    assert rel_fro(np64(op.dx), ref["dx"]) < (MXFP8_TOL if mx else BF16_TOL)
