@@ -84,6 +84,29 @@ def moe_forward(x, W1, b1, W2, b2, s, ids):
     return out, h
 
 
+def recompute_h(x, W1, ids, b1=None, mxfp8=False, fp8_act=mx.E5M2, fp8_w=mx.E4M3):
+    """Gate/up pre-activations recomputed from the layer input, h[t,k] = x_t @ W1_e + b1_e, stored in
+    bfloat16 (the checkpoint's dtype).  With mxfp8 both operands are quantised along H (the
+    contraction of this GEMM) first: x rows with fp8_act, W1_e columns with fp8_w."""
+    x, b1 = _f64(x), _f64(b1)
+    ids = np.asarray(ids)
+    T, H = x.shape
+    E, _, I2 = W1.shape
+    K = ids.shape[1]
+    h = np.zeros((T, K, I2))
+    for e in range(E):
+        t, k = rows_of_expert(ids, e)
+        if t.size == 0:
+            continue
+        W1e = _f64(W1[e])
+        xe = x[t]
+        if mxfp8:
+            xe = mx.mx_roundtrip(xe, fp8_act, 1)
+            W1e = mx.mx_roundtrip(W1e, fp8_w, 0)
+        h[t, k] = _to_bf16(xe @ W1e + (b1[e] if b1 is not None else 0.0))
+    return h
+
+
 def moe_backward(x, dout, W1, W2, s, ids, h, b2=None, with_bias=False):
     """All gradients of the MoE layer in float64 (the BF16 path's reference).
 

@@ -250,3 +250,21 @@ def test_subproblems_reproduce_full_problem(mxfp8):
     g = run(sub["x"], sub["dout"], sub["W1"], sub["W2"], sub["s"], sub["ids"], sub["h"])
     assert np.allclose(g["dx"], full["dx"][sub["tokens"]], rtol=0, atol=1e-12)
     assert np.array_equal(g["ds"], full["ds"][sub["tokens"]])
+
+
+def test_recompute_h_is_the_forward_preactivation():
+    """recompute_h equals the forward's h up to its bfloat16 storage, and with MXFP8 it quantises
+    x along H (row groups) and W1 along H (column groups): power-of-two scaling of one token row
+    scales exactly that row of h."""
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=20, H=64, I=32, E=3, K=2, seed=21)
+    _, h = om.moe_forward(x, W1, b1, W2, b2, s, ids)
+    r = om.recompute_h(x, W1, ids, b1=b1)
+    assert np.max(np.abs(r - h)) <= np.max(np.abs(h)) * 2.0 ** -8
+    rq = om.recompute_h(x, W1, ids, mxfp8=True)
+    x2 = x.copy()
+    x2[3] *= 2.0 ** 5
+    rq2 = om.recompute_h(x2, W1, ids, mxfp8=True)
+    assert np.array_equal(rq2[3], rq[3] * 2.0 ** 5) and np.array_equal(np.delete(rq2, 3, 0), np.delete(rq, 3, 0))
+    r0 = om.recompute_h(x, W1, ids)
+    err = np.linalg.norm(rq - r0) / np.linalg.norm(r0)
+    assert 1e-3 < err < 0.15
