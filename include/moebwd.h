@@ -67,6 +67,14 @@ enum { MOE_FP8_E4M3 = 0, MOE_FP8_E5M2 = 1 };
 enum { MOE_QUANT_ROWWISE = 0, MOE_QUANT_COLWISE = 1 };
 /* Layout of E8M0 scale bytes. */
 enum { MOE_SF_PLAIN = 0, MOE_SF_TILED = 1 };
+/* Source of the gate/up pre-activations h = x W1_e + b1_e that the dSwiGLU step needs.
+ * CHECKPOINT: read from [BW] gate_up_proj_act_checkpoint_T [N,2,I,B] (gate_up_ckpt).
+ * RECOMPUTE:  recomputed inside moe_bwd by a forward grouped GEMM over the gathered rows of
+ *             hidden_states and the gate/up weights (the pre-activation that checkpoint stores;
+ *             its forward is h = x W1_e + b1_e of the routed SwiGLU layer), written to a
+ *             checkpoint of the same layout in the workspace, rounded to bf16 like the stored one.
+ *             Costs 4*T*K*H*I extra FLOPs and saves the caller the [N,2,I,B] tensor. */
+enum { MOE_ACT_CHECKPOINT = 0, MOE_ACT_RECOMPUTE = 1 };
 
 /* Message of the last failed call on this host thread ("" if none). */
 const char* moe_last_error(void);
@@ -200,6 +208,14 @@ typedef struct MoeBwdArgs {
   int accumulate;         /* [BW] accumulation / grad-init: 0 overwrites dW1, dW2, db1, db2; 1 adds this
                              pass's gradients to their current contents (bf16 adds for dW, fp32 for db).
                              dx and ds are always overwritten. */
+  int act_src;            /* MOE_ACT_CHECKPOINT (gate_up_ckpt read) or MOE_ACT_RECOMPUTE (gate_up_ckpt
+                             unused, may be NULL; the fields below are read) */
+  const void* W1t;        /* (device) RECOMPUTE, BF16: bf16 [E,2I,H], W1 with each expert's block
+                             transposed (row j of expert e = column j of W1[e]) */
+  const uint8_t* W1t_q;   /* (device) RECOMPUTE, MXFP8: W1t as [E*2I, H] quantised ROWWISE (groups
+                             along H) with fp8_w */
+  const uint8_t* W1t_sf;  /*          its scales, MOE_SF_TILED for the [E*2I, H] matrix */
+  const void* b1;         /* (device) RECOMPUTE: bf16 [E,2I] gate/up bias added to h, or NULL */
 } MoeBwdArgs;
 
 /* Bytes of workspace moe_bwd needs for these shapes and options (pointers are not read). */
@@ -234,6 +250,11 @@ enum {
   MOE_WS_AP_T,               /* G3 A operand: a'^T [I,P] (s*a for affinity on I, a on H) */
   MOE_WS_AP_T_SF,
   MOE_WS_DX_EXP,             /* G2 output: dx_expanded [P,H] bf16 */
+  MOE_WS_X_G,                /* RECOMPUTE: G0 A operand, gathered x rows [P,H] (bf16 | fp8) */
+  MOE_WS_X_G_SF,
+  MOE_WS_GATE_UP_CKPT,       /* RECOMPUTE: G0 output, bf16 [Nb,2,I,B] in the checkpoint layout
+                                (Nb = moe_num_blocks_bound; only the slots of routed tile rows are
+                                written) */
   MOE_WS_NUM_REGIONS
 };
 /* Offset and size in bytes of one region inside the workspace (0 bytes when unused). */
@@ -269,7 +290,7 @@ int moe_router_bwd(int mode, int renorm, const float* logits, const float* score
 /* Instrumentation                                                                             */
 /* ------------------------------------------------------------------------------------------ */
 
-/* Stages of moe_bwd, in launch order. */
+/* Stages of moe_bwd.  Launch order: ROUTE, PREP, G0 (RECOMPUTE only), G1, G3, G2, G4, REDUCE. */
 enum {
   MOE_STAGE_ROUTE = 0, /* routing metadata */
   MOE_STAGE_PREP,      /* gathered / transposed / quantised activation operands */
@@ -278,6 +299,7 @@ enum {
   MOE_STAGE_G2,        /* dx_expanded = dh W1_e */
   MOE_STAGE_G4,        /* dW1_e = x_g^T dh */
   MOE_STAGE_REDUCE,    /* dx scatter-sum, ds, bias sums */
+  MOE_STAGE_G0,        /* RECOMPUTE only: h = x_g W1_e + b1_e (runs between PREP and G1) */
   MOE_NUM_STAGES
 };
 

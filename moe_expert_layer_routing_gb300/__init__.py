@@ -20,10 +20,11 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoebwd.s
 QUANT_ROWWISE, QUANT_COLWISE = 0, 1
 SF_PLAIN, SF_TILED = 0, 1
 STATUS_BAD_EXPERT_ID, STATUS_TIMEOUT = 1, 2
+ACT_CHECKPOINT, ACT_RECOMPUTE = 0, 1
 
 WS_REGIONS = ["EXPERT_OFFSETS", "TILE_OFFSETS", "BLOCK_OFFSETS", "TILE_ROW_FLAT", "FLAT_TILE_ROW",
               "DOUT_G", "DOUT_G_SF", "DOUT_GT", "DOUT_GT_SF", "X_GT", "X_GT_SF", "DH", "DH_SF",
-              "DH_T", "DH_T_SF", "AP_T", "AP_T_SF", "DX_EXP"]
+              "DH_T", "DH_T_SF", "AP_T", "AP_T_SF", "DX_EXP", "X_G", "X_G_SF", "GATE_UP_CKPT"]
 
 EXPORTED = ["moe_last_error", "moe_version", "moe_num_blocks_bound", "moe_route_meta_workspace_size",
             "moe_route_meta", "mxfp8_quantize", "moe_bwd_workspace_size", "moe_bwd",
@@ -31,7 +32,7 @@ EXPORTED = ["moe_last_error", "moe_version", "moe_num_blocks_bound", "moe_route_
             "linear_bwd", "moe_profile_enable", "moe_profile_read", "moe_kernel_launches",
             "moe_route_meta_noalloc", "moe_router_bwd"]
 
-STAGES = ["route", "prep", "G1_dA_dswiglu", "G3_dW2", "G2_dx_expanded", "G4_dW1", "reduce"]
+STAGES = ["route", "prep", "G1_dA_dswiglu", "G3_dW2", "G2_dx_expanded", "G4_dW1", "reduce", "G0_recompute_h"]
 
 
 class MoeError(RuntimeError):
@@ -45,7 +46,8 @@ class MoeBwdArgs(ctypes.Structure):
                [(n, ctypes.c_void_p) for n in
                 ("x", "dout", "W1", "W2", "W1_q", "W1_sf", "W2_q", "W2_sf", "b2", "s", "ids",
                  "gate_up_ckpt", "dx", "dW1", "dW2", "ds", "db1", "db2", "status_dev", "workspace")] + \
-               [("workspace_bytes", ctypes.c_size_t), ("accumulate", ctypes.c_int)]
+               [("workspace_bytes", ctypes.c_size_t), ("accumulate", ctypes.c_int), ("act_src", ctypes.c_int)] + \
+               [(n, ctypes.c_void_p) for n in ("W1t", "W1t_q", "W1t_sf", "b1")]
 
 
 _lib = None
@@ -194,8 +196,9 @@ def mxfp8_quantize(x: torch.Tensor, axis: int = QUANT_ROWWISE, fmt: int = FP8_E5
 
 
 def quantize_weights(W: torch.Tensor, fmt: int = FP8_E4M3, stream=None):
-    """Pre-quantise expert weights [E, R, C] along C (the contraction of their backward GEMM) as the
-    [E*R, C] matrix with tiled scales, the layout moe_bwd expects for W1_q/W1_sf and W2_q/W2_sf."""
+    """Pre-quantise expert weights [E, R, C] along C (the contraction of their GEMM) as the [E*R, C]
+    matrix with tiled scales, the layout moe_bwd expects for W1_q/W1_sf, W2_q/W2_sf and (given the
+    per-expert transpose of W1) W1t_q/W1t_sf."""
     E, R, C = W.shape
     return mxfp8_quantize(W.reshape(E * R, C), QUANT_ROWWISE, fmt, None, SF_TILED, stream)
 
@@ -205,9 +208,11 @@ class MoeBwd:
     run() enqueues moe_bwd on the stream (no host synchronisation)."""
 
     def __init__(self, *, T, H, I, E, K, block_size, precision=PREC_BF16, affinity=AFFINITY_ON_H,
-                 fp8_act=FP8_E5M2, fp8_w=FP8_E4M3, has_bias=False, accumulate=False, device="cuda"):
+                 fp8_act=FP8_E5M2, fp8_w=FP8_E4M3, has_bias=False, accumulate=False, act_src=ACT_CHECKPOINT,
+                 device="cuda"):
         self.a = MoeBwdArgs()
         self.a.accumulate = int(bool(accumulate))
+        self.a.act_src = int(act_src)
         for k, v in dict(T=T, H=H, I=I, E=E, K=K, block_size=block_size, precision=precision,
                          affinity=affinity, fp8_act=fp8_act, fp8_w=fp8_w, has_bias=int(bool(has_bias))).items():
             setattr(self.a, k, int(v))
@@ -226,25 +231,34 @@ class MoeBwd:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self._keep = []
 
-    def bind(self, *, x, dout, s, ids, ckpt, W1=None, W2=None, W1_q=None, W1_sf=None, W2_q=None, W2_sf=None,
-             b2=None):
-        _need_cuda(x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2)
+    def bind(self, *, x, dout, s, ids, ckpt=None, W1=None, W2=None, W1_q=None, W1_sf=None, W2_q=None, W2_sf=None,
+             b2=None, W1t=None, W1t_q=None, W1t_sf=None, b1=None):
+        """ckpt: the [N,2,I,B] checkpoint (act_src ACT_CHECKPOINT).  W1t (bf16 [E,2I,H]) or W1t_q/W1t_sf
+        and optionally b1 [E,2I]: the operands of the recomputation (act_src ACT_RECOMPUTE)."""
+        _need_cuda(x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2, W1t, W1t_q, W1t_sf, b1)
         a = self.a
-        assert x.dtype == torch.bfloat16 and dout.dtype == torch.bfloat16 and ckpt.dtype == torch.bfloat16
+        assert x.dtype == torch.bfloat16 and dout.dtype == torch.bfloat16
         assert s.dtype == torch.float32 and ids.dtype == torch.int32
         assert tuple(x.shape) == (a.T, a.H) and tuple(dout.shape) == (a.T, a.H)
         assert tuple(s.shape) == (a.T, a.K) and tuple(ids.shape) == (a.T, a.K)
-        N = num_blocks_bound(a.T, a.K, a.E, a.block_size)
-        assert tuple(ckpt.shape) == (N, 2, a.I, a.block_size), (tuple(ckpt.shape), N)
+        if ckpt is not None:
+            N = num_blocks_bound(a.T, a.K, a.E, a.block_size)
+            assert ckpt.dtype == torch.bfloat16
+            assert tuple(ckpt.shape) == (N, 2, a.I, a.block_size), (tuple(ckpt.shape), N)
+        if W1t is not None:
+            assert W1t.dtype == torch.bfloat16 and tuple(W1t.shape) == (a.E, 2 * a.I, a.H)
+        if b1 is not None:
+            assert b1.dtype == torch.bfloat16 and tuple(b1.shape) == (a.E, 2 * a.I)
         for name, t in dict(x=x, dout=dout, s=s, ids=ids, gate_up_ckpt=ckpt, W1=W1, W2=W2, W1_q=W1_q,
-                            W1_sf=W1_sf, W2_q=W2_q, W2_sf=W2_sf, b2=b2).items():
+                            W1_sf=W1_sf, W2_q=W2_q, W2_sf=W2_sf, b2=b2, W1t=W1t, W1t_q=W1t_q, W1t_sf=W1t_sf,
+                            b1=b1).items():
             setattr(a, name, None if t is None else t.data_ptr())
         for name in ("dx", "dW1", "dW2", "ds", "db1", "db2", "status"):
             t = getattr(self, name)
             setattr(a, "status_dev" if name == "status" else name, None if t is None else t.data_ptr())
         a.workspace = self.workspace.data_ptr()
         a.workspace_bytes = self.workspace.numel()
-        self._keep = [x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2]
+        self._keep = [x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2, W1t, W1t_q, W1t_sf, b1]
         return self
 
     def run(self, stream=None):
@@ -268,17 +282,19 @@ class MoeBwd:
         return tile_rows_capacity(self.a.T, self.a.K, self.a.E)
 
 
-def moe_bwd(*, x, dout, s, ids, ckpt, E, I, block_size, W1=None, W2=None, W1_q=None, W1_sf=None, W2_q=None,
-            W2_sf=None, b2=None, precision=PREC_BF16, affinity=AFFINITY_ON_H, fp8_act=FP8_E5M2, fp8_w=FP8_E4M3,
-            stream=None) -> dict:
+def moe_bwd(*, x, dout, s, ids, E, I, block_size, ckpt=None, W1=None, W2=None, W1_q=None, W1_sf=None, W2_q=None,
+            W2_sf=None, b2=None, W1t=None, W1t_q=None, W1t_sf=None, b1=None, precision=PREC_BF16,
+            affinity=AFFINITY_ON_H, fp8_act=FP8_E5M2, fp8_w=FP8_E4M3, accumulate=False, stream=None) -> dict:
     """One-shot MoE backward (allocates outputs and workspace).  Returns dx, dW1, dW2, ds, db1, db2
-    and the device status word (nonzero: invalid expert ids or a pipeline timeout)."""
+    and the device status word (nonzero: invalid expert ids or a pipeline timeout).  Without ckpt the
+    gate/up pre-activations are recomputed from x and W1t (or W1t_q/W1t_sf) plus b1."""
     T, H = x.shape
     K = ids.shape[1]
     op = MoeBwd(T=T, H=H, I=I, E=E, K=K, block_size=block_size, precision=precision, affinity=affinity,
-                fp8_act=fp8_act, fp8_w=fp8_w, has_bias=b2 is not None, device=x.device)
+                fp8_act=fp8_act, fp8_w=fp8_w, has_bias=b2 is not None, accumulate=accumulate,
+                act_src=ACT_CHECKPOINT if ckpt is not None else ACT_RECOMPUTE, device=x.device)
     op.bind(x=x, dout=dout, s=s, ids=ids, ckpt=ckpt, W1=W1, W2=W2, W1_q=W1_q, W1_sf=W1_sf, W2_q=W2_q,
-            W2_sf=W2_sf, b2=b2).run(stream)
+            W2_sf=W2_sf, b2=b2, W1t=W1t, W1t_q=W1t_q, W1t_sf=W1t_sf, b1=b1).run(stream)
     out = op.outputs()
     out["_op"] = op
     return out

@@ -50,10 +50,14 @@ struct GemmCfg {
 #else
   static constexpr bool TMA_STORE = (EPI == kEpiStore) && ((MX && BN == 256) ? 1 : 2) == 1;
 #endif
+  // Checkpoint epilogue (G0): the tile is written as bf16 into the block checkpoint [N,2,I,B]
+  // through two [32 features][128 rows] staging slabs and TMA stores.
+  static constexpr bool CKPT_STORE = EPI == kEpiCkpt;
+  static constexpr bool STAGED = TMA_STORE || CKPT_STORE;
   // one 64-column staging slab (16 KB) keeps a fourth pipeline stage in shared memory
-  static constexpr int STAGING_BYTES = TMA_STORE ? BM * 64 * 2 : 0;
-  // dSwiGLU and TMA-store epilogues: 8 warps, two per TMEM lane quarter, splitting the columns
-  static constexpr int EPI_WARPS = (EPI == kEpiDSwiGLU || TMA_STORE) ? 8 : 4;
+  static constexpr int STAGING_BYTES = STAGED ? BM * 64 * 2 : 0;
+  // dSwiGLU and staged epilogues: 8 warps, two per TMEM lane quarter, splitting the columns
+  static constexpr int EPI_WARPS = (EPI == kEpiDSwiGLU || STAGED) ? 8 : 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES + XCHG_BYTES + CK_BYTES + STAGING_BYTES;
   static constexpr int BAR_BYTES = 512;
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    if (EPI == kEpiDSwiGLU || C::TMA_STORE) prefetch_tmap(&tmC);
+    if (EPI == kEpiDSwiGLU || C::STAGED) prefetch_tmap(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -537,7 +541,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         rs = 0;
         rph ^= 1u;
       }
-      if constexpr (EPI == kEpiDSwiGLU || C::TMA_STORE) {
+      if constexpr (EPI == kEpiDSwiGLU || C::STAGED) {
         epilogue_bar<32 * C::EPI_WARPS>();  // uniform exit decision (see below)
         if (*abort_flag) break;
       }
@@ -548,7 +552,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         ck0_ready = false;
       }
       const bool got = mbar_wait_bounded(&tfull[acc], aph, p.status, abort_flag);
-      if constexpr (EPI == kEpiDSwiGLU || C::TMA_STORE) {
+      if constexpr (EPI == kEpiDSwiGLU || C::STAGED) {
         // these epilogues synchronise their four warps with a named barrier: take every exit
         // decision after a barrier, from the shared abort flag, so no warp is left waiting
         epilogue_bar<32 * C::EPI_WARPS>();
@@ -558,7 +562,65 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       }
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-      if constexpr (C::TMA_STORE) {
+      if constexpr (C::CKPT_STORE) {
+        // two 32-feature chunks per step, one per warp half: h = acc + b1_e (bf16) staged as
+        // [32 features][128 rows] and stored to the checkpoint rows of the tile's block
+        int64_t blk;
+        int b0;
+        tile_ckpt_origin(p, ti, blk, b0);
+        uint16_t* stg = reinterpret_cast<uint16_t*>(smStage) + half * (32 * 128);
+#pragma unroll 1
+        for (int cp = 0; cp < BN / 64; ++cp) {
+          if (warp == 2 && lane == 0) bulk_wait_read_all();
+          epilogue_bar<32 * C::EPI_WARPS>();
+          const int n0 = ti.nt * BN + (cp * 2 + half) * 32;  // first gate|up feature of the chunk
+          uint32_t r[32];
+          if (ti.nk > 0) {
+            tmem_ld_32x32b_x32(taddr + (cp * 2 + half) * 32, r);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+          }
+          if (cp == BN / 64 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+          if (p.b1) {
+            const uint4* bp = reinterpret_cast<const uint4*>(p.b1 + (int64_t)ti.e * 2 * p.I + n0);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const uint4 bv = __ldg(bp + q4);
+              const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                r[8 * q4 + 2 * j] = __float_as_uint(__uint_as_float(r[8 * q4 + 2 * j]) + __uint_as_float(bw[j] << 16));
+                r[8 * q4 + 2 * j + 1] =
+                    __float_as_uint(__uint_as_float(r[8 * q4 + 2 * j + 1]) + __uint_as_float(bw[j] & 0xFFFF0000u));
+              }
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) stg[j * 128 + m] = float_to_bf16_bits(__uint_as_float(r[j]));
+          fence_proxy_async_smem();
+          epilogue_bar<32 * C::EPI_WARPS>();
+          if (warp == 2 && lane == 0) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int n = ti.nt * BN + (cp * 2 + hh) * 32;
+              const int g = n >= p.I ? 1 : 0;
+              tma_store_2d(&tmC, smStage + hh * (32 * 128 * 2), b0, (int)((blk * 2 + g) * p.I + (n - g * p.I)));
+            }
+            bulk_commit();
+          }
+        }
+        if (++acc == C::ACC_STAGES) {
+          acc = 0;
+          aph ^= 1u;
+        }
+        continue;
+      } else if constexpr (C::TMA_STORE) {
         // one 64-column slab at a time through a single staging slab; TMEM is free after the last
 #pragma unroll 1
         for (int sl = 0; sl < BN / 64; ++sl) {
@@ -647,7 +709,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         aph ^= 1u;
       }
     }
-    if (C::TMA_STORE && warp == 2 && lane == 0) bulk_wait_all();  // stores complete before exit
+    if (C::STAGED && warp == 2 && lane == 0) bulk_wait_all();  // stores complete before exit
     if (ck_leader) {  // drain checkpoint copies still in flight
       for (int64_t n = ck_next; n < ck_issued; ++n) mbar_wait_drain(&ck_full[n & 1], (uint32_t)((n >> 1) & 1), p.status);
     }

@@ -6,6 +6,8 @@ namespace moebwd {
 
 int launch_gemm_mx(int BN, const GemmParams& p, const void* tmA, const void* tmB, const void* tmC, int grid,
                      cudaStream_t st) {
+  if (p.epi == kEpiCkpt)  // G0 (recomputed pre-activations): 2I is a multiple of 256
+    return gemm_launch_instance<true, 256, kEpiCkpt>(p, tmA, tmB, tmC, grid, st);
   if (p.epi == kEpiStore)
     return BN == 256 ? gemm_launch_instance<true, 256, kEpiStore>(p, tmA, tmB, tmC, grid, st)
                      : gemm_launch_instance<true, 128, kEpiStore>(p, tmA, tmB, tmC, grid, st);

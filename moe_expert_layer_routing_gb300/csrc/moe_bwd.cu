@@ -1,7 +1,8 @@
 // Host side of the MoE backward and of the dense linear backward: argument checks, workspace
 // layout, and the launch sequence on one stream (no host synchronisation):
 //
-//   route meta -> prep (gather, transpose, quantise) -> G1 dA + dSwiGLU epilogue ->
+//   route meta -> prep (gather, transpose, quantise) -> [G0 h = x_g W1_e + b1_e, when the
+//   pre-activations are recomputed] -> G1 dA + dSwiGLU epilogue ->
 //   G3 dW2 (K-grouped) -> G2 dx_expanded (M-grouped) -> G4 dW1 (K-grouped) ->
 //   dx scatter-sum, ds finalize, bias column sums
 #include <cuda.h>
@@ -47,7 +48,7 @@ enum Region {
   R_CHUNK_COUNTS, R_EXPERT_OFFSETS, R_BLOCK_OFFSETS, R_TILE_OFFSETS, R_EXPERT_ORDER, R_SCALARS,
   R_X_GATHER, R_S_SCATTER, R_S_REV, R_TPID, R_B2E, R_TILE_ROW_FLAT, R_FLAT_TILE_ROW, R_TILE_EXPERT,
   R_DOUT_G, R_DOUT_G_SF, R_DOUT_GT, R_DOUT_GT_SF, R_X_GT, R_X_GT_SF, R_DH, R_DH_SF, R_DH_T, R_DH_T_SF,
-  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_COUNT
+  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_X_G, R_X_G_SF, R_CKPT, R_COUNT
 };
 
 struct Layout {
@@ -126,6 +127,11 @@ static Layout make_layout(const MoeBwdArgs& a) {
   b[R_DS_PART] = sizeof(float) * (size_t)(P * 2 * (I / L.BN1));  // two column halves per N tile
   b[R_DS_BIAS] = a.has_bias ? sizeof(float) * (size_t)P : 0;
   b[R_COUNTERS] = 64;  // one tile counter per grouped GEMM
+  if (a.act_src == MOE_ACT_RECOMPUTE) {
+    b[R_X_G] = (size_t)(P * H * es);
+    b[R_X_G_SF] = mx ? (size_t)(P * H / 32) : 0;
+    b[R_CKPT] = (size_t)(L.Nb * 2 * I * a.block_size * 2);
+  }
   size_t off = 0;
   for (int r = 0; r < R_COUNT; ++r) {
     L.off[r] = off;
@@ -156,10 +162,20 @@ static int check_args(const MoeBwdArgs* a, bool need_ptrs) {
              (a->fp8_w != MOE_FP8_E4M3 && a->fp8_w != MOE_FP8_E5M2)))
     return fail(MOE_ERR_INVALID, "moe_bwd: bad fp8 format");
   if (mx && a->has_bias) return fail(MOE_ERR_UNSUPPORTED, "moe_bwd: bias gradients are implemented for BF16 only");
+  if (a->act_src != MOE_ACT_CHECKPOINT && a->act_src != MOE_ACT_RECOMPUTE)
+    return fail(MOE_ERR_INVALID, "moe_bwd: bad act_src");
+  const bool rec = a->act_src == MOE_ACT_RECOMPUTE;
   if (!need_ptrs) return MOE_OK;
-  const void* req[] = {a->x, a->dout, a->s, a->ids, a->gate_up_ckpt, a->dx, a->dW1, a->dW2, a->ds, a->status_dev};
+  const void* req[] = {a->x, a->dout, a->s, a->ids, a->dx, a->dW1, a->dW2, a->ds, a->status_dev};
   for (const void* q : req)
     if (!q) return fail(MOE_ERR_INVALID, "moe_bwd: required pointer is null");
+  if (!rec && !a->gate_up_ckpt) return fail(MOE_ERR_INVALID, "moe_bwd: gate_up_ckpt is null");
+  if (rec && (mx ? (!a->W1t_q || !a->W1t_sf) : !a->W1t))
+    return fail(MOE_ERR_INVALID, "moe_bwd: recomputing the pre-activations needs W1t (or W1t_q, W1t_sf)");
+  const void* al16r[] = {a->W1t, a->W1t_q, a->W1t_sf, a->b1};
+  for (const void* q : al16r)
+    if (rec && (reinterpret_cast<uintptr_t>(q) & 15))
+      return fail(MOE_ERR_INVALID, "moe_bwd: W1t and b1 must be 16-byte aligned");
   if (mx ? (!a->W1_q || !a->W1_sf || !a->W2_q || !a->W2_sf) : (!a->W1 || !a->W2))
     return fail(MOE_ERR_INVALID, "moe_bwd: weights are null");
   if (a->has_bias && (!a->b2 || !a->db1 || !a->db2)) return fail(MOE_ERR_INVALID, "moe_bwd: bias pointers are null");
@@ -223,7 +239,8 @@ extern "C" int moe_bwd_workspace_region(const MoeBwdArgs* args, int region, size
                                               R_FLAT_TILE_ROW,  R_DOUT_G,       R_DOUT_G_SF,     R_DOUT_GT,
                                               R_DOUT_GT_SF,     R_X_GT,         R_X_GT_SF,       R_DH,
                                               R_DH_SF,          R_DH_T,         R_DH_T_SF,       R_AP_T,
-                                              R_AP_T_SF,        R_DX_EXP};
+                                              R_AP_T_SF,        R_DX_EXP,         R_X_G,           R_X_G_SF,
+                                              R_CKPT};
   if (region < 0 || region >= MOE_WS_NUM_REGIONS) return fail(MOE_ERR_INVALID, "bad region");
   const Layout L = make_layout(*args);
   *offset = L.off[map[region]];
@@ -363,8 +380,42 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   pa.x_gt = reg<void>(L, ws, R_X_GT);
   pa.x_gt_sf = reg<uint8_t>(L, ws, R_X_GT_SF);
   pa.ds_bias = a.has_bias ? reg<float>(L, ws, R_DS_BIAS) : nullptr;
+  const bool rec = a.act_src == MOE_ACT_RECOMPUTE;
+  pa.x_g = rec ? reg<void>(L, ws, R_X_G) : nullptr;
+  pa.x_g_sf = rec ? reg<uint8_t>(L, ws, R_X_G_SF) : nullptr;
   if ((rc = launch_prep(pa, st))) return rc;
   prof_mark(st, slot, 2);
+
+  // 2b. G0 (recompute): h = x_g W1_e + b1_e written into a block checkpoint in the workspace
+  const void* ckpt = a.gate_up_ckpt;
+  if (rec) {
+    GemmParams p{};
+    p.mode = kMGrouped;
+    p.M = (int)P; p.N = (int)(2 * I); p.K = (int)H;
+    p.m_tiles = (int)(P / kTileM);
+    p.n_tiles = (int)(2 * I / 256);
+    p.num_experts = (int)E;
+    p.tile_expert = tile_expert;
+    p.num_tiles = scalars + 1;
+    p.b_rows_per_expert = (int)(2 * I);
+    p.sfa = reg<uint8_t>(L, ws, R_X_G_SF);
+    p.sfb = a.W1t_sf;
+    p.sfa_ktiles = p.sfb_ktiles = (int)(H / 128);
+    p.fmt_a = a.fp8_act; p.fmt_b = a.fp8_w;
+    p.epi = kEpiCkpt;
+    p.e_tile_offsets = tile_offsets;
+    p.block_offsets = block_offsets;
+    p.b1 = static_cast<const uint16_t*>(a.b1);
+    p.I = a.I; p.B = a.block_size;
+    p.P = P;
+    p.tile_counter = counters + 4;
+    p.status = a.status_dev;
+    ckpt = reg<void>(L, ws, R_CKPT);
+    if ((rc = launch_gemm(mx, 256, p, reg<void>(L, ws, R_X_G), P, H, mx ? static_cast<const void*>(a.W1t_q) : a.W1t,
+                          E * 2 * I, H, st, ckpt, L.Nb * 2 * I, a.block_size)))
+      return rc;
+  }
+  prof_mark(st, slot, 3);
 
   const void* W1 = mx ? static_cast<const void*>(a.W1_q) : a.W1;
   const void* W2 = mx ? static_cast<const void*>(a.W2_q) : a.W2;
@@ -389,7 +440,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.tile_row_flat = tile_row_flat;
     p.e_tile_offsets = tile_offsets;
     p.block_offsets = block_offsets;
-    p.ckpt = static_cast<const uint16_t*>(a.gate_up_ckpt);
+    p.ckpt = static_cast<const uint16_t*>(ckpt);
     p.I = a.I; p.B = a.block_size;
     p.affinity_on_i = a.affinity == MOE_AFFINITY_ON_I;
     p.fmt_act = a.fp8_act;
@@ -400,11 +451,11 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.ds_part = reg<float>(L, ws, R_DS_PART);
     p.tile_counter = counters + 0;
     p.status = a.status_dev;
-    if ((rc = launch_gemm(mx, L.BN1, p, reg<void>(L, ws, R_DOUT_G), P, H, W2, E * I, H, st, a.gate_up_ckpt,
-                          L.Nb * 2 * I, a.block_size)))
+    if ((rc = launch_gemm(mx, L.BN1, p, reg<void>(L, ws, R_DOUT_G), P, H, W2, E * I, H, st, ckpt, L.Nb * 2 * I,
+                          a.block_size)))
       return rc;
   }
-  prof_mark(st, slot, 3);
+  prof_mark(st, slot, 4);
   // 4. G3: dW2_e = a'^T dout_g over the expert's tile rows
   {
     GemmParams p{};
@@ -427,7 +478,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     if ((rc = launch_gemm(mx, L.BN3, p, reg<void>(L, ws, R_AP_T), I, P, reg<void>(L, ws, R_DOUT_GT), H, P, st)))
       return rc;
   }
-  prof_mark(st, slot, 4);
+  prof_mark(st, slot, 5);
   // 5. G2: dx_expanded = dh W1_e^T
   {
     GemmParams p{};
@@ -449,7 +500,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.status = a.status_dev;
     if ((rc = launch_gemm(mx, L.BN2, p, reg<void>(L, ws, R_DH), P, 2 * I, W1, E * H, 2 * I, st))) return rc;
   }
-  prof_mark(st, slot, 5);
+  prof_mark(st, slot, 6);
   // 6. G4: dW1_e = x_g^T dh over the expert's tile rows
   {
     GemmParams p{};
@@ -472,7 +523,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     if ((rc = launch_gemm(mx, L.BN4, p, reg<void>(L, ws, R_X_GT), H, P, reg<void>(L, ws, R_DH_T), 2 * I, P, st)))
       return rc;
   }
-  prof_mark(st, slot, 6);
+  prof_mark(st, slot, 7);
   // 7. reductions
   if ((rc = launch_dx_scatter_sum(reg<uint16_t>(L, ws, R_DX_EXP), flat_tile_row, a.T, a.K, a.H,
                                   static_cast<uint16_t*>(a.dx), st)))
@@ -489,7 +540,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
                                     a.accumulate)))
       return rc;
   }
-  prof_mark(st, slot, 7);
+  prof_mark(st, slot, 8);
   return MOE_OK;
 }
 
@@ -510,6 +561,10 @@ extern "C" int moe_profile_enable(int enable) {
   return MOE_OK;
 }
 
+// Event boundaries are recorded in launch order; stage of the interval between boundary i and i+1.
+static const int kStageOfInterval[MOE_NUM_STAGES] = {MOE_STAGE_ROUTE, MOE_STAGE_PREP, MOE_STAGE_G0, MOE_STAGE_G1,
+                                                     MOE_STAGE_G3,    MOE_STAGE_G2,   MOE_STAGE_G4, MOE_STAGE_REDUCE};
+
 extern "C" int moe_profile_read(double* stage_ms, int max_stages, int* calls) {
   clear_error();
   if (!stage_ms || max_stages < 0) return fail(MOE_ERR_INVALID, "moe_profile_read: null output");
@@ -519,10 +574,11 @@ extern "C" int moe_profile_read(double* stage_ms, int max_stages, int* calls) {
     cudaEvent_t* e = &g_prof.ev[(size_t)c * (MOE_NUM_STAGES + 1)];
     int rc = cuda_check(cudaEventSynchronize(e[MOE_NUM_STAGES]), "cudaEventSynchronize");
     if (rc) return rc;
-    for (int i = 0; i < MOE_NUM_STAGES && i < max_stages; ++i) {
+    for (int i = 0; i < MOE_NUM_STAGES; ++i) {
+      if (kStageOfInterval[i] >= max_stages) continue;
       float ms = 0.f;
       if ((rc = cuda_check(cudaEventElapsedTime(&ms, e[i], e[i + 1]), "cudaEventElapsedTime"))) return rc;
-      stage_ms[i] += ms;
+      stage_ms[kStageOfInterval[i]] += ms;
     }
   }
   return MOE_OK;

@@ -73,6 +73,7 @@ struct PrepArgs {
   void* dout_g; uint8_t* dout_g_sf;    // [P,H]
   void* dout_gt; uint8_t* dout_gt_sf;  // [H,P]
   void* x_gt; uint8_t* x_gt_sf;        // [H,P]
+  void* x_g; uint8_t* x_g_sf;          // [P,H] row-major (nullable: only when h is recomputed)
   float* ds_bias;                      // [P] <dout_t, b2_e> or null
 };
 int launch_prep(const PrepArgs& a, cudaStream_t st);
@@ -88,7 +89,7 @@ int launch_quant_colwise(const uint16_t* in, int64_t src_rows, int64_t rows, int
 // tcgen05 grouped GEMM (gemm_*.cu)
 // ------------------------------------------------------------------------------------------
 enum GemmMode { kMGrouped = 0, kKGrouped = 1 };
-enum EpiKind { kEpiStore = 0, kEpiDSwiGLU = 1 };
+enum EpiKind { kEpiStore = 0, kEpiDSwiGLU = 1, kEpiCkpt = 2 };
 
 struct GemmParams {
   int mode;
@@ -117,6 +118,7 @@ struct GemmParams {
   const int32_t* e_tile_offsets;
   const int32_t* block_offsets;
   const uint16_t* ckpt;         // [N,2,I,B]
+  const uint16_t* b1;           // G0 (checkpoint epilogue): [E,2I] bias or null
   int I, B, affinity_on_i, fmt_act;
   int64_t P;
   void* dh; uint8_t* dh_sf;

@@ -7,7 +7,8 @@
 //   x_gt    [H, P]  gathered x transposed                   (G4 A operand)
 //   ds_bias [P]     <dout_t, b2_e>, the bias term of ds      (sonic-moe db2_and_ds_kernel)
 // as BF16, or as MXFP8 with E8M0 scales in the tiled layout (transposed operands are quantised
-// in groups of 32 tile rows, i.e. along the GEMM contraction).  Padding rows are zero.
+// in groups of 32 tile rows, i.e. along the GEMM contraction).  Padding rows are zero.  When the
+// gate/up pre-activations are recomputed, a row-major gathered x [P,H] (G0's A operand) is written too.
 #include <cuda_runtime.h>
 
 #include "moebwd_internal.h"
@@ -70,7 +71,9 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
         const int row = warp + 8 * r;
         const int64_t prow = prow0 + row;
         if (colok) *reinterpret_cast<uint4*>(st + row * kPrepTilePitch + lane * 8) = v[r];
-        if (which != 0) continue;
+        if (which != 0 && !a.x_g) continue;  // row-major copy: dout always, x when recomputing h
+        void* rowdst = which == 0 ? a.dout_g : a.x_g;
+        uint8_t* rowsf = which == 0 ? a.dout_g_sf : a.x_g_sf;
         const uint32_t dw[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
         float d8[8];
 #pragma unroll
@@ -78,7 +81,7 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
           d8[2 * j] = __uint_as_float(dw[j] << 16);
           d8[2 * j + 1] = __uint_as_float(dw[j] & 0xFFFF0000u);
         }
-        if constexpr (BIAS) {
+        if (BIAS && which == 0) {
           const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -98,10 +101,10 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
           uint2 q;
           q.x = fp8x4(d8[0] * inv, d8[1] * inv, d8[2] * inv, d8[3] * inv, a.fmt);
           q.y = fp8x4(d8[4] * inv, d8[5] * inv, d8[6] * inv, d8[7] * inv, a.fmt);
-          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.dout_g) + prow * H + col) = q;
-          if ((lane & 3) == 0) a.dout_g_sf[sf_tiled_offset(prow, col, H)] = (uint8_t)byte;
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(rowdst) + prow * H + col) = q;
+          if ((lane & 3) == 0) rowsf[sf_tiled_offset(prow, col, H)] = (uint8_t)byte;
         } else {
-          if (colok) *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dout_g) + prow * H + col) = v[r];
+          if (colok) *reinterpret_cast<uint4*>(static_cast<uint16_t*>(rowdst) + prow * H + col) = v[r];
         }
       }
       __syncthreads();
