@@ -289,6 +289,48 @@ def time_oracle(run, flops, max_s):
 
 
 # ---------------------------------------------------------------------------------------------
+def recompute_row(mb, cfg, inp, kw, steps, stream, peak_tf, dev):
+    """The whole backward with the gate/up pre-activations recomputed by the forward grouped GEMM G0
+    (act_src RECOMPUTE) instead of read from the checkpoint: G0's own rate against the tensor peak
+    (4*T*K*H*I FLOPs, not counted as useful) and the step time."""
+    import torch
+    op = mb.MoeBwd(T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K, block_size=cfg.block_size, precision=cfg.precision,
+                   affinity=cfg.affinity, fp8_act=cfg.fp8_act, fp8_w=cfg.fp8_w, has_bias=cfg.bias,
+                   act_src=mb.ACT_RECOMPUTE, device=dev)
+    kw = {k: v for k, v in kw.items() if k != "ckpt"}
+    W1t = inp.W1.transpose(1, 2).contiguous()
+    if cfg.precision == mb.PREC_MXFP8:
+        kw["W1t_q"], kw["W1t_sf"] = mb.quantize_weights(W1t, cfg.fp8_w)
+        del W1t
+    else:
+        kw["W1t"] = W1t
+    kw["b1"] = inp.b1 if cfg.bias else None
+    op.bind(**kw)
+    for _ in range(3):
+        op.run()
+    torch.cuda.synchronize()
+    if int(op.status.item()) != 0:
+        raise SystemExit(f"device status {int(op.status.item())} (recompute)")
+    mb.profile_enable(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        op.run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    st, n = mb.profile_read()
+    mb.profile_enable(False)
+    g0 = st["G0_recompute_h"] / max(n, 1)
+    g0_flops = 4.0 * cfg.T * cfg.K * cfg.H * cfg.I
+    return dict(ms_per_step=ms, useful_tflops=cfg.useful_flops() / (ms * 1e-3) / 1e12,
+                g0_ms=g0, g0_tflops=g0_flops / (g0 * 1e-3) / 1e12, g0_frac=g0_flops / (g0 * 1e-3) / 1e12 / peak_tf,
+                g0_flops_per_launch=g0_flops, bound="tensor",
+                note="G0 recomputes h = x_g W1_e (+ b1_e) into the block checkpoint layout; its FLOPs are "
+                     "excluded from useful_tflops")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -444,6 +486,7 @@ def main():
                                          algorithmic_bytes=rbytes, achieved_gbs=gbs, peak_gbs=peaks["hbm_gbs"],
                                          frac=gbs / peaks["hbm_gbs"]))
         del dl
+        next_rows["recompute_h"] = recompute_row(mb, cfg, inp, kw, args.steps, stream, peak_tf, dev)
 
     lib_peak = recorded_mxfp8_peak()
     if prec == 1 and lib_peak:

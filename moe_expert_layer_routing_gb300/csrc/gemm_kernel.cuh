@@ -621,34 +621,35 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         }
         continue;
       } else if constexpr (C::TMA_STORE) {
-        // one 64-column slab at a time through a single staging slab; TMEM is free after the last
-#pragma unroll 1
+        // The warp's 128 columns (4 slabs x 32) are read from TMEM and packed to bf16 in registers
+        // first, so the accumulator is released after four loads; the slabs then go out one at a
+        // time through the staging slab while the next tile's MMAs run.
+        uint32_t pk[BN / 64][16];
+#pragma unroll
         for (int sl = 0; sl < BN / 64; ++sl) {
-          if (warp == 2 && lane == 0) bulk_wait_read_all();
-          epilogue_bar<32 * C::EPI_WARPS>();
-          const int c = sl * 2 + half;
           uint32_t r[32];
           if (ti.nk > 0) {
-            tmem_ld_32x32b_x32(taddr + c * 32, r);
+            tmem_ld_32x32b_x32(taddr + (sl * 2 + half) * 32, r);
             tmem_ld_wait();
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = 0u;
           }
 #pragma unroll
+          for (int j = 0; j < 16; ++j) pk[sl][j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+#pragma unroll
+        for (int sl = 0; sl < BN / 64; ++sl) {
+          if (warp == 2 && lane == 0) bulk_wait_read_all();
+          epilogue_bar<32 * C::EPI_WARPS>();
+#pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             const int chunk = half * 4 + q4;
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[8 * q4 + 0]), __uint_as_float(r[8 * q4 + 1]));
-            w.y = pack_bf16x2(__uint_as_float(r[8 * q4 + 2]), __uint_as_float(r[8 * q4 + 3]));
-            w.z = pack_bf16x2(__uint_as_float(r[8 * q4 + 4]), __uint_as_float(r[8 * q4 + 5]));
-            w.w = pack_bf16x2(__uint_as_float(r[8 * q4 + 6]), __uint_as_float(r[8 * q4 + 7]));
-            *reinterpret_cast<uint4*>(smStage + m * 128 + ((chunk ^ (m & 7)) << 4)) = w;
-          }
-          if (sl == BN / 64 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
+            *reinterpret_cast<uint4*>(smStage + m * 128 + ((chunk ^ (m & 7)) << 4)) =
+                make_uint4(pk[sl][4 * q4 + 0], pk[sl][4 * q4 + 1], pk[sl][4 * q4 + 2], pk[sl][4 * q4 + 3]);
           }
           fence_proxy_async_smem();
           epilogue_bar<32 * C::EPI_WARPS>();
