@@ -10,9 +10,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(CSRC, "_build")
 LIB = os.path.join(PKG, "libmoebwd.so")
-SOURCES = ["host.cu", "route_meta.cu", "prep.cu", "reduce.cu", "moe_bwd.cu", "gemm_bf16.cu", "gemm_mx.cu",
+SOURCES = ["host.cu", "route_meta.cu", "prep.cu", "reduce.cu", "moe_bwd.cu", "gemm_bf16.cu", "gemm_mx.cu", "gemm_pair.cu",
            "noalloc.cu", "router.cu"]
-HEADERS = ["ptx.cuh", "mx_device.cuh", "gemm_kernel.cuh", "moebwd_internal.h"]
+HEADERS = ["ptx.cuh", "mx_device.cuh", "gemm_kernel.cuh", "gemm_pair_kernel.cuh", "moebwd_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

@@ -16,14 +16,38 @@
 
 namespace moebwd {
 
+// CTA-pair GEMMs replace the single-CTA kernel for BF16 where they apply: a store or checkpoint
+// epilogue, N a multiple of 256, and M-grouped schedules that know their expert pairs (or have one
+// expert) / K-grouped M a multiple of 256.  For MXFP8 the single-CTA kernel is kept (its pair tile
+// has a single TMEM accumulator and measured slower).  MOEBWD_PAIR=0 disables pairs, MOEBWD_PAIR=2
+// also uses them for MXFP8 (comparisons and tests).
+static bool use_pair(bool mx, int BN, const GemmParams& p) {
+  const char* v = getenv("MOEBWD_PAIR");
+  const int mode = v ? atoi(v) : 1;
+  if (mode == 0 || (mx && mode != 2)) return false;
+  if (BN != 256 || (p.epi != kEpiStore && p.epi != kEpiCkpt)) return false;
+  if (p.mode == kMGrouped) return p.pair_offsets != nullptr || p.tile_expert == nullptr;
+  return p.m_tiles % 2 == 0;
+}
+
+// Width of the pair tile: 256 (MOEBWD_PAIR_BN=128 selects the narrow tile, for tuning runs).
+static int pair_bn() {
+  const char* v = getenv("MOEBWD_PAIR_BN");
+  if (v && atoi(v) == 128) return 128;
+  return 256;
+}
+
 int launch_gemm(bool mx, int BN, const GemmParams& p, const void* A, int64_t a_rows, int64_t a_cols, const void* B,
                 int64_t b_rows, int64_t b_cols, cudaStream_t st, const void* ckpt, int64_t ck_rows, int64_t ck_cols) {
-  alignas(64) CUtensorMap ta, tb, tc;
+  alignas(64) CUtensorMap ta, tb, tc, tsa, tsb;
   const int es = mx ? 1 : 2;
   const uint32_t bke = mx ? 128 : 64;
+  const bool pair = use_pair(mx, BN, p);
+  const int pbn = pair ? pair_bn() : BN;
   if (!make_tmap_2d(&ta, A, es, (uint64_t)a_rows, (uint64_t)a_cols, (uint64_t)a_cols * es, 128, bke))
     return MOE_ERR_INVALID;
-  if (!make_tmap_2d(&tb, B, es, (uint64_t)b_rows, (uint64_t)b_cols, (uint64_t)b_cols * es, (uint32_t)BN, bke))
+  if (!make_tmap_2d(&tb, B, es, (uint64_t)b_rows, (uint64_t)b_cols, (uint64_t)b_cols * es,
+                    pair ? (uint32_t)pbn / 2 : (uint32_t)BN, bke))
     return MOE_ERR_INVALID;
   if (ckpt) {  // checkpoint chunks: 32 features x 128 rows of the [N*2*I, B] view, unswizzled
     if (!make_tmap_2d(&tc, ckpt, 2, (uint64_t)ck_rows, (uint64_t)ck_cols, (uint64_t)ck_cols * 2, 32, 128, false))
@@ -34,6 +58,26 @@ int launch_gemm(bool mx, int BN, const GemmParams& p, const void* A, int64_t a_r
       return MOE_ERR_INVALID;
   } else {
     tc = ta;
+  }
+  if (pair) {
+    if (mx) {  // tiled scales as rows of 512 bytes (128 x uint32): one row per (128-row block, K tile)
+      if (!make_tmap_2d(&tsa, p.sfa, 4, (uint64_t)(a_rows / 128) * p.sfa_ktiles, 128, 512, 1, 128, false))
+        return MOE_ERR_INVALID;
+      if (!make_tmap_2d(&tsb, p.sfb, 4, (uint64_t)(b_rows / 128) * p.sfb_ktiles, 128, 512, 1, 128, false))
+        return MOE_ERR_INVALID;
+    } else {
+      tsa = ta;
+      tsb = ta;
+    }
+    GemmParams pp = p;
+    pp.n_tiles = p.N / pbn;
+    // upper bound of the pair tiles: sum_e ceil(tiles_e / 2) <= (tiles + E) / 2
+    const int64_t pairs = p.mode == kMGrouped
+                              ? (int64_t)((p.m_tiles + (p.pair_offsets ? p.num_experts : 0) + 1) / 2) * pp.n_tiles
+                              : (int64_t)p.num_experts * (p.m_tiles / 2) * pp.n_tiles;
+    const int max_pairs = (int)std::min<int64_t>(pairs, device_sm_count() / 2);
+    if (max_pairs <= 0) return MOE_OK;
+    return launch_gemm_pair(mx, pbn, pp, &ta, &tb, &tc, &tsa, &tsb, max_pairs, st);
   }
   const int64_t tiles = (int64_t)(p.mode == kMGrouped ? p.m_tiles : p.num_experts * p.m_tiles) * p.n_tiles;
   const int grid = (int)std::min<int64_t>(tiles, device_sm_count());
@@ -48,7 +92,7 @@ enum Region {
   R_CHUNK_COUNTS, R_EXPERT_OFFSETS, R_BLOCK_OFFSETS, R_TILE_OFFSETS, R_EXPERT_ORDER, R_SCALARS,
   R_X_GATHER, R_S_SCATTER, R_S_REV, R_TPID, R_B2E, R_TILE_ROW_FLAT, R_FLAT_TILE_ROW, R_TILE_EXPERT,
   R_DOUT_G, R_DOUT_G_SF, R_DOUT_GT, R_DOUT_GT_SF, R_X_GT, R_X_GT_SF, R_DH, R_DH_SF, R_DH_T, R_DH_T_SF,
-  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_X_G, R_X_G_SF, R_CKPT, R_COUNT
+  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_X_G, R_X_G_SF, R_CKPT, R_PAIR_OFFSETS, R_COUNT
 };
 
 struct Layout {
@@ -127,6 +171,7 @@ static Layout make_layout(const MoeBwdArgs& a) {
   b[R_DS_PART] = sizeof(float) * (size_t)(P * 2 * (I / L.BN1));  // two column halves per N tile
   b[R_DS_BIAS] = a.has_bias ? sizeof(float) * (size_t)P : 0;
   b[R_COUNTERS] = 64;  // one tile counter per grouped GEMM
+  b[R_PAIR_OFFSETS] = sizeof(int32_t) * (E + 1);
   if (a.act_src == MOE_ACT_RECOMPUTE) {
     b[R_X_G] = (size_t)(P * H * es);
     b[R_X_G_SF] = mx ? (size_t)(P * H / 32) : 0;
@@ -354,6 +399,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   r.flat_tile_row = flat_tile_row;
   r.tile_expert = tile_expert;
   r.num_blocks_out = nullptr;
+  r.pair_offsets = reg<int32_t>(L, ws, R_PAIR_OFFSETS);
   r.status = a.status_dev;
   if ((rc = launch_route_meta(a.ids, a.T, a.K, a.E, a.block_size, L.Nb, P, r, st))) return rc;
   prof_mark(st, slot, 1);
@@ -404,6 +450,8 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.fmt_a = a.fp8_act; p.fmt_b = a.fp8_w;
     p.epi = kEpiCkpt;
     p.e_tile_offsets = tile_offsets;
+    p.pair_offsets = reg<int32_t>(L, ws, R_PAIR_OFFSETS);
+    p.num_pairs = scalars + 2;
     p.block_offsets = block_offsets;
     p.b1 = static_cast<const uint16_t*>(a.b1);
     p.I = a.I; p.B = a.block_size;
@@ -496,6 +544,9 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.fmt_a = a.fp8_act; p.fmt_b = a.fp8_w;
     p.epi = kEpiStore;
     p.out = reg<void>(L, ws, R_DX_EXP); p.ldo = H;
+    p.e_tile_offsets = tile_offsets;
+    p.pair_offsets = reg<int32_t>(L, ws, R_PAIR_OFFSETS);
+    p.num_pairs = scalars + 2;
     p.tile_counter = counters + 2;
     p.status = a.status_dev;
     if ((rc = launch_gemm(mx, L.BN2, p, reg<void>(L, ws, R_DH), P, 2 * I, W1, E * H, 2 * I, st))) return rc;

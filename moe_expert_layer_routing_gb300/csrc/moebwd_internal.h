@@ -40,7 +40,8 @@ struct RouteBufs {
   int32_t* block_offsets;     // [E+1]
   int32_t* tile_offsets;      // [E+1]
   int32_t* expert_order;      // [E] experts by descending row count
-  int32_t* scalars;           // [4]: num_blocks, num_tiles
+  int32_t* scalars;           // [4]: num_blocks, num_tiles, num_pairs
+  int32_t* pair_offsets;      // nullable [E+1]: prefix of ceil(tiles_e / 2)
   int32_t* x_gather_idx;      // [TK]
   int32_t* s_scatter_idx;     // [TK]
   int32_t* s_reverse;         // [TK]
@@ -125,6 +126,10 @@ struct GemmParams {
   void* dht; uint8_t* dht_sf;
   void* apt; uint8_t* apt_sf;
   float* ds_part;               // [P, 2*I/BN]
+  // CTA-pair kernel, M-grouped: expert e's 128-row tiles form ceil(tiles_e / 2) pairs; pair_offsets
+  // [E+1] is their prefix (null: one expert, pairs of consecutive tiles), num_pairs its device total
+  const int32_t* pair_offsets;
+  const int32_t* num_pairs;
   int32_t* tile_counter;        // zeroed before the launch: dynamic tile claims
   int accumulate;               // store epilogue: add the tile to the output instead of overwriting
   int32_t* status;
@@ -139,6 +144,11 @@ int launch_gemm_bf16(int BN, const GemmParams& p, const void* tmA, const void* t
                      cudaStream_t st);
 int launch_gemm_mx(int BN, const GemmParams& p, const void* tmA, const void* tmB, const void* tmC, int grid,
                    cudaStream_t st);
+// CTA-pair GEMM (gemm_pair.cu): pair tiles of 256 rows x BN (128 or 256) columns, p.n_tiles = N / BN,
+// store or checkpoint epilogue; tmSFA / tmSFB map the tiled scales as rows of 512 bytes (MXFP8).
+// max_pairs bounds the pairs launched.
+int launch_gemm_pair(bool mx, int BN, const GemmParams& p, const void* tmA, const void* tmB, const void* tmC,
+                     const void* tmSFA, const void* tmSFB, int max_pairs, cudaStream_t st);
 
 // ------------------------------------------------------------------------------------------
 // reductions (reduce.cu)

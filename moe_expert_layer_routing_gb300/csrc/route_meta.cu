@@ -80,11 +80,13 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int nchunks, int E, in
                                                           int32_t* expert_offsets, int32_t* block_offsets,
                                                           int32_t* tile_offsets, int32_t* expert_order,
                                                           int32_t* block_to_expert, int32_t* tile_expert,
-                                                          int32_t* scalars, int32_t* num_blocks_out) {
+                                                          int32_t* scalars, int32_t* num_blocks_out,
+                                                          int32_t* pair_offsets) {
   __shared__ int32_t cnt[kMaxExperts + 1];
   __shared__ int32_t rows[kMaxExperts + 1];
   __shared__ int32_t blks[kMaxExperts + 1];
   __shared__ int32_t tiles[kMaxExperts + 1];
+  __shared__ int32_t prs[kMaxExperts + 1];
   __shared__ int32_t wt[33];
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int tot = 0;
@@ -93,15 +95,18 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int nchunks, int E, in
     rows[e] = tot;
     blks[e] = (tot + B - 1) / B;
     tiles[e] = (tot + kTileM - 1) / kTileM;
+    prs[e] = (tiles[e] + 1) / 2;  // the expert's tiles taken two at a time (CTA-pair GEMMs)
   }
   __syncthreads();
   const int tot_rows = block_exclusive_scan(rows, E, wt);
   const int tot_blks = block_exclusive_scan(blks, E, wt);
   const int tot_tiles = block_exclusive_scan(tiles, E, wt);
+  const int tot_pairs = block_exclusive_scan(prs, E, wt);
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     expert_offsets[e] = e < E ? rows[e] : tot_rows;
     block_offsets[e] = e < E ? blks[e] : tot_blks;
     tile_offsets[e] = (e < E ? tiles[e] : tot_tiles) * kTileM;
+    if (pair_offsets) pair_offsets[e] = e < E ? prs[e] : tot_pairs;
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = rows[e];
@@ -123,6 +128,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int nchunks, int E, in
   if (threadIdx.x == 0) {
     scalars[0] = tot_blks;
     scalars[1] = tot_tiles;
+    scalars[2] = tot_pairs;
     if (num_blocks_out) *num_blocks_out = tot_blks;
   }
 }
@@ -218,7 +224,8 @@ int launch_route_meta(const int32_t* ids, int T, int K, int E, int B, int64_t Nb
     if ((rc = cuda_check(cudaGetLastError(), "route_count"))) return rc;
   }
   route_scan_kernel<<<1, 1024, 0, st>>>(nch, E, B, r.chunk_counts, r.expert_offsets, r.block_offsets, r.tile_offsets,
-                                        r.expert_order, r.block_to_expert, r.tile_expert, r.scalars, r.num_blocks_out);
+                                        r.expert_order, r.block_to_expert, r.tile_expert, r.scalars, r.num_blocks_out,
+                                        r.pair_offsets);
   count_launch();
   if ((rc = cuda_check(cudaGetLastError(), "route_scan"))) return rc;
   if (nch > 0) {
