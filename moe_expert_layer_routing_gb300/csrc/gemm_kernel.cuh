@@ -36,11 +36,14 @@ struct GemmCfg {
   static constexpr int SFA_BYTES = MX ? 512 : 0;
   static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  // dSwiGLU epilogue: one 32x32 transposition buffer per warp and a double-buffered checkpoint chunk
+  // dSwiGLU epilogue: 4 * kG1Subs warps (kG1Subs per TMEM lane quarter, each taking NC = 32 / kG1Subs
+  // of every 32 columns), three NC x 32 fp32 transposition buffers per warp, the row-wise amax
+  // exchange of each quarter (double-buffered by chunk parity) and a double-buffered checkpoint chunk
   // (gate and up, 32 features x 128 tile rows each) filled by TMA one chunk ahead.
-  // dSwiGLU: 8 epilogue warps (two per TMEM lane quarter, each taking 16 of every 32 columns)
-  static constexpr int EPI_WARP_BYTES = (EPI == kEpiDSwiGLU) ? 3 * 16 * 33 * 4 : 0;  // fp32 transposes
-  static constexpr int XCHG_BYTES = (EPI == kEpiDSwiGLU) ? 2 * 4 * 2 * 2 * 32 * 4 : 0;  // pair amax exchange, x2 by chunk parity
+  static constexpr int G1_NC = 32 / kG1Subs;
+  static constexpr int EPI_WARP_BYTES = (EPI == kEpiDSwiGLU) ? 3 * G1_NC * 33 * 4 : 0;
+  static constexpr int XCHG_QUARTER = kG1Subs * 2 * 32;  // floats: [slice][gate|up][lane]
+  static constexpr int XCHG_BYTES = (EPI == kEpiDSwiGLU) ? 2 * 4 * XCHG_QUARTER * 4 : 0;
   static constexpr int CK_CHUNK_BYTES = 2 * 32 * 128 * 2;
   static constexpr int CK_BYTES = (EPI == kEpiDSwiGLU) ? 2 * CK_CHUNK_BYTES : 0;
   // Store epilogue with a single TMEM accumulator: the tile is drained into a 128B-swizzled bf16
@@ -56,8 +59,8 @@ struct GemmCfg {
   static constexpr bool STAGED = TMA_STORE || CKPT_STORE;
   // one 64-column staging slab (16 KB) keeps a fourth pipeline stage in shared memory
   static constexpr int STAGING_BYTES = STAGED ? BM * 64 * 2 : 0;
-  // dSwiGLU and staged epilogues: 8 warps, two per TMEM lane quarter, splitting the columns
-  static constexpr int EPI_WARPS = (EPI == kEpiDSwiGLU || STAGED) ? 8 : 4;
+  // staged epilogues: 8 warps, two per TMEM lane quarter, splitting the columns
+  static constexpr int EPI_WARPS = EPI == kEpiDSwiGLU ? 4 * kG1Subs : STAGED ? 8 : 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES + XCHG_BYTES + CK_BYTES + STAGING_BYTES;
   static constexpr int BAR_BYTES = 512;
@@ -185,125 +188,152 @@ __device__ __forceinline__ void tile_ckpt_origin(const GemmParams& p, const Tile
   b0 = (int)(slot0 - blk * p.B);
 }
 
-// Transposed store of 16 columns x 32 rows: v[j] of lane r is element (r, j).  The block is
-// transposed through shared memory as fp32 (pitch 33, conflict free); lane l then handles column
-// l % 16, rows 16*(l / 16) .. +15, so output row row0 + l % 16 gets columns p0..p0+31 from two lanes
-// (bf16, or fp8 codes with one scale quantised along all 32: the two lanes combine their amax).
-template <bool MX>
-__device__ __forceinline__ void store_transposed16(float* buf, const float (&v)[16], void* out, uint8_t* sf,
-                                                   int64_t P, int64_t row0, int64_t p0, int lane, int fmt) {
+// Transposed store of NC columns x 32 rows (NC = 8 or 16): v[j] of lane r is element (r, j).  The
+// block is transposed through shared memory as fp32 (pitch 33, conflict free); lane l then handles
+// column l % NC, rows NC*(l / NC) .. +NC-1, so output row row0 + l % NC gets columns p0..p0+31 from
+// 32/NC lanes (bf16, or fp8 codes with one scale quantised along all 32: those lanes combine their
+// amax).
+template <bool MX, int NC>
+__device__ __forceinline__ void store_transposed(float* buf, const float (&v)[NC], void* out, uint8_t* sf,
+                                                 int64_t P, int64_t row0, int64_t p0, int lane, int fmt) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) buf[j * 33 + lane] = v[j];
+  for (int j = 0; j < NC; ++j) buf[j * 33 + lane] = v[j];
   __syncwarp();
-  const int c = lane & 15, rh = lane >> 4;
-  float col[16];
+  const int c = lane % NC, rg = lane / NC;
+  float col[NC];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) col[i] = buf[c * 33 + rh * 16 + i];
+  for (int i = 0; i < NC; ++i) col[i] = buf[c * 33 + rg * NC + i];
   if constexpr (MX) {
     float am = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(col[i]));
-    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 16));
+    for (int i = 0; i < NC; ++i) am = fmaxf(am, fabsf(col[i]));
+#pragma unroll
+    for (int o = NC; o < 32; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
     const uint32_t byte = e8m0_byte(__float_as_uint(am), fmt);
     const float inv = e8m0_inv_scale(byte);
-    uint4 q;
-    q.x = fp8x4(col[0] * inv, col[1] * inv, col[2] * inv, col[3] * inv, fmt);
-    q.y = fp8x4(col[4] * inv, col[5] * inv, col[6] * inv, col[7] * inv, fmt);
-    q.z = fp8x4(col[8] * inv, col[9] * inv, col[10] * inv, col[11] * inv, fmt);
-    q.w = fp8x4(col[12] * inv, col[13] * inv, col[14] * inv, col[15] * inv, fmt);
-    *reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + (row0 + c) * P + p0 + rh * 16) = q;
-    if (rh == 0) sf[sf_tiled_offset(row0 + c, p0, P)] = (uint8_t)byte;
+    uint32_t q[NC / 4];
+#pragma unroll
+    for (int w = 0; w < NC / 4; ++w)
+      q[w] = fp8x4(col[4 * w] * inv, col[4 * w + 1] * inv, col[4 * w + 2] * inv, col[4 * w + 3] * inv, fmt);
+    uint8_t* dst = static_cast<uint8_t*>(out) + (row0 + c) * P + p0 + rg * NC;
+    if constexpr (NC == 16)
+      *reinterpret_cast<uint4*>(dst) = make_uint4(q[0], q[1], q[2], q[3]);
+    else
+      *reinterpret_cast<uint2*>(dst) = make_uint2(q[0], q[1]);
+    if (rg == 0) sf[sf_tiled_offset(row0 + c, p0, P)] = (uint8_t)byte;
   } else {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (row0 + c) * P + p0 + rh * 16);
-    dst[0] = make_uint4(pack_bf16x2(col[0], col[1]), pack_bf16x2(col[2], col[3]), pack_bf16x2(col[4], col[5]),
-                        pack_bf16x2(col[6], col[7]));
-    dst[1] = make_uint4(pack_bf16x2(col[8], col[9]), pack_bf16x2(col[10], col[11]), pack_bf16x2(col[12], col[13]),
-                        pack_bf16x2(col[14], col[15]));
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (row0 + c) * P + p0 + rg * NC);
+#pragma unroll
+    for (int w = 0; w < NC / 8; ++w)
+      dst[w] = make_uint4(pack_bf16x2(col[8 * w + 0], col[8 * w + 1]), pack_bf16x2(col[8 * w + 2], col[8 * w + 3]),
+                          pack_bf16x2(col[8 * w + 4], col[8 * w + 5]), pack_bf16x2(col[8 * w + 6], col[8 * w + 7]));
   }
   __syncwarp();
 }
 
-// G1 epilogue, 16 columns (half `half` of a 32-column chunk starting at feature i0) of one warp:
+template <int NTHREADS>
+__device__ __forceinline__ void group_bar(int id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(NTHREADS) : "memory");
+}
+
+// G1 epilogue, NC columns (slice `sub` of a 32-column chunk starting at feature i0) of one warp:
 // from dA_raw (accumulator) and the checkpointed gate/up pre-activations (staged in shared memory,
 // [gate|up][32 features][128 rows]) compute
 //   ds += <dA_raw, a>,  dA = s dA_raw,  dgate = dA up SiLU'(gate),  dup = dA SiLU(gate),  a' = s a
 // and write dh [P,2I] (row-major), dh^T [2I,P], a'^T [I,P] (bf16, or fp8 + scales).  The row-wise
-// MXFP8 groups of dh (32 features) span both warps of a pair: partial amax values are exchanged
-// through `xchg` with a pair barrier.  Padding rows produce zeros.
-template <bool MX>
-__device__ __forceinline__ void epi_dswiglu_half(const GemmParams& p, uint32_t taddr, int64_t prow, int m, int lane,
-                                                 bool valid, float sv, int i0, int half, const uint16_t* ck,
-                                                 float* tbuf, float* xchg, int pair_id, float& ds_acc) {
+// MXFP8 groups of dh (32 features) span the 32/NC warps of a TMEM lane quarter: partial amax values
+// are exchanged through `xchg` ([slice][gate|up][32 lanes]) with a barrier over those warps.
+// Padding rows produce zeros.
+template <bool MX, int NC>
+__device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t taddr, int64_t prow, int m, int lane,
+                                                 bool valid, float sv, int i0, int sub, const uint16_t* ck,
+                                                 float* tbuf, float* xchg, int bar_id, float& ds_acc) {
+  constexpr int SUBS = 32 / NC;
   const int I = p.I;
   const int64_t P = p.P;
   const int64_t p0 = prow - lane;
-  uint32_t r[16];
-  tmem_ld_32x32b_x16(taddr, r);
-  tmem_ld_wait();
-  float dg[16], du[16], ap[16];
+  // the accumulator load is in flight while the checkpoint-only terms are computed
+  uint32_t r[NC];
+  if constexpr (NC == 16)
+    tmem_ld_32x32b_x16(taddr, r);
+  else
+    tmem_ld_32x32b_x8(taddr, r);
+  float dg[NC], du[NC], ap[NC];  // SiLU(g), a and up * SiLU'(g) first, the gradients after the load
 #pragma unroll
-  for (int jj = 0; jj < 16; ++jj) {
-    float v = __uint_as_float(r[jj]);
-    float g = bf16_bits_to_float(ck[(half * 16 + jj) * 128 + m]);
-    float u = bf16_bits_to_float(ck[32 * 128 + (half * 16 + jj) * 128 + m]);
-    if (!valid) v = g = u = 0.f;
+  for (int jj = 0; jj < NC; ++jj) {
+    float g = bf16_bits_to_float(ck[(sub * NC + jj) * 128 + m]);
+    float u = bf16_bits_to_float(ck[32 * 128 + (sub * NC + jj) * 128 + m]);
+    if (!valid) g = u = 0.f;
     const float sg = __fdividef(1.f, 1.f + __expf(-g));
     const float sl = g * sg;
-    const float a = sl * u;
+    du[jj] = sl;
+    ap[jj] = sl * u;
+    dg[jj] = u * (sg * (1.f + g * (1.f - sg)));
+  }
+  tmem_ld_wait_regs<NC>(r);
+#pragma unroll
+  for (int jj = 0; jj < NC; ++jj) {
+    const float v = valid ? __uint_as_float(r[jj]) : 0.f;
+    const float a = ap[jj];
     ds_acc = fmaf(v, a, ds_acc);
     const float dA = sv * v;
-    dg[jj] = dA * u * (sg * (1.f + g * (1.f - sg)));
-    du[jj] = dA * sl;
+    dg[jj] = dA * dg[jj];
+    du[jj] = dA * du[jj];
     ap[jj] = p.affinity_on_i ? sv * a : a;
   }
-  const int c0 = i0 + half * 16;  // first feature of this warp's 16 columns
+  const int c0 = i0 + sub * NC;  // first feature of this warp's columns
   if constexpr (MX) {
     float amg = 0.f, amu = 0.f;
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) {
+    for (int jj = 0; jj < NC; ++jj) {
       amg = fmaxf(amg, fabsf(dg[jj]));
       amu = fmaxf(amu, fabsf(du[jj]));
     }
-    // xchg layout: [half][gate|up][32 lanes]
-    xchg[(half * 2 + 0) * 32 + lane] = amg;
-    xchg[(half * 2 + 1) * 32 + lane] = amu;
-    pair_bar(pair_id);
-    amg = fmaxf(amg, xchg[((1 - half) * 2 + 0) * 32 + lane]);
-    amu = fmaxf(amu, xchg[((1 - half) * 2 + 1) * 32 + lane]);
+    xchg[(sub * 2 + 0) * 32 + lane] = amg;
+    xchg[(sub * 2 + 1) * 32 + lane] = amu;
+    group_bar<32 * SUBS>(bar_id);
+#pragma unroll
+    for (int o = 0; o < SUBS; ++o) {
+      if (o == sub) continue;
+      amg = fmaxf(amg, xchg[(o * 2 + 0) * 32 + lane]);
+      amu = fmaxf(amu, xchg[(o * 2 + 1) * 32 + lane]);
+    }
     uint8_t* dh = static_cast<uint8_t*>(p.dh) + prow * (2 * (int64_t)I);
     const uint32_t bg = e8m0_byte(__float_as_uint(amg), p.fmt_act), bu = e8m0_byte(__float_as_uint(amu), p.fmt_act);
     const float ig = e8m0_inv_scale(bg), iu = e8m0_inv_scale(bu);
-    uint4 qg, qu;
-    qg.x = fp8x4(dg[0] * ig, dg[1] * ig, dg[2] * ig, dg[3] * ig, p.fmt_act);
-    qg.y = fp8x4(dg[4] * ig, dg[5] * ig, dg[6] * ig, dg[7] * ig, p.fmt_act);
-    qg.z = fp8x4(dg[8] * ig, dg[9] * ig, dg[10] * ig, dg[11] * ig, p.fmt_act);
-    qg.w = fp8x4(dg[12] * ig, dg[13] * ig, dg[14] * ig, dg[15] * ig, p.fmt_act);
-    qu.x = fp8x4(du[0] * iu, du[1] * iu, du[2] * iu, du[3] * iu, p.fmt_act);
-    qu.y = fp8x4(du[4] * iu, du[5] * iu, du[6] * iu, du[7] * iu, p.fmt_act);
-    qu.z = fp8x4(du[8] * iu, du[9] * iu, du[10] * iu, du[11] * iu, p.fmt_act);
-    qu.w = fp8x4(du[12] * iu, du[13] * iu, du[14] * iu, du[15] * iu, p.fmt_act);
-    *reinterpret_cast<uint4*>(dh + c0) = qg;
-    *reinterpret_cast<uint4*>(dh + I + c0) = qu;
-    if (half == 0) {
+    uint32_t qg[NC / 4], qu[NC / 4];
+#pragma unroll
+    for (int w = 0; w < NC / 4; ++w) {
+      qg[w] = fp8x4(dg[4 * w] * ig, dg[4 * w + 1] * ig, dg[4 * w + 2] * ig, dg[4 * w + 3] * ig, p.fmt_act);
+      qu[w] = fp8x4(du[4 * w] * iu, du[4 * w + 1] * iu, du[4 * w + 2] * iu, du[4 * w + 3] * iu, p.fmt_act);
+    }
+    if constexpr (NC == 16) {
+      *reinterpret_cast<uint4*>(dh + c0) = make_uint4(qg[0], qg[1], qg[2], qg[3]);
+      *reinterpret_cast<uint4*>(dh + I + c0) = make_uint4(qu[0], qu[1], qu[2], qu[3]);
+    } else {
+      *reinterpret_cast<uint2*>(dh + c0) = make_uint2(qg[0], qg[1]);
+      *reinterpret_cast<uint2*>(dh + I + c0) = make_uint2(qu[0], qu[1]);
+    }
+    if (sub == 0) {
       p.dh_sf[sf_tiled_offset(prow, i0, 2 * (int64_t)I)] = (uint8_t)bg;
       p.dh_sf[sf_tiled_offset(prow, I + i0, 2 * (int64_t)I)] = (uint8_t)bu;
     }
   } else {
-    pair_bar(pair_id);  // keep the pair barrier count identical on both paths
+    group_bar<32 * SUBS>(bar_id);  // keep the barrier count identical on both paths
     uint16_t* dh = static_cast<uint16_t*>(p.dh) + prow * (2 * (int64_t)I);
     uint4* dgp = reinterpret_cast<uint4*>(dh + c0);
     uint4* dup = reinterpret_cast<uint4*>(dh + I + c0);
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < NC / 8; ++q) {
       dgp[q] = make_uint4(pack_bf16x2(dg[8 * q + 0], dg[8 * q + 1]), pack_bf16x2(dg[8 * q + 2], dg[8 * q + 3]),
                           pack_bf16x2(dg[8 * q + 4], dg[8 * q + 5]), pack_bf16x2(dg[8 * q + 6], dg[8 * q + 7]));
       dup[q] = make_uint4(pack_bf16x2(du[8 * q + 0], du[8 * q + 1]), pack_bf16x2(du[8 * q + 2], du[8 * q + 3]),
                           pack_bf16x2(du[8 * q + 4], du[8 * q + 5]), pack_bf16x2(du[8 * q + 6], du[8 * q + 7]));
     }
   }
-  store_transposed16<MX>(tbuf, dg, p.dht, p.dht_sf, P, c0, p0, lane, p.fmt_act);
-  store_transposed16<MX>(tbuf + 16 * 33, du, p.dht, p.dht_sf, P, I + c0, p0, lane, p.fmt_act);
-  store_transposed16<MX>(tbuf + 2 * 16 * 33, ap, p.apt, p.apt_sf, P, c0, p0, lane, p.fmt_act);
+  store_transposed<MX, NC>(tbuf, dg, p.dht, p.dht_sf, P, c0, p0, lane, p.fmt_act);
+  store_transposed<MX, NC>(tbuf + NC * 33, du, p.dht, p.dht_sf, P, I + c0, p0, lane, p.fmt_act);
+  store_transposed<MX, NC>(tbuf + 2 * NC * 33, ap, p.apt, p.apt_sf, P, c0, p0, lane, p.fmt_act);
 }
 
 
@@ -503,9 +533,9 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
     // ---------------- epilogue warps 2..5 ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int m = 32 * q + lane;
-    const int half = (warp - 2) >> 2;  // dSwiGLU: which 16 of every 32 columns; TMA store: which half
+    const int half = (warp - 2) >> 2;  // dSwiGLU: column slice of every 32 columns; staged: which half
     uint8_t* wsm = smEPI + (warp - 2) * C::EPI_WARP_BYTES;
-    float* xchg = smXchg + q * (2 * 2 * 32);  // + (chunk parity) * 4 * 2 * 2 * 32
+    float* xchg = smXchg + q * C::XCHG_QUARTER;  // + (chunk parity) * 4 * XCHG_QUARTER
     const bool ck_leader = (EPI == kEpiDSwiGLU) && warp == 2 && lane == 0;
     // checkpoint chunk n of the schedule goes to buffer n % 2; ck_issued = chunks issued so far
     int64_t ck_next = 0, ck_issued = 0;
@@ -550,6 +580,13 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       if (ck_leader) {
         if (!ck0_ready) issue_ck(t, 0);
         ck0_ready = false;
+      }
+      // dSwiGLU: the row's flat index and score, loaded while the accumulator is still being computed
+      int row_f = -1;
+      float row_s = 0.f;
+      if constexpr (EPI == kEpiDSwiGLU) {
+        row_f = p.tile_row_flat[(int64_t)ti.mt * 128 + m];
+        if (row_f >= 0) row_s = p.s[row_f];
       }
       const bool got = mbar_wait_bounded(&tfull[acc], aph, p.status, abort_flag);
       if constexpr (EPI == kEpiDSwiGLU || C::STAGED) {
@@ -671,9 +708,8 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         epi_store<BN>(p, ti, taddr, m);
       } else {
         const int64_t prow = (int64_t)ti.mt * 128 + m;
-        const int f = p.tile_row_flat[prow];
-        const bool valid = f >= 0;
-        const float sv = valid ? p.s[f] : 0.f;
+        const bool valid = row_f >= 0;
+        const float sv = row_s;
         float ds_acc = 0.f;
 #pragma unroll 1
         for (int c = 0; c < C::NCHUNK; ++c) {
@@ -692,15 +728,16 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
           // on a failed wait the chunk is still walked (garbage in, flagged by the status word) so
           // that both warps of a pair reach the same barriers
           mbar_wait_bounded(&ck_full[buf], (uint32_t)((ck_next >> 1) & 1), p.status, abort_flag);
-          epi_dswiglu_half<MX>(p, taddr + c * 32 + half * 16, prow, m, lane, valid, sv, ti.nt * BN + c * 32, half,
-                               reinterpret_cast<const uint16_t*>(smCK + buf * C::CK_CHUNK_BYTES),
-                               reinterpret_cast<float*>(wsm), xchg + (int)(ck_next & 1) * (4 * 2 * 2 * 32), 2 + q,
-                               ds_acc);
+          epi_dswiglu_part<MX, C::G1_NC>(p, taddr + c * 32 + half * C::G1_NC, prow, m, lane, valid, sv,
+                                         ti.nt * BN + c * 32, half,
+                                         reinterpret_cast<const uint16_t*>(smCK + buf * C::CK_CHUNK_BYTES),
+                                         reinterpret_cast<float*>(wsm),
+                                         xchg + (int)(ck_next & 1) * (4 * C::XCHG_QUARTER), 2 + q, ds_acc);
           __syncwarp();
           if (lane == 0) mbar_arrive(&ck_empty[buf]);  // this warp no longer reads the buffer
           ++ck_next;
         }
-        p.ds_part[prow * (int64_t)(2 * (p.I / BN)) + 2 * ti.nt + half] = valid ? ds_acc : 0.f;
+        p.ds_part[prow * (int64_t)(kG1Subs * (p.I / BN)) + kG1Subs * ti.nt + half] = valid ? ds_acc : 0.f;
       }
       tc_fence_before();
       __syncwarp();

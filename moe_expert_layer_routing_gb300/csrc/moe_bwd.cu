@@ -92,7 +92,7 @@ enum Region {
   R_CHUNK_COUNTS, R_EXPERT_OFFSETS, R_BLOCK_OFFSETS, R_TILE_OFFSETS, R_EXPERT_ORDER, R_SCALARS,
   R_X_GATHER, R_S_SCATTER, R_S_REV, R_TPID, R_B2E, R_TILE_ROW_FLAT, R_FLAT_TILE_ROW, R_TILE_EXPERT,
   R_DOUT_G, R_DOUT_G_SF, R_DOUT_GT, R_DOUT_GT_SF, R_X_GT, R_X_GT_SF, R_DH, R_DH_SF, R_DH_T, R_DH_T_SF,
-  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_X_G, R_X_G_SF, R_CKPT, R_PAIR_OFFSETS, R_COUNT
+  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_X_G, R_X_G_SF, R_CKPT, R_PAIR_OFFSETS, R_TILE_ORDER, R_COUNT
 };
 
 struct Layout {
@@ -168,10 +168,11 @@ static Layout make_layout(const MoeBwdArgs& a) {
     b[R_AP_T_SF] = (size_t)(I * P / 32);
   }
   b[R_DX_EXP] = (size_t)(P * H * 2);
-  b[R_DS_PART] = sizeof(float) * (size_t)(P * 2 * (I / L.BN1));  // two column halves per N tile
+  b[R_DS_PART] = sizeof(float) * (size_t)(P * kG1Subs * (I / L.BN1));  // one partial per column slice and N tile
   b[R_DS_BIAS] = a.has_bias ? sizeof(float) * (size_t)P : 0;
   b[R_COUNTERS] = 64;  // one tile counter per grouped GEMM
   b[R_PAIR_OFFSETS] = sizeof(int32_t) * (E + 1);
+  b[R_TILE_ORDER] = sizeof(int32_t) * (size_t)(P / kTileM + 1);
   if (a.act_src == MOE_ACT_RECOMPUTE) {
     b[R_X_G] = (size_t)(P * H * es);
     b[R_X_G_SF] = mx ? (size_t)(P * H / 32) : 0;
@@ -402,6 +403,8 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   r.pair_offsets = reg<int32_t>(L, ws, R_PAIR_OFFSETS);
   r.status = a.status_dev;
   if ((rc = launch_route_meta(a.ids, a.T, a.K, a.E, a.block_size, L.Nb, P, r, st))) return rc;
+  int32_t* tile_order = reg<int32_t>(L, ws, R_TILE_ORDER);
+  if ((rc = launch_tile_order(tile_row_flat, scalars + 1, a.T, a.K, tile_order, st))) return rc;
   prof_mark(st, slot, 1);
 
   // 2. gathered / transposed / quantised activation operands
@@ -413,6 +416,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   pa.tile_row_flat = tile_row_flat;
   pa.tile_expert = tile_expert;
   pa.num_tiles = scalars + 1;
+  pa.tile_order = getenv("MOEBWD_PREP_ORDER") && getenv("MOEBWD_PREP_ORDER")[0] == '0' ? nullptr : tile_order;
   pa.H = a.H;
   pa.K = a.K;
   pa.P = P;
@@ -579,7 +583,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   if ((rc = launch_dx_scatter_sum(reg<uint16_t>(L, ws, R_DX_EXP), flat_tile_row, a.T, a.K, a.H,
                                   static_cast<uint16_t*>(a.dx), st)))
     return rc;
-  if ((rc = launch_ds_finalize(reg<float>(L, ws, R_DS_PART), (int)(2 * (I / L.BN1)), a.has_bias ? reg<float>(L, ws, R_DS_BIAS) : nullptr,
+  if ((rc = launch_ds_finalize(reg<float>(L, ws, R_DS_PART), (int)(kG1Subs * (I / L.BN1)), a.has_bias ? reg<float>(L, ws, R_DS_BIAS) : nullptr,
                                flat_tile_row, TK, a.ds, st)))
     return rc;
   if (a.has_bias) {

@@ -54,6 +54,9 @@ struct RouteBufs {
   int32_t* status;
 };
 int route_nchunks(int64_t TK);
+// order[0..num_tiles) = tiles sorted (bucketed) by the token of their first row
+int launch_tile_order(const int32_t* tile_row_flat, const int32_t* num_tiles, int T, int K, int32_t* order,
+                      cudaStream_t st);
 int launch_route_meta(const int32_t* ids, int T, int K, int E, int B, int64_t Nb, int64_t P,
                       const RouteBufs& r, cudaStream_t st);
 
@@ -68,6 +71,7 @@ struct PrepArgs {
   const int32_t* tile_row_flat;
   const int32_t* tile_expert;
   const int32_t* num_tiles;  // device scalar
+  const int32_t* tile_order; // nullable: processing order of the tiles (CTA i takes tile_order[i])
   int H, K;
   int64_t P;                 // tile-row capacity (leading dim of transposed outputs)
   int mx, fmt, scale_t;      // MXFP8 outputs; fp8 format; multiply dout^T by s (affinity on H)
@@ -91,6 +95,13 @@ int launch_quant_colwise(const uint16_t* in, int64_t src_rows, int64_t rows, int
 // ------------------------------------------------------------------------------------------
 enum GemmMode { kMGrouped = 0, kKGrouped = 1 };
 enum EpiKind { kEpiStore = 0, kEpiDSwiGLU = 1, kEpiCkpt = 2 };
+// dSwiGLU epilogue (G1): warps per TMEM lane quarter; each takes 32 / kG1Subs of every 32 columns
+// and writes one ds partial per (row, N tile).
+#ifndef MOEBWD_G1_SUBS
+#define MOEBWD_G1_SUBS 2
+#endif
+constexpr int kG1Subs = MOEBWD_G1_SUBS;
+static_assert(kG1Subs == 2 || kG1Subs == 4, "G1 epilogue warps per lane quarter");
 
 struct GemmParams {
   int mode;
@@ -125,7 +136,7 @@ struct GemmParams {
   void* dh; uint8_t* dh_sf;
   void* dht; uint8_t* dht_sf;
   void* apt; uint8_t* apt_sf;
-  float* ds_part;               // [P, 2*I/BN]
+  float* ds_part;               // [P, kG1Subs*I/BN]
   // CTA-pair kernel, M-grouped: expert e's 128-row tiles form ceil(tiles_e / 2) pairs; pair_offsets
   // [E+1] is their prefix (null: one expert, pairs of consecutive tiles), num_pairs its device total
   const int32_t* pair_offsets;

@@ -28,8 +28,8 @@ constexpr int kPrepSmem = 128 * kPrepTilePitch * 2;
 // bf16, per output row).
 template <bool MX, bool SCALE_T, bool BIAS>
 __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
-  const int tile = blockIdx.x;
-  if (tile >= *a.num_tiles) return;
+  if ((int)blockIdx.x >= *a.num_tiles) return;
+  const int tile = a.tile_order ? a.tile_order[blockIdx.x] : (int)blockIdx.x;
   extern __shared__ uint4 prep_smem[];
   uint16_t* st = reinterpret_cast<uint16_t*>(prep_smem);
   __shared__ int32_t s_tok[128];

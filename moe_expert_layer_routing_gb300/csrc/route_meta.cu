@@ -202,6 +202,39 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter_kernel(
   }
 }
 
+// Order of the 128-row tiles by the token of their first row (a counting sort over token buckets,
+// one CTA).  A pass that gathers token rows tile by tile in this order keeps the tokens its
+// concurrently running tiles read within a narrow window, so the K reads of a token row mostly hit
+// L2.  The order inside a bucket is arbitrary; it only changes the processing order.
+constexpr int kOrderBuckets = 4096;
+__global__ void __launch_bounds__(1024) tile_order_kernel(const int32_t* __restrict__ tile_row_flat,
+                                                          const int32_t* __restrict__ num_tiles, int T, int K,
+                                                          int32_t* __restrict__ order) {
+  __shared__ int32_t cnt[kOrderBuckets];
+  __shared__ int32_t wt[33];
+  const int n = *num_tiles;
+  for (int b = threadIdx.x; b < kOrderBuckets; b += blockDim.x) cnt[b] = 0;
+  __syncthreads();
+  auto bucket = [&](int j) {
+    const int f = tile_row_flat[(int64_t)j * kTileM];  // first row of a tile is always routed
+    const int64_t t = f >= 0 ? f / K : 0;
+    return (int)(t * kOrderBuckets / T);
+  };
+  for (int j = threadIdx.x; j < n; j += blockDim.x) atomicAdd(&cnt[bucket(j)], 1);
+  __syncthreads();
+  block_exclusive_scan(cnt, kOrderBuckets, wt);
+  __syncthreads();
+  for (int j = threadIdx.x; j < n; j += blockDim.x) order[atomicAdd(&cnt[bucket(j)], 1)] = j;
+}
+
+int launch_tile_order(const int32_t* tile_row_flat, const int32_t* num_tiles, int T, int K, int32_t* order,
+                      cudaStream_t st) {
+  if (T <= 0) return MOE_OK;
+  tile_order_kernel<<<1, 1024, 0, st>>>(tile_row_flat, num_tiles, T, K, order);
+  count_launch();
+  return cuda_check(cudaGetLastError(), "tile_order");
+}
+
 int launch_route_meta(const int32_t* ids, int T, int K, int E, int B, int64_t Nb, int64_t P, const RouteBufs& r,
                       cudaStream_t st) {
   const int64_t TK = (int64_t)T * K;
