@@ -147,6 +147,32 @@ def test_mxfp8_quantised_operands_match_oracle_codes():
     assert np.array_equal(q, rq) and np.array_equal(sf, rs)
 
 
+@pytest.mark.parametrize("affinity", [AFFINITY_ON_I, AFFINITY_ON_H])
+def test_mxfp8_transposed_operands_match_oracle_codes(affinity):
+    """The token-quantised transposed operands of the weight-gradient GEMMs (x_g^T for dW1, dout_g^T
+    for dW2, s-scaled in fp32 for affinity on H) are bit-exact: codes and scales of groups of 32 tile
+    rows, against the oracle's quantisation along the row axis."""
+    cfg = small_moe("mx_tcodes", T=300, H=384, I=256, E=5, K=2, B=256, seed=34, precision=PREC_MXFP8,
+                    affinity=affinity)
+    inp = with_ids(make_moe_inputs(cfg), _ragged_ids(300, 2, 5, seed=4, empty=(0,), single=(1,), hot=2))
+    op, got = run_gpu(inp)
+    P = op.tile_rows
+    used = int(op.region("TILE_OFFSETS").view(torch.int32)[cfg.E].item())
+    flat = op.region("TILE_ROW_FLAT").view(torch.int32).cpu().numpy()[:used]
+    valid = flat >= 0
+    t, k = np.where(valid, flat // cfg.K, 0), np.where(valid, flat % cfg.K, 0)
+    xrows = np.where(valid[:, None], inp.x.double().numpy()[t], 0.0)
+    drows = np.where(valid[:, None], inp.dout.double().numpy()[t], 0.0)
+    if affinity == AFFINITY_ON_H:  # s * dout rounded to fp32, as the kernel computes it
+        drows = (drows * inp.s.double().numpy()[t, k][:, None]).astype(np.float32).astype(np.float64)
+    for name, rows in (("X_GT", xrows), ("DOUT_GT", drows)):
+        rq, rs = omx.mx_quantize(rows, cfg.fp8_act, axis=0)
+        q = op.region(name).cpu().numpy().reshape(cfg.H, P)[:, :used].T
+        sf = tiled_sf_to_plain(op.region(name + "_SF").cpu().numpy(), cfg.H, P)[:, :used // 32].T
+        assert np.array_equal(q, rq), name
+        assert np.array_equal(sf, rs), name
+
+
 def test_linear_bwd_small_both_precisions():
     import moe_expert_layer_routing_gb300 as mb
     inp = make_linear_inputs(LinearConfig("lin_small", M=256, N=384, K=512, seed=41))
