@@ -193,9 +193,9 @@ __device__ __forceinline__ void tile_ckpt_origin(const GemmParams& p, const Tile
 // column l % NC, rows NC*(l / NC) .. +NC-1, so output row row0 + l % NC gets columns p0..p0+31 from
 // 32/NC lanes (bf16, or fp8 codes with one scale quantised along all 32: those lanes combine their
 // amax).
-template <bool MX, int NC>
+template <bool MX, int NC, int AF>
 __device__ __forceinline__ void store_transposed(float* buf, const float (&v)[NC], void* out, uint8_t* sf,
-                                                 int64_t P, int64_t row0, int64_t p0, int lane, int fmt) {
+                                                 int64_t P, int64_t row0, int64_t p0, int lane) {
 #pragma unroll
   for (int j = 0; j < NC; ++j) buf[j * 33 + lane] = v[j];
   __syncwarp();
@@ -209,18 +209,22 @@ __device__ __forceinline__ void store_transposed(float* buf, const float (&v)[NC
     for (int i = 0; i < NC; ++i) am = fmaxf(am, fabsf(col[i]));
 #pragma unroll
     for (int o = NC; o < 32; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    const uint32_t byte = e8m0_byte(__float_as_uint(am), fmt);
+    const uint32_t byte = e8m0_byte(__float_as_uint(am), AF);
     const float inv = e8m0_inv_scale(byte);
     uint32_t q[NC / 4];
 #pragma unroll
     for (int w = 0; w < NC / 4; ++w)
-      q[w] = fp8x4(col[4 * w] * inv, col[4 * w + 1] * inv, col[4 * w + 2] * inv, col[4 * w + 3] * inv, fmt);
+      q[w] = fp8x4_t<AF, false>(col[4 * w] * inv, col[4 * w + 1] * inv, col[4 * w + 2] * inv, col[4 * w + 3] * inv);
     uint8_t* dst = static_cast<uint8_t*>(out) + (row0 + c) * P + p0 + rg * NC;
     if constexpr (NC == 16)
       *reinterpret_cast<uint4*>(dst) = make_uint4(q[0], q[1], q[2], q[3]);
     else
       *reinterpret_cast<uint2*>(dst) = make_uint2(q[0], q[1]);
-    if (rg == 0) sf[sf_tiled_offset(row0 + c, p0, P)] = (uint8_t)byte;
+    if (rg == 0) {  // tiled scale layout of the [rows, P] operand (see sf_tiled_offset)
+      const int64_t r = row0 + c;
+      sf[((r >> 7) * (P >> 7) + (p0 >> 7)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + ((p0 >> 5) & 3)] =
+          (uint8_t)byte;
+    }
   } else {
     uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (row0 + c) * P + p0 + rg * NC);
 #pragma unroll
@@ -244,7 +248,7 @@ __device__ __forceinline__ void group_bar(int id) {
 // MXFP8 groups of dh (32 features) span the 32/NC warps of a TMEM lane quarter: partial amax values
 // are exchanged through `xchg` ([slice][gate|up][32 lanes]) with a barrier over those warps.
 // Padding rows produce zeros.
-template <bool MX, int NC>
+template <bool MX, int NC, int AF>
 __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t taddr, int64_t prow, int m, int lane,
                                                  bool valid, float sv, int i0, int sub, const uint16_t* ck,
                                                  float* tbuf, float* xchg, int bar_id, float& ds_acc) {
@@ -299,13 +303,13 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
       amu = fmaxf(amu, xchg[(o * 2 + 1) * 32 + lane]);
     }
     uint8_t* dh = static_cast<uint8_t*>(p.dh) + prow * (2 * (int64_t)I);
-    const uint32_t bg = e8m0_byte(__float_as_uint(amg), p.fmt_act), bu = e8m0_byte(__float_as_uint(amu), p.fmt_act);
+    const uint32_t bg = e8m0_byte(__float_as_uint(amg), AF), bu = e8m0_byte(__float_as_uint(amu), AF);
     const float ig = e8m0_inv_scale(bg), iu = e8m0_inv_scale(bu);
     uint32_t qg[NC / 4], qu[NC / 4];
 #pragma unroll
     for (int w = 0; w < NC / 4; ++w) {
-      qg[w] = fp8x4(dg[4 * w] * ig, dg[4 * w + 1] * ig, dg[4 * w + 2] * ig, dg[4 * w + 3] * ig, p.fmt_act);
-      qu[w] = fp8x4(du[4 * w] * iu, du[4 * w + 1] * iu, du[4 * w + 2] * iu, du[4 * w + 3] * iu, p.fmt_act);
+      qg[w] = fp8x4_t<AF, false>(dg[4 * w] * ig, dg[4 * w + 1] * ig, dg[4 * w + 2] * ig, dg[4 * w + 3] * ig);
+      qu[w] = fp8x4_t<AF, false>(du[4 * w] * iu, du[4 * w + 1] * iu, du[4 * w + 2] * iu, du[4 * w + 3] * iu);
     }
     if constexpr (NC == 16) {
       *reinterpret_cast<uint4*>(dh + c0) = make_uint4(qg[0], qg[1], qg[2], qg[3]);
@@ -331,9 +335,9 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
                           pack_bf16x2(du[8 * q + 4], du[8 * q + 5]), pack_bf16x2(du[8 * q + 6], du[8 * q + 7]));
     }
   }
-  store_transposed<MX, NC>(tbuf, dg, p.dht, p.dht_sf, P, c0, p0, lane, p.fmt_act);
-  store_transposed<MX, NC>(tbuf + NC * 33, du, p.dht, p.dht_sf, P, I + c0, p0, lane, p.fmt_act);
-  store_transposed<MX, NC>(tbuf + 2 * NC * 33, ap, p.apt, p.apt_sf, P, c0, p0, lane, p.fmt_act);
+  store_transposed<MX, NC, AF>(tbuf, dg, p.dht, p.dht_sf, P, c0, p0, lane);
+  store_transposed<MX, NC, AF>(tbuf + NC * 33, du, p.dht, p.dht_sf, P, I + c0, p0, lane);
+  store_transposed<MX, NC, AF>(tbuf + 2 * NC * 33, ap, p.apt, p.apt_sf, P, c0, p0, lane);
 }
 
 
@@ -663,17 +667,21 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         // time through the staging slab while the next tile's MMAs run.
         uint32_t pk[BN / 64][16];
 #pragma unroll
-        for (int sl = 0; sl < BN / 64; ++sl) {
-          uint32_t r[32];
+        for (int sl = 0; sl < BN / 64; sl += 2) {  // two loads in flight per wait
+          uint32_t r[2][32];
           if (ti.nk > 0) {
-            tmem_ld_32x32b_x32(taddr + (sl * 2 + half) * 32, r);
+            tmem_ld_32x32b_x32(taddr + (sl * 2 + half) * 32, r[0]);
+            tmem_ld_32x32b_x32(taddr + ((sl + 1) * 2 + half) * 32, r[1]);
             tmem_ld_wait();
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = 0u;
+            for (int j = 0; j < 32; ++j) r[0][j] = r[1][j] = 0u;
           }
 #pragma unroll
-          for (int j = 0; j < 16; ++j) pk[sl][j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[sl + u][j] = pack_bf16x2(__uint_as_float(r[u][2 * j]), __uint_as_float(r[u][2 * j + 1]));
         }
         tc_fence_before();
         __syncwarp();
@@ -728,11 +736,18 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
           // on a failed wait the chunk is still walked (garbage in, flagged by the status word) so
           // that both warps of a pair reach the same barriers
           mbar_wait_bounded(&ck_full[buf], (uint32_t)((ck_next >> 1) & 1), p.status, abort_flag);
-          epi_dswiglu_part<MX, C::G1_NC>(p, taddr + c * 32 + half * C::G1_NC, prow, m, lane, valid, sv,
-                                         ti.nt * BN + c * 32, half,
-                                         reinterpret_cast<const uint16_t*>(smCK + buf * C::CK_CHUNK_BYTES),
-                                         reinterpret_cast<float*>(wsm),
-                                         xchg + (int)(ck_next & 1) * (4 * C::XCHG_QUARTER), 2 + q, ds_acc);
+          {
+            const uint32_t ta = taddr + c * 32 + half * C::G1_NC;
+            const int i0 = ti.nt * BN + c * 32;
+            const uint16_t* ckb = reinterpret_cast<const uint16_t*>(smCK + buf * C::CK_CHUNK_BYTES);
+            float* xc = xchg + (int)(ck_next & 1) * (4 * C::XCHG_QUARTER);
+            if (!MX || p.fmt_act == MOE_FP8_E5M2)  // the activation format, fixed per instantiation
+              epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2>(p, ta, prow, m, lane, valid, sv, i0, half, ckb,
+                                                          reinterpret_cast<float*>(wsm), xc, 2 + q, ds_acc);
+            else
+              epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3>(p, ta, prow, m, lane, valid, sv, i0, half, ckb,
+                                                          reinterpret_cast<float*>(wsm), xc, 2 + q, ds_acc);
+          }
           __syncwarp();
           if (lane == 0) mbar_arrive(&ck_empty[buf]);  // this warp no longer reads the buffer
           ++ck_next;

@@ -65,6 +65,25 @@ __device__ __forceinline__ uint32_t fp8x4(float a, float b, float c, float d, in
   return mag | (w & nonzero);
 }
 
+// fp8x4 with the format fixed at compile time; CANON = false keeps the sign of codes that round to
+// zero (a -0 code, numerically zero for the tensor cores that consume it).
+template <int FMT, bool CANON>
+__device__ __forceinline__ uint32_t fp8x4_t(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  if constexpr (FMT == MOE_FP8_E4M3) {
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  } else {
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  }
+  const uint32_t w = (uint32_t)lo | ((uint32_t)hi << 16);
+  if constexpr (!CANON) return w;
+  const uint32_t mag = w & 0x7F7F7F7Fu;
+  const uint32_t nonzero = (mag + 0x7F7F7F7Fu) & 0x80808080u;
+  return mag | (w & nonzero);
+}
+
 // Quantise 32 values of one group into 32 FP8 codes (packed little-endian into 8 words) and
 // return the scale byte.
 __device__ __forceinline__ uint32_t quantize_group32(const float (&v)[32], int fmt, uint32_t (&w)[8]) {
@@ -76,6 +95,20 @@ __device__ __forceinline__ uint32_t quantize_group32(const float (&v)[32], int f
 #pragma unroll
   for (int j = 0; j < 8; ++j)
     w[j] = fp8x4(v[4 * j] * inv, v[4 * j + 1] * inv, v[4 * j + 2] * inv, v[4 * j + 3] * inv, fmt);
+  return byte;
+}
+
+// quantize_group32 with the format fixed at compile time (canonical +0 codes).
+template <int FMT>
+__device__ __forceinline__ uint32_t quantize_group32_t(const float (&v)[32], uint32_t (&w)[8]) {
+  float am = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) am = fmaxf(am, fabsf(v[j]));
+  const uint32_t byte = e8m0_byte(__float_as_uint(am), FMT);
+  const float inv = e8m0_inv_scale(byte);
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    w[j] = fp8x4_t<FMT, true>(v[4 * j] * inv, v[4 * j + 1] * inv, v[4 * j + 2] * inv, v[4 * j + 3] * inv);
   return byte;
 }
 

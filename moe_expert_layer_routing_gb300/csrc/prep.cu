@@ -26,7 +26,7 @@ constexpr int kPrepSmem = 128 * kPrepTilePitch * 2;
 // dout_g chunk and stages the tile in shared memory; phase 2, each thread owns one column and
 // writes its four 32-row groups of the transposed output (128 contiguous bytes for fp8, 256 for
 // bf16, per output row).
-template <bool MX, bool SCALE_T, bool BIAS>
+template <bool MX, bool SCALE_T, bool BIAS, int AF>
 __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
   if ((int)blockIdx.x >= *a.num_tiles) return;
   const int tile = a.tile_order ? a.tile_order[blockIdx.x] : (int)blockIdx.x;
@@ -96,11 +96,11 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
           am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
           am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
           if (!colok) continue;
-          const uint32_t byte = e8m0_byte(__float_as_uint(am), a.fmt);
+          const uint32_t byte = e8m0_byte(__float_as_uint(am), AF);
           const float inv = e8m0_inv_scale(byte);
           uint2 q;
-          q.x = fp8x4(d8[0] * inv, d8[1] * inv, d8[2] * inv, d8[3] * inv, a.fmt);
-          q.y = fp8x4(d8[4] * inv, d8[5] * inv, d8[6] * inv, d8[7] * inv, a.fmt);
+          q.x = fp8x4_t<AF, true>(d8[0] * inv, d8[1] * inv, d8[2] * inv, d8[3] * inv);
+          q.y = fp8x4_t<AF, true>(d8[4] * inv, d8[5] * inv, d8[6] * inv, d8[7] * inv);
           *reinterpret_cast<uint2*>(static_cast<uint8_t*>(rowdst) + prow * H + col) = q;
           if ((lane & 3) == 0) rowsf[sf_tiled_offset(prow, col, H)] = (uint8_t)byte;
         } else {
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
           const int64_t ocol = prow0 + g * 32;
           if constexpr (MX) {
             uint32_t w[8];
-            const uint32_t byte = quantize_group32(c32, a.fmt, w);
+            const uint32_t byte = quantize_group32_t<AF>(c32, w);
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(outp) + orow * P + ocol);
             dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
             dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -158,7 +158,8 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
 
 template <bool MX, bool SCALE_T, bool BIAS>
 static int prep_launch(const PrepArgs& a, int grid, cudaStream_t st) {
-  auto k = prep_kernel<MX, SCALE_T, BIAS>;
+  auto k = (!MX || a.fmt == MOE_FP8_E5M2) ? prep_kernel<MX, SCALE_T, BIAS, MOE_FP8_E5M2>
+                                          : prep_kernel<MX, SCALE_T, BIAS, MOE_FP8_E4M3>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e != cudaSuccess) return cuda_check(e, "prep attribute");
   k<<<grid, 256, kPrepSmem, st>>>(a);
