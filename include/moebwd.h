@@ -189,7 +189,9 @@ typedef struct MoeBwdArgs {
   const uint8_t* W2_sf; /*          its scales, MOE_SF_TILED for the [E*I, H] matrix */
   const void* b2;       /* (device) bf16 [E,H] down bias (has_bias) */
   const float* s;       /* (device) fp32 [T,K] routing scores */
-  const int32_t* ids;   /* (device) int32 [T,K] expert ids */
+  const int32_t* ids;   /* (device) int32 [T,K] expert ids; -1 marks an unused slot (a token routed to
+                           fewer than K experts: variable top-K); any other id outside [0,E) is
+                           reported in status_dev (MOE_STATUS_BAD_EXPERT_ID) and skipped */
   const void* gate_up_ckpt; /* (device) bf16 [N,2,I,B] gate/up pre-activation checkpoint in the
                                block layout of moe_route_meta (N = moe_num_blocks_bound):
                                gate of the j-th row of expert e at [blk,0,:,b], up at [blk,1,:,b],
@@ -216,6 +218,12 @@ typedef struct MoeBwdArgs {
                              along H) with fp8_w */
   const uint8_t* W1t_sf;  /*          its scales, MOE_SF_TILED for the [E*2I, H] matrix */
   const void* b1;         /* (device) RECOMPUTE: bf16 [E,2I] gate/up bias added to h, or NULL */
+  float* ds_masked;       /* (device) fp32 [T*E] or NULL: [BW] expert_affinities_masked_grad, ds laid out
+                             over all experts of each token: [t*E + e] = ds of the slot of token t
+                             routed to e (repeated selections add), 0 where e was not selected */
+  const int32_t* num_valid_tokens; /* (device) int32 [1] or NULL: [BW] num_valid_tokens, only the
+                             leading min(n, T) tokens are routed (values <= 0 route none); later
+                             tokens take no part and get zero dx rows and ds / ds_masked entries */
 } MoeBwdArgs;
 
 /* Bytes of workspace moe_bwd needs for these shapes and options (pointers are not read). */

@@ -47,7 +47,7 @@ class MoeBwdArgs(ctypes.Structure):
                 ("x", "dout", "W1", "W2", "W1_q", "W1_sf", "W2_q", "W2_sf", "b2", "s", "ids",
                  "gate_up_ckpt", "dx", "dW1", "dW2", "ds", "db1", "db2", "status_dev", "workspace")] + \
                [("workspace_bytes", ctypes.c_size_t), ("accumulate", ctypes.c_int), ("act_src", ctypes.c_int)] + \
-               [(n, ctypes.c_void_p) for n in ("W1t", "W1t_q", "W1t_sf", "b1")]
+               [(n, ctypes.c_void_p) for n in ("W1t", "W1t_q", "W1t_sf", "b1", "ds_masked", "num_valid_tokens")]
 
 
 _lib = None
@@ -209,7 +209,7 @@ class MoeBwd:
 
     def __init__(self, *, T, H, I, E, K, block_size, precision=PREC_BF16, affinity=AFFINITY_ON_H,
                  fp8_act=FP8_E5M2, fp8_w=FP8_E4M3, has_bias=False, accumulate=False, act_src=ACT_CHECKPOINT,
-                 device="cuda"):
+                 ds_masked=False, device="cuda"):
         self.a = MoeBwdArgs()
         self.a.accumulate = int(bool(accumulate))
         self.a.act_src = int(act_src)
@@ -228,14 +228,17 @@ class MoeBwd:
         self.ds = torch.empty(T, K, dtype=torch.float32, device=dev)
         self.db1 = torch.empty(E, 2 * I, dtype=torch.float32, device=dev) if has_bias else None
         self.db2 = torch.empty(E, H, dtype=torch.float32, device=dev) if has_bias else None
+        self.ds_masked = torch.empty(T * E, dtype=torch.float32, device=dev) if ds_masked else None
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self._keep = []
 
     def bind(self, *, x, dout, s, ids, ckpt=None, W1=None, W2=None, W1_q=None, W1_sf=None, W2_q=None, W2_sf=None,
-             b2=None, W1t=None, W1t_q=None, W1t_sf=None, b1=None):
+             b2=None, W1t=None, W1t_q=None, W1t_sf=None, b1=None, num_valid_tokens=None):
         """ckpt: the [N,2,I,B] checkpoint (act_src ACT_CHECKPOINT).  W1t (bf16 [E,2I,H]) or W1t_q/W1t_sf
         and optionally b1 [E,2I]: the operands of the recomputation (act_src ACT_RECOMPUTE)."""
-        _need_cuda(x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2, W1t, W1t_q, W1t_sf, b1)
+        _need_cuda(x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2, W1t, W1t_q, W1t_sf, b1, num_valid_tokens)
+        if num_valid_tokens is not None:
+            assert num_valid_tokens.dtype == torch.int32 and num_valid_tokens.numel() == 1
         a = self.a
         assert x.dtype == torch.bfloat16 and dout.dtype == torch.bfloat16
         assert s.dtype == torch.float32 and ids.dtype == torch.int32
@@ -251,14 +254,15 @@ class MoeBwd:
             assert b1.dtype == torch.bfloat16 and tuple(b1.shape) == (a.E, 2 * a.I)
         for name, t in dict(x=x, dout=dout, s=s, ids=ids, gate_up_ckpt=ckpt, W1=W1, W2=W2, W1_q=W1_q,
                             W1_sf=W1_sf, W2_q=W2_q, W2_sf=W2_sf, b2=b2, W1t=W1t, W1t_q=W1t_q, W1t_sf=W1t_sf,
-                            b1=b1).items():
+                            b1=b1, num_valid_tokens=num_valid_tokens).items():
             setattr(a, name, None if t is None else t.data_ptr())
-        for name in ("dx", "dW1", "dW2", "ds", "db1", "db2", "status"):
+        for name in ("dx", "dW1", "dW2", "ds", "db1", "db2", "ds_masked", "status"):
             t = getattr(self, name)
             setattr(a, "status_dev" if name == "status" else name, None if t is None else t.data_ptr())
         a.workspace = self.workspace.data_ptr()
         a.workspace_bytes = self.workspace.numel()
-        self._keep = [x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2, W1t, W1t_q, W1t_sf, b1]
+        self._keep = [x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2, W1t, W1t_q, W1t_sf, b1,
+                      num_valid_tokens]
         return self
 
     def run(self, stream=None):
@@ -267,7 +271,7 @@ class MoeBwd:
 
     def outputs(self) -> dict:
         return dict(dx=self.dx, dW1=self.dW1, dW2=self.dW2, ds=self.ds, db1=self.db1, db2=self.db2,
-                    status=self.status)
+                    ds_masked=self.ds_masked, status=self.status)
 
     def region(self, name: str) -> torch.Tensor:
         """Bytes of one workspace region (see MOE_WS_* in include/moebwd.h)."""

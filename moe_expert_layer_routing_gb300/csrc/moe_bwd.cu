@@ -213,6 +213,8 @@ static int check_args(const MoeBwdArgs* a, bool need_ptrs) {
   const bool rec = a->act_src == MOE_ACT_RECOMPUTE;
   if (!need_ptrs) return MOE_OK;
   const void* req[] = {a->x, a->dout, a->s, a->ids, a->dx, a->dW1, a->dW2, a->ds, a->status_dev};
+  if (reinterpret_cast<uintptr_t>(a->num_valid_tokens) & 3)
+    return fail(MOE_ERR_INVALID, "moe_bwd: num_valid_tokens must be 4-byte aligned");
   for (const void* q : req)
     if (!q) return fail(MOE_ERR_INVALID, "moe_bwd: required pointer is null");
   if (!rec && !a->gate_up_ckpt) return fail(MOE_ERR_INVALID, "moe_bwd: gate_up_ckpt is null");
@@ -368,6 +370,9 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
       if ((rc = cuda_check(cudaMemsetAsync(a.db1, 0, (size_t)(E * 2 * I * 4), st), "memset db1"))) return rc;
       if ((rc = cuda_check(cudaMemsetAsync(a.db2, 0, (size_t)(E * H * 4), st), "memset db2"))) return rc;
     }
+    if (a.ds_masked && a.T > 0 &&
+        (rc = cuda_check(cudaMemsetAsync(a.ds_masked, 0, sizeof(float) * (size_t)a.T * E, st), "memset ds_masked")))
+      return rc;
     return MOE_OK;
   }
 
@@ -401,6 +406,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   r.tile_expert = tile_expert;
   r.num_blocks_out = nullptr;
   r.pair_offsets = reg<int32_t>(L, ws, R_PAIR_OFFSETS);
+  r.num_valid = a.num_valid_tokens;
   r.status = a.status_dev;
   if ((rc = launch_route_meta(a.ids, a.T, a.K, a.E, a.block_size, L.Nb, P, r, st))) return rc;
   int32_t* tile_order = reg<int32_t>(L, ws, R_TILE_ORDER);
@@ -585,6 +591,8 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     return rc;
   if ((rc = launch_ds_finalize(reg<float>(L, ws, R_DS_PART), (int)(kG1Subs * (I / L.BN1)), a.has_bias ? reg<float>(L, ws, R_DS_BIAS) : nullptr,
                                flat_tile_row, TK, a.ds, st)))
+    return rc;
+  if (a.ds_masked && (rc = launch_ds_masked(a.ds, a.ids, a.num_valid_tokens, a.T, a.K, a.E, a.ds_masked, st)))
     return rc;
   if (a.has_bias) {
     if ((rc = launch_segment_rowsum(reg<uint16_t>(L, ws, R_DH_T), P, (int)(2 * I), tile_offsets, (int)E, nullptr,

@@ -42,6 +42,7 @@ struct RouteBufs {
   int32_t* expert_order;      // [E] experts by descending row count
   int32_t* scalars;           // [4]: num_blocks, num_tiles, num_pairs
   int32_t* pair_offsets;      // nullable [E+1]: prefix of ceil(tiles_e / 2)
+  const int32_t* num_valid;   // nullable device count: only tokens t < count are routed
   int32_t* x_gather_idx;      // [TK]
   int32_t* s_scatter_idx;     // [TK]
   int32_t* s_reverse;         // [TK]
@@ -166,6 +167,9 @@ int launch_gemm_pair(bool mx, int BN, const GemmParams& p, const void* tmA, cons
 // ------------------------------------------------------------------------------------------
 int launch_dx_scatter_sum(const uint16_t* dx_exp, const int32_t* flat_tile_row, int T, int K, int H,
                           uint16_t* dx, cudaStream_t st);
+// [T*E] masked view of ds: out[t*E + e] = sum of ds[t,k] over the slots k of token t routed to e
+int launch_ds_masked(const float* ds, const int32_t* ids, const int32_t* num_valid, int T, int K, int E, float* out,
+                     cudaStream_t st);
 int launch_ds_finalize(const float* ds_part, int nparts, const float* ds_bias, const int32_t* flat_tile_row,
                        int64_t TK, float* ds, cudaStream_t st);
 // out[e, j] = sum over tile rows p of expert e of buf[j, p] (* w[flat(p)] when w != null)

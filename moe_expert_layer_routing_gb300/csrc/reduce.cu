@@ -109,4 +109,27 @@ int launch_segment_rowsum(const uint16_t* buf, int64_t ld, int R, const int32_t*
   return cuda_check(cudaGetLastError(), "segment_rowsum");
 }
 
+// [BW] expert_affinities_masked_grad: ds laid out over all E experts of each token (zero where the
+// token did not select the expert; repeated selections add).  One thread per token, in slot order.
+__global__ void ds_masked_kernel(const float* __restrict__ ds, const int32_t* __restrict__ ids,
+                                 const int32_t* __restrict__ num_valid, int T, int K, int E, float* __restrict__ out) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  if (num_valid && t >= *num_valid) return;
+  float* row = out + (int64_t)t * E;
+  for (int k = 0; k < K; ++k) {
+    const int e = ids[(int64_t)t * K + k];
+    if (e >= 0 && e < E) row[e] += ds[(int64_t)t * K + k];
+  }
+}
+
+int launch_ds_masked(const float* ds, const int32_t* ids, const int32_t* num_valid, int T, int K, int E, float* out,
+                     cudaStream_t st) {
+  int rc = cuda_check(cudaMemsetAsync(out, 0, sizeof(float) * (size_t)T * E, st), "memset ds_masked");
+  if (rc || T == 0) return rc;
+  ds_masked_kernel<<<(T + 255) / 256, 256, 0, st>>>(ds, ids, num_valid, T, K, E, out);
+  count_launch();
+  return cuda_check(cudaGetLastError(), "ds_masked");
+}
+
 }  // namespace moebwd

@@ -19,19 +19,30 @@ constexpr int kIdsPerWarp = kRouteChunk / kRouteWarps;  // 512
 
 int route_nchunks(int64_t TK) { return (int)((TK + kRouteChunk - 1) / kRouteChunk); }
 
-__global__ void route_count_kernel(const int32_t* __restrict__ ids, int64_t TK, int E,
-                                   int32_t* __restrict__ chunk_counts, int32_t* status) {
+// Slots taking part in the routing: flat index f = t*K + k with t below the valid-token count.
+// An id of -1 marks an unused slot (variable top-K); any other id outside [0, E) is reported.
+__device__ __forceinline__ int64_t live_slots(const int32_t* num_valid, int64_t TK, int K) {
+  if (!num_valid) return TK;
+  const int64_t nv = *num_valid;
+  return nv <= 0 ? 0 : (nv * K < TK ? nv * K : TK);
+}
+
+__global__ void route_count_kernel(const int32_t* __restrict__ ids, int64_t TK, int K, int E,
+                                   const int32_t* __restrict__ num_valid, int32_t* __restrict__ chunk_counts,
+                                   int32_t* status) {
   extern __shared__ int32_t hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
+  const int64_t live = live_slots(num_valid, TK, K);
   const int64_t base = (int64_t)blockIdx.x * kRouteChunk;
   const int64_t end = min(base + (int64_t)kRouteChunk, TK);
   int bad = 0;
   for (int64_t f = base + threadIdx.x; f < end; f += blockDim.x) {
+    if (f >= live) break;
     const int e = ids[f];
     if (e >= 0 && e < E)
       atomicAdd(&hist[e], 1);
-    else
+    else if (e != -1)
       bad = 1;
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, MOE_STATUS_BAD_EXPERT_ID);
@@ -137,7 +148,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter_kernel(
     const int32_t* __restrict__ ids, int64_t TK, int K, int E, int B, const int32_t* __restrict__ chunk_base,
     const int32_t* __restrict__ expert_offsets, const int32_t* __restrict__ block_offsets,
     const int32_t* __restrict__ tile_offsets, int32_t* x_gather_idx, int32_t* s_scatter_idx, int32_t* s_reverse,
-    int32_t* token_position_to_id, int32_t* tile_row_flat, int32_t* flat_tile_row) {
+    int32_t* token_position_to_id, int32_t* tile_row_flat, int32_t* flat_tile_row,
+    const int32_t* __restrict__ num_valid) {
   extern __shared__ int32_t sm[];
   int32_t* wbase = sm;                       // [warps][E]
   int32_t* eo = wbase + kRouteWarps * E;     // [E]
@@ -152,10 +164,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter_kernel(
   }
   __syncthreads();
   const int64_t wbeg = (int64_t)blockIdx.x * kRouteChunk + (int64_t)w * kIdsPerWarp;
+  const int64_t live = live_slots(num_valid, TK, K);
   // pass 1: rows per expert in this warp's slice
   for (int it = 0; it < kIdsPerWarp / 32; ++it) {
     const int64_t f = wbeg + it * 32 + lane;
-    const int e = f < TK ? ids[f] : -1;
+    const int e = f < live ? ids[f] : -1;
     const bool valid = e >= 0 && e < E;
     const int key = valid ? e : -1;
     const unsigned grp = __match_any_sync(0xffffffffu, key);
@@ -177,7 +190,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter_kernel(
   for (int it = 0; it < kIdsPerWarp / 32; ++it) {
     const int64_t f = wbeg + it * 32 + lane;
     const bool in = f < TK;
-    const int e = in ? ids[f] : -1;
+    const int e = f < live ? ids[f] : -1;
     const bool valid = e >= 0 && e < E;
     const int key = valid ? e : -1;
     const unsigned grp = __match_any_sync(0xffffffffu, key);
@@ -252,7 +265,8 @@ int launch_route_meta(const int32_t* ids, int T, int K, int E, int B, int64_t Nb
     return rc;
   const int nch = route_nchunks(TK);
   if (nch > 0) {
-    route_count_kernel<<<nch, kRouteThreads, sizeof(int32_t) * E, st>>>(ids, TK, E, r.chunk_counts, r.status);
+    route_count_kernel<<<nch, kRouteThreads, sizeof(int32_t) * E, st>>>(ids, TK, K, E, r.num_valid, r.chunk_counts,
+                                                                          r.status);
     count_launch();
     if ((rc = cuda_check(cudaGetLastError(), "route_count"))) return rc;
   }
@@ -270,7 +284,7 @@ int launch_route_meta(const int32_t* ids, int T, int K, int E, int B, int64_t Nb
     route_scatter_kernel<<<nch, kRouteThreads, smem, st>>>(ids, TK, K, E, B, r.chunk_counts, r.expert_offsets,
                                                            r.block_offsets, r.tile_offsets, r.x_gather_idx,
                                                            r.s_scatter_idx, r.s_reverse, r.token_position_to_id,
-                                                           r.tile_row_flat, r.flat_tile_row);
+                                                           r.tile_row_flat, r.flat_tile_row, r.num_valid);
     count_launch();
     if ((rc = cuda_check(cudaGetLastError(), "route_scatter"))) return rc;
   }

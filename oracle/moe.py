@@ -107,6 +107,31 @@ def recompute_h(x, W1, ids, b1=None, mxfp8=False, fp8_act=mx.E5M2, fp8_w=mx.E4M3
     return h
 
 
+def ds_masked(ds, ids, E):
+    """[BW] `expert_affinities_masked_grad` [T*E]: the score gradient laid out over all E experts of
+    each token, entry t*E + e = sum of ds[t,k] over the slots k with ids[t,k] = e (the derivative of
+    the loss by the token's affinity for e when those slots share it), zero for experts the token
+    did not select.  Ids outside [0, E) contribute nothing."""
+    ds = _f64(ds)
+    ids = np.asarray(ids)
+    T, K = ids.shape
+    out = np.zeros((T, E))
+    for t in range(T):
+        for k in range(K):
+            if 0 <= ids[t, k] < E:
+                out[t, ids[t, k]] += ds[t, k]
+    return out.reshape(T * E)
+
+
+def valid_token_ids(ids, num_valid):
+    """Routing of a problem whose leading num_valid tokens hold real rows ([BW] `num_valid_tokens`):
+    the slots of later tokens become unused (-1); num_valid <= 0 routes no token, above T all."""
+    ids = np.array(ids, copy=True)
+    n = max(0, min(int(num_valid), ids.shape[0]))
+    ids[n:] = -1
+    return ids
+
+
 def moe_backward(x, dout, W1, W2, s, ids, h, b2=None, with_bias=False):
     """All gradients of the MoE layer in float64 (the BF16 path's reference).
 

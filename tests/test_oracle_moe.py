@@ -268,3 +268,41 @@ def test_recompute_h_is_the_forward_preactivation():
     r0 = om.recompute_h(x, W1, ids)
     err = np.linalg.norm(rq - r0) / np.linalg.norm(r0)
     assert 1e-3 < err < 0.15
+
+
+def test_ds_masked_is_the_gradient_of_the_masked_affinities():
+    """[T*E] affinity gradient: finite differences of <dout, out> by the affinity A[t,e] that every
+    slot of token t routed to e carries (two slots of one token share an expert here); zero where
+    no slot selects e."""
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=5, H=6, I=3, E=4, K=3, seed=31)
+    ids[2] = [1, 1, 3]  # a repeated selection
+    g = _grads(x, dout, W1, b1, W2, b2, s, ids)
+    m = om.ds_masked(g["ds"], ids, 4).reshape(5, 4)
+    eps = 1e-6
+    for t in range(5):
+        for e in range(4):
+            sel = ids[t] == e
+            sp, sm = s.copy(), s.copy()
+            sp[t, sel] += eps
+            sm[t, sel] -= eps
+            fp = np.sum(dout * om.moe_forward(x, W1, b1, W2, b2, sp, ids)[0])
+            fm = np.sum(dout * om.moe_forward(x, W1, b1, W2, b2, sm, ids)[0])
+            assert abs((fp - fm) / (2 * eps) - m[t, e]) < 1e-7, (t, e)
+            if not sel.any():
+                assert m[t, e] == 0.0
+
+
+def test_num_valid_tokens_equals_the_truncated_problem():
+    """Routing only the leading n tokens gives the gradients of the n-token problem, with zero dx
+    rows and ds entries for the others."""
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=9, H=8, I=4, E=3, K=2, seed=32)
+    n = 5
+    v = om.valid_token_ids(ids, n)
+    full = _grads(x, dout, W1, b1, W2, b2, s, v)
+    part = _grads(x[:n], dout[:n], W1, b1, W2, b2, s[:n], ids[:n])
+    for name in ("dW1", "dW2", "db1", "db2"):
+        assert np.allclose(full[name], part[name], rtol=0, atol=1e-12), name
+    assert np.allclose(full["dx"][:n], part["dx"]) and np.all(full["dx"][n:] == 0)
+    assert np.allclose(full["ds"][:n], part["ds"]) and np.all(full["ds"][n:] == 0)
+    assert np.array_equal(om.valid_token_ids(ids, 0), np.full_like(ids, -1))
+    assert np.array_equal(om.valid_token_ids(ids, 100), ids)
