@@ -75,6 +75,13 @@ enum { MOE_SF_PLAIN = 0, MOE_SF_TILED = 1 };
  *             checkpoint of the same layout in the workspace, rounded to bf16 like the stored one.
  *             Costs 4*T*K*H*I extra FLOPs and saves the caller the [N,2,I,B] tensor. */
 enum { MOE_ACT_CHECKPOINT = 0, MOE_ACT_RECOMPUTE = 1 };
+/* Gated activation a = act(gate) * up (sonic-moe `activation_type`): SwiGLU act = SiLU, GeGLU
+ * act = GELU with the exact normal CDF, GELU(z) = z * Phi(z). */
+enum { MOE_GLU_SWIGLU = 0, MOE_GLU_GEGLU = 1 };
+/* Column layout of gate and up in W1 [E,H,2I] (and in dW1, db1): CONCAT gate_i at i, up_i at I + i;
+ * INTERLEAVED gate_i at 2i, up_i at 2i + 1 (sonic-moe's interleaved gate/up layout).  The
+ * checkpoint [N,2,I,B] and W1t (recomputation) keep gate and up apart in either case. */
+enum { MOE_GATE_UP_CONCAT = 0, MOE_GATE_UP_INTERLEAVED = 1 };
 
 /* Message of the last failed call on this host thread ("" if none). */
 const char* moe_last_error(void);
@@ -213,17 +220,20 @@ typedef struct MoeBwdArgs {
   int act_src;            /* MOE_ACT_CHECKPOINT (gate_up_ckpt read) or MOE_ACT_RECOMPUTE (gate_up_ckpt
                              unused, may be NULL; the fields below are read) */
   const void* W1t;        /* (device) RECOMPUTE, BF16: bf16 [E,2I,H], W1 with each expert's block
-                             transposed (row j of expert e = column j of W1[e]) */
+                             transposed, rows [gate | up] (row j of expert e = column j of the
+                             concat-layout W1[e], whatever gate_up_layout) */
   const uint8_t* W1t_q;   /* (device) RECOMPUTE, MXFP8: W1t as [E*2I, H] quantised ROWWISE (groups
                              along H) with fp8_w */
   const uint8_t* W1t_sf;  /*          its scales, MOE_SF_TILED for the [E*2I, H] matrix */
-  const void* b1;         /* (device) RECOMPUTE: bf16 [E,2I] gate/up bias added to h, or NULL */
+  const void* b1;         /* (device) RECOMPUTE: bf16 [E,2I] gate/up bias added to h ([gate | up]), or NULL */
   float* ds_masked;       /* (device) fp32 [T*E] or NULL: [BW] expert_affinities_masked_grad, ds laid out
                              over all experts of each token: [t*E + e] = ds of the slot of token t
                              routed to e (repeated selections add), 0 where e was not selected */
   const int32_t* num_valid_tokens; /* (device) int32 [1] or NULL: [BW] num_valid_tokens, only the
                              leading min(n, T) tokens are routed (values <= 0 route none); later
                              tokens take no part and get zero dx rows and ds / ds_masked entries */
+  int glu;                /* MOE_GLU_SWIGLU (default 0) or MOE_GLU_GEGLU */
+  int gate_up_layout;     /* MOE_GATE_UP_CONCAT (default 0) or MOE_GATE_UP_INTERLEAVED */
 } MoeBwdArgs;
 
 /* Bytes of workspace moe_bwd needs for these shapes and options (pointers are not read). */

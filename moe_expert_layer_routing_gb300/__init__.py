@@ -21,6 +21,8 @@ QUANT_ROWWISE, QUANT_COLWISE = 0, 1
 SF_PLAIN, SF_TILED = 0, 1
 STATUS_BAD_EXPERT_ID, STATUS_TIMEOUT = 1, 2
 ACT_CHECKPOINT, ACT_RECOMPUTE = 0, 1
+GLU_SWIGLU, GLU_GEGLU = 0, 1
+GATE_UP_CONCAT, GATE_UP_INTERLEAVED = 0, 1
 
 WS_REGIONS = ["EXPERT_OFFSETS", "TILE_OFFSETS", "BLOCK_OFFSETS", "TILE_ROW_FLAT", "FLAT_TILE_ROW",
               "DOUT_G", "DOUT_G_SF", "DOUT_GT", "DOUT_GT_SF", "X_GT", "X_GT_SF", "DH", "DH_SF",
@@ -47,7 +49,8 @@ class MoeBwdArgs(ctypes.Structure):
                 ("x", "dout", "W1", "W2", "W1_q", "W1_sf", "W2_q", "W2_sf", "b2", "s", "ids",
                  "gate_up_ckpt", "dx", "dW1", "dW2", "ds", "db1", "db2", "status_dev", "workspace")] + \
                [("workspace_bytes", ctypes.c_size_t), ("accumulate", ctypes.c_int), ("act_src", ctypes.c_int)] + \
-               [(n, ctypes.c_void_p) for n in ("W1t", "W1t_q", "W1t_sf", "b1", "ds_masked", "num_valid_tokens")]
+               [(n, ctypes.c_void_p) for n in ("W1t", "W1t_q", "W1t_sf", "b1", "ds_masked", "num_valid_tokens")] + \
+               [(n, ctypes.c_int) for n in ("glu", "gate_up_layout")]
 
 
 _lib = None
@@ -209,8 +212,10 @@ class MoeBwd:
 
     def __init__(self, *, T, H, I, E, K, block_size, precision=PREC_BF16, affinity=AFFINITY_ON_H,
                  fp8_act=FP8_E5M2, fp8_w=FP8_E4M3, has_bias=False, accumulate=False, act_src=ACT_CHECKPOINT,
-                 ds_masked=False, device="cuda"):
+                 ds_masked=False, glu=GLU_SWIGLU, gate_up_layout=GATE_UP_CONCAT, device="cuda"):
         self.a = MoeBwdArgs()
+        self.a.glu = int(glu)
+        self.a.gate_up_layout = int(gate_up_layout)
         self.a.accumulate = int(bool(accumulate))
         self.a.act_src = int(act_src)
         for k, v in dict(T=T, H=H, I=I, E=E, K=K, block_size=block_size, precision=precision,

@@ -190,12 +190,12 @@ __device__ __forceinline__ void tile_ckpt_origin(const GemmParams& p, const Tile
 
 // Transposed store of NC columns x 32 rows (NC = 8 or 16): v[j] of lane r is element (r, j).  The
 // block is transposed through shared memory as fp32 (pitch 33, conflict free); lane l then handles
-// column l % NC, rows NC*(l / NC) .. +NC-1, so output row row0 + l % NC gets columns p0..p0+31 from
-// 32/NC lanes (bf16, or fp8 codes with one scale quantised along all 32: those lanes combine their
-// amax).
+// column l % NC, rows NC*(l / NC) .. +NC-1, so output row row0 + (l % NC) * rstride gets columns
+// p0..p0+31 from 32/NC lanes (bf16, or fp8 codes with one scale quantised along all 32: those lanes
+// combine their amax).
 template <bool MX, int NC, int AF>
 __device__ __forceinline__ void store_transposed(float* buf, const float (&v)[NC], void* out, uint8_t* sf,
-                                                 int64_t P, int64_t row0, int64_t p0, int lane) {
+                                                 int64_t P, int64_t row0, int rstride, int64_t p0, int lane) {
 #pragma unroll
   for (int j = 0; j < NC; ++j) buf[j * 33 + lane] = v[j];
   __syncwarp();
@@ -215,18 +215,19 @@ __device__ __forceinline__ void store_transposed(float* buf, const float (&v)[NC
 #pragma unroll
     for (int w = 0; w < NC / 4; ++w)
       q[w] = fp8x4_t<AF, false>(col[4 * w] * inv, col[4 * w + 1] * inv, col[4 * w + 2] * inv, col[4 * w + 3] * inv);
-    uint8_t* dst = static_cast<uint8_t*>(out) + (row0 + c) * P + p0 + rg * NC;
+    uint8_t* dst = static_cast<uint8_t*>(out) + (row0 + (int64_t)c * rstride) * P + p0 + rg * NC;
     if constexpr (NC == 16)
       *reinterpret_cast<uint4*>(dst) = make_uint4(q[0], q[1], q[2], q[3]);
     else
       *reinterpret_cast<uint2*>(dst) = make_uint2(q[0], q[1]);
     if (rg == 0) {  // tiled scale layout of the [rows, P] operand (see sf_tiled_offset)
-      const int64_t r = row0 + c;
+      const int64_t r = row0 + (int64_t)c * rstride;
       sf[((r >> 7) * (P >> 7) + (p0 >> 7)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + ((p0 >> 5) & 3)] =
           (uint8_t)byte;
     }
   } else {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (row0 + c) * P + p0 + rg * NC);
+    uint4* dst =
+        reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (row0 + (int64_t)c * rstride) * P + p0 + rg * NC);
 #pragma unroll
     for (int w = 0; w < NC / 8; ++w)
       dst[w] = make_uint4(pack_bf16x2(col[8 * w + 0], col[8 * w + 1]), pack_bf16x2(col[8 * w + 2], col[8 * w + 3]),
@@ -262,17 +263,32 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
     tmem_ld_32x32b_x16(taddr, r);
   else
     tmem_ld_32x32b_x8(taddr, r);
-  float dg[NC], du[NC], ap[NC];  // SiLU(g), a and up * SiLU'(g) first, the gradients after the load
+  float dg[NC], du[NC], ap[NC];  // act(g), a and up * act'(g) first, the gradients after the load
+  if (p.glu == MOE_GLU_GEGLU) {  // GELU(g) = g Phi(g), GELU'(g) = Phi(g) + g phi(g)
 #pragma unroll
-  for (int jj = 0; jj < NC; ++jj) {
-    float g = bf16_bits_to_float(ck[(sub * NC + jj) * 128 + m]);
-    float u = bf16_bits_to_float(ck[32 * 128 + (sub * NC + jj) * 128 + m]);
-    if (!valid) g = u = 0.f;
-    const float sg = __fdividef(1.f, 1.f + __expf(-g));
-    const float sl = g * sg;
-    du[jj] = sl;
-    ap[jj] = sl * u;
-    dg[jj] = u * (sg * (1.f + g * (1.f - sg)));
+    for (int jj = 0; jj < NC; ++jj) {
+      float g = bf16_bits_to_float(ck[(sub * NC + jj) * 128 + m]);
+      float u = bf16_bits_to_float(ck[32 * 128 + (sub * NC + jj) * 128 + m]);
+      if (!valid) g = u = 0.f;
+      const float cdf = 0.5f * (1.f + erff(g * 0.70710678118654752f));
+      const float pdf = 0.39894228040143268f * __expf(-0.5f * g * g);
+      const float act = g * cdf;
+      du[jj] = act;
+      ap[jj] = act * u;
+      dg[jj] = u * (cdf + g * pdf);
+    }
+  } else {  // SiLU(g) = g sigma(g), SiLU'(g) = sigma(g) (1 + g (1 - sigma(g)))
+#pragma unroll
+    for (int jj = 0; jj < NC; ++jj) {
+      float g = bf16_bits_to_float(ck[(sub * NC + jj) * 128 + m]);
+      float u = bf16_bits_to_float(ck[32 * 128 + (sub * NC + jj) * 128 + m]);
+      if (!valid) g = u = 0.f;
+      const float sg = __fdividef(1.f, 1.f + __expf(-g));
+      const float sl = g * sg;
+      du[jj] = sl;
+      ap[jj] = sl * u;
+      dg[jj] = u * (sg * (1.f + g * (1.f - sg)));
+    }
   }
   tmem_ld_wait_regs<NC>(r);
 #pragma unroll
@@ -286,7 +302,32 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
     ap[jj] = p.affinity_on_i ? sv * a : a;
   }
   const int c0 = i0 + sub * NC;  // first feature of this warp's columns
-  if constexpr (MX) {
+  const bool il = NC == 16 && p.interleaved;  // gate_i, up_i at columns 2i, 2i+1 (host: NC == 16)
+  if (il) {
+    // this warp's 16 (gate, up) pairs are the 32 consecutive columns 2*c0.. of dh: one MX group
+    group_bar<32 * SUBS>(bar_id);  // keep the barrier count identical on every path
+    if constexpr (MX) {
+      float am = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < NC; ++jj) am = fmaxf(am, fmaxf(fabsf(dg[jj]), fabsf(du[jj])));
+      const uint32_t byte = e8m0_byte(__float_as_uint(am), AF);
+      const float inv = e8m0_inv_scale(byte);
+      uint32_t q[NC / 2];
+#pragma unroll
+      for (int w = 0; w < NC / 2; ++w)
+        q[w] = fp8x4_t<AF, false>(dg[2 * w] * inv, du[2 * w] * inv, dg[2 * w + 1] * inv, du[2 * w + 1] * inv);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dh) + prow * (2 * (int64_t)I) + 2 * c0);
+#pragma unroll
+      for (int w = 0; w < NC / 8; ++w) dst[w] = make_uint4(q[4 * w], q[4 * w + 1], q[4 * w + 2], q[4 * w + 3]);
+      p.dh_sf[sf_tiled_offset(prow, 2 * c0, 2 * (int64_t)I)] = (uint8_t)byte;
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dh) + prow * (2 * (int64_t)I) + 2 * c0);
+#pragma unroll
+      for (int w = 0; w < NC / 4; ++w)
+        dst[w] = make_uint4(pack_bf16x2(dg[4 * w + 0], du[4 * w + 0]), pack_bf16x2(dg[4 * w + 1], du[4 * w + 1]),
+                            pack_bf16x2(dg[4 * w + 2], du[4 * w + 2]), pack_bf16x2(dg[4 * w + 3], du[4 * w + 3]));
+    }
+  } else if constexpr (MX) {
     float amg = 0.f, amu = 0.f;
 #pragma unroll
     for (int jj = 0; jj < NC; ++jj) {
@@ -335,9 +376,10 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
                           pack_bf16x2(du[8 * q + 4], du[8 * q + 5]), pack_bf16x2(du[8 * q + 6], du[8 * q + 7]));
     }
   }
-  store_transposed<MX, NC, AF>(tbuf, dg, p.dht, p.dht_sf, P, c0, p0, lane);
-  store_transposed<MX, NC, AF>(tbuf + NC * 33, du, p.dht, p.dht_sf, P, I + c0, p0, lane);
-  store_transposed<MX, NC, AF>(tbuf + 2 * NC * 33, ap, p.apt, p.apt_sf, P, c0, p0, lane);
+  // dh^T rows in W1's gate/up layout, a'^T rows by feature
+  store_transposed<MX, NC, AF>(tbuf, dg, p.dht, p.dht_sf, P, il ? 2 * c0 : c0, il ? 2 : 1, p0, lane);
+  store_transposed<MX, NC, AF>(tbuf + NC * 33, du, p.dht, p.dht_sf, P, il ? 2 * c0 + 1 : I + c0, il ? 2 : 1, p0, lane);
+  store_transposed<MX, NC, AF>(tbuf + 2 * NC * 33, ap, p.apt, p.apt_sf, P, c0, 1, p0, lane);
 }
 
 

@@ -210,6 +210,11 @@ static int check_args(const MoeBwdArgs* a, bool need_ptrs) {
   if (mx && a->has_bias) return fail(MOE_ERR_UNSUPPORTED, "moe_bwd: bias gradients are implemented for BF16 only");
   if (a->act_src != MOE_ACT_CHECKPOINT && a->act_src != MOE_ACT_RECOMPUTE)
     return fail(MOE_ERR_INVALID, "moe_bwd: bad act_src");
+  if (a->glu != MOE_GLU_SWIGLU && a->glu != MOE_GLU_GEGLU) return fail(MOE_ERR_INVALID, "moe_bwd: bad glu");
+  if (a->gate_up_layout != MOE_GATE_UP_CONCAT && a->gate_up_layout != MOE_GATE_UP_INTERLEAVED)
+    return fail(MOE_ERR_INVALID, "moe_bwd: bad gate_up_layout");
+  if (a->gate_up_layout == MOE_GATE_UP_INTERLEAVED && kG1Subs != 2)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_bwd: the interleaved layout needs 16 columns per G1 epilogue warp");
   const bool rec = a->act_src == MOE_ACT_RECOMPUTE;
   if (!need_ptrs) return MOE_OK;
   const void* req[] = {a->x, a->dout, a->s, a->ids, a->dx, a->dW1, a->dW2, a->ds, a->status_dev};
@@ -502,6 +507,8 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.I = a.I; p.B = a.block_size;
     p.affinity_on_i = a.affinity == MOE_AFFINITY_ON_I;
     p.fmt_act = a.fp8_act;
+    p.glu = a.glu;
+    p.interleaved = a.gate_up_layout == MOE_GATE_UP_INTERLEAVED;
     p.P = P;
     p.dh = reg<void>(L, ws, R_DH); p.dh_sf = reg<uint8_t>(L, ws, R_DH_SF);
     p.dht = reg<void>(L, ws, R_DH_T); p.dht_sf = reg<uint8_t>(L, ws, R_DH_T_SF);

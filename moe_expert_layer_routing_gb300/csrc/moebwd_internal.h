@@ -133,6 +133,8 @@ struct GemmParams {
   const uint16_t* ckpt;         // [N,2,I,B]
   const uint16_t* b1;           // G0 (checkpoint epilogue): [E,2I] bias or null
   int I, B, affinity_on_i, fmt_act;
+  int glu;                      // MOE_GLU_SWIGLU or MOE_GLU_GEGLU
+  int interleaved;              // dh (and W1, dW1, db1) columns: gate_i, up_i at 2i, 2i+1
   int64_t P;
   void* dh; uint8_t* dh_sf;
   void* dht; uint8_t* dht_sf;

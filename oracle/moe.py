@@ -20,7 +20,9 @@ colvec_scale=s, colvec_reduce=True)`, `db2_and_ds_kernel`, `_down_projection_bac
     dW1_e  = sum_rows x_t^T dh              db1_e   = sum_rows dh
     dx_t   = sum_k dh @ W1_e^T
 
-The gate/up pre-activation h of each (t, k) is an input (the forward's checkpoint).
+The gate/up pre-activation h of each (t, k) is an input (the forward's checkpoint), always as
+[gate | up].  Variants: `activation` "geglu" replaces SiLU by GELU (exact normal CDF); `gate_up`
+"interleaved" puts gate_i and up_i in columns 2i, 2i+1 of W1_e (and of dh, dW1_e, db1_e).
 """
 from __future__ import annotations
 
@@ -54,6 +56,33 @@ def dsilu(z):
     return sg * (1.0 + z * (1.0 - sg))
 
 
+def gelu(z):
+    """GELU(z) = z * Phi(z) with the exact normal CDF (the GeGLU activation of sonic-moe's
+    `activation_type` "geglu"; the page names the activation but prints no formula)."""
+    from scipy.special import erf
+    return 0.5 * z * (1.0 + erf(z / np.sqrt(2.0)))
+
+
+def dgelu(z):
+    from scipy.special import erf
+    return 0.5 * (1.0 + erf(z / np.sqrt(2.0))) + z * np.exp(-0.5 * z * z) / np.sqrt(2.0 * np.pi)
+
+
+ACTIVATIONS = {"swiglu": (silu, dsilu), "geglu": (gelu, dgelu)}
+
+
+def gate_up_columns(I, layout="concat"):
+    """Columns of W1_e (and of dh, dW1_e, db1_e) holding gate_i and up_i: concat (gate block then up
+    block) or interleaved (gate_i at 2i, up_i at 2i+1; sonic-moe's interleaved gate/up layout that
+    its db1 kernel remaps to concat)."""
+    i = np.arange(I)
+    if layout == "concat":
+        return i, I + i
+    if layout == "interleaved":
+        return 2 * i, 2 * i + 1
+    raise ValueError(layout)
+
+
 def rows_of_expert(ids: np.ndarray, e: int):
     """(t, k) of every row routed to expert e, in ascending flat order t*K + k."""
     flat = np.nonzero(np.asarray(ids).reshape(-1) == e)[0]
@@ -61,8 +90,9 @@ def rows_of_expert(ids: np.ndarray, e: int):
     return flat // K, flat % K
 
 
-def moe_forward(x, W1, b1, W2, b2, s, ids):
-    """out [T,H] and the pre-activations h [T,K,2I] (used by the pins, never by the GPU path)."""
+def moe_forward(x, W1, b1, W2, b2, s, ids, activation="swiglu", gate_up="concat"):
+    """out [T,H] and the pre-activations h [T,K,2I] as [gate | up] whatever W1's layout (used by the
+    pins, never by the GPU path)."""
     x, W1, W2, s = _f64(x), _f64(W1), _f64(W2), _f64(s)
     b1, b2 = _f64(b1), _f64(b2)
     ids = np.asarray(ids)
@@ -76,8 +106,10 @@ def moe_forward(x, W1, b1, W2, b2, s, ids):
         t, k = rows_of_expert(ids, e)
         if t.size == 0:
             continue
+        gc, uc = gate_up_columns(I, gate_up)
         he = x[t] @ W1[e] + (b1[e] if b1 is not None else 0.0)
-        a = silu(he[:, :I]) * he[:, I:]
+        he = np.concatenate([he[:, gc], he[:, uc]], axis=1)
+        a = ACTIVATIONS[activation][0](he[:, :I]) * he[:, I:]
         y = a @ W2[e] + (b2[e] if b2 is not None else 0.0)
         np.add.at(out, t, s[t, k][:, None] * y)
         h[t, k] = he
@@ -132,12 +164,12 @@ def valid_token_ids(ids, num_valid):
     return ids
 
 
-def moe_backward(x, dout, W1, W2, s, ids, h, b2=None, with_bias=False):
+def moe_backward(x, dout, W1, W2, s, ids, h, b2=None, with_bias=False, activation="swiglu", gate_up="concat"):
     """All gradients of the MoE layer in float64 (the BF16 path's reference).
 
-    x, dout [T,H]; W1 [E,H,2I]; W2 [E,I,H]; s [T,K]; ids [T,K]; h [T,K,2I]; b2 [E,H] or None.
-    Returns dict(dx [T,H], dW1 [E,H,2I], dW2 [E,I,H], ds [T,K], db1 [E,2I], db2 [E,H]);
-    db1/db2 are None unless with_bias.
+    x, dout [T,H]; W1 [E,H,2I]; W2 [E,I,H]; s [T,K]; ids [T,K]; h [T,K,2I] ([gate | up]); b2 [E,H]
+    or None.  Returns dict(dx [T,H], dW1 [E,H,2I], dW2 [E,I,H], ds [T,K], db1 [E,2I], db2 [E,H]);
+    db1/db2 are None unless with_bias.  dW1 and db1 follow W1's gate/up layout.
     """
     x, dout, s, h = map(_f64, (x, dout, s, h))
     b2 = _f64(b2)
@@ -152,6 +184,8 @@ def moe_backward(x, dout, W1, W2, s, ids, h, b2=None, with_bias=False):
     dW2 = np.zeros((E, I, H))
     db1 = np.zeros((E, I2)) if with_bias else None
     db2 = np.zeros((E, H)) if with_bias else None
+    act, dact = ACTIVATIONS[activation]
+    gc, uc = gate_up_columns(I, gate_up)
     for e in range(E):
         t, k = rows_of_expert(ids, e)
         if t.size == 0:
@@ -159,14 +193,16 @@ def moe_backward(x, dout, W1, W2, s, ids, h, b2=None, with_bias=False):
         W1e, W2e = _f64(W1[e]), _f64(W2[e])
         g = dout[t]                                   # gathered upstream gradient rows
         gate, up = h[t, k, :I], h[t, k, I:]
-        a = silu(gate) * up
+        a = act(gate) * up
         sr = s[t, k][:, None]
         dA_raw = g @ W2e.T
         ds[t, k] = np.sum(dA_raw * a, axis=1)
         if b2 is not None:
             ds[t, k] += g @ b2[e]
         dA = sr * dA_raw
-        dh = np.concatenate([dA * up * dsilu(gate), dA * silu(gate)], axis=1)
+        dh = np.zeros((t.size, I2))
+        dh[:, gc] = dA * up * dact(gate)
+        dh[:, uc] = dA * act(gate)
         dW2[e] = (sr * a).T @ g
         dW1[e] = x[t].T @ dh
         if with_bias:
@@ -202,7 +238,8 @@ def _col_roundtrip(v, fmt, quant):
 
 
 def moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=1, fp8_act=mx.E5M2, fp8_w=mx.E4M3,
-                       b2=None, with_bias=False, experts=None, tokens=None, quant=None):
+                       b2=None, with_bias=False, experts=None, tokens=None, quant=None, activation="swiglu",
+                       gate_up="concat"):
     """MoE backward with every GEMM operand MXFP8-quantised along its contraction dimension.
 
     Quantisation points (reading of the MXFP8 blockwise backward page; weights pre-quantised,
@@ -216,7 +253,8 @@ def moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=1, fp8_act=mx.E5M2, 
     before their quantisation, as the kernel quantises float32 values.  ds, db1 and db2 use the
     unquantised epilogue values.  `experts` limits dW1/dW2/db1/db2 to those experts, `tokens`
     limits dx/ds to those tokens (both default to all).  `quant(v, fmt, axis)` defaults to the
-    MX round trip; tests substitute the identity to check the wiring.
+    MX round trip; tests substitute the identity to check the wiring.  dh, W1_e, dW1 and db1 are in
+    W1's gate/up layout, so the 32-column groups of Q_2I follow that layout.
     """
     quant = quant or mx.mx_roundtrip
     x, dout, s, h = map(_f64, (x, dout, s, h))
@@ -238,6 +276,8 @@ def moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=1, fp8_act=mx.E5M2, 
     db1 = np.zeros((E, I2)) if with_bias else None
     db2 = np.zeros((E, H)) if with_bias else None
     want_w = set(expert_set)
+    act, dact = ACTIVATIONS[activation]
+    gc, uc = gate_up_columns(I, gate_up)
     for e in range(E):
         t, k = rows_of_expert(ids, e)
         if t.size == 0:
@@ -252,14 +292,17 @@ def moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=1, fp8_act=mx.E5M2, 
         g = dout[t]
         gq = quant(g, fp8_act, 1)
         gate, up = h[t, k, :I], h[t, k, I:]
-        a = silu(gate) * up
+        a = act(gate) * up
         sr = s[t, k][:, None]
         dA_raw = gq @ W2q.T
         dsv = np.sum(dA_raw * a, axis=1)
         if b2 is not None:
             dsv = dsv + g @ b2[e]
         dA = sr * dA_raw
-        dh = _to_f32(np.concatenate([dA * up * dsilu(gate), dA * silu(gate)], axis=1))
+        dh = np.zeros((t.size, I2))
+        dh[:, gc] = dA * up * dact(gate)
+        dh[:, uc] = dA * act(gate)
+        dh = _to_f32(dh)
         dx_exp = _to_bf16(quant(dh, fp8_act, 1) @ W1q.T)
         tm = token_mask[t]
         ds[t[tm], k[tm]] = dsv[tm]
@@ -277,7 +320,8 @@ def moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=1, fp8_act=mx.E5M2, 
 
 
 def moe_backward_sampled(x, dout, W1, W2, s, ids, h, experts, tokens, b2=None, with_bias=False):
-    """BF16-path backward restricted to dW/db of `experts` and dx/ds of `tokens` (same formulas)."""
+    """BF16-path backward restricted to dW/db of `experts` and dx/ds of `tokens` (same formulas;
+    SwiGLU, concatenated gate/up)."""
     x, dout, W1, W2, s, h = map(_f64, (x, dout, W1, W2, s, h))
     b2 = _f64(b2)
     ids = np.asarray(ids)

@@ -22,17 +22,20 @@ def _problem(T=6, H=8, I=4, E=3, K=2, seed=0, bias=True):
     return x, dout, W1, b1, W2, b2, s, ids
 
 
-def _grads(x, dout, W1, b1, W2, b2, s, ids):
-    _, h = om.moe_forward(x, W1, b1, W2, b2, s, ids)
-    return om.moe_backward(x, dout, W1, W2, s, ids, h, b2=b2, with_bias=b1 is not None)
+def _grads(x, dout, W1, b1, W2, b2, s, ids, activation="swiglu", gate_up="concat"):
+    _, h = om.moe_forward(x, W1, b1, W2, b2, s, ids, activation, gate_up)
+    return om.moe_backward(x, dout, W1, W2, s, ids, h, b2=b2, with_bias=b1 is not None, activation=activation,
+                           gate_up=gate_up)
 
 
-def test_finite_differences():
+@pytest.mark.parametrize("activation,gate_up", [("swiglu", "concat"), ("geglu", "concat"),
+                                                ("swiglu", "interleaved"), ("geglu", "interleaved")])
+def test_finite_differences(activation, gate_up):
     x, dout, W1, b1, W2, b2, s, ids = _problem()
-    g = _grads(x, dout, W1, b1, W2, b2, s, ids)
+    g = _grads(x, dout, W1, b1, W2, b2, s, ids, activation, gate_up)
 
     def loss(x, W1, b1, W2, b2, s):
-        out, _ = om.moe_forward(x, W1, b1, W2, b2, s, ids)
+        out, _ = om.moe_forward(x, W1, b1, W2, b2, s, ids, activation, gate_up)
         return float(np.sum(out * dout))
 
     args = dict(x=x, W1=W1, b1=b1, W2=W2, b2=b2, s=s)
@@ -51,17 +54,20 @@ def test_finite_differences():
         assert rel < 1e-7, (name, rel)
 
 
-def _torch_forward(x, W1, b1, W2, b2, s, ids):
-    """Loop-over-experts forward in torch float64 (differentiated by torch autograd)."""
+def _torch_forward(x, W1, b1, W2, b2, s, ids, activation="swiglu", gate_up="concat"):
+    """Loop-over-experts forward in torch float64 (differentiated by torch autograd).  Interleaved
+    gate/up: gate_i in column 2i, up_i in 2i+1."""
     T, H = x.shape
     I = W1.shape[2] // 2
+    act = torch.nn.functional.silu if activation == "swiglu" else torch.nn.functional.gelu
     out = torch.zeros(T, H, dtype=torch.float64)
     for e in range(W1.shape[0]):
         t, k = torch.nonzero(ids == e, as_tuple=True)
         if t.numel() == 0:
             continue
         h = x[t] @ W1[e] + (b1[e] if b1 is not None else 0)
-        a = torch.nn.functional.silu(h[:, :I]) * h[:, I:]
+        gate, up = (h[:, :I], h[:, I:]) if gate_up == "concat" else (h[:, 0::2], h[:, 1::2])
+        a = act(gate) * up
         y = a @ W2[e] + (b2[e] if b2 is not None else 0)
         out = out.index_add(0, t, s[t, k][:, None] * y)
     return out
@@ -85,6 +91,36 @@ def test_torch_autograd_tiny_config_shapes(bias):
         ref = t.grad.numpy()
         err = np.linalg.norm(g[name] - ref) / np.linalg.norm(ref)
         assert err < 1e-12, (name, err)
+
+
+@pytest.mark.parametrize("activation,gate_up", [("geglu", "concat"), ("swiglu", "interleaved"),
+                                                ("geglu", "interleaved")])
+def test_torch_autograd_variants(activation, gate_up):
+    """GeGLU (torch's exact-erf GELU) and the interleaved gate/up layout against torch autograd."""
+    T, H, I, E, K = 64, 32, 16, 3, 2
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T, H, I, E, K, seed=13, bias=True)
+    g = _grads(x, dout, W1, b1, W2, b2, s, ids, activation, gate_up)
+    tt = {n: torch.tensor(v, requires_grad=True) for n, v in dict(x=x, W1=W1, b1=b1, W2=W2, b2=b2, s=s).items()}
+    out = _torch_forward(tt["x"], tt["W1"], tt["b1"], tt["W2"], tt["b2"], tt["s"], torch.tensor(ids), activation,
+                         gate_up)
+    (out * torch.tensor(dout)).sum().backward()
+    for name, key in (("dx", "x"), ("dW1", "W1"), ("dW2", "W2"), ("ds", "s"), ("db1", "b1"), ("db2", "b2")):
+        ref = tt[key].grad.numpy()
+        err = np.linalg.norm(g[name] - ref) / np.linalg.norm(ref)
+        assert err < 1e-12, (name, err)
+
+
+def test_interleaved_layout_is_a_column_permutation():
+    """The interleaved layout is the concat layout with W1's columns (and so dW1's, db1's) permuted."""
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=8, H=6, I=3, E=2, K=1, seed=14)
+    perm = np.empty(6, dtype=int)
+    perm[0::2], perm[1::2] = np.arange(3), 3 + np.arange(3)   # interleaved column j <- concat column perm[j]
+    gi = _grads(x, dout, W1[:, :, perm], b1[:, perm], W2, b2, s, ids, "swiglu", "interleaved")
+    gc = _grads(x, dout, W1, b1, W2, b2, s, ids, "swiglu", "concat")
+    assert np.allclose(gi["dW1"], gc["dW1"][:, :, perm], rtol=0, atol=1e-13)
+    assert np.allclose(gi["db1"], gc["db1"][:, perm], rtol=0, atol=1e-13)
+    for name in ("dx", "dW2", "ds", "db2"):
+        assert np.allclose(gi[name], gc[name], rtol=0, atol=1e-13), name
 
 
 def test_dense_mlp_reduction():
