@@ -234,6 +234,15 @@ typedef struct MoeBwdArgs {
                              tokens take no part and get zero dx rows and ds / ds_masked entries */
   int glu;                /* MOE_GLU_SWIGLU (default 0) or MOE_GLU_GEGLU */
   int gate_up_layout;     /* MOE_GATE_UP_CONCAT (default 0) or MOE_GATE_UP_INTERLEAVED */
+  /* [BW] optional checkpoints: forward values that replace recomputed ones in the dW_down product
+   * (dW2_e = sum a'^T (s dout)); each (device) bf16 in the block layout of gate_up_ckpt, or NULL.
+   * With one given, moe_bwd builds that operand from it and does not compute it itself. */
+  const void* intermediate_ckpt;        /* [N,I,B] a = act(gate)*up (intermediate_checkpoint_T); with
+                                           the affinity on I, dW_down uses s * this */
+  const void* scaled_intermediate_ckpt; /* [N,I,B] s*a (scaled_intermediate_checkpoint_T), affinity on I
+                                           only; preferred over intermediate_ckpt */
+  const void* down_proj_act_ckpt;       /* [N,B,H] s*dout per slot (down_proj_act_checkpoint), affinity
+                                           on H only; also the rows summed into db2 */
 } MoeBwdArgs;
 
 /* Bytes of workspace moe_bwd needs for these shapes and options (pointers are not read). */

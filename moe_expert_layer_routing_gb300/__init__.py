@@ -50,7 +50,8 @@ class MoeBwdArgs(ctypes.Structure):
                  "gate_up_ckpt", "dx", "dW1", "dW2", "ds", "db1", "db2", "status_dev", "workspace")] + \
                [("workspace_bytes", ctypes.c_size_t), ("accumulate", ctypes.c_int), ("act_src", ctypes.c_int)] + \
                [(n, ctypes.c_void_p) for n in ("W1t", "W1t_q", "W1t_sf", "b1", "ds_masked", "num_valid_tokens")] + \
-               [(n, ctypes.c_int) for n in ("glu", "gate_up_layout")]
+               [(n, ctypes.c_int) for n in ("glu", "gate_up_layout")] + \
+               [(n, ctypes.c_void_p) for n in ("intermediate_ckpt", "scaled_intermediate_ckpt", "down_proj_act_ckpt")]
 
 
 _lib = None
@@ -238,13 +239,20 @@ class MoeBwd:
         self._keep = []
 
     def bind(self, *, x, dout, s, ids, ckpt=None, W1=None, W2=None, W1_q=None, W1_sf=None, W2_q=None, W2_sf=None,
-             b2=None, W1t=None, W1t_q=None, W1t_sf=None, b1=None, num_valid_tokens=None):
+             b2=None, W1t=None, W1t_q=None, W1t_sf=None, b1=None, num_valid_tokens=None, intermediate_ckpt=None,
+             scaled_intermediate_ckpt=None, down_proj_act_ckpt=None):
         """ckpt: the [N,2,I,B] checkpoint (act_src ACT_CHECKPOINT).  W1t (bf16 [E,2I,H]) or W1t_q/W1t_sf
         and optionally b1 [E,2I]: the operands of the recomputation (act_src ACT_RECOMPUTE)."""
-        _need_cuda(x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2, W1t, W1t_q, W1t_sf, b1, num_valid_tokens)
+        _need_cuda(x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2, W1t, W1t_q, W1t_sf, b1, num_valid_tokens,
+                   intermediate_ckpt, scaled_intermediate_ckpt, down_proj_act_ckpt)
         if num_valid_tokens is not None:
             assert num_valid_tokens.dtype == torch.int32 and num_valid_tokens.numel() == 1
         a = self.a
+        Nb = num_blocks_bound(a.T, a.K, a.E, a.block_size)
+        for t in (intermediate_ckpt, scaled_intermediate_ckpt):
+            assert t is None or (t.dtype == torch.bfloat16 and tuple(t.shape) == (Nb, a.I, a.block_size))
+        assert down_proj_act_ckpt is None or (down_proj_act_ckpt.dtype == torch.bfloat16 and
+                                              tuple(down_proj_act_ckpt.shape) == (Nb, a.block_size, a.H))
         assert x.dtype == torch.bfloat16 and dout.dtype == torch.bfloat16
         assert s.dtype == torch.float32 and ids.dtype == torch.int32
         assert tuple(x.shape) == (a.T, a.H) and tuple(dout.shape) == (a.T, a.H)
@@ -259,7 +267,9 @@ class MoeBwd:
             assert b1.dtype == torch.bfloat16 and tuple(b1.shape) == (a.E, 2 * a.I)
         for name, t in dict(x=x, dout=dout, s=s, ids=ids, gate_up_ckpt=ckpt, W1=W1, W2=W2, W1_q=W1_q,
                             W1_sf=W1_sf, W2_q=W2_q, W2_sf=W2_sf, b2=b2, W1t=W1t, W1t_q=W1t_q, W1t_sf=W1t_sf,
-                            b1=b1, num_valid_tokens=num_valid_tokens).items():
+                            b1=b1, num_valid_tokens=num_valid_tokens, intermediate_ckpt=intermediate_ckpt,
+                            scaled_intermediate_ckpt=scaled_intermediate_ckpt,
+                            down_proj_act_ckpt=down_proj_act_ckpt).items():
             setattr(a, name, None if t is None else t.data_ptr())
         for name in ("dx", "dW1", "dW2", "ds", "db1", "db2", "ds_masked", "status"):
             t = getattr(self, name)
@@ -267,7 +277,7 @@ class MoeBwd:
         a.workspace = self.workspace.data_ptr()
         a.workspace_bytes = self.workspace.numel()
         self._keep = [x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2, W1t, W1t_q, W1t_sf, b1,
-                      num_valid_tokens]
+                      num_valid_tokens, intermediate_ckpt, scaled_intermediate_ckpt, down_proj_act_ckpt]
         return self
 
     def run(self, stream=None):

@@ -379,7 +379,8 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
   // dh^T rows in W1's gate/up layout, a'^T rows by feature
   store_transposed<MX, NC, AF>(tbuf, dg, p.dht, p.dht_sf, P, il ? 2 * c0 : c0, il ? 2 : 1, p0, lane);
   store_transposed<MX, NC, AF>(tbuf + NC * 33, du, p.dht, p.dht_sf, P, il ? 2 * c0 + 1 : I + c0, il ? 2 : 1, p0, lane);
-  store_transposed<MX, NC, AF>(tbuf + 2 * NC * 33, ap, p.apt, p.apt_sf, P, c0, 1, p0, lane);
+  if (p.apt)  // a'^T (null: built from a saved checkpoint of a or s*a)
+    store_transposed<MX, NC, AF>(tbuf + 2 * NC * 33, ap, p.apt, p.apt_sf, P, c0, 1, p0, lane);
 }
 
 

@@ -92,7 +92,7 @@ enum Region {
   R_CHUNK_COUNTS, R_EXPERT_OFFSETS, R_BLOCK_OFFSETS, R_TILE_OFFSETS, R_EXPERT_ORDER, R_SCALARS,
   R_X_GATHER, R_S_SCATTER, R_S_REV, R_TPID, R_B2E, R_TILE_ROW_FLAT, R_FLAT_TILE_ROW, R_TILE_EXPERT,
   R_DOUT_G, R_DOUT_G_SF, R_DOUT_GT, R_DOUT_GT_SF, R_X_GT, R_X_GT_SF, R_DH, R_DH_SF, R_DH_T, R_DH_T_SF,
-  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_X_G, R_X_G_SF, R_CKPT, R_PAIR_OFFSETS, R_TILE_ORDER, R_COUNT
+  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_X_G, R_X_G_SF, R_CKPT, R_PAIR_OFFSETS, R_TILE_ORDER, R_TILE_ROW_SLOT, R_COUNT
 };
 
 struct Layout {
@@ -173,6 +173,7 @@ static Layout make_layout(const MoeBwdArgs& a) {
   b[R_COUNTERS] = 64;  // one tile counter per grouped GEMM
   b[R_PAIR_OFFSETS] = sizeof(int32_t) * (E + 1);
   b[R_TILE_ORDER] = sizeof(int32_t) * (size_t)(P / kTileM + 1);
+  b[R_TILE_ROW_SLOT] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, P);  // saved s*dout rows (pointers not read)
   if (a.act_src == MOE_ACT_RECOMPUTE) {
     b[R_X_G] = (size_t)(P * H * es);
     b[R_X_G_SF] = mx ? (size_t)(P * H / 32) : 0;
@@ -213,6 +214,15 @@ static int check_args(const MoeBwdArgs* a, bool need_ptrs) {
   if (a->glu != MOE_GLU_SWIGLU && a->glu != MOE_GLU_GEGLU) return fail(MOE_ERR_INVALID, "moe_bwd: bad glu");
   if (a->gate_up_layout != MOE_GATE_UP_CONCAT && a->gate_up_layout != MOE_GATE_UP_INTERLEAVED)
     return fail(MOE_ERR_INVALID, "moe_bwd: bad gate_up_layout");
+  if (a->scaled_intermediate_ckpt && a->affinity != MOE_AFFINITY_ON_I)
+    return fail(MOE_ERR_INVALID, "moe_bwd: scaled_intermediate_ckpt needs the affinity on I");
+  if (a->down_proj_act_ckpt && a->affinity != MOE_AFFINITY_ON_H)
+    return fail(MOE_ERR_INVALID, "moe_bwd: down_proj_act_ckpt needs the affinity on H");
+  {
+    const void* al[] = {a->intermediate_ckpt, a->scaled_intermediate_ckpt, a->down_proj_act_ckpt};
+    for (const void* q : al)
+      if (reinterpret_cast<uintptr_t>(q) & 15) return fail(MOE_ERR_INVALID, "moe_bwd: checkpoints must be 16-byte aligned");
+  }
   if (a->gate_up_layout == MOE_GATE_UP_INTERLEAVED && kG1Subs != 2)
     return fail(MOE_ERR_UNSUPPORTED, "moe_bwd: the interleaved layout needs 16 columns per G1 epilogue warp");
   const bool rec = a->act_src == MOE_ACT_RECOMPUTE;
@@ -444,7 +454,26 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   const bool rec = a.act_src == MOE_ACT_RECOMPUTE;
   pa.x_g = rec ? reg<void>(L, ws, R_X_G) : nullptr;
   pa.x_g_sf = rec ? reg<uint8_t>(L, ws, R_X_G_SF) : nullptr;
+  pa.skip_dout_t = a.down_proj_act_ckpt != nullptr;
   if ((rc = launch_prep(pa, st))) return rc;
+  // dW_down operands from saved forward values ([BW] optional checkpoints)
+  const void* inter = a.scaled_intermediate_ckpt ? a.scaled_intermediate_ckpt : a.intermediate_ckpt;
+  if (inter && (rc = launch_apt_from_ckpt(static_cast<const uint16_t*>(inter), a.I, a.block_size, P, scalars + 1,
+                                         tile_expert, tile_offsets, block_offsets, tile_row_flat,
+                                         (!a.scaled_intermediate_ckpt && a.affinity == MOE_AFFINITY_ON_I) ? a.s
+                                                                                                         : nullptr,
+                                         mx, a.fp8_act, reg<void>(L, ws, R_AP_T), reg<uint8_t>(L, ws, R_AP_T_SF), st)))
+    return rc;
+  if (a.down_proj_act_ckpt) {
+    int32_t* slot = reg<int32_t>(L, ws, R_TILE_ROW_SLOT);
+    if ((rc = launch_tile_row_slot(P, a.block_size, scalars + 1, tile_expert, tile_offsets, block_offsets,
+                                   tile_row_flat, slot, st)))
+      return rc;
+    if ((rc = launch_quant_colwise(static_cast<const uint16_t*>(a.down_proj_act_ckpt), L.Nb * a.block_size, P, H, H,
+                                   slot, mx, a.fp8_act, reg<void>(L, ws, R_DOUT_GT), reg<uint8_t>(L, ws, R_DOUT_GT_SF),
+                                   1, st)))
+      return rc;
+  }
   prof_mark(st, slot, 2);
 
   // 2b. G0 (recompute): h = x_g W1_e + b1_e written into a block checkpoint in the workspace
@@ -512,7 +541,8 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.P = P;
     p.dh = reg<void>(L, ws, R_DH); p.dh_sf = reg<uint8_t>(L, ws, R_DH_SF);
     p.dht = reg<void>(L, ws, R_DH_T); p.dht_sf = reg<uint8_t>(L, ws, R_DH_T_SF);
-    p.apt = reg<void>(L, ws, R_AP_T); p.apt_sf = reg<uint8_t>(L, ws, R_AP_T_SF);
+    p.apt = inter ? nullptr : reg<void>(L, ws, R_AP_T);
+    p.apt_sf = inter ? nullptr : reg<uint8_t>(L, ws, R_AP_T_SF);
     p.ds_part = reg<float>(L, ws, R_DS_PART);
     p.tile_counter = counters + 0;
     p.status = a.status_dev;

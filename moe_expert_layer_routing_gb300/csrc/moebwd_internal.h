@@ -80,9 +80,19 @@ struct PrepArgs {
   void* dout_gt; uint8_t* dout_gt_sf;  // [H,P]
   void* x_gt; uint8_t* x_gt_sf;        // [H,P]
   void* x_g; uint8_t* x_g_sf;          // [P,H] row-major (nullable: only when h is recomputed)
+  int skip_dout_t;                     // dout_gt is built elsewhere (from a saved s*dout checkpoint)
   float* ds_bias;                      // [P] <dout_t, b2_e> or null
 };
 int launch_prep(const PrepArgs& a, cudaStream_t st);
+// a'^T [I,P] from an [N,I,B] block checkpoint of a (times s when s_or_null) or s*a
+int launch_apt_from_ckpt(const uint16_t* ckpt, int I, int B, int64_t P, const int32_t* num_tiles,
+                         const int32_t* tile_expert, const int32_t* tile_offsets, const int32_t* block_offsets,
+                         const int32_t* tile_row_flat, const float* s_or_null, int mx, int fmt, void* out,
+                         uint8_t* out_sf, cudaStream_t st);
+// slot[p] = block-layout slot of tile row p, -1 for padding
+int launch_tile_row_slot(int64_t P, int B, const int32_t* num_tiles, const int32_t* tile_expert,
+                         const int32_t* tile_offsets, const int32_t* block_offsets, const int32_t* tile_row_flat,
+                         int32_t* slot, cudaStream_t st);
 
 int launch_quant_rowwise(const uint16_t* in, int64_t src_rows, int64_t rows, int64_t cols, int64_t ld,
                          const int32_t* row_index, int fmt, uint8_t* q, uint8_t* sf, int tiled, cudaStream_t st);

@@ -108,8 +108,8 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
         }
       }
       __syncthreads();
-      // ---- phase 2 ----
-      if (tid < ncol) {
+      // ---- phase 2 ---- (dout^T comes from a saved s*dout checkpoint when skip_dout_t)
+      if (tid < ncol && !(which == 0 && a.skip_dout_t)) {
         const int h = tid;
         const int64_t orow = h0 + h;
         void* outp = which == 0 ? a.dout_gt : a.x_gt;
@@ -177,6 +177,118 @@ int launch_prep(const PrepArgs& a, cudaStream_t st) {
   }
   if (a.scale_t) return bias ? prep_launch<false, true, true>(a, grid, st) : prep_launch<false, true, false>(a, grid, st);
   return bias ? prep_launch<false, false, true>(a, grid, st) : prep_launch<false, false, false>(a, grid, st);
+}
+
+// ------------------------------------------------------------------------------------------
+// operands from saved forward values ([N, I, B] and [N, B, H] block checkpoints)
+// ------------------------------------------------------------------------------------------
+
+// a'^T [I, P] (dW_down's token-side operand) from a feature-major block checkpoint [N, I, B] of a (or
+// s*a): tile row p of expert e is slot block_offsets[e]*B + (p - tile_offsets[e]), and a tile's 128
+// rows are 128 consecutive slots of one block.  Thread (feature i, 32-row group g) reads 64
+// contiguous bytes, multiplies by s when SCALE, zeroes padding rows, and writes one group (bf16, or
+// fp8 codes with their scale).
+template <bool MX, bool SCALE, int AF>
+__global__ void __launch_bounds__(256) apt_from_ckpt_kernel(const uint16_t* __restrict__ ckpt, int I, int B,
+                                                            int64_t P, const int32_t* __restrict__ num_tiles,
+                                                            const int32_t* __restrict__ tile_expert,
+                                                            const int32_t* __restrict__ tile_offsets,
+                                                            const int32_t* __restrict__ block_offsets,
+                                                            const int32_t* __restrict__ tile_row_flat,
+                                                            const float* __restrict__ s, void* out, uint8_t* out_sf) {
+  const int tile = blockIdx.x;
+  if (tile >= *num_tiles) return;
+  const int i = blockIdx.y * 64 + (threadIdx.x >> 2);
+  const int g = threadIdx.x & 3;
+  if (i >= I) return;
+  const int e = tile_expert[tile];
+  const int64_t p0 = (int64_t)tile * 128 + g * 32;
+  const int64_t slot = (int64_t)block_offsets[e] * B + ((int64_t)tile * 128 - tile_offsets[e]) + g * 32;
+  const int64_t blk = slot / B, b = slot - blk * B;
+  const uint4* src = reinterpret_cast<const uint4*>(ckpt + (blk * I + i) * B + b);
+  float v[32];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 w = src[q];
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * q + 2 * j] = __uint_as_float(ww[j] << 16);
+      v[8 * q + 2 * j + 1] = __uint_as_float(ww[j] & 0xFFFF0000u);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const int f = tile_row_flat[p0 + r];
+    if (f < 0)
+      v[r] = 0.f;
+    else if (SCALE)
+      v[r] *= s[f];
+  }
+  if constexpr (MX) {
+    uint32_t w[8];
+    const uint32_t byte = quantize_group32_t<AF>(v, w);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + (int64_t)i * P + p0);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    out_sf[sf_tiled_offset(i, p0, P)] = (uint8_t)byte;
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (int64_t)i * P + p0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      dst[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                          pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+  }
+}
+
+int launch_apt_from_ckpt(const uint16_t* ckpt, int I, int B, int64_t P, const int32_t* num_tiles,
+                         const int32_t* tile_expert, const int32_t* tile_offsets, const int32_t* block_offsets,
+                         const int32_t* tile_row_flat, const float* s_or_null, int mx, int fmt, void* out,
+                         uint8_t* out_sf, cudaStream_t st) {
+  const dim3 grid((unsigned)(P / 128), (unsigned)((I + 63) / 64));
+  if (grid.x == 0) return MOE_OK;
+  const bool sc = s_or_null != nullptr;
+#define APT_LAUNCH(MXV, SCV, AFV)                                                                          \
+  apt_from_ckpt_kernel<MXV, SCV, AFV><<<grid, 256, 0, st>>>(ckpt, I, B, P, num_tiles, tile_expert, tile_offsets, \
+                                                             block_offsets, tile_row_flat, s_or_null, out, out_sf)
+  if (mx) {
+    if (fmt == MOE_FP8_E4M3) {
+      if (sc) APT_LAUNCH(true, true, MOE_FP8_E4M3); else APT_LAUNCH(true, false, MOE_FP8_E4M3);
+    } else {
+      if (sc) APT_LAUNCH(true, true, MOE_FP8_E5M2); else APT_LAUNCH(true, false, MOE_FP8_E5M2);
+    }
+  } else {
+    if (sc) APT_LAUNCH(false, true, MOE_FP8_E5M2); else APT_LAUNCH(false, false, MOE_FP8_E5M2);
+  }
+#undef APT_LAUNCH
+  count_launch();
+  return cuda_check(cudaGetLastError(), "apt_from_ckpt");
+}
+
+// Slot of every tile row in the block layout (-1 for padding rows and unused tiles).
+__global__ void tile_row_slot_kernel(int64_t P, int B, const int32_t* __restrict__ num_tiles,
+                                     const int32_t* __restrict__ tile_expert, const int32_t* __restrict__ tile_offsets,
+                                     const int32_t* __restrict__ block_offsets,
+                                     const int32_t* __restrict__ tile_row_flat, int32_t* __restrict__ slot) {
+  const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= P) return;
+  const int tile = (int)(p / 128);
+  if (tile >= *num_tiles || tile_row_flat[p] < 0) {
+    slot[p] = -1;
+    return;
+  }
+  const int e = tile_expert[tile];
+  slot[p] = (int32_t)((int64_t)block_offsets[e] * B + (p - tile_offsets[e]));
+}
+
+int launch_tile_row_slot(int64_t P, int B, const int32_t* num_tiles, const int32_t* tile_expert,
+                         const int32_t* tile_offsets, const int32_t* block_offsets, const int32_t* tile_row_flat,
+                         int32_t* slot, cudaStream_t st) {
+  if (P == 0) return MOE_OK;
+  tile_row_slot_kernel<<<(unsigned)((P + 255) / 256), 256, 0, st>>>(P, B, num_tiles, tile_expert, tile_offsets,
+                                                                     block_offsets, tile_row_flat, slot);
+  count_launch();
+  return cuda_check(cudaGetLastError(), "tile_row_slot");
 }
 
 // ------------------------------------------------------------------------------------------

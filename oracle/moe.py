@@ -164,12 +164,19 @@ def valid_token_ids(ids, num_valid):
     return ids
 
 
-def moe_backward(x, dout, W1, W2, s, ids, h, b2=None, with_bias=False, activation="swiglu", gate_up="concat"):
+def moe_backward(x, dout, W1, W2, s, ids, h, b2=None, with_bias=False, activation="swiglu", gate_up="concat",
+                 affinity=1, inter=None, sdout=None):
     """All gradients of the MoE layer in float64 (the BF16 path's reference).
 
     x, dout [T,H]; W1 [E,H,2I]; W2 [E,I,H]; s [T,K]; ids [T,K]; h [T,K,2I] ([gate | up]); b2 [E,H]
     or None.  Returns dict(dx [T,H], dW1 [E,H,2I], dW2 [E,I,H], ds [T,K], db1 [E,2I], db2 [E,H]);
     db1/db2 are None unless with_bias.  dW1 and db1 follow W1's gate/up layout.
+
+    Forward values saved by the caller ([BW] optional checkpoints) replace recomputed ones in the
+    dW_down product dW2_e = sum a'^T (s dout) with the affinity on I (affinity=1) or H (0):
+      inter [T,K,I]  the factor that carries the activation: s*a on I, a on H
+                     (`scaled_intermediate_checkpoint_T` / `intermediate_checkpoint_T`)
+      sdout [T,K,H]  s*dout on H (`down_proj_act_checkpoint`), also summed into db2
     """
     x, dout, s, h = map(_f64, (x, dout, s, h))
     b2 = _f64(b2)
@@ -203,10 +210,12 @@ def moe_backward(x, dout, W1, W2, s, ids, h, b2=None, with_bias=False, activatio
         dh = np.zeros((t.size, I2))
         dh[:, gc] = dA * up * dact(gate)
         dh[:, uc] = dA * act(gate)
-        dW2[e] = (sr * a).T @ g
+        av = (sr * a if affinity == 1 else a) if inter is None else _f64(inter)[t, k]
+        gv = (g if affinity == 1 else sr * g) if sdout is None or affinity == 1 else _f64(sdout)[t, k]
+        dW2[e] = av.T @ gv
         dW1[e] = x[t].T @ dh
         if with_bias:
-            db2[e] = np.sum(sr * g, axis=0)
+            db2[e] = np.sum(sr * g if sdout is None or affinity == 1 else gv, axis=0)
             db1[e] = np.sum(dh, axis=0)
         np.add.at(dx, t, dh @ W1e.T)
     return dict(dx=dx, dW1=dW1, dW2=dW2, ds=ds, db1=db1, db2=db2)
@@ -239,7 +248,7 @@ def _col_roundtrip(v, fmt, quant):
 
 def moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=1, fp8_act=mx.E5M2, fp8_w=mx.E4M3,
                        b2=None, with_bias=False, experts=None, tokens=None, quant=None, activation="swiglu",
-                       gate_up="concat"):
+                       gate_up="concat", inter=None, sdout=None):
     """MoE backward with every GEMM operand MXFP8-quantised along its contraction dimension.
 
     Quantisation points (reading of the MXFP8 blockwise backward page; weights pre-quantised,
@@ -254,7 +263,8 @@ def moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=1, fp8_act=mx.E5M2, 
     unquantised epilogue values.  `experts` limits dW1/dW2/db1/db2 to those experts, `tokens`
     limits dx/ds to those tokens (both default to all).  `quant(v, fmt, axis)` defaults to the
     MX round trip; tests substitute the identity to check the wiring.  dh, W1_e, dW1 and db1 are in
-    W1's gate/up layout, so the 32-column groups of Q_2I follow that layout.
+    W1's gate/up layout, so the 32-column groups of Q_2I follow that layout.  `inter` and `sdout`
+    replace the dW_down factors as in moe_backward (saved forward values; quantised the same way).
     """
     quant = quant or mx.mx_roundtrip
     x, dout, s, h = map(_f64, (x, dout, s, h))
@@ -308,10 +318,12 @@ def moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=1, fp8_act=mx.E5M2, 
         ds[t[tm], k[tm]] = dsv[tm]
         np.add.at(dx, t[tm], dx_exp[tm])
         if need_w:
+            av = _to_f32(sr * a if affinity == 1 else a) if inter is None else _f64(inter)[t, k]
             if affinity == 1:
-                dW2[e] = _col_roundtrip(_to_f32(sr * a), fp8_act, quant).T @ _col_roundtrip(g, fp8_act, quant)
+                dW2[e] = _col_roundtrip(av, fp8_act, quant).T @ _col_roundtrip(g, fp8_act, quant)
             else:
-                dW2[e] = _col_roundtrip(_to_f32(a), fp8_act, quant).T @ _col_roundtrip(_to_f32(sr * g), fp8_act, quant)
+                gv = _to_f32(sr * g) if sdout is None else _f64(sdout)[t, k]
+                dW2[e] = _col_roundtrip(av, fp8_act, quant).T @ _col_roundtrip(gv, fp8_act, quant)
             dW1[e] = _col_roundtrip(x[t], fp8_act, quant).T @ _col_roundtrip(dh, fp8_act, quant)
             if with_bias:
                 db2[e] = np.sum(sr * g, axis=0)

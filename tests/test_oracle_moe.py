@@ -342,3 +342,30 @@ def test_num_valid_tokens_equals_the_truncated_problem():
     assert np.allclose(full["ds"][:n], part["ds"]) and np.all(full["ds"][n:] == 0)
     assert np.array_equal(om.valid_token_ids(ids, 0), np.full_like(ids, -1))
     assert np.array_equal(om.valid_token_ids(ids, 100), ids)
+
+
+@pytest.mark.parametrize("affinity", [0, 1])
+def test_saved_dw_down_factors_reproduce_the_recomputed_ones(affinity):
+    """Passing the forward's own a (or s*a) and s*dout as saved factors changes nothing; a saved
+    factor that differs only in its affinity placement still gives the same dW2 (a' dout = a (s dout))."""
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=7, H=6, I=3, E=3, K=2, seed=33)
+    _, h = om.moe_forward(x, W1, b1, W2, b2, s, ids)
+    ref = om.moe_backward(x, dout, W1, W2, s, ids, h, b2=b2, with_bias=True, affinity=affinity)
+    a = om.silu(h[..., :3]) * h[..., 3:]
+    inter = s[..., None] * a if affinity == 1 else a
+    sdout = s[..., None] * dout[:, None, :]
+    got = om.moe_backward(x, dout, W1, W2, s, ids, h, b2=b2, with_bias=True, affinity=affinity, inter=inter,
+                          sdout=sdout)
+    for name in ("dx", "dW1", "dW2", "ds", "db1", "db2"):
+        assert np.allclose(got[name], ref[name], rtol=1e-13, atol=1e-13), name
+    other = om.moe_backward(x, dout, W1, W2, s, ids, h, b2=b2, with_bias=True, affinity=1 - affinity)
+    assert np.allclose(other["dW2"], ref["dW2"], rtol=1e-13, atol=1e-13)
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=40, H=64, I=32, E=3, K=2, seed=34)
+    _, h = om.moe_forward(x, W1, b1, W2, b2, s, ids)
+    a = om.silu(h[..., :32]) * h[..., 32:]
+    inter = s[..., None] * a if affinity == 1 else a
+    sdout = s[..., None] * dout[:, None, :]
+    mq = om.moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=affinity)
+    mg = om.moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=affinity, inter=om._to_f32(inter),
+                               sdout=om._to_f32(sdout) if affinity == 0 else None)
+    assert np.array_equal(mq["dW2"], mg["dW2"])
