@@ -41,7 +41,10 @@ struct GemmCfg {
   // exchange of each quarter (double-buffered by chunk parity) and a double-buffered checkpoint chunk
   // (gate and up, 32 features x 128 tile rows each) filled by TMA one chunk ahead.
   static constexpr int G1_NC = 32 / kG1Subs;
-  static constexpr int EPI_WARP_BYTES = (EPI == kEpiDSwiGLU) ? 3 * G1_NC * 33 * 4 : 0;
+  // fp32 transpose buffers per warp: MXFP8 shares one between the three transposes (the shared memory
+  // saved buys a fifth pipeline stage); BF16 has stages enough and keeps three, which overlap
+  static constexpr int G1_TBUFS = MX ? 1 : 3;
+  static constexpr int EPI_WARP_BYTES = (EPI == kEpiDSwiGLU) ? G1_TBUFS * G1_NC * 33 * 4 : 0;
   static constexpr int XCHG_QUARTER = kG1Subs * 2 * 32;  // floats: [slice][gate|up][lane]
   static constexpr int XCHG_BYTES = (EPI == kEpiDSwiGLU) ? 2 * 4 * XCHG_QUARTER * 4 : 0;
   static constexpr int CK_CHUNK_BYTES = 2 * 32 * 128 * 2;
@@ -249,7 +252,7 @@ __device__ __forceinline__ void group_bar(int id) {
 // MXFP8 groups of dh (32 features) span the 32/NC warps of a TMEM lane quarter: partial amax values
 // are exchanged through `xchg` ([slice][gate|up][32 lanes]) with a barrier over those warps.
 // Padding rows produce zeros.
-template <bool MX, int NC, int AF>
+template <bool MX, int NC, int AF, bool GENERIC>
 __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t taddr, int64_t prow, int m, int lane,
                                                  bool valid, float sv, int i0, int sub, const uint16_t* ck,
                                                  float* tbuf, float* xchg, int bar_id, float& ds_acc) {
@@ -264,7 +267,8 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
   else
     tmem_ld_32x32b_x8(taddr, r);
   float dg[NC], du[NC], ap[NC];  // act(g), a and up * act'(g) first, the gradients after the load
-  if (p.glu == MOE_GLU_GEGLU) {  // GELU(g) = g Phi(g), GELU'(g) = Phi(g) + g phi(g)
+  // GENERIC: the activation and the gate/up layout are read at run time; otherwise SwiGLU, concat
+  if (GENERIC && p.glu == MOE_GLU_GEGLU) {  // GELU(g) = g Phi(g), GELU'(g) = Phi(g) + g phi(g)
 #pragma unroll
     for (int jj = 0; jj < NC; ++jj) {
       float g = bf16_bits_to_float(ck[(sub * NC + jj) * 128 + m]);
@@ -302,7 +306,7 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
     ap[jj] = p.affinity_on_i ? sv * a : a;
   }
   const int c0 = i0 + sub * NC;  // first feature of this warp's columns
-  const bool il = NC == 16 && p.interleaved;  // gate_i, up_i at columns 2i, 2i+1 (host: NC == 16)
+  const bool il = GENERIC && NC == 16 && p.interleaved;  // gate_i, up_i at columns 2i, 2i+1 (host: NC == 16)
   if (il) {
     // this warp's 16 (gate, up) pairs are the 32 consecutive columns 2*c0.. of dh: one MX group
     group_bar<32 * SUBS>(bar_id);  // keep the barrier count identical on every path
@@ -377,10 +381,12 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
     }
   }
   // dh^T rows in W1's gate/up layout, a'^T rows by feature
+  // MXFP8: the three transposes share the warp's buffer (each ends with the warp's reads done)
+  constexpr int TB = MX ? 0 : NC * 33;
   store_transposed<MX, NC, AF>(tbuf, dg, p.dht, p.dht_sf, P, il ? 2 * c0 : c0, il ? 2 : 1, p0, lane);
-  store_transposed<MX, NC, AF>(tbuf + NC * 33, du, p.dht, p.dht_sf, P, il ? 2 * c0 + 1 : I + c0, il ? 2 : 1, p0, lane);
+  store_transposed<MX, NC, AF>(tbuf + TB, du, p.dht, p.dht_sf, P, il ? 2 * c0 + 1 : I + c0, il ? 2 : 1, p0, lane);
   if (p.apt)  // a'^T (null: built from a saved checkpoint of a or s*a)
-    store_transposed<MX, NC, AF>(tbuf + 2 * NC * 33, ap, p.apt, p.apt_sf, P, c0, 1, p0, lane);
+    store_transposed<MX, NC, AF>(tbuf + 2 * TB, ap, p.apt, p.apt_sf, P, c0, 1, p0, lane);
 }
 
 
@@ -784,12 +790,24 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
             const int i0 = ti.nt * BN + c * 32;
             const uint16_t* ckb = reinterpret_cast<const uint16_t*>(smCK + buf * C::CK_CHUNK_BYTES);
             float* xc = xchg + (int)(ck_next & 1) * (4 * C::XCHG_QUARTER);
-            if (!MX || p.fmt_act == MOE_FP8_E5M2)  // the activation format, fixed per instantiation
-              epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2>(p, ta, prow, m, lane, valid, sv, i0, half, ckb,
-                                                          reinterpret_cast<float*>(wsm), xc, 2 + q, ds_acc);
-            else
-              epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3>(p, ta, prow, m, lane, valid, sv, i0, half, ckb,
-                                                          reinterpret_cast<float*>(wsm), xc, 2 + q, ds_acc);
+            // the activation format fixed per instantiation; SwiGLU with concat gate/up specialised
+            const bool generic = p.glu != MOE_GLU_SWIGLU || p.interleaved;
+            float* tb = reinterpret_cast<float*>(wsm);
+            if (!MX || p.fmt_act == MOE_FP8_E5M2) {
+              if (generic)
+                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2, true>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, tb,
+                                                                  xc, 2 + q, ds_acc);
+              else
+                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2, false>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, tb,
+                                                                   xc, 2 + q, ds_acc);
+            } else {
+              if (generic)
+                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3, true>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, tb,
+                                                                  xc, 2 + q, ds_acc);
+              else
+                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3, false>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, tb,
+                                                                   xc, 2 + q, ds_acc);
+            }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&ck_empty[buf]);  // this warp no longer reads the buffer
