@@ -217,7 +217,7 @@ __device__ __forceinline__ void store_transposed(float* buf, const float (&v)[NC
     uint32_t q[NC / 4];
 #pragma unroll
     for (int w = 0; w < NC / 4; ++w)
-      q[w] = fp8x4_t<AF, false>(col[4 * w] * inv, col[4 * w + 1] * inv, col[4 * w + 2] * inv, col[4 * w + 3] * inv);
+      q[w] = fp8x4_t<AF>(col[4 * w] * inv, col[4 * w + 1] * inv, col[4 * w + 2] * inv, col[4 * w + 3] * inv);
     uint8_t* dst = static_cast<uint8_t*>(out) + (row0 + (int64_t)c * rstride) * P + p0 + rg * NC;
     if constexpr (NC == 16)
       *reinterpret_cast<uint4*>(dst) = make_uint4(q[0], q[1], q[2], q[3]);
@@ -319,7 +319,7 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
       uint32_t q[NC / 2];
 #pragma unroll
       for (int w = 0; w < NC / 2; ++w)
-        q[w] = fp8x4_t<AF, false>(dg[2 * w] * inv, du[2 * w] * inv, dg[2 * w + 1] * inv, du[2 * w + 1] * inv);
+        q[w] = fp8x4_t<AF>(dg[2 * w] * inv, du[2 * w] * inv, dg[2 * w + 1] * inv, du[2 * w + 1] * inv);
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dh) + prow * (2 * (int64_t)I) + 2 * c0);
 #pragma unroll
       for (int w = 0; w < NC / 8; ++w) dst[w] = make_uint4(q[4 * w], q[4 * w + 1], q[4 * w + 2], q[4 * w + 3]);
@@ -353,8 +353,8 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
     uint32_t qg[NC / 4], qu[NC / 4];
 #pragma unroll
     for (int w = 0; w < NC / 4; ++w) {
-      qg[w] = fp8x4_t<AF, false>(dg[4 * w] * ig, dg[4 * w + 1] * ig, dg[4 * w + 2] * ig, dg[4 * w + 3] * ig);
-      qu[w] = fp8x4_t<AF, false>(du[4 * w] * iu, du[4 * w + 1] * iu, du[4 * w + 2] * iu, du[4 * w + 3] * iu);
+      qg[w] = fp8x4_t<AF>(dg[4 * w] * ig, dg[4 * w + 1] * ig, dg[4 * w + 2] * ig, dg[4 * w + 3] * ig);
+      qu[w] = fp8x4_t<AF>(du[4 * w] * iu, du[4 * w + 1] * iu, du[4 * w + 2] * iu, du[4 * w + 3] * iu);
     }
     if constexpr (NC == 16) {
       *reinterpret_cast<uint4*>(dh + c0) = make_uint4(qg[0], qg[1], qg[2], qg[3]);

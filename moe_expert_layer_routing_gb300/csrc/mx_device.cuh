@@ -20,14 +20,6 @@ __device__ __forceinline__ float e8m0_inv_scale(uint32_t byte) {
   return __uint_as_float((254u - byte) << 23);
 }
 
-// Round-to-nearest-even FP8 code of x, saturating to the largest finite value; zero -> 0x00.
-__device__ __forceinline__ uint32_t fp8_code(float x, int fmt) {
-  const __nv_fp8_storage_t c =
-      __nv_cvt_float_to_fp8(x, __NV_SATFINITE, fmt == MOE_FP8_E4M3 ? __NV_E4M3 : __NV_E5M2);
-  const uint32_t u = (uint32_t)c;
-  return (u & 0x7Fu) ? u : 0u;
-}
-
 // Byte offset of the scale of element (r, c) of an [R, C] matrix quantised along C, in the tiled
 // layout consumed by the block-scaled MMA: 512-byte atoms of 128 rows x 4 groups, atom grid
 // row-major over (R/128, C/128), inside an atom (r%32)*16 + ((r%128)/32)*4 + (c/32)%4.
@@ -49,7 +41,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Four FP8 codes (little-endian in one word) of a, b, c, d: two paired round-to-nearest-even
-// saturating conversions, then every code with zero magnitude made +0 (code 0x00).
+// saturating conversions (the sign is kept: a negative value rounding to zero gives -0, 0x80).
 __device__ __forceinline__ uint32_t fp8x4(float a, float b, float c, float d, int fmt) {
   uint16_t lo, hi;
   if (fmt == MOE_FP8_E4M3) {
@@ -59,15 +51,11 @@ __device__ __forceinline__ uint32_t fp8x4(float a, float b, float c, float d, in
     asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
     asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
   }
-  const uint32_t w = (uint32_t)lo | ((uint32_t)hi << 16);
-  const uint32_t mag = w & 0x7F7F7F7Fu;
-  const uint32_t nonzero = (mag + 0x7F7F7F7Fu) & 0x80808080u;  // per byte: 0x80 iff magnitude != 0
-  return mag | (w & nonzero);
+  return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-// fp8x4 with the format fixed at compile time; CANON = false keeps the sign of codes that round to
-// zero (a -0 code, numerically zero for the tensor cores that consume it).
-template <int FMT, bool CANON>
+// fp8x4 with the format fixed at compile time.
+template <int FMT>
 __device__ __forceinline__ uint32_t fp8x4_t(float a, float b, float c, float d) {
   uint16_t lo, hi;
   if constexpr (FMT == MOE_FP8_E4M3) {
@@ -77,11 +65,7 @@ __device__ __forceinline__ uint32_t fp8x4_t(float a, float b, float c, float d) 
     asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
     asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
   }
-  const uint32_t w = (uint32_t)lo | ((uint32_t)hi << 16);
-  if constexpr (!CANON) return w;
-  const uint32_t mag = w & 0x7F7F7F7Fu;
-  const uint32_t nonzero = (mag + 0x7F7F7F7Fu) & 0x80808080u;
-  return mag | (w & nonzero);
+  return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
 // Quantise 32 values of one group into 32 FP8 codes (packed little-endian into 8 words) and
@@ -98,7 +82,7 @@ __device__ __forceinline__ uint32_t quantize_group32(const float (&v)[32], int f
   return byte;
 }
 
-// quantize_group32 with the format fixed at compile time (canonical +0 codes).
+// quantize_group32 with the format fixed at compile time.
 template <int FMT>
 __device__ __forceinline__ uint32_t quantize_group32_t(const float (&v)[32], uint32_t (&w)[8]) {
   float am = 0.f;
@@ -108,7 +92,7 @@ __device__ __forceinline__ uint32_t quantize_group32_t(const float (&v)[32], uin
   const float inv = e8m0_inv_scale(byte);
 #pragma unroll
   for (int j = 0; j < 8; ++j)
-    w[j] = fp8x4_t<FMT, true>(v[4 * j] * inv, v[4 * j + 1] * inv, v[4 * j + 2] * inv, v[4 * j + 3] * inv);
+    w[j] = fp8x4_t<FMT>(v[4 * j] * inv, v[4 * j + 1] * inv, v[4 * j + 2] * inv, v[4 * j + 3] * inv);
   return byte;
 }
 

@@ -99,8 +99,8 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
           const uint32_t byte = e8m0_byte(__float_as_uint(am), AF);
           const float inv = e8m0_inv_scale(byte);
           uint2 q;
-          q.x = fp8x4_t<AF, true>(d8[0] * inv, d8[1] * inv, d8[2] * inv, d8[3] * inv);
-          q.y = fp8x4_t<AF, true>(d8[4] * inv, d8[5] * inv, d8[6] * inv, d8[7] * inv);
+          q.x = fp8x4_t<AF>(d8[0] * inv, d8[1] * inv, d8[2] * inv, d8[3] * inv);
+          q.y = fp8x4_t<AF>(d8[4] * inv, d8[5] * inv, d8[6] * inv, d8[7] * inv);
           *reinterpret_cast<uint2*>(static_cast<uint8_t*>(rowdst) + prow * H + col) = q;
           if ((lane & 3) == 0) rowsf[sf_tiled_offset(prow, col, H)] = (uint8_t)byte;
         } else {

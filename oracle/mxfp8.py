@@ -10,8 +10,9 @@ float8_dtype default "float8_e5m2").  The scale rule is the OCP Microscaling (MX
     element    = RNE(v / 2^(byte - 127)) in the FP8 format, saturating to +-max finite
 
 with floor(log2(amax)) read off the binary exponent of amax (exact, no log), amax = 0 (or a
-subnormal amax) giving byte 0, and a zero result encoded as +0 (code 0x00).  NaN / Inf inputs are
-outside the contract.
+subnormal amax) giving byte 0.  The sign is kept: a negative value (or -0) that rounds to zero
+gives -0 (code 0x80), as torch's float8 dtypes (the matmul page's float8_dtype) convert.  NaN / Inf
+inputs are outside the contract.
 
 Bit-exact by construction: the decode tables come from the format definitions; encoding is the
 nearest table value with ties going to the even code.
@@ -51,7 +52,8 @@ def fp8_max(fmt: int) -> float:
 
 
 def fp8_encode(y: np.ndarray, fmt: int) -> np.ndarray:
-    """Round-to-nearest-even into the FP8 format, saturating to +-max; zero -> code 0x00."""
+    """Round-to-nearest-even into the FP8 format, saturating to +-max; the sign bit is kept (a
+    negative value rounding to zero gives -0)."""
     y = np.asarray(y, dtype=np.float64)
     table = fp8_decode_table(fmt)
     maxc = _SPEC[fmt][4]
@@ -63,7 +65,7 @@ def fp8_encode(y: np.ndarray, fmt: int) -> np.ndarray:
     d_lo = a - pos[lo]
     pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
     mag = np.where(pick_hi, hi, lo).astype(np.uint8)
-    sign = ((y < 0) & (mag != 0)).astype(np.uint8) << 7
+    sign = np.signbit(y).astype(np.uint8) << 7
     return (mag | sign).astype(np.uint8)
 
 

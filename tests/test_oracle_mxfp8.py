@@ -33,8 +33,7 @@ def test_encode_matches_torch_rne_on_all_bf16_patterns(fmt):
         w = v * 2.0 ** shift
         ok = torch.isfinite(w) & (w.abs() <= vmax)
         w = w[ok]
-        ref = w.to(TORCH_FMT[fmt]).view(torch.uint8).numpy().copy()
-        ref[(ref & 0x7F) == 0] = 0              # zero is encoded as +0 (oracle convention)
+        ref = w.to(TORCH_FMT[fmt]).view(torch.uint8).numpy().copy()   # signed zeros included
         ours = mx.fp8_encode(w.numpy(), fmt)
         assert np.array_equal(ours, ref), f"shift {shift}"
 
