@@ -34,7 +34,10 @@ struct GemmCfg {
   static constexpr int A_BYTES = BM * BK_BYTES;
   static constexpr int B_BYTES = BN * BK_BYTES;
   static constexpr int SFA_BYTES = MX ? 512 : 0;
-  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
+  // scales of B: one 512-byte atom per 128 rows; a 192-column tile takes two atoms (the second half
+  // padding), so its scales come re-tiled per tile (see sf_retile_tiles)
+  static constexpr int SFB_ATOMS = (BN + 127) / 128;
+  static constexpr int SFB_BYTES = MX ? SFB_ATOMS * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   // dSwiGLU epilogue: 4 * kG1Subs warps (kG1Subs per TMEM lane quarter, each taking NC = 32 / kG1Subs
   // of every 32 columns), three NC x 32 fp32 transposition buffers per warp, the row-wise amax
@@ -71,8 +74,10 @@ struct GemmCfg {
   static constexpr int STAGES_FIT = (kSmemLimit - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int ACC_STAGES = (MX && BN == 256) ? 1 : 2;
-  static constexpr int SF_COLS = MX ? 4 + 4 * (BN / 128) : 0;   // TMEM columns of scales per stage
-  static constexpr int SF_BASE = ACC_STAGES * BN;
+  static constexpr int SF_COLS = MX ? 4 + 4 * SFB_ATOMS : 0;   // TMEM columns of scales per stage
+  // TMEM column distance of the two accumulators: 192-column tiles keep them 256 apart
+  static constexpr int ACC_STRIDE = BN == 192 ? 256 : BN;
+  static constexpr int SF_BASE = (ACC_STAGES - 1) * ACC_STRIDE + BN;
   static constexpr int COLS_NEEDED = SF_BASE + STAGES * SF_COLS;
   static constexpr int TMEM_COLS = COLS_NEEDED <= 32 ? 32 : COLS_NEEDED <= 64 ? 64 : COLS_NEEDED <= 128 ? 128
                                  : COLS_NEEDED <= 256 ? 256 : 512;
@@ -493,9 +498,10 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
             bulk_load(smSFA + s * C::SFA_BYTES, p.sfa + ((int64_t)(ti.a_row / 128) * p.sfa_ktiles + kt) * 512, 512,
                       &full[s]);
 #pragma unroll
-            for (int h = 0; h < BN / 128; ++h)
+            for (int h = 0; h < C::SFB_ATOMS; ++h)
               bulk_load(smSFB + s * C::SFB_BYTES + h * 512,
-                        p.sfb + ((int64_t)(ti.b_row / 128 + h) * p.sfb_ktiles + kt) * 512, 512, &full[s]);
+                        p.sfb + ((int64_t)((ti.b_row / BN) * C::SFB_ATOMS + h) * p.sfb_ktiles + kt) * 512, 512,
+                        &full[s]);
           }
           ++issued;
           if (++s == C::STAGES) {
@@ -532,7 +538,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         const TileInfo ti = gemm_decode_tile<BN, C::BKE>(p, t);
         if (!mbar_wait_bounded(&tempty[acc], aph ^ 1u, p.status, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        const uint32_t d = tmem_base + (uint32_t)(acc * C::ACC_STRIDE);
         for (int kb = 0; kb < ti.nk; ++kb) {
           if (!mbar_wait_bounded(&full[s], ph, p.status, abort_flag)) {
             ok = false;
@@ -546,7 +552,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
             const uint32_t sfb_t = sfa_t + 4;
             tmem_cp_32x128b_warpx4(sfa_t, make_smem_desc(smem_u32(smSFA + s * C::SFA_BYTES), 0, 128, kSwizzleNone));
 #pragma unroll
-            for (int h = 0; h < BN / 128; ++h)
+            for (int h = 0; h < C::SFB_ATOMS; ++h)
               tmem_cp_32x128b_warpx4(sfb_t + 4 * h, make_smem_desc(smem_u32(smSFB + s * C::SFB_BYTES + h * 512), 0,
                                                                    128, kSwizzleNone));
 // one MMA per 32-wide K step over all BN columns; the scales of B rows 128..255 sit in the four
@@ -651,7 +657,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+      const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
       if constexpr (C::CKPT_STORE) {
         // two 32-feature chunks per step, one per warp half: h = acc + b1_e (bf16) staged as
         // [32 features][128 rows] and stored to the checkpoint rows of the tile's block

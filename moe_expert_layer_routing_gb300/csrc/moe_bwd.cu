@@ -92,7 +92,7 @@ enum Region {
   R_CHUNK_COUNTS, R_EXPERT_OFFSETS, R_BLOCK_OFFSETS, R_TILE_OFFSETS, R_EXPERT_ORDER, R_SCALARS,
   R_X_GATHER, R_S_SCATTER, R_S_REV, R_TPID, R_B2E, R_TILE_ROW_FLAT, R_FLAT_TILE_ROW, R_TILE_EXPERT,
   R_DOUT_G, R_DOUT_G_SF, R_DOUT_GT, R_DOUT_GT_SF, R_X_GT, R_X_GT_SF, R_DH, R_DH_SF, R_DH_T, R_DH_T_SF,
-  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_X_G, R_X_G_SF, R_CKPT, R_PAIR_OFFSETS, R_TILE_ORDER, R_TILE_ROW_SLOT, R_COUNT
+  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_X_G, R_X_G_SF, R_CKPT, R_PAIR_OFFSETS, R_TILE_ORDER, R_TILE_ROW_SLOT, R_W2_SF_T, R_COUNT
 };
 
 struct Layout {
@@ -117,12 +117,13 @@ static int64_t blocks_bound(int64_t T, int K, int E, int B) {
   return (num + B - 1) / B + E - 1;
 }
 
-// Tile-width override for tuning runs: the variable, if set to 128 or 256 dividing n, wins.
-static int bn_override(const char* name, int dflt, int64_t n) {
+// Tile-width override for tuning runs: the variable, if set to 128 or 256 (or 192 where allowed)
+// dividing n, wins.
+static int bn_override(const char* name, int dflt, int64_t n, bool allow192 = false) {
   const char* v = getenv(name);
   if (!v) return dflt;
   const int bn = atoi(v);
-  return (bn == 128 || bn == 256) && n % bn == 0 ? bn : dflt;
+  return (bn == 128 || bn == 256 || (allow192 && bn == 192)) && n % bn == 0 ? bn : dflt;
 }
 
 static Layout make_layout(const MoeBwdArgs& a) {
@@ -132,13 +133,14 @@ static Layout make_layout(const MoeBwdArgs& a) {
   L.TK = (int64_t)a.T * a.K;
   L.P = tile_capacity(L.TK, a.E);
   L.Nb = blocks_bound(a.T, a.K, a.E, a.block_size);
-  // N-tile widths: G1 carries the heavy dSwiGLU epilogue, so it takes 128 columns with a
-  // double-buffered TMEM accumulator; the store-epilogue GEMMs take 256 where N allows.
-  L.BN1 = 128;
+  // N-tile widths: G1 carries the heavy dSwiGLU epilogue, so it keeps a double-buffered TMEM
+  // accumulator: 128 columns, or for MXFP8 192 where I allows (two 192-column accumulators and the
+  // scales fit TMEM; 256 would leave room for one); the store-epilogue GEMMs take 256 where N allows.
+  L.BN1 = mx && a.I % 192 == 0 ? 192 : 128;
   L.BN2 = a.H % 256 == 0 ? 256 : 128;
   L.BN3 = L.BN2;
   L.BN4 = 256;
-  L.BN1 = bn_override("MOEBWD_BN_G1", L.BN1, a.I);
+  L.BN1 = bn_override("MOEBWD_BN_G1", L.BN1, a.I, mx);
   L.BN2 = bn_override("MOEBWD_BN_G2", L.BN2, a.H);
   L.BN3 = bn_override("MOEBWD_BN_G3", L.BN3, a.H);
   L.BN4 = bn_override("MOEBWD_BN_G4", L.BN4, 2 * a.I);
@@ -174,6 +176,8 @@ static Layout make_layout(const MoeBwdArgs& a) {
   b[R_PAIR_OFFSETS] = sizeof(int32_t) * (E + 1);
   b[R_TILE_ORDER] = sizeof(int32_t) * (size_t)(P / kTileM + 1);
   b[R_TILE_ROW_SLOT] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, P);  // saved s*dout rows (pointers not read)
+  // W2's scales re-tiled for 192-column G1 tiles: two atoms per tile
+  if (mx && L.BN1 % 128) b[R_W2_SF_T] = (size_t)(E * I / L.BN1) * ((L.BN1 + 127) / 128) * (size_t)(H / 128) * 512;
   if (a.act_src == MOE_ACT_RECOMPUTE) {
     b[R_X_G] = (size_t)(P * H * es);
     b[R_X_G_SF] = mx ? (size_t)(P * H / 32) : 0;
@@ -525,6 +529,11 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.b_rows_per_expert = (int)I;
     p.sfa = reg<uint8_t>(L, ws, R_DOUT_G_SF);
     p.sfb = a.W2_sf;
+    if (mx && L.BN1 % 128) {  // W2's scales in whole atoms per 192-row tile
+      uint8_t* t = reg<uint8_t>(L, ws, R_W2_SF_T);
+      if ((rc = launch_sf_retile(a.W2_sf, E * I, H, L.BN1, t, st))) return rc;
+      p.sfb = t;
+    }
     p.sfa_ktiles = p.sfb_ktiles = (int)(H / 128);
     p.fmt_a = a.fp8_act; p.fmt_b = a.fp8_w;
     p.epi = kEpiDSwiGLU;

@@ -94,6 +94,10 @@ int launch_tile_row_slot(int64_t P, int B, const int32_t* num_tiles, const int32
                          const int32_t* tile_offsets, const int32_t* block_offsets, const int32_t* tile_row_flat,
                          int32_t* slot, cudaStream_t st);
 
+// scales of an [R, C] MXFP8 B operand re-tiled into ceil(bn / 128) atoms per bn-row tile
+// (R % bn == 0, R and C multiples of 128); dst holds (R / bn) * ceil(bn / 128) * (C / 128) * 512 bytes
+int launch_sf_retile(const uint8_t* src, int64_t R, int64_t C, int bn, uint8_t* dst, cudaStream_t st);
+
 int launch_quant_rowwise(const uint16_t* in, int64_t src_rows, int64_t rows, int64_t cols, int64_t ld,
                          const int32_t* row_index, int fmt, uint8_t* q, uint8_t* sf, int tiled, cudaStream_t st);
 // colwise: out is the transposed [cols, rows] matrix, fp8 (+scales) when mx, else bf16

@@ -291,6 +291,42 @@ int launch_tile_row_slot(int64_t P, int B, const int32_t* num_tiles, const int32
   return cuda_check(cudaGetLastError(), "tile_row_slot");
 }
 
+// Scales of a [R, C] MXFP8 operand (tiled layout, 128-row atoms) re-tiled for B tiles of `bn` rows
+// (bn % 128 != 0): tile j's scales fill ceil(bn / 128) whole atoms, rows j*bn .. j*bn + bn - 1 in
+// order and the rest of the last atom zero.  The four scale bytes of one row inside an atom are
+// contiguous in both layouts, so each thread moves one 32-bit word.
+__global__ void __launch_bounds__(256) sf_retile_kernel(const uint32_t* __restrict__ src, int64_t R, int64_t C,
+                                                        int bn, int atoms, uint32_t* __restrict__ dst) {
+  const int64_t ktiles = C / 128;
+  const int64_t words = (R / bn) * atoms * ktiles * 128;
+  const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (w >= words) return;
+  const int r = (int)(w & 127);           // row inside the destination atom
+  const int64_t a = w >> 7;               // destination atom: ((tile * atoms + h) * ktiles + kt)
+  const int64_t kt = a % ktiles;
+  const int64_t th = a / ktiles;
+  const int h = (int)(th % atoms);
+  const int64_t tile = th / atoms;
+  const int tr = h * 128 + r;              // row inside the tile
+  uint32_t v = 0u;
+  if (tr < bn) {
+    const int64_t sr = tile * bn + tr;     // source row
+    v = src[(((sr >> 7) * ktiles + kt) * 512 + (sr & 31) * 16 + ((sr & 127) >> 5) * 4) >> 2];
+  }
+  dst[(a * 512 + (r & 31) * 16 + (r >> 5) * 4) >> 2] = v;
+}
+
+int launch_sf_retile(const uint8_t* src, int64_t R, int64_t C, int bn, uint8_t* dst, cudaStream_t st) {
+  if (bn <= 0 || R % bn || R % 128 || C % 128) return fail(MOE_ERR_INVALID, "sf_retile: bad sizes");
+  const int atoms = (bn + 127) / 128;
+  const int64_t words = (R / bn) * atoms * (C / 128) * 128;
+  if (words == 0) return MOE_OK;
+  sf_retile_kernel<<<(unsigned)((words + 255) / 256), 256, 0, st>>>(reinterpret_cast<const uint32_t*>(src), R, C,
+                                                                    bn, atoms, reinterpret_cast<uint32_t*>(dst));
+  count_launch();
+  return cuda_check(cudaGetLastError(), "sf_retile");
+}
+
 // ------------------------------------------------------------------------------------------
 // generic quantisers
 // ------------------------------------------------------------------------------------------
