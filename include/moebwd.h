@@ -243,6 +243,12 @@ typedef struct MoeBwdArgs {
                                            only; preferred over intermediate_ckpt */
   const void* down_proj_act_ckpt;       /* [N,B,H] s*dout per slot (down_proj_act_checkpoint), affinity
                                            on H only; also the rows summed into db2 */
+  /* [BW] gate_act_checkpoint_T: (device) bf16 [N,I,B] act(gate) saved by the forward (SiLU, or GELU
+   * with MOE_GLU_GEGLU), in the block layout of gate_up_ckpt, or NULL.  Given, the dSwiGLU step takes
+   * act(gate) from it wherever the activation's value enters (a = act(gate)*up for ds and the dW_down
+   * factor, dup = dA*act(gate)); act'(gate) in dgate still needs the pre-activation, so gate_up_ckpt
+   * (or the recomputation) stays required.  16-byte aligned. */
+  const void* gate_act_ckpt;
 } MoeBwdArgs;
 
 /* Bytes of workspace moe_bwd needs for these shapes and options (pointers are not read). */

@@ -51,7 +51,8 @@ class MoeBwdArgs(ctypes.Structure):
                [("workspace_bytes", ctypes.c_size_t), ("accumulate", ctypes.c_int), ("act_src", ctypes.c_int)] + \
                [(n, ctypes.c_void_p) for n in ("W1t", "W1t_q", "W1t_sf", "b1", "ds_masked", "num_valid_tokens")] + \
                [(n, ctypes.c_int) for n in ("glu", "gate_up_layout")] + \
-               [(n, ctypes.c_void_p) for n in ("intermediate_ckpt", "scaled_intermediate_ckpt", "down_proj_act_ckpt")]
+               [(n, ctypes.c_void_p) for n in ("intermediate_ckpt", "scaled_intermediate_ckpt", "down_proj_act_ckpt",
+                                               "gate_act_ckpt")]
 
 
 _lib = None
@@ -240,16 +241,18 @@ class MoeBwd:
 
     def bind(self, *, x, dout, s, ids, ckpt=None, W1=None, W2=None, W1_q=None, W1_sf=None, W2_q=None, W2_sf=None,
              b2=None, W1t=None, W1t_q=None, W1t_sf=None, b1=None, num_valid_tokens=None, intermediate_ckpt=None,
-             scaled_intermediate_ckpt=None, down_proj_act_ckpt=None):
+             scaled_intermediate_ckpt=None, down_proj_act_ckpt=None, gate_act_ckpt=None):
         """ckpt: the [N,2,I,B] checkpoint (act_src ACT_CHECKPOINT).  W1t (bf16 [E,2I,H]) or W1t_q/W1t_sf
-        and optionally b1 [E,2I]: the operands of the recomputation (act_src ACT_RECOMPUTE)."""
+        and optionally b1 [E,2I]: the operands of the recomputation (act_src ACT_RECOMPUTE).
+        intermediate_ckpt / scaled_intermediate_ckpt / gate_act_ckpt [N,I,B] and down_proj_act_ckpt
+        [N,B,H] (bf16, block layout): saved forward values, see the MoeBwdArgs fields."""
         _need_cuda(x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2, W1t, W1t_q, W1t_sf, b1, num_valid_tokens,
-                   intermediate_ckpt, scaled_intermediate_ckpt, down_proj_act_ckpt)
+                   intermediate_ckpt, scaled_intermediate_ckpt, down_proj_act_ckpt, gate_act_ckpt)
         if num_valid_tokens is not None:
             assert num_valid_tokens.dtype == torch.int32 and num_valid_tokens.numel() == 1
         a = self.a
         Nb = num_blocks_bound(a.T, a.K, a.E, a.block_size)
-        for t in (intermediate_ckpt, scaled_intermediate_ckpt):
+        for t in (intermediate_ckpt, scaled_intermediate_ckpt, gate_act_ckpt):
             assert t is None or (t.dtype == torch.bfloat16 and tuple(t.shape) == (Nb, a.I, a.block_size))
         assert down_proj_act_ckpt is None or (down_proj_act_ckpt.dtype == torch.bfloat16 and
                                               tuple(down_proj_act_ckpt.shape) == (Nb, a.block_size, a.H))
@@ -269,7 +272,7 @@ class MoeBwd:
                             W1_sf=W1_sf, W2_q=W2_q, W2_sf=W2_sf, b2=b2, W1t=W1t, W1t_q=W1t_q, W1t_sf=W1t_sf,
                             b1=b1, num_valid_tokens=num_valid_tokens, intermediate_ckpt=intermediate_ckpt,
                             scaled_intermediate_ckpt=scaled_intermediate_ckpt,
-                            down_proj_act_ckpt=down_proj_act_ckpt).items():
+                            down_proj_act_ckpt=down_proj_act_ckpt, gate_act_ckpt=gate_act_ckpt).items():
             setattr(a, name, None if t is None else t.data_ptr())
         for name in ("dx", "dW1", "dW2", "ds", "db1", "db2", "ds_masked", "status"):
             t = getattr(self, name)
@@ -277,7 +280,7 @@ class MoeBwd:
         a.workspace = self.workspace.data_ptr()
         a.workspace_bytes = self.workspace.numel()
         self._keep = [x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2, W1t, W1t_q, W1t_sf, b1,
-                      num_valid_tokens, intermediate_ckpt, scaled_intermediate_ckpt, down_proj_act_ckpt]
+                      num_valid_tokens, intermediate_ckpt, scaled_intermediate_ckpt, down_proj_act_ckpt, gate_act_ckpt]
         return self
 
     def run(self, stream=None):

@@ -256,11 +256,14 @@ __device__ __forceinline__ void group_bar(int id) {
 // and write dh [P,2I] (row-major), dh^T [2I,P], a'^T [I,P] (bf16, or fp8 + scales).  The row-wise
 // MXFP8 groups of dh (32 features) span the 32/NC warps of a TMEM lane quarter: partial amax values
 // are exchanged through `xchg` ([slice][gate|up][32 lanes]) with a barrier over those warps.
+// GENERIC with `ga` (this row's slot in a saved act(gate) checkpoint [N,I,B], feature stride B):
+// act(gate) is read from it, act'(gate) still computed from the pre-activation.
 // Padding rows produce zeros.
 template <bool MX, int NC, int AF, bool GENERIC>
 __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t taddr, int64_t prow, int m, int lane,
                                                  bool valid, float sv, int i0, int sub, const uint16_t* ck,
-                                                 float* tbuf, float* xchg, int bar_id, float& ds_acc) {
+                                                 const uint16_t* ga, float* tbuf, float* xchg, int bar_id,
+                                                 float& ds_acc) {
   constexpr int SUBS = 32 / NC;
   const int I = p.I;
   const int64_t P = p.P;
@@ -272,7 +275,17 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
   else
     tmem_ld_32x32b_x8(taddr, r);
   float dg[NC], du[NC], ap[NC];  // act(g), a and up * act'(g) first, the gradients after the load
-  // GENERIC: the activation and the gate/up layout are read at run time; otherwise SwiGLU, concat
+  // GENERIC: the activation, the gate/up layout and a saved act(gate) are read at run time;
+  // otherwise SwiGLU, concat
+  float sa[GENERIC ? NC : 1];
+  const bool saved = GENERIC && ga != nullptr;
+  if constexpr (GENERIC) {
+    if (saved) {
+#pragma unroll
+      for (int jj = 0; jj < NC; ++jj)
+        sa[jj] = valid ? bf16_bits_to_float(__ldg(ga + (int64_t)(i0 + sub * NC + jj) * p.B)) : 0.f;
+    }
+  }
   if (GENERIC && p.glu == MOE_GLU_GEGLU) {  // GELU(g) = g Phi(g), GELU'(g) = Phi(g) + g phi(g)
 #pragma unroll
     for (int jj = 0; jj < NC; ++jj) {
@@ -281,7 +294,8 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
       if (!valid) g = u = 0.f;
       const float cdf = 0.5f * (1.f + erff(g * 0.70710678118654752f));
       const float pdf = 0.39894228040143268f * __expf(-0.5f * g * g);
-      const float act = g * cdf;
+      float act = g * cdf;
+      if constexpr (GENERIC) act = saved ? sa[jj] : act;
       du[jj] = act;
       ap[jj] = act * u;
       dg[jj] = u * (cdf + g * pdf);
@@ -293,7 +307,8 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
       float u = bf16_bits_to_float(ck[32 * 128 + (sub * NC + jj) * 128 + m]);
       if (!valid) g = u = 0.f;
       const float sg = __fdividef(1.f, 1.f + __expf(-g));
-      const float sl = g * sg;
+      float sl = g * sg;
+      if constexpr (GENERIC) sl = saved ? sa[jj] : sl;
       du[jj] = sl;
       ap[jj] = sl * u;
       dg[jj] = u * (sg * (1.f + g * (1.f - sg)));
@@ -774,6 +789,13 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         const bool valid = row_f >= 0;
         const float sv = row_s;
         float ds_acc = 0.f;
+        const uint16_t* ga = nullptr;  // this row's slot in the saved act(gate) checkpoint
+        if (p.gate_act) {
+          int64_t blk;
+          int b0;
+          tile_ckpt_origin(p, ti, blk, b0);
+          ga = p.gate_act + blk * (int64_t)p.I * p.B + b0 + m;
+        }
 #pragma unroll 1
         for (int c = 0; c < C::NCHUNK; ++c) {
           if (ck_leader) {  // keep one chunk in flight ahead of the one being consumed
@@ -797,21 +819,21 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
             const uint16_t* ckb = reinterpret_cast<const uint16_t*>(smCK + buf * C::CK_CHUNK_BYTES);
             float* xc = xchg + (int)(ck_next & 1) * (4 * C::XCHG_QUARTER);
             // the activation format fixed per instantiation; SwiGLU with concat gate/up specialised
-            const bool generic = p.glu != MOE_GLU_SWIGLU || p.interleaved;
+            const bool generic = p.glu != MOE_GLU_SWIGLU || p.interleaved || p.gate_act != nullptr;
             float* tb = reinterpret_cast<float*>(wsm);
             if (!MX || p.fmt_act == MOE_FP8_E5M2) {
               if (generic)
-                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2, true>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, tb,
+                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2, true>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
                                                                   xc, 2 + q, ds_acc);
               else
-                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2, false>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, tb,
+                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2, false>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
                                                                    xc, 2 + q, ds_acc);
             } else {
               if (generic)
-                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3, true>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, tb,
+                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3, true>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
                                                                   xc, 2 + q, ds_acc);
               else
-                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3, false>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, tb,
+                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3, false>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
                                                                    xc, 2 + q, ds_acc);
             }
           }

@@ -223,7 +223,7 @@ static int check_args(const MoeBwdArgs* a, bool need_ptrs) {
   if (a->down_proj_act_ckpt && a->affinity != MOE_AFFINITY_ON_H)
     return fail(MOE_ERR_INVALID, "moe_bwd: down_proj_act_ckpt needs the affinity on H");
   {
-    const void* al[] = {a->intermediate_ckpt, a->scaled_intermediate_ckpt, a->down_proj_act_ckpt};
+    const void* al[] = {a->intermediate_ckpt, a->scaled_intermediate_ckpt, a->down_proj_act_ckpt, a->gate_act_ckpt};
     for (const void* q : al)
       if (reinterpret_cast<uintptr_t>(q) & 15) return fail(MOE_ERR_INVALID, "moe_bwd: checkpoints must be 16-byte aligned");
   }
@@ -547,6 +547,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.fmt_act = a.fp8_act;
     p.glu = a.glu;
     p.interleaved = a.gate_up_layout == MOE_GATE_UP_INTERLEAVED;
+    p.gate_act = static_cast<const uint16_t*>(a.gate_act_ckpt);
     p.P = P;
     p.dh = reg<void>(L, ws, R_DH); p.dh_sf = reg<uint8_t>(L, ws, R_DH_SF);
     p.dht = reg<void>(L, ws, R_DH_T); p.dht_sf = reg<uint8_t>(L, ws, R_DH_T_SF);

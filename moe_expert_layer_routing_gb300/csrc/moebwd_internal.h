@@ -149,6 +149,7 @@ struct GemmParams {
   int I, B, affinity_on_i, fmt_act;
   int glu;                      // MOE_GLU_SWIGLU or MOE_GLU_GEGLU
   int interleaved;              // dh (and W1, dW1, db1) columns: gate_i, up_i at 2i, 2i+1
+  const uint16_t* gate_act;     // [N,I,B] saved act(gate) (block layout) or null
   int64_t P;
   void* dh; uint8_t* dh_sf;
   void* dht; uint8_t* dht_sf;

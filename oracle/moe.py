@@ -165,7 +165,7 @@ def valid_token_ids(ids, num_valid):
 
 
 def moe_backward(x, dout, W1, W2, s, ids, h, b2=None, with_bias=False, activation="swiglu", gate_up="concat",
-                 affinity=1, inter=None, sdout=None):
+                 affinity=1, inter=None, sdout=None, gate_act=None):
     """All gradients of the MoE layer in float64 (the BF16 path's reference).
 
     x, dout [T,H]; W1 [E,H,2I]; W2 [E,I,H]; s [T,K]; ids [T,K]; h [T,K,2I] ([gate | up]); b2 [E,H]
@@ -177,6 +177,9 @@ def moe_backward(x, dout, W1, W2, s, ids, h, b2=None, with_bias=False, activatio
       inter [T,K,I]  the factor that carries the activation: s*a on I, a on H
                      (`scaled_intermediate_checkpoint_T` / `intermediate_checkpoint_T`)
       sdout [T,K,H]  s*dout on H (`down_proj_act_checkpoint`), also summed into db2
+    and `gate_act` [T,K,I] (`gate_act_checkpoint_T`, a saved act(gate)) replaces the recomputed
+    act(gate) wherever the activation's value enters: a = act(gate)*up (ds, the dW_down factor) and
+    dup = dA*act(gate); act'(gate) in dgate still comes from the pre-activation.
     """
     x, dout, s, h = map(_f64, (x, dout, s, h))
     b2 = _f64(b2)
@@ -200,7 +203,8 @@ def moe_backward(x, dout, W1, W2, s, ids, h, b2=None, with_bias=False, activatio
         W1e, W2e = _f64(W1[e]), _f64(W2[e])
         g = dout[t]                                   # gathered upstream gradient rows
         gate, up = h[t, k, :I], h[t, k, I:]
-        a = act(gate) * up
+        ag = act(gate) if gate_act is None else _f64(gate_act)[t, k]
+        a = ag * up
         sr = s[t, k][:, None]
         dA_raw = g @ W2e.T
         ds[t, k] = np.sum(dA_raw * a, axis=1)
@@ -209,7 +213,7 @@ def moe_backward(x, dout, W1, W2, s, ids, h, b2=None, with_bias=False, activatio
         dA = sr * dA_raw
         dh = np.zeros((t.size, I2))
         dh[:, gc] = dA * up * dact(gate)
-        dh[:, uc] = dA * act(gate)
+        dh[:, uc] = dA * ag
         av = (sr * a if affinity == 1 else a) if inter is None else _f64(inter)[t, k]
         gv = (g if affinity == 1 else sr * g) if sdout is None or affinity == 1 else _f64(sdout)[t, k]
         dW2[e] = av.T @ gv
@@ -248,7 +252,7 @@ def _col_roundtrip(v, fmt, quant):
 
 def moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=1, fp8_act=mx.E5M2, fp8_w=mx.E4M3,
                        b2=None, with_bias=False, experts=None, tokens=None, quant=None, activation="swiglu",
-                       gate_up="concat", inter=None, sdout=None):
+                       gate_up="concat", inter=None, sdout=None, gate_act=None):
     """MoE backward with every GEMM operand MXFP8-quantised along its contraction dimension.
 
     Quantisation points (reading of the MXFP8 blockwise backward page; weights pre-quantised,
@@ -264,7 +268,8 @@ def moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=1, fp8_act=mx.E5M2, 
     limits dx/ds to those tokens (both default to all).  `quant(v, fmt, axis)` defaults to the
     MX round trip; tests substitute the identity to check the wiring.  dh, W1_e, dW1 and db1 are in
     W1's gate/up layout, so the 32-column groups of Q_2I follow that layout.  `inter` and `sdout`
-    replace the dW_down factors as in moe_backward (saved forward values; quantised the same way).
+    replace the dW_down factors and `gate_act` the activation's value, as in moe_backward (saved
+    forward values; quantised the same way).
     """
     quant = quant or mx.mx_roundtrip
     x, dout, s, h = map(_f64, (x, dout, s, h))
@@ -302,7 +307,8 @@ def moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=1, fp8_act=mx.E5M2, 
         g = dout[t]
         gq = quant(g, fp8_act, 1)
         gate, up = h[t, k, :I], h[t, k, I:]
-        a = act(gate) * up
+        ag = act(gate) if gate_act is None else _f64(gate_act)[t, k]
+        a = ag * up
         sr = s[t, k][:, None]
         dA_raw = gq @ W2q.T
         dsv = np.sum(dA_raw * a, axis=1)
@@ -311,7 +317,7 @@ def moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=1, fp8_act=mx.E5M2, 
         dA = sr * dA_raw
         dh = np.zeros((t.size, I2))
         dh[:, gc] = dA * up * dact(gate)
-        dh[:, uc] = dA * act(gate)
+        dh[:, uc] = dA * ag
         dh = _to_f32(dh)
         dx_exp = _to_bf16(quant(dh, fp8_act, 1) @ W1q.T)
         tm = token_mask[t]

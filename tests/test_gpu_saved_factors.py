@@ -121,3 +121,51 @@ def test_saved_factors_are_used():
     got = op.outputs()
     ref = om.moe_backward(inp.x, inp.dout, inp.W1, inp.W2, inp.s, inp.ids.numpy(), h, affinity=0, inter=a2)
     compare_outputs(got, ref, BF16_TOL)
+
+
+GATE_ACT_CASES = [(PREC_BF16, AFFINITY_ON_H, "swiglu", "concat", 256, 1.0),
+                  (PREC_BF16, AFFINITY_ON_I, "geglu", "interleaved", 256, 2.0),
+                  (PREC_MXFP8, AFFINITY_ON_I, "swiglu", "concat", 384, 1.0),
+                  (PREC_MXFP8, AFFINITY_ON_H, "geglu", "interleaved", 256, 2.0),
+                  (PREC_MXFP8, AFFINITY_ON_I, "swiglu", "concat", 256, 2.0)]
+
+
+@pytest.mark.parametrize("prec,aff,glu,layout,I,c", GATE_ACT_CASES)
+def test_saved_gate_act(prec, aff, glu, layout, I, c):
+    """[BW] gate_act_checkpoint_T: a saved act(gate) (c = 1: the forward's own, rounded to bf16; c = 2:
+    a value the recomputation would not give) enters ds, a' and dup; the oracle gets the same values."""
+    import moe_expert_layer_routing_gb300 as mb
+    bias = prec == PREC_BF16
+    cfg = small_moe("gact", T=300, H=256, I=I, E=5, K=2, B=256, seed=84, precision=prec, affinity=aff, bias=bias)
+    inp = make_moe_inputs(cfg)
+    meta = oracle_meta(inp)
+    h = oracle_h(inp, meta)
+    T, K, B = cfg.T, cfg.K, cfg.block_size
+    Nb = mb.num_blocks_bound(T, K, cfg.E, B)
+    slot = _slots(meta, T, K, B)
+    ga = np.asarray(_bf16(c * om.ACTIVATIONS[glu][0](h[..., :I])).double())
+    d = to_device(inp)
+    op = mb.MoeBwd(T=T, H=cfg.H, I=I, E=cfg.E, K=K, block_size=B, precision=prec, affinity=aff, fp8_act=cfg.fp8_act,
+                   fp8_w=cfg.fp8_w, has_bias=bias, glu=mb.GLU_GEGLU if glu == "geglu" else mb.GLU_SWIGLU,
+                   gate_up_layout=mb.GATE_UP_INTERLEAVED if layout == "interleaved" else mb.GATE_UP_CONCAT)
+    kw = dict(x=d.x, dout=d.dout, s=d.s, ids=d.ids, ckpt=d.ckpt, b2=d.b2 if bias else None,
+              gate_act_ckpt=_bf16(_feature_major(ga, slot, Nb, B)).cuda())
+    if prec == PREC_MXFP8:
+        W1_q, W1_sf = mb.quantize_weights(d.W1, cfg.fp8_w)
+        W2_q, W2_sf = mb.quantize_weights(d.W2, cfg.fp8_w)
+        kw.update(W1_q=W1_q, W1_sf=W1_sf, W2_q=W2_q, W2_sf=W2_sf)
+    else:
+        kw.update(W1=d.W1, W2=d.W2)
+    op.bind(**kw).run()
+    torch.cuda.synchronize()
+    got = op.outputs()
+    assert int(got["status"].item()) == 0
+    ids = inp.ids.numpy()
+    if prec == PREC_MXFP8:
+        ref = om.moe_backward_mxfp8(inp.x, inp.dout, inp.W1, inp.W2, inp.s, ids, h, affinity=aff, fp8_act=cfg.fp8_act,
+                                    fp8_w=cfg.fp8_w, activation=glu, gate_up=layout, gate_act=ga)
+        compare_outputs(got, ref, MXFP8_TOL)
+    else:
+        ref = om.moe_backward(inp.x, inp.dout, inp.W1, inp.W2, inp.s, ids, h, b2=inp.b2, with_bias=True,
+                              affinity=aff, activation=glu, gate_up=layout, gate_act=ga)
+        compare_outputs(got, ref, BF16_TOL)

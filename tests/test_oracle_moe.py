@@ -369,3 +369,48 @@ def test_saved_dw_down_factors_reproduce_the_recomputed_ones(affinity):
     mg = om.moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=affinity, inter=om._to_f32(inter),
                                sdout=om._to_f32(sdout) if affinity == 0 else None)
     assert np.array_equal(mq["dW2"], mg["dW2"])
+
+
+@pytest.mark.parametrize("activation,gate_up", [("swiglu", "concat"), ("geglu", "interleaved")])
+def test_saved_gate_act_enters_only_through_the_activation_value(activation, gate_up):
+    """A saved act(gate) equal to the recomputed one changes nothing (both precisions); scaled by c it
+    moves exactly the terms that carry the activation's value: ds, dW2, the up columns of dW1 and
+    db1 scale by c, the gate columns (act'(gate) from the pre-activation) do not move, and dx is
+    affine in c with its c = 0 part the gate columns' contribution alone."""
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=9, H=6, I=4, E=3, K=2, seed=35)
+    _, h = om.moe_forward(x, W1, b1, W2, None, s, ids, activation, gate_up)
+    act = om.ACTIVATIONS[activation][0](h[..., :4])
+    gc, uc = om.gate_up_columns(4, gate_up)
+    kw = dict(with_bias=True, activation=activation, gate_up=gate_up)
+    ref = om.moe_backward(x, dout, W1, W2, s, ids, h, **kw)
+    same = om.moe_backward(x, dout, W1, W2, s, ids, h, gate_act=act, **kw)
+    for name in ("dx", "dW1", "dW2", "ds", "db1"):
+        assert np.array_equal(same[name], ref[name]), name
+    by = {c: om.moe_backward(x, dout, W1, W2, s, ids, h, gate_act=c * act, **kw) for c in (0.0, 2.0, 3.0)}
+    assert np.all(by[0.0]["ds"] == 0) and np.all(by[0.0]["dW2"] == 0)
+    assert np.all(by[0.0]["dW1"][:, :, uc] == 0) and np.all(by[0.0]["db1"][:, uc] == 0)
+    for c in (0.0, 2.0, 3.0):
+        g = by[c]
+        assert np.allclose(g["ds"], c * ref["ds"], rtol=1e-12, atol=1e-14)
+        assert np.allclose(g["dW2"], c * ref["dW2"], rtol=1e-12, atol=1e-14)
+        assert np.allclose(g["dW1"][:, :, uc], c * ref["dW1"][:, :, uc], rtol=1e-12, atol=1e-14)
+        assert np.allclose(g["db1"][:, uc], c * ref["db1"][:, uc], rtol=1e-12, atol=1e-14)
+        assert np.array_equal(g["dW1"][:, :, gc], ref["dW1"][:, :, gc])
+        assert np.allclose(g["dx"], by[0.0]["dx"] + c * (ref["dx"] - by[0.0]["dx"]), rtol=1e-12, atol=1e-13)
+    # the gate columns' dx part, written out: (dA up act'(gate)) W1_gate^T summed over the slots
+    dact = om.ACTIVATIONS[activation][1]
+    dxg = np.zeros_like(x)
+    for t in range(x.shape[0]):
+        for k in range(ids.shape[1]):
+            e = ids[t, k]
+            dA = s[t, k] * (dout[t] @ W2[e].T)
+            dxg[t] += (dA * h[t, k, 4:] * dact(h[t, k, :4])) @ W1[e][:, gc].T
+    assert np.allclose(by[0.0]["dx"], dxg, rtol=1e-12, atol=1e-13)
+    # MXFP8: the recomputed act in float64 as the saved value reproduces the quantised path exactly
+    x, dout, W1, b1, W2, b2, s, ids = _problem(T=40, H=64, I=32, E=3, K=2, seed=36)
+    _, h = om.moe_forward(x, W1, b1, W2, None, s, ids, activation, gate_up)
+    act = om.ACTIVATIONS[activation][0](h[..., :32])
+    mq = om.moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, activation=activation, gate_up=gate_up)
+    mg = om.moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, activation=activation, gate_up=gate_up, gate_act=act)
+    for name in ("dx", "dW1", "dW2", "ds"):
+        assert np.array_equal(mq[name], mg[name]), name
