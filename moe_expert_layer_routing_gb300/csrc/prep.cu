@@ -1,6 +1,6 @@
 // Operand preparation for the grouped GEMMs, and the public mxfp8_quantize.
 //
-// prep_kernel (one CTA per 128-row tile of the tile-row space, H walked in 64-column chunks)
+// prep_kernel (one CTA per 128-row tile of the tile-row space, H walked in 256-column chunks)
 // gathers the token rows of every routed (t, k) once and writes, in one pass over dout and x:
 //   dout_g  [P, H]  gathered dout rows                      (G1 A operand, groups along H)
 //   dout_gt [H, P]  gathered dout transposed, s-scaled for affinity on H (G3 B operand)
@@ -23,9 +23,9 @@ constexpr int kPrepSmem = 128 * kPrepTilePitch * 2;
 
 // Per 256-column chunk and per tensor (dout, then x): phase 1, each warp reads whole 512-byte row
 // segments of 16 gathered rows (16-byte vectors, 16 in flight per thread), writes the row-major
-// dout_g chunk and stages the tile in shared memory; phase 2, each thread owns one column and
-// writes its four 32-row groups of the transposed output (128 contiguous bytes for fp8, 256 for
-// bf16, per output row).
+// dout_g chunk and stages the tile in shared memory; phase 2 writes the transposed output in 32-row
+// groups (128 contiguous bytes for fp8, 256 for bf16, per output row): for MXFP8 each thread owns
+// one column and its four groups, for BF16 a column pair (32-bit shared-memory reads) and two groups.
 template <bool MX, bool SCALE_T, bool BIAS, int AF>
 __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
   if ((int)blockIdx.x >= *a.num_tiles) return;
@@ -109,35 +109,58 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
       }
       __syncthreads();
       // ---- phase 2 ---- (dout^T comes from a saved s*dout checkpoint when skip_dout_t)
-      if (tid < ncol && !(which == 0 && a.skip_dout_t)) {
-        const int h = tid;
-        const int64_t orow = h0 + h;
-        void* outp = which == 0 ? a.dout_gt : a.x_gt;
-        uint8_t* outsf = which == 0 ? a.dout_gt_sf : a.x_gt_sf;
+      // MXFP8: thread = one column, its four 32-row groups.  BF16: thread = a column pair (one 32-bit
+      // shared-memory word per row) and two of the groups; ncol is a multiple of 128, so a pair is whole.
+      if constexpr (MX) {
+        if (tid < ncol && !(which == 0 && a.skip_dout_t)) {
+          const int h = tid;
+          const int64_t orow = h0 + h;
+          uint8_t* outp = static_cast<uint8_t*>(which == 0 ? a.dout_gt : a.x_gt);
+          uint8_t* outsf = which == 0 ? a.dout_gt_sf : a.x_gt_sf;
 #pragma unroll 1
-        for (int g = 0; g < 4; ++g) {
-          float c32[32];
+          for (int g = 0; g < 4; ++g) {
+            float c32[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int row = g * 32 + j;
-            float x = bf16_bits_to_float(st[row * kPrepTilePitch + h]);
-            if (SCALE_T && which == 0) x *= s_s[row];
-            c32[j] = x;
-          }
-          const int64_t ocol = prow0 + g * 32;
-          if constexpr (MX) {
+            for (int j = 0; j < 32; ++j) {
+              const int row = g * 32 + j;
+              float x = bf16_bits_to_float(st[row * kPrepTilePitch + h]);
+              if (SCALE_T && which == 0) x *= s_s[row];
+              c32[j] = x;
+            }
+            const int64_t ocol = prow0 + g * 32;
             uint32_t w[8];
             const uint32_t byte = quantize_group32_t<AF>(c32, w);
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(outp) + orow * P + ocol);
+            uint4* dst = reinterpret_cast<uint4*>(outp + orow * P + ocol);
             dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
             dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
             outsf[sf_tiled_offset(orow, ocol, P)] = (uint8_t)byte;
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(outp) + orow * P + ocol);
+          }
+        }
+      } else {
+        const int cp = tid & 127;
+        if (2 * cp < ncol && !(which == 0 && a.skip_dout_t)) {
+          uint16_t* outp = static_cast<uint16_t*>(which == 0 ? a.dout_gt : a.x_gt);
+#pragma unroll 1
+          for (int g = 2 * (tid >> 7); g < 2 * (tid >> 7) + 2; ++g) {
+            uint32_t wv[32];
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[q] = make_uint4(pack_bf16x2(c32[8 * q + 0], c32[8 * q + 1]), pack_bf16x2(c32[8 * q + 2], c32[8 * q + 3]),
-                                  pack_bf16x2(c32[8 * q + 4], c32[8 * q + 5]), pack_bf16x2(c32[8 * q + 6], c32[8 * q + 7]));
+            for (int j = 0; j < 32; ++j)
+              wv[j] = *reinterpret_cast<const uint32_t*>(st + (g * 32 + j) * kPrepTilePitch + 2 * cp);
+            auto elem = [&](int j, int half) {  // column 2*cp + half, row g*32 + j
+              float x = __uint_as_float(half ? (wv[j] & 0xFFFF0000u) : (wv[j] << 16));
+              if (SCALE_T && which == 0) x *= s_s[g * 32 + j];
+              return x;
+            };
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              uint4* dst = reinterpret_cast<uint4*>(outp + (h0 + 2 * cp + half) * P + prow0 + g * 32);
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(pack_bf16x2(elem(8 * q + 0, half), elem(8 * q + 1, half)),
+                                    pack_bf16x2(elem(8 * q + 2, half), elem(8 * q + 3, half)),
+                                    pack_bf16x2(elem(8 * q + 4, half), elem(8 * q + 5, half)),
+                                    pack_bf16x2(elem(8 * q + 6, half), elem(8 * q + 7, half)));
+            }
           }
         }
       }
