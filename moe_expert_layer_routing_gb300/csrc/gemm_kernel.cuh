@@ -25,6 +25,7 @@
 namespace moebwd {
 
 constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block on sm_103a
+constexpr int kTransPitch = 36;   // fp32 row pitch of the epilogue transpose buffers (16-byte rows, no bank conflicts)
 
 template <bool MX, int BN, int EPI>
 struct GemmCfg {
@@ -47,7 +48,7 @@ struct GemmCfg {
   // fp32 transpose buffers per warp: MXFP8 shares one between the three transposes (the shared memory
   // saved buys a fifth pipeline stage); BF16 has stages enough and keeps three, which overlap
   static constexpr int G1_TBUFS = MX ? 1 : 3;
-  static constexpr int EPI_WARP_BYTES = (EPI == kEpiDSwiGLU) ? G1_TBUFS * G1_NC * 33 * 4 : 0;
+  static constexpr int EPI_WARP_BYTES = (EPI == kEpiDSwiGLU) ? G1_TBUFS * G1_NC * kTransPitch * 4 : 0;
   static constexpr int XCHG_QUARTER = kG1Subs * 2 * 32;  // floats: [slice][gate|up][lane]
   static constexpr int XCHG_BYTES = (EPI == kEpiDSwiGLU) ? 2 * 4 * XCHG_QUARTER * 4 : 0;
   static constexpr int CK_CHUNK_BYTES = 2 * 32 * 128 * 2;
@@ -197,7 +198,8 @@ __device__ __forceinline__ void tile_ckpt_origin(const GemmParams& p, const Tile
 }
 
 // Transposed store of NC columns x 32 rows (NC = 8 or 16): v[j] of lane r is element (r, j).  The
-// block is transposed through shared memory as fp32 (pitch 33, conflict free); lane l then handles
+// block is transposed through shared memory as fp32 (pitch kTransPitch = 36: the column-wise writes
+// and the 16-byte row reads are both free of bank conflicts); lane l then handles
 // column l % NC, rows NC*(l / NC) .. +NC-1, so output row row0 + (l % NC) * rstride gets columns
 // p0..p0+31 from 32/NC lanes (bf16, or fp8 codes with one scale quantised along all 32: those lanes
 // combine their amax).
@@ -205,12 +207,18 @@ template <bool MX, int NC, int AF>
 __device__ __forceinline__ void store_transposed(float* buf, const float (&v)[NC], void* out, uint8_t* sf,
                                                  int64_t P, int64_t row0, int rstride, int64_t p0, int lane) {
 #pragma unroll
-  for (int j = 0; j < NC; ++j) buf[j * 33 + lane] = v[j];
+  for (int j = 0; j < NC; ++j) buf[j * kTransPitch + lane] = v[j];
   __syncwarp();
   const int c = lane % NC, rg = lane / NC;
   float col[NC];
 #pragma unroll
-  for (int i = 0; i < NC; ++i) col[i] = buf[c * 33 + rg * NC + i];
+  for (int i = 0; i < NC; i += 4) {
+    const float4 f = *reinterpret_cast<const float4*>(buf + c * kTransPitch + rg * NC + i);
+    col[i] = f.x;
+    col[i + 1] = f.y;
+    col[i + 2] = f.z;
+    col[i + 3] = f.w;
+  }
   if constexpr (MX) {
     float am = 0.f;
 #pragma unroll
@@ -402,7 +410,7 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
   }
   // dh^T rows in W1's gate/up layout, a'^T rows by feature
   // MXFP8: the three transposes share the warp's buffer (each ends with the warp's reads done)
-  constexpr int TB = MX ? 0 : NC * 33;
+  constexpr int TB = MX ? 0 : NC * kTransPitch;
   store_transposed<MX, NC, AF>(tbuf, dg, p.dht, p.dht_sf, P, il ? 2 * c0 : c0, il ? 2 : 1, p0, lane);
   store_transposed<MX, NC, AF>(tbuf + TB, du, p.dht, p.dht_sf, P, il ? 2 * c0 + 1 : I + c0, il ? 2 : 1, p0, lane);
   if (p.apt)  // a'^T (null: built from a saved checkpoint of a or s*a)
