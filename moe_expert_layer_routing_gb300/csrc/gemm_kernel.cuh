@@ -68,7 +68,11 @@ struct GemmCfg {
   static constexpr int STAGING_BYTES = STAGED ? BM * 64 * 2 : 0;
   // staged epilogues: 8 warps, two per TMEM lane quarter, splitting the columns
   static constexpr int EPI_WARPS = EPI == kEpiDSwiGLU ? 4 * kG1Subs : STAGED ? 8 : 4;
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  // dSwiGLU: one more warp whose lane 0 streams the checkpoint chunks into their two buffers, each as
+  // soon as every epilogue warp has released it (ten or eleven warps share the 168-register cap)
+  static constexpr bool CK_LOADER = EPI == kEpiDSwiGLU;
+  static constexpr int CK_LOADER_WARP = 2 + EPI_WARPS;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS + (CK_LOADER ? 32 : 0);
   static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES + XCHG_BYTES + CK_BYTES + STAGING_BYTES;
   static constexpr int BAR_BYTES = 512;
   static constexpr int RING = 4;  // tile indices published by the producer ahead of the consumers
@@ -466,7 +470,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
     mbar_init(done, 1);
     for (int r = 0; r < C::RING; ++r) {
       mbar_init(&tile_full[r], 1);
-      mbar_init(&tile_empty[r], 1 + C::EPI_WARPS);
+      mbar_init(&tile_empty[r], 1 + C::EPI_WARPS + (C::CK_LOADER ? 1 : 0));
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -611,34 +615,56 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       mma_commit(done);
       mbar_wait_drain(done, 0, p.status);
     }
+  } else if (C::CK_LOADER && warp == C::CK_LOADER_WARP) {
+    if (lane == 0) {
+      // ---------------- checkpoint loader (dSwiGLU) ----------------
+      // chunk n of the schedule (the tiles in ring order, NCHUNK chunks each) goes to buffer n % 2
+      // once every epilogue warp has released chunk n - 2
+      int64_t issued = 0;
+      int rs = 0;
+      uint32_t rph = 0;
+      bool ok = true;
+      while (ok) {
+        if (!mbar_wait_bounded(&tile_full[rs], rph, p.status, abort_flag)) break;
+        const int t = tile_ring[rs];
+        mbar_arrive(&tile_empty[rs]);
+        if (++rs == C::RING) {
+          rs = 0;
+          rph ^= 1u;
+        }
+        if (t < 0) break;
+        const TileInfo tn = gemm_decode_tile<BN, C::BKE>(p, t);
+        int64_t blk;
+        int b0;
+        tile_ckpt_origin(p, tn, blk, b0);
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          const int buf = (int)(issued & 1);
+          if (issued >= 2 &&
+              !mbar_wait_bounded(&ck_empty[buf], (uint32_t)(((issued - 2) >> 1) & 1), p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = smCK + buf * C::CK_CHUNK_BYTES;
+          const int i0 = tn.nt * BN + c * 32;
+          mbar_arrive_expect_tx(&ck_full[buf], C::CK_CHUNK_BYTES);
+          tma_load_2d(dst, &tmC, &ck_full[buf], b0, (int)((blk * 2 + 0) * p.I + i0));
+          tma_load_2d(dst + C::CK_CHUNK_BYTES / 2, &tmC, &ck_full[buf], b0, (int)((blk * 2 + 1) * p.I + i0));
+          ++issued;
+        }
+      }
+      // Drain: the last two chunks' copies land before the CTA may exit.
+      for (int64_t n = issued > 2 ? issued - 2 : 0; n < issued; ++n)
+        mbar_wait_drain(&ck_full[n & 1], (uint32_t)((n >> 1) & 1), p.status);
+    }
   } else {
-    // ---------------- epilogue warps 2..5 ----------------
+    // ---------------- epilogue warps 2..5 (2..9) ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int m = 32 * q + lane;
     const int half = (warp - 2) >> 2;  // dSwiGLU: column slice of every 32 columns; staged: which half
     uint8_t* wsm = smEPI + (warp - 2) * C::EPI_WARP_BYTES;
     float* xchg = smXchg + q * C::XCHG_QUARTER;  // + (chunk parity) * 4 * XCHG_QUARTER
-    const bool ck_leader = (EPI == kEpiDSwiGLU) && warp == 2 && lane == 0;
-    // checkpoint chunk n of the schedule goes to buffer n % 2; ck_issued = chunks issued so far
-    int64_t ck_next = 0, ck_issued = 0;
-    auto issue_ck = [&](int t, int c) {
-      const TileInfo tn = gemm_decode_tile<BN, C::BKE>(p, t);
-      int64_t blk;
-      int b0;
-      tile_ckpt_origin(p, tn, blk, b0);
-      const int buf = (int)(ck_issued & 1);
-      uint8_t* dst = smCK + buf * C::CK_CHUNK_BYTES;
-      const int i0 = tn.nt * BN + c * 32;
-      // the buffer's previous chunk (two back) must have been consumed by every epilogue warp
-      if (ck_issued >= 2 &&
-          !mbar_wait_bounded(&ck_empty[buf], (uint32_t)(((ck_issued - 2) >> 1) & 1), p.status, abort_flag))
-        return;
-      mbar_arrive_expect_tx(&ck_full[buf], C::CK_CHUNK_BYTES);
-      tma_load_2d(dst, &tmC, &ck_full[buf], b0, (int)((blk * 2 + 0) * p.I + i0));
-      tma_load_2d(dst + C::CK_CHUNK_BYTES / 2, &tmC, &ck_full[buf], b0, (int)((blk * 2 + 1) * p.I + i0));
-      ++ck_issued;
-    };
-    bool ck0_ready = false;  // chunk 0 of the coming tile already issued (prefetched)
+    // checkpoint chunk n of the schedule is read from buffer n % 2 (filled by the loader warp)
+    int64_t ck_next = 0;
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
@@ -659,10 +685,6 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       }
       if (t < 0) break;
       const TileInfo ti = gemm_decode_tile<BN, C::BKE>(p, t);
-      if (ck_leader) {
-        if (!ck0_ready) issue_ck(t, 0);
-        ck0_ready = false;
-      }
       // dSwiGLU: the row's flat index and score, loaded while the accumulator is still being computed
       int row_f = -1;
       float row_s = 0.f;
@@ -806,17 +828,6 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         }
 #pragma unroll 1
         for (int c = 0; c < C::NCHUNK; ++c) {
-          if (ck_leader) {  // keep one chunk in flight ahead of the one being consumed
-            if (c + 1 < C::NCHUNK) {
-              issue_ck(t, c + 1);
-            } else if (mbar_wait_bounded(&tile_full[rs], rph, p.status, abort_flag)) {
-              const int tn = tile_ring[rs];  // peek: the slot stays valid until this warp reads it
-              if (tn >= 0) {
-                issue_ck(tn, 0);
-                ck0_ready = true;
-              }
-            }
-          }
           const int buf = (int)(ck_next & 1);
           // on a failed wait the chunk is still walked (garbage in, flagged by the status word) so
           // that both warps of a pair reach the same barriers
@@ -860,9 +871,6 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       }
     }
     if (C::STAGED && warp == 2 && lane == 0) bulk_wait_all();  // stores complete before exit
-    if (ck_leader) {  // drain checkpoint copies still in flight
-      for (int64_t n = ck_next; n < ck_issued; ++n) mbar_wait_drain(&ck_full[n & 1], (uint32_t)((n >> 1) & 1), p.status);
-    }
   }
 
   tc_fence_before();
