@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
           // the tile's four 32-row groups have adjacent scale bytes (k = g in the tiled layout, the
           // tile's first row a multiple of 128): one 32-bit store per column
           uint32_t sfw = 0u;
-#pragma unroll 1
+#pragma unroll 2
           for (int g = 0; g < 4; ++g) {
             float c32[32];
 #pragma unroll
