@@ -766,22 +766,23 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         // first, so the accumulator is released after four loads; the slabs then go out one at a
         // time through the staging slab while the next tile's MMAs run.
         uint32_t pk[BN / 64][16];
-#pragma unroll
-        for (int sl = 0; sl < BN / 64; sl += 2) {  // two loads in flight per wait
-          uint32_t r[2][32];
+        {  // all of the warp's slabs in flight under one wait, packed to bf16 afterwards
+          uint32_t r[BN / 64][32];
           if (ti.nk > 0) {
-            tmem_ld_32x32b_x32(taddr + (sl * 2 + half) * 32, r[0]);
-            tmem_ld_32x32b_x32(taddr + ((sl + 1) * 2 + half) * 32, r[1]);
+#pragma unroll
+            for (int sl = 0; sl < BN / 64; ++sl) tmem_ld_32x32b_x32(taddr + (sl * 2 + half) * 32, r[sl]);
             tmem_ld_wait();
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[0][j] = r[1][j] = 0u;
+            for (int sl = 0; sl < BN / 64; ++sl)
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[sl][j] = 0u;
           }
 #pragma unroll
-          for (int u = 0; u < 2; ++u)
+          for (int sl = 0; sl < BN / 64; ++sl)
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              pk[sl + u][j] = pack_bf16x2(__uint_as_float(r[u][2 * j]), __uint_as_float(r[u][2 * j + 1]));
+              pk[sl][j] = pack_bf16x2(__uint_as_float(r[sl][2 * j]), __uint_as_float(r[sl][2 * j + 1]));
         }
         tc_fence_before();
         __syncwarp();
