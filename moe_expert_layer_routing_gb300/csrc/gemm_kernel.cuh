@@ -710,24 +710,28 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         int b0;
         tile_ckpt_origin(p, ti, blk, b0);
         uint16_t* stg = reinterpret_cast<uint16_t*>(smStage) + half * (32 * 128);
-#pragma unroll 1
+        // the warp's four 32-column chunks come out of TMEM under one wait and the accumulator is
+        // released at once; bias, staging and stores then run from registers
+        uint32_t rr[BN / 64][32];
+        if (ti.nk > 0) {
+#pragma unroll
+          for (int cp = 0; cp < BN / 64; ++cp) tmem_ld_32x32b_x32(taddr + (cp * 2 + half) * 32, rr[cp]);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int cp = 0; cp < BN / 64; ++cp)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) rr[cp][j] = 0u;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+#pragma unroll
         for (int cp = 0; cp < BN / 64; ++cp) {
           if (warp == 2 && lane == 0) bulk_wait_read_all();
           epilogue_bar<32 * C::EPI_WARPS>();
           const int n0 = ti.nt * BN + (cp * 2 + half) * 32;  // first gate|up feature of the chunk
-          uint32_t r[32];
-          if (ti.nk > 0) {
-            tmem_ld_32x32b_x32(taddr + (cp * 2 + half) * 32, r);
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = 0u;
-          }
-          if (cp == BN / 64 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
-          }
+          uint32_t (&r)[32] = rr[cp];
           if (p.b1) {
             const uint4* bp = reinterpret_cast<const uint4*>(p.b1 + (int64_t)ti.e * 2 * p.I + n0);
 #pragma unroll
@@ -766,7 +770,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         // first, so the accumulator is released after four loads; the slabs then go out one at a
         // time through the staging slab while the next tile's MMAs run.
         uint32_t pk[BN / 64][16];
-        {  // all of the warp's slabs in flight under one wait, packed to bf16 afterwards
+        {  // all of the warp's slabs in flight under one wait; TMEM is released before the packing
           uint32_t r[BN / 64][32];
           if (ti.nk > 0) {
 #pragma unroll
@@ -778,15 +782,15 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) r[sl][j] = 0u;
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);
 #pragma unroll
           for (int sl = 0; sl < BN / 64; ++sl)
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               pk[sl][j] = pack_bf16x2(__uint_as_float(r[sl][2 * j]), __uint_as_float(r[sl][2 * j + 1]));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
 #pragma unroll
         for (int sl = 0; sl < BN / 64; ++sl) {
           if (warp == 2 && lane == 0) bulk_wait_read_all();
