@@ -42,12 +42,17 @@ def load_peaks():
 
 
 def source_sha():
+    """Hash of the kernel sources' code (comments and whitespace dropped, so that an edit of a comment
+    does not retire the ncu counters recorded for that code)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_expert_layer_routing_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", " ", text)
+            h.update(name.encode() + " ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -10,10 +10,12 @@
 //              tile_offsets[e+1]) of the transposed operands (G3: dW2_e = a'^T dout_g,
 //              G4: dW1_e = x_g^T dh); an expert without rows writes zeros.
 //
-// CTA = 6 warps: warp 0 issues TMA loads into a STAGES-deep shared-memory ring, warp 1 owns TMEM
-// and issues tcgen05.mma (one elected lane), warps 2-5 drain the TMEM accumulator (double
-// buffered where TMEM allows) through the epilogue.  One CTA per SM walks a static tile schedule.
-// Every wait is bounded (MOE_STATUS_TIMEOUT on expiry, then an orderly drain and exit).
+// One persistent CTA per SM.  Warp 0 (one lane) claims tiles from a global counter, publishes them
+// through a small ring and issues the TMA loads into a STAGES-deep shared-memory ring; warp 1 owns
+// TMEM and issues tcgen05.mma (one lane); the epilogue warps drain the TMEM accumulator (double
+// buffered where TMEM allows): 4 for the plain store, 8 for the staged store / checkpoint epilogues
+// and for the dSwiGLU epilogue, which also has a checkpoint-loader warp.  Every wait is bounded
+// (MOE_STATUS_TIMEOUT on expiry, then an orderly drain and exit).
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -43,7 +45,7 @@ struct GemmCfg {
   // dSwiGLU epilogue: 4 * kG1Subs warps (kG1Subs per TMEM lane quarter, each taking NC = 32 / kG1Subs
   // of every 32 columns), three NC x 32 fp32 transposition buffers per warp, the row-wise amax
   // exchange of each quarter (double-buffered by chunk parity) and a double-buffered checkpoint chunk
-  // (gate and up, 32 features x 128 tile rows each) filled by TMA one chunk ahead.
+  // (gate and up, 32 features x 128 tile rows each) refilled by the loader warp's TMA copies.
   static constexpr int G1_NC = 32 / kG1Subs;
   // fp32 transpose buffers per warp: MXFP8 shares one between the three transposes (the shared memory
   // saved buys a fifth pipeline stage); BF16 has stages enough and keeps three, which overlap
@@ -657,7 +659,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         mbar_wait_drain(&ck_full[n & 1], (uint32_t)((n >> 1) & 1), p.status);
     }
   } else {
-    // ---------------- epilogue warps 2..5 (2..9) ----------------
+    // ---------------- epilogue warps (2..5, or 2..9) ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int m = 32 * q + lane;
     const int half = (warp - 2) >> 2;  // dSwiGLU: column slice of every 32 columns; staged: which half
@@ -766,9 +768,9 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         }
         continue;
       } else if constexpr (C::TMA_STORE) {
-        // The warp's 128 columns (4 slabs x 32) are read from TMEM and packed to bf16 in registers
-        // first, so the accumulator is released after four loads; the slabs then go out one at a
-        // time through the staging slab while the next tile's MMAs run.
+        // The warp's 128 columns (4 slabs x 32) are read from TMEM under one wait and the accumulator
+        // is released at once; packed to bf16 in registers, the slabs then go out one at a time
+        // through the staging slab while the next tile's MMAs run.
         uint32_t pk[BN / 64][16];
         {  // all of the warp's slabs in flight under one wait; TMEM is released before the packing
           uint32_t r[BN / 64][32];
