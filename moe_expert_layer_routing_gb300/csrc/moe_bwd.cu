@@ -2,7 +2,8 @@
 // layout, and the launch sequence on one stream (no host synchronisation):
 //
 //   route meta -> prep (gather, transpose, quantise) -> [G0 h = x_g W1_e + b1_e, when the
-//   pre-activations are recomputed] -> G1 dA + dSwiGLU epilogue ->
+//   pre-activations are recomputed] -> [W2's scales re-tiled, for 192-column MXFP8 G1 tiles] ->
+//   G1 dA + dSwiGLU epilogue ->
 //   G3 dW2 (K-grouped) -> G2 dx_expanded (M-grouped) -> G4 dW1 (K-grouped) ->
 //   dx scatter-sum, ds finalize, bias column sums
 #include <cuda.h>
