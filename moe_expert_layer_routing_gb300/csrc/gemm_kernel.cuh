@@ -47,9 +47,10 @@ struct GemmCfg {
   // exchange of each quarter (double-buffered by chunk parity) and a double-buffered checkpoint chunk
   // (gate and up, 32 features x 128 tile rows each) refilled by the loader warp's TMA copies.
   static constexpr int G1_NC = 32 / kG1Subs;
-  // fp32 transpose buffers per warp: MXFP8 shares one between the three transposes (the shared memory
-  // saved buys a fifth pipeline stage); BF16 has stages enough and keeps three, which overlap
-  static constexpr int G1_TBUFS = MX ? 1 : 3;
+  // fp32 transpose buffers per warp: MXFP8, and BF16 at 256 columns, share one between the three
+  // transposes (the shared memory saved buys a pipeline stage); BF16 at 128 columns has stages enough
+  // and keeps three, which overlap
+  static constexpr int G1_TBUFS = (MX || BN == 256) ? 1 : 3;
   static constexpr int EPI_WARP_BYTES = (EPI == kEpiDSwiGLU) ? G1_TBUFS * G1_NC * kTransPitch * 4 : 0;
   static constexpr int XCHG_QUARTER = kG1Subs * 2 * 32;  // floats: [slice][gate|up][lane]
   static constexpr int XCHG_BYTES = (EPI == kEpiDSwiGLU) ? 2 * 4 * XCHG_QUARTER * 4 : 0;
@@ -273,7 +274,7 @@ __device__ __forceinline__ void group_bar(int id) {
 // GENERIC with `ga` (this row's slot in a saved act(gate) checkpoint [N,I,B], feature stride B):
 // act(gate) is read from it, act'(gate) still computed from the pre-activation.
 // Padding rows produce zeros.
-template <bool MX, int NC, int AF, bool GENERIC>
+template <bool MX, int NC, int AF, bool GENERIC, bool SHARED_TBUF>
 __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t taddr, int64_t prow, int m, int lane,
                                                  bool valid, float sv, int i0, int sub, const uint16_t* ck,
                                                  const uint16_t* ga, float* tbuf, float* xchg, int bar_id,
@@ -415,8 +416,8 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
     }
   }
   // dh^T rows in W1's gate/up layout, a'^T rows by feature
-  // MXFP8: the three transposes share the warp's buffer (each ends with the warp's reads done)
-  constexpr int TB = MX ? 0 : NC * kTransPitch;
+  // SHARED_TBUF: the three transposes share the warp's buffer (each ends with the warp's reads done)
+  constexpr int TB = SHARED_TBUF ? 0 : NC * kTransPitch;
   store_transposed<MX, NC, AF>(tbuf, dg, p.dht, p.dht_sf, P, il ? 2 * c0 : c0, il ? 2 : 1, p0, lane);
   store_transposed<MX, NC, AF>(tbuf + TB, du, p.dht, p.dht_sf, P, il ? 2 * c0 + 1 : I + c0, il ? 2 : 1, p0, lane);
   if (p.apt)  // a'^T (null: built from a saved checkpoint of a or s*a)
@@ -849,17 +850,17 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
             float* tb = reinterpret_cast<float*>(wsm);
             if (!MX || p.fmt_act == MOE_FP8_E5M2) {
               if (generic)
-                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2, true>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
+                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2, true, C::G1_TBUFS == 1>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
                                                                   xc, 2 + q, ds_acc);
               else
-                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2, false>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
+                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2, false, C::G1_TBUFS == 1>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
                                                                    xc, 2 + q, ds_acc);
             } else {
               if (generic)
-                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3, true>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
+                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3, true, C::G1_TBUFS == 1>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
                                                                   xc, 2 + q, ds_acc);
               else
-                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3, false>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
+                epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3, false, C::G1_TBUFS == 1>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
                                                                    xc, 2 + q, ds_acc);
             }
           }

@@ -135,9 +135,10 @@ static Layout make_layout(const MoeBwdArgs& a) {
   L.P = tile_capacity(L.TK, a.E);
   L.Nb = blocks_bound(a.T, a.K, a.E, a.block_size);
   // N-tile widths: G1 carries the heavy dSwiGLU epilogue, so it keeps a double-buffered TMEM
-  // accumulator: 128 columns, or for MXFP8 192 where I allows (two 192-column accumulators and the
-  // scales fit TMEM; 256 would leave room for one); the store-epilogue GEMMs take 256 where N allows.
-  L.BN1 = mx && a.I % 192 == 0 ? 192 : 128;
+  // accumulator: for MXFP8 192 columns where I allows (two 192-column accumulators and the scales fit
+  // TMEM; 256 would leave room for one), for BF16 256 where I allows (three stages with one shared
+  // transpose buffer), else 128; the store-epilogue GEMMs take 256 where N allows.
+  L.BN1 = mx ? (a.I % 192 == 0 ? 192 : 128) : (a.I % 256 == 0 ? 256 : 128);
   L.BN2 = a.H % 256 == 0 ? 256 : 128;
   L.BN3 = L.BN2;
   L.BN4 = 256;
