@@ -93,7 +93,7 @@ enum Region {
   R_CHUNK_COUNTS, R_EXPERT_OFFSETS, R_BLOCK_OFFSETS, R_TILE_OFFSETS, R_EXPERT_ORDER, R_SCALARS,
   R_X_GATHER, R_S_SCATTER, R_S_REV, R_TPID, R_B2E, R_TILE_ROW_FLAT, R_FLAT_TILE_ROW, R_TILE_EXPERT,
   R_DOUT_G, R_DOUT_G_SF, R_DOUT_GT, R_DOUT_GT_SF, R_X_GT, R_X_GT_SF, R_DH, R_DH_SF, R_DH_T, R_DH_T_SF,
-  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_X_G, R_X_G_SF, R_CKPT, R_PAIR_OFFSETS, R_TILE_ORDER, R_TILE_ROW_SLOT, R_W2_SF_T, R_COUNT
+  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_X_G, R_X_G_SF, R_CKPT, R_PAIR_OFFSETS, R_TILE_ORDER, R_TILE_ROW_SLOT, R_W2_SF_T, R_DB1_PART, R_DB2_PART, R_COUNT
 };
 
 struct Layout {
@@ -180,6 +180,11 @@ static Layout make_layout(const MoeBwdArgs& a) {
   b[R_TILE_ROW_SLOT] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, P);  // saved s*dout rows (pointers not read)
   // W2's scales re-tiled for 192-column G1 tiles: two atoms per tile
   if (mx && L.BN1 % 128) b[R_W2_SF_T] = (size_t)(E * I / L.BN1) * ((L.BN1 + 127) / 128) * (size_t)(H / 128) * 512;
+  // BF16 bias gradients: per-tile column sums from G1's transposes (four lane quarters) and prep (two halves)
+  if (a.has_bias && !mx) {
+    b[R_DB1_PART] = sizeof(float) * (size_t)(P / kTileM) * 4 * (size_t)(2 * I);
+    b[R_DB2_PART] = sizeof(float) * (size_t)(P / kTileM) * 2 * (size_t)H;
+  }
   if (a.act_src == MOE_ACT_RECOMPUTE) {
     b[R_X_G] = (size_t)(P * H * es);
     b[R_X_G_SF] = mx ? (size_t)(P * H / 32) : 0;
@@ -461,6 +466,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   pa.x_g = rec ? reg<void>(L, ws, R_X_G) : nullptr;
   pa.x_g_sf = rec ? reg<uint8_t>(L, ws, R_X_G_SF) : nullptr;
   pa.skip_dout_t = a.down_proj_act_ckpt != nullptr;
+  pa.db2_part = (a.has_bias && !mx && !pa.skip_dout_t) ? reg<float>(L, ws, R_DB2_PART) : nullptr;
   if ((rc = launch_prep(pa, st))) return rc;
   // dW_down operands from saved forward values ([BW] optional checkpoints)
   const void* inter = a.scaled_intermediate_ckpt ? a.scaled_intermediate_ckpt : a.intermediate_ckpt;
@@ -556,6 +562,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.apt = inter ? nullptr : reg<void>(L, ws, R_AP_T);
     p.apt_sf = inter ? nullptr : reg<uint8_t>(L, ws, R_AP_T_SF);
     p.ds_part = reg<float>(L, ws, R_DS_PART);
+    p.db1_part = a.has_bias ? reg<float>(L, ws, R_DB1_PART) : nullptr;
     p.tile_counter = counters + 0;
     p.status = a.status_dev;
     if ((rc = launch_gemm(mx, L.BN1, p, reg<void>(L, ws, R_DOUT_G), P, H, W2, E * I, H, st, ckpt, L.Nb * 2 * I,
@@ -643,14 +650,17 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     return rc;
   if (a.ds_masked && (rc = launch_ds_masked(a.ds, a.ids, a.num_valid_tokens, a.T, a.K, a.E, a.ds_masked, st)))
     return rc;
-  if (a.has_bias) {
-    if ((rc = launch_segment_rowsum(reg<uint16_t>(L, ws, R_DH_T), P, (int)(2 * I), tile_offsets, (int)E, nullptr,
-                                    tile_row_flat, a.db1, st, a.accumulate)))
+  if (a.has_bias) {  // per-expert sums of the per-tile partials (dout_gt read again only when it was not built here)
+    if ((rc = launch_bias_parts_reduce(reg<float>(L, ws, R_DB1_PART), 4, 2 * I, tile_offsets, (int)E, a.db1, st,
+                                       a.accumulate)))
       return rc;
-    if ((rc = launch_segment_rowsum(reg<uint16_t>(L, ws, R_DOUT_GT), P, (int)H, tile_offsets, (int)E,
-                                    a.affinity == MOE_AFFINITY_ON_I ? a.s : nullptr, tile_row_flat, a.db2, st,
-                                    a.accumulate)))
-      return rc;
+    if (pa.db2_part)
+      rc = launch_bias_parts_reduce(pa.db2_part, 2, H, tile_offsets, (int)E, a.db2, st, a.accumulate);
+    else
+      rc = launch_segment_rowsum(reg<uint16_t>(L, ws, R_DOUT_GT), P, (int)H, tile_offsets, (int)E,
+                                 a.affinity == MOE_AFFINITY_ON_I ? a.s : nullptr, tile_row_flat, a.db2, st,
+                                 a.accumulate);
+    if (rc) return rc;
   }
   prof_mark(st, slot, 8);
   return MOE_OK;

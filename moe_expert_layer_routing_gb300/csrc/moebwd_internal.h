@@ -82,6 +82,8 @@ struct PrepArgs {
   void* x_g; uint8_t* x_g_sf;          // [P,H] row-major (nullable: only when h is recomputed)
   int skip_dout_t;                     // dout_gt is built elsewhere (from a saved s*dout checkpoint)
   float* ds_bias;                      // [P] <dout_t, b2_e> or null
+  float* db2_part;                     // BF16 with biases: [P/128][2][H] column sums of s*dout per
+                                       // tile (two halves of its rows), or null
 };
 int launch_prep(const PrepArgs& a, cudaStream_t st);
 // a'^T [I,P] from an [N,I,B] block checkpoint of a (times s when s_or_null) or s*a
@@ -155,6 +157,8 @@ struct GemmParams {
   void* dht; uint8_t* dht_sf;
   void* apt; uint8_t* apt_sf;
   float* ds_part;               // [P, kG1Subs*I/BN]
+  float* db1_part;              // BF16 with biases: [P/128][4][2I] column sums of dh per tile and TMEM
+                                // lane quarter (W1's gate/up layout), or null
   // CTA-pair kernel, M-grouped: expert e's 128-row tiles form ceil(tiles_e / 2) pairs; pair_offsets
   // [E+1] is their prefix (null: one expert, pairs of consecutive tiles), num_pairs its device total
   const int32_t* pair_offsets;
@@ -193,5 +197,9 @@ int launch_ds_finalize(const float* ds_part, int nparts, const float* ds_bias, c
 int launch_segment_rowsum(const uint16_t* buf, int64_t ld, int R, const int32_t* tile_offsets, int E,
                           const float* w, const int32_t* tile_row_flat, float* out, cudaStream_t st,
                           int accumulate = 0);
+// out[e, f] (+)= sum over expert e's 128-row tiles t and k < parts of part[(t * parts + k) * F + f]
+// (in that order: deterministic)
+int launch_bias_parts_reduce(const float* part, int parts, int64_t F, const int32_t* tile_offsets, int E,
+                             float* out, cudaStream_t st, int accumulate);
 
 }  // namespace moebwd

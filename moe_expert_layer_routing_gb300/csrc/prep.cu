@@ -152,6 +152,9 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
         const int cp = tid & 127;
         if (2 * cp < ncol && !(which == 0 && a.skip_dout_t)) {
           uint16_t* outp = static_cast<uint16_t*>(which == 0 ? a.dout_gt : a.x_gt);
+          // db2: this thread's share of the tile's column sums of s*dout (its two 32-row groups)
+          const bool db2 = BIAS && which == 0 && a.db2_part != nullptr;
+          float cs0 = 0.f, cs1 = 0.f;
 #pragma unroll 1
           for (int g = 2 * (tid >> 7); g < 2 * (tid >> 7) + 2; ++g) {
             uint32_t wv[32];
@@ -163,6 +166,14 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
               if (SCALE_T && which == 0) x *= s_s[g * 32 + j];
               return x;
             };
+            if (db2) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float w = SCALE_T ? 1.f : s_s[g * 32 + j];  // s*dout (already scaled when SCALE_T)
+                cs0 = fmaf(elem(j, 0), w, cs0);
+                cs1 = fmaf(elem(j, 1), w, cs1);
+              }
+            }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               uint4* dst = reinterpret_cast<uint4*>(outp + (h0 + 2 * cp + half) * P + prow0 + g * 32);
@@ -174,6 +185,9 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
                                     pack_bf16x2(elem(8 * q + 6, half), elem(8 * q + 7, half)));
             }
           }
+          if (db2)
+            *reinterpret_cast<float2*>(a.db2_part + ((int64_t)tile * 2 + (tid >> 7)) * H + h0 + 2 * cp) =
+                make_float2(cs0, cs1);
         }
       }
       __syncthreads();

@@ -100,6 +100,29 @@ __global__ void __launch_bounds__(256) segment_rowsum_kernel(const uint16_t* __r
   if (lane == 0) out[(int64_t)e * R + j] = accumulate ? out[(int64_t)e * R + j] + acc : acc;
 }
 
+// One thread per (expert, column): the expert's tile partials summed in tile order.
+__global__ void __launch_bounds__(256) bias_parts_reduce_kernel(const float* __restrict__ part, int parts, int64_t F,
+                                                                const int32_t* __restrict__ tile_offsets,
+                                                                float* __restrict__ out, int accumulate) {
+  const int e = blockIdx.y;
+  const int64_t f = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (f >= F) return;
+  const int t0 = tile_offsets[e] / 128, t1 = tile_offsets[e + 1] / 128;
+  float acc = 0.f;
+  for (int t = t0; t < t1; ++t)
+    for (int k = 0; k < parts; ++k) acc += part[((int64_t)t * parts + k) * F + f];
+  out[(int64_t)e * F + f] = accumulate ? out[(int64_t)e * F + f] + acc : acc;
+}
+
+int launch_bias_parts_reduce(const float* part, int parts, int64_t F, const int32_t* tile_offsets, int E, float* out,
+                             cudaStream_t st, int accumulate) {
+  if (F == 0 || E == 0) return MOE_OK;
+  dim3 grid((unsigned)((F + 255) / 256), (unsigned)E);
+  bias_parts_reduce_kernel<<<grid, 256, 0, st>>>(part, parts, F, tile_offsets, out, accumulate);
+  count_launch();
+  return cuda_check(cudaGetLastError(), "bias_parts_reduce");
+}
+
 int launch_segment_rowsum(const uint16_t* buf, int64_t ld, int R, const int32_t* tile_offsets, int E, const float* w,
                           const int32_t* tile_row_flat, float* out, cudaStream_t st, int accumulate) {
   if (R == 0 || E == 0) return MOE_OK;
