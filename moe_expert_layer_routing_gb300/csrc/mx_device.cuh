@@ -27,6 +27,14 @@ __device__ __forceinline__ int64_t sf_tiled_offset(int64_t r, int64_t c, int64_t
   return ((r >> 7) * (C >> 7) + (c >> 7)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + ((c >> 5) & 3);
 }
 
+// One 32-byte global store (a whole L2 sector); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_32b(void* p, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                              uint32_t w4, uint32_t w5, uint32_t w6, uint32_t w7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w0), "r"(w1), "r"(w2),
+               "r"(w3), "r"(w4), "r"(w5), "r"(w6), "r"(w7)
+               : "memory");
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(((uint32_t)b) << 16);
 }

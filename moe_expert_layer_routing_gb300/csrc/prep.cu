@@ -141,9 +141,7 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
             const int64_t ocol = prow0 + g * 32;
             uint32_t w[8];
             const uint32_t byte = quantize_group32_t<AF>(c32, w);
-            uint4* dst = reinterpret_cast<uint4*>(outp + orow * P + ocol);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            st_global_32b(outp + orow * P + ocol, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
             sfw |= byte << (8 * g);
           }
           *reinterpret_cast<uint32_t*>(outsf + sf_tiled_offset(orow, prow0, P)) = sfw;
@@ -176,13 +174,17 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
             }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-              uint4* dst = reinterpret_cast<uint4*>(outp + (h0 + 2 * cp + half) * P + prow0 + g * 32);
+              uint16_t* dst = outp + (h0 + 2 * cp + half) * P + prow0 + g * 32;
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                dst[q] = make_uint4(pack_bf16x2(elem(8 * q + 0, half), elem(8 * q + 1, half)),
-                                    pack_bf16x2(elem(8 * q + 2, half), elem(8 * q + 3, half)),
-                                    pack_bf16x2(elem(8 * q + 4, half), elem(8 * q + 5, half)),
-                                    pack_bf16x2(elem(8 * q + 6, half), elem(8 * q + 7, half)));
+              for (int q = 0; q < 2; ++q)
+                st_global_32b(dst + 16 * q, pack_bf16x2(elem(16 * q + 0, half), elem(16 * q + 1, half)),
+                              pack_bf16x2(elem(16 * q + 2, half), elem(16 * q + 3, half)),
+                              pack_bf16x2(elem(16 * q + 4, half), elem(16 * q + 5, half)),
+                              pack_bf16x2(elem(16 * q + 6, half), elem(16 * q + 7, half)),
+                              pack_bf16x2(elem(16 * q + 8, half), elem(16 * q + 9, half)),
+                              pack_bf16x2(elem(16 * q + 10, half), elem(16 * q + 11, half)),
+                              pack_bf16x2(elem(16 * q + 12, half), elem(16 * q + 13, half)),
+                              pack_bf16x2(elem(16 * q + 14, half), elem(16 * q + 15, half)));
             }
           }
           if (db2)
