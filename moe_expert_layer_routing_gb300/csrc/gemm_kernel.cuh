@@ -183,15 +183,11 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const TileInfo& t
         }
       }
     }
+    auto pk = [&](int j) { return pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])); };
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 w;
-      w.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
-      w.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
-      w.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
-      w.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
-      d4[q] = w;
-    }
+    for (int q = 0; q < 2; ++q)  // whole 32-byte sectors (the output is caller-owned: 16-byte alignment)
+      st_global_32b_or_halves(d4 + 2 * q, pk(16 * q), pk(16 * q + 2), pk(16 * q + 4), pk(16 * q + 6), pk(16 * q + 8),
+                    pk(16 * q + 10), pk(16 * q + 12), pk(16 * q + 14));
   }
 }
 
@@ -259,12 +255,12 @@ __device__ __forceinline__ void store_transposed(float* buf, const float (&v)[NC
       for (int o = NC; o < 32; o <<= 1) cs += __shfl_xor_sync(0xffffffffu, cs, o);
       if (rg == 0) colsum[row0 + (int64_t)c * rstride] = cs;
     }
-    uint4* dst =
-        reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (row0 + (int64_t)c * rstride) * P + p0 + rg * NC);
-#pragma unroll
-    for (int w = 0; w < NC / 8; ++w)
-      dst[w] = make_uint4(pack_bf16x2(col[8 * w + 0], col[8 * w + 1]), pack_bf16x2(col[8 * w + 2], col[8 * w + 3]),
-                          pack_bf16x2(col[8 * w + 4], col[8 * w + 5]), pack_bf16x2(col[8 * w + 6], col[8 * w + 7]));
+    uint16_t* dst = static_cast<uint16_t*>(out) + (row0 + (int64_t)c * rstride) * P + p0 + rg * NC;
+    auto pk = [&](int j) { return pack_bf16x2(col[j], col[j + 1]); };
+    if constexpr (NC == 16)  // one whole 32-byte sector
+      st_global_32b(dst, pk(0), pk(2), pk(4), pk(6), pk(8), pk(10), pk(12), pk(14));
+    else
+      *reinterpret_cast<uint4*>(dst) = make_uint4(pk(0), pk(2), pk(4), pk(6));
   }
   __syncwarp();
 }
@@ -365,16 +361,19 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
 #pragma unroll
       for (int w = 0; w < NC / 2; ++w)
         q[w] = fp8x4_t<AF>(dg[2 * w] * inv, du[2 * w] * inv, dg[2 * w + 1] * inv, du[2 * w + 1] * inv);
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dh) + prow * (2 * (int64_t)I) + 2 * c0);
-#pragma unroll
-      for (int w = 0; w < NC / 8; ++w) dst[w] = make_uint4(q[4 * w], q[4 * w + 1], q[4 * w + 2], q[4 * w + 3]);
+      uint8_t* dst = static_cast<uint8_t*>(p.dh) + prow * (2 * (int64_t)I) + 2 * c0;
+      if constexpr (NC == 16)  // one whole 32-byte sector
+        st_global_32b(dst, q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
+      else
+        *reinterpret_cast<uint4*>(dst) = make_uint4(q[0], q[1], q[2], q[3]);
       p.dh_sf[sf_tiled_offset(prow, 2 * c0, 2 * (int64_t)I)] = (uint8_t)byte;
     } else {
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dh) + prow * (2 * (int64_t)I) + 2 * c0);
+      uint16_t* dst = static_cast<uint16_t*>(p.dh) + prow * (2 * (int64_t)I) + 2 * c0;
+      auto pk = [&](int j) { return pack_bf16x2(dg[j], du[j]); };
 #pragma unroll
-      for (int w = 0; w < NC / 4; ++w)
-        dst[w] = make_uint4(pack_bf16x2(dg[4 * w + 0], du[4 * w + 0]), pack_bf16x2(dg[4 * w + 1], du[4 * w + 1]),
-                            pack_bf16x2(dg[4 * w + 2], du[4 * w + 2]), pack_bf16x2(dg[4 * w + 3], du[4 * w + 3]));
+      for (int w = 0; w < NC / 8; ++w)  // whole 32-byte sectors
+        st_global_32b(dst + 16 * w, pk(8 * w), pk(8 * w + 1), pk(8 * w + 2), pk(8 * w + 3), pk(8 * w + 4),
+                      pk(8 * w + 5), pk(8 * w + 6), pk(8 * w + 7));
     }
   } else if constexpr (MX) {
     float amg = 0.f, amu = 0.f;
@@ -415,14 +414,14 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
   } else {
     group_bar<32 * SUBS>(bar_id);  // keep the barrier count identical on both paths
     uint16_t* dh = static_cast<uint16_t*>(p.dh) + prow * (2 * (int64_t)I);
-    uint4* dgp = reinterpret_cast<uint4*>(dh + c0);
-    uint4* dup = reinterpret_cast<uint4*>(dh + I + c0);
-#pragma unroll
-    for (int q = 0; q < NC / 8; ++q) {
-      dgp[q] = make_uint4(pack_bf16x2(dg[8 * q + 0], dg[8 * q + 1]), pack_bf16x2(dg[8 * q + 2], dg[8 * q + 3]),
-                          pack_bf16x2(dg[8 * q + 4], dg[8 * q + 5]), pack_bf16x2(dg[8 * q + 6], dg[8 * q + 7]));
-      dup[q] = make_uint4(pack_bf16x2(du[8 * q + 0], du[8 * q + 1]), pack_bf16x2(du[8 * q + 2], du[8 * q + 3]),
-                          pack_bf16x2(du[8 * q + 4], du[8 * q + 5]), pack_bf16x2(du[8 * q + 6], du[8 * q + 7]));
+    auto pg = [&](int j) { return pack_bf16x2(dg[j], dg[j + 1]); };
+    auto pu = [&](int j) { return pack_bf16x2(du[j], du[j + 1]); };
+    if constexpr (NC == 16) {  // whole 32-byte sectors
+      st_global_32b(dh + c0, pg(0), pg(2), pg(4), pg(6), pg(8), pg(10), pg(12), pg(14));
+      st_global_32b(dh + I + c0, pu(0), pu(2), pu(4), pu(6), pu(8), pu(10), pu(12), pu(14));
+    } else {
+      *reinterpret_cast<uint4*>(dh + c0) = make_uint4(pg(0), pg(2), pg(4), pg(6));
+      *reinterpret_cast<uint4*>(dh + I + c0) = make_uint4(pu(0), pu(2), pu(4), pu(6));
     }
   }
   // dh^T rows in W1's gate/up layout, a'^T rows by feature

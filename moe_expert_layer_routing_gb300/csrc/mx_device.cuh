@@ -35,6 +35,17 @@ __device__ __forceinline__ void st_global_32b(void* p, uint32_t w0, uint32_t w1,
                : "memory");
 }
 
+// The same 32 bytes where p may be only 16-byte aligned (caller-owned outputs): two 16-byte stores then.
+__device__ __forceinline__ void st_global_32b_or_halves(void* p, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                                        uint32_t w4, uint32_t w5, uint32_t w6, uint32_t w7) {
+  if ((reinterpret_cast<uintptr_t>(p) & 31u) == 0) {
+    st_global_32b(p, w0, w1, w2, w3, w4, w5, w6, w7);
+  } else {
+    reinterpret_cast<uint4*>(p)[0] = make_uint4(w0, w1, w2, w3);
+    reinterpret_cast<uint4*>(p)[1] = make_uint4(w4, w5, w6, w7);
+  }
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(((uint32_t)b) << 16);
 }

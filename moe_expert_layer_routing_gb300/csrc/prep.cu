@@ -279,16 +279,15 @@ __global__ void __launch_bounds__(256) apt_from_ckpt_kernel(const uint16_t* __re
   if constexpr (MX) {
     uint32_t w[8];
     const uint32_t byte = quantize_group32_t<AF>(v, w);
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + (int64_t)i * P + p0);
-    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    st_global_32b(static_cast<uint8_t*>(out) + (int64_t)i * P + p0, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
     out_sf[sf_tiled_offset(i, p0, P)] = (uint8_t)byte;
   } else {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (int64_t)i * P + p0);
+    uint16_t* dst = static_cast<uint16_t*>(out) + (int64_t)i * P + p0;
+    auto pk = [&](int j) { return pack_bf16x2(v[j], v[j + 1]); };
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      dst[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                          pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    for (int q = 0; q < 2; ++q)  // whole 32-byte sectors
+      st_global_32b(dst + 16 * q, pk(16 * q), pk(16 * q + 2), pk(16 * q + 4), pk(16 * q + 6), pk(16 * q + 8),
+                    pk(16 * q + 10), pk(16 * q + 12), pk(16 * q + 14));
   }
 }
 
@@ -462,16 +461,16 @@ __global__ void __launch_bounds__(256) quant_colwise_kernel(const uint16_t* __re
   if constexpr (MX) {
     uint32_t w[8];
     const uint32_t byte = quantize_group32(v, fmt, w);
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(q) + oc * rows + orr);
-    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    st_global_32b_or_halves(static_cast<uint8_t*>(q) + oc * rows + orr, w[0], w[1], w[2], w[3], w[4], w[5], w[6],
+                            w[7]);
     sf[tiled ? sf_tiled_offset(oc, orr, rows) : oc * (rows / 32) + orr / 32] = (uint8_t)byte;
   } else {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(q) + oc * rows + orr);
+    uint16_t* dst = static_cast<uint16_t*>(q) + oc * rows + orr;
+    auto pk = [&](int j) { return pack_bf16x2(v[j], v[j + 1]); };
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      dst[k] = make_uint4(pack_bf16x2(v[8 * k + 0], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
-                          pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+    for (int k = 0; k < 2; ++k)  // whole 32-byte sectors (q is caller-owned: 16-byte alignment)
+      st_global_32b_or_halves(dst + 16 * k, pk(16 * k), pk(16 * k + 2), pk(16 * k + 4), pk(16 * k + 6), pk(16 * k + 8),
+                    pk(16 * k + 10), pk(16 * k + 12), pk(16 * k + 14));
   }
 }
 

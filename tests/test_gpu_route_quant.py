@@ -109,3 +109,25 @@ def test_quantize_colwise_bit_exact(fmt, layout, gather):
     s = sf.cpu().numpy()
     s = tiled_sf_to_plain(s, rq.shape[0], rq.shape[1]) if layout == 1 else s.reshape(rq.shape[0], -1)
     assert np.array_equal(s, rs)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_quantize_colwise_16_byte_aligned_output(fmt):
+    """The codes go to a caller buffer that is 16- but not 32-byte aligned (the public contract):
+    same bytes as into an aligned buffer, and the oracle's."""
+    mb = _lib()
+    x = _wide_bf16(416, 128, seed=30 + fmt)
+    q_al, sf_al = mb.mxfp8_quantize(x.cuda(), mb.QUANT_COLWISE, fmt, None, 0)
+    buf = torch.zeros(128 * 416 + 64, dtype=torch.uint8, device="cuda")
+    base = buf.data_ptr()
+    off = (32 - base % 32) % 32 + 16          # 16 bytes past a 32-byte boundary
+    sf = torch.zeros(128 * 416 // 32, dtype=torch.uint8, device="cuda")
+    xd = x.cuda()
+    rc = mb.lib().mxfp8_quantize(xd.data_ptr(), 416, 416, 128, 128, None, mb.QUANT_COLWISE, fmt, base + off,
+                                 sf.data_ptr(), 0, None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    q = buf[off:off + 128 * 416].view(128, 416)
+    assert torch.equal(q, q_al) and torch.equal(sf, sf_al)
+    rq, _ = omx.mx_quantize(x.double().numpy().T, fmt, axis=1)
+    assert np.array_equal(q.cpu().numpy(), rq)
