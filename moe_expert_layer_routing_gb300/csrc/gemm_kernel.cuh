@@ -54,6 +54,9 @@ struct GemmCfg {
   static constexpr int EPI_WARP_BYTES = (EPI == kEpiDSwiGLU) ? G1_TBUFS * G1_NC * kTransPitch * 4 : 0;
   static constexpr int XCHG_QUARTER = kG1Subs * 2 * 32;  // floats: [slice][gate|up][lane]
   static constexpr int XCHG_BYTES = (EPI == kEpiDSwiGLU) ? 2 * 4 * XCHG_QUARTER * 4 : 0;
+  // MXFP8 row-wise dh: the two column slices of a quarter swap 16-byte halves of their quantised gate
+  // and up columns ([quarter][slice][lane] uint4), so that each writes one whole 32-byte sector
+  static constexpr int QX_BYTES = (EPI == kEpiDSwiGLU && MX && G1_NC == 16) ? 4 * 2 * 32 * 16 : 0;
   static constexpr int CK_CHUNK_BYTES = 2 * 32 * 128 * 2;
   static constexpr int CK_BYTES = (EPI == kEpiDSwiGLU) ? 2 * CK_CHUNK_BYTES : 0;
   // Store epilogue with a single TMEM accumulator: the tile is drained into a 128B-swizzled bf16
@@ -76,7 +79,7 @@ struct GemmCfg {
   static constexpr bool CK_LOADER = EPI == kEpiDSwiGLU;
   static constexpr int CK_LOADER_WARP = 2 + EPI_WARPS;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS + (CK_LOADER ? 32 : 0);
-  static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES + XCHG_BYTES + CK_BYTES + STAGING_BYTES;
+  static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES + XCHG_BYTES + QX_BYTES + CK_BYTES + STAGING_BYTES;
   static constexpr int BAR_BYTES = 512;
   static constexpr int RING = 4;  // tile indices published by the producer ahead of the consumers
   static constexpr int STAGES_FIT = (kSmemLimit - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
@@ -283,8 +286,8 @@ __device__ __forceinline__ void group_bar(int id) {
 template <bool MX, int NC, int AF, bool GENERIC, bool SHARED_TBUF>
 __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t taddr, int64_t prow, int m, int lane,
                                                  bool valid, float sv, int i0, int sub, const uint16_t* ck,
-                                                 const uint16_t* ga, float* tbuf, float* xchg, int bar_id,
-                                                 float& ds_acc) {
+                                                 const uint16_t* ga, float* tbuf, float* xchg, uint4* qx,
+                                                 int bar_id, float& ds_acc) {
   constexpr int SUBS = 32 / NC;
   const int I = p.I;
   const int64_t P = p.P;
@@ -401,8 +404,15 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
       qu[w] = fp8x4_t<AF>(du[4 * w] * iu, du[4 * w + 1] * iu, du[4 * w + 2] * iu, du[4 * w + 3] * iu);
     }
     if constexpr (NC == 16) {
-      *reinterpret_cast<uint4*>(dh + c0) = make_uint4(qg[0], qg[1], qg[2], qg[3]);
-      *reinterpret_cast<uint4*>(dh + I + c0) = make_uint4(qu[0], qu[1], qu[2], qu[3]);
+      // slice 0 writes the row's 32 gate columns i0.., slice 1 its 32 up columns I + i0..: each takes
+      // the other's half from shared memory (one more barrier of the quarter's two warps)
+      qx[sub * 32 + lane] = sub == 0 ? make_uint4(qu[0], qu[1], qu[2], qu[3]) : make_uint4(qg[0], qg[1], qg[2], qg[3]);
+      group_bar<32 * SUBS>(bar_id);
+      const uint4 o = qx[(1 - sub) * 32 + lane];
+      if (sub == 0)
+        st_global_32b(dh + i0, qg[0], qg[1], qg[2], qg[3], o.x, o.y, o.z, o.w);
+      else
+        st_global_32b(dh + I + i0, o.x, o.y, o.z, o.w, qu[0], qu[1], qu[2], qu[3]);
     } else {
       *reinterpret_cast<uint2*>(dh + c0) = make_uint2(qg[0], qg[1]);
       *reinterpret_cast<uint2*>(dh + I + c0) = make_uint2(qu[0], qu[1]);
@@ -413,6 +423,7 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
     }
   } else {
     group_bar<32 * SUBS>(bar_id);  // keep the barrier count identical on both paths
+    if constexpr (MX && NC == 16) group_bar<32 * SUBS>(bar_id);
     uint16_t* dh = static_cast<uint16_t*>(p.dh) + prow * (2 * (int64_t)I);
     auto pg = [&](int j) { return pack_bf16x2(dg[j], dg[j + 1]); };
     auto pu = [&](int j) { return pack_bf16x2(du[j], du[j + 1]); };
@@ -455,7 +466,9 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
   uint8_t* smCK = smSFB + C::STAGES * C::SFB_BYTES;     // checkpoint chunks (dSwiGLU epilogue), 512-aligned
   uint8_t* smEPI = smCK + C::CK_BYTES;
   float* smXchg = reinterpret_cast<float*>(smEPI + C::EPI_WARPS * C::EPI_WARP_BYTES);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smEPI + C::EPI_WARPS * C::EPI_WARP_BYTES + C::XCHG_BYTES);
+  uint4* smQx = reinterpret_cast<uint4*>(smEPI + C::EPI_WARPS * C::EPI_WARP_BYTES + C::XCHG_BYTES);
+  uint64_t* full =
+      reinterpret_cast<uint64_t*>(smEPI + C::EPI_WARPS * C::EPI_WARP_BYTES + C::XCHG_BYTES + C::QX_BYTES);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
@@ -857,23 +870,24 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
             const int i0 = ti.nt * BN + c * 32;
             const uint16_t* ckb = reinterpret_cast<const uint16_t*>(smCK + buf * C::CK_CHUNK_BYTES);
             float* xc = xchg + (int)(ck_next & 1) * (4 * C::XCHG_QUARTER);
+            uint4* qx = smQx + q * 64;
             // the activation format fixed per instantiation; SwiGLU with concat gate/up specialised
             const bool generic = p.glu != MOE_GLU_SWIGLU || p.interleaved || p.gate_act != nullptr;
             float* tb = reinterpret_cast<float*>(wsm);
             if (!MX || p.fmt_act == MOE_FP8_E5M2) {
               if (generic)
                 epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2, true, C::G1_TBUFS == 1>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
-                                                                  xc, 2 + q, ds_acc);
+                                                                  xc, qx, 2 + q, ds_acc);
               else
                 epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2, false, C::G1_TBUFS == 1>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
-                                                                   xc, 2 + q, ds_acc);
+                                                                   xc, qx, 2 + q, ds_acc);
             } else {
               if (generic)
                 epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3, true, C::G1_TBUFS == 1>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
-                                                                  xc, 2 + q, ds_acc);
+                                                                  xc, qx, 2 + q, ds_acc);
               else
                 epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3, false, C::G1_TBUFS == 1>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
-                                                                   xc, 2 + q, ds_acc);
+                                                                   xc, qx, 2 + q, ds_acc);
             }
           }
           __syncwarp();
