@@ -185,6 +185,26 @@ def test_linear_bwd_small_both_precisions():
         assert rel_fro(np64(got["dW"]), ref["dW"]) < tol
 
 
+def test_linear_bwd_outputs_16_byte_aligned():
+    """Outputs in caller buffers that are 16- but not 32-byte aligned (the public contract), through
+    the direct-store epilogue (K = 384: 128-column tiles): identical to aligned outputs."""
+    import moe_expert_layer_routing_gb300 as mb
+    inp = make_linear_inputs(LinearConfig("lin_align", M=256, N=256, K=384, seed=43))
+    dY, W, X = inp.dY.cuda(), inp.W.cuda(), inp.X.cuda()
+    ref = mb.linear_bwd(dY, W, X, precision=mb.PREC_MXFP8)
+    op = mb.LinearBwd(256, 256, 384, mb.PREC_MXFP8, device="cuda")
+    views = []
+    for rows in (256, 256):
+        buf = torch.zeros(rows * 384 + 32, dtype=torch.bfloat16, device="cuda")
+        off = ((32 - buf.data_ptr() % 32) % 32 + 16) // 2   # elements to 16 bytes past a 32-byte boundary
+        views.append(buf[off:off + rows * 384].view(rows, 384))
+    op.dX, op.dW = views
+    assert op.dX.data_ptr() % 32 == 16 and op.dW.data_ptr() % 32 == 16
+    op.run(dY, W, X)
+    torch.cuda.synchronize()
+    assert torch.equal(op.dX, ref["dX"]) and torch.equal(op.dW, ref["dW"])
+
+
 def test_linear_bwd_dense_4096_config():
     """The dense MXFP8 workload at full size (oracle float64 matmuls of 4096^3)."""
     import moe_expert_layer_routing_gb300 as mb
