@@ -353,7 +353,9 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
   const bool il = GENERIC && NC == 16 && p.interleaved;  // gate_i, up_i at columns 2i, 2i+1 (host: NC == 16)
   if (il) {
     // this warp's 16 (gate, up) pairs are the 32 consecutive columns 2*c0.. of dh: one MX group
-    group_bar<32 * SUBS>(bar_id);  // keep the barrier count identical on every path
+    // (the layout is fixed per launch: a quarter's warps take the same branch and meet at the same
+    // named barriers)
+    group_bar<32 * SUBS>(bar_id);
     if constexpr (MX) {
       float am = 0.f;
 #pragma unroll
@@ -422,8 +424,7 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
       p.dh_sf[sf_tiled_offset(prow, I + i0, 2 * (int64_t)I)] = (uint8_t)bu;
     }
   } else {
-    group_bar<32 * SUBS>(bar_id);  // keep the barrier count identical on both paths
-    if constexpr (MX && NC == 16) group_bar<32 * SUBS>(bar_id);
+    group_bar<32 * SUBS>(bar_id);  // the amax exchange's barrier on the MXFP8 branch (its partner's reads)
     uint16_t* dh = static_cast<uint16_t*>(p.dh) + prow * (2 * (int64_t)I);
     auto pg = [&](int j) { return pack_bf16x2(dg[j], dg[j + 1]); };
     auto pu = [&](int j) { return pack_bf16x2(du[j], du[j + 1]); };
