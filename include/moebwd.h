@@ -98,7 +98,8 @@ const char* moe_version(void);
  * T*K < E - 1; 0 when T*K == 0.  Pure host function. */
 int64_t moe_num_blocks_bound(int64_t T, int K, int E, int block_size);
 
-/* Bytes of workspace moe_route_meta needs. */
+/* Bytes of workspace moe_route_meta needs; 0 for sizes moe_route_meta rejects (block_size outside
+ * {128,256,512,1024}, E outside [1, 1024], K <= 0, T < 0). */
 size_t moe_route_meta_workspace_size(int T, int K, int E, int block_size);
 
 /* Routing metadata from expert ids ([BW] token_position_to_id, block_to_expert; [SM]
@@ -116,7 +117,7 @@ size_t moe_route_meta_workspace_size(int T, int K, int E, int block_size);
  *   num_blocks [1]              total blocks in use
  * status_dev (device) int32 [1]: MOE_STATUS_BAD_EXPERT_ID is OR-ed in for ids outside [0,E).
  * Entries x_gather_idx / s_scatter_idx [TKv, T*K) are left unchanged.  block_size must be one of
- * 128, 256, 512, 1024; 1 <= E <= 4096; T*K < 2^31. */
+ * 128, 256, 512, 1024; 1 <= E <= 1024; T*K < 2^31. */
 int moe_route_meta(const int32_t* ids, int T, int K, int E, int block_size, int32_t* expert_offsets,
                    int32_t* x_gather_idx, int32_t* s_scatter_idx, int32_t* s_reverse_scatter_idx,
                    int32_t* token_position_to_id, int32_t* block_to_expert, int32_t* block_offsets,
@@ -127,7 +128,8 @@ int moe_route_meta(const int32_t* ids, int T, int K, int E, int block_size, int3
  * a memory pool or arena without raw allocations, hooks that may not call cudaMalloc mid-step,
  * callers that must not allocate after start-up).  None of the source pages has a counterpart: it is
  * an interface addition of this library.  Same arguments, outputs and errors as moe_route_meta, minus
- * the workspace: the scratch is a fixed 4 MiB device array owned by the library (held on every GPU
+ * the workspace (its size arguments are checked first, in moe_route_meta's order, with the same
+ * codes): the scratch is a fixed 4 MiB device array owned by the library (held on every GPU
  * that loads it, until exit), which admits about T*K <= 150k routed rows for E <= 128 (the exact
  * limit is moe_route_meta_workspace_size(T,K,E,B) <= 4 MiB; larger sizes return
  * MOE_ERR_UNSUPPORTED with a message and launch nothing).  The first call on a device looks up the
@@ -147,7 +149,8 @@ int moe_route_meta_noalloc(const int32_t* ids, int T, int K, int E, int block_si
  * E8M0 scale ([BW] first paragraph, gate_up_weight_scales; [MM] float8_dtype).  Scale rule (OCP
  * MX v1.0): byte = clamp(floor(log2(amax)) - emax + 127, 0, 254), emax = 8 (e4m3) / 15 (e5m2),
  * floor(log2) taken from the binary exponent of amax; element = round-to-nearest-even of
- * v * 2^(127 - byte), saturated to +-448 / +-57344; zero encodes as 0x00.
+ * v * 2^(127 - byte), saturated to +-448 / +-57344, the sign kept: a value that rounds to zero
+ * encodes as 0x00 when positive and 0x80 (-0) when negative, as a float8 cast of the scaled value does.
  *
  * in (device) bf16 [src_rows, cols] with row stride `ld` elements (ld >= cols, ld % 8 == 0).
  * row_index (device, nullable) int32 [rows]: output row r reads input row row_index[r], -1 reads
@@ -257,7 +260,7 @@ size_t moe_bwd_workspace_size(const MoeBwdArgs* args);
 /* The whole backward on `stream`: routing metadata, gathers/quantisation, the four grouped GEMMs
  * (dA with the fused dSwiGLU/ds epilogue, dW_down, dx_expanded, dW_gate_up), the top-K
  * scatter-sum into dx, ds and the bias gradients.  Requirements: H % 128 == 0, I % 128 == 0,
- * 1 <= K <= E <= 4096, T*K < 2^31, x/dout/weights 16-byte aligned. */
+ * 1 <= K <= E <= 1024, T*K < 2^31, x/dout/weights 16-byte aligned. */
 int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream);
 
 /* Regions of the moe_bwd workspace (for inspection of intermediates in tests and debugging).

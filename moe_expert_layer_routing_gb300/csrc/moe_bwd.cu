@@ -322,8 +322,20 @@ extern "C" int moe_bwd_workspace_region(const MoeBwdArgs* args, int region, size
   return MOE_OK;
 }
 
+// Size arguments of the routing-metadata entry points, checked in one order so that every entry
+// point reports the same error for the same input.
+int moebwd::check_route_sizes(const char* who, int T, int K, int E, int block_size) {
+  if (T < 0 || K <= 0 || E <= 0 || K > E) return fail(MOE_ERR_INVALID, "%s: bad sizes", who);
+  if (E > kMaxExperts) return fail(MOE_ERR_UNSUPPORTED, "%s: E above %d", who, kMaxExperts);
+  if (block_size != 128 && block_size != 256 && block_size != 512 && block_size != 1024)
+    return fail(MOE_ERR_UNSUPPORTED, "%s: block_size must be 128, 256, 512 or 1024", who);
+  if ((int64_t)T * K >= (int64_t)1 << 31) return fail(MOE_ERR_UNSUPPORTED, "%s: T*K too large", who);
+  return MOE_OK;
+}
+
 extern "C" size_t moe_route_meta_workspace_size(int T, int K, int E, int block_size) {
   if (T < 0 || K <= 0 || E <= 0 || E > kMaxExperts) return 0;
+  if (block_size != 128 && block_size != 256 && block_size != 512 && block_size != 1024) return 0;
   MoeBwdArgs a{};
   a.T = T; a.K = K; a.E = E; a.block_size = block_size; a.H = 128; a.I = 128;
   const Layout L = make_layout(a);
@@ -337,11 +349,8 @@ extern "C" int moe_route_meta(const int32_t* ids, int T, int K, int E, int block
                               int32_t* num_blocks, int32_t* status_dev, void* workspace, size_t workspace_bytes,
                               moe_stream_t stream) {
   clear_error();
-  if (T < 0 || K <= 0 || E <= 0 || K > E) return fail(MOE_ERR_INVALID, "moe_route_meta: bad sizes");
-  if (E > kMaxExperts) return fail(MOE_ERR_UNSUPPORTED, "moe_route_meta: E above %d", kMaxExperts);
-  if (block_size != 128 && block_size != 256 && block_size != 512 && block_size != 1024)
-    return fail(MOE_ERR_UNSUPPORTED, "moe_route_meta: block_size must be 128, 256, 512 or 1024");
-  if ((int64_t)T * K >= (int64_t)1 << 31) return fail(MOE_ERR_UNSUPPORTED, "moe_route_meta: T*K too large");
+  int rc0 = check_route_sizes("moe_route_meta", T, K, E, block_size);
+  if (rc0) return rc0;
   if (!ids || !expert_offsets || !x_gather_idx || !s_scatter_idx || !s_reverse_scatter_idx || !token_position_to_id ||
       !block_to_expert || !block_offsets || !num_blocks || !status_dev || !workspace)
     return fail(MOE_ERR_INVALID, "moe_route_meta: null pointer");

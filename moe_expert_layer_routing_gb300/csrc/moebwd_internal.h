@@ -55,6 +55,8 @@ struct RouteBufs {
   int32_t* status;
 };
 int route_nchunks(int64_t TK);
+// size checks shared by moe_route_meta and moe_route_meta_noalloc (same order, same messages)
+int check_route_sizes(const char* who, int T, int K, int E, int block_size);
 // order[0..num_tiles) = tiles sorted (bucketed) by the token of their first row
 int launch_tile_order(const int32_t* tile_row_flat, const int32_t* num_tiles, int T, int K, int32_t* order,
                       cudaStream_t st);

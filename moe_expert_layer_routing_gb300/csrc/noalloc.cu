@@ -59,16 +59,18 @@ extern "C" int moe_route_meta_noalloc(const int32_t* ids, int T, int K, int E, i
                                       int32_t* block_to_expert, int32_t* block_offsets, int32_t* num_blocks,
                                       int32_t* status_dev, moe_stream_t stream) {
   clear_error();
-  if (T < 0 || K <= 0 || E <= 0 || K > E) return fail(MOE_ERR_INVALID, "moe_route_meta_noalloc: bad sizes");
+  // the size checks of moe_route_meta, in its order and with its messages, before the scratch size
+  // is computed from them
+  int rc = check_route_sizes("moe_route_meta_noalloc", T, K, E, block_size);
+  if (rc) return rc;
   const size_t need = moe_route_meta_workspace_size(T, K, E, block_size);
-  if (need == 0) return fail(MOE_ERR_UNSUPPORTED, "moe_route_meta_noalloc: unsupported sizes");
   if (need > kNoAllocScratchBytes)
     return fail(MOE_ERR_UNSUPPORTED,
                 "moe_route_meta_noalloc: T=%d K=%d E=%d need %zu bytes of scratch, above the fixed %zu; "
                 "use moe_route_meta with a workspace",
                 T, K, E, need, kNoAllocScratchBytes);
   void* scratch = nullptr;
-  int rc = noalloc_scratch(&scratch);
+  rc = noalloc_scratch(&scratch);
   if (rc) return rc;
   return moe_route_meta(ids, T, K, E, block_size, expert_offsets, x_gather_idx, s_scatter_idx, s_reverse_scatter_idx,
                         token_position_to_id, block_to_expert, block_offsets, num_blocks, status_dev, scratch,

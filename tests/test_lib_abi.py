@@ -77,3 +77,29 @@ def test_product_path_refuses_cpu_tensors():
     import moe_expert_layer_routing_gb300 as mb
     with pytest.raises(mb.MoeError):
         mb.mxfp8_quantize(torch.zeros(32, 32, dtype=torch.bfloat16))
+
+
+@pytest.mark.parametrize("T,K,E,B,code,text", [
+    (1000, 2, 8, 0, -2, b"block_size"),      # used to divide by zero in the scratch-size query
+    (1000, 2, 8, 100, -2, b"block_size"),
+    (1000, 2, 2048, 128, -2, b"E above"),
+    (1000, 9, 8, 128, -1, b"bad sizes"),     # K > E
+    (-1, 2, 8, 128, -1, b"bad sizes"),
+])
+def test_route_meta_entry_points_reject_bad_sizes_alike(lib, T, K, E, B, code, text):
+    """moe_route_meta and moe_route_meta_noalloc check their size arguments in the same order with the
+    same codes, before anything else (no CUDA call, no launch): this runs without a GPU."""
+    import moe_expert_layer_routing_gb300 as mb
+    before = mb.kernel_launches()
+    assert lib.moe_route_meta(None, T, K, E, B, *([None] * 10), 0, None) == code
+    assert text in lib.moe_last_error()
+    assert lib.moe_route_meta_noalloc(None, T, K, E, B, *([None] * 10)) == code
+    msg = lib.moe_last_error()
+    assert text in msg and msg.startswith(b"moe_route_meta_noalloc")
+    assert mb.kernel_launches() == before
+
+
+def test_route_meta_workspace_size_is_zero_for_rejected_sizes(lib):
+    for B in (0, -128, 100):
+        assert lib.moe_route_meta_workspace_size(1000, 2, 8, B) == 0
+    assert lib.moe_route_meta_workspace_size(1000, 2, 2048, 128) == 0

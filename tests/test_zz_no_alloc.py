@@ -53,3 +53,18 @@ def test_noalloc_rejects_sizes_above_its_scratch():
     assert rc == -2
     assert b"scratch" in mb.lib().moe_last_error()
     assert mb.kernel_launches() == launches
+
+
+@pytest.mark.parametrize("B,E,K,code,text", [(0, 8, 2, -2, b"block_size"), (100, 8, 2, -2, b"block_size"),
+                                             (128, 2048, 2, -2, b"E above"), (128, 8, 9, -1, b"bad sizes")])
+def test_noalloc_bad_arguments_return_codes_without_launching(B, E, K, code, text):
+    """Bad sizes are refused before the scratch size is computed: a code, moe_route_meta's message and
+    no kernel launched (block_size 0 once reached a division by zero on the host)."""
+    import moe_expert_layer_routing_gb300 as mb
+    ids = torch.zeros(64, K, dtype=torch.int32, device="cuda")
+    launches = mb.kernel_launches()
+    rc = mb.lib().moe_route_meta_noalloc(ctypes.c_void_p(ids.data_ptr()), 64, K, E, B, *([None] * 9),
+                                         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == code
+    assert text in mb.lib().moe_last_error()
+    assert mb.kernel_launches() == launches
