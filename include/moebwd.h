@@ -351,6 +351,38 @@ int moe_profile_read(double* stage_ms, int max_stages, int* calls);
 uint64_t moe_kernel_launches(void);
 
 /* ------------------------------------------------------------------------------------------ */
+/* Options                                                                                     */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Process-wide options, read by every later call on any host thread (set them while no call is
+ * running).  None is needed for correct results: the defaults are the measured-fastest choices, and
+ * every choice computes the same gradients (tile widths only change the order of fp32 additions
+ * inside a GEMM).  They exist for tests, tuning runs and diagnosis.  A tile width that does not
+ * divide the GEMM's N dimension falls back to the default; options that change a tile width change
+ * moe_bwd_workspace_size, so query it after setting them. */
+enum {
+  MOE_OPT_WAIT_LIMIT_NS = 0, /* limit of each pipeline wait inside the GEMM kernels before the kernel
+                                reports MOE_STATUS_TIMEOUT, drains what it has in flight and returns;
+                                1 .. 6e10 ns, default 2e9 (2 s).  A short limit on a real workload makes
+                                the kernels give up (a way to exercise that path without a fault); the
+                                waits that drain copies and tensor-core work before a CTA exits keep 2 s */
+  MOE_OPT_PAIR_GEMMS,        /* CTA-pair GEMMs: 0 never, 1 the BF16 store/recompute GEMMs where they
+                                apply (default), 2 also MXFP8 */
+  MOE_OPT_PAIR_TILE_N,       /* N width of the pair tile: 256 (default) or 128 */
+  MOE_OPT_G1_TILE_N,         /* N tile of the dA/dSwiGLU GEMM: 0 automatic (default: MXFP8 192 where it
+                                divides I, BF16 256 where it divides I, else 128), 128, 192 (MXFP8), 256 */
+  MOE_OPT_G2_TILE_N,         /* N tile of dx_expanded: 0 automatic (256 where it divides H), 128, 256 */
+  MOE_OPT_G3_TILE_N,         /* N tile of dW_down: 0 automatic (256 where it divides H), 128, 256 */
+  MOE_OPT_G4_TILE_N,         /* N tile of dW_gate_up: 0 automatic (256), 128, 256 */
+  MOE_OPT_PREP_TILE_ORDER,   /* 1 (default): the gather pass walks tiles in token order; 0: in index order */
+  MOE_NUM_OPTIONS
+};
+/* Set an option; value -1 restores its default.  MOE_ERR_INVALID for an unknown option or value. */
+int moe_set_option(int option, int64_t value);
+/* Current value of an option (-1 for an unknown option). */
+int64_t moe_get_option(int option);
+
+/* ------------------------------------------------------------------------------------------ */
 /* Dense linear backward (the E=1, K=1 degenerate case)                                        */
 /* ------------------------------------------------------------------------------------------ */
 

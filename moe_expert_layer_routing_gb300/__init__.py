@@ -32,7 +32,11 @@ EXPORTED = ["moe_last_error", "moe_version", "moe_num_blocks_bound", "moe_route_
             "moe_route_meta", "mxfp8_quantize", "moe_bwd_workspace_size", "moe_bwd",
             "moe_bwd_workspace_region", "moe_tile_rows_capacity", "linear_bwd_workspace_size",
             "linear_bwd", "moe_profile_enable", "moe_profile_read", "moe_kernel_launches",
-            "moe_route_meta_noalloc", "moe_router_bwd"]
+            "moe_route_meta_noalloc", "moe_router_bwd", "moe_set_option", "moe_get_option"]
+
+# library options (moe_set_option)
+OPTIONS = ["WAIT_LIMIT_NS", "PAIR_GEMMS", "PAIR_TILE_N", "G1_TILE_N", "G2_TILE_N", "G3_TILE_N", "G4_TILE_N",
+           "PREP_TILE_ORDER"]
 
 STAGES = ["route", "prep", "G1_dA_dswiglu", "G3_dW2", "G2_dx_expanded", "G4_dW1", "reduce", "G0_recompute_h"]
 
@@ -86,6 +90,8 @@ def lib():
         "moe_kernel_launches": ([], ctypes.c_uint64),
         "moe_route_meta_noalloc": ([vp, i32, i32, i32, i32] + [vp] * 9 + [vp], i32),
         "moe_router_bwd": ([i32, i32, vp, vp, vp, vp, i32, i32, i32, vp, vp], i32),
+        "moe_set_option": ([i32, i64], i32),
+        "moe_get_option": ([i32], i64),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -128,6 +134,31 @@ def profile_read() -> tuple[dict, int]:
     calls = ctypes.c_int()
     _check(lib().moe_profile_read(arr, len(STAGES), ctypes.byref(calls)), "moe_profile_read")
     return {n: arr[i] for i, n in enumerate(STAGES)}, calls.value
+
+
+def set_option(name: str, value: int | None):
+    """Set a library option by its name in OPTIONS (None restores the default)."""
+    _check(lib().moe_set_option(OPTIONS.index(name), -1 if value is None else int(value)), "moe_set_option")
+
+
+def get_option(name: str) -> int:
+    return int(lib().moe_get_option(OPTIONS.index(name)))
+
+
+class option:
+    """Context manager: set a library option for the duration of a block, then restore its old value."""
+
+    def __init__(self, name: str, value: int):
+        self.name, self.value = name, value
+
+    def __enter__(self):
+        self.old = get_option(self.name)
+        set_option(self.name, self.value)
+        return self
+
+    def __exit__(self, *exc):
+        set_option(self.name, self.old)
+        return False
 
 
 def kernel_launches() -> int:

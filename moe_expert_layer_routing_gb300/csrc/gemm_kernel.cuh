@@ -138,7 +138,9 @@ __device__ __forceinline__ TileInfo gemm_decode_tile(const GemmParams& p, int t)
   return ti;
 }
 
-// Wait without giving up when another role aborted (used to drain copies / MMAs in flight).
+// Wait without giving up when another role aborted (used to drain copies / MMAs in flight).  It keeps
+// the fixed 2 s limit whatever the launch's pipeline-wait limit, so that copies and tensor-core work
+// in flight land before a CTA frees its shared memory and TMEM.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int* status) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = globaltimer_ns();
@@ -530,7 +532,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       for (;;) {
         int t = atomicAdd(p.tile_counter, 1);
         if (t >= total) t = -1;
-        if (!mbar_wait_bounded(&tile_empty[rs], rph ^ 1u, p.status, abort_flag)) break;
+        if (!mbar_wait_bounded(&tile_empty[rs], rph ^ 1u, p.status, abort_flag, p.wait_ns)) break;
         tile_ring[rs] = t;
         mbar_arrive(&tile_full[rs]);
         if (++rs == C::RING) {
@@ -541,7 +543,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         const TileInfo ti = gemm_decode_tile<BN, C::BKE>(p, t);
         bool ok = true;
         for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, abort_flag)) {
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -583,7 +585,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       int rs = 0;
       uint32_t rph = 0;
       while (ok) {
-        if (!mbar_wait_bounded(&tile_full[rs], rph, p.status, abort_flag)) break;
+        if (!mbar_wait_bounded(&tile_full[rs], rph, p.status, abort_flag, p.wait_ns)) break;
         const int t = tile_ring[rs];
         mbar_arrive(&tile_empty[rs]);
         if (++rs == C::RING) {
@@ -592,11 +594,11 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         }
         if (t < 0) break;
         const TileInfo ti = gemm_decode_tile<BN, C::BKE>(p, t);
-        if (!mbar_wait_bounded(&tempty[acc], aph ^ 1u, p.status, abort_flag)) break;
+        if (!mbar_wait_bounded(&tempty[acc], aph ^ 1u, p.status, abort_flag, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * C::ACC_STRIDE);
         for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait_bounded(&full[s], ph, p.status, abort_flag)) {
+          if (!mbar_wait_bounded(&full[s], ph, p.status, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -654,7 +656,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       uint32_t rph = 0;
       bool ok = true;
       while (ok) {
-        if (!mbar_wait_bounded(&tile_full[rs], rph, p.status, abort_flag)) break;
+        if (!mbar_wait_bounded(&tile_full[rs], rph, p.status, abort_flag, p.wait_ns)) break;
         const int t = tile_ring[rs];
         mbar_arrive(&tile_empty[rs]);
         if (++rs == C::RING) {
@@ -669,7 +671,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         for (int c = 0; c < C::NCHUNK; ++c) {
           const int buf = (int)(issued & 1);
           if (issued >= 2 &&
-              !mbar_wait_bounded(&ck_empty[buf], (uint32_t)(((issued - 2) >> 1) & 1), p.status, abort_flag)) {
+              !mbar_wait_bounded(&ck_empty[buf], (uint32_t)(((issued - 2) >> 1) & 1), p.status, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -700,7 +702,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
     int rs = 0;
     uint32_t rph = 0;
     while (ok) {
-      const bool gt = mbar_wait_bounded(&tile_full[rs], rph, p.status, abort_flag);
+      const bool gt = mbar_wait_bounded(&tile_full[rs], rph, p.status, abort_flag, p.wait_ns);
       const int t = gt ? tile_ring[rs] : -1;
       __syncwarp();
       if (lane == 0) mbar_arrive(&tile_empty[rs]);
@@ -709,8 +711,8 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         rph ^= 1u;
       }
       if constexpr (EPI == kEpiDSwiGLU || C::STAGED) {
-        epilogue_bar<32 * C::EPI_WARPS>();  // uniform exit decision (see below)
-        if (*abort_flag) break;
+        // uniform exit decision (see below)
+        if (epilogue_bar_any<32 * C::EPI_WARPS>(*abort_flag != 0)) break;
       }
       if (t < 0) break;
       const TileInfo ti = gemm_decode_tile<BN, C::BKE>(p, t);
@@ -721,12 +723,11 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         row_f = p.tile_row_flat[(int64_t)ti.mt * 128 + m];
         if (row_f >= 0) row_s = p.s[row_f];
       }
-      const bool got = mbar_wait_bounded(&tfull[acc], aph, p.status, abort_flag);
+      const bool got = mbar_wait_bounded(&tfull[acc], aph, p.status, abort_flag, p.wait_ns);
       if constexpr (EPI == kEpiDSwiGLU || C::STAGED) {
-        // these epilogues synchronise their four warps with a named barrier: take every exit
-        // decision after a barrier, from the shared abort flag, so no warp is left waiting
-        epilogue_bar<32 * C::EPI_WARPS>();
-        if (*abort_flag) break;
+        // these epilogues synchronise their warps with named barriers: every exit decision is the
+        // OR of the shared abort flag over all of them, taken at a barrier, so no warp is left waiting
+        if (epilogue_bar_any<32 * C::EPI_WARPS>(*abort_flag != 0)) break;
       } else if (!got) {
         break;
       }
@@ -865,7 +866,8 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
           const int buf = (int)(ck_next & 1);
           // on a failed wait the chunk is still walked (garbage in, flagged by the status word) so
           // that both warps of a pair reach the same barriers
-          mbar_wait_bounded(&ck_full[buf], (uint32_t)((ck_next >> 1) & 1), p.status, abort_flag);
+          const bool ck_ok =
+              mbar_wait_bounded(&ck_full[buf], (uint32_t)((ck_next >> 1) & 1), p.status, abort_flag, p.wait_ns);
           {
             const uint32_t ta = taddr + c * 32 + half * C::G1_NC;
             const int i0 = ti.nt * BN + c * 32;
@@ -892,7 +894,9 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
             }
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&ck_empty[buf]);  // this warp no longer reads the buffer
+          // this warp no longer reads the buffer; a chunk whose copy was not seen to land is never
+          // released, so the loader cannot refill a buffer while a copy into it is still in flight
+          if (lane == 0 && ck_ok) mbar_arrive(&ck_empty[buf]);
           ++ck_next;
         }
         p.ds_part[prow * (int64_t)(kG1Subs * (p.I / BN)) + kG1Subs * ti.nt + half] = valid ? ds_acc : 0.f;

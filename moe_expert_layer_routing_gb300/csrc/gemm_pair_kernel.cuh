@@ -123,16 +123,16 @@ __device__ __forceinline__ PairTile pair_decode(const GemmParams& p, int t, int 
 // and both CTAs' abort flags are raised.
 template <bool CLUSTER_ACQUIRE = false>
 __device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort_flag,
-                                          uint32_t peer_abort) {
+                                          uint32_t peer_abort, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   auto poll = [&]() { return CLUSTER_ACQUIRE ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
   if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (poll()) return true;
-    if ((it & 255u) == 0) {
+    if ((it & 15u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         if (status) atomicOr(status, MOE_STATUS_TIMEOUT);
         *abort_flag = 1;
         st_shared_cluster_u32(peer_abort, 1u);
@@ -222,13 +222,13 @@ __global__ void __launch_bounds__(PairCfg<MX, BN, EPI>::THREADS, 1)
         if (leader) {
           t = atomicAdd(p.tile_counter, 1);
           if (t >= total) t = -1;
-          if (!pair_wait(&tile_empty[rs], rph ^ 1u, p.status, abort_flag, peer_abort)) break;
+          if (!pair_wait(&tile_empty[rs], rph ^ 1u, p.status, abort_flag, peer_abort, p.wait_ns)) break;
           tile_ring[rs] = t;
           st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(&tile_ring[rs])), peer), (uint32_t)t);
           mbar_arrive(&tile_full[rs]);
           mbar_arrive_cluster(mapa_shared(smem_u32(&tile_full[rs]), peer));
         } else {
-          if (!pair_wait<true>(&tile_full[rs], rph, p.status, abort_flag, peer_abort)) break;
+          if (!pair_wait<true>(&tile_full[rs], rph, p.status, abort_flag, peer_abort, p.wait_ns)) break;
           t = tile_ring[rs];
           mbar_arrive_cluster(mapa_shared(smem_u32(&tile_empty[rs]), 0));
         }
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(PairCfg<MX, BN, EPI>::THREADS, 1)
         const PairTile ti = pair_decode<BN, C::BKE>(p, t, (int)rank);
         bool ok = true;
         for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!pair_wait(&empty[s], ph ^ 1u, p.status, abort_flag, peer_abort)) {
+          if (!pair_wait(&empty[s], ph ^ 1u, p.status, abort_flag, peer_abort, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(PairCfg<MX, BN, EPI>::THREADS, 1)
       int rs = 0;
       uint32_t rph = 0;
       while (ok) {
-        if (!pair_wait<true>(&tile_full[rs], rph, p.status, abort_flag, peer_abort)) break;
+        if (!pair_wait<true>(&tile_full[rs], rph, p.status, abort_flag, peer_abort, p.wait_ns)) break;
         const int t = tile_ring[rs];
         mbar_arrive(&tile_empty[rs]);
         if (++rs == C::RING) {
@@ -293,11 +293,11 @@ __global__ void __launch_bounds__(PairCfg<MX, BN, EPI>::THREADS, 1)
         }
         if (t < 0) break;
         const PairTile ti = pair_decode<BN, C::BKE>(p, t, 0);
-        if (!pair_wait(&tempty[acc], aph ^ 1u, p.status, abort_flag, peer_abort)) break;
+        if (!pair_wait(&tempty[acc], aph ^ 1u, p.status, abort_flag, peer_abort, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * C::BN);
         for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!pair_wait(&full[s], ph, p.status, abort_flag, peer_abort)) {
+          if (!pair_wait(&full[s], ph, p.status, abort_flag, peer_abort, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(PairCfg<MX, BN, EPI>::THREADS, 1)
     int rs = 0;
     uint32_t rph = 0;
     for (;;) {
-      const bool gt = pair_wait<true>(&tile_full[rs], rph, p.status, abort_flag, peer_abort);
+      const bool gt = pair_wait<true>(&tile_full[rs], rph, p.status, abort_flag, peer_abort, p.wait_ns);
       const int t = gt ? tile_ring[rs] : -1;
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(lead_tile_empty + (uint32_t)(rs * 8));
@@ -366,13 +366,12 @@ __global__ void __launch_bounds__(PairCfg<MX, BN, EPI>::THREADS, 1)
         rs = 0;
         rph ^= 1u;
       }
-      epilogue_bar<32 * C::EPI_WARPS>();  // exit decisions are taken together, after a barrier
-      if (*abort_flag) break;
+      // exit decisions are taken together: the OR of the abort flag over the epilogue warps at a barrier
+      if (epilogue_bar_any<32 * C::EPI_WARPS>(*abort_flag != 0)) break;
       if (t < 0) break;
       const PairTile ti = pair_decode<BN, C::BKE>(p, t, (int)rank);
-      pair_wait(&tfull[acc], aph, p.status, abort_flag, peer_abort);
-      epilogue_bar<32 * C::EPI_WARPS>();
-      if (*abort_flag) break;
+      pair_wait(&tfull[acc], aph, p.status, abort_flag, peer_abort, p.wait_ns);
+      if (epilogue_bar_any<32 * C::EPI_WARPS>(*abort_flag != 0)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * C::BN);
       // this CTA's 128 x 256 accumulator -> registers (bf16), then release it to the leader

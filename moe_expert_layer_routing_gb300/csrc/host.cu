@@ -41,6 +41,41 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 static std::atomic<uint64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+// Library options (moe_set_option): process-wide, read by every later call.
+static std::atomic<int64_t> g_opt[MOE_NUM_OPTIONS];
+static const int64_t kOptDefault[MOE_NUM_OPTIONS] = {
+    (int64_t)kWaitLimitNs,  // MOE_OPT_WAIT_LIMIT_NS
+    1,                      // MOE_OPT_PAIR_GEMMS
+    256,                    // MOE_OPT_PAIR_TILE_N
+    0, 0, 0, 0,             // MOE_OPT_G1_TILE_N .. MOE_OPT_G4_TILE_N (automatic)
+    1,                      // MOE_OPT_PREP_TILE_ORDER
+};
+static std::once_flag g_opt_once;
+static void opt_init() {
+  std::call_once(g_opt_once, [] {
+    for (int i = 0; i < MOE_NUM_OPTIONS; ++i) g_opt[i].store(kOptDefault[i]);
+  });
+}
+
+int64_t option(int o) {
+  opt_init();
+  return g_opt[o].load(std::memory_order_relaxed);
+}
+
+static bool option_value_ok(int o, int64_t v) {
+  switch (o) {
+    case MOE_OPT_WAIT_LIMIT_NS: return v >= 1 && v <= 60000000000ll;
+    case MOE_OPT_PAIR_GEMMS: return v >= 0 && v <= 2;
+    case MOE_OPT_PAIR_TILE_N: return v == 128 || v == 256;
+    case MOE_OPT_G1_TILE_N: return v == 0 || v == 128 || v == 192 || v == 256;
+    case MOE_OPT_G2_TILE_N:
+    case MOE_OPT_G3_TILE_N:
+    case MOE_OPT_G4_TILE_N: return v == 0 || v == 128 || v == 256;
+    case MOE_OPT_PREP_TILE_ORDER: return v == 0 || v == 1;
+    default: return false;
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -91,3 +126,19 @@ bool make_tmap_2d(void* out_tmap, const void* base, int elem_bytes, uint64_t row
 extern "C" const char* moe_last_error(void) { return moebwd::g_err; }
 extern "C" uint64_t moe_kernel_launches(void) { return moebwd::g_launches.load(); }
 extern "C" const char* moe_version(void) { return "moebwd 0.1 (sm_103a tcgen05)"; }
+
+extern "C" int moe_set_option(int opt, int64_t value) {
+  moebwd::clear_error();
+  if (opt < 0 || opt >= MOE_NUM_OPTIONS) return moebwd::fail(MOE_ERR_INVALID, "moe_set_option: unknown option %d", opt);
+  if (value == -1) value = moebwd::kOptDefault[opt];
+  if (!moebwd::option_value_ok(opt, value))
+    return moebwd::fail(MOE_ERR_INVALID, "moe_set_option: value %lld not allowed for option %d", (long long)value, opt);
+  moebwd::opt_init();
+  moebwd::g_opt[opt].store(value);
+  return MOE_OK;
+}
+
+extern "C" int64_t moe_get_option(int opt) {
+  if (opt < 0 || opt >= MOE_NUM_OPTIONS) return -1;
+  return moebwd::option(opt);
+}

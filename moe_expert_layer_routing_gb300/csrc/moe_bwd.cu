@@ -20,26 +20,24 @@ namespace moebwd {
 // CTA-pair GEMMs replace the single-CTA kernel for BF16 where they apply: a store or checkpoint
 // epilogue, N a multiple of 256, and M-grouped schedules that know their expert pairs (or have one
 // expert) / K-grouped M a multiple of 256.  For MXFP8 the single-CTA kernel is kept (its pair tile
-// has a single TMEM accumulator and measured slower).  MOEBWD_PAIR=0 disables pairs, MOEBWD_PAIR=2
-// also uses them for MXFP8 (comparisons and tests).
+// has a single TMEM accumulator and measured slower).  MOE_OPT_PAIR_GEMMS = 0 disables pairs, 2 also
+// uses them for MXFP8.
 static bool use_pair(bool mx, int BN, const GemmParams& p) {
-  const char* v = getenv("MOEBWD_PAIR");
-  const int mode = v ? atoi(v) : 1;
+  const int64_t mode = option(MOE_OPT_PAIR_GEMMS);
   if (mode == 0 || (mx && mode != 2)) return false;
   if (BN != 256 || (p.epi != kEpiStore && p.epi != kEpiCkpt)) return false;
   if (p.mode == kMGrouped) return p.pair_offsets != nullptr || p.tile_expert == nullptr;
   return p.m_tiles % 2 == 0;
 }
 
-// Width of the pair tile: 256 (MOEBWD_PAIR_BN=128 selects the narrow tile, for tuning runs).
-static int pair_bn() {
-  const char* v = getenv("MOEBWD_PAIR_BN");
-  if (v && atoi(v) == 128) return 128;
-  return 256;
-}
+// Width of the pair tile: 256, or 128 (MOE_OPT_PAIR_TILE_N).
+static int pair_bn() { return option(MOE_OPT_PAIR_TILE_N) == 128 ? 128 : 256; }
 
-int launch_gemm(bool mx, int BN, const GemmParams& p, const void* A, int64_t a_rows, int64_t a_cols, const void* B,
-                int64_t b_rows, int64_t b_cols, cudaStream_t st, const void* ckpt, int64_t ck_rows, int64_t ck_cols) {
+int launch_gemm(bool mx, int BN, const GemmParams& p_in, const void* A, int64_t a_rows, int64_t a_cols,
+                const void* B, int64_t b_rows, int64_t b_cols, cudaStream_t st, const void* ckpt, int64_t ck_rows,
+                int64_t ck_cols) {
+  GemmParams p = p_in;
+  p.wait_ns = (uint64_t)option(MOE_OPT_WAIT_LIMIT_NS);
   alignas(64) CUtensorMap ta, tb, tc, tsa, tsb;
   const int es = mx ? 1 : 2;
   const uint32_t bke = mx ? 128 : 64;
@@ -118,12 +116,10 @@ static int64_t blocks_bound(int64_t T, int K, int E, int B) {
   return (num + B - 1) / B + E - 1;
 }
 
-// Tile-width override for tuning runs: the variable, if set to 128 or 256 (or 192 where allowed)
-// dividing n, wins.
-static int bn_override(const char* name, int dflt, int64_t n, bool allow192 = false) {
-  const char* v = getenv(name);
-  if (!v) return dflt;
-  const int bn = atoi(v);
+// Tile width chosen by an option (MOE_OPT_G*_TILE_N): a nonzero value that divides n (192 only
+// where allowed) replaces the default.
+static int bn_option(int opt, int dflt, int64_t n, bool allow192 = false) {
+  const int bn = (int)option(opt);
   return (bn == 128 || bn == 256 || (allow192 && bn == 192)) && n % bn == 0 ? bn : dflt;
 }
 
@@ -142,10 +138,10 @@ static Layout make_layout(const MoeBwdArgs& a) {
   L.BN2 = a.H % 256 == 0 ? 256 : 128;
   L.BN3 = L.BN2;
   L.BN4 = 256;
-  L.BN1 = bn_override("MOEBWD_BN_G1", L.BN1, a.I, mx);
-  L.BN2 = bn_override("MOEBWD_BN_G2", L.BN2, a.H);
-  L.BN3 = bn_override("MOEBWD_BN_G3", L.BN3, a.H);
-  L.BN4 = bn_override("MOEBWD_BN_G4", L.BN4, 2 * a.I);
+  L.BN1 = bn_option(MOE_OPT_G1_TILE_N, L.BN1, a.I, mx);
+  L.BN2 = bn_option(MOE_OPT_G2_TILE_N, L.BN2, a.H);
+  L.BN3 = bn_option(MOE_OPT_G3_TILE_N, L.BN3, a.H);
+  L.BN4 = bn_option(MOE_OPT_G4_TILE_N, L.BN4, 2 * a.I);
   const int64_t P = L.P, H = a.H, I = a.I, E = a.E;
   size_t b[R_COUNT] = {};
   b[R_CHUNK_COUNTS] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, route_nchunks(L.TK)) * E;
@@ -457,7 +453,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   pa.tile_row_flat = tile_row_flat;
   pa.tile_expert = tile_expert;
   pa.num_tiles = scalars + 1;
-  pa.tile_order = getenv("MOEBWD_PREP_ORDER") && getenv("MOEBWD_PREP_ORDER")[0] == '0' ? nullptr : tile_order;
+  pa.tile_order = option(MOE_OPT_PREP_TILE_ORDER) ? tile_order : nullptr;
   pa.H = a.H;
   pa.K = a.K;
   pa.P = P;

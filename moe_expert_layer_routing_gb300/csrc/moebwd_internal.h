@@ -8,7 +8,8 @@
 
 namespace moebwd {
 
-// Upper limit of any single pipeline wait inside a kernel before it reports MOE_STATUS_TIMEOUT.
+// Default limit of a pipeline wait inside a GEMM kernel before it reports MOE_STATUS_TIMEOUT
+// (MOE_OPT_WAIT_LIMIT_NS changes it); the drain waits before a CTA exits always keep this one.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 constexpr int kTileM = 128;       // rows of a GEMM tile = UMMA M = tile-row padding granule
@@ -24,6 +25,7 @@ int cuda_check(cudaError_t e, const char* what);
 int device_sm_count();
 size_t align_up(size_t v, size_t a);
 void count_launch();   // one kernel launched by this library
+int64_t option(int opt);  // current value of a MOE_OPT_* option
 
 // 2D tensor map over a row-major [rows, cols] matrix of `elem_bytes`-byte elements with the given
 // row pitch, box [box_rows, box_cols], 128-byte swizzle (or none).  Returns false on failure (message set).
@@ -168,6 +170,7 @@ struct GemmParams {
   int32_t* tile_counter;        // zeroed before the launch: dynamic tile claims
   int accumulate;               // store epilogue: add the tile to the output instead of overwriting
   int32_t* status;
+  uint64_t wait_ns;             // limit of each pipeline wait (set by launch_gemm from MOE_OPT_WAIT_LIMIT_NS)
 };
 
 // A [rows, K] and B [rows, K] K-major operands (bf16 or fp8 bytes), tile counts in p.

@@ -55,19 +55,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, for at most kWaitLimitNs.  On timeout the
-// device status word gets MOE_STATUS_TIMEOUT, *abort is raised and false is returned.  A raised
-// *abort (another role gave up) also ends the wait with false.
+// Wait for the phase with the given parity to complete, for at most limit_ns (the pipeline-wait limit
+// of the launch, GemmParams::wait_ns).  On timeout the device status word gets MOE_STATUS_TIMEOUT,
+// *abort is raised and false is returned.  A raised *abort (another role gave up) also ends the wait
+// with false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status,
-                                                  volatile int* abort_flag) {
+                                                  volatile int* abort_flag, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((it & 255u) == 0) {
+    if ((it & 15u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         if (status) atomicOr(status, MOE_STATUS_TIMEOUT);
         *abort_flag = 1;
         return false;
@@ -351,6 +352,23 @@ __device__ __forceinline__ void tmem_cp_pair_32x128b_warpx4(uint32_t taddr, uint
 // Named barriers: id 1 over the epilogue warps, ids 2.. over pairs of warps (64 threads).
 template <int NTHREADS>
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory"); }
+// Barrier 1 over the epilogue warps that also returns the OR of `pred` over all of them, the same
+// value in every thread.  Exit decisions taken from a flag that another role may raise at any moment
+// go through it: each thread reads the flag before the barrier, so no two warps can read it on
+// different sides of the moment it was raised (one leaving, one waiting at the next barrier).
+template <int NTHREADS>
+__device__ __forceinline__ bool epilogue_bar_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(NTHREADS)
+      : "memory");
+  return r != 0;
+}
 __device__ __forceinline__ void pair_bar(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -21,3 +21,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture
+def set_option():
+    """Set library options (moe_set_option) for one test; their old values come back afterwards."""
+    import moe_expert_layer_routing_gb300 as mb
+    saved = {}
+
+    def _set(name, value):
+        if name not in saved:
+            saved[name] = mb.get_option(name)
+        mb.set_option(name, value)
+
+    yield _set
+    for name, value in saved.items():
+        mb.set_option(name, value)

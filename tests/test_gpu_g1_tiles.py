@@ -1,6 +1,6 @@
 """GPU parity of the dSwiGLU GEMM (dA = dout_g W2_e^T with its epilogue) at both of its MXFP8 tile
 widths: 192 columns (the default where I is a multiple of 192; W2's scales re-tiled into two atoms
-per tile) and 128 (MOEBWD_BN_G1=128), against the oracle on the same inputs, over ragged expert
+per tile) and 128 (library option G1_TILE_N = 128), against the oracle on the same inputs, over ragged expert
 loads, both activation formats, both affinity modes and the GeGLU / interleaved variant; and the two
 widths agree on the quantised dh operand."""
 import numpy as np
@@ -26,11 +26,11 @@ def _ragged_ids(T, K, E, seed):
     return torch.from_numpy(ids.astype(np.int32))
 
 
-@pytest.mark.parametrize("bn", ["192", "128"])
+@pytest.mark.parametrize("bn", [192, 128])
 @pytest.mark.parametrize("I", [384, 768])
 @pytest.mark.parametrize("fmt_act,aff", [(FP8_E5M2, AFFINITY_ON_I), (FP8_E4M3, AFFINITY_ON_H)])
-def test_mxfp8_g1_tile_widths(monkeypatch, bn, I, fmt_act, aff):
-    monkeypatch.setenv("MOEBWD_BN_G1", bn)
+def test_mxfp8_g1_tile_widths(set_option, bn, I, fmt_act, aff):
+    set_option("G1_TILE_N", bn)
     cfg = small_moe("g1w", T=520, H=256, I=I, E=6, K=2, B=256, seed=91, precision=PREC_MXFP8, affinity=aff,
                     fp8_act=fmt_act)
     inp = with_ids(make_moe_inputs(cfg), _ragged_ids(520, 2, 6, seed=11))
@@ -39,10 +39,10 @@ def test_mxfp8_g1_tile_widths(monkeypatch, bn, I, fmt_act, aff):
     compare_outputs(got, oracle_bwd(inp), MXFP8_TOL)
 
 
-def test_mxfp8_g1_variant_at_192(monkeypatch):
+def test_mxfp8_g1_variant_at_192(set_option):
     """GeGLU with the interleaved gate/up layout through the 192-column tiles."""
     import moe_expert_layer_routing_gb300 as mb
-    monkeypatch.setenv("MOEBWD_BN_G1", "192")
+    set_option("G1_TILE_N", 192)
     cfg = small_moe("g1v", T=400, H=256, I=384, E=5, K=2, B=128, seed=92, precision=PREC_MXFP8,
                     affinity=AFFINITY_ON_I)
     inp = with_ids(make_moe_inputs(cfg), _ragged_ids(400, 2, 5, seed=12))
@@ -63,7 +63,7 @@ def test_mxfp8_g1_variant_at_192(monkeypatch):
     compare_outputs(got, ref, MXFP8_TOL)
 
 
-def test_g1_widths_agree_on_dh(monkeypatch):
+def test_g1_widths_agree_on_dh(set_option):
     """The quantised dh of the two tile widths: each output element's contraction is the same, so the
     codes and scales agree except where fp32 accumulation order moves a value across a rounding
     boundary (none expected; at most a handful allowed)."""
@@ -71,14 +71,14 @@ def test_g1_widths_agree_on_dh(monkeypatch):
                     affinity=AFFINITY_ON_I)
     inp = make_moe_inputs(cfg)
     outs = {}
-    for bn in ("192", "128"):
-        monkeypatch.setenv("MOEBWD_BN_G1", bn)
+    for bn in (192, 128):
+        set_option("G1_TILE_N", bn)
         op, got = run_gpu(inp)
         assert int(got["status"].item()) == 0
         used = int(op.region("TILE_OFFSETS").view(torch.int32)[cfg.E].item())
         dh = op.region("DH").cpu().numpy().reshape(op.tile_rows, 2 * cfg.I)[:used]
         outs[bn] = (dh.copy(), got["ds"].double().cpu().numpy())
-    diff = np.count_nonzero(outs["192"][0] != outs["128"][0])
-    assert diff <= outs["128"][0].size * 1e-4, diff
-    ds192, ds128 = outs["192"][1], outs["128"][1]   # partial sums per tile width: summation order differs
+    diff = np.count_nonzero(outs[192][0] != outs[128][0])
+    assert diff <= outs[128][0].size * 1e-4, diff
+    ds192, ds128 = outs[192][1], outs[128][1]   # partial sums per tile width: summation order differs
     np.testing.assert_allclose(ds192, ds128, rtol=1e-4, atol=1e-5 * np.abs(ds128).max())

@@ -28,11 +28,11 @@ def _ids(T, K, E, seed):
     return torch.from_numpy(ids.astype(np.int32))
 
 
-# MOEBWD_PAIR: "2" pairs for both precisions (the MXFP8 default is the single-CTA kernel), "0" none
-@pytest.mark.parametrize("pair", ["2", "0"])
+# PAIR_GEMMS: 2 pairs for both precisions (the MXFP8 default is the single-CTA kernel), 0 none
+@pytest.mark.parametrize("pair", [2, 0])
 @pytest.mark.parametrize("prec,aff", [(PREC_BF16, AFFINITY_ON_H), (PREC_MXFP8, AFFINITY_ON_I)])
-def test_moe_bwd_pair_and_single_cta(pair, prec, aff, monkeypatch):
-    monkeypatch.setenv("MOEBWD_PAIR", pair)
+def test_moe_bwd_pair_and_single_cta(pair, prec, aff, set_option):
+    set_option("PAIR_GEMMS", pair)
     cfg = small_moe("pair", T=700, H=512, I=256, E=6, K=2, B=256, seed=51, precision=prec, affinity=aff)
     inp = with_ids(make_moe_inputs(cfg), _ids(700, 2, 6, seed=9))
     counts = np.bincount(inp.ids.numpy().reshape(-1), minlength=6)
@@ -43,10 +43,10 @@ def test_moe_bwd_pair_and_single_cta(pair, prec, aff, monkeypatch):
     compare_outputs(got, oracle_bwd(inp), MXFP8_TOL if prec == PREC_MXFP8 else BF16_TOL)
 
 
-@pytest.mark.parametrize("pair", ["2", "0"])
-def test_linear_bwd_odd_tiles_pair_and_single_cta(pair, monkeypatch):
+@pytest.mark.parametrize("pair", [2, 0])
+def test_linear_bwd_odd_tiles_pair_and_single_cta(pair, set_option):
     import moe_expert_layer_routing_gb300 as mb
-    monkeypatch.setenv("MOEBWD_PAIR", pair)
+    set_option("PAIR_GEMMS", pair)
     inp = make_linear_inputs(LinearConfig("lin_odd", M=384, N=512, K=768, seed=52))
     for prec, tol, fn in ((mb.PREC_MXFP8, MXFP8_TOL, olin.linear_backward_mxfp8),
                           (mb.PREC_BF16, BF16_TOL, olin.linear_backward)):
@@ -57,21 +57,17 @@ def test_linear_bwd_odd_tiles_pair_and_single_cta(pair, monkeypatch):
         assert rel_fro(np64(got["dW"]), ref["dW"]) < tol
 
 
-@pytest.mark.parametrize("bn", ["256", "128"])
-def test_pair_and_single_cta_give_the_same_gradients_to_rounding(bn, monkeypatch):
+@pytest.mark.parametrize("bn", [256, 128])
+def test_pair_and_single_cta_give_the_same_gradients_to_rounding(bn, set_option):
     """The two GEMM paths differ only in the order of the fp32 sums: their bf16 outputs agree to a
     few bf16 ulps relative to the gradient's size."""
-    import os
-    monkeypatch.setenv("MOEBWD_PAIR_BN", bn)
+    set_option("PAIR_TILE_N", bn)
     cfg = small_moe("pair_eq", T=512, H=512, I=256, E=4, K=2, B=128, seed=53, precision=PREC_MXFP8)
     inp = make_moe_inputs(cfg)
     outs = []
-    for pair in ("2", "0"):
-        os.environ["MOEBWD_PAIR"] = pair
-        try:
-            _, got = run_gpu(inp)
-        finally:
-            os.environ.pop("MOEBWD_PAIR", None)
+    for pair in (2, 0):
+        set_option("PAIR_GEMMS", pair)
+        _, got = run_gpu(inp)
         outs.append({k: np64(v) for k, v in got.items() if v is not None and k != "status"})
     for n in ("dx", "dW1", "dW2", "ds"):
         a, b = outs[0][n], outs[1][n]

@@ -102,10 +102,10 @@ def test_recompute_bf16_no_bias_single_expert():
     _check(make_moe_inputs(cfg), PREC_BF16, has_bias=False, use_b1=False, tol=BF16_TOL)
 
 
-@pytest.mark.parametrize("B,pair", [(128, "1"), (512, "1"), (512, "2")])
-def test_recompute_mxfp8_with_gate_up_bias(B, pair, monkeypatch):
-    # MOEBWD_PAIR=2 runs the recomputation GEMM on CTA pairs (the MXFP8 default is one CTA per tile)
-    monkeypatch.setenv("MOEBWD_PAIR", pair)
+@pytest.mark.parametrize("B,pair", [(128, 1), (512, 1), (512, 2)])
+def test_recompute_mxfp8_with_gate_up_bias(B, pair, set_option):
+    # PAIR_GEMMS = 2 runs the recomputation GEMM on CTA pairs (the MXFP8 default is one CTA per tile)
+    set_option("PAIR_GEMMS", pair)
     # b1 enters the recomputation only (bias gradients are BF16-only); inputs drawn with biases
     cfg = small_moe("rec_mx", T=320, H=512, I=256, E=6, K=2, B=B, seed=43, bias=True, precision=PREC_MXFP8,
                     affinity=AFFINITY_ON_I)

@@ -103,3 +103,26 @@ def test_route_meta_workspace_size_is_zero_for_rejected_sizes(lib):
     for B in (0, -128, 100):
         assert lib.moe_route_meta_workspace_size(1000, 2, 8, B) == 0
     assert lib.moe_route_meta_workspace_size(1000, 2, 2048, 128) == 0
+
+
+def test_options_defaults_and_validation(lib):
+    import moe_expert_layer_routing_gb300 as mb
+    assert mb.get_option("WAIT_LIMIT_NS") == 2_000_000_000
+    assert mb.get_option("PAIR_GEMMS") == 1 and mb.get_option("PAIR_TILE_N") == 256
+    assert mb.get_option("G1_TILE_N") == 0 and mb.get_option("PREP_TILE_ORDER") == 1
+    assert lib.moe_set_option(99, 1) == -1 and b"unknown option" in lib.moe_last_error()
+    assert lib.moe_get_option(99) == -1
+    for name, bad in (("WAIT_LIMIT_NS", 0), ("PAIR_GEMMS", 3), ("PAIR_TILE_N", 192), ("G1_TILE_N", 64),
+                      ("G2_TILE_N", 192), ("PREP_TILE_ORDER", 2)):
+        assert lib.moe_set_option(mb.OPTIONS.index(name), bad) == -1
+        assert b"not allowed" in lib.moe_last_error()
+    with mb.option("G1_TILE_N", 192):
+        assert mb.get_option("G1_TILE_N") == 192
+        a = mb.MoeBwdArgs(T=256, H=256, I=384, E=4, K=2, block_size=128, precision=1)
+        n192 = lib.moe_bwd_workspace_size(ctypes.byref(a))
+    assert mb.get_option("G1_TILE_N") == 0
+    mb.set_option("G1_TILE_N", 128)
+    n128 = lib.moe_bwd_workspace_size(ctypes.byref(a))
+    mb.set_option("G1_TILE_N", None)
+    assert mb.get_option("G1_TILE_N") == 0
+    assert n192 > 0 and n128 > 0 and n192 != n128   # the tile width moves the ds partials' region
