@@ -319,10 +319,11 @@ def moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, affinity=1, fp8_act=mx.E5M2, 
         dh[:, gc] = dA * up * dact(gate)
         dh[:, uc] = dA * ag
         dh = _to_f32(dh)
-        dx_exp = _to_bf16(quant(dh, fp8_act, 1) @ W1q.T)
         tm = token_mask[t]
         ds[t[tm], k[tm]] = dsv[tm]
-        np.add.at(dx, t[tm], dx_exp[tm])
+        if tm.any():   # dx_expanded only for rows whose token is wanted
+            dx_exp = _to_bf16(quant(dh[tm], fp8_act, 1) @ W1q.T)
+            np.add.at(dx, t[tm], dx_exp)
         if need_w:
             av = _to_f32(sr * a if affinity == 1 else a) if inter is None else _f64(inter)[t, k]
             if affinity == 1:

@@ -112,3 +112,45 @@ def mx_roundtrip(v: np.ndarray, fmt: int, axis: int = -1) -> np.ndarray:
     """dequantize(quantize(v)) along `axis`: the value an MXFP8 GEMM operand carries."""
     q, s = mx_quantize(v, fmt, axis)
     return mx_dequantize(q, s, fmt, axis)
+
+
+def mx_roundtrip_torch(v: np.ndarray, fmt: int, axis: int = -1) -> np.ndarray:
+    """mx_roundtrip of a 2-D array of float32 numbers with torch's CPU float8 cast as the element
+    rounding, for operands of a quarter of a billion elements (the full-size parity tests), where the
+    table search above takes minutes.
+
+    The same rule, step by step: the group amax (a tree of pairwise maxima), the scale byte from its
+    binary exponent, the scaled value (a division by a power of two, exact in float32 wherever the
+    result can round to a nonzero code) clamped to +-max finite, then round-to-nearest-even into the
+    format by the cast, which keeps the sign of zero; the dequantised value (an FP8 value times a power
+    of two) is exact in float32 for float32 inputs.  The oracle quantises only float32 numbers (bf16
+    inputs, intermediates rounded to float32 first); other inputs raise.  Pinned equal to
+    mx_roundtrip (tests/test_oracle_mxfp8.py)."""
+    import torch
+    a = np.asarray(v, dtype=np.float64)
+    assert a.ndim == 2 and axis in (0, 1, -1), "2-D operands, groups along one of the two axes"
+    t64 = torch.from_numpy(np.ascontiguousarray(a))
+    t = t64.to(torch.float32)
+    if not torch.equal(t.to(torch.float64), t64):
+        raise ValueError("mx_roundtrip_torch quantises float32 numbers only")
+    R, C = t.shape
+    if axis == 0:
+        assert R % 32 == 0, "group axis must be a multiple of 32"
+        g = t.view(R // 32, 32, C)        # group index, element of the group, column
+        gdim = 1
+    else:
+        assert C % 32 == 0, "group axis must be a multiple of 32"
+        g = t.view(R, C // 32, 32)
+        gdim = 2
+    m = g.abs()
+    width = 32
+    while width > 1:                     # amax of each group by halving
+        width //= 2
+        m = torch.maximum(m.narrow(gdim, 0, width), m.narrow(gdim, width, width))
+    amax = m.squeeze(gdim)
+    byte = e8m0_byte(amax.to(torch.float64).numpy(), fmt).astype(np.int64)
+    scale = torch.from_numpy(np.ldexp(1.0, byte - 127)).to(torch.float32).unsqueeze(gdim)
+    maxv = fp8_max(fmt)
+    dt = torch.float8_e4m3fn if fmt == E4M3 else torch.float8_e5m2
+    y = (g / scale).clamp_(-maxv, maxv).to(dt).to(torch.float32) * scale
+    return y.reshape(R, C).to(torch.float64).numpy()

@@ -414,3 +414,48 @@ def test_saved_gate_act_enters_only_through_the_activation_value(activation, gat
     mg = om.moe_backward_mxfp8(x, dout, W1, W2, s, ids, h, activation=activation, gate_up=gate_up, gate_act=act)
     for name in ("dx", "dW1", "dW2", "ds"):
         assert np.array_equal(mq[name], mg[name]), name
+
+
+@pytest.mark.parametrize("mxfp8", [False, True])
+def test_feature_slice_reproduces_full_weight_gradients(mxfp8):
+    """oracle.sample features mode: one expert with all its rows and a range of 32 intermediate
+    features gives that expert's dW1 columns (gate and up) and dW2 rows of those features, and its
+    db1 columns and db2, as the full problem does; the MXFP8 problem is run with the torch-cast round
+    trip the full-size tests use, which must give the same values as the default one."""
+    from oracle import mxfp8 as mxq
+    from oracle import route_meta as orm
+    from oracle import sample as osm
+    rng = np.random.default_rng(23)
+    T, H, I, E, K, B = 200, 64, 96, 4, 2, 128
+    x = torch.from_numpy(rng.standard_normal((T, H))).to(torch.bfloat16)
+    dout = torch.from_numpy(rng.standard_normal((T, H))).to(torch.bfloat16)
+    W1 = torch.from_numpy(rng.standard_normal((E, H, 2 * I)) * 0.1).to(torch.bfloat16)
+    W2 = torch.from_numpy(rng.standard_normal((E, I, H)) * 0.1).to(torch.bfloat16)
+    b2 = torch.from_numpy(rng.standard_normal((E, H)) * 0.01).to(torch.bfloat16)
+    ids = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    ids[:150, 0] = 2                                   # expert 2 hot: several 32-row token groups
+    ids[:150, 1] = np.where(ids[:150, 1] == 2, 0, ids[:150, 1])
+    s = rng.random((T, K))
+    N = orm.num_blocks_bound(T, K, E, B)
+    ckpt = torch.from_numpy(rng.standard_normal((N, 2, I, B))).to(torch.bfloat16)
+    meta = orm.route_meta(ids, E, B)
+    h = orm.checkpoint_rows(ckpt.double().numpy(), meta, T, K)
+    if mxfp8:
+        full = om.moe_backward_mxfp8(x, dout, W1, W2, s, ids, h)
+    else:
+        full = om.moe_backward(x, dout, W1, W2, s, ids, h, b2=b2, with_bias=True)
+    for e in (2, 1):
+        sub = osm.subproblem(x, dout, W1, W2, s, ids, ckpt, B, experts=[e], features=(32, 32), b2=b2)
+        cols = sub["columns"]
+        assert list(cols[:32]) == list(range(32, 64)) and list(cols[32:]) == list(range(I + 32, I + 64))
+        if mxfp8:
+            g = om.moe_backward_mxfp8(sub["x"], sub["dout"], sub["W1"], sub["W2"], sub["s"], sub["ids"], sub["h"],
+                                      tokens=[], quant=mxq.mx_roundtrip_torch)
+        else:
+            g = om.moe_backward(sub["x"], sub["dout"], sub["W1"], sub["W2"], sub["s"], sub["ids"], sub["h"],
+                                b2=sub["b2"], with_bias=True)
+            assert np.allclose(g["db1"][0], full["db1"][e][cols], rtol=1e-12, atol=1e-12)
+            assert np.allclose(g["db2"][0], full["db2"][e], rtol=1e-12, atol=1e-12)
+        assert np.allclose(g["dW1"][0], full["dW1"][e][:, cols], rtol=1e-12, atol=1e-12)
+        assert np.allclose(g["dW2"][0], full["dW2"][e][32:64], rtol=1e-12, atol=1e-12)
+        assert not np.allclose(g["dW1"][0], full["dW1"][e][:, :64])   # the slice is not the leading one

@@ -121,3 +121,54 @@ def test_quantize_axis_and_padding_shapes():
     assert q.shape == (64, 3) and s.shape == (2, 3)
     with pytest.raises(AssertionError):
         mx.mx_quantize(np.ones((3, 33)), mx.E5M2, axis=1)
+
+
+def _same_values(a, b):
+    """Equal as numbers and in the sign of every zero."""
+    return np.array_equal(a, b) and np.array_equal(np.signbit(a), np.signbit(b))
+
+
+@pytest.mark.parametrize("fmt", [mx.E4M3, mx.E5M2])
+@pytest.mark.parametrize("axis", [0, 1])
+def test_torch_cast_roundtrip_equals_the_definition(fmt, axis):
+    """mx_roundtrip_torch (the fast form the full-size tests use) gives bit for bit what mx_roundtrip
+    gives: float32 values spread over 2^-140 .. 2^+100 within a group, zeros of both signs, groups of
+    a single huge or tiny value, ties of the element rounding."""
+    rng = np.random.default_rng(3)
+    shape = (256, 192)
+    mant = rng.standard_normal(shape)
+    expo = rng.integers(-140, 100, size=shape)
+    v = np.asarray(np.ldexp(mant, expo), dtype=np.float32).astype(np.float64)
+    v[rng.random(shape) < 0.05] = 0.0
+    v[rng.random(shape) < 0.05] = -0.0
+    v[:32, :32] = 0.0
+    v[0, 0] = float(np.float32(3.0e38)) if axis == 1 else v[0, 0]
+    # ties: values exactly halfway between two FP8 neighbours once scaled (group amax 2^emax)
+    emax = {mx.E4M3: 8, mx.E5M2: 15}[fmt]
+    mbits = {mx.E4M3: 3, mx.E5M2: 2}[fmt]
+    ties = (1.0 + (2 * np.arange(31) + 1) / 2.0 ** (mbits + 1)) * 2.0 ** (emax - 3)
+    if axis == 1:
+        v[40, :32] = np.concatenate([[2.0 ** emax], ties])
+        v[41, :32] = -v[40, :32]
+    else:
+        v[:32, 40] = np.concatenate([[2.0 ** emax], ties])
+        v[:32, 41] = -v[:32, 40]
+    assert _same_values(mx.mx_roundtrip_torch(v, fmt, axis), mx.mx_roundtrip(v, fmt, axis))
+
+
+@pytest.mark.parametrize("fmt", [mx.E4M3, mx.E5M2])
+def test_torch_cast_roundtrip_on_all_bf16_patterns(fmt):
+    """Every finite bf16 value, in groups of 32 consecutive patterns, through both round trips."""
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    v = bits.view(torch.bfloat16).to(torch.float64).numpy()
+    v = np.where(np.isfinite(v), v, 0.0).reshape(-1, 32)
+    for shift in (0, -20, 20):
+        w = np.ldexp(v, shift)
+        w = np.where(w.astype(np.float32).astype(np.float64) == w, w, 0.0)   # float32 numbers only
+        assert _same_values(mx.mx_roundtrip_torch(w, fmt, 1), mx.mx_roundtrip(w, fmt, 1)), shift
+        assert _same_values(mx.mx_roundtrip_torch(w.T.copy(), fmt, 0), mx.mx_roundtrip(w.T.copy(), fmt, 0)), shift
+
+
+def test_torch_cast_roundtrip_refuses_values_beyond_float32():
+    with pytest.raises(ValueError):
+        mx.mx_roundtrip_torch(np.full((1, 32), 1e300), mx.E5M2, 1)
