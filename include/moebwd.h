@@ -54,7 +54,9 @@ enum {
 /* Bits of the device status word. */
 enum {
   MOE_STATUS_BAD_EXPERT_ID = 1, /* some ids[t,k] outside [0,E); those rows are skipped */
-  MOE_STATUS_TIMEOUT = 2        /* a pipeline wait exceeded its time limit; outputs invalid */
+  MOE_STATUS_TIMEOUT = 2,       /* a pipeline wait exceeded its time limit; outputs invalid */
+  MOE_STATUS_BAD_ROUTE_META = 4 /* caller-supplied routing metadata is not a routing of the ids
+                                   (moe_bwd with expert_offsets given); outputs invalid */
 };
 
 enum { MOE_PREC_BF16 = 0, MOE_PREC_MXFP8 = 1 };
@@ -252,6 +254,26 @@ typedef struct MoeBwdArgs {
    * factor, dup = dA*act(gate)); act'(gate) in dgate still needs the pre-activation, so gate_up_ckpt
    * (or the recomputation) stays required.  16-byte aligned. */
   const void* gate_act_ckpt;
+  /* Routing metadata from the caller ([BW] token_position_to_id, block_to_expert, "Dimensions";
+   * [SM] expert_frequency_offset, s_scatter_idx), e.g. kept from the forward pass, in the layout
+   * moe_route_meta writes (all (device) int32).  All NULL: moe_bwd computes it from ids.  Given,
+   * expert_offsets, s_scatter_idx and block_offsets are required and moe_bwd takes from them which
+   * grouped row is which (token, slot), the rows of each expert in the given order (the MXFP8
+   * token-direction groups are 32 consecutive rows in that order), and where each row's checkpoint
+   * column sits: row j of expert e at block-layout slot block_offsets[e]*B + j.  ids stay required
+   * and must agree.  Everything is checked on the device before use: offsets that do not start at 0,
+   * decrease, exceed the routed slots or give an expert fewer blocks than ceil(rows/B) (or blocks
+   * beyond N) make every row drop out; a row whose flat index is out of range, repeated, or routed to
+   * another expert by ids drops out; a routed slot that no row names, or a given token_position_to_id
+   * / block_to_expert entry that disagrees, is reported too -- each case OR-s
+   * MOE_STATUS_BAD_ROUTE_META into status_dev (outputs then invalid, but no access goes out of
+   * bounds).  With num_valid_tokens, rows may name only the leading valid tokens' slots. */
+  const int32_t* expert_offsets;       /* [E+1] [SM] expert_frequency_offset: rows of expert e are the
+                                          grouped rows expert_offsets[e] .. expert_offsets[e+1]-1 */
+  const int32_t* s_scatter_idx;        /* [T*K] grouped row -> flat slot t*K + k */
+  const int32_t* block_offsets;        /* [E+1] first block of each expert in the block layout */
+  const int32_t* token_position_to_id; /* [N*B] or NULL: [BW] slot -> token (checked only) */
+  const int32_t* block_to_expert;      /* [N] or NULL: [BW] block -> expert (checked only) */
 } MoeBwdArgs;
 
 /* Bytes of workspace moe_bwd needs for these shapes and options (pointers are not read). */

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoebwd.s
 
 QUANT_ROWWISE, QUANT_COLWISE = 0, 1
 SF_PLAIN, SF_TILED = 0, 1
-STATUS_BAD_EXPERT_ID, STATUS_TIMEOUT = 1, 2
+STATUS_BAD_EXPERT_ID, STATUS_TIMEOUT, STATUS_BAD_ROUTE_META = 1, 2, 4
 ACT_CHECKPOINT, ACT_RECOMPUTE = 0, 1
 GLU_SWIGLU, GLU_GEGLU = 0, 1
 GATE_UP_CONCAT, GATE_UP_INTERLEAVED = 0, 1
@@ -56,7 +56,11 @@ class MoeBwdArgs(ctypes.Structure):
                [(n, ctypes.c_void_p) for n in ("W1t", "W1t_q", "W1t_sf", "b1", "ds_masked", "num_valid_tokens")] + \
                [(n, ctypes.c_int) for n in ("glu", "gate_up_layout")] + \
                [(n, ctypes.c_void_p) for n in ("intermediate_ckpt", "scaled_intermediate_ckpt", "down_proj_act_ckpt",
-                                               "gate_act_ckpt")]
+                                               "gate_act_ckpt")] + \
+               [(n, ctypes.c_void_p) for n in ("expert_offsets", "s_scatter_idx", "block_offsets",
+                                               "token_position_to_id", "block_to_expert")]
+
+ROUTE_META_FIELDS = ("expert_offsets", "s_scatter_idx", "block_offsets", "token_position_to_id", "block_to_expert")
 
 
 _lib = None
@@ -272,11 +276,14 @@ class MoeBwd:
 
     def bind(self, *, x, dout, s, ids, ckpt=None, W1=None, W2=None, W1_q=None, W1_sf=None, W2_q=None, W2_sf=None,
              b2=None, W1t=None, W1t_q=None, W1t_sf=None, b1=None, num_valid_tokens=None, intermediate_ckpt=None,
-             scaled_intermediate_ckpt=None, down_proj_act_ckpt=None, gate_act_ckpt=None):
+             scaled_intermediate_ckpt=None, down_proj_act_ckpt=None, gate_act_ckpt=None, route_meta=None):
         """ckpt: the [N,2,I,B] checkpoint (act_src ACT_CHECKPOINT).  W1t (bf16 [E,2I,H]) or W1t_q/W1t_sf
         and optionally b1 [E,2I]: the operands of the recomputation (act_src ACT_RECOMPUTE).
         intermediate_ckpt / scaled_intermediate_ckpt / gate_act_ckpt [N,I,B] and down_proj_act_ckpt
-        [N,B,H] (bf16, block layout): saved forward values, see the MoeBwdArgs fields."""
+        [N,B,H] (bf16, block layout): saved forward values, see the MoeBwdArgs fields.
+        route_meta: routing metadata from the caller (a dict with int32 CUDA tensors expert_offsets,
+        s_scatter_idx, block_offsets and optionally token_position_to_id, block_to_expert -- e.g.
+        route_meta()'s result); None: moe_bwd computes it from ids."""
         _need_cuda(x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2, W1t, W1t_q, W1t_sf, b1, num_valid_tokens,
                    intermediate_ckpt, scaled_intermediate_ckpt, down_proj_act_ckpt, gate_act_ckpt)
         if num_valid_tokens is not None:
@@ -308,10 +315,16 @@ class MoeBwd:
         for name in ("dx", "dW1", "dW2", "ds", "db1", "db2", "ds_masked", "status"):
             t = getattr(self, name)
             setattr(a, "status_dev" if name == "status" else name, None if t is None else t.data_ptr())
+        rm = {k: (route_meta or {}).get(k) for k in ROUTE_META_FIELDS}
+        for k, t in rm.items():
+            _need_cuda(t)
+            assert t is None or t.dtype == torch.int32, k
+            setattr(a, k, None if t is None else t.data_ptr())
         a.workspace = self.workspace.data_ptr()
         a.workspace_bytes = self.workspace.numel()
         self._keep = [x, dout, s, ids, ckpt, W1, W2, W1_q, W1_sf, W2_q, W2_sf, b2, W1t, W1t_q, W1t_sf, b1,
-                      num_valid_tokens, intermediate_ckpt, scaled_intermediate_ckpt, down_proj_act_ckpt, gate_act_ckpt]
+                      num_valid_tokens, intermediate_ckpt, scaled_intermediate_ckpt, down_proj_act_ckpt, gate_act_ckpt,
+                      *rm.values()]
         return self
 
     def run(self, stream=None):

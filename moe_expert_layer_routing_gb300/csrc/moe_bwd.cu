@@ -240,6 +240,17 @@ static int check_args(const MoeBwdArgs* a, bool need_ptrs) {
   for (const void* q : req)
     if (!q) return fail(MOE_ERR_INVALID, "moe_bwd: required pointer is null");
   if (!rec && !a->gate_up_ckpt) return fail(MOE_ERR_INVALID, "moe_bwd: gate_up_ckpt is null");
+  {
+    const int given = (a->expert_offsets != nullptr) + (a->s_scatter_idx != nullptr) + (a->block_offsets != nullptr);
+    if (given != 0 && given != 3)
+      return fail(MOE_ERR_INVALID, "moe_bwd: routing metadata needs expert_offsets, s_scatter_idx and block_offsets");
+    if (given == 0 && (a->token_position_to_id || a->block_to_expert))
+      return fail(MOE_ERR_INVALID, "moe_bwd: token_position_to_id / block_to_expert come with expert_offsets");
+    const void* m[] = {a->expert_offsets, a->s_scatter_idx, a->block_offsets, a->token_position_to_id,
+                       a->block_to_expert};
+    for (const void* q : m)
+      if (reinterpret_cast<uintptr_t>(q) & 3) return fail(MOE_ERR_INVALID, "moe_bwd: routing metadata must be 4-byte aligned");
+  }
   if (rec && (mx ? (!a->W1t_q || !a->W1t_sf) : !a->W1t))
     return fail(MOE_ERR_INVALID, "moe_bwd: recomputing the pre-activations needs W1t (or W1t_q, W1t_sf)");
   const void* al16r[] = {a->W1t, a->W1t_q, a->W1t_sf, a->b1};
@@ -439,7 +450,12 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   r.pair_offsets = reg<int32_t>(L, ws, R_PAIR_OFFSETS);
   r.num_valid = a.num_valid_tokens;
   r.status = a.status_dev;
-  if ((rc = launch_route_meta(a.ids, a.T, a.K, a.E, a.block_size, L.Nb, P, r, st))) return rc;
+  if (a.expert_offsets) {  // the caller's metadata, checked; tile tables derived from it
+    RouteMetaIn in{a.expert_offsets, a.s_scatter_idx, a.block_offsets, a.token_position_to_id, a.block_to_expert};
+    if ((rc = launch_route_meta_in(in, a.ids, a.T, a.K, a.E, a.block_size, L.Nb, P, r, st))) return rc;
+  } else if ((rc = launch_route_meta(a.ids, a.T, a.K, a.E, a.block_size, L.Nb, P, r, st))) {
+    return rc;
+  }
   int32_t* tile_order = reg<int32_t>(L, ws, R_TILE_ORDER);
   if ((rc = launch_tile_order(tile_row_flat, scalars + 1, a.T, a.K, tile_order, st))) return rc;
   prof_mark(st, slot, 1);

@@ -64,6 +64,16 @@ int launch_tile_order(const int32_t* tile_row_flat, const int32_t* num_tiles, in
                       cudaStream_t st);
 int launch_route_meta(const int32_t* ids, int T, int K, int E, int B, int64_t Nb, int64_t P,
                       const RouteBufs& r, cudaStream_t st);
+// routing metadata supplied by the caller (checked; tile tables derived into r)
+struct RouteMetaIn {
+  const int32_t* expert_offsets;        // [E+1]
+  const int32_t* s_scatter_idx;         // [T*K]
+  const int32_t* block_offsets;         // [E+1]
+  const int32_t* token_position_to_id;  // [Nb*B] or null (checked only)
+  const int32_t* block_to_expert;       // [Nb] or null (checked only)
+};
+int launch_route_meta_in(const RouteMetaIn& in, const int32_t* ids, int T, int K, int E, int B, int64_t Nb, int64_t P,
+                         const RouteBufs& r, cudaStream_t st);
 
 // ------------------------------------------------------------------------------------------
 // gathers / quantisation (prep.cu)

@@ -9,6 +9,8 @@
 //   route_scatter one CTA per chunk: warp-level match_any ranks give every row its stable position
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "moebwd_internal.h"
 
 namespace moebwd {
@@ -238,6 +240,170 @@ __global__ void __launch_bounds__(1024) tile_order_kernel(const int32_t* __restr
   block_exclusive_scan(cnt, kOrderBuckets, wt);
   __syncthreads();
   for (int j = threadIdx.x; j < n; j += blockDim.x) order[atomicAdd(&cnt[bucket(j)], 1)] = j;
+}
+
+// ------------------------------------------------------------------------------------------
+// Routing metadata supplied by the caller
+// ------------------------------------------------------------------------------------------
+// The grouped form (expert_offsets, s_scatter_idx) and the block layout (block_offsets; the
+// token_position_to_id / block_to_expert tables when given, which are only checked) are taken as
+// they come, e.g. kept from the forward pass; the tables the GEMMs use (tile offsets, tile owners,
+// tile row -> flat index and back, processing order) are derived from them.  Every caller value is
+// checked before it is used as an index.  Metadata that is not a routing of the ids raises
+// MOE_STATUS_BAD_ROUTE_META: bad offsets make every row drop out (an empty routing), a bad row
+// (flat index out of range, taken twice, or routed to another expert by the ids) drops that row.
+
+// Owner of grouped row r: the largest e < E with eo[e] <= r (offsets nondecreasing, eo[0] = 0).
+__device__ __forceinline__ int owner_of_row(const int32_t* eo, int E, int r) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (eo[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(1024) route_in_scan_kernel(
+    const int32_t* __restrict__ eo_in, const int32_t* __restrict__ bo_in, const int32_t* __restrict__ b2e_in,
+    int64_t TK, const int32_t* __restrict__ num_valid, int K, int E, int B, int64_t Nb, int32_t* expert_offsets,
+    int32_t* block_offsets, int32_t* tile_offsets, int32_t* expert_order, int32_t* tile_expert, int32_t* scalars,
+    int32_t* pair_offsets, int32_t* status) {
+  __shared__ int32_t cnt[kMaxExperts + 1];
+  __shared__ int32_t tiles[kMaxExperts + 1];
+  __shared__ int32_t prs[kMaxExperts + 1];
+  __shared__ int32_t wt[33];
+  __shared__ int bad;
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  const int64_t live = live_slots(num_valid, TK, K);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int64_t r0 = eo_in[e], r1 = eo_in[e + 1], b0 = bo_in[e], b1 = bo_in[e + 1];
+    bool ok = r1 >= r0 && b1 >= b0 && (b1 - b0) * B >= r1 - r0;  // the expert's blocks hold its rows
+    if (e == 0) ok = ok && r0 == 0 && b0 == 0;
+    if (e == E - 1) ok = ok && r1 <= live && b1 <= Nb;
+    if (!ok) bad = 1;
+  }
+  __syncthreads();
+  const bool ok = bad == 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int n = ok ? eo_in[e + 1] - eo_in[e] : 0;
+    cnt[e] = n;
+    tiles[e] = (n + kTileM - 1) / kTileM;
+    prs[e] = (tiles[e] + 1) / 2;
+  }
+  __syncthreads();
+  // tile_offsets / pair_offsets from exclusive scans of the counts
+  const int tot_tiles = block_exclusive_scan(tiles, E, wt);
+  const int tot_pairs = block_exclusive_scan(prs, E, wt);
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    expert_offsets[e] = ok ? eo_in[e] : 0;
+    block_offsets[e] = ok ? bo_in[e] : 0;
+    tile_offsets[e] = (e < E ? tiles[e] : tot_tiles) * kTileM;
+    if (pair_offsets) pair_offsets[e] = e < E ? prs[e] : tot_pairs;
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int t_end = (e + 1 < E) ? tiles[e + 1] : tot_tiles;
+    for (int t = tiles[e]; t < t_end; ++t) tile_expert[t] = e;
+    const int me = cnt[e];
+    int rank = 0;
+    for (int o = 0; o < E; ++o) rank += (cnt[o] > me) || (cnt[o] == me && o < e);
+    expert_order[rank] = e;
+    // the block table, when given, names e for every block that holds e's rows
+    if (ok && b2e_in) {
+      const int nb = (me + B - 1) / B;
+      for (int j = 0; j < nb; ++j)
+        if (b2e_in[bo_in[e] + j] != e) bad = 2;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    scalars[0] = ok ? bo_in[E] : 0;
+    scalars[1] = tot_tiles;
+    scalars[2] = tot_pairs;
+    if (bad) atomicOr(status, MOE_STATUS_BAD_ROUTE_META);
+  }
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_in_rows_kernel(
+    const int32_t* __restrict__ s_scatter_in, const int32_t* __restrict__ tpid_in, const int32_t* __restrict__ ids,
+    int64_t TK, const int32_t* __restrict__ num_valid, int K, int E, int B, const int32_t* __restrict__ expert_offsets,
+    const int32_t* __restrict__ block_offsets, const int32_t* __restrict__ tile_offsets, int32_t* tile_row_flat,
+    int32_t* flat_tile_row, int32_t* status) {
+  extern __shared__ int32_t eo[];  // [E+1] checked copy of the expert offsets
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) eo[e] = expert_offsets[e];
+  __syncthreads();
+  const int total = eo[E];  // <= live slots <= TK (checked by the scan)
+  const int64_t live = live_slots(num_valid, TK, K);
+  int bad = 0;
+  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < total; r += (int64_t)gridDim.x * blockDim.x) {
+    const int e = owner_of_row(eo, E, (int)r);
+    const int j = (int)r - eo[e];
+    const int f = s_scatter_in[r];
+    bool ok = f >= 0 && f < live && ids[f] == e;
+    if (ok && tpid_in) ok = tpid_in[(int64_t)block_offsets[e] * B + j] == f / K;
+    if (ok) {
+      const int p = tile_offsets[e] + j;
+      if (atomicCAS(&flat_tile_row[f], -1, p) == -1)
+        tile_row_flat[p] = f;
+      else
+        ok = false;  // a flat index taken by two rows: the later one drops out
+    }
+    if (!ok) bad = 1;
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, MOE_STATUS_BAD_ROUTE_META);
+}
+
+// Every routed slot must be some row of the metadata; ids outside [0, E) other than -1 are reported
+// as by the routing kernels.
+__global__ void __launch_bounds__(kRouteThreads) route_in_cover_kernel(const int32_t* __restrict__ ids, int64_t TK,
+                                                                       const int32_t* __restrict__ num_valid, int K,
+                                                                       int E, const int32_t* __restrict__ flat_tile_row,
+                                                                       int32_t* status) {
+  const int64_t live = live_slots(num_valid, TK, K);
+  int miss = 0, badid = 0;
+  for (int64_t f = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; f < live; f += (int64_t)gridDim.x * blockDim.x) {
+    const int e = ids[f];
+    if (e >= 0 && e < E)
+      miss |= flat_tile_row[f] < 0;
+    else if (e != -1)
+      badid = 1;
+  }
+  const int m = __syncthreads_or(miss), b = __syncthreads_or(badid);
+  if (threadIdx.x == 0) {
+    if (m) atomicOr(status, MOE_STATUS_BAD_ROUTE_META);
+    if (b) atomicOr(status, MOE_STATUS_BAD_EXPERT_ID);
+  }
+}
+
+int launch_route_meta_in(const RouteMetaIn& in, const int32_t* ids, int T, int K, int E, int B, int64_t Nb, int64_t P,
+                         const RouteBufs& r, cudaStream_t st) {
+  const int64_t TK = (int64_t)T * K;
+  int rc;
+  if ((rc = cuda_check(cudaMemsetAsync(r.tile_row_flat, 0xFF, sizeof(int32_t) * (size_t)P, st), "memset tile rows")))
+    return rc;
+  if ((rc = cuda_check(cudaMemsetAsync(r.tile_expert, 0xFF, sizeof(int32_t) * (size_t)(P / kTileM + 1), st),
+                       "memset tile experts")))
+    return rc;
+  if ((rc = cuda_check(cudaMemsetAsync(r.flat_tile_row, 0xFF, sizeof(int32_t) * (size_t)(TK > 0 ? TK : 1), st),
+                       "memset flat rows")))
+    return rc;
+  route_in_scan_kernel<<<1, 1024, 0, st>>>(in.expert_offsets, in.block_offsets, in.block_to_expert, TK, r.num_valid,
+                                           K, E, B, Nb, r.expert_offsets, r.block_offsets, r.tile_offsets,
+                                           r.expert_order, r.tile_expert, r.scalars, r.pair_offsets, r.status);
+  count_launch();
+  if ((rc = cuda_check(cudaGetLastError(), "route_in_scan"))) return rc;
+  if (TK > 0) {
+    const int grid = (int)std::min<int64_t>((TK + kRouteThreads - 1) / kRouteThreads, 4 * 152);
+    route_in_rows_kernel<<<grid, kRouteThreads, sizeof(int32_t) * (size_t)(E + 1), st>>>(
+        in.s_scatter_idx, in.token_position_to_id, ids, TK, r.num_valid, K, E, B, r.expert_offsets, r.block_offsets,
+        r.tile_offsets, r.tile_row_flat, r.flat_tile_row, r.status);
+    count_launch();
+    if ((rc = cuda_check(cudaGetLastError(), "route_in_rows"))) return rc;
+    route_in_cover_kernel<<<grid, kRouteThreads, 0, st>>>(ids, TK, r.num_valid, K, E, r.flat_tile_row, r.status);
+    count_launch();
+    if ((rc = cuda_check(cudaGetLastError(), "route_in_cover"))) return rc;
+  }
+  return MOE_OK;
 }
 
 int launch_tile_order(const int32_t* tile_row_flat, const int32_t* num_tiles, int T, int K, int32_t* order,
