@@ -9,6 +9,10 @@ excluded) with inputs resident in HBM; `e2e` is the same metric with the step's 
 from pinned host memory and dx/ds copied back inside the timed region.  With N > 1 (torchrun), every
 rank runs an independent replica (the pass has no exchange step), value = sum over ranks / max time.
 `--impl reference` times the CPU float64 oracle on a bounded sample of the same workload.
+The headline timed region records nothing but its two events; the per-stage times (stage_ms, the
+roofline's dominant kernel) come from a second pass of the same steps.  The default run then times
+the other workloads with a throughput bar (fine-grained BF16, many-expert MXFP8, the dense 4096^3
+MXFP8 linear backward) the same way, under `workloads`.
 """
 from __future__ import annotations
 
@@ -336,6 +340,133 @@ def recompute_row(mb, cfg, inp, kw, steps, stream, peak_tf, dev):
                      "excluded from useful_tflops")
 
 
+def setup_problem(mb, cfg, dev):
+    """Inputs, device buffers and the step of one workload (untimed); MXFP8 weights are quantised
+    once here, outside any timed region."""
+    from moe_expert_layer_routing_gb300.inputs import LinearConfig, make_linear_inputs, make_moe_inputs
+    if isinstance(cfg, LinearConfig):
+        inp = make_linear_inputs(cfg, device=dev)
+        op = mb.LinearBwd(cfg.M, cfg.N, cfg.K, mb.PREC_MXFP8, cfg.fp8, dev)
+        return dict(is_linear=True, inp=inp, op=op, kw=None, step=lambda: op.run(inp.dY, inp.W, inp.X),
+                    flops=float(cfg.useful_flops()), tokens=cfg.M, prec=mb.PREC_MXFP8,
+                    in_bytes=sum(t.numel() * t.element_size() for t in (inp.dY, inp.W, inp.X)))
+    inp = make_moe_inputs(cfg, device=dev)
+    op = mb.MoeBwd(T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K, block_size=cfg.block_size,
+                   precision=cfg.precision, affinity=cfg.affinity, fp8_act=cfg.fp8_act, fp8_w=cfg.fp8_w,
+                   has_bias=cfg.bias, device=dev)
+    kw = dict(x=inp.x, dout=inp.dout, s=inp.s, ids=inp.ids, ckpt=inp.ckpt, b2=inp.b2 if cfg.bias else None)
+    if cfg.precision == mb.PREC_MXFP8:
+        W1_q, W1_sf = mb.quantize_weights(inp.W1, cfg.fp8_w)
+        W2_q, W2_sf = mb.quantize_weights(inp.W2, cfg.fp8_w)
+        kw.update(W1_q=W1_q, W1_sf=W1_sf, W2_q=W2_q, W2_sf=W2_sf)
+    else:
+        kw.update(W1=inp.W1, W2=inp.W2)
+    op.bind(**kw)
+    return dict(is_linear=False, inp=inp, op=op, kw=kw, step=lambda: op.run(), flops=float(cfg.useful_flops()),
+                tokens=cfg.T, prec=cfg.precision,
+                in_bytes=sum(t.numel() * t.element_size() for t in kw.values() if t is not None))
+
+
+def time_problem(mb, P, steps, warmup, world, local, stream):
+    """Warm-up, then `steps` timed steps with nothing else recorded on the stream (the headline time,
+    CUDA events, max over ranks, clocks sampled meanwhile), then -- for the MoE backward -- a second
+    pass of the same steps with the library's per-stage events on (stage_ms, and that pass's own
+    time to show the events cost nothing measurable)."""
+    import torch
+    step = P["step"]
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if not P["is_linear"]:
+        st0 = int(P["op"].status.item())
+        if st0 != 0:
+            raise SystemExit(f"device status {st0} after warm-up")
+    launches0 = mb.kernel_launches()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = allreduce_max(ev0.elapsed_time(ev1) / steps, world)
+    launches = mb.kernel_launches() - launches0
+    out = dict(ms=ms, launches=launches, clocks=clk.summary(), stages=None, profiled_ms=None)
+    if not P["is_linear"]:
+        mb.profile_enable(True)
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        stages, ncalls = mb.profile_read()
+        mb.profile_enable(False)
+        out["stages"] = {k: v / max(ncalls, 1) for k, v in stages.items()}
+        out["profiled_ms"] = ev0.elapsed_time(ev1) / steps
+        if int(P["op"].status.item()) != 0:
+            raise SystemExit(f"device status {int(P['op'].status.item())} after the timed steps")
+    return out
+
+
+def dominant_roofline(cfg, stages, per_gpu_value, prec, peak_tf, peak_src):
+    """Roofline line of the dominant kernel: the grouped-GEMM stage with the largest time (its
+    useful FLOPs over its average duration from the stage events), or the whole dense step."""
+    if stages is None:
+        return dict(bound="tensor", kernel="linear_bwd (dX and dW GEMMs + quantisation)", achieved=per_gpu_value,
+                    peak=peak_tf, unit="TFLOP/s", frac=per_gpu_value / peak_tf, traffic=None,
+                    peak_source=f"{peak_src} bf16 burst x2 (nominal fp8/bf16)")
+    H, I, TK = cfg.H, cfg.I, cfg.T * cfg.K
+    stage_flops = {"G1_dA_dswiglu": 2.0 * TK * H * I, "G3_dW2": 2.0 * TK * H * I,
+                   "G2_dx_expanded": 4.0 * TK * H * I, "G4_dW1": 4.0 * TK * H * I}
+    dom = max(stage_flops, key=lambda k: stages[k])
+    achieved = stage_flops[dom] / (stages[dom] * 1e-3) / 1e12
+    return dict(bound="tensor", kernel=dom, achieved=achieved, peak=peak_tf, unit="TFLOP/s",
+                frac=achieved / peak_tf, traffic=recorded_traffic(cfg.name, dom),
+                algorithmic_flops_per_launch=stage_flops[dom],
+                per_stage_frac={k: stage_flops[k] / (stages[k] * 1e-3) / 1e12 / peak_tf for k in stage_flops},
+                peak_source=f"{peak_src} bf16 burst" + (" x2 (nominal fp8/bf16)" if prec == 1 else ""),
+                timing="stage events of a second pass of the same steps (profiled_ms_per_step)")
+
+
+EXTRA_WORKLOADS = ("finegrained_bf16", "manyexpert_mxfp8", "dense_mxfp8_4096")
+
+
+def extra_workloads(mb, args, world, local, stream, peaks, peak_src, dev):
+    """The other configurations with a throughput bar, each timed like the headline (device-resident,
+    unprofiled timed region, stage events in a second pass, own clock record)."""
+    import torch
+    from moe_expert_layer_routing_gb300.inputs import CONFIGS
+    lib_peak = recorded_mxfp8_peak()
+    out = {}
+    for name in EXTRA_WORKLOADS:
+        if name == args.workload:
+            continue
+        cfg = CONFIGS[name]
+        P = setup_problem(mb, cfg, dev)
+        T = time_problem(mb, P, args.steps, args.warmup, world, local, stream)
+        value = P["flops"] * world / (T["ms"] * 1e-3) / 1e12
+        peak_tf = peaks["bf16_tflops"] * (FP8_OVER_BF16 if P["prec"] == 1 else 1.0)
+        rl = dominant_roofline(cfg, T["stages"], value / world, P["prec"], peak_tf, peak_src)
+        if P["prec"] == 1 and lib_peak:
+            rl["frac_of_mxfp8_library"] = rl["achieved"] / lib_peak[0]
+        out[name] = dict(value=value, unit="TFLOP/s", ms_per_step=T["ms"], profiled_ms_per_step=T["profiled_ms"],
+                         dtype="mxfp8" if P["prec"] == 1 else "bf16",
+                         pct_of_tensor_peak=100.0 * value / world / peak_tf,
+                         pct_of_mxfp8_library_peak=(100.0 * value / world / lib_peak[0])
+                         if (P["prec"] == 1 and lib_peak) else None,
+                         tokens_per_s=P["tokens"] * world / (T["ms"] * 1e-3), gpu_launches=T["launches"],
+                         roofline=dict(kernel=rl["kernel"], achieved=rl["achieved"], frac=rl["frac"],
+                                       peak=rl["peak"], per_stage_frac=rl.get("per_stage_frac")),
+                         stage_ms=T["stages"], clocks=T["clocks"], config=workload_config(cfg, P["is_linear"], world))
+        del P
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -345,6 +476,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other bar workloads after the headline")
     ap.add_argument("--measure-peaks", action="store_true", help="library GEMM peaks only")
     args = ap.parse_args()
     if args.measure_peaks:
@@ -392,83 +524,14 @@ def main():
     stream = torch.cuda.current_stream()
     peaks, peak_src = load_peaks()
 
-    # ---------------------------------------------------------------- problem setup (untimed)
-    if is_linear:
-        inp = make_linear_inputs(cfg, device=dev)
-        op = mb.LinearBwd(cfg.M, cfg.N, cfg.K, mb.PREC_MXFP8, cfg.fp8, dev)
-        step = lambda: op.run(inp.dY, inp.W, inp.X)  # noqa: E731
-        flops = float(cfg.useful_flops())
-        tokens = cfg.M
-        prec = mb.PREC_MXFP8
-        in_bytes = sum(t.numel() * t.element_size() for t in (inp.dY, inp.W, inp.X))
-    else:
-        inp = make_moe_inputs(cfg, device=dev)
-        op = mb.MoeBwd(T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K, block_size=cfg.block_size,
-                       precision=cfg.precision, affinity=cfg.affinity, fp8_act=cfg.fp8_act, fp8_w=cfg.fp8_w,
-                       has_bias=cfg.bias, device=dev)
-        kw = dict(x=inp.x, dout=inp.dout, s=inp.s, ids=inp.ids, ckpt=inp.ckpt, b2=inp.b2 if cfg.bias else None)
-        if cfg.precision == mb.PREC_MXFP8:       # weights pre-quantised once, outside the timed region
-            W1_q, W1_sf = mb.quantize_weights(inp.W1, cfg.fp8_w)
-            W2_q, W2_sf = mb.quantize_weights(inp.W2, cfg.fp8_w)
-            kw.update(W1_q=W1_q, W1_sf=W1_sf, W2_q=W2_q, W2_sf=W2_sf)
-        else:
-            kw.update(W1=inp.W1, W2=inp.W2)
-        op.bind(**kw)
-        step = lambda: op.run()  # noqa: E731
-        flops = float(cfg.useful_flops())
-        tokens = cfg.T
-        prec = cfg.precision
-        in_bytes = sum(t.numel() * t.element_size() for t in kw.values() if t is not None)
-
-    # ---------------------------------------------------------------- device-resident timing
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if not is_linear:
-        st0 = int(op.status.item())
-        if st0 != 0:
-            raise SystemExit(f"device status {st0} after warm-up")
-    launches0 = mb.kernel_launches()
-    if not is_linear:
-        mb.profile_enable(True)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
-        torch.cuda.synchronize()
-    barrier(world)
-    ms = ev0.elapsed_time(ev1) / args.steps
-    ms = allreduce_max(ms, world)
-    launches = mb.kernel_launches() - launches0
-    stages = None
-    if not is_linear:
-        stages, ncalls = mb.profile_read()
-        mb.profile_enable(False)
-        stages = {k: v / max(ncalls, 1) for k, v in stages.items()}
+    P = setup_problem(mb, cfg, dev)
+    op, inp, kw, flops, tokens, prec, in_bytes = (P[k] for k in ("op", "inp", "kw", "flops", "tokens", "prec",
+                                                                   "in_bytes"))
+    T = time_problem(mb, P, args.steps, args.warmup, world, local, stream)
+    ms, launches, clocks, stages = T["ms"], T["launches"], T["clocks"], T["stages"]
     value = flops * world / (ms * 1e-3) / 1e12
-
-    # ---------------------------------------------------------------- roofline of the dominant kernel
     peak_tf = peaks["bf16_tflops"] * (FP8_OVER_BF16 if prec == 1 else 1.0)
-    if not is_linear:
-        H, I, TK = cfg.H, cfg.I, cfg.T * cfg.K
-        stage_flops = {"G1_dA_dswiglu": 2.0 * TK * H * I, "G3_dW2": 2.0 * TK * H * I,
-                       "G2_dx_expanded": 4.0 * TK * H * I, "G4_dW1": 4.0 * TK * H * I}
-        dom = max(stage_flops, key=lambda k: stages[k])
-        achieved = stage_flops[dom] / (stages[dom] * 1e-3) / 1e12
-        roofline = dict(bound="tensor", kernel=dom, achieved=achieved, peak=peak_tf, unit="TFLOP/s",
-                        frac=achieved / peak_tf, traffic=recorded_traffic(cfg.name, dom),
-                        algorithmic_flops_per_launch=stage_flops[dom],
-                        peak_source=f"{peak_src} bf16 burst" + (" x2 (nominal fp8/bf16)" if prec == 1 else ""))
-    else:
-        achieved = value / world
-        roofline = dict(bound="tensor", kernel="linear_bwd (dX and dW GEMMs + quantisation)", achieved=achieved,
-                        peak=peak_tf, unit="TFLOP/s", frac=achieved / peak_tf, traffic=None,
-                        peak_source=f"{peak_src} bf16 burst x2 (nominal fp8/bf16)")
+    roofline = dominant_roofline(cfg, stages, value / world, prec, peak_tf, peak_src)
 
     # ---------------------------------------------------------------- router backward (consumes ds)
     next_rows = None
@@ -568,6 +631,11 @@ def main():
                          else "dY, W, X in; dX, dW out; copies overlap the previous step"))
         del ops, dev_in
 
+    # ---------------------------------------------------------------- the other bar workloads (N=1)
+    extra = None
+    if world == 1 and not args.no_extra and args.workload == DEFAULT_WORKLOAD:
+        extra = extra_workloads(mb, args, world, local, stream, peaks, peak_src, dev)
+
     if rank != 0:
         barrier(world)
         return
@@ -590,9 +658,9 @@ def main():
         dtype="mxfp8" if prec == 1 else "bf16", data="synthetic (seeded; shapes and routing of the workload)",
         config=conf, tokens_per_s=tokens * world / (ms * 1e-3), pct_of_tensor_peak=100.0 * value / world / peak_tf,
         pct_of_mxfp8_library_peak=(100.0 * value / world / lib_peak[0]) if (prec == 1 and lib_peak) else None,
-        roofline=roofline, cpu_baseline=cpu_baseline, e2e=e2e, clocks=clk.summary(), gpu_launches=launches,
-        next_rows=next_rows,
-        stage_ms=stages, source_sha=source_sha())
+        roofline=roofline, cpu_baseline=cpu_baseline, e2e=e2e, clocks=clocks, gpu_launches=launches,
+        next_rows=next_rows, stage_ms=stages, profiled_ms_per_step=T["profiled_ms"], workloads=extra,
+        source_sha=source_sha())
     print(json.dumps(line), flush=True)
     barrier(world)
 
