@@ -26,7 +26,7 @@ GATE_UP_CONCAT, GATE_UP_INTERLEAVED = 0, 1
 
 WS_REGIONS = ["EXPERT_OFFSETS", "TILE_OFFSETS", "BLOCK_OFFSETS", "TILE_ROW_FLAT", "FLAT_TILE_ROW",
               "DOUT_G", "DOUT_G_SF", "DOUT_GT", "DOUT_GT_SF", "X_GT", "X_GT_SF", "DH", "DH_SF",
-              "DH_T", "DH_T_SF", "AP_T", "AP_T_SF", "DX_EXP", "X_G", "X_G_SF", "GATE_UP_CKPT"]
+              "DH_T", "DH_T_SF", "AP_T", "AP_T_SF", "DX_EXP", "X_G", "X_G_SF", "GATE_UP_CKPT", "DOUT_Q"]
 
 EXPORTED = ["moe_last_error", "moe_version", "moe_num_blocks_bound", "moe_route_meta_workspace_size",
             "moe_route_meta", "mxfp8_quantize", "moe_bwd_workspace_size", "moe_bwd",
@@ -36,7 +36,7 @@ EXPORTED = ["moe_last_error", "moe_version", "moe_num_blocks_bound", "moe_route_
 
 # library options (moe_set_option)
 OPTIONS = ["WAIT_LIMIT_NS", "PAIR_GEMMS", "PAIR_TILE_N", "G1_TILE_N", "G2_TILE_N", "G3_TILE_N", "G4_TILE_N",
-           "PREP_TILE_ORDER"]
+           "PREP_TILE_ORDER", "G1_GATHER"]
 
 STAGES = ["route", "prep", "G1_dA_dswiglu", "G3_dW2", "G2_dx_expanded", "G4_dW1", "reduce", "G0_recompute_h"]
 

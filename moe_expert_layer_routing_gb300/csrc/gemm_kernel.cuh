@@ -451,6 +451,117 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
 }
 
 
+// Producer with a gathered A operand (the whole warp 0; dSwiGLU GEMM with p.a_gather).  Lane 0 claims
+// and publishes tiles and loads B (and, for MXFP8, both operands' scale atoms) by TMA as the plain
+// producer does; all 32 lanes copy A's 128 rows of each k-block from their source rows with 16-byte
+// cp.async: piece c (16 bytes) of row r lands at r*128 + ((c ^ (r % 8)) * 16), where the 128-byte
+// swizzle of a TMA tile load would put it (the stage is 1024-byte aligned).  A stage's copies are
+// completed kLag stages later -- cp.async.wait_group, the proxy fence that makes them visible to the
+// tensor core, then lane 0's second arrival on the stage's full barrier (initialised with two) -- so
+// that each lane keeps kLag stages of gathers in flight.  kLag < STAGES: the stage the producer waits
+// to refill was completed kLag stages after it was issued, so the MMA can always drain it.
+template <typename C, int BN, bool MX>
+__device__ __forceinline__ void producer_gather(const GemmParams& p, const CUtensorMap* tmB, uint8_t* smA,
+                                                uint8_t* smB, uint8_t* smSFA, uint8_t* smSFB, uint64_t* full,
+                                                uint64_t* empty, uint64_t* tile_full, uint64_t* tile_empty,
+                                                volatile int* tile_ring, volatile int* abort_flag, int total,
+                                                int lane) {
+  constexpr int kLag = 2;
+  static_assert(kLag <= C::STAGES - 1, "gathered A needs more stages than its completion lag");
+  const char* src = static_cast<const char*>(p.a_gather);
+  const int piece = lane & 7;
+  int s = 0;
+  uint32_t ph = 0;
+  int64_t issued = 0, completed = 0;
+  int rs = 0;
+  uint32_t rph = 0;
+  for (;;) {
+    int t = 0;
+    if (lane == 0) {
+      t = atomicAdd(p.tile_counter, 1);
+      if (t >= total) t = -1;
+    }
+    t = __shfl_sync(0xffffffffu, t, 0);
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait_bounded(&tile_empty[rs], rph ^ 1u, p.status, abort_flag, p.wait_ns);
+    if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    if (lane == 0) {
+      tile_ring[rs] = t;
+      mbar_arrive(&tile_full[rs]);
+    }
+    if (++rs == C::RING) {
+      rs = 0;
+      rph ^= 1u;
+    }
+    if (t < 0) break;
+    const TileInfo ti = gemm_decode_tile<BN, C::BKE>(p, t);
+    // source rows of this lane's tile rows r = (lane >> 3) + 4 i (padding rows read row 0)
+    uint32_t rowi[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int f = p.tile_row_flat[(int64_t)ti.a_row + (lane >> 3) + 4 * i];
+      rowi[i] = f >= 0 ? (uint32_t)(f / p.a_gather_div) : 0u;
+    }
+    for (int kb = 0; kb < ti.nk; ++kb) {
+      int w = 1;
+      if (lane == 0) w = mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, abort_flag, p.wait_ns);
+      if (!__shfl_sync(0xffffffffu, w, 0)) {
+        ok = 0;
+        break;
+      }
+      const int kc = ti.k0 + kb * C::BKE;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES - C::A_BYTES);
+        tma_load_2d(smB + s * C::B_BYTES, tmB, &full[s], kc, ti.b_row);
+        if constexpr (MX) {
+          const int kt = kc / 128;
+          bulk_load(smSFA + s * C::SFA_BYTES, p.sfa + ((int64_t)(ti.a_row / 128) * p.sfa_ktiles + kt) * 512, 512,
+                    &full[s]);
+#pragma unroll
+          for (int h = 0; h < C::SFB_ATOMS; ++h)
+            bulk_load(smSFB + s * C::SFB_BYTES + h * 512,
+                      p.sfb + ((int64_t)((ti.b_row / BN) * C::SFB_ATOMS + h) * p.sfb_ktiles + kt) * 512, 512,
+                      &full[s]);
+        }
+      }
+      const uint32_t dst0 = smem_u32(smA + s * C::A_BYTES);
+      const int64_t koff = (int64_t)kc * (MX ? 1 : 2) + piece * 16;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int r = (lane >> 3) + 4 * i;
+        cp_async_16(dst0 + r * 128 + ((piece ^ (r & 7)) << 4), src + (int64_t)rowi[i] * p.a_gather_ld + koff);
+      }
+      cp_async_commit();
+      ++issued;
+      if (issued - completed > kLag) {  // the stage issued kLag stages ago is complete for every lane
+        cp_async_wait<kLag>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[completed % C::STAGES]);
+        ++completed;
+      }
+      if (++s == C::STAGES) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    if (!ok) break;
+  }
+  // Drain: every gather completes and is released, then every TMA copy issued lands, before the CTA
+  // may exit.
+  cp_async_wait<0>();
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    for (; completed < issued; ++completed) mbar_arrive(&full[completed % C::STAGES]);
+    const int64_t n = issued < C::STAGES ? issued : C::STAGES;
+    for (int64_t i = 1; i <= n; ++i) {
+      const int64_t q = issued - i;
+      mbar_wait_drain(&full[q % C::STAGES], (uint32_t)((q / C::STAGES) & 1), p.status);
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------------
@@ -488,8 +599,10 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    // a gathered A operand arrives on a stage's full barrier a second time (see producer_gather)
+    const uint32_t full_count = (EPI == kEpiDSwiGLU && p.a_gather) ? 2u : 1u;
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], full_count);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -522,7 +635,11 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
   // the K-grouped order) and publishes each index, then -1, through the ring.
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (EPI == kEpiDSwiGLU && p.a_gather) {
+      // ---------------- producer with gathered A rows (whole warp) ----------------
+      producer_gather<C, BN, MX>(p, &tmB, smA, smB, smSFA, smSFB, full, empty, tile_full, tile_empty, tile_ring,
+                                 abort_flag, total, lane);
+    } else if (lane == 0) {
       // ---------------- TMA producer ----------------
       int s = 0;
       uint32_t ph = 0;

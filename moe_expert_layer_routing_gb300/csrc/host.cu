@@ -49,6 +49,7 @@ static const int64_t kOptDefault[MOE_NUM_OPTIONS] = {
     256,                    // MOE_OPT_PAIR_TILE_N
     0, 0, 0, 0,             // MOE_OPT_G1_TILE_N .. MOE_OPT_G4_TILE_N (automatic)
     1,                      // MOE_OPT_PREP_TILE_ORDER
+    1,                      // MOE_OPT_G1_GATHER
 };
 static std::once_flag g_opt_once;
 static void opt_init() {
@@ -71,7 +72,8 @@ static bool option_value_ok(int o, int64_t v) {
     case MOE_OPT_G2_TILE_N:
     case MOE_OPT_G3_TILE_N:
     case MOE_OPT_G4_TILE_N: return v == 0 || v == 128 || v == 256;
-    case MOE_OPT_PREP_TILE_ORDER: return v == 0 || v == 1;
+    case MOE_OPT_PREP_TILE_ORDER:
+    case MOE_OPT_G1_GATHER: return v == 0 || v == 1;
     default: return false;
   }
 }

@@ -91,7 +91,7 @@ enum Region {
   R_CHUNK_COUNTS, R_EXPERT_OFFSETS, R_BLOCK_OFFSETS, R_TILE_OFFSETS, R_EXPERT_ORDER, R_SCALARS,
   R_X_GATHER, R_S_SCATTER, R_S_REV, R_TPID, R_B2E, R_TILE_ROW_FLAT, R_FLAT_TILE_ROW, R_TILE_EXPERT,
   R_DOUT_G, R_DOUT_G_SF, R_DOUT_GT, R_DOUT_GT_SF, R_X_GT, R_X_GT_SF, R_DH, R_DH_SF, R_DH_T, R_DH_T_SF,
-  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_X_G, R_X_G_SF, R_CKPT, R_PAIR_OFFSETS, R_TILE_ORDER, R_TILE_ROW_SLOT, R_W2_SF_T, R_DB1_PART, R_DB2_PART, R_COUNT
+  R_AP_T, R_AP_T_SF, R_DX_EXP, R_DS_PART, R_DS_BIAS, R_COUNTERS, R_X_G, R_X_G_SF, R_CKPT, R_PAIR_OFFSETS, R_TILE_ORDER, R_TILE_ROW_SLOT, R_W2_SF_T, R_DB1_PART, R_DB2_PART, R_DOUT_Q, R_COUNT
 };
 
 struct Layout {
@@ -100,6 +100,7 @@ struct Layout {
   size_t total;
   int64_t P, Nb, TK;
   int BN1, BN2, BN3, BN4;
+  bool gather;  // G1 gathers its dout rows (MOE_OPT_G1_GATHER)
 };
 
 static int64_t tile_capacity(int64_t TK, int E) {
@@ -153,7 +154,9 @@ static Layout make_layout(const MoeBwdArgs& a) {
   b[R_B2E] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, L.Nb);
   b[R_TILE_ROW_FLAT] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, P);
   b[R_TILE_EXPERT] = sizeof(int32_t) * (size_t)(P / kTileM + 1);
-  b[R_DOUT_G] = (size_t)(P * H * es);
+  L.gather = option(MOE_OPT_G1_GATHER) != 0;
+  b[R_DOUT_G] = L.gather ? 0 : (size_t)(P * H * es);
+  b[R_DOUT_Q] = (L.gather && mx) ? (size_t)((int64_t)a.T * H) : 0;  // dout codes per token
   b[R_DOUT_GT] = (size_t)(H * P * es);
   b[R_X_GT] = (size_t)(H * P * es);
   b[R_DH] = (size_t)(P * 2 * I * es);
@@ -321,7 +324,7 @@ extern "C" int moe_bwd_workspace_region(const MoeBwdArgs* args, int region, size
                                               R_DOUT_GT_SF,     R_X_GT,         R_X_GT_SF,       R_DH,
                                               R_DH_SF,          R_DH_T,         R_DH_T_SF,       R_AP_T,
                                               R_AP_T_SF,        R_DX_EXP,         R_X_G,           R_X_G_SF,
-                                              R_CKPT};
+                                              R_CKPT,           R_DOUT_Q};
   if (region < 0 || region >= MOE_WS_NUM_REGIONS) return fail(MOE_ERR_INVALID, "bad region");
   const Layout L = make_layout(*args);
   *offset = L.off[map[region]];
@@ -476,7 +479,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   pa.mx = mx;
   pa.fmt = a.fp8_act;
   pa.scale_t = a.affinity == MOE_AFFINITY_ON_H;
-  pa.dout_g = reg<void>(L, ws, R_DOUT_G);
+  pa.dout_g = reg<void>(L, ws, R_DOUT_G);  // null when G1 gathers its rows
   pa.dout_g_sf = reg<uint8_t>(L, ws, R_DOUT_G_SF);
   pa.dout_gt = reg<void>(L, ws, R_DOUT_GT);
   pa.dout_gt_sf = reg<uint8_t>(L, ws, R_DOUT_GT_SF);
@@ -489,6 +492,10 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   pa.skip_dout_t = a.down_proj_act_ckpt != nullptr;
   pa.db2_part = (a.has_bias && !mx && !pa.skip_dout_t) ? reg<float>(L, ws, R_DB2_PART) : nullptr;
   if ((rc = launch_prep(pa, st))) return rc;
+  if (L.gather && mx &&  // the rows G1 gathers: dout quantised once per token (the scales come from prep)
+      (rc = launch_quant_rowwise(pa.dout, a.T, a.T, H, H, nullptr, a.fp8_act, reg<uint8_t>(L, ws, R_DOUT_Q), nullptr,
+                                 1, st)))
+    return rc;
   // dW_down operands from saved forward values ([BW] optional checkpoints)
   const void* inter = a.scaled_intermediate_ckpt ? a.scaled_intermediate_ckpt : a.intermediate_ckpt;
   if (inter && (rc = launch_apt_from_ckpt(static_cast<const uint16_t*>(inter), a.I, a.block_size, P, scalars + 1,
@@ -586,8 +593,16 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.db1_part = a.has_bias ? reg<float>(L, ws, R_DB1_PART) : nullptr;
     p.tile_counter = counters + 0;
     p.status = a.status_dev;
-    if ((rc = launch_gemm(mx, L.BN1, p, reg<void>(L, ws, R_DOUT_G), P, H, W2, E * I, H, st, ckpt, L.Nb * 2 * I,
-                          a.block_size)))
+    const void* A = reg<void>(L, ws, R_DOUT_G);
+    int64_t a_rows = P;
+    if (L.gather) {  // A rows gathered from dout (BF16) or its per-token codes (MXFP8): row = flat / K
+      p.a_gather = mx ? static_cast<const void*>(reg<uint8_t>(L, ws, R_DOUT_Q)) : a.dout;
+      p.a_gather_ld = H * (mx ? 1 : 2);
+      p.a_gather_div = a.K;
+      A = p.a_gather;
+      a_rows = a.T;
+    }
+    if ((rc = launch_gemm(mx, L.BN1, p, A, a_rows, H, W2, E * I, H, st, ckpt, L.Nb * 2 * I, a.block_size)))
       return rc;
   }
   prof_mark(st, slot, 4);

@@ -181,6 +181,12 @@ struct GemmParams {
   int accumulate;               // store epilogue: add the tile to the output instead of overwriting
   int32_t* status;
   uint64_t wait_ns;             // limit of each pipeline wait (set by launch_gemm from MOE_OPT_WAIT_LIMIT_NS)
+  // dSwiGLU GEMM (G1) with a gathered A operand: A row p is row tile_row_flat[p] / a_gather_div of
+  // a_gather (row pitch a_gather_ld bytes; padding rows read row 0, whose results are discarded),
+  // copied by the producer warp into the swizzled stage; null: A comes through the tensor map
+  const void* a_gather;
+  int64_t a_gather_ld;
+  int a_gather_div;
 };
 
 // A [rows, K] and B [rows, K] K-major operands (bf16 or fp8 bytes), tile counts in p.

@@ -2,7 +2,8 @@
 //
 // prep_kernel (one CTA per 128-row tile of the tile-row space, H walked in 256-column chunks)
 // gathers the token rows of every routed (t, k) once and writes, in one pass over dout and x:
-//   dout_g  [P, H]  gathered dout rows                      (G1 A operand, groups along H)
+//   dout_g  [P, H]  gathered dout rows                      (G1 A operand, groups along H; when G1
+//                   gathers its rows itself, nothing for BF16 and only the tiled scales for MXFP8)
 //   dout_gt [H, P]  gathered dout transposed, s-scaled for affinity on H (G3 B operand)
 //   x_gt    [H, P]  gathered x transposed                   (G4 A operand)
 //   ds_bias [P]     <dout_t, b2_e>, the bias term of ds      (sonic-moe db2_and_ds_kernel)
@@ -104,14 +105,16 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
           am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
           if (!colok) continue;
           const uint32_t byte = e8m0_byte(__float_as_uint(am), AF);
-          const float inv = e8m0_inv_scale(byte);
-          uint2 q;
-          q.x = fp8x4_t<AF>(d8[0] * inv, d8[1] * inv, d8[2] * inv, d8[3] * inv);
-          q.y = fp8x4_t<AF>(d8[4] * inv, d8[5] * inv, d8[6] * inv, d8[7] * inv);
-          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(rowdst) + prow * H + col) = q;
+          if (rowdst) {  // no codes when G1 gathers its rows from dout quantised per token
+            const float inv = e8m0_inv_scale(byte);
+            uint2 q;
+            q.x = fp8x4_t<AF>(d8[0] * inv, d8[1] * inv, d8[2] * inv, d8[3] * inv);
+            q.y = fp8x4_t<AF>(d8[4] * inv, d8[5] * inv, d8[6] * inv, d8[7] * inv);
+            *reinterpret_cast<uint2*>(static_cast<uint8_t*>(rowdst) + prow * H + col) = q;
+          }
           if ((lane & 3) == 0) rowsf[sf_tiled_offset(prow, col, H)] = (uint8_t)byte;
         } else {
-          if (colok) *reinterpret_cast<uint4*>(static_cast<uint16_t*>(rowdst) + prow * H + col) = v[i];
+          if (colok && rowdst) *reinterpret_cast<uint4*>(static_cast<uint16_t*>(rowdst) + prow * H + col) = v[i];
         }
       }
       }
@@ -419,7 +422,7 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint16_t* __re
     o.x = fp8x4(d[0] * inv, d[1] * inv, d[2] * inv, d[3] * inv, fmt);
     o.y = fp8x4(d[4] * inv, d[5] * inv, d[6] * inv, d[7] * inv, fmt);
     *reinterpret_cast<uint2*>(q + r * cols + c) = o;
-    if (((c >> 3) & 3) == 0) sf[tiled ? sf_tiled_offset(r, c, cols) : r * (cols / 32) + c / 32] = (uint8_t)byte;
+    if (sf && ((c >> 3) & 3) == 0) sf[tiled ? sf_tiled_offset(r, c, cols) : r * (cols / 32) + c / 32] = (uint8_t)byte;
   }
 }
 

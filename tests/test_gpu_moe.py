@@ -76,8 +76,11 @@ def test_bf16_invalid_ids_are_reported_and_skipped():
     assert float(got["ds"][5, 0]) == 0.0 and float(got["ds"][9, 1]) == 0.0
 
 
-def test_bf16_intermediates_match_oracle():
-    """dh and the gathered operands in the workspace match the oracle's own values."""
+@pytest.mark.parametrize("gather", [1, 0])
+def test_bf16_intermediates_match_oracle(gather, set_option):
+    """dh and the gathered operands in the workspace match the oracle's own values (G1 gathering its
+    dout rows itself, or reading the gathered copy)."""
+    set_option("G1_GATHER", gather)
     inp = make_moe_inputs(CONFIGS["tiny_bf16"])
     op, got = run_gpu(inp)
     meta = oracle_meta(inp)
@@ -88,9 +91,12 @@ def test_bf16_intermediates_match_oracle():
     flat = op.region("TILE_ROW_FLAT").view(torch.int32).cpu().numpy()[:used]
     valid = flat >= 0
     t, k = flat[valid] // cfg.K, flat[valid] % cfg.K
-    dout_g = op.region("DOUT_G").view(torch.bfloat16).reshape(P, cfg.H).cpu()[:used]
-    assert torch.equal(dout_g[torch.from_numpy(valid)], inp.dout[torch.from_numpy(t)])
-    assert torch.all(dout_g[torch.from_numpy(~valid)] == 0)
+    if gather:   # no gathered copy: G1 reads dout's rows
+        assert op.region("DOUT_G").numel() == 0
+    else:
+        dout_g = op.region("DOUT_G").view(torch.bfloat16).reshape(P, cfg.H).cpu()[:used]
+        assert torch.equal(dout_g[torch.from_numpy(valid)], inp.dout[torch.from_numpy(t)])
+        assert torch.all(dout_g[torch.from_numpy(~valid)] == 0)
     x_gt = op.region("X_GT").view(torch.bfloat16).reshape(cfg.H, P).cpu()[:, :used]
     assert torch.equal(x_gt.T[torch.from_numpy(valid)], inp.x[torch.from_numpy(t)])
     # dh from the oracle's formulas
@@ -128,9 +134,11 @@ def test_mxfp8_ragged_many_tiles():
     _check(inp, MXFP8_TOL)
 
 
-def test_mxfp8_quantised_operands_match_oracle_codes():
-    """The gathered dout operand of G1 is quantised bit-exactly; dh codes agree with the oracle's
-    quantisation of its own dh except for rare rounding-boundary cases."""
+@pytest.mark.parametrize("gather", [1, 0])
+def test_mxfp8_quantised_operands_match_oracle_codes(gather, set_option):
+    """G1's dout operand is quantised bit-exactly: per token (the rows G1 gathers) or as the gathered
+    copy, with the gathered tiled scales either way."""
+    set_option("G1_GATHER", gather)
     cfg = small_moe("mx_codes", T=256, H=256, I=256, E=4, K=2, B=256, seed=33, precision=PREC_MXFP8,
                     affinity=AFFINITY_ON_I)
     inp = make_moe_inputs(cfg)
@@ -142,9 +150,15 @@ def test_mxfp8_quantised_operands_match_oracle_codes():
     t = flat // cfg.K
     rows = np.where(valid[:, None], inp.dout.double().numpy()[np.where(valid, t, 0)], 0.0)
     rq, rs = omx.mx_quantize(rows, cfg.fp8_act, axis=1)
-    q = op.region("DOUT_G").cpu().numpy().reshape(P, cfg.H)[:used]
     sf = tiled_sf_to_plain(op.region("DOUT_G_SF").cpu().numpy(), P, cfg.H)[:used]
-    assert np.array_equal(q, rq) and np.array_equal(sf, rs)
+    assert np.array_equal(sf, rs)
+    if gather:
+        tq, _ = omx.mx_quantize(inp.dout.double().numpy(), cfg.fp8_act, axis=1)
+        assert op.region("DOUT_G").numel() == 0
+        assert np.array_equal(op.region("DOUT_Q").cpu().numpy().reshape(cfg.T, cfg.H), tq)
+    else:
+        q = op.region("DOUT_G").cpu().numpy().reshape(P, cfg.H)[:used]
+        assert np.array_equal(q, rq)
 
 
 @pytest.mark.parametrize("affinity", [AFFINITY_ON_I, AFFINITY_ON_H])
