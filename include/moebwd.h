@@ -295,7 +295,7 @@ enum {
   MOE_WS_BLOCK_OFFSETS,      /* int32 [E+1] */
   MOE_WS_TILE_ROW_FLAT,      /* int32 [P]   tile row -> flat t*K+k, -1 padding */
   MOE_WS_FLAT_TILE_ROW,      /* int32 [T*K] flat -> tile row, -1 invalid id */
-  MOE_WS_DOUT_G,             /* G1 A operand: dout rows [P,H] (bf16 | fp8); empty with MOE_OPT_G1_GATHER */
+  MOE_WS_DOUT_G,             /* G1 A operand: dout rows [P,H] (bf16 | fp8); empty with MOE_OPT_G1_GATHER = 1 */
   MOE_WS_DOUT_G_SF,          /*   its tiled scales (MXFP8) */
   MOE_WS_DOUT_GT,            /* G3 B operand: [H,P] (bf16 | fp8), s-scaled for affinity on H */
   MOE_WS_DOUT_GT_SF,
@@ -313,7 +313,7 @@ enum {
   MOE_WS_GATE_UP_CKPT,       /* RECOMPUTE: G0 output, bf16 [Nb,2,I,B] in the checkpoint layout
                                 (Nb = moe_num_blocks_bound; only the slots of routed tile rows are
                                 written) */
-  MOE_WS_DOUT_Q,             /* MXFP8 with MOE_OPT_G1_GATHER: dout quantised once per token [T,H] fp8
+  MOE_WS_DOUT_Q,             /* MXFP8 with MOE_OPT_G1_GATHER = 1: dout quantised once per token [T,H] fp8
                                 (groups along H), the rows G1 gathers; DOUT_G then holds no codes, only
                                 its tiled scales DOUT_G_SF (gathered) */
   MOE_WS_NUM_REGIONS
@@ -400,9 +400,11 @@ enum {
   MOE_OPT_G3_TILE_N,         /* N tile of dW_down: 0 automatic (256 where it divides H), 128, 256 */
   MOE_OPT_G4_TILE_N,         /* N tile of dW_gate_up: 0 automatic (256), 128, 256 */
   MOE_OPT_PREP_TILE_ORDER,   /* 1 (default): the gather pass walks tiles in token order; 0: in index order */
-  MOE_OPT_G1_GATHER,         /* 1 (default): the dA/dSwiGLU GEMM gathers its dout rows itself (from dout,
-                                or for MXFP8 from dout quantised once per token, MOE_WS_DOUT_Q); 0: it reads
-                                a gathered copy written by the gather pass (MOE_WS_DOUT_G) */
+  MOE_OPT_G1_GATHER,         /* 0 (default): the dA/dSwiGLU GEMM reads a gathered copy of dout written by
+                                the gather pass (MOE_WS_DOUT_G); 1: it gathers the rows itself (from dout,
+                                or for MXFP8 from dout quantised once per token, MOE_WS_DOUT_Q) with 16-byte
+                                asynchronous copies -- same results, less memory, but slower (the copies of
+                                one producer warp keep fewer bytes in flight than tensor-map loads) */
   MOE_NUM_OPTIONS
 };
 /* Set an option; value -1 restores its default.  MOE_ERR_INVALID for an unknown option or value. */

@@ -49,7 +49,7 @@ static const int64_t kOptDefault[MOE_NUM_OPTIONS] = {
     256,                    // MOE_OPT_PAIR_TILE_N
     0, 0, 0, 0,             // MOE_OPT_G1_TILE_N .. MOE_OPT_G4_TILE_N (automatic)
     1,                      // MOE_OPT_PREP_TILE_ORDER
-    1,                      // MOE_OPT_G1_GATHER
+    0,                      // MOE_OPT_G1_GATHER (measured slower: see the option's comment)
 };
 static std::once_flag g_opt_once;
 static void opt_init() {
