@@ -423,8 +423,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
 
   const int slot = prof_slot();
   prof_mark(st, slot, 0);
-  int32_t* counters = reg<int32_t>(L, ws, R_COUNTERS);
-  if ((rc = cuda_check(cudaMemsetAsync(counters, 0, L.bytes[R_COUNTERS], st), "memset tile counters"))) return rc;
+  int32_t* counters = reg<int32_t>(L, ws, R_COUNTERS);  // zeroed by the routing kernels
   int32_t* tile_offsets = reg<int32_t>(L, ws, R_TILE_OFFSETS);
   int32_t* expert_order = reg<int32_t>(L, ws, R_EXPERT_ORDER);
   int32_t* scalars = reg<int32_t>(L, ws, R_SCALARS);
@@ -453,6 +452,8 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   r.pair_offsets = reg<int32_t>(L, ws, R_PAIR_OFFSETS);
   r.num_valid = a.num_valid_tokens;
   r.status = a.status_dev;
+  r.zero_counters = counters;
+  r.nzero = (int)(L.bytes[R_COUNTERS] / sizeof(int32_t));
   if (a.expert_offsets) {  // the caller's metadata, checked; tile tables derived from it
     RouteMetaIn in{a.expert_offsets, a.s_scatter_idx, a.block_offsets, a.token_position_to_id, a.block_to_expert};
     if ((rc = launch_route_meta_in(in, a.ids, a.T, a.K, a.E, a.block_size, L.Nb, P, r, st))) return rc;
@@ -687,15 +688,17 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   if (a.ds_masked && (rc = launch_ds_masked(a.ds, a.ids, a.num_valid_tokens, a.T, a.K, a.E, a.ds_masked, st)))
     return rc;
   if (a.has_bias) {  // per-expert sums of the per-tile partials (dout_gt read again only when it was not built here)
-    if ((rc = launch_bias_parts_reduce(reg<float>(L, ws, R_DB1_PART), 4, 2 * I, tile_offsets, (int)E, a.db1, st,
-                                       a.accumulate)))
-      return rc;
-    if (pa.db2_part)
-      rc = launch_bias_parts_reduce(pa.db2_part, 2, H, tile_offsets, (int)E, a.db2, st, a.accumulate);
-    else
+    if (pa.db2_part) {  // db1 and db2 from their per-tile partials in one launch
+      rc = launch_bias_parts_reduce(reg<float>(L, ws, R_DB1_PART), 4, 2 * I, tile_offsets, (int)E, a.db1, st,
+                                    a.accumulate, pa.db2_part, 2, H, a.db2);
+    } else {
+      if ((rc = launch_bias_parts_reduce(reg<float>(L, ws, R_DB1_PART), 4, 2 * I, tile_offsets, (int)E, a.db1, st,
+                                         a.accumulate)))
+        return rc;
       rc = launch_segment_rowsum(reg<uint16_t>(L, ws, R_DOUT_GT), P, (int)H, tile_offsets, (int)E,
                                  a.affinity == MOE_AFFINITY_ON_I ? a.s : nullptr, tile_row_flat, a.db2, st,
                                  a.accumulate);
+    }
     if (rc) return rc;
   }
   prof_mark(st, slot, 8);

@@ -55,6 +55,8 @@ struct RouteBufs {
   int32_t* tile_expert;       // [P/128]
   int32_t* num_blocks_out;    // nullable public copy of scalars[0]
   int32_t* status;
+  int32_t* zero_counters;     // nullable: nzero counters set to 0 by the routing kernels
+  int nzero;
 };
 int route_nchunks(int64_t TK);
 // size checks shared by moe_route_meta and moe_route_meta_noalloc (same order, same messages)
@@ -220,7 +222,9 @@ int launch_segment_rowsum(const uint16_t* buf, int64_t ld, int R, const int32_t*
                           int accumulate = 0);
 // out[e, f] (+)= sum over expert e's 128-row tiles t and k < parts of part[(t * parts + k) * F + f]
 // (in that order: deterministic)
+// and, in the same launch when part2 is given, out2[e, f] (+)= the same sums of part2 (parts2, F2)
 int launch_bias_parts_reduce(const float* part, int parts, int64_t F, const int32_t* tile_offsets, int E,
-                             float* out, cudaStream_t st, int accumulate);
+                             float* out, cudaStream_t st, int accumulate, const float* part2 = nullptr,
+                             int parts2 = 0, int64_t F2 = 0, float* out2 = nullptr);
 
 }  // namespace moebwd

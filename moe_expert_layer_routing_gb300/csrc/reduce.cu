@@ -100,25 +100,64 @@ __global__ void __launch_bounds__(256) segment_rowsum_kernel(const uint16_t* __r
   if (lane == 0) out[(int64_t)e * R + j] = accumulate ? out[(int64_t)e * R + j] + acc : acc;
 }
 
-// One thread per (expert, column): the expert's tile partials summed in tile order.
-__global__ void __launch_bounds__(256) bias_parts_reduce_kernel(const float* __restrict__ part, int parts, int64_t F,
+// One thread per (expert, column) of one or two partial arrays: the expert's tile partials summed in a
+// fixed order (tiles two at a time into two accumulators, added at the end): deterministic.
+struct BiasJob {
+  const float* part;
+  int64_t F;
+  float* out;
+  int parts;
+  unsigned blocks;  // blocks of 256 columns
+};
+
+template <int PARTS>
+__device__ __forceinline__ float bias_sum(const float* __restrict__ part, int64_t F, int64_t f, int t0, int t1) {
+  float a0 = 0.f, a1 = 0.f;
+  int t = t0;
+  for (; t + 1 < t1; t += 2) {
+#pragma unroll
+    for (int k = 0; k < PARTS; ++k) {
+      a0 += part[((int64_t)t * PARTS + k) * F + f];
+      a1 += part[((int64_t)(t + 1) * PARTS + k) * F + f];
+    }
+  }
+  if (t < t1) {
+#pragma unroll
+    for (int k = 0; k < PARTS; ++k) a0 += part[((int64_t)t * PARTS + k) * F + f];
+  }
+  return a0 + a1;
+}
+
+__global__ void __launch_bounds__(256) bias_parts_reduce_kernel(BiasJob j0, BiasJob j1,
                                                                 const int32_t* __restrict__ tile_offsets,
-                                                                float* __restrict__ out, int accumulate) {
+                                                                int accumulate) {
   const int e = blockIdx.y;
-  const int64_t f = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (f >= F) return;
+  const bool second = blockIdx.x >= j0.blocks;
+  const BiasJob& j = second ? j1 : j0;
+  const int64_t f = (int64_t)(blockIdx.x - (second ? j0.blocks : 0u)) * blockDim.x + threadIdx.x;
+  if (f >= j.F) return;
   const int t0 = tile_offsets[e] / 128, t1 = tile_offsets[e + 1] / 128;
-  float acc = 0.f;
-  for (int t = t0; t < t1; ++t)
-    for (int k = 0; k < parts; ++k) acc += part[((int64_t)t * parts + k) * F + f];
-  out[(int64_t)e * F + f] = accumulate ? out[(int64_t)e * F + f] + acc : acc;
+  float acc;
+  if (j.parts == 4)
+    acc = bias_sum<4>(j.part, j.F, f, t0, t1);
+  else if (j.parts == 2)
+    acc = bias_sum<2>(j.part, j.F, f, t0, t1);
+  else
+    acc = bias_sum<1>(j.part, j.F, f, t0, t1);
+  float* o = j.out + (int64_t)e * j.F + f;
+  *o = accumulate ? *o + acc : acc;
 }
 
 int launch_bias_parts_reduce(const float* part, int parts, int64_t F, const int32_t* tile_offsets, int E, float* out,
-                             cudaStream_t st, int accumulate) {
-  if (F == 0 || E == 0) return MOE_OK;
-  dim3 grid((unsigned)((F + 255) / 256), (unsigned)E);
-  bias_parts_reduce_kernel<<<grid, 256, 0, st>>>(part, parts, F, tile_offsets, out, accumulate);
+                             cudaStream_t st, int accumulate, const float* part2, int parts2, int64_t F2,
+                             float* out2) {
+  if (E == 0 || (F == 0 && F2 == 0)) return MOE_OK;
+  if ((parts != 1 && parts != 2 && parts != 4) || (part2 && parts2 != 1 && parts2 != 2 && parts2 != 4))
+    return fail(MOE_ERR_INVALID, "bias_parts_reduce: parts must be 1, 2 or 4");
+  BiasJob j0{part, F, out, parts, (unsigned)((F + 255) / 256)};
+  BiasJob j1{part2, part2 ? F2 : 0, out2, parts2, part2 ? (unsigned)((F2 + 255) / 256) : 0u};
+  dim3 grid(j0.blocks + j1.blocks, (unsigned)E);
+  bias_parts_reduce_kernel<<<grid, 256, 0, st>>>(j0, j1, tile_offsets, accumulate);
   count_launch();
   return cuda_check(cudaGetLastError(), "bias_parts_reduce");
 }

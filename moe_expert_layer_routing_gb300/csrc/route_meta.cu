@@ -15,9 +15,9 @@
 
 namespace moebwd {
 
-constexpr int kRouteThreads = 256;
+constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
-constexpr int kIdsPerWarp = kRouteChunk / kRouteWarps;  // 512
+constexpr int kIdsPerWarp = kRouteChunk / kRouteWarps;  // 128
 
 int route_nchunks(int64_t TK) { return (int)((TK + kRouteChunk - 1) / kRouteChunk); }
 
@@ -29,11 +29,29 @@ __device__ __forceinline__ int64_t live_slots(const int32_t* num_valid, int64_t 
   return nv <= 0 ? 0 : (nv * K < TK ? nv * K : TK);
 }
 
-__global__ void route_count_kernel(const int32_t* __restrict__ ids, int64_t TK, int K, int E,
-                                   const int32_t* __restrict__ num_valid, int32_t* __restrict__ chunk_counts,
-                                   int32_t* status) {
+// Tables the later kernels fill sparsely, set to -1 (and, optionally, a few counters to 0) by the
+// counting kernel's threads instead of separate memsets.
+struct RouteFill {
+  int32_t* neg[4];
+  int64_t n[4];
+  int32_t* zero;
+  int nzero;
+};
+
+__global__ void __launch_bounds__(kRouteThreads) route_count_kernel(const int32_t* __restrict__ ids, int64_t TK,
+                                                                    int K, int E,
+                                                                    const int32_t* __restrict__ num_valid,
+                                                                    int32_t* __restrict__ chunk_counts,
+                                                                    int32_t* status, RouteFill fill) {
   extern __shared__ int32_t hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  {
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, stride = (int64_t)gridDim.x * blockDim.x;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      for (int64_t i = tid; i < fill.n[j]; i += stride) fill.neg[j][i] = -1;
+    if (tid < fill.nzero) fill.zero[tid] = 0;
+  }
   __syncthreads();
   const int64_t live = live_slots(num_valid, TK, K);
   const int64_t base = (int64_t)blockIdx.x * kRouteChunk;
@@ -379,6 +397,9 @@ int launch_route_meta_in(const RouteMetaIn& in, const int32_t* ids, int T, int K
                          const RouteBufs& r, cudaStream_t st) {
   const int64_t TK = (int64_t)T * K;
   int rc;
+  if (r.zero_counters &&
+      (rc = cuda_check(cudaMemsetAsync(r.zero_counters, 0, sizeof(int32_t) * (size_t)r.nzero, st), "memset counters")))
+    return rc;
   if ((rc = cuda_check(cudaMemsetAsync(r.tile_row_flat, 0xFF, sizeof(int32_t) * (size_t)P, st), "memset tile rows")))
     return rc;
   if ((rc = cuda_check(cudaMemsetAsync(r.tile_expert, 0xFF, sizeof(int32_t) * (size_t)(P / kTileM + 1), st),
@@ -418,24 +439,19 @@ int launch_route_meta(const int32_t* ids, int T, int K, int E, int B, int64_t Nb
                       cudaStream_t st) {
   const int64_t TK = (int64_t)T * K;
   int rc;
-  if ((rc = cuda_check(cudaMemsetAsync(r.token_position_to_id, 0xFF, sizeof(int32_t) * (size_t)(Nb * B), st),
-                       "memset token_position_to_id")))
-    return rc;
-  if ((rc = cuda_check(cudaMemsetAsync(r.block_to_expert, 0xFF, sizeof(int32_t) * (size_t)(Nb > 0 ? Nb : 1), st),
-                       "memset block_to_expert")))
-    return rc;
-  if ((rc = cuda_check(cudaMemsetAsync(r.tile_row_flat, 0xFF, sizeof(int32_t) * (size_t)P, st), "memset tile rows")))
-    return rc;
-  if ((rc = cuda_check(cudaMemsetAsync(r.tile_expert, 0xFF, sizeof(int32_t) * (size_t)(P / kTileM + 1), st),
-                       "memset tile experts")))
-    return rc;
+  // padding entries of the block and tile tables are -1: filled by route_count's threads (one extra
+  // CTA when there is nothing to count), before route_scatter writes the routed entries
+  RouteFill fill{};
+  fill.neg[0] = r.token_position_to_id; fill.n[0] = Nb * B;
+  fill.neg[1] = r.block_to_expert;      fill.n[1] = Nb > 0 ? Nb : 1;
+  fill.neg[2] = r.tile_row_flat;        fill.n[2] = P;
+  fill.neg[3] = r.tile_expert;          fill.n[3] = P / kTileM + 1;
+  fill.zero = r.zero_counters;          fill.nzero = r.zero_counters ? r.nzero : 0;
   const int nch = route_nchunks(TK);
-  if (nch > 0) {
-    route_count_kernel<<<nch, kRouteThreads, sizeof(int32_t) * E, st>>>(ids, TK, K, E, r.num_valid, r.chunk_counts,
-                                                                          r.status);
-    count_launch();
-    if ((rc = cuda_check(cudaGetLastError(), "route_count"))) return rc;
-  }
+  route_count_kernel<<<nch > 0 ? nch : 1, kRouteThreads, sizeof(int32_t) * E, st>>>(ids, TK, K, E, r.num_valid,
+                                                                                   r.chunk_counts, r.status, fill);
+  count_launch();
+  if ((rc = cuda_check(cudaGetLastError(), "route_count"))) return rc;
   route_scan_kernel<<<1, 1024, 0, st>>>(nch, E, B, r.chunk_counts, r.expert_offsets, r.block_offsets, r.tile_offsets,
                                         r.expert_order, r.block_to_expert, r.tile_expert, r.scalars, r.num_blocks_out,
                                         r.pair_offsets);
