@@ -236,11 +236,11 @@ __device__ __forceinline__ void store_transposed(float* buf, const float (&v)[NC
 #pragma unroll
     for (int o = NC; o < 32; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
     const uint32_t byte = e8m0_byte(__float_as_uint(am), AF);
-    const float inv = e8m0_inv_scale(byte);
+    const uint64_t inv2 = f2_splat(e8m0_inv_scale(byte));
     uint32_t q[NC / 4];
 #pragma unroll
     for (int w = 0; w < NC / 4; ++w)
-      q[w] = fp8x4_t<AF>(col[4 * w] * inv, col[4 * w + 1] * inv, col[4 * w + 2] * inv, col[4 * w + 3] * inv);
+      q[w] = fp8x4_scaled<AF>(col[4 * w], col[4 * w + 1], col[4 * w + 2], col[4 * w + 3], inv2);
     uint8_t* dst = static_cast<uint8_t*>(out) + (row0 + (int64_t)c * rstride) * P + p0 + rg * NC;
     if constexpr (NC == 16)
       *reinterpret_cast<uint4*>(dst) = make_uint4(q[0], q[1], q[2], q[3]);
@@ -326,7 +326,7 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
       ap[jj] = act * u;
       dg[jj] = u * (cdf + g * pdf);
     }
-  } else {  // SiLU(g) = g sigma(g), SiLU'(g) = sigma(g) (1 + g (1 - sigma(g)))
+  } else if constexpr (GENERIC) {  // SiLU(g) = g sigma(g), SiLU'(g) = sigma(g) (1 + g (1 - sigma(g)))
 #pragma unroll
     for (int jj = 0; jj < NC; ++jj) {
       float g = bf16_bits_to_float(ck[(sub * NC + jj) * 128 + m]);
@@ -334,22 +334,67 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
       if (!valid) g = u = 0.f;
       const float sg = __fdividef(1.f, 1.f + __expf(-g));
       float sl = g * sg;
-      if constexpr (GENERIC) sl = saved ? sa[jj] : sl;
+      sl = saved ? sa[jj] : sl;
       du[jj] = sl;
       ap[jj] = sl * u;
       dg[jj] = u * (sg * (1.f + g * (1.f - sg)));
     }
+  } else {
+    // the same SwiGLU terms two features at a time in paired fp32 arithmetic; sigma(g) = 1 / (1 +
+    // 2^(-g log2(e))) from the exp2 and reciprocal approximations, one value per instruction
+    const uint64_t one2 = f2_splat(1.f), neg1 = f2_splat(-1.f), nl2e = f2_splat(-1.4426950408889634f);
+#pragma unroll
+    for (int jj = 0; jj < NC; jj += 2) {
+      float g0 = bf16_bits_to_float(ck[(sub * NC + jj) * 128 + m]);
+      float g1 = bf16_bits_to_float(ck[(sub * NC + jj + 1) * 128 + m]);
+      float u0 = bf16_bits_to_float(ck[32 * 128 + (sub * NC + jj) * 128 + m]);
+      float u1 = bf16_bits_to_float(ck[32 * 128 + (sub * NC + jj + 1) * 128 + m]);
+      if (!valid) g0 = g1 = u0 = u1 = 0.f;
+      const uint64_t G = f2_pack(g0, g1), U = f2_pack(u0, u1);
+      float x0, x1;
+      f2_unpack(f2_mul(G, nl2e), x0, x1);
+      float e0, e1, s0, s1;
+      asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(x0));
+      asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(x1));
+      f2_unpack(f2_add(f2_pack(e0, e1), one2), x0, x1);
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(s0) : "f"(x0));
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(s1) : "f"(x1));
+      const uint64_t SG = f2_pack(s0, s1);
+      const uint64_t SL = f2_mul(G, SG);
+      const uint64_t T = f2_fma(G, f2_fma(SG, neg1, one2), one2);  // 1 + g (1 - sigma)
+      f2_unpack(SL, du[jj], du[jj + 1]);
+      f2_unpack(f2_mul(SL, U), ap[jj], ap[jj + 1]);
+      f2_unpack(f2_mul(U, f2_mul(SG, T)), dg[jj], dg[jj + 1]);
+    }
   }
   tmem_ld_wait_regs<NC>(r);
+  if constexpr (GENERIC) {
 #pragma unroll
-  for (int jj = 0; jj < NC; ++jj) {
-    const float v = valid ? __uint_as_float(r[jj]) : 0.f;
-    const float a = ap[jj];
-    ds_acc = fmaf(v, a, ds_acc);
-    const float dA = sv * v;
-    dg[jj] = dA * dg[jj];
-    du[jj] = dA * du[jj];
-    ap[jj] = p.affinity_on_i ? sv * a : a;
+    for (int jj = 0; jj < NC; ++jj) {
+      const float v = valid ? __uint_as_float(r[jj]) : 0.f;
+      const float a = ap[jj];
+      ds_acc = fmaf(v, a, ds_acc);
+      const float dA = sv * v;
+      dg[jj] = dA * dg[jj];
+      du[jj] = dA * du[jj];
+      ap[jj] = p.affinity_on_i ? sv * a : a;
+    }
+  } else {
+    const uint64_t sv2 = f2_splat(sv);
+    uint64_t DS = f2_splat(0.f);
+#pragma unroll
+    for (int jj = 0; jj < NC; jj += 2) {
+      const uint64_t V = valid ? f2_pack(__uint_as_float(r[jj]), __uint_as_float(r[jj + 1])) : f2_splat(0.f);
+      const uint64_t A = f2_pack(ap[jj], ap[jj + 1]);
+      DS = f2_fma(V, A, DS);
+      const uint64_t DA = f2_mul(sv2, V);
+      f2_unpack(f2_mul(DA, f2_pack(dg[jj], dg[jj + 1])), dg[jj], dg[jj + 1]);
+      f2_unpack(f2_mul(DA, f2_pack(du[jj], du[jj + 1])), du[jj], du[jj + 1]);
+      if (p.affinity_on_i) f2_unpack(f2_mul(sv2, A), ap[jj], ap[jj + 1]);
+    }
+    float d0, d1;
+    f2_unpack(DS, d0, d1);
+    ds_acc += d0 + d1;
   }
   const int c0 = i0 + sub * NC;  // first feature of this warp's columns
   const bool il = GENERIC && NC == 16 && p.interleaved;  // gate_i, up_i at columns 2i, 2i+1 (host: NC == 16)
@@ -400,12 +445,12 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
     }
     uint8_t* dh = static_cast<uint8_t*>(p.dh) + prow * (2 * (int64_t)I);
     const uint32_t bg = e8m0_byte(__float_as_uint(amg), AF), bu = e8m0_byte(__float_as_uint(amu), AF);
-    const float ig = e8m0_inv_scale(bg), iu = e8m0_inv_scale(bu);
+    const uint64_t ig = f2_splat(e8m0_inv_scale(bg)), iu = f2_splat(e8m0_inv_scale(bu));
     uint32_t qg[NC / 4], qu[NC / 4];
 #pragma unroll
     for (int w = 0; w < NC / 4; ++w) {
-      qg[w] = fp8x4_t<AF>(dg[4 * w] * ig, dg[4 * w + 1] * ig, dg[4 * w + 2] * ig, dg[4 * w + 3] * ig);
-      qu[w] = fp8x4_t<AF>(du[4 * w] * iu, du[4 * w + 1] * iu, du[4 * w + 2] * iu, du[4 * w + 3] * iu);
+      qg[w] = fp8x4_scaled<AF>(dg[4 * w], dg[4 * w + 1], dg[4 * w + 2], dg[4 * w + 3], ig);
+      qu[w] = fp8x4_scaled<AF>(du[4 * w], du[4 * w + 1], du[4 * w + 2], du[4 * w + 3], iu);
     }
     if constexpr (NC == 16) {
       // slice 0 writes the row's 32 gate columns i0.., slice 1 its 32 up columns I + i0..: each takes

@@ -87,6 +87,44 @@ __device__ __forceinline__ uint32_t fp8x4_t(float a, float b, float c, float d) 
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
+// Two fp32 values in one 64-bit register for the paired fp32 arithmetic of sm_100-family SMs: each
+// add / mul / fma of .f32x2 performs two round-to-nearest-even operations, each exactly the scalar
+// one, in one instruction.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_splat(float x) { return f2_pack(x, x); }
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// Four FP8 codes of (a, b, c, d) * inv (inv a power of two: the products are exact), the products
+// formed two at a time.
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x4_scaled(float a, float b, float c, float d, uint64_t inv2) {
+  float x0, x1, x2, x3;
+  f2_unpack(f2_mul(f2_pack(a, b), inv2), x0, x1);
+  f2_unpack(f2_mul(f2_pack(c, d), inv2), x2, x3);
+  return fp8x4_t<FMT>(x0, x1, x2, x3);
+}
+
 // Quantise 32 values of one group into 32 FP8 codes (packed little-endian into 8 words) and
 // return the scale byte.
 __device__ __forceinline__ uint32_t quantize_group32(const float (&v)[32], int fmt, uint32_t (&w)[8]) {
@@ -108,10 +146,9 @@ __device__ __forceinline__ uint32_t quantize_group32_t(const float (&v)[32], uin
 #pragma unroll
   for (int j = 0; j < 32; ++j) am = fmaxf(am, fabsf(v[j]));
   const uint32_t byte = e8m0_byte(__float_as_uint(am), FMT);
-  const float inv = e8m0_inv_scale(byte);
+  const uint64_t inv2 = f2_splat(e8m0_inv_scale(byte));
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-    w[j] = fp8x4_t<FMT>(v[4 * j] * inv, v[4 * j + 1] * inv, v[4 * j + 2] * inv, v[4 * j + 3] * inv);
+  for (int j = 0; j < 8; ++j) w[j] = fp8x4_scaled<FMT>(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3], inv2);
   return byte;
 }
 
