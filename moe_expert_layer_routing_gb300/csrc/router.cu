@@ -7,8 +7,11 @@
 //                        dl = p (dp - <dr, r>)   for every logit
 //   plain top-K          s = l[idx]:                     dl[idx_k] = g_k
 //
-// One warp per token, fp32; lane j owns logits j, j+32, ...; the K selected slots are read by every
-// lane (K <= 64).  Ids outside [0, E) are skipped.
+// One warp per token, fp32.  router_bwd_vec_kernel (E a multiple of 4, E <= 1024, K <= 32): one pass
+// over the token's logits, held in registers as float4 (lane l owns columns 128 j + 4 l .. + 3), the
+// slot weights scattered once through a per-warp shared buffer (repeated ids summed in slot order),
+// the row written as float4.  router_bwd_kernel (any E, K <= 64): lane j owns logits j, j+32, ..., the
+// K selected slots broadcast by shuffles per 32 logits.  Ids outside [0, E) are skipped.
 #include <cuda_runtime.h>
 
 #include "moebwd_internal.h"
@@ -88,6 +91,98 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(int mode, int renorm, c
   }
 }
 
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+template <int NV>  // float4 column groups per lane: ceil(E / 128)
+__global__ void __launch_bounds__(256) router_bwd_vec_kernel(int mode, int renorm, const float* __restrict__ logits,
+                                                             const float* __restrict__ scores,
+                                                             const float* __restrict__ g,
+                                                             const int32_t* __restrict__ ids, int T, int K, int E,
+                                                             float* __restrict__ dl) {
+  __shared__ float4 sbuf[8][NV * 32];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + w;
+  if (t >= T) return;  // only warp-level synchronisation below
+  float4* buf = sbuf[w];
+  int id = -1;
+  float gk = 0.f, sk = 0.f;
+  if (lane < K) {
+    id = ids[(int64_t)t * K + lane];
+    gk = g[(int64_t)t * K + lane];
+    if (scores) sk = scores[(int64_t)t * K + lane];
+    if (id < 0 || id >= E) id = -1;
+  }
+  const float* lt = logits ? logits + (int64_t)t * E : nullptr;
+  float4 L[NV];
+  float mx = 0.f, inv = 1.f, dot = 0.f, wk = 0.f;
+  if (mode == MOE_ROUTER_TOPK) {
+    wk = gk;
+  } else if (mode == MOE_ROUTER_SOFTMAX_OVER_TOPK) {
+    const float d = warp_sum(id >= 0 ? gk * sk : 0.f);
+    wk = sk * (gk - d);
+  } else {
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int c = j * 128 + 4 * lane;
+      L[j] = c < E ? reinterpret_cast<const float4*>(lt)[j * 32 + lane]
+                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      m = fmaxf(m, fmaxf(fmaxf(L[j].x, L[j].y), fmaxf(L[j].z, L[j].w)));
+    }
+    mx = warp_max(m);
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+      sum += __expf(L[j].x - mx) + __expf(L[j].y - mx) + __expf(L[j].z - mx) + __expf(L[j].w - mx);
+    inv = 1.f / warp_sum(sum);
+    const float pk = id >= 0 ? __expf(lt[id] - mx) * inv : 0.f;
+    const float S = warp_sum(pk), dsum = warp_sum(id >= 0 ? gk * sk : 0.f);
+    wk = renorm ? (gk - dsum) / S : gk;  // dr of the slot
+    dot = warp_sum(id >= 0 ? wk * pk : 0.f);
+  }
+#pragma unroll
+  for (int j = 0; j < NV; ++j) buf[j * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncwarp();
+  // the first slot of each distinct id writes the sum of its slots' weights, in slot order
+  float tot = 0.f;
+  for (int j = 0; j < K; ++j) {
+    const int idj = __shfl_sync(0xffffffffu, id, j);
+    const float wj = __shfl_sync(0xffffffffu, wk, j);
+    if (idj == id) tot += wj;
+  }
+  const unsigned same = __match_any_sync(0xffffffffu, id);
+  if (id >= 0 && lane == __ffs(same) - 1) reinterpret_cast<float*>(buf)[id] = tot;
+  __syncwarp();
+  float4* out = reinterpret_cast<float4*>(dl + (int64_t)t * E);
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    if (j * 128 + 4 * lane >= E) continue;
+    float4 v = buf[j * 32 + lane];
+    if (mode == MOE_ROUTER_TOPK_OVER_SOFTMAX) {
+      v.x = __expf(L[j].x - mx) * inv * (v.x - dot);
+      v.y = __expf(L[j].y - mx) * inv * (v.y - dot);
+      v.z = __expf(L[j].z - mx) * inv * (v.z - dot);
+      v.w = __expf(L[j].w - mx) * inv * (v.w - dot);
+    }
+    out[j * 32 + lane] = v;
+  }
+}
+
+template <int NV>
+static void router_vec_launch(int mode, int renorm, const float* logits, const float* scores, const float* dscores,
+                              const int32_t* ids, int T, int K, int E, float* dlogits, cudaStream_t st) {
+  router_bwd_vec_kernel<NV><<<(T + 7) / 8, 256, 0, st>>>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits);
+}
+
 }  // namespace moebwd
 
 using namespace moebwd;
@@ -103,8 +198,20 @@ extern "C" int moe_router_bwd(int mode, int renorm, const float* logits, const f
   if ((mode == MOE_ROUTER_SOFTMAX_OVER_TOPK || (mode == MOE_ROUTER_TOPK_OVER_SOFTMAX && renorm)) && !scores)
     return fail(MOE_ERR_INVALID, "moe_router_bwd: forward scores needed");
   if (T == 0) return MOE_OK;
-  router_bwd_kernel<<<(T + 7) / 8, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool aligned = ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(dlogits)) & 15) == 0;
+  if (E % 4 == 0 && E <= 1024 && K <= 32 && aligned) {  // one pass, the row in registers
+    const int nv = (E + 127) / 128;
+    switch (nv) {
+      case 1: router_vec_launch<1>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+      case 2: router_vec_launch<2>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+      case 3:
+      case 4: router_vec_launch<4>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+      default: router_vec_launch<8>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+    }
+  } else {
+    router_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits);
+  }
   count_launch();
   return cuda_check(cudaGetLastError(), "router_bwd");
 }

@@ -21,12 +21,30 @@ def _case(T, E, K, seed):
     return logits, ids, g
 
 
+def _scores(mode, logits, ids, renorm, E):
+    """The forward's scores of each row over its slots with ids in [0, E) (0 for the others)."""
+    s = np.zeros(ids.shape)
+    for t in range(ids.shape[0]):
+        ok = (ids[t] >= 0) & (ids[t] < E)
+        if ok.any():
+            s[t, ok] = orr.router_forward(mode, logits[t:t + 1], ids[t:t + 1, ok], renorm)[0]
+    return s
+
+
 @pytest.mark.parametrize("mode,renorm", [(0, False), (1, False), (1, True), (2, False)])
-@pytest.mark.parametrize("T,E,K", [(1000, 128, 8), (37, 40, 3), (5, 1024, 64)])
-def test_router_bwd(mode, renorm, T, E, K):
+@pytest.mark.parametrize("T,E,K,odd", [(1000, 128, 8, False), (37, 40, 3, False), (5, 1024, 64, False),
+                                        (300, 132, 32, True), (65, 520, 5, True), (40, 130, 4, True),
+                                        (50, 1028, 2, False)])
+def test_router_bwd(mode, renorm, T, E, K, odd):
+    """One-pass kernel (E a multiple of 4 up to 1024, K <= 32) and the general one (K = 64, E = 130,
+    E = 1028); `odd` rows repeat an id (the slots' gradients add) and carry ids outside [0, E)."""
     import moe_expert_layer_routing_gb300 as mb
     logits, ids, g = _case(T, E, K, seed=T + E)
-    scores = orr.router_forward(mode, logits, ids, renorm).astype(np.float32)
+    if odd:
+        ids[::3, K - 1] = ids[::3, 0]        # repeated id
+        ids[1::7, K - 1] = -1                # unused slot
+        ids[2::11, 0] = E                    # out of range
+    scores = _scores(mode, logits, ids, renorm, E).astype(np.float32)
     c = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
     got = mb.router_bwd(mode, c(ids), c(g), E, logits=c(logits), scores=c(scores), renorm=renorm)
     torch.cuda.synchronize()
