@@ -141,10 +141,21 @@ __global__ void __launch_bounds__(256) router_bwd_vec_kernel(int mode, int renor
     mx = warp_max(m);
     float sum = 0.f;
 #pragma unroll
-    for (int j = 0; j < NV; ++j)
-      sum += __expf(L[j].x - mx) + __expf(L[j].y - mx) + __expf(L[j].z - mx) + __expf(L[j].w - mx);
+    for (int j = 0; j < NV; ++j) {  // L now holds exp(l - max) (0 past E)
+      L[j] = make_float4(__expf(L[j].x - mx), __expf(L[j].y - mx), __expf(L[j].z - mx), __expf(L[j].w - mx));
+      sum += (L[j].x + L[j].y) + (L[j].z + L[j].w);
+    }
     inv = 1.f / warp_sum(sum);
-    const float pk = id >= 0 ? __expf(lt[id] - mx) * inv : 0.f;
+    // exp(l[id] - max) of this lane's slot, from the lane that holds column id in registers
+    const int src = (id & 127) >> 2, grp = id >> 7, cmp = id & 3;
+    float ek = 0.f;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const float ex = __shfl_sync(0xffffffffu, L[j].x, src), ey = __shfl_sync(0xffffffffu, L[j].y, src);
+      const float ez = __shfl_sync(0xffffffffu, L[j].z, src), ew = __shfl_sync(0xffffffffu, L[j].w, src);
+      if (grp == j) ek = cmp == 0 ? ex : cmp == 1 ? ey : cmp == 2 ? ez : ew;
+    }
+    const float pk = id >= 0 ? ek * inv : 0.f;
     const float S = warp_sum(pk), dsum = warp_sum(id >= 0 ? gk * sk : 0.f);
     wk = renorm ? (gk - dsum) / S : gk;  // dr of the slot
     dot = warp_sum(id >= 0 ? wk * pk : 0.f);
@@ -168,10 +179,10 @@ __global__ void __launch_bounds__(256) router_bwd_vec_kernel(int mode, int renor
     if (j * 128 + 4 * lane >= E) continue;
     float4 v = buf[j * 32 + lane];
     if (mode == MOE_ROUTER_TOPK_OVER_SOFTMAX) {
-      v.x = __expf(L[j].x - mx) * inv * (v.x - dot);
-      v.y = __expf(L[j].y - mx) * inv * (v.y - dot);
-      v.z = __expf(L[j].z - mx) * inv * (v.z - dot);
-      v.w = __expf(L[j].w - mx) * inv * (v.w - dot);
+      v.x = L[j].x * inv * (v.x - dot);
+      v.y = L[j].y * inv * (v.y - dot);
+      v.z = L[j].z * inv * (v.z - dot);
+      v.w = L[j].w * inv * (v.w - dot);
     }
     out[j * 32 + lane] = v;
   }
