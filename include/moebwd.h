@@ -189,7 +189,8 @@ typedef struct MoeBwdArgs {
   int affinity;       /* MOE_AFFINITY_ON_H or MOE_AFFINITY_ON_I */
   int fp8_act;        /* MXFP8: format of activation-side operands (dout, x, dh, a'), default E5M2 */
   int fp8_w;          /* MXFP8: format of the pre-quantised weights, default E4M3 */
-  int has_bias;       /* produce db1/db2 and add <dout_t, b2_e> to ds (BF16 precision only) */
+  int has_bias;       /* produce db1/db2 and add <dout_t, b2_e> to ds (from the unquantised values in
+                         both precisions; MXFP8 with down_proj_act_ckpt returns MOE_ERR_UNSUPPORTED) */
 
   const void* x;     /* (device) bf16 [T,H]  hidden_states */
   const void* dout;  /* (device) bf16 [T,H]  output_hidden_states_grad */

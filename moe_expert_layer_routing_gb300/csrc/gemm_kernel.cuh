@@ -210,8 +210,8 @@ __device__ __forceinline__ void tile_ckpt_origin(const GemmParams& p, const Tile
 // and the 16-byte row reads are both free of bank conflicts); lane l then handles
 // column l % NC, rows NC*(l / NC) .. +NC-1, so output row row0 + (l % NC) * rstride gets columns
 // p0..p0+31 from 32/NC lanes (bf16, or fp8 codes with one scale quantised along all 32: those lanes
-// combine their amax).  BF16 with `colsum`: the sum of the 32 rows of every output row (column) goes
-// to colsum[output row] as well (the bias gradient's share of these rows).
+// combine their amax).  With `colsum`: the sum of the 32 (unquantised) rows of every output row
+// (column) goes to colsum[output row] as well (the bias gradient's share of these rows).
 template <bool MX, int NC, int AF>
 __device__ __forceinline__ void store_transposed(float* buf, const float (&v)[NC], void* out, uint8_t* sf,
                                                  int64_t P, int64_t row0, int rstride, int64_t p0, int lane,
@@ -228,6 +228,14 @@ __device__ __forceinline__ void store_transposed(float* buf, const float (&v)[NC
     col[i + 1] = f.y;
     col[i + 2] = f.z;
     col[i + 3] = f.w;
+  }
+  if (colsum) {  // with biases: the sum of the 32 rows of this output row (column)
+    float cs = 0.f;
+#pragma unroll
+    for (int i = 0; i < NC; ++i) cs += col[i];
+#pragma unroll
+    for (int o = NC; o < 32; o <<= 1) cs += __shfl_xor_sync(0xffffffffu, cs, o);
+    if (rg == 0) colsum[row0 + (int64_t)c * rstride] = cs;
   }
   if constexpr (MX) {
     float am = 0.f;
@@ -252,14 +260,6 @@ __device__ __forceinline__ void store_transposed(float* buf, const float (&v)[NC
           (uint8_t)byte;
     }
   } else {
-    if (colsum) {
-      float cs = 0.f;
-#pragma unroll
-      for (int i = 0; i < NC; ++i) cs += col[i];
-#pragma unroll
-      for (int o = NC; o < 32; o <<= 1) cs += __shfl_xor_sync(0xffffffffu, cs, o);
-      if (rg == 0) colsum[row0 + (int64_t)c * rstride] = cs;
-    }
     uint16_t* dst = static_cast<uint16_t*>(out) + (row0 + (int64_t)c * rstride) * P + p0 + rg * NC;
     auto pk = [&](int j) { return pack_bf16x2(col[j], col[j + 1]); };
     if constexpr (NC == 16)  // one whole 32-byte sector
@@ -487,7 +487,7 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
   // SHARED_TBUF: the three transposes share the warp's buffer (each ends with the warp's reads done)
   constexpr int TB = SHARED_TBUF ? 0 : NC * kTransPitch;
   // db1 (BF16 with biases): this tile's and lane quarter's column sums of dh, in W1's layout
-  float* db1p = (!MX && p.db1_part) ? p.db1_part + ((prow >> 7) * 4 + (m >> 5)) * (2 * (int64_t)I) : nullptr;
+  float* db1p = p.db1_part ? p.db1_part + ((prow >> 7) * 4 + (m >> 5)) * (2 * (int64_t)I) : nullptr;
   store_transposed<MX, NC, AF>(tbuf, dg, p.dht, p.dht_sf, P, il ? 2 * c0 : c0, il ? 2 : 1, p0, lane, db1p);
   store_transposed<MX, NC, AF>(tbuf + TB, du, p.dht, p.dht_sf, P, il ? 2 * c0 + 1 : I + c0, il ? 2 : 1, p0, lane,
                                db1p);

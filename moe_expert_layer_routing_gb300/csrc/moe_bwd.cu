@@ -179,8 +179,8 @@ static Layout make_layout(const MoeBwdArgs& a) {
   b[R_TILE_ROW_SLOT] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, P);  // saved s*dout rows (pointers not read)
   // W2's scales re-tiled for 192-column G1 tiles: two atoms per tile
   if (mx && L.BN1 % 128) b[R_W2_SF_T] = (size_t)(E * I / L.BN1) * ((L.BN1 + 127) / 128) * (size_t)(H / 128) * 512;
-  // BF16 bias gradients: per-tile column sums from G1's transposes (four lane quarters) and prep (two halves)
-  if (a.has_bias && !mx) {
+  // bias gradients: per-tile column sums from G1's transposes (four lane quarters) and prep (two halves)
+  if (a.has_bias) {
     b[R_DB1_PART] = sizeof(float) * (size_t)(P / kTileM) * 4 * (size_t)(2 * I);
     b[R_DB2_PART] = sizeof(float) * (size_t)(P / kTileM) * 2 * (size_t)H;
   }
@@ -218,7 +218,8 @@ static int check_args(const MoeBwdArgs* a, bool need_ptrs) {
   if (mx && ((a->fp8_act != MOE_FP8_E4M3 && a->fp8_act != MOE_FP8_E5M2) ||
              (a->fp8_w != MOE_FP8_E4M3 && a->fp8_w != MOE_FP8_E5M2)))
     return fail(MOE_ERR_INVALID, "moe_bwd: bad fp8 format");
-  if (mx && a->has_bias) return fail(MOE_ERR_UNSUPPORTED, "moe_bwd: bias gradients are implemented for BF16 only");
+  if (mx && a->has_bias && a->down_proj_act_ckpt)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_bwd: MXFP8 bias gradients with a saved down_proj_act_ckpt are not implemented");
   if (a->act_src != MOE_ACT_CHECKPOINT && a->act_src != MOE_ACT_RECOMPUTE)
     return fail(MOE_ERR_INVALID, "moe_bwd: bad act_src");
   if (a->glu != MOE_GLU_SWIGLU && a->glu != MOE_GLU_GEGLU) return fail(MOE_ERR_INVALID, "moe_bwd: bad glu");
@@ -491,7 +492,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   pa.x_g = rec ? reg<void>(L, ws, R_X_G) : nullptr;
   pa.x_g_sf = rec ? reg<uint8_t>(L, ws, R_X_G_SF) : nullptr;
   pa.skip_dout_t = a.down_proj_act_ckpt != nullptr;
-  pa.db2_part = (a.has_bias && !mx && !pa.skip_dout_t) ? reg<float>(L, ws, R_DB2_PART) : nullptr;
+  pa.db2_part = (a.has_bias && !pa.skip_dout_t) ? reg<float>(L, ws, R_DB2_PART) : nullptr;
   if ((rc = launch_prep(pa, st))) return rc;
   if (L.gather && mx &&  // the rows G1 gathers: dout quantised once per token (the scales come from prep)
       (rc = launch_quant_rowwise(pa.dout, a.T, a.T, H, H, nullptr, a.fp8_act, reg<uint8_t>(L, ws, R_DOUT_Q), nullptr,

@@ -131,6 +131,9 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
           // the tile's four 32-row groups have adjacent scale bytes (k = g in the tiled layout, the
           // tile's first row a multiple of 128): one 32-bit store per column
           uint32_t sfw = 0u;
+          // with biases: this column's sums of s*dout over the tile's row halves (db2's partials)
+          const bool db2 = BIAS && which == 0 && a.db2_part != nullptr;
+          float cs[2] = {0.f, 0.f};
 #pragma unroll 2
           for (int g = 0; g < 4; ++g) {
             float c32[32];
@@ -140,6 +143,7 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
               float x = bf16_bits_to_float(st[row * kPrepTilePitch + h]);
               if (SCALE_T && which == 0) x *= s_s[row];
               c32[j] = x;
+              if (db2) cs[g >> 1] = fmaf(x, SCALE_T ? 1.f : s_s[row], cs[g >> 1]);
             }
             const int64_t ocol = prow0 + g * 32;
             uint32_t w[8];
@@ -148,6 +152,10 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
             sfw |= byte << (8 * g);
           }
           *reinterpret_cast<uint32_t*>(outsf + sf_tiled_offset(orow, prow0, P)) = sfw;
+          if (db2) {
+            a.db2_part[((int64_t)tile * 2 + 0) * H + orow] = cs[0];
+            a.db2_part[((int64_t)tile * 2 + 1) * H + orow] = cs[1];
+          }
         }
       } else {
         const int cp = tid & 127;

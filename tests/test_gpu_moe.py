@@ -50,6 +50,18 @@ def test_bf16_bias_ragged(affinity):
     _check(inp, BF16_TOL)
 
 
+@pytest.mark.parametrize("affinity", [AFFINITY_ON_I, AFFINITY_ON_H])
+@pytest.mark.parametrize("I", [384, 256])
+def test_mxfp8_bias_ragged(affinity, I):
+    """MXFP8 with biases: db1 and db2 (sums of the unquantised dh and s*dout) and the <dout, b2> term of
+    ds, over ragged experts (an empty one, a single-row one, a hot one), 192- and 128-column G1 tiles."""
+    cfg = small_moe("mx_bias", T=300, H=256, I=I, E=8, K=3, B=256, seed=24, bias=True, precision=PREC_MXFP8,
+                    affinity=affinity)
+    inp = with_ids(make_moe_inputs(cfg), _ragged_ids(300, 3, 8, seed=6, hot=2))
+    errs = _check(inp, MXFP8_TOL)
+    assert {"db1", "db2"} <= set(errs)
+
+
 def test_bf16_single_expert_top1():
     cfg = small_moe("dense_like", T=200, H=384, I=128, E=1, K=1, B=128, seed=22)
     _check(make_moe_inputs(cfg), BF16_TOL)
@@ -239,7 +251,7 @@ def test_accumulate_adds_weight_and_bias_gradients(mx):
     from helpers import to_device
     if mx:
         cfg = small_moe("acc_mx", T=300, H=256, I=256, E=4, K=2, B=256, seed=41, precision=PREC_MXFP8,
-                        affinity=AFFINITY_ON_I)
+                        affinity=AFFINITY_ON_I, bias=True)
     else:
         cfg = small_moe("acc_bf16", T=300, H=256, I=384, E=6, K=2, B=128, seed=42, bias=True)
     inp = make_moe_inputs(cfg)

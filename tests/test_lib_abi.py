@@ -127,3 +127,12 @@ def test_options_defaults_and_validation(lib):
     mb.set_option("G1_TILE_N", None)
     assert mb.get_option("G1_TILE_N") == 0
     assert n192 > 0 and n128 > 0 and n192 != n128   # the tile width moves the ds partials' region
+
+
+def test_mxfp8_bias_with_saved_scaled_dout_is_refused(lib):
+    import moe_expert_layer_routing_gb300 as mb
+    a = mb.MoeBwdArgs(T=256, H=128, I=256, E=4, K=2, block_size=128, precision=1, has_bias=1, affinity=0)
+    assert lib.moe_bwd_workspace_size(ctypes.byref(a)) > 0          # MXFP8 with biases is supported
+    a.down_proj_act_ckpt = 4096                                     # (pointer value only checked for presence)
+    assert lib.moe_bwd_workspace_size(ctypes.byref(a)) == 0
+    assert b"down_proj_act_ckpt" in lib.moe_last_error()
