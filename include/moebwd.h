@@ -406,6 +406,9 @@ enum {
                                 or for MXFP8 from dout quantised once per token, MOE_WS_DOUT_Q) with 16-byte
                                 asynchronous copies -- same results, less memory, but slower (the copies of
                                 one producer warp keep fewer bytes in flight than tensor-map loads) */
+  MOE_OPT_PDL,               /* 1 (default): the kernels of a call are launched with programmatic dependent
+                                launch (each may be scheduled while the previous one finishes and waits on
+                                the device for its results); 0: plain stream order */
   MOE_NUM_OPTIONS
 };
 /* Set an option; value -1 restores its default.  MOE_ERR_INVALID for an unknown option or value. */

@@ -675,6 +675,10 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the prologue above (barriers, TMEM, tensor-map prefetch) overlaps the previous kernel's tail;
+  // nothing written by earlier work is read before this point
+  pdl_wait();
+  pdl_trigger();
   const int total = gemm_total_tiles(p);
   // Dynamic schedule: the producer claims tiles from a global counter (heaviest experts first in
   // the K-grouped order) and publishes each index, then -1, through the ring.
@@ -1089,11 +1093,9 @@ int gemm_launch_instance(const GemmParams& p, const void* tmA, const void* tmB, 
   auto kern = gemm_kernel<MX, BN, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(gemm)");
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(*static_cast<const CUtensorMap*>(tmA),
-                                        *static_cast<const CUtensorMap*>(tmB),
-                                        *static_cast<const CUtensorMap*>(tmC), p);
-  count_launch();
-  return cuda_check(cudaGetLastError(), "gemm launch");
+  return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, st, "gemm launch",
+                    *static_cast<const CUtensorMap*>(tmA), *static_cast<const CUtensorMap*>(tmB),
+                    *static_cast<const CUtensorMap*>(tmC), p);
 }
 
 }  // namespace moebwd

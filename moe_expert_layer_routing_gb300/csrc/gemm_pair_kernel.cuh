@@ -206,6 +206,10 @@ __global__ void __launch_bounds__(PairCfg<MX, BN, EPI>::THREADS, 1)
   cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the prologue above (barriers, TMEM, tensor-map prefetch) overlaps the previous kernel's tail;
+  // nothing written by earlier work is read before this point
+  pdl_wait();
+  pdl_trigger();
   const int total = pair_total_tiles(p);
 
   if (warp == 0) {
@@ -494,11 +498,13 @@ int gemm_pair_launch_instance(const GemmParams& p, const void* tmA, const void* 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(gemm pair)");
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = st;
@@ -511,6 +517,7 @@ int gemm_pair_launch_instance(const GemmParams& p, const void* tmA, const void* 
   if (clusters <= 0) return fail(MOE_ERR_CUDA, "gemm pair kernel: no cluster of two fits on this device");
   const int pairs = max_pairs < clusters ? max_pairs : clusters;
   cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.numAttrs = option(MOE_OPT_PDL) ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, kern, *static_cast<const CUtensorMap*>(tmA), *static_cast<const CUtensorMap*>(tmB),
                          *static_cast<const CUtensorMap*>(tmC), *static_cast<const CUtensorMap*>(tmSFA),
                          *static_cast<const CUtensorMap*>(tmSFB), p);

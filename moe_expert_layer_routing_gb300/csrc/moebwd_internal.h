@@ -27,6 +27,35 @@ size_t align_up(size_t v, size_t a);
 void count_launch();   // one kernel launched by this library
 int64_t option(int opt);  // current value of a MOE_OPT_* option
 
+// Programmatic dependent launch, device side: wait until the grids this one depends on have completed
+// and their memory is visible (a no-op without such a dependency); allow the dependent grid to be
+// scheduled (its CTAs then wait in their own pdl_wait).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch with programmatic dependent launch (unless MOE_OPT_PDL is 0): the kernel's CTAs may be
+// scheduled while the previous kernel on the stream finishes; every kernel launched this way calls
+// pdl_wait() before it touches memory that earlier work wrote, and pdl_trigger() to let the next
+// kernel be scheduled early in turn.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, const char* what,
+               Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = option(MOE_OPT_PDL) ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  count_launch();
+  if (e != cudaSuccess) return cuda_check(e, what);
+  return cuda_check(cudaGetLastError(), what);
+}
+
 // 2D tensor map over a row-major [rows, cols] matrix of `elem_bytes`-byte elements with the given
 // row pitch, box [box_rows, box_cols], 128-byte swizzle (or none).  Returns false on failure (message set).
 bool make_tmap_2d(void* out_tmap /* CUtensorMap* */, const void* base, int elem_bytes, uint64_t rows,

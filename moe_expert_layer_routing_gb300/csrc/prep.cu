@@ -33,6 +33,8 @@ constexpr int kPrepBatch = 8;
 
 template <bool MX, bool SCALE_T, bool BIAS, int AF>
 __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   if ((int)blockIdx.x >= *a.num_tiles) return;
   const int tile = a.tile_order ? a.tile_order[blockIdx.x] : (int)blockIdx.x;
   extern __shared__ uint4 prep_smem[];
@@ -224,9 +226,7 @@ static int prep_launch(const PrepArgs& a, int grid, cudaStream_t st) {
                                           : prep_kernel<MX, SCALE_T, BIAS, MOE_FP8_E4M3>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e != cudaSuccess) return cuda_check(e, "prep attribute");
-  k<<<grid, 256, kPrepSmem, st>>>(a);
-  count_launch();
-  return cuda_check(cudaGetLastError(), "prep");
+  return launch_pdl(k, dim3(grid), dim3(256), kPrepSmem, st, "prep", a);
 }
 
 int launch_prep(const PrepArgs& a, cudaStream_t st) {
@@ -258,6 +258,8 @@ __global__ void __launch_bounds__(256) apt_from_ckpt_kernel(const uint16_t* __re
                                                             const int32_t* __restrict__ block_offsets,
                                                             const int32_t* __restrict__ tile_row_flat,
                                                             const float* __restrict__ s, void* out, uint8_t* out_sf) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   const int tile = blockIdx.x;
   if (tile >= *num_tiles) return;
   const int i = blockIdx.y * 64 + (threadIdx.x >> 2);
@@ -331,6 +333,8 @@ __global__ void tile_row_slot_kernel(int64_t P, int B, const int32_t* __restrict
                                      const int32_t* __restrict__ tile_expert, const int32_t* __restrict__ tile_offsets,
                                      const int32_t* __restrict__ block_offsets,
                                      const int32_t* __restrict__ tile_row_flat, int32_t* __restrict__ slot) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (p >= P) return;
   const int tile = (int)(p / 128);
@@ -358,6 +362,8 @@ int launch_tile_row_slot(int64_t P, int B, const int32_t* num_tiles, const int32
 // contiguous in both layouts, so each thread moves one 32-bit word.
 __global__ void __launch_bounds__(256) sf_retile_kernel(const uint32_t* __restrict__ src, int64_t R, int64_t C,
                                                         int bn, int atoms, uint32_t* __restrict__ dst) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   const int64_t ktiles = C / 128;
   const int64_t words = (R / bn) * atoms * ktiles * 128;
   const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -382,10 +388,8 @@ int launch_sf_retile(const uint8_t* src, int64_t R, int64_t C, int bn, uint8_t* 
   const int atoms = (bn + 127) / 128;
   const int64_t words = (R / bn) * atoms * (C / 128) * 128;
   if (words == 0) return MOE_OK;
-  sf_retile_kernel<<<(unsigned)((words + 255) / 256), 256, 0, st>>>(reinterpret_cast<const uint32_t*>(src), R, C,
-                                                                    bn, atoms, reinterpret_cast<uint32_t*>(dst));
-  count_launch();
-  return cuda_check(cudaGetLastError(), "sf_retile");
+  return launch_pdl(sf_retile_kernel, dim3((unsigned)((words + 255) / 256)), dim3(256), 0, st, "sf_retile",
+                    reinterpret_cast<const uint32_t*>(src), R, C, bn, atoms, reinterpret_cast<uint32_t*>(dst));
 }
 
 // ------------------------------------------------------------------------------------------
@@ -398,6 +402,8 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint16_t* __re
                                                             const int32_t* __restrict__ row_index, int fmt,
                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                                             int tiled) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   const int64_t vpr = cols / 8;
   const int64_t total = rows * vpr;
   const int lane = threadIdx.x & 31;
@@ -442,6 +448,8 @@ __global__ void __launch_bounds__(256) quant_colwise_kernel(const uint16_t* __re
                                                             const int32_t* __restrict__ row_index, int fmt,
                                                             void* __restrict__ q, uint8_t* __restrict__ sf,
                                                             int tiled) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   __shared__ uint16_t tile[128 * kPrepPitch];
   const int tid = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.x * 128;
@@ -492,9 +500,8 @@ int launch_quant_rowwise(const uint16_t* in, int64_t src_rows, int64_t rows, int
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = (int64_t)device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
-  quant_rowwise_kernel<<<(unsigned)blocks, 256, 0, st>>>(in, src_rows, rows, cols, ld, row_index, fmt, q, sf, tiled);
-  count_launch();
-  return cuda_check(cudaGetLastError(), "quant_rowwise");
+  return launch_pdl(quant_rowwise_kernel, dim3((unsigned)blocks), dim3(256), 0, st, "quant_rowwise", in, src_rows, rows,
+                    cols, ld, row_index, fmt, q, sf, tiled);
 }
 
 int launch_quant_colwise(const uint16_t* in, int64_t src_rows, int64_t rows, int64_t cols, int64_t ld,

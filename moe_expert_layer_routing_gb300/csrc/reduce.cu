@@ -15,6 +15,8 @@ namespace moebwd {
 __global__ void __launch_bounds__(256) dx_scatter_sum_kernel(const uint16_t* __restrict__ dx_exp,
                                                              const int32_t* __restrict__ flat_tile_row, int K, int H,
                                                              uint16_t* __restrict__ dx) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   const int64_t t = blockIdx.x;
   __shared__ int32_t rows[64];
   if (threadIdx.x < K) rows[threadIdx.x] = flat_tile_row[t * K + threadIdx.x];
@@ -42,13 +44,13 @@ int launch_dx_scatter_sum(const uint16_t* dx_exp, const int32_t* flat_tile_row, 
                           cudaStream_t st) {
   if (T == 0) return MOE_OK;
   if (K > 64) return fail(MOE_ERR_UNSUPPORTED, "top-K above 64");
-  dx_scatter_sum_kernel<<<T, 256, 0, st>>>(dx_exp, flat_tile_row, K, H, dx);
-  count_launch();
-  return cuda_check(cudaGetLastError(), "dx_scatter_sum");
+  return launch_pdl(dx_scatter_sum_kernel, dim3(T), dim3(256), 0, st, "dx_scatter_sum", dx_exp, flat_tile_row, K, H, dx);
 }
 
 __global__ void ds_finalize_kernel(const float* __restrict__ ds_part, int nparts, const float* __restrict__ ds_bias,
                                    const int32_t* __restrict__ flat_tile_row, int64_t TK, float* __restrict__ ds) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   const int64_t f = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (f >= TK) return;
   const int p = flat_tile_row[f];
@@ -63,9 +65,8 @@ __global__ void ds_finalize_kernel(const float* __restrict__ ds_part, int nparts
 int launch_ds_finalize(const float* ds_part, int nparts, const float* ds_bias, const int32_t* flat_tile_row,
                        int64_t TK, float* ds, cudaStream_t st) {
   if (TK == 0) return MOE_OK;
-  ds_finalize_kernel<<<(unsigned)((TK + 255) / 256), 256, 0, st>>>(ds_part, nparts, ds_bias, flat_tile_row, TK, ds);
-  count_launch();
-  return cuda_check(cudaGetLastError(), "ds_finalize");
+  return launch_pdl(ds_finalize_kernel, dim3((unsigned)((TK + 255) / 256)), dim3(256), 0, st, "ds_finalize", ds_part,
+                    nparts, ds_bias, flat_tile_row, TK, ds);
 }
 
 __global__ void __launch_bounds__(256) segment_rowsum_kernel(const uint16_t* __restrict__ buf, int64_t ld, int R,
@@ -73,6 +74,8 @@ __global__ void __launch_bounds__(256) segment_rowsum_kernel(const uint16_t* __r
                                                              const float* __restrict__ w,
                                                              const int32_t* __restrict__ tile_row_flat,
                                                              float* __restrict__ out, int accumulate) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   const int e = blockIdx.y;
   const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -131,6 +134,8 @@ __device__ __forceinline__ float bias_sum(const float* __restrict__ part, int64_
 __global__ void __launch_bounds__(256) bias_parts_reduce_kernel(BiasJob j0, BiasJob j1,
                                                                 const int32_t* __restrict__ tile_offsets,
                                                                 int accumulate) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   const int e = blockIdx.y;
   const bool second = blockIdx.x >= j0.blocks;
   const BiasJob& j = second ? j1 : j0;
@@ -157,9 +162,8 @@ int launch_bias_parts_reduce(const float* part, int parts, int64_t F, const int3
   BiasJob j0{part, F, out, parts, (unsigned)((F + 255) / 256)};
   BiasJob j1{part2, part2 ? F2 : 0, out2, parts2, part2 ? (unsigned)((F2 + 255) / 256) : 0u};
   dim3 grid(j0.blocks + j1.blocks, (unsigned)E);
-  bias_parts_reduce_kernel<<<grid, 256, 0, st>>>(j0, j1, tile_offsets, accumulate);
-  count_launch();
-  return cuda_check(cudaGetLastError(), "bias_parts_reduce");
+  return launch_pdl(bias_parts_reduce_kernel, grid, dim3(256), 0, st, "bias_parts_reduce", j0, j1, tile_offsets,
+                    accumulate);
 }
 
 int launch_segment_rowsum(const uint16_t* buf, int64_t ld, int R, const int32_t* tile_offsets, int E, const float* w,
@@ -175,6 +179,8 @@ int launch_segment_rowsum(const uint16_t* buf, int64_t ld, int R, const int32_t*
 // token did not select the expert; repeated selections add).  One thread per token, in slot order.
 __global__ void ds_masked_kernel(const float* __restrict__ ds, const int32_t* __restrict__ ids,
                                  const int32_t* __restrict__ num_valid, int T, int K, int E, float* __restrict__ out) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   if (num_valid && t >= *num_valid) return;

@@ -43,6 +43,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_count_kernel(const int32_
                                                                     const int32_t* __restrict__ num_valid,
                                                                     int32_t* __restrict__ chunk_counts,
                                                                     int32_t* status, RouteFill fill) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   extern __shared__ int32_t hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   {
@@ -113,6 +115,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int nchunks, int E, in
                                                           int32_t* block_to_expert, int32_t* tile_expert,
                                                           int32_t* scalars, int32_t* num_blocks_out,
                                                           int32_t* pair_offsets) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   __shared__ int32_t cnt[kMaxExperts + 1];
   __shared__ int32_t rows[kMaxExperts + 1];
   __shared__ int32_t blks[kMaxExperts + 1];
@@ -170,6 +174,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter_kernel(
     const int32_t* __restrict__ tile_offsets, int32_t* x_gather_idx, int32_t* s_scatter_idx, int32_t* s_reverse,
     int32_t* token_position_to_id, int32_t* tile_row_flat, int32_t* flat_tile_row,
     const int32_t* __restrict__ num_valid) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   extern __shared__ int32_t sm[];
   int32_t* wbase = sm;                       // [warps][E]
   int32_t* eo = wbase + kRouteWarps * E;     // [E]
@@ -243,6 +249,8 @@ constexpr int kOrderBuckets = 4096;
 __global__ void __launch_bounds__(1024) tile_order_kernel(const int32_t* __restrict__ tile_row_flat,
                                                           const int32_t* __restrict__ num_tiles, int T, int K,
                                                           int32_t* __restrict__ order) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   __shared__ int32_t cnt[kOrderBuckets];
   __shared__ int32_t wt[33];
   const int n = *num_tiles;
@@ -286,6 +294,8 @@ __global__ void __launch_bounds__(1024) route_in_scan_kernel(
     int64_t TK, const int32_t* __restrict__ num_valid, int K, int E, int B, int64_t Nb, int32_t* expert_offsets,
     int32_t* block_offsets, int32_t* tile_offsets, int32_t* expert_order, int32_t* tile_expert, int32_t* scalars,
     int32_t* pair_offsets, int32_t* status) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   __shared__ int32_t cnt[kMaxExperts + 1];
   __shared__ int32_t tiles[kMaxExperts + 1];
   __shared__ int32_t prs[kMaxExperts + 1];
@@ -347,6 +357,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_in_rows_kernel(
     int64_t TK, const int32_t* __restrict__ num_valid, int K, int E, int B, const int32_t* __restrict__ expert_offsets,
     const int32_t* __restrict__ block_offsets, const int32_t* __restrict__ tile_offsets, int32_t* tile_row_flat,
     int32_t* flat_tile_row, int32_t* status) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   extern __shared__ int32_t eo[];  // [E+1] checked copy of the expert offsets
   for (int e = threadIdx.x; e <= E; e += blockDim.x) eo[e] = expert_offsets[e];
   __syncthreads();
@@ -377,6 +389,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_in_cover_kernel(const int
                                                                        const int32_t* __restrict__ num_valid, int K,
                                                                        int E, const int32_t* __restrict__ flat_tile_row,
                                                                        int32_t* status) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   const int64_t live = live_slots(num_valid, TK, K);
   int miss = 0, badid = 0;
   for (int64_t f = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; f < live; f += (int64_t)gridDim.x * blockDim.x) {
@@ -430,9 +444,7 @@ int launch_route_meta_in(const RouteMetaIn& in, const int32_t* ids, int T, int K
 int launch_tile_order(const int32_t* tile_row_flat, const int32_t* num_tiles, int T, int K, int32_t* order,
                       cudaStream_t st) {
   if (T <= 0) return MOE_OK;
-  tile_order_kernel<<<1, 1024, 0, st>>>(tile_row_flat, num_tiles, T, K, order);
-  count_launch();
-  return cuda_check(cudaGetLastError(), "tile_order");
+  return launch_pdl(tile_order_kernel, dim3(1), dim3(1024), 0, st, "tile_order", tile_row_flat, num_tiles, T, K, order);
 }
 
 int launch_route_meta(const int32_t* ids, int T, int K, int E, int B, int64_t Nb, int64_t P, const RouteBufs& r,
@@ -448,27 +460,25 @@ int launch_route_meta(const int32_t* ids, int T, int K, int E, int B, int64_t Nb
   fill.neg[3] = r.tile_expert;          fill.n[3] = P / kTileM + 1;
   fill.zero = r.zero_counters;          fill.nzero = r.zero_counters ? r.nzero : 0;
   const int nch = route_nchunks(TK);
-  route_count_kernel<<<nch > 0 ? nch : 1, kRouteThreads, sizeof(int32_t) * E, st>>>(ids, TK, K, E, r.num_valid,
-                                                                                   r.chunk_counts, r.status, fill);
-  count_launch();
-  if ((rc = cuda_check(cudaGetLastError(), "route_count"))) return rc;
-  route_scan_kernel<<<1, 1024, 0, st>>>(nch, E, B, r.chunk_counts, r.expert_offsets, r.block_offsets, r.tile_offsets,
-                                        r.expert_order, r.block_to_expert, r.tile_expert, r.scalars, r.num_blocks_out,
-                                        r.pair_offsets);
-  count_launch();
-  if ((rc = cuda_check(cudaGetLastError(), "route_scan"))) return rc;
+  if ((rc = launch_pdl(route_count_kernel, dim3(nch > 0 ? nch : 1), dim3(kRouteThreads), sizeof(int32_t) * E, st,
+                       "route_count", ids, TK, K, E, r.num_valid, r.chunk_counts, r.status, fill)))
+    return rc;
+  if ((rc = launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, st, "route_scan", nch, E, B, r.chunk_counts,
+                       r.expert_offsets, r.block_offsets, r.tile_offsets, r.expert_order, r.block_to_expert,
+                       r.tile_expert, r.scalars, r.num_blocks_out, r.pair_offsets)))
+    return rc;
   if (nch > 0) {
     const size_t smem = sizeof(int32_t) * (size_t)(kRouteWarps * E + 3 * E);
     if (smem > 48 * 1024) {
       cudaError_t e = cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if ((rc = cuda_check(e, "route_scatter attribute"))) return rc;
     }
-    route_scatter_kernel<<<nch, kRouteThreads, smem, st>>>(ids, TK, K, E, B, r.chunk_counts, r.expert_offsets,
-                                                           r.block_offsets, r.tile_offsets, r.x_gather_idx,
-                                                           r.s_scatter_idx, r.s_reverse, r.token_position_to_id,
-                                                           r.tile_row_flat, r.flat_tile_row, r.num_valid);
-    count_launch();
-    if ((rc = cuda_check(cudaGetLastError(), "route_scatter"))) return rc;
+    if ((rc = launch_pdl(route_scatter_kernel, dim3(nch), dim3(kRouteThreads), smem, st, "route_scatter", ids, TK, K,
+                         E, B, (const int32_t*)r.chunk_counts, (const int32_t*)r.expert_offsets,
+                         (const int32_t*)r.block_offsets, (const int32_t*)r.tile_offsets, r.x_gather_idx,
+                         r.s_scatter_idx, r.s_reverse, r.token_position_to_id, r.tile_row_flat, r.flat_tile_row,
+                         r.num_valid)))
+      return rc;
   }
   return MOE_OK;
 }

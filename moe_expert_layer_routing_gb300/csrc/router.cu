@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(int mode, int renorm, c
                                                          const float* __restrict__ scores,
                                                          const float* __restrict__ g, const int32_t* __restrict__ ids,
                                                          int T, int K, int E, float* __restrict__ dl) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -108,6 +110,8 @@ __global__ void __launch_bounds__(256) router_bwd_vec_kernel(int mode, int renor
                                                              const float* __restrict__ g,
                                                              const int32_t* __restrict__ ids, int T, int K, int E,
                                                              float* __restrict__ dl) {
+  pdl_wait();  // results of the previous kernel on the stream
+  pdl_trigger();
   __shared__ float4 sbuf[8][NV * 32];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + w;

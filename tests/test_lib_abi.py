@@ -110,7 +110,7 @@ def test_options_defaults_and_validation(lib):
     assert mb.get_option("WAIT_LIMIT_NS") == 2_000_000_000
     assert mb.get_option("PAIR_GEMMS") == 1 and mb.get_option("PAIR_TILE_N") == 256
     assert mb.get_option("G1_TILE_N") == 0 and mb.get_option("PREP_TILE_ORDER") == 1
-    assert mb.get_option("G1_GATHER") == 0
+    assert mb.get_option("G1_GATHER") == 0 and mb.get_option("PDL") == 1
     assert lib.moe_set_option(99, 1) == -1 and b"unknown option" in lib.moe_last_error()
     assert lib.moe_get_option(99) == -1
     for name, bad in (("WAIT_LIMIT_NS", 0), ("PAIR_GEMMS", 3), ("PAIR_TILE_N", 192), ("G1_TILE_N", 64),
