@@ -232,15 +232,13 @@ __device__ __forceinline__ void store_transposed(float* buf, const float (&v)[NC
   if (colsum) {  // with biases: the sum of the 32 rows of this output row (column)
     float cs = 0.f;
 #pragma unroll
-    for (int i = 0; i < NC; ++i) cs += col[i];
+    for (int i = 0; i < NC; ++i) cs += col[i];  // in order: the same sums as before
 #pragma unroll
     for (int o = NC; o < 32; o <<= 1) cs += __shfl_xor_sync(0xffffffffu, cs, o);
     if (rg == 0) colsum[row0 + (int64_t)c * rstride] = cs;
   }
   if constexpr (MX) {
-    float am = 0.f;
-#pragma unroll
-    for (int i = 0; i < NC; ++i) am = fmaxf(am, fabsf(col[i]));
+    float am = amax_tree<NC>(col);
 #pragma unroll
     for (int o = NC; o < 32; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
     const uint32_t byte = e8m0_byte(__float_as_uint(am), AF);
@@ -381,6 +379,7 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
     }
   } else {
     const uint64_t sv2 = f2_splat(sv);
+    const uint64_t sa2 = f2_splat(p.affinity_on_i ? sv : 1.f);  // a' = s a (affinity on I) or a (x 1, exact)
     uint64_t DS = f2_splat(0.f);
 #pragma unroll
     for (int jj = 0; jj < NC; jj += 2) {
@@ -390,7 +389,7 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
       const uint64_t DA = f2_mul(sv2, V);
       f2_unpack(f2_mul(DA, f2_pack(dg[jj], dg[jj + 1])), dg[jj], dg[jj + 1]);
       f2_unpack(f2_mul(DA, f2_pack(du[jj], du[jj + 1])), du[jj], du[jj + 1]);
-      if (p.affinity_on_i) f2_unpack(f2_mul(sv2, A), ap[jj], ap[jj + 1]);
+      f2_unpack(f2_mul(sa2, A), ap[jj], ap[jj + 1]);
     }
     float d0, d1;
     f2_unpack(DS, d0, d1);
@@ -404,9 +403,7 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
     // named barriers)
     group_bar<32 * SUBS>(bar_id);
     if constexpr (MX) {
-      float am = 0.f;
-#pragma unroll
-      for (int jj = 0; jj < NC; ++jj) am = fmaxf(am, fmaxf(fabsf(dg[jj]), fabsf(du[jj])));
+      const float am = fmaxf(amax_tree<NC>(dg), amax_tree<NC>(du));
       const uint32_t byte = e8m0_byte(__float_as_uint(am), AF);
       const float inv = e8m0_inv_scale(byte);
       uint32_t q[NC / 2];
@@ -428,12 +425,7 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
                       pk(8 * w + 5), pk(8 * w + 6), pk(8 * w + 7));
     }
   } else if constexpr (MX) {
-    float amg = 0.f, amu = 0.f;
-#pragma unroll
-    for (int jj = 0; jj < NC; ++jj) {
-      amg = fmaxf(amg, fabsf(dg[jj]));
-      amu = fmaxf(amu, fabsf(du[jj]));
-    }
+    float amg = amax_tree<NC>(dg), amu = amax_tree<NC>(du);
     xchg[(sub * 2 + 0) * 32 + lane] = amg;
     xchg[(sub * 2 + 1) * 32 + lane] = amu;
     group_bar<32 * SUBS>(bar_id);

@@ -27,6 +27,18 @@ __device__ __forceinline__ int64_t sf_tiled_offset(int64_t r, int64_t c, int64_t
   return ((r >> 7) * (C >> 7) + (c >> 7)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + ((c >> 5) & 3);
 }
 
+// max |v[i]| over N values (N a power of two) as a tree of pairwise maxima: log2(N) dependent steps
+// instead of N (the maximum is exact in any order).
+template <int N>
+__device__ __forceinline__ float amax_tree(const float* v) {
+  static_assert((N & (N - 1)) == 0, "power of two");
+  if constexpr (N == 1) {
+    return fabsf(v[0]);
+  } else {
+    return fmaxf(amax_tree<N / 2>(v), amax_tree<N / 2>(v + N / 2));
+  }
+}
+
 // One 32-byte global store (a whole L2 sector); p must be 32-byte aligned.
 __device__ __forceinline__ void st_global_32b(void* p, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
                                               uint32_t w4, uint32_t w5, uint32_t w6, uint32_t w7) {
@@ -128,9 +140,7 @@ __device__ __forceinline__ uint32_t fp8x4_scaled(float a, float b, float c, floa
 // Quantise 32 values of one group into 32 FP8 codes (packed little-endian into 8 words) and
 // return the scale byte.
 __device__ __forceinline__ uint32_t quantize_group32(const float (&v)[32], int fmt, uint32_t (&w)[8]) {
-  float am = 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) am = fmaxf(am, fabsf(v[j]));
+  const float am = amax_tree<32>(v);
   const uint32_t byte = e8m0_byte(__float_as_uint(am), fmt);
   const float inv = e8m0_inv_scale(byte);
 #pragma unroll
@@ -142,9 +152,7 @@ __device__ __forceinline__ uint32_t quantize_group32(const float (&v)[32], int f
 // quantize_group32 with the format fixed at compile time.
 template <int FMT>
 __device__ __forceinline__ uint32_t quantize_group32_t(const float (&v)[32], uint32_t (&w)[8]) {
-  float am = 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) am = fmaxf(am, fabsf(v[j]));
+  const float am = amax_tree<32>(v);
   const uint32_t byte = e8m0_byte(__float_as_uint(am), FMT);
   const uint64_t inv2 = f2_splat(e8m0_inv_scale(byte));
 #pragma unroll

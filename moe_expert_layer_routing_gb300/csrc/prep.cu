@@ -100,9 +100,7 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
           }
         }
         if constexpr (MX) {
-          float am = 0.f;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(d8[j]));
+          float am = amax_tree<8>(d8);
           am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
           am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
           if (!colok) continue;
@@ -424,9 +422,7 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint16_t* __re
       d[2 * j] = __uint_as_float(w[j] << 16);
       d[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
     }
-    float am = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(d[j]));
+    float am = amax_tree<8>(d);
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
     if (!in_range) continue;
