@@ -47,18 +47,23 @@ struct GemmCfg {
   // exchange of each quarter (double-buffered by chunk parity) and a double-buffered checkpoint chunk
   // (gate and up, 32 features x 128 tile rows each) refilled by the loader warp's TMA copies.
   static constexpr int G1_NC = 32 / kG1Subs;
+  // dSwiGLU epilogues; kEpiDSwiGLU2 runs two groups of 4 * kG1Subs warps, group g taking the chunks
+  // c = g, g + 2, ... of every tile, with three checkpoint buffers (each group one chunk ahead)
+  static constexpr bool DSW = EPI == kEpiDSwiGLU || EPI == kEpiDSwiGLU2;
+  static constexpr int G1_GROUPS = EPI == kEpiDSwiGLU2 ? 2 : 1;
+  static constexpr int CK_BUFS = G1_GROUPS == 2 ? 3 : 2;
   // fp32 transpose buffers per warp: MXFP8, and BF16 at 256 columns, share one between the three
   // transposes (the shared memory saved buys a pipeline stage); BF16 at 128 columns has stages enough
   // and keeps three, which overlap
   static constexpr int G1_TBUFS = (MX || BN == 256) ? 1 : 3;
-  static constexpr int EPI_WARP_BYTES = (EPI == kEpiDSwiGLU) ? G1_TBUFS * G1_NC * kTransPitch * 4 : 0;
+  static constexpr int EPI_WARP_BYTES = DSW ? G1_TBUFS * G1_NC * kTransPitch * 4 : 0;
   static constexpr int XCHG_QUARTER = kG1Subs * 2 * 32;  // floats: [slice][gate|up][lane]
-  static constexpr int XCHG_BYTES = (EPI == kEpiDSwiGLU) ? 2 * 4 * XCHG_QUARTER * 4 : 0;
+  static constexpr int XCHG_BYTES = DSW ? G1_GROUPS * 2 * 4 * XCHG_QUARTER * 4 : 0;
   // MXFP8 row-wise dh: the two column slices of a quarter swap 16-byte halves of their quantised gate
   // and up columns ([quarter][slice][lane] uint4), so that each writes one whole 32-byte sector
-  static constexpr int QX_BYTES = (EPI == kEpiDSwiGLU && MX && G1_NC == 16) ? 4 * 2 * 32 * 16 : 0;
+  static constexpr int QX_BYTES = (DSW && MX && G1_NC == 16) ? G1_GROUPS * 4 * 2 * 32 * 16 : 0;
   static constexpr int CK_CHUNK_BYTES = 2 * 32 * 128 * 2;
-  static constexpr int CK_BYTES = (EPI == kEpiDSwiGLU) ? 2 * CK_CHUNK_BYTES : 0;
+  static constexpr int CK_BYTES = DSW ? CK_BUFS * CK_CHUNK_BYTES : 0;
   // Store epilogue with a single TMEM accumulator: the tile is drained into a 128B-swizzled bf16
   // staging tile in shared memory (TMEM released at once) and written by TMA stores.
 #ifdef MOEBWD_NO_TMA_STORE
@@ -73,12 +78,15 @@ struct GemmCfg {
   // one 64-column staging slab (16 KB) keeps a fourth pipeline stage in shared memory
   static constexpr int STAGING_BYTES = STAGED ? BM * 64 * 2 : 0;
   // staged epilogues: 8 warps, two per TMEM lane quarter, splitting the columns
-  static constexpr int EPI_WARPS = EPI == kEpiDSwiGLU ? 4 * kG1Subs : STAGED ? 8 : 4;
+  static constexpr int EPI_WARPS = DSW ? 4 * kG1Subs * G1_GROUPS : STAGED ? 8 : 4;
   // dSwiGLU: one more warp whose lane 0 streams the checkpoint chunks into their two buffers, each as
   // soon as every epilogue warp has released it (ten or eleven warps share the 168-register cap)
-  static constexpr bool CK_LOADER = EPI == kEpiDSwiGLU;
+  static constexpr bool CK_LOADER = DSW;
   static constexpr int CK_LOADER_WARP = 2 + EPI_WARPS;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS + (CK_LOADER ? 32 : 0);
+  // registers per thread: the launch bound's share of the register file (multiples of 8), which the
+  // sixteen-warp dSwiGLU epilogue needs stated (ptxas would otherwise settle below it)
+  static constexpr int MAX_REGS = (65536 / THREADS) / 8 * 8 > 255 ? 255 : (65536 / THREADS) / 8 * 8;
   static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES + XCHG_BYTES + QX_BYTES + CK_BYTES + STAGING_BYTES;
   static constexpr int BAR_BYTES = 512;
   static constexpr int RING = 4;  // tile indices published by the producer ahead of the consumers
@@ -603,7 +611,7 @@ __device__ __forceinline__ void producer_gather(const GemmParams& p, const CUten
 // the kernel
 // ------------------------------------------------------------------------------------------
 template <bool MX, int BN, int EPI>
-__global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
+__global__ void __launch_bounds__((GemmCfg<MX, BN, EPI>::THREADS), 1) __maxnreg__((GemmCfg<MX, BN, EPI>::MAX_REGS))
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams p) {
   using C = GemmCfg<MX, BN, EPI>;
@@ -624,8 +632,8 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* ck_full = tempty + 2;
-  uint64_t* ck_empty = ck_full + 2;  // every epilogue warp has consumed the checkpoint buffer
-  uint64_t* done = ck_empty + 2;
+  uint64_t* ck_empty = ck_full + C::CK_BUFS;  // every warp of the chunk's group has consumed the buffer
+  uint64_t* done = ck_empty + C::CK_BUFS;
   uint64_t* tile_full = done + 1;          // ring slot r holds a tile index (producer arrives)
   uint64_t* tile_empty = tile_full + C::RING;  // every consumer warp has read slot r
   volatile int* tile_ring = reinterpret_cast<volatile int*>(tile_empty + C::RING);
@@ -637,7 +645,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     // a gathered A operand arrives on a stage's full barrier a second time (see producer_gather)
-    const uint32_t full_count = (EPI == kEpiDSwiGLU && p.a_gather) ? 2u : 1u;
+    const uint32_t full_count = (C::DSW && p.a_gather) ? 2u : 1u;
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], full_count);
       mbar_init(&empty[s], 1);
@@ -645,8 +653,10 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], C::EPI_WARPS);
+    }
+    for (int a = 0; a < C::CK_BUFS; ++a) {
       mbar_init(&ck_full[a], 1);
-      mbar_init(&ck_empty[a], C::EPI_WARPS);
+      mbar_init(&ck_empty[a], C::EPI_WARPS / C::G1_GROUPS);
     }
     mbar_init(done, 1);
     for (int r = 0; r < C::RING; ++r) {
@@ -657,7 +667,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    if (EPI == kEpiDSwiGLU || C::STAGED) prefetch_tmap(&tmC);
+    if (C::DSW || C::STAGED) prefetch_tmap(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -676,7 +686,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
   // the K-grouped order) and publishes each index, then -1, through the ring.
 
   if (warp == 0) {
-    if (EPI == kEpiDSwiGLU && p.a_gather) {
+    if (C::DSW && p.a_gather) {
       // ---------------- producer with gathered A rows (whole warp) ----------------
       producer_gather<C, BN, MX>(p, &tmB, smA, smB, smSFA, smSFB, full, empty, tile_full, tile_empty, tile_ring,
                                  abort_flag, total, lane);
@@ -807,8 +817,8 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
   } else if (C::CK_LOADER && warp == C::CK_LOADER_WARP) {
     if (lane == 0) {
       // ---------------- checkpoint loader (dSwiGLU) ----------------
-      // chunk n of the schedule (the tiles in ring order, NCHUNK chunks each) goes to buffer n % 2
-      // once every epilogue warp has released chunk n - 2
+      // chunk n of the schedule (the tiles in ring order, NCHUNK chunks each) goes to buffer
+      // n % CK_BUFS once every warp of its group has released chunk n - CK_BUFS
       int64_t issued = 0;
       int rs = 0;
       uint32_t rph = 0;
@@ -827,9 +837,10 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         int b0;
         tile_ckpt_origin(p, tn, blk, b0);
         for (int c = 0; c < C::NCHUNK; ++c) {
-          const int buf = (int)(issued & 1);
-          if (issued >= 2 &&
-              !mbar_wait_bounded(&ck_empty[buf], (uint32_t)(((issued - 2) >> 1) & 1), p.status, abort_flag, p.wait_ns)) {
+          const int buf = (int)(issued % C::CK_BUFS);
+          if (issued >= C::CK_BUFS &&
+              !mbar_wait_bounded(&ck_empty[buf], (uint32_t)(((issued - C::CK_BUFS) / C::CK_BUFS) & 1), p.status,
+                                 abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -841,19 +852,23 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
           ++issued;
         }
       }
-      // Drain: the last two chunks' copies land before the CTA may exit.
-      for (int64_t n = issued > 2 ? issued - 2 : 0; n < issued; ++n)
-        mbar_wait_drain(&ck_full[n & 1], (uint32_t)((n >> 1) & 1), p.status);
+      // Drain: the last CK_BUFS chunks' copies land before the CTA may exit.
+      for (int64_t n = issued > C::CK_BUFS ? issued - C::CK_BUFS : 0; n < issued; ++n)
+        mbar_wait_drain(&ck_full[n % C::CK_BUFS], (uint32_t)((n / C::CK_BUFS) & 1), p.status);
     }
   } else {
-    // ---------------- epilogue warps (2..5, or 2..9) ----------------
+    // ---------------- epilogue warps (2..5, 2..9, or 2..17) ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int m = 32 * q + lane;
-    const int half = (warp - 2) >> 2;  // dSwiGLU: column slice of every 32 columns; staged: which half
+    // dSwiGLU: column slice of every 32 columns and (two groups) the warp's chunk group; staged: which half
+    const int half = ((warp - 2) >> 2) & 1;
+    const int grp = (warp - 2) >> 3;
     uint8_t* wsm = smEPI + (warp - 2) * C::EPI_WARP_BYTES;
-    float* xchg = smXchg + q * C::XCHG_QUARTER;  // + (chunk parity) * 4 * XCHG_QUARTER
-    // checkpoint chunk n of the schedule is read from buffer n % 2 (filled by the loader warp)
-    int64_t ck_next = 0;
+    // the amax exchange of the group's quarter: [group][chunk parity][quarter][XCHG_QUARTER]
+    float* xchg = smXchg + grp * (8 * C::XCHG_QUARTER) + q * C::XCHG_QUARTER;
+    // checkpoint chunk n of the schedule (n = tiles before this one * NCHUNK + c) is read from buffer
+    // n % CK_BUFS (filled by the loader warp); `done_chunks` counts this warp's chunks (pair parity)
+    int64_t tile_seq = 0, done_chunks = 0;
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
@@ -868,7 +883,7 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
         rs = 0;
         rph ^= 1u;
       }
-      if constexpr (EPI == kEpiDSwiGLU || C::STAGED) {
+      if constexpr (C::DSW || C::STAGED) {
         // uniform exit decision (see below)
         if (epilogue_bar_any<32 * C::EPI_WARPS>(*abort_flag != 0)) break;
       }
@@ -877,12 +892,12 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
       // dSwiGLU: the row's flat index and score, loaded while the accumulator is still being computed
       int row_f = -1;
       float row_s = 0.f;
-      if constexpr (EPI == kEpiDSwiGLU) {
+      if constexpr (C::DSW) {
         row_f = p.tile_row_flat[(int64_t)ti.mt * 128 + m];
         if (row_f >= 0) row_s = p.s[row_f];
       }
       const bool got = mbar_wait_bounded(&tfull[acc], aph, p.status, abort_flag, p.wait_ns);
-      if constexpr (EPI == kEpiDSwiGLU || C::STAGED) {
+      if constexpr (C::DSW || C::STAGED) {
         // these epilogues synchronise their warps with named barriers: every exit decision is the
         // OR of the shared abort flag over all of them, taken at a barrier, so no warp is left waiting
         if (epilogue_bar_any<32 * C::EPI_WARPS>(*abort_flag != 0)) break;
@@ -1019,45 +1034,50 @@ __global__ void __launch_bounds__(GemmCfg<MX, BN, EPI>::THREADS, 1)
           tile_ckpt_origin(p, ti, blk, b0);
           ga = p.gate_act + blk * (int64_t)p.I * p.B + b0 + m;
         }
+        const int bar_id = 2 + q + 4 * grp;  // the pair of this quarter and group
 #pragma unroll 1
-        for (int c = 0; c < C::NCHUNK; ++c) {
-          const int buf = (int)(ck_next & 1);
+        for (int c = grp; c < C::NCHUNK; c += C::G1_GROUPS) {
+          const int64_t n = tile_seq * C::NCHUNK + c;  // the chunk's place in the loader's schedule
+          const int buf = (int)(n % C::CK_BUFS);
           // on a failed wait the chunk is still walked (garbage in, flagged by the status word) so
           // that both warps of a pair reach the same barriers
-          const bool ck_ok =
-              mbar_wait_bounded(&ck_full[buf], (uint32_t)((ck_next >> 1) & 1), p.status, abort_flag, p.wait_ns);
+          const bool ck_ok = mbar_wait_bounded(&ck_full[buf], (uint32_t)((n / C::CK_BUFS) & 1), p.status, abort_flag,
+                                               p.wait_ns);
           {
             const uint32_t ta = taddr + c * 32 + half * C::G1_NC;
             const int i0 = ti.nt * BN + c * 32;
             const uint16_t* ckb = reinterpret_cast<const uint16_t*>(smCK + buf * C::CK_CHUNK_BYTES);
-            float* xc = xchg + (int)(ck_next & 1) * (4 * C::XCHG_QUARTER);
-            uint4* qx = smQx + q * 64;
+            float* xc = xchg + (int)(done_chunks & 1) * (4 * C::XCHG_QUARTER);
+            uint4* qx = smQx + (grp * 4 + q) * 64;
             // the activation format fixed per instantiation; SwiGLU with concat gate/up specialised
             const bool generic = p.glu != MOE_GLU_SWIGLU || p.interleaved || p.gate_act != nullptr;
             float* tb = reinterpret_cast<float*>(wsm);
             if (!MX || p.fmt_act == MOE_FP8_E5M2) {
               if (generic)
                 epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2, true, C::G1_TBUFS == 1>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
-                                                                  xc, qx, 2 + q, ds_acc);
+                                                                  xc, qx, bar_id, ds_acc);
               else
                 epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E5M2, false, C::G1_TBUFS == 1>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
-                                                                   xc, qx, 2 + q, ds_acc);
+                                                                   xc, qx, bar_id, ds_acc);
             } else {
               if (generic)
                 epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3, true, C::G1_TBUFS == 1>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
-                                                                  xc, qx, 2 + q, ds_acc);
+                                                                  xc, qx, bar_id, ds_acc);
               else
                 epi_dswiglu_part<MX, C::G1_NC, MOE_FP8_E4M3, false, C::G1_TBUFS == 1>(p, ta, prow, m, lane, valid, sv, i0, half, ckb, ga, tb,
-                                                                   xc, qx, 2 + q, ds_acc);
+                                                                   xc, qx, bar_id, ds_acc);
             }
           }
           __syncwarp();
           // this warp no longer reads the buffer; a chunk whose copy was not seen to land is never
           // released, so the loader cannot refill a buffer while a copy into it is still in flight
           if (lane == 0 && ck_ok) mbar_arrive(&ck_empty[buf]);
-          ++ck_next;
+          ++done_chunks;
         }
-        p.ds_part[prow * (int64_t)(kG1Subs * (p.I / BN)) + kG1Subs * ti.nt + half] = valid ? ds_acc : 0.f;
+        ++tile_seq;
+        // one ds partial per (row, N tile, group, column slice)
+        constexpr int kParts = kG1Subs * C::G1_GROUPS;
+        p.ds_part[prow * (int64_t)(kParts * (p.I / BN)) + kParts * ti.nt + grp * kG1Subs + half] = valid ? ds_acc : 0.f;
       }
       tc_fence_before();
       __syncwarp();

@@ -11,6 +11,10 @@ int launch_gemm_mx(int BN, const GemmParams& p, const void* tmA, const void* tmB
   if (p.epi == kEpiStore)
     return BN == 256 ? gemm_launch_instance<true, 256, kEpiStore>(p, tmA, tmB, tmC, grid, st)
                      : gemm_launch_instance<true, 128, kEpiStore>(p, tmA, tmB, tmC, grid, st);
+  // G1 with two groups of epilogue warps (128- or 192-column tiles)
+  if (p.epi == kEpiDSwiGLU2)
+    return BN == 192 ? gemm_launch_instance<true, 192, kEpiDSwiGLU2>(p, tmA, tmB, tmC, grid, st)
+                     : gemm_launch_instance<true, 128, kEpiDSwiGLU2>(p, tmA, tmB, tmC, grid, st);
   // G1: 192 columns (two TMEM accumulators, scales of W2 re-tiled per tile) where I allows
   if (BN == 192) return gemm_launch_instance<true, 192, kEpiDSwiGLU>(p, tmA, tmB, tmC, grid, st);
   return BN == 256 ? gemm_launch_instance<true, 256, kEpiDSwiGLU>(p, tmA, tmB, tmC, grid, st)

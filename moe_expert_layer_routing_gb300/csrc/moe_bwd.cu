@@ -101,6 +101,7 @@ struct Layout {
   int64_t P, Nb, TK;
   int BN1, BN2, BN3, BN4;
   bool gather;  // G1 gathers its dout rows (MOE_OPT_G1_GATHER)
+  int g1_groups; // G1 epilogue warp groups: 2 (sixteen warps) or 1 (MOE_OPT_G1_WARPS)
 };
 
 static int64_t tile_capacity(int64_t TK, int E) {
@@ -143,6 +144,11 @@ static Layout make_layout(const MoeBwdArgs& a) {
   L.BN2 = bn_option(MOE_OPT_G2_TILE_N, L.BN2, a.H);
   L.BN3 = bn_option(MOE_OPT_G3_TILE_N, L.BN3, a.H);
   L.BN4 = bn_option(MOE_OPT_G4_TILE_N, L.BN4, 2 * a.I);
+  {  // sixteen G1 epilogue warps: MXFP8, 128- or 192-column tiles, automatic where K = H is small
+    const int64_t w = option(MOE_OPT_G1_WARPS);
+    const bool two = w == 16 || (w == 0 && a.H <= 2048);
+    L.g1_groups = (mx && two && (L.BN1 == 128 || L.BN1 == 192)) ? 2 : 1;
+  }
   const int64_t P = L.P, H = a.H, I = a.I, E = a.E;
   size_t b[R_COUNT] = {};
   b[R_CHUNK_COUNTS] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, route_nchunks(L.TK)) * E;
@@ -171,7 +177,8 @@ static Layout make_layout(const MoeBwdArgs& a) {
     b[R_AP_T_SF] = (size_t)(I * P / 32);
   }
   b[R_DX_EXP] = (size_t)(P * H * 2);
-  b[R_DS_PART] = sizeof(float) * (size_t)(P * kG1Subs * (I / L.BN1));  // one partial per column slice and N tile
+  // one partial per column slice, warp group and N tile
+  b[R_DS_PART] = sizeof(float) * (size_t)(P * kG1Subs * L.g1_groups * (I / L.BN1));
   b[R_DS_BIAS] = a.has_bias ? sizeof(float) * (size_t)P : 0;
   b[R_COUNTERS] = 64;  // one tile counter per grouped GEMM
   b[R_PAIR_OFFSETS] = sizeof(int32_t) * (E + 1);
@@ -574,7 +581,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     }
     p.sfa_ktiles = p.sfb_ktiles = (int)(H / 128);
     p.fmt_a = a.fp8_act; p.fmt_b = a.fp8_w;
-    p.epi = kEpiDSwiGLU;
+    p.epi = L.g1_groups == 2 ? kEpiDSwiGLU2 : kEpiDSwiGLU;
     p.s = a.s;
     p.tile_row_flat = tile_row_flat;
     p.e_tile_offsets = tile_offsets;
@@ -683,7 +690,8 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   if ((rc = launch_dx_scatter_sum(reg<uint16_t>(L, ws, R_DX_EXP), flat_tile_row, a.T, a.K, a.H,
                                   static_cast<uint16_t*>(a.dx), st)))
     return rc;
-  if ((rc = launch_ds_finalize(reg<float>(L, ws, R_DS_PART), (int)(kG1Subs * (I / L.BN1)), a.has_bias ? reg<float>(L, ws, R_DS_BIAS) : nullptr,
+  if ((rc = launch_ds_finalize(reg<float>(L, ws, R_DS_PART), (int)(kG1Subs * L.g1_groups * (I / L.BN1)),
+                               a.has_bias ? reg<float>(L, ws, R_DS_BIAS) : nullptr,
                                flat_tile_row, TK, a.ds, st)))
     return rc;
   if (a.ds_masked && (rc = launch_ds_masked(a.ds, a.ids, a.num_valid_tokens, a.T, a.K, a.E, a.ds_masked, st)))

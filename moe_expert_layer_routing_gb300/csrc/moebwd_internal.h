@@ -156,7 +156,9 @@ int launch_quant_colwise(const uint16_t* in, int64_t src_rows, int64_t rows, int
 // tcgen05 grouped GEMM (gemm_*.cu)
 // ------------------------------------------------------------------------------------------
 enum GemmMode { kMGrouped = 0, kKGrouped = 1 };
-enum EpiKind { kEpiStore = 0, kEpiDSwiGLU = 1, kEpiCkpt = 2 };
+// kEpiDSwiGLU2: the dSwiGLU epilogue with two groups of epilogue warps taking alternate 32-feature
+// chunks (sixteen warps, three checkpoint buffers, one pipeline stage fewer)
+enum EpiKind { kEpiStore = 0, kEpiDSwiGLU = 1, kEpiCkpt = 2, kEpiDSwiGLU2 = 3 };
 // dSwiGLU epilogue (G1): warps per TMEM lane quarter; each takes 32 / kG1Subs of every 32 columns
 // and writes one ds partial per (row, N tile).
 #ifndef MOEBWD_G1_SUBS
@@ -201,7 +203,7 @@ struct GemmParams {
   void* dh; uint8_t* dh_sf;
   void* dht; uint8_t* dht_sf;
   void* apt; uint8_t* apt_sf;
-  float* ds_part;               // [P, kG1Subs*I/BN]
+  float* ds_part;               // [P, kG1Subs*groups*I/BN] (groups: 2 for kEpiDSwiGLU2, else 1)
   float* db1_part;              // BF16 with biases: [P/128][4][2I] column sums of dh per tile and TMEM
                                 // lane quarter (W1's gate/up layout), or null
   // CTA-pair kernel, M-grouped: expert e's 128-row tiles form ceil(tiles_e / 2) pairs; pair_offsets

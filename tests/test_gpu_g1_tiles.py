@@ -26,11 +26,14 @@ def _ragged_ids(T, K, E, seed):
     return torch.from_numpy(ids.astype(np.int32))
 
 
+@pytest.mark.parametrize("warps", [16, 8])
 @pytest.mark.parametrize("bn", [192, 128])
 @pytest.mark.parametrize("I", [384, 768])
 @pytest.mark.parametrize("fmt_act,aff", [(FP8_E5M2, AFFINITY_ON_I), (FP8_E4M3, AFFINITY_ON_H)])
-def test_mxfp8_g1_tile_widths(set_option, bn, I, fmt_act, aff):
+def test_mxfp8_g1_tile_widths(set_option, bn, I, fmt_act, aff, warps):
+    """Both G1 tile widths with eight epilogue warps or sixteen (two groups taking alternate chunks)."""
     set_option("G1_TILE_N", bn)
+    set_option("G1_WARPS", warps)
     cfg = small_moe("g1w", T=520, H=256, I=I, E=6, K=2, B=256, seed=91, precision=PREC_MXFP8, affinity=aff,
                     fp8_act=fmt_act)
     inp = with_ids(make_moe_inputs(cfg), _ragged_ids(520, 2, 6, seed=11))
@@ -39,10 +42,12 @@ def test_mxfp8_g1_tile_widths(set_option, bn, I, fmt_act, aff):
     compare_outputs(got, oracle_bwd(inp), MXFP8_TOL)
 
 
-def test_mxfp8_g1_variant_at_192(set_option):
+@pytest.mark.parametrize("warps", [16, 8])
+def test_mxfp8_g1_variant_at_192(set_option, warps):
     """GeGLU with the interleaved gate/up layout through the 192-column tiles."""
     import moe_expert_layer_routing_gb300 as mb
     set_option("G1_TILE_N", 192)
+    set_option("G1_WARPS", warps)
     cfg = small_moe("g1v", T=400, H=256, I=384, E=5, K=2, B=128, seed=92, precision=PREC_MXFP8,
                     affinity=AFFINITY_ON_I)
     inp = with_ids(make_moe_inputs(cfg), _ragged_ids(400, 2, 5, seed=12))
@@ -63,7 +68,8 @@ def test_mxfp8_g1_variant_at_192(set_option):
     compare_outputs(got, ref, MXFP8_TOL)
 
 
-def test_g1_widths_agree_on_dh(set_option):
+@pytest.mark.parametrize("warps", [16, 8])
+def test_g1_widths_agree_on_dh(set_option, warps):
     """The quantised dh of the two tile widths: each output element's contraction is the same, so the
     codes and scales agree except where fp32 accumulation order moves a value across a rounding
     boundary (none expected; at most a handful allowed)."""
@@ -71,6 +77,7 @@ def test_g1_widths_agree_on_dh(set_option):
                     affinity=AFFINITY_ON_I)
     inp = make_moe_inputs(cfg)
     outs = {}
+    set_option("G1_WARPS", warps)
     for bn in (192, 128):
         set_option("G1_TILE_N", bn)
         op, got = run_gpu(inp)
@@ -82,3 +89,21 @@ def test_g1_widths_agree_on_dh(set_option):
     assert diff <= outs[128][0].size * 1e-4, diff
     ds192, ds128 = outs[192][1], outs[128][1]   # partial sums per tile width: summation order differs
     np.testing.assert_allclose(ds192, ds128, rtol=1e-4, atol=1e-5 * np.abs(ds128).max())
+
+
+def test_g1_eight_and_sixteen_epilogue_warps_are_bit_identical(set_option):
+    """The two epilogue layouts compute every element the same way (only the ds partials are summed in
+    another grouping): dx, dW1, dW2 bit-identical, ds to fp32 rounding."""
+    import torch
+    cfg = small_moe("g1warps", T=600, H=512, I=384, E=6, K=2, B=256, seed=94, precision=PREC_MXFP8,
+                    affinity=AFFINITY_ON_I, bias=True)
+    inp = with_ids(make_moe_inputs(cfg), _ragged_ids(600, 2, 6, seed=13))
+    outs = {}
+    for warps in (16, 8):
+        set_option("G1_WARPS", warps)
+        _, got = run_gpu(inp)
+        assert int(got["status"].item()) == 0
+        outs[warps] = {k: v.clone() for k, v in got.items() if v is not None}
+    for n in ("dx", "dW1", "dW2", "db1", "db2"):
+        assert torch.equal(outs[16][n], outs[8][n]), n
+    torch.testing.assert_close(outs[16]["ds"], outs[8]["ds"], rtol=1e-5, atol=1e-6)

@@ -117,6 +117,7 @@ def test_options_defaults_and_validation(lib):
                       ("G2_TILE_N", 192), ("PREP_TILE_ORDER", 2)):
         assert lib.moe_set_option(mb.OPTIONS.index(name), bad) == -1
         assert b"not allowed" in lib.moe_last_error()
+    mb.set_option("G1_WARPS", 8)
     with mb.option("G1_TILE_N", 192):
         assert mb.get_option("G1_TILE_N") == 192
         a = mb.MoeBwdArgs(T=256, H=256, I=384, E=4, K=2, block_size=128, precision=1)
@@ -125,7 +126,8 @@ def test_options_defaults_and_validation(lib):
     mb.set_option("G1_TILE_N", 128)
     n128 = lib.moe_bwd_workspace_size(ctypes.byref(a))
     mb.set_option("G1_TILE_N", None)
-    assert mb.get_option("G1_TILE_N") == 0
+    mb.set_option("G1_WARPS", None)
+    assert mb.get_option("G1_TILE_N") == 0 and mb.get_option("G1_WARPS") == 0
     assert n192 > 0 and n128 > 0 and n192 != n128   # the tile width moves the ds partials' region
 
 
