@@ -406,10 +406,10 @@ enum {
                                 or for MXFP8 from dout quantised once per token, MOE_WS_DOUT_Q) with 16-byte
                                 asynchronous copies -- same results, less memory, but slower (the copies of
                                 one producer warp keep fewer bytes in flight than tensor-map loads) */
-  MOE_OPT_G1_WARPS,          /* epilogue warps of the MXFP8 dA/dSwiGLU GEMM: 0 automatic (default: 16 where
-                                H <= 2048 -- the epilogue, not the mainloop, bounds it there -- else 8),
-                                8, or 16 (two groups taking alternate 32-feature chunks, one pipeline
-                                stage fewer); BF16 always uses 8 */
+  MOE_OPT_G1_WARPS,          /* epilogue warps of the MXFP8 dA/dSwiGLU GEMM: 0 automatic (8), 8, or 16 (two
+                                groups taking alternate 32-feature chunks, three checkpoint buffers, one
+                                pipeline stage fewer: measured no faster -- the epilogue is bound by the
+                                load/store unit's wavefronts, not by warps to hide latency); BF16 uses 8 */
   MOE_OPT_PDL,               /* 1 (default): the kernels of a call are launched with programmatic dependent
                                 launch (each may be scheduled while the previous one finishes and waits on
                                 the device for its results); 0: plain stream order */

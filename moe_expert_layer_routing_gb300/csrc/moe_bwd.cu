@@ -144,9 +144,9 @@ static Layout make_layout(const MoeBwdArgs& a) {
   L.BN2 = bn_option(MOE_OPT_G2_TILE_N, L.BN2, a.H);
   L.BN3 = bn_option(MOE_OPT_G3_TILE_N, L.BN3, a.H);
   L.BN4 = bn_option(MOE_OPT_G4_TILE_N, L.BN4, 2 * a.I);
-  {  // sixteen G1 epilogue warps: MXFP8, 128- or 192-column tiles, automatic where K = H is small
+  {  // sixteen G1 epilogue warps (MXFP8, 128- or 192-column tiles) only on request: measured no faster
     const int64_t w = option(MOE_OPT_G1_WARPS);
-    const bool two = w == 16 || (w == 0 && a.H <= 2048);
+    const bool two = w == 16;
     L.g1_groups = (mx && two && (L.BN1 == 128 || L.BN1 == 192)) ? 2 : 1;
   }
   const int64_t P = L.P, H = a.H, I = a.I, E = a.E;
