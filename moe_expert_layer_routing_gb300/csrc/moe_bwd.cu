@@ -186,10 +186,10 @@ static Layout make_layout(const MoeBwdArgs& a) {
   b[R_TILE_ROW_SLOT] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, P);  // saved s*dout rows (pointers not read)
   // W2's scales re-tiled for 192-column G1 tiles: two atoms per tile
   if (mx && L.BN1 % 128) b[R_W2_SF_T] = (size_t)(E * I / L.BN1) * ((L.BN1 + 127) / 128) * (size_t)(H / 128) * 512;
-  // bias gradients: per-tile column sums from G1's transposes (four lane quarters) and prep (two halves)
+  // bias gradients: per-tile column sums from G1's transposes (four lane quarters) and prep (four row quarters)
   if (a.has_bias) {
     b[R_DB1_PART] = sizeof(float) * (size_t)(P / kTileM) * 4 * (size_t)(2 * I);
-    b[R_DB2_PART] = sizeof(float) * (size_t)(P / kTileM) * 2 * (size_t)H;
+    b[R_DB2_PART] = sizeof(float) * (size_t)(P / kTileM) * 4 * (size_t)H;
   }
   if (a.act_src == MOE_ACT_RECOMPUTE) {
     b[R_X_G] = (size_t)(P * H * es);
@@ -699,7 +699,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   if (a.has_bias) {  // per-expert sums of the per-tile partials (dout_gt read again only when it was not built here)
     if (pa.db2_part) {  // db1 and db2 from their per-tile partials in one launch
       rc = launch_bias_parts_reduce(reg<float>(L, ws, R_DB1_PART), 4, 2 * I, tile_offsets, (int)E, a.db1, st,
-                                    a.accumulate, pa.db2_part, 2, H, a.db2);
+                                    a.accumulate, pa.db2_part, 4, H, a.db2);
     } else {
       if ((rc = launch_bias_parts_reduce(reg<float>(L, ws, R_DB1_PART), 4, 2 * I, tile_offsets, (int)E, a.db1, st,
                                          a.accumulate)))

@@ -127,8 +127,10 @@ struct PrepArgs {
   void* x_g; uint8_t* x_g_sf;          // [P,H] row-major (nullable: only when h is recomputed)
   int skip_dout_t;                     // dout_gt is built elsewhere (from a saved s*dout checkpoint)
   float* ds_bias;                      // [P] <dout_t, b2_e> or null
-  float* db2_part;                     // BF16 with biases: [P/128][2][H] column sums of s*dout per
-                                       // tile (two halves of its rows), or null
+  float* db2_part;                     // with biases: [P/128][4][H] column sums of s*dout per tile
+                                       // (four 32-row quarters of its rows), or null
+  uint32_t k_mul; int k_shift;         // set by launch_prep: f / K = umulhi(f, k_mul) >> (k_shift - 1)
+                                       // for 0 <= f < 2^31 (k_shift = 0: K = 1)
 };
 int launch_prep(const PrepArgs& a, cudaStream_t st);
 // a'^T [I,P] from an [N,I,B] block checkpoint of a (times s when s_or_null) or s*a

@@ -160,4 +160,29 @@ __device__ __forceinline__ uint32_t quantize_group32_t(const float (&v)[32], uin
   return byte;
 }
 
+// quantize_group32_t with the group's amax given as the bits of an fp32 value (only its exponent
+// field is used).
+template <int FMT>
+__device__ __forceinline__ uint32_t quantize_group32_am(const float (&v)[32], uint32_t am_bits, uint32_t (&w)[8]) {
+  const uint32_t byte = e8m0_byte(am_bits, FMT);
+  const uint64_t inv2 = f2_splat(e8m0_inv_scale(byte));
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = fp8x4_scaled<FMT>(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3], inv2);
+  return byte;
+}
+
+// Per half, max |x| over 32 words of two bf16 values each (a tree of max.xorsign.abs.bf16x2: the
+// magnitudes are maxima of magnitudes at every step, the sign bits are cleared at the end).  The
+// maximum of bf16 magnitudes is itself a bf16 value, so this is the fp32 amax of either half exactly.
+__device__ __forceinline__ uint32_t bf16x2_absmax32(const uint32_t (&w)[32]) {
+  uint32_t t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(t[i]) : "r"(w[i]), "r"(w[i + 16]));
+#pragma unroll
+  for (int n = 8; n > 0; n >>= 1)
+#pragma unroll
+    for (int i = 0; i < n; ++i) asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(t[i]) : "r"(t[i]), "r"(t[i + n]));
+  return t[0] & 0x7FFF7FFFu;
+}
+
 }  // namespace moebwd

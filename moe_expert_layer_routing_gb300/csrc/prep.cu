@@ -1,6 +1,6 @@
 // Operand preparation for the grouped GEMMs, and the public mxfp8_quantize.
 //
-// prep_kernel (one CTA per 128-row tile of the tile-row space, H walked in 256-column chunks)
+// prep_kernel (persistent; 128-row tiles of the tile-row space, H walked in 128-column chunks)
 // gathers the token rows of every routed (t, k) once and writes, in one pass over dout and x:
 //   dout_g  [P, H]  gathered dout rows                      (G1 A operand, groups along H; when G1
 //                   gathers its rows itself, nothing for BF16 and only the tiled scales for MXFP8)
@@ -10,100 +10,231 @@
 // as BF16, or as MXFP8 with E8M0 scales in the tiled layout (transposed operands are quantised
 // in groups of 32 tile rows, i.e. along the GEMM contraction).  Padding rows are zero.  When the
 // gate/up pre-activations are recomputed, a row-major gathered x [P,H] (G0's A operand) is written too.
+#include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
 
 #include "moebwd_internal.h"
 #include "mx_device.cuh"
+#include "ptx.cuh"
 
 namespace moebwd {
 
 constexpr int kPrepPitch = 66;       // bf16 row pitch of the 64-column tiles of the generic quantiser
-constexpr int kPrepCols = 256;       // H columns per step of the MoE prep kernel
-constexpr int kPrepTilePitch = 264;  // bf16 row pitch of its [128][256] tile (528 B: 16 B aligned)
-constexpr int kPrepSmem = 128 * kPrepTilePitch * 2;
+// ---- MoE prep kernel ----
+// Persistent CTAs (two per SM) walk work items: a whole tile (128 tile rows x all of H) when the bias
+// term of ds is wanted (its row dot products span H), else one 128-column chunk of a tile.  An item
+// is a sequence of units, one per chunk and tensor (dout when anything is built from it, then x);
+// a unit's [128 rows x 128 columns] bf16 tile is gathered by cp.async (16-byte pieces, padding rows
+// zero-filled) into one of two shared buffers one unit ahead, so the gather of unit u+1 overlaps
+// the quantisation of unit u.  Per unit:
+//   phase A (dout; x too when h is recomputed): each thread quantises the 16-byte pieces of eight
+//     rows row-wise (MXFP8 groups of 32 columns = 4 lanes) into the row-major copy and its scales,
+//     and accumulates the rows' dot products with b2;
+//   phase B: thread (column pair, 32-row quarter) reads 32 words, quantises (MXFP8) or rounds (BF16)
+//     the two transposed 32-element groups into a staging tile in the 128-byte swizzled layout of
+//     the output's tensor map (16-byte piece c of staging row r at r * 128 + ((c ^ (r % 8)) * 16)),
+//     written by one elected thread's tiled bulk stores; MXFP8 scale bytes go to one staged 512-byte
+//     atom of the tiled layout, written by a plain bulk copy.
+// Rows and tokens: tile row p holds flat index f = tile_row_flat[p] (token f / K, or padding when
+// f < 0); the divide is a multiply by a constant from the host.
+constexpr int kPrepCols = 128;                       // H columns per unit
+constexpr int kPrepTilePitch = 136;                  // bf16 row pitch of a unit tile (272 B: 16-B aligned,
+                                                     // consecutive rows four banks apart)
+constexpr int kPrepTile = 128 * kPrepTilePitch * 2;  // bytes of one unit buffer
+// MXFP8 staging: two buffers (by unit parity) of a unit's transposed fp8 codes (16 KB) and its scale
+// atom (512 B), 17 KB apart.  (BF16 writes its transposed rows directly: 64 contiguous bytes per
+// output row and group.)
+constexpr int kPrepStageMx = 128 * 128;
+constexpr int kPrepStageMxStride = 17 * 1024;
+template <bool MX>
+constexpr int prep_smem_bytes() {  // 1024-byte alignment slack, staging, two unit buffers, s and b2 per buffer
+  return 1024 + (MX ? 2 * kPrepStageMxStride : 0) + 2 * kPrepTile + 2 * 128 * 4 + 2 * 128 * 2;
+}
 
-// Per 256-column chunk and per tensor (dout, then x): phase 1, each warp reads whole 512-byte row
-// segments of 16 gathered rows (16-byte vectors, 16 in flight per thread), writes the row-major
-// dout_g chunk and stages the tile in shared memory; phase 2 writes the transposed output in 32-row
-// groups (128 contiguous bytes for fp8, 256 for bf16, per output row): for MXFP8 each thread owns
-// one column and its four groups, for BF16 a column pair (32-bit shared-memory reads) and two groups.
-// Gathered rows in flight per thread in phase 1: 8 (two batches per 16 rows) measured as fast as 16
-// at 2 CTAs per SM with half the registers; 3 CTAs per SM measured slower.
-constexpr int kPrepBatch = 8;
+__device__ __forceinline__ int prep_token(const PrepArgs& a, int f) {
+  if (f < 0) return -1;
+  return a.k_shift == 0 ? f : (int)(__umulhi((uint32_t)f, a.k_mul) >> (a.k_shift - 1));
+}
 
 template <bool MX, bool SCALE_T, bool BIAS, int AF>
-__global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
+__global__ void __launch_bounds__(256, 2)
+    prep_kernel(const PrepArgs a, const __grid_constant__ CUtensorMap tm_dout_gt,
+                const __grid_constant__ CUtensorMap tm_x_gt) {
   pdl_wait();  // results of the previous kernel on the stream
   pdl_trigger();
-  if ((int)blockIdx.x >= *a.num_tiles) return;
-  const int tile = a.tile_order ? a.tile_order[blockIdx.x] : (int)blockIdx.x;
-  extern __shared__ uint4 prep_smem[];
-  uint16_t* st = reinterpret_cast<uint16_t*>(prep_smem);
-  __shared__ int32_t s_tok[128];
-  __shared__ float s_s[128];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = a.H;
+  const int H = a.H, nch = H / kPrepCols;
   const int64_t P = a.P;
-  const int64_t prow0 = (int64_t)tile * 128;
-  if (tid < 128) {
-    const int f = a.tile_row_flat[prow0 + tid];
-    s_tok[tid] = f >= 0 ? f / a.K : -1;
-    s_s[tid] = f >= 0 ? a.s[f] : 0.f;
+  const int ntiles = *a.num_tiles;
+  const int nitems = BIAS ? ntiles : ntiles * nch;
+  if ((int)blockIdx.x >= nitems) return;
+  extern __shared__ uint4 prep_smem[];
+  uint8_t* const stage0 =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(prep_smem) + 1023) & ~uintptr_t(1023));
+  uint16_t* const tiles = reinterpret_cast<uint16_t*>(stage0 + (MX ? 2 * kPrepStageMxStride : 0));
+  float* const s_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tiles) + 2 * kPrepTile);  // [2][128]
+  uint16_t* const s_b2 = reinterpret_cast<uint16_t*>(s_s + 2 * 128);                                 // [2][128]
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int rl = tid >> 4;  // this thread gathers and row-quantises rows rl + 16k (k < 8) of a unit ...
+  const int pc = tid & 15;  // ... their 16-byte piece pc (columns 8pc .. 8pc+7 of the chunk)
+  const bool need_s = SCALE_T || (BIAS && a.db2_part != nullptr);  // s per tile row in dout's phase B
+  const bool dout_t = !a.skip_dout_t;
+  const bool dout_rows = MX || a.dout_g != nullptr || BIAS;  // phase A has work on dout
+  const int nw = (dout_t || dout_rows) ? 2 : 1;             // units per chunk: dout (if any work), x
+  const int nu = (BIAS ? nch : 1) * nw;                      // units per item
+  const int G = (int)gridDim.x;
+  // item it -> (tile list index ti, first chunk c), chunk-major without biases (it = c * ntiles + ti:
+  // the items in flight are one chunk of consecutive tiles of the token-ordered schedule, so the K
+  // gathers of a token's row segment come close together and hit L2); the CTA's items are it, it + G, ...
+  const int dgi = BIAS ? G : G % ntiles, dgc = BIAS ? 0 : G / ntiles;
+  auto next_item = [&](int& it, int& ti, int& c) {
+    it += G;
+    ti += dgi;
+    c += dgc;
+    if (!BIAS && ti >= ntiles) {
+      ti -= ntiles;
+      ++c;
+    }
+  };
+  auto tile_of = [&](int ti) { return a.tile_order ? a.tile_order[ti] : ti; };
+
+  // loader: item l_* (tokens lt[], the flat index l_fs of row rl + 16pc for s, expert l_e), unit l_j;
+  // the next item p_* has its flat indices pf[] and expert in flight; the tile of the one after, q_tile
+  int l_it = (int)blockIdx.x, l_ti = BIAS ? l_it : l_it % ntiles, l_c = BIAS ? 0 : l_it / ntiles;
+  int l_tile = tile_of(l_ti), l_e = 0, l_fs = -1, l_j = 0;
+  int lt[8], pf[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) pf[k] = a.tile_row_flat[(int64_t)l_tile * 128 + rl + 16 * k];
+  if (BIAS) l_e = a.tile_expert[l_tile];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    lt[k] = prep_token(a, pf[k]);
+    if (k == pc) l_fs = pf[k];
   }
-  const int e = BIAS ? a.tile_expert[tile] : 0;
-  __syncthreads();
-  float bias_acc[16];
+  int p_it = l_it, p_ti = l_ti, p_c = l_c;
+  next_item(p_it, p_ti, p_c);
+  int p_tile = p_it < nitems ? tile_of(p_ti) : 0, p_e = 0;
+  if (p_it < nitems) {
 #pragma unroll
-  for (int r = 0; r < 16; ++r) bias_acc[r] = 0.f;
-  for (int h0 = 0; h0 < H; h0 += kPrepCols) {
-    const int ncol = min(kPrepCols, H - h0);
-    const int col = h0 + lane * 8;
-    const bool colok = lane * 8 < ncol;
-#pragma unroll 1
-    for (int which = 0; which < 2; ++which) {
-      const uint16_t* src = which == 0 ? a.dout : a.x;
-      // ---- phase 1 ----
-      uint4 bv = make_uint4(0, 0, 0, 0);
-      if (BIAS && which == 0 && colok) bv = *reinterpret_cast<const uint4*>(a.b2 + (int64_t)e * H + col);
+    for (int k = 0; k < 8; ++k) pf[k] = a.tile_row_flat[(int64_t)p_tile * 128 + rl + 16 * k];
+    if (BIAS) p_e = a.tile_expert[p_tile];
+  }
+  int q_tile = 0;
+  {
+    int q_it = p_it, q_ti = p_ti, q_c = p_c;
+    next_item(q_it, q_ti, q_c);
+    if (q_it < nitems) q_tile = tile_of(q_ti);
+  }
+
+  // gathers unit (chunk c, tensor w) of the loader's item into buffer b
+  auto issue = [&](int b, int c, int w) {
+    const uint16_t* src = w == 0 ? a.dout : a.x;
+    const uint32_t dst = smem_u32(tiles + b * (128 * kPrepTilePitch) + rl * kPrepTilePitch + pc * 8);
+    const int col = c * kPrepCols + pc * 8;
 #pragma unroll
-      for (int rb = 0; rb < 16; rb += kPrepBatch) {
-      uint4 v[kPrepBatch];
+    for (int k = 0; k < 8; ++k) {
+      const bool ok = lt[k] >= 0;
+      cp_async_16_zfill(dst + k * 16 * kPrepTilePitch * 2, ok ? src + (int64_t)lt[k] * H + col : src,
+                        ok ? 16u : 0u);
+    }
+    if (w == 0) {
+      if (need_s && pc < 8)
+        cp_async_4_zfill(smem_u32(s_s + b * 128 + rl + 16 * pc), l_fs >= 0 ? a.s + l_fs : a.s, l_fs >= 0 ? 4u : 0u);
+      if (BIAS && tid < 16)
+        cp_async_16(smem_u32(s_b2 + b * 128 + tid * 8), a.b2 + (int64_t)l_e * H + c * kPrepCols + tid * 8);
+    }
+    cp_async_commit();
+  };
+
+  float bias_acc[8];
 #pragma unroll
-      for (int i = 0; i < kPrepBatch; ++i) {
-        const int row = warp + 8 * (rb + i);
-        const int t = s_tok[row];
-        v[i] = make_uint4(0, 0, 0, 0);
-        if (t >= 0 && colok) v[i] = *reinterpret_cast<const uint4*>(src + (int64_t)t * H + col);
+  for (int k = 0; k < 8; ++k) bias_acc[k] = 0.f;
+  // the unit being processed (tile, chunk, tensor) and the one gathered ahead of it
+  int cur_tile = l_tile, cur_c = l_c, cur_w = nw == 2 ? 0 : 1;
+  issue(0, cur_c, cur_w);
+  int buf = 0;
+  while (true) {
+    // ---- advance the loader one unit and gather it into the other buffer ----
+    int nx_tile = 0, nx_c = 0, nx_w = 0;
+    bool has_next = true;
+    if (++l_j == nu) {  // next item: its tokens were fetched one item ago
+      l_j = 0;
+      l_it = p_it;
+      l_ti = p_ti;
+      l_c = p_c;
+      has_next = l_it < nitems;
+      if (has_next) {
+        l_tile = p_tile;
+        l_e = p_e;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          lt[k] = prep_token(a, pf[k]);
+          if (k == pc) l_fs = pf[k];
+        }
+        next_item(p_it, p_ti, p_c);
+        p_tile = q_tile;
+        if (p_it < nitems) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) pf[k] = a.tile_row_flat[(int64_t)p_tile * 128 + rl + 16 * k];
+          if (BIAS) p_e = a.tile_expert[p_tile];
+          int q_it = p_it, q_ti = p_ti, q_c = p_c;
+          next_item(q_it, q_ti, q_c);
+          if (q_it < nitems) q_tile = tile_of(q_ti);
+        }
       }
+    }
+    if (has_next) {
+      nx_tile = l_tile;
+      nx_c = l_c + (nw == 2 ? l_j >> 1 : l_j);
+      nx_w = nw == 2 ? (l_j & 1) : 1;
+      issue(buf ^ 1, nx_c, nx_w);
+      cp_async_wait<1>();  // this thread's pieces of the current unit have landed
+    } else {
+      cp_async_wait<0>();
+    }
+    // MXFP8: the staging buffer of this unit's parity was last read by the stores of unit u - 2
+    if (MX && tid == 0) bulk_wait_read<1>();
+    __syncthreads();  // everyone's pieces of the current unit are in
+    uint8_t* const stage = stage0 + (MX ? buf * kPrepStageMxStride : 0);
+    uint8_t* const stage_sf = stage + kPrepStageMx;  // MXFP8
+
+    const uint16_t* tb = tiles + buf * (128 * kPrepTilePitch);
+    const int64_t prow0 = (int64_t)cur_tile * 128;
+    // ---- phase A: row-major copy (codes and scales) and the rows' dot products with b2 ----
+    if (cur_w == 0 ? dout_rows : a.x_g != nullptr) {
+      void* rowdst = cur_w == 0 ? a.dout_g : a.x_g;
+      uint8_t* rowsf = cur_w == 0 ? a.dout_g_sf : a.x_g_sf;
+      const int col = cur_c * kPrepCols + pc * 8;
+      uint4 bv = make_uint4(0, 0, 0, 0);
+      if (BIAS && cur_w == 0) bv = *reinterpret_cast<const uint4*>(s_b2 + buf * 128 + pc * 8);
+      // scale of row prow0 + rl + 16k, columns col.. (a 128-aligned tile): atom (tile, chunk), byte
+      // (rl + 16 (k % 2)) * 16 + (k / 2) * 4 + pc / 4
+      uint8_t* const sfrow = MX ? rowsf + ((int64_t)cur_tile * (H >> 7) + cur_c) * 512 + rl * 16 + (pc >> 2) : nullptr;
 #pragma unroll
-      for (int i = 0; i < kPrepBatch; ++i) {
-        const int r = rb + i;
-        const int row = warp + 8 * r;
-        const int64_t prow = prow0 + row;
-        if (colok) *reinterpret_cast<uint4*>(st + row * kPrepTilePitch + lane * 8) = v[i];
-        if (which != 0 && !a.x_g) continue;  // row-major copy: dout always, x when recomputing h
-        void* rowdst = which == 0 ? a.dout_g : a.x_g;
-        uint8_t* rowsf = which == 0 ? a.dout_g_sf : a.x_g_sf;
-        const uint32_t dw[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      for (int k = 0; k < 8; ++k) {
+        const int64_t prow = prow0 + rl + 16 * k;
+        const uint4 v = *reinterpret_cast<const uint4*>(tb + (rl + 16 * k) * kPrepTilePitch + pc * 8);
+        const uint32_t dw[4] = {v.x, v.y, v.z, v.w};
         float d8[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           d8[2 * j] = __uint_as_float(dw[j] << 16);
           d8[2 * j + 1] = __uint_as_float(dw[j] & 0xFFFF0000u);
         }
-        if (BIAS && which == 0) {
+        if (BIAS && cur_w == 0) {
           const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            bias_acc[r] = fmaf(d8[2 * j], __uint_as_float(bw[j] << 16), bias_acc[r]);
-            bias_acc[r] = fmaf(d8[2 * j + 1], __uint_as_float(bw[j] & 0xFFFF0000u), bias_acc[r]);
+            bias_acc[k] = fmaf(d8[2 * j], __uint_as_float(bw[j] << 16), bias_acc[k]);
+            bias_acc[k] = fmaf(d8[2 * j + 1], __uint_as_float(bw[j] & 0xFFFF0000u), bias_acc[k]);
           }
         }
         if constexpr (MX) {
           float am = amax_tree<8>(d8);
           am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
           am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-          if (!colok) continue;
           const uint32_t byte = e8m0_byte(__float_as_uint(am), AF);
           if (rowdst) {  // no codes when G1 gathers its rows from dout quantised per token
             const float inv = e8m0_inv_scale(byte);
@@ -112,125 +243,132 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const PrepArgs a) {
             q.y = fp8x4_t<AF>(d8[4] * inv, d8[5] * inv, d8[6] * inv, d8[7] * inv);
             *reinterpret_cast<uint2*>(static_cast<uint8_t*>(rowdst) + prow * H + col) = q;
           }
-          if ((lane & 3) == 0) rowsf[sf_tiled_offset(prow, col, H)] = (uint8_t)byte;
+          if ((lane & 3) == 0) sfrow[(k & 1) * 256 + (k >> 1) * 4] = (uint8_t)byte;
         } else {
-          if (colok && rowdst) *reinterpret_cast<uint4*>(static_cast<uint16_t*>(rowdst) + prow * H + col) = v[i];
+          if (rowdst) *reinterpret_cast<uint4*>(static_cast<uint16_t*>(rowdst) + prow * H + col) = v;
         }
       }
-      }
-      __syncthreads();
-      // ---- phase 2 ---- (dout^T comes from a saved s*dout checkpoint when skip_dout_t)
-      // MXFP8: thread = one column, its four 32-row groups.  BF16: thread = a column pair (one 32-bit
-      // shared-memory word per row) and two of the groups; ncol is a multiple of 128, so a pair is whole.
-      if constexpr (MX) {
-        if (tid < ncol && !(which == 0 && a.skip_dout_t)) {
-          const int h = tid;
-          const int64_t orow = h0 + h;
-          uint8_t* outp = static_cast<uint8_t*>(which == 0 ? a.dout_gt : a.x_gt);
-          uint8_t* outsf = which == 0 ? a.dout_gt_sf : a.x_gt_sf;
-          // the tile's four 32-row groups have adjacent scale bytes (k = g in the tiled layout, the
-          // tile's first row a multiple of 128): one 32-bit store per column
-          uint32_t sfw = 0u;
-          // with biases: this column's sums of s*dout over the tile's row halves (db2's partials)
-          const bool db2 = BIAS && which == 0 && a.db2_part != nullptr;
-          float cs[2] = {0.f, 0.f};
-#pragma unroll 2
-          for (int g = 0; g < 4; ++g) {
-            float c32[32];
+      if (BIAS && cur_w == 0 && cur_c == nch - 1) {  // the tile's last chunk: ds_bias of its rows
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int row = g * 32 + j;
-              float x = bf16_bits_to_float(st[row * kPrepTilePitch + h]);
-              if (SCALE_T && which == 0) x *= s_s[row];
-              c32[j] = x;
-              if (db2) cs[g >> 1] = fmaf(x, SCALE_T ? 1.f : s_s[row], cs[g >> 1]);
-            }
-            const int64_t ocol = prow0 + g * 32;
-            uint32_t w[8];
-            const uint32_t byte = quantize_group32_t<AF>(c32, w);
-            st_global_32b(outp + orow * P + ocol, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
-            sfw |= byte << (8 * g);
-          }
-          *reinterpret_cast<uint32_t*>(outsf + sf_tiled_offset(orow, prow0, P)) = sfw;
-          if (db2) {
-            a.db2_part[((int64_t)tile * 2 + 0) * H + orow] = cs[0];
-            a.db2_part[((int64_t)tile * 2 + 1) * H + orow] = cs[1];
-          }
-        }
-      } else {
-        const int cp = tid & 127;
-        if (2 * cp < ncol && !(which == 0 && a.skip_dout_t)) {
-          uint16_t* outp = static_cast<uint16_t*>(which == 0 ? a.dout_gt : a.x_gt);
-          // db2: this thread's share of the tile's column sums of s*dout (its two 32-row groups)
-          const bool db2 = BIAS && which == 0 && a.db2_part != nullptr;
-          float cs0 = 0.f, cs1 = 0.f;
-#pragma unroll 1
-          for (int g = 2 * (tid >> 7); g < 2 * (tid >> 7) + 2; ++g) {
-            uint32_t wv[32];
+        for (int k = 0; k < 8; ++k) {
+          float v = bias_acc[k];
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              wv[j] = *reinterpret_cast<const uint32_t*>(st + (g * 32 + j) * kPrepTilePitch + 2 * cp);
-            auto elem = [&](int j, int half) {  // column 2*cp + half, row g*32 + j
-              float x = __uint_as_float(half ? (wv[j] & 0xFFFF0000u) : (wv[j] << 16));
-              if (SCALE_T && which == 0) x *= s_s[g * 32 + j];
-              return x;
-            };
-            if (db2) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float w = SCALE_T ? 1.f : s_s[g * 32 + j];  // s*dout (already scaled when SCALE_T)
-                cs0 = fmaf(elem(j, 0), w, cs0);
-                cs1 = fmaf(elem(j, 1), w, cs1);
-              }
-            }
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              uint16_t* dst = outp + (h0 + 2 * cp + half) * P + prow0 + g * 32;
-#pragma unroll
-              for (int q = 0; q < 2; ++q)
-                st_global_32b(dst + 16 * q, pack_bf16x2(elem(16 * q + 0, half), elem(16 * q + 1, half)),
-                              pack_bf16x2(elem(16 * q + 2, half), elem(16 * q + 3, half)),
-                              pack_bf16x2(elem(16 * q + 4, half), elem(16 * q + 5, half)),
-                              pack_bf16x2(elem(16 * q + 6, half), elem(16 * q + 7, half)),
-                              pack_bf16x2(elem(16 * q + 8, half), elem(16 * q + 9, half)),
-                              pack_bf16x2(elem(16 * q + 10, half), elem(16 * q + 11, half)),
-                              pack_bf16x2(elem(16 * q + 12, half), elem(16 * q + 13, half)),
-                              pack_bf16x2(elem(16 * q + 14, half), elem(16 * q + 15, half)));
-            }
-          }
-          if (db2)
-            *reinterpret_cast<float2*>(a.db2_part + ((int64_t)tile * 2 + (tid >> 7)) * H + h0 + 2 * cp) =
-                make_float2(cs0, cs1);
+          for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          // (the loader is still in this item: lt[] are this tile's tokens; padding rows give 0)
+          if (pc == 0) a.ds_bias[prow0 + rl + 16 * k] = lt[k] >= 0 ? v : 0.f;
+          bias_acc[k] = 0.f;
         }
       }
-      __syncthreads();
     }
-  }
-  if constexpr (BIAS) {
+    // ---- phase B: the transposed output through the staging tile ----
+    const bool do_t = cur_w == 1 || dout_t;
+    if (do_t) {
+      const int cp = tid & 63, g = tid >> 6;  // columns 2cp, 2cp+1; tile rows 32g .. 32g+31
+      const bool db2 = BIAS && cur_w == 0 && a.db2_part != nullptr;
+      const float* ss = s_s + buf * 128 + g * 32;
+      uint32_t wv[32];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float v = bias_acc[r];
+      for (int j = 0; j < 32; ++j)
+        wv[j] = *reinterpret_cast<const uint32_t*>(tb + (g * 32 + j) * kPrepTilePitch + 2 * cp);
+      // lanes with bit 2 of cp set write the two halves of a row's piece pair in the other order: with
+      // the swizzle, a warp's 32 16-byte stores of one instruction then cover all eight pieces of a
+      // 128-byte row position four times (no bank conflict)
+      const int flip = (cp >> 2) & 1;
+      // MXFP8 without the s factor: both columns' amax from the packed words
+      uint32_t am2 = 0u;
+      if (MX && !(SCALE_T && cur_w == 0)) am2 = bf16x2_absmax32(wv);
+      float cs[2] = {0.f, 0.f};
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      const int row = warp + 8 * r;
-      if (lane == 0) a.ds_bias[prow0 + row] = s_tok[row] >= 0 ? v : 0.f;
+      for (int q = 0; q < 2; ++q) {  // column 2cp + q = staging row r
+        float c32[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float x = __uint_as_float(q ? (wv[j] & 0xFFFF0000u) : (wv[j] << 16));
+          if (SCALE_T && cur_w == 0) x *= ss[j];
+          c32[j] = x;
+          if (db2) cs[q] = fmaf(x, SCALE_T ? 1.f : ss[j], cs[q]);
+        }
+        const int r = 2 * cp + q;
+        if constexpr (MX) {
+          uint32_t w8[8];
+          const uint32_t byte = (SCALE_T && cur_w == 0) ? quantize_group32_t<AF>(c32, w8)
+                                                        : quantize_group32_am<AF>(c32, q ? am2 & 0xFFFF0000u : am2 << 16, w8);
+          uint8_t* rowp = stage + r * 128;  // tile rows 32g.. are bytes 32g.. of the row: pieces 2g, 2g+1
+          const uint4 lo = make_uint4(w8[0], w8[1], w8[2], w8[3]), hi = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+          *reinterpret_cast<uint4*>(rowp + (((2 * g + flip) ^ (r & 7)) << 4)) = flip ? hi : lo;
+          *reinterpret_cast<uint4*>(rowp + (((2 * g + 1 - flip) ^ (r & 7)) << 4)) = flip ? lo : hi;
+          // scale byte (row r of the chunk's atom, k-group g: the tile's first row is a multiple of 128)
+          stage_sf[(r & 31) * 16 + (r >> 5) * 4 + g] = (uint8_t)byte;
+        } else {
+          // BF16: the group's 64 bytes of output row h straight to global memory, two whole sectors
+          uint16_t* dst = static_cast<uint16_t*>(cur_w == 0 ? a.dout_gt : a.x_gt) +
+                          ((int64_t)cur_c * kPrepCols + r) * P + prow0 + g * 32;
+#pragma unroll
+          for (int hq = 0; hq < 2; ++hq)
+            st_global_32b(dst + 16 * hq, pack_bf16x2(c32[16 * hq + 0], c32[16 * hq + 1]),
+                          pack_bf16x2(c32[16 * hq + 2], c32[16 * hq + 3]), pack_bf16x2(c32[16 * hq + 4], c32[16 * hq + 5]),
+                          pack_bf16x2(c32[16 * hq + 6], c32[16 * hq + 7]), pack_bf16x2(c32[16 * hq + 8], c32[16 * hq + 9]),
+                          pack_bf16x2(c32[16 * hq + 10], c32[16 * hq + 11]),
+                          pack_bf16x2(c32[16 * hq + 12], c32[16 * hq + 13]),
+                          pack_bf16x2(c32[16 * hq + 14], c32[16 * hq + 15]));
+        }
+      }
+      if (db2)
+        *reinterpret_cast<float2*>(a.db2_part + ((int64_t)cur_tile * 4 + g) * H + cur_c * kPrepCols + 2 * cp) =
+            make_float2(cs[0], cs[1]);
     }
+    if (MX) fence_proxy_async_smem();  // staged bytes are read by the bulk copies (async proxy)
+    __syncthreads();                    // phase A and B reads of the buffer, and the staging writes, are done
+    if (MX && do_t && tid == 0) {
+      const void* tm = cur_w == 0 ? static_cast<const void*>(&tm_dout_gt) : static_cast<const void*>(&tm_x_gt);
+      tma_store_2d(tm, stage, (int)prow0, cur_c * kPrepCols);
+      uint8_t* outsf = cur_w == 0 ? a.dout_gt_sf : a.x_gt_sf;
+      bulk_store(outsf + ((int64_t)cur_c * (P >> 7) + cur_tile) * 512, stage_sf, 512);
+      bulk_commit();
+    }
+    if (!has_next) break;
+    cur_tile = nx_tile;
+    cur_c = nx_c;
+    cur_w = nx_w;
+    buf ^= 1;
   }
+  if (MX && tid == 0) bulk_wait_all();  // the last bulk stores complete before the CTA exits
 }
 
 template <bool MX, bool SCALE_T, bool BIAS>
 static int prep_launch(const PrepArgs& a, int grid, cudaStream_t st) {
   auto k = (!MX || a.fmt == MOE_FP8_E5M2) ? prep_kernel<MX, SCALE_T, BIAS, MOE_FP8_E5M2>
                                           : prep_kernel<MX, SCALE_T, BIAS, MOE_FP8_E4M3>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+  // MXFP8: tensor maps of the transposed [H, P] code matrices, boxes of 128 rows x 128 bytes, 128-byte swizzle
+  alignas(64) CUtensorMap tm_dgt, tm_xgt;
+  std::memset(&tm_dgt, 0, sizeof(tm_dgt));
+  std::memset(&tm_xgt, 0, sizeof(tm_xgt));
+  if (MX) {
+    if (!a.skip_dout_t &&
+        !make_tmap_2d(&tm_dgt, a.dout_gt, 1, (uint64_t)a.H, (uint64_t)a.P, (uint64_t)a.P, 128, 128, true))
+      return MOE_ERR_INVALID;
+    if (!make_tmap_2d(&tm_xgt, a.x_gt, 1, (uint64_t)a.H, (uint64_t)a.P, (uint64_t)a.P, 128, 128, true))
+      return MOE_ERR_INVALID;
+  }
+  const int smem = prep_smem_bytes<MX>();
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_check(e, "prep attribute");
-  return launch_pdl(k, dim3(grid), dim3(256), kPrepSmem, st, "prep", a);
+  return launch_pdl(k, dim3(grid), dim3(256), smem, st, "prep", a, tm_dgt, tm_xgt);
 }
 
-int launch_prep(const PrepArgs& a, cudaStream_t st) {
-  const int grid = (int)(a.P / 128);
-  if (grid == 0) return MOE_OK;
+int launch_prep(const PrepArgs& args, cudaStream_t st) {
+  const int64_t tiles = args.P / 128;
+  if (tiles == 0) return MOE_OK;
+  PrepArgs a = args;
+  // f / K for 0 <= f < 2^31: with l = ceil(log2 K) and m = ceil(2^(31+l) / K) (< 2^32), the quotient
+  // is floor(f m / 2^(31+l)): m K - 2^(31+l) < K <= 2^l keeps the error term below 1/K
+  int l = 0;
+  while ((1ll << l) < a.K) ++l;
+  a.k_shift = l;
+  a.k_mul = l == 0 ? 0u : (uint32_t)(((1ull << (31 + l)) + (uint64_t)a.K - 1) / (uint64_t)a.K);
   const bool bias = a.ds_bias != nullptr;
+  const int64_t items = bias ? tiles : tiles * (a.H / kPrepCols);
+  const int grid = (int)std::min<int64_t>(items, 2 * (int64_t)device_sm_count());
   if (a.mx) {
     if (a.scale_t) return bias ? prep_launch<true, true, true>(a, grid, st) : prep_launch<true, true, false>(a, grid, st);
     return bias ? prep_launch<true, false, true>(a, grid, st) : prep_launch<true, false, false>(a, grid, st);
