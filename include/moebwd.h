@@ -304,7 +304,7 @@ enum {
   MOE_WS_X_GT_SF,
   MOE_WS_DH,                 /* G2 A operand: dh [P,2I] */
   MOE_WS_DH_SF,
-  MOE_WS_DH_T,               /* G4 B operand: dh^T [2I,P] */
+  MOE_WS_DH_T,               /* G4 B operand: dh^T [2I,P] (empty for BF16 under MOE_OPT_MN_OPERANDS, the default) */
   MOE_WS_DH_T_SF,
   MOE_WS_AP_T,               /* G3 A operand: a'^T [I,P] (s*a for affinity on I, a on H) */
   MOE_WS_AP_T_SF,
@@ -413,6 +413,9 @@ enum {
   MOE_OPT_PDL,               /* 1 (default): the kernels of a call are launched with programmatic dependent
                                 launch (each may be scheduled while the previous one finishes and waits on
                                 the device for its results); 0: plain stream order */
+  MOE_OPT_MN_OPERANDS,       /* BF16: 1 (default) the dW1 GEMM reads dh [P,2I] itself as an MN-major operand
+                                (no transposed dh^T copy is written; the workspace's DH_T region is empty);
+                                0: dh^T is built by the dA GEMM's epilogue as for MXFP8 */
   MOE_NUM_OPTIONS
 };
 /* Set an option; value -1 restores its default.  MOE_ERR_INVALID for an unknown option or value. */

@@ -276,6 +276,35 @@ __device__ __forceinline__ void store_transposed(float* buf, const float (&v)[NC
   __syncwarp();
 }
 
+// Column sums over the warp's 32 lanes (rows) of 2 * NC values per lane (a, then b), by a butterfly
+// reduce-scatter: lane l returns the sum of value l % (2 NC) (2 NC = 16: the lane halves folded first).
+template <int NC>
+__device__ __forceinline__ float colsum_butterfly(const float (&a)[NC], const float (&b)[NC], int lane) {
+  constexpr int NV = 2 * NC;
+  static_assert(NV == 16 || NV == 32, "16 or 32 values");
+  float v[NV];
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    v[i] = a[i];
+    v[NC + i] = b[i];
+  }
+  if constexpr (NV == 16) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], 16);
+  }
+#pragma unroll
+  for (int w = NV / 2; w >= 1; w >>= 1) {  // lane bit w picks the half of the values this lane keeps
+    const bool up = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = up ? v[i] : v[i + w];
+      const float keep = up ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
+
 template <int NTHREADS>
 __device__ __forceinline__ void group_bar(int id) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(NTHREADS) : "memory");
@@ -488,9 +517,15 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
   constexpr int TB = SHARED_TBUF ? 0 : NC * kTransPitch;
   // db1 (BF16 with biases): this tile's and lane quarter's column sums of dh, in W1's layout
   float* db1p = p.db1_part ? p.db1_part + ((prow >> 7) * 4 + (m >> 5)) * (2 * (int64_t)I) : nullptr;
-  store_transposed<MX, NC, AF>(tbuf, dg, p.dht, p.dht_sf, P, il ? 2 * c0 : c0, il ? 2 : 1, p0, lane, db1p);
-  store_transposed<MX, NC, AF>(tbuf + TB, du, p.dht, p.dht_sf, P, il ? 2 * c0 + 1 : I + c0, il ? 2 : 1, p0, lane,
-                               db1p);
+  if (p.dht) {
+    store_transposed<MX, NC, AF>(tbuf, dg, p.dht, p.dht_sf, P, il ? 2 * c0 : c0, il ? 2 : 1, p0, lane, db1p);
+    store_transposed<MX, NC, AF>(tbuf + TB, du, p.dht, p.dht_sf, P, il ? 2 * c0 + 1 : I + c0, il ? 2 : 1, p0, lane,
+                                 db1p);
+  } else if (db1p) {  // no dh^T (BF16: the weight-gradient GEMM reads dh): the quarter's column sums
+    const float v = colsum_butterfly<NC>(dg, du, lane);
+    const int idx = lane, f = idx % NC, gu = idx / NC;  // value idx: dg[f] (gu = 0) or du[f] (gu = 1)
+    if (idx < 2 * NC) db1p[il ? 2 * (c0 + f) + gu : gu * I + c0 + f] = v;
+  }
   if (p.apt)  // a'^T (null: built from a saved checkpoint of a or s*a)
     store_transposed<MX, NC, AF>(tbuf + 2 * TB, ap, p.apt, p.apt_sf, P, c0, 1, p0, lane);
 }
@@ -717,8 +752,19 @@ __global__ void __launch_bounds__((GemmCfg<MX, BN, EPI>::THREADS), 1) __maxnreg_
           }
           mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
           const int kc = ti.k0 + kb * C::BKE;
-          tma_load_2d(smA + s * C::A_BYTES, &tmA, &full[s], kc, ti.a_row);
-          tma_load_2d(smB + s * C::B_BYTES, &tmB, &full[s], kc, ti.b_row);
+          if (!MX && p.a_mn) {  // [K, M] operand: 64 x 64 boxes, 8 KB apart along M
+#pragma unroll
+            for (int j = 0; j < 2; ++j) tma_load_2d(smA + s * C::A_BYTES + j * 8192, &tmA, &full[s], ti.a_row + 64 * j, kc);
+          } else {
+            tma_load_2d(smA + s * C::A_BYTES, &tmA, &full[s], kc, ti.a_row);
+          }
+          if (!MX && p.b_mn) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(smB + s * C::B_BYTES + j * 8192, &tmB, &full[s], ti.b_row + 64 * j, kc);
+          } else {
+            tma_load_2d(smB + s * C::B_BYTES, &tmB, &full[s], kc, ti.b_row);
+          }
           if constexpr (MX) {
             const int kt = kc / 128;
             bulk_load(smSFA + s * C::SFA_BYTES, p.sfa + ((int64_t)(ti.a_row / 128) * p.sfa_ktiles + kt) * 512, 512,
@@ -789,9 +835,12 @@ __global__ void __launch_bounds__((GemmCfg<MX, BN, EPI>::THREADS), 1) __maxnreg_
                        idesc_mxf8(128, BN, (uint32_t)p.fmt_a, (uint32_t)p.fmt_b, (uint32_t)kk, (uint32_t)kk), sfa_t,
                        sfb_t, (kb | kk) != 0);
           } else {
+            // K step kk: 32 bytes into each 128-byte K-major row, or two 8-row atoms of an MN-major tile
+            const uint32_t idesc = idesc_bf16(128, BN, (uint32_t)p.a_mn, (uint32_t)p.b_mn);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16(d, kmajor_sw128_desc(a0 + kk * 32), kmajor_sw128_desc(b0 + kk * 32), idesc_bf16(128, BN),
+              mma_bf16(d, p.a_mn ? mnmajor_sw128_desc(a0 + kk * 2048, 8192) : kmajor_sw128_desc(a0 + kk * 32),
+                       p.b_mn ? mnmajor_sw128_desc(b0 + kk * 2048, 8192) : kmajor_sw128_desc(b0 + kk * 32), idesc,
                        (kb | kk) != 0);
           }
           mma_commit(&empty[s]);

@@ -251,8 +251,21 @@ __global__ void __launch_bounds__(PairCfg<MX, BN, EPI>::THREADS, 1)
           if (leader) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE_BYTES);
           const uint32_t fb = lead_full + (uint32_t)(s * 8);
           const int kc = ti.k0 + kb * C::BKE;
-          tma_load_2d_pair(smA + s * C::A_BYTES, &tmA, fb, kc, ti.a_row);
-          tma_load_2d_pair(smB + s * C::B_BYTES, &tmB, fb, kc, ti.b_base + (BN / 2) * (int)rank);
+          if (!MX && p.a_mn) {  // [K, M] operand: 64 x 64 boxes, 8 KB apart along M
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d_pair(smA + s * C::A_BYTES + j * 8192, &tmA, fb, ti.a_row + 64 * j, kc);
+          } else {
+            tma_load_2d_pair(smA + s * C::A_BYTES, &tmA, fb, kc, ti.a_row);
+          }
+          if (!MX && p.b_mn) {  // this CTA's BN / 2 columns of the [K, N] operand
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j)
+              tma_load_2d_pair(smB + s * C::B_BYTES + j * 8192, &tmB, fb, ti.b_base + (BN / 2) * (int)rank + 64 * j,
+                               kc);
+          } else {
+            tma_load_2d_pair(smB + s * C::B_BYTES, &tmB, fb, kc, ti.b_base + (BN / 2) * (int)rank);
+          }
           if constexpr (MX) {
             const int kt = kc / 128;
             tma_load_2d_pair(smSFA + s * C::SFA_BYTES, &tmSFA, fb, 0, (ti.a_row / 128) * p.sfa_ktiles + kt);
@@ -322,10 +335,13 @@ __global__ void __launch_bounds__(PairCfg<MX, BN, EPI>::THREADS, 1)
                             idesc_mxf8(256, C::BN, (uint32_t)p.fmt_a, (uint32_t)p.fmt_b, (uint32_t)kk, (uint32_t)kk),
                             sfa_t, sfb_t, (kb | kk) != 0);
           } else {
+            // K step kk: 32 bytes into each 128-byte K-major row, or two 8-row atoms of an MN-major tile
+            const uint32_t idesc = idesc_bf16(256, C::BN, (uint32_t)p.a_mn, (uint32_t)p.b_mn);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_pair(d, kmajor_sw128_desc(a0 + kk * 32), kmajor_sw128_desc(b0 + kk * 32),
-                            idesc_bf16(256, C::BN), (kb | kk) != 0);
+              mma_bf16_pair(d, p.a_mn ? mnmajor_sw128_desc(a0 + kk * 2048, 8192) : kmajor_sw128_desc(a0 + kk * 32),
+                            p.b_mn ? mnmajor_sw128_desc(b0 + kk * 2048, 8192) : kmajor_sw128_desc(b0 + kk * 32), idesc,
+                            (kb | kk) != 0);
           }
           mma_commit_pair(mapa_shared(smem_u32(&empty[s]), 0));
           mma_commit_pair(mapa_shared(smem_u32(&empty[s]), 1));

@@ -52,6 +52,7 @@ static const int64_t kOptDefault[MOE_NUM_OPTIONS] = {
     0,                      // MOE_OPT_G1_GATHER (measured slower: see the option's comment)
     0,                      // MOE_OPT_G1_WARPS (automatic)
     1,                      // MOE_OPT_PDL
+    1,                      // MOE_OPT_MN_OPERANDS
 };
 static std::once_flag g_opt_once;
 static void opt_init() {
@@ -76,7 +77,8 @@ static bool option_value_ok(int o, int64_t v) {
     case MOE_OPT_G4_TILE_N: return v == 0 || v == 128 || v == 256;
     case MOE_OPT_PREP_TILE_ORDER:
     case MOE_OPT_G1_GATHER:
-    case MOE_OPT_PDL: return v == 0 || v == 1;
+    case MOE_OPT_PDL:
+    case MOE_OPT_MN_OPERANDS: return v == 0 || v == 1;
     case MOE_OPT_G1_WARPS: return v == 0 || v == 8 || v == 16;
     default: return false;
   }

@@ -43,10 +43,14 @@ int launch_gemm(bool mx, int BN, const GemmParams& p_in, const void* A, int64_t 
   const uint32_t bke = mx ? 128 : 64;
   const bool pair = use_pair(mx, BN, p);
   const int pbn = pair ? pair_bn() : BN;
-  if (!make_tmap_2d(&ta, A, es, (uint64_t)a_rows, (uint64_t)a_cols, (uint64_t)a_cols * es, 128, bke))
+  if (mx && (p.a_mn || p.b_mn)) return fail(MOE_ERR_UNSUPPORTED, "MN-major operands are BF16-only");
+  // K-major operand: [rows, K] boxes of the tile's rows x one K stage; MN-major ([K, M] / [K, N]):
+  // 64 x 64 boxes (a K stage of rows, 64 columns)
+  if (!make_tmap_2d(&ta, A, es, (uint64_t)a_rows, (uint64_t)a_cols, (uint64_t)a_cols * es, p.a_mn ? 64 : 128,
+                    p.a_mn ? 64 : bke))
     return MOE_ERR_INVALID;
   if (!make_tmap_2d(&tb, B, es, (uint64_t)b_rows, (uint64_t)b_cols, (uint64_t)b_cols * es,
-                    pair ? (uint32_t)pbn / 2 : (uint32_t)BN, bke))
+                    p.b_mn ? 64 : pair ? (uint32_t)pbn / 2 : (uint32_t)BN, p.b_mn ? 64 : bke))
     return MOE_ERR_INVALID;
   if (ckpt) {  // checkpoint chunks: 32 features x 128 rows of the [N*2*I, B] view, unswizzled
     if (!make_tmap_2d(&tc, ckpt, 2, (uint64_t)ck_rows, (uint64_t)ck_cols, (uint64_t)ck_cols * 2, 32, 128, false))
@@ -101,6 +105,7 @@ struct Layout {
   int64_t P, Nb, TK;
   int BN1, BN2, BN3, BN4;
   bool gather;  // G1 gathers its dout rows (MOE_OPT_G1_GATHER)
+  bool mn;      // BF16: the weight-gradient GEMMs read row-major operands MN-major (MOE_OPT_MN_OPERANDS)
   int g1_groups; // G1 epilogue warp groups: 2 (sixteen warps) or 1 (MOE_OPT_G1_WARPS)
 };
 
@@ -161,12 +166,13 @@ static Layout make_layout(const MoeBwdArgs& a) {
   b[R_TILE_ROW_FLAT] = sizeof(int32_t) * (size_t)std::max<int64_t>(1, P);
   b[R_TILE_EXPERT] = sizeof(int32_t) * (size_t)(P / kTileM + 1);
   L.gather = option(MOE_OPT_G1_GATHER) != 0;
+  L.mn = !mx && option(MOE_OPT_MN_OPERANDS) != 0;
   b[R_DOUT_G] = L.gather ? 0 : (size_t)(P * H * es);
   b[R_DOUT_Q] = (L.gather && mx) ? (size_t)((int64_t)a.T * H) : 0;  // dout codes per token
   b[R_DOUT_GT] = (size_t)(H * P * es);
   b[R_X_GT] = (size_t)(H * P * es);
   b[R_DH] = (size_t)(P * 2 * I * es);
-  b[R_DH_T] = (size_t)(2 * I * P * es);
+  b[R_DH_T] = L.mn ? 0 : (size_t)(2 * I * P * es);  // BF16: G4 reads dh itself (MN-major)
   b[R_AP_T] = (size_t)(I * P * es);
   if (mx) {
     b[R_DOUT_G_SF] = (size_t)(P * H / 32);
@@ -682,7 +688,11 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.accumulate = a.accumulate;
     p.tile_counter = counters + 3;
     p.status = a.status_dev;
-    if ((rc = launch_gemm(mx, L.BN4, p, reg<void>(L, ws, R_X_GT), H, P, reg<void>(L, ws, R_DH_T), 2 * I, P, st)))
+    // BF16 (MN_OPERANDS): B is dh itself, [P, 2I] read MN-major (no transposed copy); else dh^T (for
+    // MXFP8 quantised along tokens)
+    p.b_mn = L.mn;
+    if ((rc = L.mn ? launch_gemm(mx, L.BN4, p, reg<void>(L, ws, R_X_GT), H, P, reg<void>(L, ws, R_DH), P, 2 * I, st)
+                   : launch_gemm(mx, L.BN4, p, reg<void>(L, ws, R_X_GT), H, P, reg<void>(L, ws, R_DH_T), 2 * I, P, st)))
       return rc;
   }
   prof_mark(st, slot, 7);

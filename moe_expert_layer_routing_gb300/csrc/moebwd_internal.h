@@ -222,6 +222,9 @@ struct GemmParams {
   const void* a_gather;
   int64_t a_gather_ld;
   int a_gather_div;
+  // BF16: operand A (B) stored MN-major, i.e. as the [K, M] ([K, N]) matrix with M (N) contiguous,
+  // read through 64 x 64 tensor-map boxes and the tensor core's MN-major descriptors
+  int a_mn, b_mn;
 };
 
 // A [rows, K] and B [rows, K] K-major operands (bf16 or fp8 bytes), tile counts in p.

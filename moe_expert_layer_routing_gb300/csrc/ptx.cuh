@@ -276,9 +276,18 @@ __device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t saddr) {
   return make_smem_desc(saddr, 16, 1024, kSwizzle128B);
 }
 
-// Instruction descriptor, kind::f16 with BF16 A/B and FP32 D, both operands K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// MN-major operand tile with 128B swizzle: atoms of 64 elements along MN (128 bytes) by 8 along K
+// (1024 bytes), the atoms along MN mn_stride bytes apart (leading byte offset), along K 1024 apart
+// (stride byte offset); a K step of 16 advances the start by two atoms (2048 bytes).
+__device__ __forceinline__ uint64_t mnmajor_sw128_desc(uint32_t saddr, uint32_t mn_stride) {
+  return make_smem_desc(saddr, mn_stride, 1024, kSwizzle128B);
+}
+
+// Instruction descriptor, kind::f16 with BF16 A/B and FP32 D; a_mn / b_mn: that operand MN-major
+// (bits 15 / 16), else K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, uint32_t a_mn = 0, uint32_t b_mn = 0) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn << 15) | (b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
 }
 
 // Instruction descriptor, kind::mxf8f6f4 block-scaled, E8M0 scales, both operands K-major.
