@@ -298,15 +298,19 @@ enum {
   MOE_WS_FLAT_TILE_ROW,      /* int32 [T*K] flat -> tile row, -1 invalid id */
   MOE_WS_DOUT_G,             /* G1 A operand: dout rows [P,H] (bf16 | fp8); empty with MOE_OPT_G1_GATHER = 1 */
   MOE_WS_DOUT_G_SF,          /*   its tiled scales (MXFP8) */
-  MOE_WS_DOUT_GT,            /* G3 B operand: [H,P] (bf16 | fp8), s-scaled for affinity on H */
+  MOE_WS_DOUT_GT,            /* G3 B operand: [H,P] (bf16 | fp8), s-scaled for affinity on H; BF16 under
+                                MOE_OPT_MN_OPERANDS: the rows [P,H] of s*dout (affinity on H; dout rows
+                                when G1 gathers its own), unused for affinity on I (G3 reads DOUT_G) */
   MOE_WS_DOUT_GT_SF,
-  MOE_WS_X_GT,               /* G4 A operand: [H,P] */
+  MOE_WS_X_GT,               /* G4 A operand: [H,P]; BF16 under MOE_OPT_MN_OPERANDS: x's gathered rows [P,H]
+                                (unused when h is recomputed: G4 reads X_G) */
   MOE_WS_X_GT_SF,
   MOE_WS_DH,                 /* G2 A operand: dh [P,2I] */
   MOE_WS_DH_SF,
   MOE_WS_DH_T,               /* G4 B operand: dh^T [2I,P] (empty for BF16 under MOE_OPT_MN_OPERANDS, the default) */
   MOE_WS_DH_T_SF,
-  MOE_WS_AP_T,               /* G3 A operand: a'^T [I,P] (s*a for affinity on I, a on H) */
+  MOE_WS_AP_T,               /* G3 A operand: a'^T [I,P] (s*a for affinity on I, a on H); BF16 under
+                                MOE_OPT_MN_OPERANDS: a' rows [P,I] */
   MOE_WS_AP_T_SF,
   MOE_WS_DX_EXP,             /* G2 output: dx_expanded [P,H] bf16 */
   MOE_WS_X_G,                /* RECOMPUTE: G0 A operand, gathered x rows [P,H] (bf16 | fp8) */
@@ -413,9 +417,13 @@ enum {
   MOE_OPT_PDL,               /* 1 (default): the kernels of a call are launched with programmatic dependent
                                 launch (each may be scheduled while the previous one finishes and waits on
                                 the device for its results); 0: plain stream order */
-  MOE_OPT_MN_OPERANDS,       /* BF16: 1 (default) the dW1 GEMM reads dh [P,2I] itself as an MN-major operand
-                                (no transposed dh^T copy is written; the workspace's DH_T region is empty);
-                                0: dh^T is built by the dA GEMM's epilogue as for MXFP8 */
+  MOE_OPT_MN_OPERANDS,       /* BF16: 1 (default) the weight-gradient GEMMs read their token-major operands
+                                as row-major [tokens, features] matrices through the tensor core's MN-major
+                                layout: dW1 reads x's gathered rows and dh itself, dW2 reads a' rows and
+                                dout (s*dout for affinity on H) rows, so prep builds no transposed copies
+                                and the dA GEMM no dh^T or a'^T (the DH_T region is empty; X_GT, DOUT_GT
+                                and AP_T hold rows; operands made from saved checkpoints stay transposed);
+                                0: transposed copies as for MXFP8 */
   MOE_NUM_OPTIONS
 };
 /* Set an option; value -1 restores its default.  MOE_ERR_INVALID for an unknown option or value. */

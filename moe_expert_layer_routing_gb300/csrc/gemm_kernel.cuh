@@ -526,8 +526,18 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
     const int idx = lane, f = idx % NC, gu = idx / NC;  // value idx: dg[f] (gu = 0) or du[f] (gu = 1)
     if (idx < 2 * NC) db1p[il ? 2 * (c0 + f) + gu : gu * I + c0 + f] = v;
   }
-  if (p.apt)  // a'^T (null: built from a saved checkpoint of a or s*a)
-    store_transposed<MX, NC, AF>(tbuf + 2 * TB, ap, p.apt, p.apt_sf, P, c0, 1, p0, lane);
+  if (p.apt) {  // a'^T (null: built from a saved checkpoint of a or s*a)
+    if (!MX && p.ap_rows) {  // BF16 whose dW2 GEMM reads a' MN-major: the row's NC features of a'
+      uint16_t* dst = static_cast<uint16_t*>(p.apt) + prow * (int64_t)I + c0;
+      auto pa2 = [&](int j) { return pack_bf16x2(ap[j], ap[j + 1]); };
+      if constexpr (NC == 16)
+        st_global_32b(dst, pa2(0), pa2(2), pa2(4), pa2(6), pa2(8), pa2(10), pa2(12), pa2(14));
+      else
+        *reinterpret_cast<uint4*>(dst) = make_uint4(pa2(0), pa2(2), pa2(4), pa2(6));
+    } else {
+      store_transposed<MX, NC, AF>(tbuf + 2 * TB, ap, p.apt, p.apt_sf, P, c0, 1, p0, lane);
+    }
+  }
 }
 
 

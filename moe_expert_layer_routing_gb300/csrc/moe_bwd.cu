@@ -506,6 +506,18 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   pa.x_g_sf = rec ? reg<uint8_t>(L, ws, R_X_G_SF) : nullptr;
   pa.skip_dout_t = a.down_proj_act_ckpt != nullptr;
   pa.db2_part = (a.has_bias && !pa.skip_dout_t) ? reg<float>(L, ws, R_DB2_PART) : nullptr;
+  // BF16 with MN-major weight-gradient operands: no transposed copies; x rows for the dW1 GEMM (the
+  // recomputation's copy when there is one, else in the X_GT region), the dW2 GEMM's B rows (s*dout
+  // for affinity on H, or dout when G1 gathers its rows and writes no dout_g) in the DOUT_GT region
+  void* x_rows = L.mn ? (rec ? reg<void>(L, ws, R_X_G) : reg<void>(L, ws, R_X_GT)) : nullptr;
+  void* g3_b_rows = nullptr;
+  if (L.mn && !pa.skip_dout_t)
+    g3_b_rows = (a.affinity == MOE_AFFINITY_ON_H || L.gather) ? reg<void>(L, ws, R_DOUT_GT) : reg<void>(L, ws, R_DOUT_G);
+  if (L.mn) {
+    pa.no_t = 1;
+    pa.x_g = x_rows;
+    pa.dout_b = g3_b_rows == reg<void>(L, ws, R_DOUT_GT) ? g3_b_rows : nullptr;
+  }
   if ((rc = launch_prep(pa, st))) return rc;
   if (L.gather && mx &&  // the rows G1 gathers: dout quantised once per token (the scales come from prep)
       (rc = launch_quant_rowwise(pa.dout, a.T, a.T, H, H, nullptr, a.fp8_act, reg<uint8_t>(L, ws, R_DOUT_Q), nullptr,
@@ -603,6 +615,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.dh = reg<void>(L, ws, R_DH); p.dh_sf = reg<uint8_t>(L, ws, R_DH_SF);
     p.dht = reg<void>(L, ws, R_DH_T); p.dht_sf = reg<uint8_t>(L, ws, R_DH_T_SF);
     p.apt = inter ? nullptr : reg<void>(L, ws, R_AP_T);
+    p.ap_rows = L.mn;  // BF16: a' rows [P,I] for the dW2 GEMM's MN-major read
     p.apt_sf = inter ? nullptr : reg<uint8_t>(L, ws, R_AP_T_SF);
     p.ds_part = reg<float>(L, ws, R_DS_PART);
     p.db1_part = a.has_bias ? reg<float>(L, ws, R_DB1_PART) : nullptr;
@@ -640,7 +653,12 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.accumulate = a.accumulate;
     p.tile_counter = counters + 1;
     p.status = a.status_dev;
-    if ((rc = launch_gemm(mx, L.BN3, p, reg<void>(L, ws, R_AP_T), I, P, reg<void>(L, ws, R_DOUT_GT), H, P, st)))
+    // BF16 (MN_OPERANDS): a' rows and the dout rows read MN-major, except operands built from saved
+    // checkpoints (a'^T from the intermediate, dout^T from down_proj_act), which stay transposed
+    p.a_mn = L.mn && !inter;
+    p.b_mn = g3_b_rows != nullptr;
+    if ((rc = launch_gemm(mx, L.BN3, p, reg<void>(L, ws, R_AP_T), p.a_mn ? P : I, p.a_mn ? I : P,
+                          p.b_mn ? g3_b_rows : reg<void>(L, ws, R_DOUT_GT), p.b_mn ? P : H, p.b_mn ? H : P, st)))
       return rc;
   }
   prof_mark(st, slot, 5);
@@ -690,8 +708,8 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.status = a.status_dev;
     // BF16 (MN_OPERANDS): B is dh itself, [P, 2I] read MN-major (no transposed copy); else dh^T (for
     // MXFP8 quantised along tokens)
-    p.b_mn = L.mn;
-    if ((rc = L.mn ? launch_gemm(mx, L.BN4, p, reg<void>(L, ws, R_X_GT), H, P, reg<void>(L, ws, R_DH), P, 2 * I, st)
+    p.a_mn = p.b_mn = L.mn;  // BF16: x rows and dh, both read MN-major
+    if ((rc = L.mn ? launch_gemm(mx, L.BN4, p, x_rows, P, H, reg<void>(L, ws, R_DH), P, 2 * I, st)
                    : launch_gemm(mx, L.BN4, p, reg<void>(L, ws, R_X_GT), H, P, reg<void>(L, ws, R_DH_T), 2 * I, P, st)))
       return rc;
   }
@@ -709,7 +727,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   if (a.has_bias) {  // per-expert sums of the per-tile partials (dout_gt read again only when it was not built here)
     if (pa.db2_part) {  // db1 and db2 from their per-tile partials in one launch
       rc = launch_bias_parts_reduce(reg<float>(L, ws, R_DB1_PART), 4, 2 * I, tile_offsets, (int)E, a.db1, st,
-                                    a.accumulate, pa.db2_part, 4, H, a.db2);
+                                    a.accumulate, pa.db2_part, L.mn ? 1 : 4, H, a.db2);
     } else {
       if ((rc = launch_bias_parts_reduce(reg<float>(L, ws, R_DB1_PART), 4, 2 * I, tile_offsets, (int)E, a.db1, st,
                                          a.accumulate)))

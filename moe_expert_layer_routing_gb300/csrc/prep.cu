@@ -50,8 +50,9 @@ constexpr int kPrepTile = 128 * kPrepTilePitch * 2;  // bytes of one unit buffer
 constexpr int kPrepStageMx = 128 * 128;
 constexpr int kPrepStageMxStride = 17 * 1024;
 template <bool MX>
-constexpr int prep_smem_bytes() {  // 1024-byte alignment slack, staging, two unit buffers, s and b2 per buffer
-  return 1024 + (MX ? 2 * kPrepStageMxStride : 0) + 2 * kPrepTile + 2 * 128 * 4 + 2 * 128 * 2;
+constexpr int prep_smem_bytes() {  // 1024-byte alignment slack, staging (MXFP8) or the column-sum scratch
+                                   // (BF16), two unit buffers, s and b2 per buffer
+  return 1024 + (MX ? 2 * kPrepStageMxStride : 8 * 128 * 4) + 2 * kPrepTile + 2 * 128 * 4 + 2 * 128 * 2;
 }
 
 __device__ __forceinline__ int prep_token(const PrepArgs& a, int f) {
@@ -73,15 +74,17 @@ __global__ void __launch_bounds__(256, 2)
   extern __shared__ uint4 prep_smem[];
   uint8_t* const stage0 =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(prep_smem) + 1023) & ~uintptr_t(1023));
-  uint16_t* const tiles = reinterpret_cast<uint16_t*>(stage0 + (MX ? 2 * kPrepStageMxStride : 0));
+  uint16_t* const tiles = reinterpret_cast<uint16_t*>(stage0 + (MX ? 2 * kPrepStageMxStride : 8 * 128 * 4));
+  float* const colred = reinterpret_cast<float*>(stage0);  // BF16: [8 warps][128] column partial sums
   float* const s_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tiles) + 2 * kPrepTile);  // [2][128]
   uint16_t* const s_b2 = reinterpret_cast<uint16_t*>(s_s + 2 * 128);                                 // [2][128]
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rl = tid >> 4;  // this thread gathers and row-quantises rows rl + 16k (k < 8) of a unit ...
   const int pc = tid & 15;  // ... their 16-byte piece pc (columns 8pc .. 8pc+7 of the chunk)
   const bool need_s = SCALE_T || (BIAS && a.db2_part != nullptr);  // s per tile row in dout's phase B
-  const bool dout_t = !a.skip_dout_t;
-  const bool dout_rows = MX || a.dout_g != nullptr || BIAS;  // phase A has work on dout
+  const bool dout_t = !a.skip_dout_t && !a.no_t;
+  const bool dout_rows = MX || a.dout_g != nullptr || BIAS || a.dout_b != nullptr;  // phase A has work on dout
+  const bool db2_rows = !MX && BIAS && a.no_t && a.db2_part != nullptr;  // db2's partials in phase A
   const int nw = (dout_t || dout_rows) ? 2 : 1;             // units per chunk: dout (if any work), x
   const int nu = (BIAS ? nch : 1) * nw;                      // units per item
   const int G = (int)gridDim.x;
@@ -212,6 +215,9 @@ __global__ void __launch_bounds__(256, 2)
       // scale of row prow0 + rl + 16k, columns col.. (a 128-aligned tile): atom (tile, chunk), byte
       // (rl + 16 (k % 2)) * 16 + (k / 2) * 4 + pc / 4
       uint8_t* const sfrow = MX ? rowsf + ((int64_t)cur_tile * (H >> 7) + cur_c) * 512 + rl * 16 + (pc >> 2) : nullptr;
+      float cs8[8];  // db2_rows: this thread's column sums of s*dout over its eight rows
+#pragma unroll
+      for (int j = 0; j < 8; ++j) cs8[j] = 0.f;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const int64_t prow = prow0 + rl + 16 * k;
@@ -246,6 +252,35 @@ __global__ void __launch_bounds__(256, 2)
           if ((lane & 3) == 0) sfrow[(k & 1) * 256 + (k >> 1) * 4] = (uint8_t)byte;
         } else {
           if (rowdst) *reinterpret_cast<uint4*>(static_cast<uint16_t*>(rowdst) + prow * H + col) = v;
+          if (cur_w == 0 && (a.dout_b || db2_rows)) {
+            const float sr = s_s[buf * 128 + rl + 16 * k];
+            if (a.dout_b) {  // the dW2 GEMM's B rows: s*dout in fp32, rounded (affinity on H), else dout
+              uint4 o = v;
+              if (SCALE_T)
+                o = make_uint4(pack_bf16x2(d8[0] * sr, d8[1] * sr), pack_bf16x2(d8[2] * sr, d8[3] * sr),
+                               pack_bf16x2(d8[4] * sr, d8[5] * sr), pack_bf16x2(d8[6] * sr, d8[7] * sr));
+              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dout_b) + prow * H + col) = o;
+            }
+            if (db2_rows) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) cs8[j] = fmaf(d8[j], sr, cs8[j]);
+            }
+          }
+        }
+      }
+      if (db2_rows && cur_w == 0) {  // the tile's column sums of s*dout: lane pairs, then the eight warps
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cs8[j] += __shfl_xor_sync(0xffffffffu, cs8[j], 16);
+        if (lane < 16) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) colred[warp * 128 + pc * 8 + j] = cs8[j];
+        }
+        __syncthreads();
+        if (tid < 128) {
+          float v = 0.f;
+#pragma unroll
+          for (int w = 0; w < 8; ++w) v += colred[w * 128 + tid];
+          a.db2_part[(int64_t)cur_tile * H + cur_c * kPrepCols + tid] = v;
         }
       }
       if (BIAS && cur_w == 0 && cur_c == nch - 1) {  // the tile's last chunk: ds_bias of its rows
@@ -261,7 +296,7 @@ __global__ void __launch_bounds__(256, 2)
       }
     }
     // ---- phase B: the transposed output through the staging tile ----
-    const bool do_t = cur_w == 1 || dout_t;
+    const bool do_t = cur_w == 1 ? !a.no_t : dout_t;
     if (do_t) {
       const int cp = tid & 63, g = tid >> 6;  // columns 2cp, 2cp+1; tile rows 32g .. 32g+31
       const bool db2 = BIAS && cur_w == 0 && a.db2_part != nullptr;

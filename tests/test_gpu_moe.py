@@ -115,8 +115,10 @@ def test_bf16_intermediates_match_oracle(gather, set_option):
         dout_g = op.region("DOUT_G").view(torch.bfloat16).reshape(P, cfg.H).cpu()[:used]
         assert torch.equal(dout_g[torch.from_numpy(valid)], inp.dout[torch.from_numpy(t)])
         assert torch.all(dout_g[torch.from_numpy(~valid)] == 0)
-    x_gt = op.region("X_GT").view(torch.bfloat16).reshape(cfg.H, P).cpu()[:, :used]
-    assert torch.equal(x_gt.T[torch.from_numpy(valid)], inp.x[torch.from_numpy(t)])
+    # BF16: the dW1 GEMM reads x's gathered rows MN-major (held in the X_GT region), padding rows zero
+    x_rows = op.region("X_GT").view(torch.bfloat16).reshape(P, cfg.H).cpu()[:used]
+    assert torch.equal(x_rows[torch.from_numpy(valid)], inp.x[torch.from_numpy(t)])
+    assert torch.all(x_rows[torch.from_numpy(~valid)] == 0)
     # dh from the oracle's formulas
     from oracle import moe as om
     x, dout, W2, s = map(om._f64, (inp.x, inp.dout, inp.W2, inp.s))

@@ -1,9 +1,10 @@
 """prep's gathered operands at sizes where every persistent prep CTA walks several work items (more
 128-column chunk items, or whole tiles with biases, than two CTAs per SM), so the gathers of one
 item overlap the quantisation of the previous one and the tokens of each next tile come from the
-prefetch: the row-major dout_g copy (G1's A operand), the transposed x_g^T and dout_g^T (G4's and
-G3's token-major operands, dout s-scaled in fp32 for affinity on H) and their scales, bit-exact
-against the oracle's gather and quantisation."""
+prefetch: the row-major dout_g copy (G1's A operand) and the weight-gradient GEMMs' operands — for
+MXFP8 (and BF16 without MN-major operands) the transposed x_g^T and dout_g^T with their scales, for
+BF16 by default x's gathered rows and, for affinity on H, the rows of s*dout — bit-exact against
+the oracle's gather and quantisation (dout s-scaled in fp32 for affinity on H)."""
 import numpy as np
 import pytest
 import torch
@@ -24,10 +25,14 @@ def _bf16_bits(a: torch.Tensor) -> np.ndarray:
     return a.contiguous().view(torch.int16).numpy()
 
 
+@pytest.mark.parametrize("mn", [1, 0])
 @pytest.mark.parametrize("prec", [PREC_MXFP8, PREC_BF16])
 @pytest.mark.parametrize("affinity", [AFFINITY_ON_I, AFFINITY_ON_H])
 @pytest.mark.parametrize("T,H,bias", SHAPES)
-def test_prep_operands_many_items(prec, affinity, T, H, bias):
+def test_prep_operands_many_items(prec, affinity, T, H, bias, mn, set_option):
+    if prec == PREC_MXFP8 and mn == 0:
+        pytest.skip("MXFP8 builds the transposed operands either way")
+    set_option("MN_OPERANDS", mn)
     cfg = small_moe("prep_items", T=T, H=H, I=256, E=8, K=4, B=256, seed=101 + T % 7, precision=prec,
                     affinity=affinity, bias=bias)
     inp = make_moe_inputs(cfg)
@@ -62,6 +67,10 @@ def test_prep_operands_many_items(prec, affinity, T, H, bias):
     else:
         g = op.region("DOUT_G").cpu().view(torch.bfloat16).reshape(P, H)[:used]
         assert np.array_equal(_bf16_bits(g), _bf16_bits(drows))
-        for name, rows in (("X_GT", xrows), ("DOUT_GT", sd.to(torch.bfloat16))):
-            gt = op.region(name).cpu().view(torch.bfloat16).reshape(H, P)[:, :used].T
-            assert np.array_equal(_bf16_bits(gt), _bf16_bits(rows)), name
+        checks = [("X_GT", xrows)]
+        if not mn or affinity == AFFINITY_ON_H:  # MN-major with affinity on I: dW2 reads dout_g itself
+            checks.append(("DOUT_GT", sd.to(torch.bfloat16)))
+        for name, rows in checks:
+            r = op.region(name).cpu().view(torch.bfloat16)
+            got_rows = r.reshape(P, H)[:used] if mn else r.reshape(H, P)[:, :used].T
+            assert np.array_equal(_bf16_bits(got_rows), _bf16_bits(rows)), name
