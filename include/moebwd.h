@@ -299,8 +299,9 @@ enum {
   MOE_WS_DOUT_G,             /* G1 A operand: dout rows [P,H] (bf16 | fp8); empty with MOE_OPT_G1_GATHER = 1 */
   MOE_WS_DOUT_G_SF,          /*   its tiled scales (MXFP8) */
   MOE_WS_DOUT_GT,            /* G3 B operand: [H,P] (bf16 | fp8), s-scaled for affinity on H; BF16 under
-                                MOE_OPT_MN_OPERANDS: the rows [P,H] of s*dout (affinity on H; dout rows
-                                when G1 gathers its own), unused for affinity on I (G3 reads DOUT_G) */
+                                MOE_OPT_MN_OPERANDS: rows [P,H] of dout when G1 gathers its own, of s*dout
+                                when a' comes from a saved intermediate (affinity on H), else unused (G3
+                                reads DOUT_G; for affinity on H, G1 writes a' = s*a) */
   MOE_WS_DOUT_GT_SF,
   MOE_WS_X_GT,               /* G4 A operand: [H,P]; BF16 under MOE_OPT_MN_OPERANDS: x's gathered rows [P,H]
                                 (unused when h is recomputed: G4 reads X_G) */
@@ -310,7 +311,7 @@ enum {
   MOE_WS_DH_T,               /* G4 B operand: dh^T [2I,P] (empty for BF16 under MOE_OPT_MN_OPERANDS, the default) */
   MOE_WS_DH_T_SF,
   MOE_WS_AP_T,               /* G3 A operand: a'^T [I,P] (s*a for affinity on I, a on H); BF16 under
-                                MOE_OPT_MN_OPERANDS: a' rows [P,I] */
+                                MOE_OPT_MN_OPERANDS: a' rows [P,I], s*a for both affinities */
   MOE_WS_AP_T_SF,
   MOE_WS_DX_EXP,             /* G2 output: dx_expanded [P,H] bf16 */
   MOE_WS_X_G,                /* RECOMPUTE: G0 A operand, gathered x rows [P,H] (bf16 | fp8) */

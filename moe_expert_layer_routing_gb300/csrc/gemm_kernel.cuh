@@ -412,11 +412,12 @@ __device__ __forceinline__ void epi_dswiglu_part(const GemmParams& p, uint32_t t
       const float dA = sv * v;
       dg[jj] = dA * dg[jj];
       du[jj] = dA * du[jj];
-      ap[jj] = p.affinity_on_i ? sv * a : a;
+      ap[jj] = (p.affinity_on_i || p.ap_s) ? sv * a : a;
     }
   } else {
     const uint64_t sv2 = f2_splat(sv);
-    const uint64_t sa2 = f2_splat(p.affinity_on_i ? sv : 1.f);  // a' = s a (affinity on I) or a (x 1, exact)
+    // a' = s a (affinity on I, or on H with s moved from dout to a') or a (x 1, exact)
+    const uint64_t sa2 = f2_splat((p.affinity_on_i || p.ap_s) ? sv : 1.f);
     uint64_t DS = f2_splat(0.f);
 #pragma unroll
     for (int jj = 0; jj < NC; jj += 2) {

@@ -509,14 +509,19 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
   // BF16 with MN-major weight-gradient operands: no transposed copies; x rows for the dW1 GEMM (the
   // recomputation's copy when there is one, else in the X_GT region), the dW2 GEMM's B rows (s*dout
   // for affinity on H, or dout when G1 gathers its rows and writes no dout_g) in the DOUT_GT region
+  // For affinity on H the factor s goes to a' (G1 writes s*a) unless a' comes from a saved intermediate;
+  // the dW2 GEMM then reads dout_g itself, and an s*dout copy is made only in that saved case.
+  const void* inter = a.scaled_intermediate_ckpt ? a.scaled_intermediate_ckpt : a.intermediate_ckpt;
+  const bool g3_b_scaled = a.affinity == MOE_AFFINITY_ON_H && inter != nullptr;
   void* x_rows = L.mn ? (rec ? reg<void>(L, ws, R_X_G) : reg<void>(L, ws, R_X_GT)) : nullptr;
   void* g3_b_rows = nullptr;
   if (L.mn && !pa.skip_dout_t)
-    g3_b_rows = (a.affinity == MOE_AFFINITY_ON_H || L.gather) ? reg<void>(L, ws, R_DOUT_GT) : reg<void>(L, ws, R_DOUT_G);
+    g3_b_rows = (g3_b_scaled || L.gather) ? reg<void>(L, ws, R_DOUT_GT) : reg<void>(L, ws, R_DOUT_G);
   if (L.mn) {
     pa.no_t = 1;
     pa.x_g = x_rows;
     pa.dout_b = g3_b_rows == reg<void>(L, ws, R_DOUT_GT) ? g3_b_rows : nullptr;
+    pa.dout_b_s = g3_b_scaled;
   }
   if ((rc = launch_prep(pa, st))) return rc;
   if (L.gather && mx &&  // the rows G1 gathers: dout quantised once per token (the scales come from prep)
@@ -524,7 +529,6 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
                                  1, st)))
     return rc;
   // dW_down operands from saved forward values ([BW] optional checkpoints)
-  const void* inter = a.scaled_intermediate_ckpt ? a.scaled_intermediate_ckpt : a.intermediate_ckpt;
   if (inter && (rc = launch_apt_from_ckpt(static_cast<const uint16_t*>(inter), a.I, a.block_size, P, scalars + 1,
                                          tile_expert, tile_offsets, block_offsets, tile_row_flat,
                                          (!a.scaled_intermediate_ckpt && a.affinity == MOE_AFFINITY_ON_I) ? a.s
@@ -616,6 +620,7 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.dht = reg<void>(L, ws, R_DH_T); p.dht_sf = reg<uint8_t>(L, ws, R_DH_T_SF);
     p.apt = inter ? nullptr : reg<void>(L, ws, R_AP_T);
     p.ap_rows = L.mn;  // BF16: a' rows [P,I] for the dW2 GEMM's MN-major read
+    p.ap_s = L.mn && a.affinity == MOE_AFFINITY_ON_H;  // ... scaled by s (then dW2 reads dout itself)
     p.apt_sf = inter ? nullptr : reg<uint8_t>(L, ws, R_AP_T_SF);
     p.ds_part = reg<float>(L, ws, R_DS_PART);
     p.db1_part = a.has_bias ? reg<float>(L, ws, R_DB1_PART) : nullptr;

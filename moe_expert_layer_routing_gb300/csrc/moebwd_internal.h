@@ -130,10 +130,11 @@ struct PrepArgs {
   float* db2_part;                     // with biases: [P/128][4][H] column sums of s*dout per tile
                                        // (four 32-row quarters of its rows; [P/128][H] with no_t), or null
   // BF16 with MN-major weight-gradient operands: no transposed outputs (no_t); dout_b, when not null,
-  // gets the rows of the dW2 GEMM's B operand ([P,H]: s*dout for affinity on H, else dout), and db2's
+  // gets the rows of the dW2 GEMM's B operand ([P,H]: s*dout with dout_b_s, else dout), and db2's
   // partials are per-tile column sums ([P/128][H]) taken in the row-wise phase
   int no_t;
   void* dout_b;
+  int dout_b_s;                        // dout_b rows are s*dout (else dout)
   uint32_t k_mul; int k_shift;         // set by launch_prep: f / K = umulhi(f, k_mul) >> (k_shift - 1)
                                        // for 0 <= f < 2^31 (k_shift = 0: K = 1)
 };
@@ -231,6 +232,7 @@ struct GemmParams {
   // read through 64 x 64 tensor-map boxes and the tensor core's MN-major descriptors
   int a_mn, b_mn;
   int ap_rows;                  // BF16 dSwiGLU GEMM: a' written as rows [P,I] at apt (for an MN-major read)
+  int ap_s;                     // a' = s a also for affinity on H (the dW2 GEMM then reads unscaled dout)
 };
 
 // A [rows, K] and B [rows, K] K-major operands (bf16 or fp8 bytes), tile counts in p.

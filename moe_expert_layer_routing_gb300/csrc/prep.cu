@@ -254,9 +254,9 @@ __global__ void __launch_bounds__(256, 2)
           if (rowdst) *reinterpret_cast<uint4*>(static_cast<uint16_t*>(rowdst) + prow * H + col) = v;
           if (cur_w == 0 && (a.dout_b || db2_rows)) {
             const float sr = s_s[buf * 128 + rl + 16 * k];
-            if (a.dout_b) {  // the dW2 GEMM's B rows: s*dout in fp32, rounded (affinity on H), else dout
+            if (a.dout_b) {  // the dW2 GEMM's B rows: s*dout in fp32, rounded (dout_b_s), else dout
               uint4 o = v;
-              if (SCALE_T)
+              if (SCALE_T && a.dout_b_s)
                 o = make_uint4(pack_bf16x2(d8[0] * sr, d8[1] * sr), pack_bf16x2(d8[2] * sr, d8[3] * sr),
                                pack_bf16x2(d8[4] * sr, d8[5] * sr), pack_bf16x2(d8[6] * sr, d8[7] * sr));
               *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dout_b) + prow * H + col) = o;

@@ -3,8 +3,8 @@
 item overlap the quantisation of the previous one and the tokens of each next tile come from the
 prefetch: the row-major dout_g copy (G1's A operand) and the weight-gradient GEMMs' operands — for
 MXFP8 (and BF16 without MN-major operands) the transposed x_g^T and dout_g^T with their scales, for
-BF16 by default x's gathered rows and, for affinity on H, the rows of s*dout — bit-exact against
-the oracle's gather and quantisation (dout s-scaled in fp32 for affinity on H)."""
+BF16 by default x's gathered rows (the dW2 GEMM then reads dout_g itself) — bit-exact against the
+oracle's gather and quantisation (dout s-scaled in fp32 for affinity on H)."""
 import numpy as np
 import pytest
 import torch
@@ -68,7 +68,7 @@ def test_prep_operands_many_items(prec, affinity, T, H, bias, mn, set_option):
         g = op.region("DOUT_G").cpu().view(torch.bfloat16).reshape(P, H)[:used]
         assert np.array_equal(_bf16_bits(g), _bf16_bits(drows))
         checks = [("X_GT", xrows)]
-        if not mn or affinity == AFFINITY_ON_H:  # MN-major with affinity on I: dW2 reads dout_g itself
+        if not mn:  # MN-major: the dW2 GEMM reads dout_g itself (s moves to a' for affinity on H)
             checks.append(("DOUT_GT", sd.to(torch.bfloat16)))
         for name, rows in checks:
             r = op.region(name).cpu().view(torch.bfloat16)
