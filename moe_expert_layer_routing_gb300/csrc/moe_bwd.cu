@@ -620,7 +620,8 @@ extern "C" int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream) {
     p.dht = reg<void>(L, ws, R_DH_T); p.dht_sf = reg<uint8_t>(L, ws, R_DH_T_SF);
     p.apt = inter ? nullptr : reg<void>(L, ws, R_AP_T);
     p.ap_rows = L.mn;  // BF16: a' rows [P,I] for the dW2 GEMM's MN-major read
-    p.ap_s = L.mn && a.affinity == MOE_AFFINITY_ON_H;  // ... scaled by s (then dW2 reads dout itself)
+    // ... scaled by s for affinity on H when the dW2 GEMM reads unscaled dout rows (not with a saved s*dout)
+    p.ap_s = L.mn && a.affinity == MOE_AFFINITY_ON_H && !pa.skip_dout_t;
     p.apt_sf = inter ? nullptr : reg<uint8_t>(L, ws, R_AP_T_SF);
     p.ds_part = reg<float>(L, ws, R_DS_PART);
     p.db1_part = a.has_bias ? reg<float>(L, ws, R_DB1_PART) : nullptr;
