@@ -131,6 +131,30 @@ def test_options_defaults_and_validation(lib):
     assert n192 > 0 and n128 > 0 and n192 != n128   # the tile width moves the ds partials' region
 
 
+def test_mn_operands_option_moves_the_bf16_layout(lib):
+    """MOE_OPT_MN_OPERANDS (default 1): BF16's dW1 GEMM reads dh itself, so the DH_T region is empty;
+    with 0 it holds dh^T [2I,P] bf16.  MXFP8 keeps dh^T either way.  Host-only (workspace sizes)."""
+    import moe_expert_layer_routing_gb300 as mb
+    assert mb.get_option("MN_OPERANDS") == 1
+    assert lib.moe_set_option(mb.OPTIONS.index("MN_OPERANDS"), 2) == -1
+
+    def dh_t_bytes(precision):
+        a = mb.MoeBwdArgs(T=256, H=256, I=384, E=4, K=2, block_size=128, precision=precision)
+        off, nb = ctypes.c_size_t(), ctypes.c_size_t()
+        assert lib.moe_bwd_workspace_region(ctypes.byref(a), mb.WS_REGIONS.index("DH_T"), ctypes.byref(off),
+                                            ctypes.byref(nb)) == 0
+        return nb.value, lib.moe_bwd_workspace_size(ctypes.byref(a))
+
+    P = mb.tile_rows_capacity(256, 2, 4)
+    nb_mn, total_mn = dh_t_bytes(0)
+    assert nb_mn == 0 and dh_t_bytes(1)[0] == 2 * 384 * P
+    with mb.option("MN_OPERANDS", 0):
+        nb, total = dh_t_bytes(0)
+        assert nb == 2 * 384 * P * 2 and total >= total_mn + nb   # bf16 dh^T back in the workspace
+        assert dh_t_bytes(1)[0] == 2 * 384 * P
+    assert mb.get_option("MN_OPERANDS") == 1
+
+
 def test_mxfp8_bias_with_saved_scaled_dout_is_refused(lib):
     import moe_expert_layer_routing_gb300 as mb
     a = mb.MoeBwdArgs(T=256, H=128, I=256, E=4, K=2, block_size=128, precision=1, has_bias=1, affinity=0)
