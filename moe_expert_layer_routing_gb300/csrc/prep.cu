@@ -10,6 +10,8 @@
 // as BF16, or as MXFP8 with E8M0 scales in the tiled layout (transposed operands are quantised
 // in groups of 32 tile rows, i.e. along the GEMM contraction).  Padding rows are zero.  When the
 // gate/up pre-activations are recomputed, a row-major gathered x [P,H] (G0's A operand) is written too.
+// BF16 whose weight-gradient GEMMs read MN-major operands (no_t): no transposed outputs; x's gathered
+// rows go to x_g and, where the dW2 GEMM cannot read dout_g itself, dout (or s*dout) rows to dout_b.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -33,11 +35,14 @@ constexpr int kPrepPitch = 66;       // bf16 row pitch of the 64-column tiles of
 //   phase A (dout; x too when h is recomputed): each thread quantises the 16-byte pieces of eight
 //     rows row-wise (MXFP8 groups of 32 columns = 4 lanes) into the row-major copy and its scales,
 //     and accumulates the rows' dot products with b2;
-//   phase B: thread (column pair, 32-row quarter) reads 32 words, quantises (MXFP8) or rounds (BF16)
-//     the two transposed 32-element groups into a staging tile in the 128-byte swizzled layout of
-//     the output's tensor map (16-byte piece c of staging row r at r * 128 + ((c ^ (r % 8)) * 16)),
-//     written by one elected thread's tiled bulk stores; MXFP8 scale bytes go to one staged 512-byte
-//     atom of the tiled layout, written by a plain bulk copy.
+//     (no_t: also the dout_b rows and db2's per-tile column sums: lane pairs, then eight warps through
+//     shared memory);
+//   phase B (not with no_t): thread (column pair, 32-row quarter) reads 32 words, quantises (MXFP8) or
+//     rounds (BF16) the two transposed 32-element groups — MXFP8 into a staging tile in the 128-byte
+//     swizzled layout of the output's tensor map (16-byte piece c of staging row r at
+//     r * 128 + ((c ^ (r % 8)) * 16)), written by one elected thread's tiled bulk stores, its scale
+//     bytes into one staged 512-byte atom of the tiled layout written by a plain bulk copy; BF16 as
+//     whole 32-byte sectors straight to global memory — and adds db2's quarter sums.
 // Rows and tokens: tile row p holds flat index f = tile_row_flat[p] (token f / K, or padding when
 // f < 0); the divide is a multiply by a constant from the host.
 constexpr int kPrepCols = 128;                       // H columns per unit
