@@ -72,3 +72,23 @@ def test_pair_and_single_cta_give_the_same_gradients_to_rounding(bn, set_option)
     for n in ("dx", "dW1", "dW2", "ds"):
         a, b = outs[0][n], outs[1][n]
         assert np.linalg.norm(a - b) <= 4e-3 * np.linalg.norm(b), n
+
+
+@pytest.mark.parametrize("mn", [1, 0])
+@pytest.mark.parametrize("pair", [2, 0])
+def test_bf16_128_column_weight_gradient_tiles(pair, mn, set_option):
+    """BF16 weight-gradient GEMMs at 128 columns — pair tiles of 128 (one 64-column box of an MN-major
+    B per CTA) or single-CTA tiles of 128 (two boxes) — with MN-major and with transposed operands."""
+    set_option("PAIR_GEMMS", pair)
+    set_option("MN_OPERANDS", mn)
+    if pair:
+        set_option("PAIR_TILE_N", 128)
+    else:
+        set_option("G3_TILE_N", 128)
+        set_option("G4_TILE_N", 128)
+    cfg = small_moe("wgrad128", T=700, H=512, I=256, E=6, K=2, B=256, seed=54, precision=PREC_BF16,
+                    affinity=AFFINITY_ON_H)
+    inp = with_ids(make_moe_inputs(cfg), _ids(700, 2, 6, seed=10))
+    op, got = run_gpu(inp)
+    assert int(got["status"].item()) == 0
+    compare_outputs(got, oracle_bwd(inp), BF16_TOL)
