@@ -424,6 +424,7 @@ enum {
                                 dout (s*dout for affinity on H) rows, so prep builds no transposed copies
                                 and the dA GEMM no dh^T or a'^T (the DH_T region is empty; X_GT, DOUT_GT
                                 and AP_T hold rows; operands made from saved checkpoints stay transposed);
+                                linear_bwd's BF16 GEMMs read dY, W and X themselves (no workspace copies);
                                 0: transposed copies as for MXFP8 */
   MOE_NUM_OPTIONS
 };

@@ -799,10 +799,12 @@ LinLayout lin_layout(int64_t M, int64_t N, int64_t K, int precision) {
   LinLayout L{};
   const bool mx = precision == MOE_PREC_MXFP8;
   const int64_t es = mx ? 1 : 2;
+  // BF16 with MN-major operands (MOE_OPT_MN_OPERANDS): both GEMMs read dY, W and X themselves, no copies
+  const int64_t tc = (mx || option(MOE_OPT_MN_OPERANDS) == 0) ? 1 : 0;
   // 0 dY (rowwise, mx only) 1 its sf | 2 W^T [K,N] 3 sf | 4 dY^T [N,M] 5 sf | 6 X^T [K,M] 7 sf | 8 counters
-  size_t b[9] = {mx ? (size_t)(M * N) : 0, mx ? (size_t)(M * N / 32) : 0, (size_t)(K * N * es), mx ? (size_t)(K * N / 32) : 0,
-                 (size_t)(N * M * es), mx ? (size_t)(N * M / 32) : 0, (size_t)(K * M * es), mx ? (size_t)(K * M / 32) : 0,
-                 64 /* tile counters */};
+  size_t b[9] = {mx ? (size_t)(M * N) : 0, mx ? (size_t)(M * N / 32) : 0, (size_t)(K * N * es * tc),
+                 mx ? (size_t)(K * N / 32) : 0, (size_t)(N * M * es * tc), mx ? (size_t)(N * M / 32) : 0,
+                 (size_t)(K * M * es * tc), mx ? (size_t)(K * M / 32) : 0, 64 /* tile counters */};
   size_t off = 0;
   for (int i = 0; i < 9; ++i) {
     L.off[i] = off;
@@ -843,18 +845,22 @@ extern "C" int linear_bwd(const void* dY, const void* W, const void* X, int64_t 
   int32_t* counters = static_cast<int32_t*>(R(8));
   int rc = cuda_check(cudaMemsetAsync(counters, 0, L.bytes[8], st), "memset tile counters");
   if (rc) return rc;
-  // operands: dX = dY @ W contracts over N, dW = dY^T @ X contracts over M
+  // operands: dX = dY @ W contracts over N, dW = dY^T @ X contracts over M; BF16 with MN-major operands
+  // reads W (dX's B), dY (dW's A) and X (dW's B) row-major, so only MXFP8 (or transposed BF16) copies
+  const bool mn = !mx && L.bytes[2] == 0;
   if (mx && (rc = launch_quant_rowwise(dYb, M, M, N, N, nullptr, fp8_fmt, static_cast<uint8_t*>(R(0)),
                                        static_cast<uint8_t*>(R(1)), 1, st)))
     return rc;
-  if ((rc = launch_quant_colwise(static_cast<const uint16_t*>(W), N, N, K, K, nullptr, mx, fp8_fmt, R(2),
-                                 static_cast<uint8_t*>(R(3)), 1, st)))
-    return rc;
-  if ((rc = launch_quant_colwise(dYb, M, M, N, N, nullptr, mx, fp8_fmt, R(4), static_cast<uint8_t*>(R(5)), 1, st)))
-    return rc;
-  if ((rc = launch_quant_colwise(static_cast<const uint16_t*>(X), M, M, K, K, nullptr, mx, fp8_fmt, R(6),
-                                 static_cast<uint8_t*>(R(7)), 1, st)))
-    return rc;
+  if (!mn) {
+    if ((rc = launch_quant_colwise(static_cast<const uint16_t*>(W), N, N, K, K, nullptr, mx, fp8_fmt, R(2),
+                                   static_cast<uint8_t*>(R(3)), 1, st)))
+      return rc;
+    if ((rc = launch_quant_colwise(dYb, M, M, N, N, nullptr, mx, fp8_fmt, R(4), static_cast<uint8_t*>(R(5)), 1, st)))
+      return rc;
+    if ((rc = launch_quant_colwise(static_cast<const uint16_t*>(X), M, M, K, K, nullptr, mx, fp8_fmt, R(6),
+                                   static_cast<uint8_t*>(R(7)), 1, st)))
+      return rc;
+  }
   const int BN = K % 256 == 0 ? 256 : 128;
   {
     GemmParams p{};
@@ -870,7 +876,10 @@ extern "C" int linear_bwd(const void* dY, const void* W, const void* X, int64_t 
     p.epi = kEpiStore;
     p.out = dX; p.ldo = K;
     p.tile_counter = counters + 0;
-    if ((rc = launch_gemm(mx, BN, p, mx ? R(0) : dY, M, N, R(2), K, N, st))) return rc;
+    p.b_mn = mn;  // W itself: [N, K] = [contraction, output columns]
+    if ((rc = mn ? launch_gemm(mx, BN, p, dY, M, N, W, N, K, st)
+                 : launch_gemm(mx, BN, p, mx ? R(0) : dY, M, N, R(2), K, N, st)))
+      return rc;
   }
   {
     GemmParams p{};
@@ -886,7 +895,9 @@ extern "C" int linear_bwd(const void* dY, const void* W, const void* X, int64_t 
     p.epi = kEpiStore;
     p.out = dW; p.ldo = K;
     p.tile_counter = counters + 1;
-    if ((rc = launch_gemm(mx, BN, p, R(4), N, M, R(6), K, M, st))) return rc;
+    p.a_mn = p.b_mn = mn;  // dY [M, N] and X [M, K]: both [contraction, output] row-major
+    if ((rc = mn ? launch_gemm(mx, BN, p, dY, M, N, X, M, K, st) : launch_gemm(mx, BN, p, R(4), N, M, R(6), K, M, st)))
+      return rc;
   }
   return MOE_OK;
 }

@@ -218,6 +218,20 @@ def test_linear_bwd_small_both_precisions():
         assert rel_fro(np64(got["dW"]), ref["dW"]) < tol
 
 
+@pytest.mark.parametrize("mn", [1, 0])
+def test_linear_bwd_bf16_operand_layouts(mn, set_option):
+    """BF16 linear backward reading dY, W and X themselves as MN-major operands (no copies), or through
+    transposed copies; odd tile counts and 128-column tiles."""
+    import moe_expert_layer_routing_gb300 as mb
+    set_option("MN_OPERANDS", mn)
+    inp = make_linear_inputs(LinearConfig("lin_mn", M=384, N=256, K=640, seed=43))
+    got = mb.linear_bwd(inp.dY.cuda(), inp.W.cuda(), inp.X.cuda(), precision=mb.PREC_BF16)
+    torch.cuda.synchronize()
+    ref = olin.linear_backward(inp.dY, inp.W, inp.X)
+    assert rel_fro(np64(got["dX"]), ref["dX"]) < BF16_TOL
+    assert rel_fro(np64(got["dW"]), ref["dW"]) < BF16_TOL
+
+
 def test_linear_bwd_outputs_16_byte_aligned():
     """Outputs in caller buffers that are 16- but not 32-byte aligned (the public contract), through
     the direct-store epilogue (K = 384: 128-column tiles): identical to aligned outputs."""
