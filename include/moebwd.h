@@ -441,7 +441,9 @@ int64_t moe_get_option(int option);
  * and dW = dY^T @ X [N,K] in bf16.  precision MOE_PREC_MXFP8 quantises every operand in 32-groups
  * along its GEMM's contraction dimension (dY and W along N for dX; dY and X along M for dW) with
  * `fp8_fmt` (the page's default is e5m2); MOE_PREC_BF16 multiplies the BF16 values directly.
- * dY, W, X, dX, dW (device) bf16; M, N, K multiples of 128. */
+ * dY, W, X, dX, dW (device) bf16; M, N, K multiples of 128.  The workspace holds the quantised or
+ * transposed operand copies (none for BF16 under MOE_OPT_MN_OPERANDS, the default: its size is taken
+ * with the option as it stands, which must not change between the size query and the call). */
 size_t linear_bwd_workspace_size(int64_t M, int64_t N, int64_t K, int precision);
 int linear_bwd(const void* dY, const void* W, const void* X, int64_t M, int64_t N, int64_t K, int precision,
                int fp8_fmt, void* dX, void* dW, void* workspace, size_t workspace_bytes, moe_stream_t stream);
