@@ -381,21 +381,42 @@ def time_problem(mb, P, steps, warmup, world, local, stream):
         st0 = int(P["op"].status.item())
         if st0 != 0:
             raise SystemExit(f"device status {st0} after warm-up")
+    # resident inputs larger than L2: back-to-back steps; otherwise L2 is flushed before every step (a
+    # buffer of twice its size written on the stream) and each step is timed by its own pair of events
+    l2_bytes = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    flush = None
+    if P["in_bytes"] <= l2_bytes:
+        flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=torch.cuda.current_device())
+        l2_note = (f"L2 flushed before each timed step ({P['in_bytes'] / 1e9:.2f} GB resident inputs <= "
+                   f"{l2_bytes / 1e9:.2f} GB L2: a {2 * l2_bytes / 1e9:.2f} GB buffer written between steps, "
+                   f"each step timed by its own events)")
+    else:
+        l2_note = f"inputs larger than L2 ({P['in_bytes'] / 1e9:.2f} GB resident inputs > {l2_bytes / 1e9:.2f} GB L2)"
     launches0 = mb.kernel_launches()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        ev0.record(stream)
-        for _ in range(steps):
-            step()
-        ev1.record(stream)
+        if flush is None:
+            ev0.record(stream)
+            for _ in range(steps):
+                step()
+            ev1.record(stream)
+        else:
+            for i in range(steps):
+                flush.fill_(i & 255)
+                evs[i][0].record(stream)
+                step()
+                evs[i][1].record(stream)
         torch.cuda.synchronize()
     barrier(world)
-    ms = allreduce_max(ev0.elapsed_time(ev1) / steps, world)
+    local_ms = (ev0.elapsed_time(ev1) if flush is None else sum(a.elapsed_time(b) for a, b in evs)) / steps
+    ms = allreduce_max(local_ms, world)
     launches = mb.kernel_launches() - launches0
-    out = dict(ms=ms, launches=launches, clocks=clk.summary(), stages=None, profiled_ms=None)
+    del flush
+    out = dict(ms=ms, launches=launches, clocks=clk.summary(), stages=None, profiled_ms=None, l2=l2_note)
     if not P["is_linear"]:
         mb.profile_enable(True)
         ev0.record(stream)
@@ -461,7 +482,8 @@ def extra_workloads(mb, args, world, local, stream, peaks, peak_src, dev):
                          tokens_per_s=P["tokens"] * world / (T["ms"] * 1e-3), gpu_launches=T["launches"],
                          roofline=dict(kernel=rl["kernel"], achieved=rl["achieved"], frac=rl["frac"],
                                        peak=rl["peak"], per_stage_frac=rl.get("per_stage_frac")),
-                         stage_ms=T["stages"], clocks=T["clocks"], config=workload_config(cfg, P["is_linear"], world))
+                         stage_ms=T["stages"], clocks=T["clocks"],
+                         config=dict(workload_config(cfg, P["is_linear"], world), l2=T["l2"]))
         del P
         torch.cuda.empty_cache()
     return out
@@ -525,8 +547,7 @@ def main():
     peaks, peak_src = load_peaks()
 
     P = setup_problem(mb, cfg, dev)
-    op, inp, kw, flops, tokens, prec, in_bytes = (P[k] for k in ("op", "inp", "kw", "flops", "tokens", "prec",
-                                                                   "in_bytes"))
+    op, inp, kw, flops, tokens, prec = (P[k] for k in ("op", "inp", "kw", "flops", "tokens", "prec"))
     T = time_problem(mb, P, args.steps, args.warmup, world, local, stream)
     ms, launches, clocks, stages = T["ms"], T["launches"], T["clocks"], T["stages"]
     value = flops * world / (ms * 1e-3) / 1e12
@@ -650,7 +671,7 @@ def main():
         cpu_baseline = dict(value=cval, unit="TFLOP/s", cores=cores, kind="oracle", sample=desc + f"; {n} run(s)")
 
     conf = workload_config(cfg, is_linear, world)
-    conf["l2"] = f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB resident inputs > 0.13 GB L2)"
+    conf["l2"] = T["l2"]
     line = dict(
         metric=METRIC_LINEAR if is_linear else METRIC_MOE,
         value=value, unit="TFLOP/s", n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=ms,

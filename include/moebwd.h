@@ -426,6 +426,12 @@ enum {
                                 and AP_T hold rows; operands made from saved checkpoints stay transposed);
                                 linear_bwd's BF16 GEMMs read dY, W and X themselves (no workspace copies);
                                 0: transposed copies as for MXFP8 */
+  MOE_OPT_LINEAR_CONCURRENT, /* linear_bwd: 1 (default) the dW GEMM runs on a second stream owned by the
+                                library, concurrently with the dX GEMM on the caller's stream (ordered
+                                after the quantised operands, joined back before the call returns, so
+                                the caller's stream sees both results as before); the persistent CTAs of
+                                one GEMM fill the SMs the other's last wave leaves idle.  0: both on the
+                                caller's stream, one after the other */
   MOE_NUM_OPTIONS
 };
 /* Set an option; value -1 restores its default.  MOE_ERR_INVALID for an unknown option or value. */
@@ -443,7 +449,11 @@ int64_t moe_get_option(int option);
  * `fp8_fmt` (the page's default is e5m2); MOE_PREC_BF16 multiplies the BF16 values directly.
  * dY, W, X, dX, dW (device) bf16; M, N, K multiples of 128.  The workspace holds the quantised or
  * transposed operand copies (none for BF16 under MOE_OPT_MN_OPERANDS, the default: its size is taken
- * with the option as it stands, which must not change between the size query and the call). */
+ * with the option as it stands, which must not change between the size query and the call).
+ * Stream: everything is ordered on `stream` as seen by the caller.  Under MOE_OPT_LINEAR_CONCURRENT
+ * (the default) the dW GEMM runs on a stream the library creates on first use (one per device, with
+ * two events), forked from `stream` and joined back to it inside the call; the call may be captured
+ * into a CUDA graph once that stream exists (any earlier call on the device creates it). */
 size_t linear_bwd_workspace_size(int64_t M, int64_t N, int64_t K, int precision);
 int linear_bwd(const void* dY, const void* W, const void* X, int64_t M, int64_t N, int64_t K, int precision,
                int fp8_fmt, void* dX, void* dW, void* workspace, size_t workspace_bytes, moe_stream_t stream);

@@ -36,7 +36,7 @@ EXPORTED = ["moe_last_error", "moe_version", "moe_num_blocks_bound", "moe_route_
 
 # library options (moe_set_option)
 OPTIONS = ["WAIT_LIMIT_NS", "PAIR_GEMMS", "PAIR_TILE_N", "G1_TILE_N", "G2_TILE_N", "G3_TILE_N", "G4_TILE_N",
-           "PREP_TILE_ORDER", "G1_GATHER", "G1_WARPS", "PDL", "MN_OPERANDS"]
+           "PREP_TILE_ORDER", "G1_GATHER", "G1_WARPS", "PDL", "MN_OPERANDS", "LINEAR_CONCURRENT"]
 
 STAGES = ["route", "prep", "G1_dA_dswiglu", "G3_dW2", "G2_dx_expanded", "G4_dW1", "reduce", "G0_recompute_h"]
 

@@ -11,7 +11,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(CSRC, "_build")
 LIB = os.path.join(PKG, "libmoebwd.so")
 SOURCES = ["host.cu", "route_meta.cu", "prep.cu", "reduce.cu", "moe_bwd.cu", "gemm_bf16.cu", "gemm_mx.cu", "gemm_pair.cu",
-           "noalloc.cu", "router.cu"]
+           "noalloc.cu", "router.cu", "linear.cu"]
 HEADERS = ["ptx.cuh", "mx_device.cuh", "gemm_kernel.cuh", "gemm_pair_kernel.cuh", "moebwd_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]

@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstring>
 #include <atomic>
+#include <functional>
 #include <mutex>
 
 #include "moebwd_internal.h"
@@ -53,6 +54,7 @@ static const int64_t kOptDefault[MOE_NUM_OPTIONS] = {
     0,                      // MOE_OPT_G1_WARPS (automatic)
     1,                      // MOE_OPT_PDL
     1,                      // MOE_OPT_MN_OPERANDS
+    1,                      // MOE_OPT_LINEAR_CONCURRENT
 };
 static std::once_flag g_opt_once;
 static void opt_init() {
@@ -78,10 +80,52 @@ static bool option_value_ok(int o, int64_t v) {
     case MOE_OPT_PREP_TILE_ORDER:
     case MOE_OPT_G1_GATHER:
     case MOE_OPT_PDL:
-    case MOE_OPT_MN_OPERANDS: return v == 0 || v == 1;
+    case MOE_OPT_MN_OPERANDS:
+    case MOE_OPT_LINEAR_CONCURRENT: return v == 0 || v == 1;
     case MOE_OPT_G1_WARPS: return v == 0 || v == 8 || v == 16;
     default: return false;
   }
+}
+
+// A second stream and a fork / join event pair per device, created on first use.  Enqueueing on it
+// holds g_aux_mu from the fork to the join, so concurrent callers never re-record an event between
+// another caller's record and the wait on it.
+namespace {
+constexpr int kMaxDevices = 64;
+struct AuxStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+AuxStream g_aux[kMaxDevices];
+std::mutex g_aux_mu;
+}  // namespace
+
+int fork_join(cudaStream_t st, const std::function<int(cudaStream_t)>& side, const std::function<int()>& main) {
+  int dev = 0;
+  int rc = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_UNSUPPORTED, "device index %d above the library's limit", dev);
+  std::lock_guard<std::mutex> lock(g_aux_mu);
+  AuxStream& a = g_aux[dev];
+  if (!a.s) {
+    if ((rc = cuda_check(cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking), "second stream"))) return rc;
+    if ((rc = cuda_check(cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming), "fork event")) ||
+        (rc = cuda_check(cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming), "join event"))) {
+      if (a.fork) cudaEventDestroy(a.fork);
+      cudaStreamDestroy(a.s);
+      a = AuxStream{};
+      return rc;
+    }
+  }
+  if ((rc = cuda_check(cudaEventRecord(a.fork, st), "fork record")) ||
+      (rc = cuda_check(cudaStreamWaitEvent(a.s, a.fork, 0), "fork wait")))
+    return rc;
+  const int rc_side = side(a.s);
+  // the join is enqueued whatever the side work returned, so the caller's stream never runs ahead of it
+  if ((rc = cuda_check(cudaEventRecord(a.join, a.s), "join record"))) return rc;
+  const int rc_main = rc_side ? MOE_OK : main();
+  if ((rc = cuda_check(cudaStreamWaitEvent(st, a.join, 0), "join wait"))) return rc;
+  return rc_side ? rc_side : rc_main;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

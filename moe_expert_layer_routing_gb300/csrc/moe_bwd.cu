@@ -848,21 +848,22 @@ extern "C" int linear_bwd(const void* dY, const void* W, const void* X, int64_t 
   // operands: dX = dY @ W contracts over N, dW = dY^T @ X contracts over M; BF16 with MN-major operands
   // reads W (dX's B), dY (dW's A) and X (dW's B) row-major, so only MXFP8 (or transposed BF16) copies
   const bool mn = !mx && L.bytes[2] == 0;
-  if (mx && (rc = launch_quant_rowwise(dYb, M, M, N, N, nullptr, fp8_fmt, static_cast<uint8_t*>(R(0)),
-                                       static_cast<uint8_t*>(R(1)), 1, st)))
-    return rc;
-  if (!mn) {
-    if ((rc = launch_quant_colwise(static_cast<const uint16_t*>(W), N, N, K, K, nullptr, mx, fp8_fmt, R(2),
-                                   static_cast<uint8_t*>(R(3)), 1, st)))
+  if (mx) {  // dY row-wise and the three transposed operands, one launch
+    if ((rc = launch_linear_quant(dYb, static_cast<const uint16_t*>(W), static_cast<const uint16_t*>(X), M, N, K, fp8_fmt,
+                                  static_cast<uint8_t*>(R(0)), static_cast<uint8_t*>(R(1)), static_cast<uint8_t*>(R(2)),
+                                  static_cast<uint8_t*>(R(3)), static_cast<uint8_t*>(R(4)), static_cast<uint8_t*>(R(5)),
+                                  static_cast<uint8_t*>(R(6)), static_cast<uint8_t*>(R(7)), st)))
       return rc;
-    if ((rc = launch_quant_colwise(dYb, M, M, N, N, nullptr, mx, fp8_fmt, R(4), static_cast<uint8_t*>(R(5)), 1, st)))
-      return rc;
-    if ((rc = launch_quant_colwise(static_cast<const uint16_t*>(X), M, M, K, K, nullptr, mx, fp8_fmt, R(6),
-                                   static_cast<uint8_t*>(R(7)), 1, st)))
+  } else if (!mn) {  // BF16 with transposed copies
+    if ((rc = launch_quant_colwise(static_cast<const uint16_t*>(W), N, N, K, K, nullptr, 0, fp8_fmt, R(2), nullptr, 1,
+                                   st)) ||
+        (rc = launch_quant_colwise(dYb, M, M, N, N, nullptr, 0, fp8_fmt, R(4), nullptr, 1, st)) ||
+        (rc = launch_quant_colwise(static_cast<const uint16_t*>(X), M, M, K, K, nullptr, 0, fp8_fmt, R(6), nullptr, 1,
+                                   st)))
       return rc;
   }
   const int BN = K % 256 == 0 ? 256 : 128;
-  {
+  auto gemm_dx = [&](cudaStream_t s) {
     GemmParams p{};
     p.mode = kMGrouped;
     p.M = (int)M; p.N = (int)K; p.K = (int)N;
@@ -877,11 +878,9 @@ extern "C" int linear_bwd(const void* dY, const void* W, const void* X, int64_t 
     p.out = dX; p.ldo = K;
     p.tile_counter = counters + 0;
     p.b_mn = mn;  // W itself: [N, K] = [contraction, output columns]
-    if ((rc = mn ? launch_gemm(mx, BN, p, dY, M, N, W, N, K, st)
-                 : launch_gemm(mx, BN, p, mx ? R(0) : dY, M, N, R(2), K, N, st)))
-      return rc;
-  }
-  {
+    return mn ? launch_gemm(mx, BN, p, dY, M, N, W, N, K, s) : launch_gemm(mx, BN, p, mx ? R(0) : dY, M, N, R(2), K, N, s);
+  };
+  auto gemm_dw = [&](cudaStream_t s) {
     GemmParams p{};
     p.mode = kMGrouped;
     p.M = (int)N; p.N = (int)K; p.K = (int)M;
@@ -896,8 +895,10 @@ extern "C" int linear_bwd(const void* dY, const void* W, const void* X, int64_t 
     p.out = dW; p.ldo = K;
     p.tile_counter = counters + 1;
     p.a_mn = p.b_mn = mn;  // dY [M, N] and X [M, K]: both [contraction, output] row-major
-    if ((rc = mn ? launch_gemm(mx, BN, p, dY, M, N, X, M, K, st) : launch_gemm(mx, BN, p, R(4), N, M, R(6), K, M, st)))
-      return rc;
-  }
-  return MOE_OK;
+    return mn ? launch_gemm(mx, BN, p, dY, M, N, X, M, K, s) : launch_gemm(mx, BN, p, R(4), N, M, R(6), K, M, s);
+  };
+  // the two GEMMs are independent: dW on the library's second stream beside dX (MOE_OPT_LINEAR_CONCURRENT)
+  if (option(MOE_OPT_LINEAR_CONCURRENT)) return fork_join(st, gemm_dw, [&] { return gemm_dx(st); });
+  if ((rc = gemm_dx(st))) return rc;
+  return gemm_dw(st);
 }

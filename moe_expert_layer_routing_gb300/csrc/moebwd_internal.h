@@ -2,6 +2,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <functional>
 #include <cuda_runtime.h>
 
 #include "../../include/moebwd.h"
@@ -26,6 +27,10 @@ int device_sm_count();
 size_t align_up(size_t v, size_t a);
 void count_launch();   // one kernel launched by this library
 int64_t option(int opt);  // current value of a MOE_OPT_* option
+// Runs `side` on a library-owned second stream of the current device, ordered after the work already
+// enqueued on `st`, and `main` on `st` meanwhile; `st` then waits for the side work.  Returns the first
+// nonzero code (main is skipped when side failed).
+int fork_join(cudaStream_t st, const std::function<int(cudaStream_t)>& side, const std::function<int()>& main);
 
 // Programmatic dependent launch, device side: wait until the grids this one depends on have completed
 // and their memory is visible (a no-op without such a dependency); allow the dependent grid to be
@@ -159,6 +164,12 @@ int launch_quant_rowwise(const uint16_t* in, int64_t src_rows, int64_t rows, int
 int launch_quant_colwise(const uint16_t* in, int64_t src_rows, int64_t rows, int64_t cols, int64_t ld,
                          const int32_t* row_index, int mx, int fmt, void* q, uint8_t* sf, int tiled,
                          cudaStream_t st);
+
+// MXFP8 operands of the dense linear backward in one launch (linear.cu): dY row-wise [M,N], and the
+// transposed W^T [K,N], dY^T [N,M], X^T [K,M], each with tiled scales; M, N, K multiples of 128
+int launch_linear_quant(const uint16_t* dY, const uint16_t* W, const uint16_t* X, int64_t M, int64_t N, int64_t K,
+                        int fmt, uint8_t* dY_q, uint8_t* dY_sf, uint8_t* Wt_q, uint8_t* Wt_sf, uint8_t* dYt_q,
+                        uint8_t* dYt_sf, uint8_t* Xt_q, uint8_t* Xt_sf, cudaStream_t st);
 
 // ------------------------------------------------------------------------------------------
 // tcgen05 grouped GEMM (gemm_*.cu)

@@ -111,10 +111,13 @@ def test_options_defaults_and_validation(lib):
     assert mb.get_option("PAIR_GEMMS") == 1 and mb.get_option("PAIR_TILE_N") == 256
     assert mb.get_option("G1_TILE_N") == 0 and mb.get_option("PREP_TILE_ORDER") == 1
     assert mb.get_option("G1_GATHER") == 0 and mb.get_option("PDL") == 1
+    assert mb.get_option("LINEAR_CONCURRENT") == 1
+    # the binding names every option the library has: the last is valid, the one past it is not
+    assert lib.moe_get_option(len(mb.OPTIONS) - 1) >= 0 and lib.moe_get_option(len(mb.OPTIONS)) == -1
     assert lib.moe_set_option(99, 1) == -1 and b"unknown option" in lib.moe_last_error()
     assert lib.moe_get_option(99) == -1
     for name, bad in (("WAIT_LIMIT_NS", 0), ("PAIR_GEMMS", 3), ("PAIR_TILE_N", 192), ("G1_TILE_N", 64),
-                      ("G2_TILE_N", 192), ("PREP_TILE_ORDER", 2)):
+                      ("G2_TILE_N", 192), ("PREP_TILE_ORDER", 2), ("LINEAR_CONCURRENT", 2)):
         assert lib.moe_set_option(mb.OPTIONS.index(name), bad) == -1
         assert b"not allowed" in lib.moe_last_error()
     mb.set_option("G1_WARPS", 8)
