@@ -1,10 +1,11 @@
-"""Per-GEMM parity of the MXFP8 store GEMMs on their own operands.  The quantised operands the GPU
+"""Per-GEMM parity of the store GEMMs on their own operands.  MXFP8: the quantised operands the GPU
 wrote to the workspace -- dh row-wise (dx_expanded's A), dh^T, x_g^T (dW1's), a'^T, dout_g^T (dW2's),
 each with its tiled scales -- and the weights quantised by the oracle (the GPU's own weight codes are
-pinned bit-exact to those elsewhere) are dequantised exactly and contracted in float64, expert by
-expert over its tile rows.  Both sides read the same codes, so quantisation near-ties cannot enter:
-what remains is the tensor core's accumulation and the bf16 rounding of the GEMM outputs.  Compared:
-G2's dx_expanded (the workspace's DX_EXP rows, padding rows included), G4's dW1 and G3's dW2."""
+pinned bit-exact to those elsewhere) are dequantised exactly; BF16: the operand rows (or transposed
+copies) as written.  They are contracted in float64, expert by expert over its tile rows.  Both sides
+read the same values, so quantisation near-ties cannot enter: what remains is the tensor core's
+accumulation and the bf16 rounding of the GEMM outputs.  Compared: G2's dx_expanded (the workspace's
+DX_EXP rows, padding rows included), G4's dW1 and G3's dW2."""
 import numpy as np
 import pytest
 import torch
@@ -144,3 +145,53 @@ def test_mxfp8_store_gemms_on_their_own_operands_hot_expert_full_size():
             "G2_dx_expanded": _check("dx_expanded rows", dx_exp, *contract(dh, W1e))}
     print(f"expert {e}, {b - a} tile rows:",
           {k: (f"{u:.2e}", f"{v:.3%}", f"{w:.2f}") for k, (u, v, w) in errs.items()})
+
+
+@pytest.mark.parametrize("mn", [1, 0])
+@pytest.mark.parametrize("affinity", [AFFINITY_ON_I, AFFINITY_ON_H])
+def test_bf16_store_gemms_on_their_own_operands(affinity, mn, set_option):
+    """BF16: the GEMMs' operands as the GPU wrote them -- row-major x_g, dh, a' and dout_g read through
+    the MN-major layout (MN_OPERANDS = 1), or their transposed copies (0) -- contracted in float64 and
+    compared with dx_expanded, dW1 and dW2 the same way as the MXFP8 ones."""
+    from moe_expert_layer_routing_gb300.inputs import PREC_BF16
+    set_option("MN_OPERANDS", mn)
+    cfg = small_moe("bf16_l1", T=700, H=384, I=256, E=6, K=2, B=256, seed=37, precision=PREC_BF16,
+                    affinity=affinity)
+    inp = with_ids(make_moe_inputs(cfg), _ragged_ids(700, 2, 6, seed=9))
+    op, got = run_gpu(inp)
+    assert int(got["status"].item()) == 0
+    P, H, I = op.tile_rows, cfg.H, cfg.I
+    toff = op.region("TILE_OFFSETS").view(torch.int32).cpu().numpy()
+    used = int(toff[cfg.E])
+
+    def rows(name, cols):   # [used, cols] token rows: the row-major region, or the transposed copy
+        r = op.region(name).view(torch.bfloat16)
+        return np64(r.reshape(P, cols)[:used] if mn else r.reshape(cols, P)[:, :used].T)
+
+    dh = np64(op.region("DH").view(torch.bfloat16).reshape(P, 2 * I))[:used]
+    dh_w = dh if mn else rows("DH_T", 2 * I)     # the dW1 GEMM's B operand
+    x = rows("X_GT", H)
+    ap = rows("AP_T", I)
+    # the dW2 GEMM's B operand: dout_g itself with MN-major operands (s moved to a' for affinity on
+    # H), else the transposed copy (s-scaled for affinity on H)
+    dout = np64(op.region("DOUT_G").view(torch.bfloat16).reshape(P, H))[:used] if mn else rows("DOUT_GT", H)
+    W1 = np64(inp.W1)
+    dx_exp = np64(op.region("DX_EXP").view(torch.bfloat16).reshape(P, H))[:used]
+    ref = {n: (np.zeros(shape), np.zeros(shape)) for n, shape in
+           (("dx", (used, H)), ("dW1", (cfg.E, H, 2 * I)), ("dW2", (cfg.E, I, H)))}
+
+    def put(n, idx, A, B):
+        ref[n][0][idx] = A @ B.T
+        ref[n][1][idx] = np.abs(A) @ np.abs(B).T
+
+    for e in range(cfg.E):
+        a, b = int(toff[e]), int(toff[e + 1])
+        if a == b:
+            continue
+        put("dx", slice(a, b), dh[a:b], W1[e])
+        put("dW1", e, x[a:b].T, dh_w[a:b].T)
+        put("dW2", e, ap[a:b].T, dout[a:b].T)
+    errs = {"G2_dx_expanded": _check("dx_expanded", dx_exp, *ref["dx"]),
+            "G4_dW1": _check("dW1", np64(got["dW1"]), *ref["dW1"]),
+            "G3_dW2": _check("dW2", np64(got["dW2"]), *ref["dW2"])}
+    print({k: (f"{a:.2e}", f"{b:.3%}", f"{c:.2f}") for k, (a, b, c) in errs.items()})
