@@ -5,7 +5,8 @@ pinned bit-exact to those elsewhere) are dequantised exactly; BF16: the operand 
 copies) as written.  They are contracted in float64, expert by expert over its tile rows.  Both sides
 read the same values, so quantisation near-ties cannot enter: what remains is the tensor core's
 accumulation and the bf16 rounding of the GEMM outputs.  Compared: G2's dx_expanded (the workspace's
-DX_EXP rows, padding rows included), G4's dW1 and G3's dW2."""
+DX_EXP rows, padding rows included), G4's dW1 and G3's dW2, and G1's epilogue outputs (dh, ds, and
+for MXFP8 the codes and scales of dh, dh^T and a'^T) from dA_raw on the rows the GPU gathered."""
 import numpy as np
 import pytest
 import torch
@@ -195,3 +196,122 @@ def test_bf16_store_gemms_on_their_own_operands(affinity, mn, set_option):
             "G4_dW1": _check("dW1", np64(got["dW1"]), *ref["dW1"]),
             "G3_dW2": _check("dW2", np64(got["dW2"]), *ref["dW2"])}
     print({k: (f"{a:.2e}", f"{b:.3%}", f"{c:.2f}") for k, (a, b, c) in errs.items()})
+
+
+# ---------------------------------------------------------------------------------------------------
+# G1: dA_raw = dout_g W2_e^T on the dout rows the GPU gathered (and quantised), then the dSwiGLU
+# epilogue written out in float64 on the same checkpoint values
+# ---------------------------------------------------------------------------------------------------
+
+def _fp8_ordered(c: np.ndarray) -> np.ndarray:
+    """FP8 codes (sign-magnitude bytes) as integers in the order of their values."""
+    c = c.astype(np.int64)
+    return np.where(c < 0x80, c, 0x80 - c)
+
+
+def _g1_reference(inp, op, mx):
+    """Per used tile row: the float64 dA_raw from the GPU's own A operand and the weights (quantised by
+    the oracle for MXFP8), its magnitude sum |dout_g| |W2_e|^T, and the row's gate, up and s."""
+    from helpers import oracle_h, oracle_meta
+    cfg = inp.cfg
+    P, H, I = op.tile_rows, cfg.H, cfg.I
+    toff = op.region("TILE_OFFSETS").view(torch.int32).cpu().numpy()
+    used = int(toff[cfg.E])
+    flat = op.region("TILE_ROW_FLAT").view(torch.int32).cpu().numpy()[:used]
+    valid = flat >= 0
+    t, k = np.where(valid, flat // cfg.K, 0), np.where(valid, flat % cfg.K, 0)
+    if mx:
+        g = _deq(op, "DOUT_G", P, H, cfg.fp8_act)[:used]
+        W2q, W2s = omx.mx_quantize(inp.W2.double().numpy(), cfg.fp8_w, axis=-1)   # [E, I, H], groups along H
+        W2 = omx.mx_dequantize(W2q, W2s, cfg.fp8_w, axis=-1)
+    else:
+        g = np64(op.region("DOUT_G").view(torch.bfloat16).reshape(P, H))[:used]
+        W2 = np64(inp.W2)
+    dA_raw, mag = np.zeros((used, I)), np.zeros((used, I))
+    for e in range(cfg.E):
+        a, b = int(toff[e]), int(toff[e + 1])
+        dA_raw[a:b] = g[a:b] @ W2[e].T
+        mag[a:b] = np.abs(g[a:b]) @ np.abs(W2[e]).T
+    h = oracle_h(inp, oracle_meta(inp))[t, k] * valid[:, None]
+    s = inp.s.double().numpy()[t, k] * valid
+    return dict(used=used, valid=valid, t=t, k=k, dA_raw=dA_raw, mag=mag, gate=h[:, :I], up=h[:, I:], s=s)
+
+
+def _dswiglu(ref):
+    """dh = [dgate | dup] in float64, and the factors that multiply dA_raw in each (for error terms)."""
+    from oracle import moe as om
+    gate, up, s = ref["gate"], ref["up"], ref["s"][:, None]
+    cg, cu = s * up * om.dsilu(gate), s * om.silu(gate)
+    return np.concatenate([cg * ref["dA_raw"], cu * ref["dA_raw"]], 1), np.concatenate([cg, cu], 1)
+
+
+@pytest.mark.parametrize("affinity", [AFFINITY_ON_I, AFFINITY_ON_H])
+def test_bf16_g1_epilogue_on_its_own_operands(affinity):
+    """BF16 G1: dh within one bf16 ulp of the float64 dSwiGLU of the float64 dA_raw (plus the
+    accumulation term and 2^-20 relative for the epilogue's fp32 SiLU), ds within 2^-16 of
+    sum |dA_raw a| per slot."""
+    from moe_expert_layer_routing_gb300.inputs import PREC_BF16
+    from oracle import moe as om
+    cfg = small_moe("g1_l1", T=700, H=384, I=256, E=6, K=2, B=256, seed=38, precision=PREC_BF16,
+                    affinity=affinity)
+    inp = with_ids(make_moe_inputs(cfg), _ragged_ids(700, 2, 6, seed=10))
+    op, got = run_gpu(inp)
+    assert int(got["status"].item()) == 0
+    ref = _g1_reference(inp, op, mx=False)
+    used, I = ref["used"], cfg.I
+    dh_ref, coef = _dswiglu(ref)
+    dh = np64(op.region("DH").view(torch.bfloat16).reshape(op.tile_rows, 2 * I))[:used]
+    ulp = np.ldexp(1.0, np.floor(np.log2(np.maximum(np.abs(dh_ref), 1e-300))).astype(np.int64) - 7)
+    bound = ulp + ACC_EPS * np.abs(coef) * np.concatenate([ref["mag"]] * 2, 1) + 2.0 ** -20 * np.abs(dh_ref)
+    excess = float(np.max(np.abs(dh - dh_ref) / bound))
+    share = float(np.count_nonzero(_ordered(dh) != _ordered(dh_ref))) / dh.size
+    assert excess <= 1.0 and share <= FLIP_SHARE, (excess, share)
+    # ds[t, k] = <dA_raw, a> over the slot's row
+    a = om.silu(ref["gate"]) * ref["up"]
+    v = ref["valid"]
+    ds_ref = np.zeros((cfg.T, cfg.K))
+    ds_mag = np.zeros((cfg.T, cfg.K))
+    ds_ref[ref["t"][v], ref["k"][v]] = np.sum(ref["dA_raw"] * a, 1)[v]
+    ds_mag[ref["t"][v], ref["k"][v]] = (np.sum(np.abs(ref["dA_raw"] * a), 1) * 2.0 ** -16
+                                        + ACC_EPS * np.sum(ref["mag"] * np.abs(a), 1))[v]
+    ds = np64(got["ds"])
+    ds_excess = float(np.max(np.abs(ds - ds_ref) / (ds_mag + 1e-300)))
+    assert ds_excess <= 1.0, ds_excess
+    print(f"dh: excess {excess:.2f}, {share:.3%} off the rounded result; ds: excess {ds_excess:.3f}")
+
+
+@pytest.mark.parametrize("affinity", [AFFINITY_ON_I, AFFINITY_ON_H])
+def test_mxfp8_g1_epilogue_on_its_own_operands(affinity):
+    """MXFP8 G1: the float64 dh, and a' = (s) SiLU(gate) up, quantised by the oracle -- row-wise for dh
+    (G2's operand), along 32 tile rows for dh^T and a'^T (G4's and G3's) -- against the GPU's codes and
+    scales: scale bytes equal but for a few groups whose amax sits at a power of two, codes equal but
+    for a small share one step apart (the GPU's fp32 value and the float64 one on the two sides of a
+    rounding boundary)."""
+    from oracle import moe as om
+    cfg = small_moe("g1_l1_mx", T=700, H=384, I=256, E=6, K=2, B=256, seed=39, precision=PREC_MXFP8,
+                    affinity=affinity)
+    inp = with_ids(make_moe_inputs(cfg), _ragged_ids(700, 2, 6, seed=11))
+    op, got = run_gpu(inp)
+    assert int(got["status"].item()) == 0
+    ref = _g1_reference(inp, op, mx=True)
+    used, I, P, fa = ref["used"], cfg.I, op.tile_rows, cfg.fp8_act
+    dh_ref, _ = _dswiglu(ref)
+    a_ref = om.silu(ref["gate"]) * ref["up"] * (ref["s"][:, None] if affinity == AFFINITY_ON_I else 1.0)
+    out = {}
+    for name, vals, R, C, axis in (("DH", dh_ref, P, 2 * I, 1), ("DH_T", dh_ref, 2 * I, P, 0),
+                                   ("AP_T", a_ref, I, P, 0)):
+        q_ref, s_ref = omx.mx_quantize(vals, fa, axis=axis)        # [used, C'] codes, scales along axis
+        q = op.region(name).cpu().numpy().reshape(R, C)
+        sf = tiled_sf_to_plain(op.region(name + "_SF").cpu().numpy(), R, C)
+        if axis == 0:   # transposed outputs: [features, tile rows]
+            q, sf = q[:, :used].T, sf[:, :used // 32].T
+        else:
+            q, sf = q[:used], sf[:used]
+        same_sf = sf == s_ref
+        sf_share = 1.0 - float(np.count_nonzero(same_sf)) / same_sf.size
+        same_group = np.repeat(same_sf, 32, axis=axis)
+        d = np.abs(_fp8_ordered(q) - _fp8_ordered(q_ref))[same_group]
+        steps, share = int(d.max()), float(np.count_nonzero(d)) / d.size
+        out[name] = (f"{sf_share:.3%} scales, {share:.3%} codes, max {steps} step")
+        assert sf_share <= 0.01 and steps <= 1 and share <= FLIP_SHARE, (name, out[name])
+    print(out)
