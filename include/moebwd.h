@@ -453,7 +453,9 @@ int64_t moe_get_option(int option);
  * Stream: everything is ordered on `stream` as seen by the caller.  Under MOE_OPT_LINEAR_CONCURRENT
  * (the default) the dW GEMM runs on a stream the library creates on first use (one per device, with
  * two events), forked from `stream` and joined back to it inside the call; the call may be captured
- * into a CUDA graph once that stream exists (any earlier call on the device creates it). */
+ * into a CUDA graph once that stream exists (any earlier call on the device creates it).  That stream
+ * belongs to the device's primary context: a process that resets the device (cudaDeviceReset) sets
+ * MOE_OPT_LINEAR_CONCURRENT to 0 before calling again. */
 size_t linear_bwd_workspace_size(int64_t M, int64_t N, int64_t K, int precision);
 int linear_bwd(const void* dY, const void* W, const void* X, int64_t M, int64_t N, int64_t K, int precision,
                int fp8_fmt, void* dX, void* dW, void* workspace, size_t workspace_bytes, moe_stream_t stream);
