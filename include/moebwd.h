@@ -283,7 +283,8 @@ size_t moe_bwd_workspace_size(const MoeBwdArgs* args);
 /* The whole backward on `stream`: routing metadata, gathers/quantisation, the four grouped GEMMs
  * (dA with the fused dSwiGLU/ds epilogue, dW_down, dx_expanded, dW_gate_up), the top-K
  * scatter-sum into dx, ds and the bias gradients.  Requirements: H % 128 == 0, I % 128 == 0,
- * 1 <= K <= E <= 1024, T*K < 2^31, x/dout/weights 16-byte aligned. */
+ * 1 <= K <= E <= 1024, K <= 64, T*K < 2^31, x/dout/weights 16-byte aligned; other sizes return
+ * MOE_ERR_INVALID or MOE_ERR_UNSUPPORTED before any launch. */
 int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream);
 
 /* Regions of the moe_bwd workspace (for inspection of intermediates in tests and debugging).

@@ -165,3 +165,20 @@ def test_mxfp8_bias_with_saved_scaled_dout_is_refused(lib):
     a.down_proj_act_ckpt = 4096                                     # (pointer value only checked for presence)
     assert lib.moe_bwd_workspace_size(ctypes.byref(a)) == 0
     assert b"down_proj_act_ckpt" in lib.moe_last_error()
+
+
+def test_moe_bwd_size_limits_refused_on_the_host(lib):
+    """The documented limits (1 <= K <= E <= 1024, K <= 64, H and I multiples of 128, the four block
+    sizes) are checked before any work: the workspace query returns 0 with a message, at the limits
+    it returns a size."""
+    import moe_expert_layer_routing_gb300 as mb
+
+    def size(**kw):
+        a = mb.MoeBwdArgs(**dict(dict(T=256, H=128, I=128, E=128, K=8, block_size=128, precision=0), **kw))
+        return lib.moe_bwd_workspace_size(ctypes.byref(a))
+
+    assert size(E=1024, K=64) > 0 and size(block_size=1024) > 0
+    for kw, text in ((dict(E=128, K=65), b"K <= 64"), (dict(E=4, K=5), b"K <= E"), (dict(E=1025), b"E above"),
+                     (dict(H=192), b"multiples of 128"), (dict(block_size=2048), b"block_size")):
+        assert size(**kw) == 0, kw
+        assert text in lib.moe_last_error(), (kw, lib.moe_last_error())
