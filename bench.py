@@ -33,6 +33,7 @@ DEFAULT_WORKLOAD = "imbalanced_mxfp8"
 METRIC_MOE = "MoE-backward TFLOP/s (BF16, MXFP8) & % of tensor peak; tokens/s"
 METRIC_LINEAR = "dense MXFP8 linear-backward TFLOP/s & % of tensor peak"
 FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
+L2_BYTES_GB300 = 126 * 2 ** 20 + 2 ** 19   # without a device to ask (the timed arm asks its own)
 FP8_OVER_BF16 = 2.0   # nominal dense ratio 4.5 / 2.25 PFLOP/s
 
 
@@ -340,6 +341,36 @@ def recompute_row(mb, cfg, inp, kw, steps, stream, peak_tf, dev):
                      "excluded from useful_tflops")
 
 
+def resident_input_bytes(cfg) -> int:
+    """Bytes of the inputs a step reads from HBM as the timed step holds them: dY, W, X (bf16) for the
+    dense case; x, dout, s, ids, the [N,2,I,B] checkpoint, b2 and the weights (bf16, or MXFP8 codes
+    with one scale byte per 32) for the MoE backward."""
+    from moe_expert_layer_routing_gb300.inputs import LinearConfig, num_blocks_bound
+    if isinstance(cfg, LinearConfig):
+        return 2 * (cfg.M * cfg.N + cfg.N * cfg.K + cfg.M * cfg.K)
+    T, H, I, E, K, B = cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.block_size
+    w = E * H * 2 * I + E * I * H
+    wbytes = w + w // 32 if cfg.precision == 1 else 2 * w
+    return (2 * 2 * T * H + 2 * 4 * T * K + 2 * num_blocks_bound(T, K, E, B) * 2 * I * B
+            + (2 * E * H if cfg.bias else 0) + wbytes)
+
+
+def l2_note(in_bytes: int, l2_bytes: int) -> str:
+    """How the timed steps keep L2 from serving the inputs (recorded in the JSON line's config)."""
+    if in_bytes <= l2_bytes:
+        return (f"L2 flushed before each timed step ({in_bytes / 1e9:.2f} GB resident inputs <= "
+                f"{l2_bytes / 1e9:.2f} GB L2: a {2 * l2_bytes / 1e9:.2f} GB buffer written between steps, "
+                f"each step timed by its own events)")
+    return f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB resident inputs > {l2_bytes / 1e9:.2f} GB L2)"
+
+
+def device_l2_bytes() -> int:
+    import torch
+    if torch.cuda.is_available():
+        return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    return L2_BYTES_GB300
+
+
 def setup_problem(mb, cfg, dev):
     """Inputs, device buffers and the step of one workload (untimed); MXFP8 weights are quantised
     once here, outside any timed region."""
@@ -349,7 +380,7 @@ def setup_problem(mb, cfg, dev):
         op = mb.LinearBwd(cfg.M, cfg.N, cfg.K, mb.PREC_MXFP8, cfg.fp8, dev)
         return dict(is_linear=True, inp=inp, op=op, kw=None, step=lambda: op.run(inp.dY, inp.W, inp.X),
                     flops=float(cfg.useful_flops()), tokens=cfg.M, prec=mb.PREC_MXFP8,
-                    in_bytes=sum(t.numel() * t.element_size() for t in (inp.dY, inp.W, inp.X)))
+                    in_bytes=resident_input_bytes(cfg))
     inp = make_moe_inputs(cfg, device=dev)
     op = mb.MoeBwd(T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K, block_size=cfg.block_size,
                    precision=cfg.precision, affinity=cfg.affinity, fp8_act=cfg.fp8_act, fp8_w=cfg.fp8_w,
@@ -363,8 +394,7 @@ def setup_problem(mb, cfg, dev):
         kw.update(W1=inp.W1, W2=inp.W2)
     op.bind(**kw)
     return dict(is_linear=False, inp=inp, op=op, kw=kw, step=lambda: op.run(), flops=float(cfg.useful_flops()),
-                tokens=cfg.T, prec=cfg.precision,
-                in_bytes=sum(t.numel() * t.element_size() for t in kw.values() if t is not None))
+                tokens=cfg.T, prec=cfg.precision, in_bytes=resident_input_bytes(cfg))
 
 
 def time_problem(mb, P, steps, warmup, world, local, stream):
@@ -383,15 +413,10 @@ def time_problem(mb, P, steps, warmup, world, local, stream):
             raise SystemExit(f"device status {st0} after warm-up")
     # resident inputs larger than L2: back-to-back steps; otherwise L2 is flushed before every step (a
     # buffer of twice its size written on the stream) and each step is timed by its own pair of events
-    l2_bytes = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    l2_bytes = device_l2_bytes()
     flush = None
     if P["in_bytes"] <= l2_bytes:
         flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=torch.cuda.current_device())
-        l2_note = (f"L2 flushed before each timed step ({P['in_bytes'] / 1e9:.2f} GB resident inputs <= "
-                   f"{l2_bytes / 1e9:.2f} GB L2: a {2 * l2_bytes / 1e9:.2f} GB buffer written between steps, "
-                   f"each step timed by its own events)")
-    else:
-        l2_note = f"inputs larger than L2 ({P['in_bytes'] / 1e9:.2f} GB resident inputs > {l2_bytes / 1e9:.2f} GB L2)"
     launches0 = mb.kernel_launches()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -416,7 +441,8 @@ def time_problem(mb, P, steps, warmup, world, local, stream):
     ms = allreduce_max(local_ms, world)
     launches = mb.kernel_launches() - launches0
     del flush
-    out = dict(ms=ms, launches=launches, clocks=clk.summary(), stages=None, profiled_ms=None, l2=l2_note)
+    out = dict(ms=ms, launches=launches, clocks=clk.summary(), stages=None, profiled_ms=None,
+               l2=l2_note(P["in_bytes"], l2_bytes))
     if not P["is_linear"]:
         mb.profile_enable(True)
         ev0.record(stream)
@@ -530,7 +556,9 @@ def main():
         line = dict(metric=METRIC_LINEAR if is_linear else METRIC_MOE, value=value,
                     unit="TFLOP/s", n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=dt * 1e3,
                     higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
-                    impl="reference", config=workload_config(cfg, is_linear, 1),
+                    impl="reference",
+                    config=dict(workload_config(cfg, is_linear, world),
+                                l2=l2_note(resident_input_bytes(cfg), device_l2_bytes())),
                     cpu_baseline=dict(value=value, unit="TFLOP/s", cores=cores, kind="oracle", sample=desc),
                     e2e=dict(value=value, unit="TFLOP/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
         print(json.dumps(line), flush=True)
