@@ -572,7 +572,26 @@ int launch_sf_retile(const uint8_t* src, int64_t R, int64_t C, int bn, uint8_t* 
 // generic quantisers
 // ------------------------------------------------------------------------------------------
 
-// Row-wise: 8 elements per thread, 4 threads per 32-group.
+// Row-wise: one warp per row (rows strided over the grid's warps); a lane takes 16-byte pieces lane,
+// lane + 32, ... of the row, two at a time, so an aligned quad of lanes holds each 32-column group.
+// sf may be null (codes only: the per-token dout codes whose gathered scales prep writes).
+__device__ __forceinline__ uint2 quant_piece(const uint4 v, int fmt, uint32_t& byte) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float d[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    d[2 * j] = __uint_as_float(w[j] << 16);
+    d[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+  float am = amax_tree<8>(d);
+  am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+  am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+  byte = e8m0_byte(__float_as_uint(am), fmt);
+  const float inv = e8m0_inv_scale(byte);
+  return make_uint2(fp8x4(d[0] * inv, d[1] * inv, d[2] * inv, d[3] * inv, fmt),
+                    fp8x4(d[4] * inv, d[5] * inv, d[6] * inv, d[7] * inv, fmt));
+}
+
 __global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint16_t* __restrict__ in, int64_t src_rows,
                                                             int64_t rows, int64_t cols, int64_t ld,
                                                             const int32_t* __restrict__ row_index, int fmt,
@@ -580,37 +599,31 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const uint16_t* __re
                                                             int tiled) {
   pdl_wait();  // results of the previous kernel on the stream
   pdl_trigger();
-  const int64_t vpr = cols / 8;
-  const int64_t total = rows * vpr;
   const int lane = threadIdx.x & 31;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane; base < total; base += stride) {
-    const int64_t idx = base + lane;
-    const bool in_range = idx < total;
-    const int64_t r = in_range ? idx / vpr : 0;
-    const int64_t c = in_range ? (idx - r * vpr) * 8 : 0;
-    int64_t sr = r;
-    if (row_index) sr = in_range ? row_index[r] : -1;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (in_range && sr >= 0 && sr < src_rows) v = *reinterpret_cast<const uint4*>(in + sr * ld + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float d[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      d[2 * j] = __uint_as_float(w[j] << 16);
-      d[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t pieces = cols >> 3;  // a multiple of 4: cols is a multiple of 32
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nw) {
+    const int64_t sr = row_index ? row_index[r] : r;
+    const bool have = sr >= 0 && sr < src_rows;
+    const uint4* src = reinterpret_cast<const uint4*>(in + (have ? sr : 0) * ld);
+    uint8_t* dst = q + r * cols;
+    for (int64_t p0 = lane; p0 - lane < pieces; p0 += 64) {  // warp-uniform: every lane reaches the shuffles
+      const int64_t p1 = p0 + 32;
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      const uint4 v0 = (have && p0 < pieces) ? src[p0] : z;
+      const uint4 v1 = (have && p1 < pieces) ? src[p1] : z;
+      uint32_t b0, b1;
+      const uint2 o0 = quant_piece(v0, fmt, b0);
+      const uint2 o1 = quant_piece(v1, fmt, b1);
+      if (p0 < pieces) {
+        *reinterpret_cast<uint2*>(dst + 8 * p0) = o0;
+        if (sf && (p0 & 3) == 0) sf[tiled ? sf_tiled_offset(r, 8 * p0, cols) : r * (cols / 32) + p0 / 4] = (uint8_t)b0;
+      }
+      if (p1 < pieces) {
+        *reinterpret_cast<uint2*>(dst + 8 * p1) = o1;
+        if (sf && (p1 & 3) == 0) sf[tiled ? sf_tiled_offset(r, 8 * p1, cols) : r * (cols / 32) + p1 / 4] = (uint8_t)b1;
+      }
     }
-    float am = amax_tree<8>(d);
-    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-    if (!in_range) continue;
-    const uint32_t byte = e8m0_byte(__float_as_uint(am), fmt);
-    const float inv = e8m0_inv_scale(byte);
-    uint2 o;
-    o.x = fp8x4(d[0] * inv, d[1] * inv, d[2] * inv, d[3] * inv, fmt);
-    o.y = fp8x4(d[4] * inv, d[5] * inv, d[6] * inv, d[7] * inv, fmt);
-    *reinterpret_cast<uint2*>(q + r * cols + c) = o;
-    if (sf && ((c >> 3) & 3) == 0) sf[tiled ? sf_tiled_offset(r, c, cols) : r * (cols / 32) + c / 32] = (uint8_t)byte;
   }
 }
 
@@ -669,9 +682,8 @@ __global__ void __launch_bounds__(256) quant_colwise_kernel(const uint16_t* __re
 
 int launch_quant_rowwise(const uint16_t* in, int64_t src_rows, int64_t rows, int64_t cols, int64_t ld,
                          const int32_t* row_index, int fmt, uint8_t* q, uint8_t* sf, int tiled, cudaStream_t st) {
-  const int64_t total = rows * (cols / 8);
-  if (total == 0) return MOE_OK;
-  int64_t blocks = (total + 255) / 256;
+  if (rows == 0 || cols == 0) return MOE_OK;
+  int64_t blocks = (rows + 7) / 8;  // eight warps (rows) per block
   const int64_t cap = (int64_t)device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
   return launch_pdl(quant_rowwise_kernel, dim3((unsigned)blocks), dim3(256), 0, st, "quant_rowwise", in, src_rows, rows,
