@@ -119,7 +119,9 @@ size_t moe_route_meta_workspace_size(int T, int K, int E, int block_size);
  *   num_blocks [1]              total blocks in use
  * status_dev (device) int32 [1]: MOE_STATUS_BAD_EXPERT_ID is OR-ed in for ids outside [0,E).
  * Entries x_gather_idx / s_scatter_idx [TKv, T*K) are left unchanged.  block_size must be one of
- * 128, 256, 512, 1024; 1 <= E <= 1024; T*K < 2^31. */
+ * 128, 256, 512, 1024; 1 <= E <= 1024; T*K < 2^31.  T = 0: the offsets and num_blocks are zeroed and
+ * nothing else is written (ids, the [T*K] and [N*B] arrays, block_to_expert and the workspace may then
+ * be null). */
 int moe_route_meta(const int32_t* ids, int T, int K, int E, int block_size, int32_t* expert_offsets,
                    int32_t* x_gather_idx, int32_t* s_scatter_idx, int32_t* s_reverse_scatter_idx,
                    int32_t* token_position_to_id, int32_t* block_to_expert, int32_t* block_offsets,
@@ -284,7 +286,8 @@ size_t moe_bwd_workspace_size(const MoeBwdArgs* args);
  * (dA with the fused dSwiGLU/ds epilogue, dW_down, dx_expanded, dW_gate_up), the top-K
  * scatter-sum into dx, ds and the bias gradients.  Requirements: H % 128 == 0, I % 128 == 0,
  * 1 <= K <= E <= 1024, K <= 64, T*K < 2^31, x/dout/weights 16-byte aligned; other sizes return
- * MOE_ERR_INVALID or MOE_ERR_UNSUPPORTED before any launch. */
+ * MOE_ERR_INVALID or MOE_ERR_UNSUPPORTED before any launch.  T = 0: dW1, dW2 (and db1, db2) are
+ * zeroed, or left as they are with accumulate; the token-sized pointers may then be null. */
 int moe_bwd(const MoeBwdArgs* args, moe_stream_t stream);
 
 /* Regions of the moe_bwd workspace (for inspection of intermediates in tests and debugging).

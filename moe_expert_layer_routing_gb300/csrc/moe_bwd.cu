@@ -251,12 +251,16 @@ static int check_args(const MoeBwdArgs* a, bool need_ptrs) {
     return fail(MOE_ERR_UNSUPPORTED, "moe_bwd: the interleaved layout needs 16 columns per G1 epilogue warp");
   const bool rec = a->act_src == MOE_ACT_RECOMPUTE;
   if (!need_ptrs) return MOE_OK;
-  const void* req[] = {a->x, a->dout, a->s, a->ids, a->dx, a->dW1, a->dW2, a->ds, a->status_dev};
+  // token-sized arrays may be null when there are no tokens (T = 0: only the weight gradients, zeroed)
+  const void* req_tok[] = {a->x, a->dout, a->s, a->ids, a->dx, a->ds};
+  const void* req[] = {a->dW1, a->dW2, a->status_dev};
   if (reinterpret_cast<uintptr_t>(a->num_valid_tokens) & 3)
     return fail(MOE_ERR_INVALID, "moe_bwd: num_valid_tokens must be 4-byte aligned");
   for (const void* q : req)
     if (!q) return fail(MOE_ERR_INVALID, "moe_bwd: required pointer is null");
-  if (!rec && !a->gate_up_ckpt) return fail(MOE_ERR_INVALID, "moe_bwd: gate_up_ckpt is null");
+  for (const void* q : req_tok)
+    if (!q && a->T > 0) return fail(MOE_ERR_INVALID, "moe_bwd: required pointer is null");
+  if (!rec && !a->gate_up_ckpt && a->T > 0) return fail(MOE_ERR_INVALID, "moe_bwd: gate_up_ckpt is null");
   {
     const int given = (a->expert_offsets != nullptr) + (a->s_scatter_idx != nullptr) + (a->block_offsets != nullptr);
     if (given != 0 && given != 3)
@@ -375,6 +379,16 @@ extern "C" int moe_route_meta(const int32_t* ids, int T, int K, int E, int block
   clear_error();
   int rc0 = check_route_sizes("moe_route_meta", T, K, E, block_size);
   if (rc0) return rc0;
+  if (T == 0) {  // no routed rows: zero offsets and block count; the per-row arrays are empty (may be null)
+    if (!expert_offsets || !block_offsets || !num_blocks || !status_dev)
+      return fail(MOE_ERR_INVALID, "moe_route_meta: null pointer");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int rc = cuda_check(cudaMemsetAsync(status_dev, 0, sizeof(int32_t), st), "memset status");
+    if (!rc) rc = cuda_check(cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (size_t)(E + 1), st), "memset offsets");
+    if (!rc) rc = cuda_check(cudaMemsetAsync(block_offsets, 0, sizeof(int32_t) * (size_t)(E + 1), st), "memset offsets");
+    if (!rc) rc = cuda_check(cudaMemsetAsync(num_blocks, 0, sizeof(int32_t), st), "memset num_blocks");
+    return rc;
+  }
   if (!ids || !expert_offsets || !x_gather_idx || !s_scatter_idx || !s_reverse_scatter_idx || !token_position_to_id ||
       !block_to_expert || !block_offsets || !num_blocks || !status_dev || !workspace)
     return fail(MOE_ERR_INVALID, "moe_route_meta: null pointer");

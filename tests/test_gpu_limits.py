@@ -65,3 +65,40 @@ def test_moe_bwd_at_the_limits(case, prec, tol):
         assert torch.count_nonzero(got["dW2"][int(e)]).item() == 0
     errs = compare_outputs(got, oracle_bwd(inp), tol)
     print(case, prec, {k: f"{v:.2e}" for k, v in errs.items()}, f"{len(empty)} empty experts")
+
+
+@pytest.mark.parametrize("prec", [PREC_BF16, PREC_MXFP8])
+def test_zero_tokens(prec):
+    """T = 0: the routing metadata is all zero offsets and no blocks; the backward zeroes the weight
+    gradients (or leaves them as they are with accumulate), with the token-sized arrays empty."""
+    import moe_expert_layer_routing_gb300 as mb
+    H, I, E, K, B = 128, 128, 4, 2, 128
+    ids = torch.empty(0, K, dtype=torch.int32, device="cuda")
+    meta = mb.route_meta(ids, E, B)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(meta["expert_offsets"]) == 0 and torch.count_nonzero(meta["block_offsets"]) == 0
+    assert int(meta["num_blocks"][0]) == 0 and int(meta["status"][0]) == 0
+    g = torch.Generator(device="cuda").manual_seed(5)
+    W1 = (torch.randn(E, H, 2 * I, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    W2 = (torch.randn(E, I, H, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    kw = dict(x=torch.empty(0, H, dtype=torch.bfloat16, device="cuda"),
+              dout=torch.empty(0, H, dtype=torch.bfloat16, device="cuda"),
+              s=torch.empty(0, K, dtype=torch.float32, device="cuda"), ids=ids,
+              ckpt=torch.empty(0, 2, I, B, dtype=torch.bfloat16, device="cuda"))
+    if prec == PREC_MXFP8:
+        W1_q, W1_sf = mb.quantize_weights(W1)
+        W2_q, W2_sf = mb.quantize_weights(W2)
+        kw.update(W1_q=W1_q, W1_sf=W1_sf, W2_q=W2_q, W2_sf=W2_sf)
+    else:
+        kw.update(W1=W1, W2=W2)
+    for accumulate in (False, True):
+        op = mb.MoeBwd(T=0, H=H, I=I, E=E, K=K, block_size=B, precision=prec, accumulate=accumulate)
+        op.dW1.fill_(1.0)
+        op.dW2.fill_(1.0)
+        op.bind(**kw).run()
+        torch.cuda.synchronize()
+        got = op.outputs()
+        assert int(got["status"].item()) == 0
+        want = 1.0 if accumulate else 0.0
+        assert bool((got["dW1"] == want).all()) and bool((got["dW2"] == want).all())
+        assert got["dx"].numel() == 0 and got["ds"].numel() == 0
