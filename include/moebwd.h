@@ -169,7 +169,7 @@ int moe_route_meta_noalloc(const int32_t* ids, int T, int K, int E, int block_si
  * C/128 grid, row-major) at byte ((r/128)*(C/128) + c/128)*512, inside it byte
  * (r%32)*16 + ((r%128)/32)*4 + (c/32)%4.  It requires R % 128 == 0 and C % 128 == 0.
  * The grouped dimension must be a multiple of 32, the other a multiple of 16 (ROWWISE) or
- * 128 (COLWISE). */
+ * 128 (COLWISE).  rows == 0 or cols == 0: nothing is written (the pointers may be null). */
 int mxfp8_quantize(const void* in, int64_t src_rows, int64_t rows, int64_t cols, int64_t ld,
                    const int32_t* row_index, int axis, int fp8_fmt, uint8_t* q, uint8_t* scales,
                    int scale_layout, moe_stream_t stream);
@@ -353,7 +353,7 @@ enum {
  *   TOPK:              dlogits[idx_k] = g_k, 0 elsewhere.
  * logits (device) fp32 [T,E]; scores, dscores (device) fp32 [T,K]; ids (device) int32 [T,K];
  * dlogits (device) fp32 [T,E], fully written.  K <= 64.  Repeated ids accumulate; ids outside [0,E)
- * are skipped.  fp32 arithmetic. */
+ * are skipped.  fp32 arithmetic.  T = 0: nothing is written (the pointers may be null). */
 int moe_router_bwd(int mode, int renorm, const float* logits, const float* scores, const float* dscores,
                    const int32_t* ids, int T, int K, int E, float* dlogits, moe_stream_t stream);
 
@@ -454,6 +454,8 @@ int64_t moe_get_option(int option);
  * dY, W, X, dX, dW (device) bf16; M, N, K multiples of 128.  The workspace holds the quantised or
  * transposed operand copies (none for BF16 under MOE_OPT_MN_OPERANDS, the default: its size is taken
  * with the option as it stands, which must not change between the size query and the call).
+ * M, N or K = 0 (multiples of 128 too): an empty contraction gives zeros -- dX is zeroed when N = 0,
+ * dW when M = 0 -- and empty outputs need no pointer.
  * Stream: everything is ordered on `stream` as seen by the caller.  Under MOE_OPT_LINEAR_CONCURRENT
  * (the default) the dW GEMM runs on a stream the library creates on first use (one per device, with
  * two events), forked from `stream` and joined back to it inside the call; the call may be captured

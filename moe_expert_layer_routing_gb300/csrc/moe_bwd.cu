@@ -838,11 +838,19 @@ extern "C" size_t linear_bwd_workspace_size(int64_t M, int64_t N, int64_t K, int
 extern "C" int linear_bwd(const void* dY, const void* W, const void* X, int64_t M, int64_t N, int64_t K, int precision,
                           int fp8_fmt, void* dX, void* dW, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   clear_error();
-  if (!dY || !W || !X || !dX || !dW || !workspace) return fail(MOE_ERR_INVALID, "linear_bwd: null pointer");
-  if (M <= 0 || N <= 0 || K <= 0) return fail(MOE_ERR_INVALID, "linear_bwd: sizes must be positive");
+  if (M < 0 || N < 0 || K < 0) return fail(MOE_ERR_INVALID, "linear_bwd: negative size");
   if (M % 128 || N % 128 || K % 128) return fail(MOE_ERR_UNSUPPORTED, "linear_bwd: M, N, K must be multiples of 128");
-  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return fail(MOE_ERR_UNSUPPORTED, "linear_bwd: too large");
   if (precision != MOE_PREC_BF16 && precision != MOE_PREC_MXFP8) return fail(MOE_ERR_INVALID, "linear_bwd: bad precision");
+  if (M == 0 || N == 0 || K == 0) {  // an empty contraction gives zeros; empty outputs need no pointer
+    cudaStream_t st0 = reinterpret_cast<cudaStream_t>(stream);
+    if (M * K > 0 && !dX) return fail(MOE_ERR_INVALID, "linear_bwd: null pointer");
+    if (N * K > 0 && !dW) return fail(MOE_ERR_INVALID, "linear_bwd: null pointer");
+    int rc0 = M * K > 0 ? cuda_check(cudaMemsetAsync(dX, 0, (size_t)(M * K * 2), st0), "memset dX") : MOE_OK;
+    if (!rc0 && N * K > 0) rc0 = cuda_check(cudaMemsetAsync(dW, 0, (size_t)(N * K * 2), st0), "memset dW");
+    return rc0;
+  }
+  if (!dY || !W || !X || !dX || !dW || !workspace) return fail(MOE_ERR_INVALID, "linear_bwd: null pointer");
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return fail(MOE_ERR_UNSUPPORTED, "linear_bwd: too large");
   if (precision == MOE_PREC_MXFP8 && fp8_fmt != MOE_FP8_E4M3 && fp8_fmt != MOE_FP8_E5M2)
     return fail(MOE_ERR_INVALID, "linear_bwd: bad fp8 format");
   const void* al[] = {dY, W, X, dX, dW};

@@ -710,8 +710,10 @@ extern "C" int mxfp8_quantize(const void* in, int64_t src_rows, int64_t rows, in
                               const int32_t* row_index, int axis, int fp8_fmt, uint8_t* q, uint8_t* scales,
                               int scale_layout, moe_stream_t stream) {
   clear_error();
-  if (!in || !q || !scales) return fail(MOE_ERR_INVALID, "mxfp8_quantize: null pointer");
   if (rows < 0 || cols < 0 || src_rows < 0) return fail(MOE_ERR_INVALID, "mxfp8_quantize: negative size");
+  if (axis != MOE_QUANT_ROWWISE && axis != MOE_QUANT_COLWISE) return fail(MOE_ERR_INVALID, "mxfp8_quantize: bad axis");
+  if (rows == 0 || cols == 0) return MOE_OK;  // nothing to write (the pointers may be null)
+  if (!in || !q || !scales) return fail(MOE_ERR_INVALID, "mxfp8_quantize: null pointer");
   if (ld < cols || ld % 8 != 0) return fail(MOE_ERR_INVALID, "mxfp8_quantize: ld must be >= cols and a multiple of 8");
   if ((reinterpret_cast<uintptr_t>(in) & 15) || (reinterpret_cast<uintptr_t>(q) & 15))
     return fail(MOE_ERR_INVALID, "mxfp8_quantize: in and q must be 16-byte aligned");

@@ -208,11 +208,11 @@ extern "C" int moe_router_bwd(int mode, int renorm, const float* logits, const f
   if (T < 0 || K <= 0 || E <= 0 || K > 64) return fail(MOE_ERR_INVALID, "moe_router_bwd: bad sizes (need K <= 64)");
   if (mode != MOE_ROUTER_SOFTMAX_OVER_TOPK && mode != MOE_ROUTER_TOPK_OVER_SOFTMAX && mode != MOE_ROUTER_TOPK)
     return fail(MOE_ERR_INVALID, "moe_router_bwd: bad mode");
+  if (T == 0) return MOE_OK;  // nothing to write (the pointers may be null)
   if (!dscores || !ids || !dlogits) return fail(MOE_ERR_INVALID, "moe_router_bwd: null pointer");
   if (mode == MOE_ROUTER_TOPK_OVER_SOFTMAX && !logits) return fail(MOE_ERR_INVALID, "moe_router_bwd: logits needed");
   if ((mode == MOE_ROUTER_SOFTMAX_OVER_TOPK || (mode == MOE_ROUTER_TOPK_OVER_SOFTMAX && renorm)) && !scores)
     return fail(MOE_ERR_INVALID, "moe_router_bwd: forward scores needed");
-  if (T == 0) return MOE_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool aligned = ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(dlogits)) & 15) == 0;
   if (E % 4 == 0 && E <= 1024 && K <= 32 && aligned) {  // one pass, the row in registers

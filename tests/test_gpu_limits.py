@@ -102,3 +102,20 @@ def test_zero_tokens(prec):
         want = 1.0 if accumulate else 0.0
         assert bool((got["dW1"] == want).all()) and bool((got["dW2"] == want).all())
         assert got["dx"].numel() == 0 and got["ds"].numel() == 0
+
+
+@pytest.mark.parametrize("prec", [PREC_BF16, PREC_MXFP8])
+def test_linear_bwd_empty_contractions(prec):
+    """M = 0 (no rows): dW = dY^T X is an empty sum, all zeros; N = 0 (no output features): dX = dY W is
+    all zeros.  The empty operands are not read."""
+    import moe_expert_layer_routing_gb300 as mb
+    for M, N, K in ((0, 256, 384), (256, 0, 384)):
+        op = mb.LinearBwd(M, N, K, prec, device="cuda")
+        op.dX.fill_(3.0)
+        op.dW.fill_(3.0)
+        dY = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        W = torch.randn(N, K, device="cuda").to(torch.bfloat16)
+        X = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+        op.run(dY, W, X)
+        torch.cuda.synchronize()
+        assert bool((op.dX == 0).all()) and bool((op.dW == 0).all())

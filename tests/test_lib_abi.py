@@ -182,3 +182,18 @@ def test_moe_bwd_size_limits_refused_on_the_host(lib):
                      (dict(H=192), b"multiples of 128"), (dict(block_size=2048), b"block_size")):
         assert size(**kw) == 0, kw
         assert text in lib.moe_last_error(), (kw, lib.moe_last_error())
+
+
+def test_empty_calls_return_without_work(lib):
+    """Empty problems are valid and do nothing (their pointers may be null): a quantisation of zero rows
+    or columns, a router backward of zero tokens, a linear backward whose outputs are all empty (K = 0);
+    no kernel is launched (host-only: no device is touched)."""
+    import moe_expert_layer_routing_gb300 as mb
+    before = mb.kernel_launches()
+    assert lib.mxfp8_quantize(None, 0, 0, 32, 32, None, 0, 0, None, None, 0, None) == 0
+    assert lib.mxfp8_quantize(None, 0, 64, 0, 0, None, 1, 1, None, None, 1, None) == 0
+    assert lib.moe_router_bwd(1, 1, None, None, None, None, 0, 2, 8, None, None) == 0
+    assert lib.linear_bwd(None, None, None, 128, 128, 0, 1, 1, None, None, None, 0, None) == 0
+    assert lib.linear_bwd(None, None, None, 128, 128, 0, 7, 1, None, None, None, 0, None) == -1   # precision
+    assert lib.linear_bwd(None, None, None, 100, 128, 0, 1, 1, None, None, None, 0, None) == -2   # not x128
+    assert mb.kernel_launches() == before
