@@ -7,10 +7,11 @@
 //                        dl = p (dp - <dr, r>)   for every logit
 //   plain top-K          s = l[idx]:                     dl[idx_k] = g_k
 //
-// One warp per token, fp32.  router_bwd_vec_kernel (E a multiple of 4, E <= 1024, K <= 32): one pass
-// over the token's logits, held in registers as float4 (lane l owns columns 128 j + 4 l .. + 3), the
-// slot weights scattered once through a per-warp shared buffer (repeated ids summed in slot order),
-// the row written as float4.  router_bwd_kernel (any E, K <= 64): lane j owns logits j, j+32, ..., the
+// fp32.  router_bwd_vec_kernel (E a multiple of 4): one token per 8 lanes (E <= 256, K <= 8), per
+// half-warp (E <= 512, K <= 16) or per warp (E <= 1024, K <= 32), one pass over the token's logits
+// held in registers as float4 (lane l of a segment of L lanes owns columns 4 L j + 4 l .. + 3), the
+// slot weights scattered once through a per-segment shared buffer (repeated ids summed in slot
+// order), the row written as float4.  router_bwd_kernel (any E, K <= 64): lane j owns logits j, j+32, ..., the
 // K selected slots broadcast by shuffles per 32 logits.  Ids outside [0, E) are skipped.
 #include <cuda_runtime.h>
 
@@ -104,7 +105,23 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-template <int NV>  // float4 column groups per lane: ceil(E / 128)
+// One token per segment of LANES lanes (a whole warp, or 16 or 8 of its lanes: more rows in flight
+// and reductions one or two shuffle steps shorter); NV float4 column groups per lane:
+// ceil(E / (4 LANES)).
+template <int LANES>
+__device__ __forceinline__ float seg_sum(float v, unsigned mask) {
+#pragma unroll
+  for (int o = LANES / 2; o > 0; o >>= 1) v += __shfl_xor_sync(mask, v, o);
+  return v;
+}
+template <int LANES>
+__device__ __forceinline__ float seg_max(float v, unsigned mask) {
+#pragma unroll
+  for (int o = LANES / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(mask, v, o));
+  return v;
+}
+
+template <int NV, int LANES>
 __global__ void __launch_bounds__(256) router_bwd_vec_kernel(int mode, int renorm, const float* __restrict__ logits,
                                                              const float* __restrict__ scores,
                                                              const float* __restrict__ g,
@@ -112,17 +129,20 @@ __global__ void __launch_bounds__(256) router_bwd_vec_kernel(int mode, int renor
                                                              float* __restrict__ dl) {
   pdl_wait();  // results of the previous kernel on the stream
   pdl_trigger();
-  __shared__ float4 sbuf[8][NV * 32];
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + w;
-  if (t >= T) return;  // only warp-level synchronisation below
-  float4* buf = sbuf[w];
+  constexpr int SEGS = 32 / LANES;  // tokens per warp
+  constexpr int COLS = 4 * LANES;   // logits of one float4 column group across the segment
+  __shared__ float4 sbuf[8 * SEGS][NV * LANES];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, seg = lane / LANES, sl = lane % LANES;
+  const unsigned mask = (0xffffffffu >> (32 - LANES)) << (LANES * seg);  // this segment's lanes
+  const int t = (blockIdx.x * 8 + w) * SEGS + seg;
+  if (t >= T) return;  // only segment-level synchronisation below
+  float4* buf = sbuf[w * SEGS + seg];
   int id = -1;
   float gk = 0.f, sk = 0.f;
-  if (lane < K) {
-    id = ids[(int64_t)t * K + lane];
-    gk = g[(int64_t)t * K + lane];
-    if (scores) sk = scores[(int64_t)t * K + lane];
+  if (sl < K) {
+    id = ids[(int64_t)t * K + sl];
+    gk = g[(int64_t)t * K + sl];
+    if (scores) sk = scores[(int64_t)t * K + sl];
     if (id < 0 || id >= E) id = -1;
   }
   const float* lt = logits ? logits + (int64_t)t * E : nullptr;
@@ -131,71 +151,73 @@ __global__ void __launch_bounds__(256) router_bwd_vec_kernel(int mode, int renor
   if (mode == MOE_ROUTER_TOPK) {
     wk = gk;
   } else if (mode == MOE_ROUTER_SOFTMAX_OVER_TOPK) {
-    const float d = warp_sum(id >= 0 ? gk * sk : 0.f);
+    const float d = seg_sum<LANES>(id >= 0 ? gk * sk : 0.f, mask);
     wk = sk * (gk - d);
   } else {
     float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      const int c = j * 128 + 4 * lane;
-      L[j] = c < E ? reinterpret_cast<const float4*>(lt)[j * 32 + lane]
+      const int c = j * COLS + 4 * sl;
+      L[j] = c < E ? reinterpret_cast<const float4*>(lt)[j * LANES + sl]
                    : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       m = fmaxf(m, fmaxf(fmaxf(L[j].x, L[j].y), fmaxf(L[j].z, L[j].w)));
     }
-    mx = warp_max(m);
+    mx = seg_max<LANES>(m, mask);
     float sum = 0.f;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {  // L now holds exp(l - max) (0 past E)
       L[j] = make_float4(__expf(L[j].x - mx), __expf(L[j].y - mx), __expf(L[j].z - mx), __expf(L[j].w - mx));
       sum += (L[j].x + L[j].y) + (L[j].z + L[j].w);
     }
-    inv = 1.f / warp_sum(sum);
-    // exp(l[id] - max) of this lane's slot, from the lane that holds column id in registers
-    const int src = (id & 127) >> 2, grp = id >> 7, cmp = id & 3;
+    inv = 1.f / seg_sum<LANES>(sum, mask);
+    // exp(l[id] - max) of this lane's slot, from the lane of the segment that holds column id
+    const int src = (id % COLS) >> 2, grp = id / COLS, cmp = id & 3;
     float ek = 0.f;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      const float ex = __shfl_sync(0xffffffffu, L[j].x, src), ey = __shfl_sync(0xffffffffu, L[j].y, src);
-      const float ez = __shfl_sync(0xffffffffu, L[j].z, src), ew = __shfl_sync(0xffffffffu, L[j].w, src);
+      const float ex = __shfl_sync(mask, L[j].x, src, LANES), ey = __shfl_sync(mask, L[j].y, src, LANES);
+      const float ez = __shfl_sync(mask, L[j].z, src, LANES), ew = __shfl_sync(mask, L[j].w, src, LANES);
       if (grp == j) ek = cmp == 0 ? ex : cmp == 1 ? ey : cmp == 2 ? ez : ew;
     }
     const float pk = id >= 0 ? ek * inv : 0.f;
-    const float S = warp_sum(pk), dsum = warp_sum(id >= 0 ? gk * sk : 0.f);
+    const float S = seg_sum<LANES>(pk, mask), dsum = seg_sum<LANES>(id >= 0 ? gk * sk : 0.f, mask);
     wk = renorm ? (gk - dsum) / S : gk;  // dr of the slot
-    dot = warp_sum(id >= 0 ? wk * pk : 0.f);
+    dot = seg_sum<LANES>(id >= 0 ? wk * pk : 0.f, mask);
   }
 #pragma unroll
-  for (int j = 0; j < NV; ++j) buf[j * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
-  __syncwarp();
+  for (int j = 0; j < NV; ++j) buf[j * LANES + sl] = make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncwarp(mask);
   // the first slot of each distinct id writes the sum of its slots' weights, in slot order
   float tot = 0.f;
   for (int j = 0; j < K; ++j) {
-    const int idj = __shfl_sync(0xffffffffu, id, j);
-    const float wj = __shfl_sync(0xffffffffu, wk, j);
+    const int idj = __shfl_sync(mask, id, j, LANES);
+    const float wj = __shfl_sync(mask, wk, j, LANES);
     if (idj == id) tot += wj;
   }
-  const unsigned same = __match_any_sync(0xffffffffu, id);
+  const unsigned same = __match_any_sync(mask, id);
   if (id >= 0 && lane == __ffs(same) - 1) reinterpret_cast<float*>(buf)[id] = tot;
-  __syncwarp();
+  __syncwarp(mask);
   float4* out = reinterpret_cast<float4*>(dl + (int64_t)t * E);
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
-    if (j * 128 + 4 * lane >= E) continue;
-    float4 v = buf[j * 32 + lane];
+    if (j * COLS + 4 * sl >= E) continue;
+    float4 v = buf[j * LANES + sl];
     if (mode == MOE_ROUTER_TOPK_OVER_SOFTMAX) {
       v.x = L[j].x * inv * (v.x - dot);
       v.y = L[j].y * inv * (v.y - dot);
       v.z = L[j].z * inv * (v.z - dot);
       v.w = L[j].w * inv * (v.w - dot);
     }
-    out[j * 32 + lane] = v;
+    out[j * LANES + sl] = v;
   }
 }
 
-template <int NV>
+template <int NV, int LANES>
 static void router_vec_launch(int mode, int renorm, const float* logits, const float* scores, const float* dscores,
                               const int32_t* ids, int T, int K, int E, float* dlogits, cudaStream_t st) {
-  router_bwd_vec_kernel<NV><<<(T + 7) / 8, 256, 0, st>>>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits);
+  constexpr int per_block = 8 * (32 / LANES);  // tokens per 256-thread block
+  router_bwd_vec_kernel<NV, LANES><<<(T + per_block - 1) / per_block, 256, 0, st>>>(mode, renorm, logits, scores,
+                                                                                  dscores, ids, T, K, E, dlogits);
 }
 
 }  // namespace moebwd
@@ -215,14 +237,32 @@ extern "C" int moe_router_bwd(int mode, int renorm, const float* logits, const f
     return fail(MOE_ERR_INVALID, "moe_router_bwd: forward scores needed");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool aligned = ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(dlogits)) & 15) == 0;
-  if (E % 4 == 0 && E <= 1024 && K <= 32 && aligned) {  // one pass, the row in registers
+  if (E % 4 == 0 && E <= 256 && K <= 8 && aligned) {  // one pass, the row in registers, four tokens a warp
+    const int nv = (E + 31) / 32;
+    switch (nv) {
+      case 1: router_vec_launch<1, 8>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+      case 2: router_vec_launch<2, 8>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+      case 3:
+      case 4: router_vec_launch<4, 8>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+      default: router_vec_launch<8, 8>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+    }
+  } else if (E % 4 == 0 && E <= 512 && K <= 16 && aligned) {  // two tokens a warp
+    const int nv = (E + 63) / 64;
+    switch (nv) {
+      case 1: router_vec_launch<1, 16>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+      case 2: router_vec_launch<2, 16>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+      case 3:
+      case 4: router_vec_launch<4, 16>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+      default: router_vec_launch<8, 16>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+    }
+  } else if (E % 4 == 0 && E <= 1024 && K <= 32 && aligned) {  // one pass, the row in registers
     const int nv = (E + 127) / 128;
     switch (nv) {
-      case 1: router_vec_launch<1>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
-      case 2: router_vec_launch<2>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+      case 1: router_vec_launch<1, 32>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+      case 2: router_vec_launch<2, 32>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
       case 3:
-      case 4: router_vec_launch<4>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
-      default: router_vec_launch<8>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+      case 4: router_vec_launch<4, 32>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
+      default: router_vec_launch<8, 32>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits, st); break;
     }
   } else {
     router_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(mode, renorm, logits, scores, dscores, ids, T, K, E, dlogits);

@@ -34,10 +34,14 @@ def _scores(mode, logits, ids, renorm, E):
 @pytest.mark.parametrize("mode,renorm", [(0, False), (1, False), (1, True), (2, False)])
 @pytest.mark.parametrize("T,E,K,odd", [(1000, 128, 8, False), (37, 40, 3, False), (5, 1024, 64, False),
                                         (300, 132, 32, True), (65, 520, 5, True), (40, 130, 4, True),
-                                        (50, 1028, 2, False)])
+                                        (50, 1028, 2, False), (301, 256, 16, True), (77, 512, 8, True),
+                                        (33, 68, 2, True), (129, 256, 8, True), (50, 32, 8, True)])
 def test_router_bwd(mode, renorm, T, E, K, odd):
-    """One-pass kernel (E a multiple of 4 up to 1024, K <= 32) and the general one (K = 64, E = 130,
-    E = 1028); `odd` rows repeat an id (the slots' gradients add) and carry ids outside [0, E)."""
+    """One-pass kernel with a token per 8 lanes (E a multiple of 4 up to 256, K <= 8: E = 32, 40, 68,
+    128, 256 -- a partial column group at 68, odd token counts), per half-warp (up to 512, K <= 16:
+    E = 256 with K = 16, E = 512) or per warp (up to 1024, K <= 32: E = 132 with K = 32, E = 520), and
+    the general one (K = 64, E = 130, E = 1028); `odd` rows repeat an id (the slots' gradients add) and
+    carry ids outside [0, E)."""
     import moe_expert_layer_routing_gb300 as mb
     logits, ids, g = _case(T, E, K, seed=T + E)
     if odd:
