@@ -9,9 +9,9 @@
 //
 // fp32.  router_bwd_vec_kernel (E a multiple of 4): one token per 8 lanes (E <= 256, K <= 8), per
 // half-warp (E <= 512, K <= 16) or per warp (E <= 1024, K <= 32), one pass over the token's logits
-// held in registers as float4 (lane l of a segment of L lanes owns columns 4 L j + 4 l .. + 3), the
-// slot weights scattered once through a per-segment shared buffer (repeated ids summed in slot
-// order), the row written as float4.  router_bwd_kernel (any E, K <= 64): lane j owns logits j, j+32, ..., the
+// held in registers as float4 (lane l of a segment of L lanes owns columns 4 L j + 4 l .. + 3), each
+// slot's own exponential from its logit re-read, the slot weights scattered once through a
+// per-segment shared buffer (repeated ids summed in slot order), the row written as float4.  router_bwd_kernel (any E, K <= 64): lane j owns logits j, j+32, ..., the
 // K selected slots broadcast by shuffles per 32 logits.  Ids outside [0, E) are skipped.
 #include <cuda_runtime.h>
 
@@ -170,16 +170,9 @@ __global__ void __launch_bounds__(256) router_bwd_vec_kernel(int mode, int renor
       sum += (L[j].x + L[j].y) + (L[j].z + L[j].w);
     }
     inv = 1.f / seg_sum<LANES>(sum, mask);
-    // exp(l[id] - max) of this lane's slot, from the lane of the segment that holds column id
-    const int src = (id % COLS) >> 2, grp = id / COLS, cmp = id & 3;
-    float ek = 0.f;
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      const float ex = __shfl_sync(mask, L[j].x, src, LANES), ey = __shfl_sync(mask, L[j].y, src, LANES);
-      const float ez = __shfl_sync(mask, L[j].z, src, LANES), ew = __shfl_sync(mask, L[j].w, src, LANES);
-      if (grp == j) ek = cmp == 0 ? ex : cmp == 1 ? ey : cmp == 2 ? ez : ew;
-    }
-    const float pk = id >= 0 ? ek * inv : 0.f;
+    // exp(l[id] - max) of this lane's slot: the same expression as the row's, on the logit re-read
+    // from the row just loaded (a cache hit) instead of 4 NV shuffles from the lane that holds it
+    const float pk = id >= 0 ? __expf(lt[id] - mx) * inv : 0.f;
     const float S = seg_sum<LANES>(pk, mask), dsum = seg_sum<LANES>(id >= 0 ? gk * sk : 0.f, mask);
     wk = renorm ? (gk - dsum) / S : gk;  // dr of the slot
     dot = seg_sum<LANES>(id >= 0 ? wk * pk : 0.f, mask);
