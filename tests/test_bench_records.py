@@ -37,3 +37,27 @@ def test_committed_traffic_lines_match_the_sources():
         pytest.skip("kernel code changed since the traffic capture (bench then reports traffic null)")
     for stage in ("G1_dA_dswiglu", "G3_dW2", "G2_dx_expanded", "G4_dW1"):
         assert bench.recorded_traffic("imbalanced_mxfp8", stage) > 0
+
+
+@pytest.mark.parametrize("name", ["tiny_bf16", "dense_mxfp8_4096", "bias_bf16", "small_mxfp8"])
+def test_resident_input_bytes_match_the_tensors(name):
+    """The L2 statement of the JSON line rests on the resident input bytes, computed from the shapes: they
+    equal the bytes of the tensors a step holds (MXFP8 weights as codes and one scale byte per 32)."""
+    import bench
+    from moe_expert_layer_routing_gb300.inputs import (CONFIGS, LinearConfig, make_linear_inputs, make_moe_inputs,
+                                                       small_moe)
+    cfg = {"bias_bf16": small_moe("b", T=300, H=256, I=256, E=8, K=3, B=256, bias=True),
+           "small_mxfp8": small_moe("m", T=300, H=256, I=256, E=8, K=3, B=256, precision=1)}.get(name) or CONFIGS[name]
+    if isinstance(cfg, LinearConfig):
+        inp = make_linear_inputs(cfg)
+        held = sum(t.numel() * t.element_size() for t in (inp.dY, inp.W, inp.X))
+    else:
+        inp = make_moe_inputs(cfg)
+        held = sum(t.numel() * t.element_size() for t in [inp.x, inp.dout, inp.s, inp.ids, inp.ckpt] +
+                   ([inp.b2] if cfg.bias else []))
+        w = inp.W1.numel() + inp.W2.numel()
+        held += w + w // 32 if cfg.precision == 1 else 2 * w
+    assert bench.resident_input_bytes(cfg) == held
+    l2 = 132 * 2 ** 20
+    note = bench.l2_note(held, l2)
+    assert note.startswith("L2 flushed" if held <= l2 else "inputs larger than L2")
