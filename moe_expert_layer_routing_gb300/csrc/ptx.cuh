@@ -18,10 +18,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-__device__ __forceinline__ bool elect_one_lane() {
-  return (threadIdx.x & 31) == 0;
-}
-
 // ------------------------------------------------------------------------------------------
 // mbarrier
 // ------------------------------------------------------------------------------------------
@@ -411,7 +407,6 @@ __device__ __forceinline__ bool epilogue_bar_any(bool pred) {
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ void pair_bar(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -94,17 +94,6 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(int mode, int renorm, c
   }
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
 // One token per segment of LANES lanes (a whole warp, or 16 or 8 of its lanes: more rows in flight
 // and reductions one or two shuffle steps shorter); NV float4 column groups per lane:
 // ceil(E / (4 LANES)).
