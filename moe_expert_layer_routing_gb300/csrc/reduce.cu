@@ -55,8 +55,21 @@ __global__ void ds_finalize_kernel(const float* __restrict__ ds_part, int nparts
   if (f >= TK) return;
   const int p = flat_tile_row[f];
   float v = 0.f;
-  if (p >= 0) {
-    for (int n = 0; n < nparts; ++n) v += ds_part[(int64_t)p * nparts + n];
+  if (p >= 0) {  // the row's partials in order, read as 16- or 8-byte vectors where nparts allows
+    const float* src = ds_part + (int64_t)p * nparts;
+    if ((nparts & 3) == 0) {
+      for (int n = 0; n < nparts; n += 4) {
+        const float4 q = *reinterpret_cast<const float4*>(src + n);
+        v += q.x; v += q.y; v += q.z; v += q.w;
+      }
+    } else if ((nparts & 1) == 0) {
+      for (int n = 0; n < nparts; n += 2) {
+        const float2 q = *reinterpret_cast<const float2*>(src + n);
+        v += q.x; v += q.y;
+      }
+    } else {
+      for (int n = 0; n < nparts; ++n) v += src[n];
+    }
     if (ds_bias) v += ds_bias[p];
   }
   ds[f] = v;
